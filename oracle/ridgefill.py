@@ -1,0 +1,266 @@
+"""Plain, slow, float64 CPU oracle of the RidgeFill late-layer fill and fit.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports, calls or
+executes this module: only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` use it.  It shares no code with the CUDA
+library.
+
+Source of every formula: "RidgeFill: Training-Free Late-Layer Cache Fill for
+Faster Prefill" (arXiv 2611.09709), section and equation named on each
+function.  All inputs are widened to float64; nothing is rounded in between.
+Matrix products, the Cholesky factor and triangular solves are library
+primitives (numpy / scipy); nothing is blocked, fused or reordered.
+
+Notation.  The paper writes column vectors, ``x_hat = A x_S + b`` with ``A``
+of shape ``d_out x d_in``.  Arrays here hold one row per token, so a batch of
+predictions is ``H @ A.T + b``; ``A`` keeps the paper's orientation.
+
+Readings where the paper is silent (each applied below):
+
+* R1 ridge centring: ``X`` and ``Y`` in the closed form are mean-centred and
+  the offset ``b`` is unpenalised (section 2.2: means subtracted, offset makes
+  the map right on average).
+* R2 penalty trace: ``alpha = lambda * tr(X^T X) / d_in`` uses the centred X,
+  the matrix that enters the solve.
+* R3 layer norm: RMSNorm with a plain gain, ``x / sqrt(mean(x^2) + eps) * g``.
+* R4 rotary embedding: rotate-half pairs ``(i, i + hd/2)``, frequency
+  ``theta^(-2i/hd)``, position = absolute prompt row; keys only.
+* R5 Gated DeltaNet: gates read the normed input ``u`` like ``k`` and ``v``,
+  ``alpha = sigmoid(u . w_a)``, ``beta = sigmoid(u . w_b)``, no short
+  convolution; ``k`` is L2-normalised with ``k / sqrt(sum k^2 + 1e-6)``; state
+  ``S`` is ``d_v x d_k`` and starts at zero unless given.
+* R6 rows: every prefix row is filled; the tail is not touched.
+
+Parity status: every function below is pinned by a test in ``tests/`` that
+does not re-evaluate its own formula (closed forms, exact rational
+arithmetic, library routines for the same textbook problem, invariants, the
+paper's printed numbers).
+"""
+from __future__ import annotations
+
+from typing import Optional, Sequence
+
+import numpy as np
+import scipy.linalg
+
+
+def _f64(a) -> np.ndarray:
+    return np.asarray(a, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Fit  (section 2.2, "The ridge map", "Fitting", "The penalty")
+# --------------------------------------------------------------------------
+
+def ridge_fit(X, Y, lam: float):
+    """Closed-form ridge map per late layer, section 2.2.
+
+    ``X`` [n, d_in] split states, ``Y`` [L, n, d_out] layer inputs.  Both are
+    centred by their means (R1); ``alpha = lam * tr(X^T X) / d_in`` (R2);
+    ``A_l = Y_l^T X (X^T X + alpha I)^{-1}`` and ``b_l = mu_l - A_l mu_S``.
+
+    Returns ``A`` [L, d_out, d_in], ``b`` [L, d_out], ``alpha``.
+    """
+    X = _f64(X)
+    Y = _f64(Y)
+    n, d_in = X.shape
+    mu_S = X.mean(axis=0)
+    Xc = X - mu_S
+    G = Xc.T @ Xc
+    alpha = lam * np.trace(G) / d_in
+    chol = scipy.linalg.cho_factor(G + alpha * np.eye(d_in), lower=True)
+    L = Y.shape[0]
+    A = np.empty((L, Y.shape[2], d_in))
+    b = np.empty((L, Y.shape[2]))
+    for l in range(L):
+        mu_l = Y[l].mean(axis=0)
+        Yc = Y[l] - mu_l
+        # (X^T X + alpha I) is symmetric, so A_l^T = (X^T X + alpha I)^{-1} X^T Y_l
+        A[l] = scipy.linalg.cho_solve(chol, Xc.T @ Yc).T
+        b[l] = mu_l - A[l] @ mu_S
+    return A, b, alpha
+
+
+def fit_sums(X, Y):
+    """Running sums of one capture pass, section 2.2 "Fitting".
+
+    Returns ``(n, sx, sy, G, C)``: row count, ``sum x`` [d_in], ``sum y_l``
+    [L, d_out], ``X^T X`` [d_in, d_in] and ``X^T Y_l`` as [d_in, L*d_out]
+    (column block ``l`` holds layer ``l``).  Uncentred; additive over rows.
+    """
+    X = _f64(X)
+    Y = _f64(Y)
+    L = Y.shape[0]
+    G = X.T @ X
+    C = np.concatenate([X.T @ Y[l] for l in range(L)], axis=1)
+    return X.shape[0], X.sum(axis=0), Y.sum(axis=1), G, C
+
+
+def ridge_solve_from_sums(n, sx, sy, G, C, lam: float):
+    """The same solve as :func:`ridge_fit`, from the running sums.
+
+    Centring of sums: ``X~^T X~ = G - n mu_S mu_S^T`` and
+    ``X~^T Y~_l = C_l - n mu_S mu_l^T``.
+    """
+    sx, sy, G, C = _f64(sx), _f64(sy), _f64(G), _f64(C)
+    d_in = G.shape[0]
+    L, d_out = sy.shape
+    mu_S = sx / n
+    mu = sy / n
+    Gc = G - n * np.outer(mu_S, mu_S)
+    alpha = lam * np.trace(Gc) / d_in
+    chol = scipy.linalg.cho_factor(Gc + alpha * np.eye(d_in), lower=True)
+    A = np.empty((L, d_out, d_in))
+    b = np.empty((L, d_out))
+    for l in range(L):
+        Cl = C[:, l * d_out:(l + 1) * d_out] - n * np.outer(mu_S, mu[l])
+        A[l] = scipy.linalg.cho_solve(chol, Cl).T
+        b[l] = mu[l] - A[l] @ mu_S
+    return A, b, alpha
+
+
+# --------------------------------------------------------------------------
+# Fill, attention layers  (section 2.1, 2.2 "At inference ...")
+# --------------------------------------------------------------------------
+
+def map_apply(H, A_l, b_l):
+    """``x_hat = A_l x_S + b_l`` for every row of ``H`` [rows, d_in] (section 2.2)."""
+    return _f64(H) @ _f64(A_l).T + _f64(b_l)
+
+
+def rms_norm(x, g, eps: float):
+    """The layer's own normalisation applied to a predicted input (R3)."""
+    x = _f64(x)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps) * _f64(g)
+
+
+def rope_rotate_half(k, pos, theta: float):
+    """Rotary embedding of keys ``k`` [..., rows, hd] at positions ``pos`` [rows] (R4)."""
+    k = _f64(k)
+    hd = k.shape[-1]
+    half = hd // 2
+    inv_freq = theta ** (-(2.0 * np.arange(half)) / hd)
+    ang = _f64(pos)[:, None] * inv_freq[None, :]
+    c, s = np.cos(ang), np.sin(ang)
+    k1, k2 = k[..., :half], k[..., half:]
+    return np.concatenate([k1 * c - k2 * s, k2 * c + k1 * s], axis=-1)
+
+
+def late_layer_kv(x_hat, g, Wk, Wv, pos, eps: float, theta: float, n_kv: int, hd: int):
+    """What a late attention layer writes for predicted inputs ``x_hat`` [rows, d].
+
+    Section 2.1/2.2: the layer's own norm, its key and value projections
+    (``Wk``, ``Wv`` as [n_kv*hd, d]) and the rotary embedding on keys.
+    Returns ``K``, ``V`` as [n_kv, rows, hd].
+    """
+    u = rms_norm(x_hat, g, eps)
+    rows = u.shape[0]
+    k = (u @ _f64(Wk).T).reshape(rows, n_kv, hd).transpose(1, 0, 2)
+    v = (u @ _f64(Wv).T).reshape(rows, n_kv, hd).transpose(1, 0, 2)
+    return rope_rotate_half(k, pos, theta), v
+
+
+def fill_attention(H, pos, A, b, g, Wk, Wv, eps: float, theta: float, n_kv: int, hd: int,
+                   layers: Optional[Sequence[int]] = None):
+    """The late-layer cache fill for the given prefix rows (sections 2.1-2.2).
+
+    ``H`` [rows, d_in] split states of the rows, ``pos`` [rows] their absolute
+    positions, ``A`` [L, d_out, d_in], ``b`` [L, d_out], ``g`` [L, d_out],
+    ``Wk``/``Wv`` [L, n_kv*hd, d_out].  Returns ``K``, ``V`` as
+    [len(layers), n_kv, rows, hd].
+    """
+    Ls = range(np.shape(A)[0]) if layers is None else layers
+    Ks, Vs = [], []
+    for l in Ls:
+        xh = map_apply(H, A[l], b[l])
+        k, v = late_layer_kv(xh, g[l], Wk[l], Wv[l], pos, eps, theta, n_kv, hd)
+        Ks.append(k)
+        Vs.append(v)
+    return np.stack(Ks), np.stack(Vs)
+
+
+# --------------------------------------------------------------------------
+# Fill, Gated DeltaNet layers  (section 2.3)
+# --------------------------------------------------------------------------
+
+def _sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def gdn_projections(x_hat, g, Wk, Wv, Wa, Wb, eps: float, n_heads: int, dk: int, dv: int,
+                    l2_eps: float = 1e-6):
+    """Per-row ``k`` [rows, H, dk] (L2-normalised), ``v`` [rows, H, dv] and gates
+    ``alpha``, ``beta`` [rows, H] of a GDN layer, from its normed input (R5)."""
+    u = rms_norm(x_hat, g, eps)
+    rows = u.shape[0]
+    k = (u @ _f64(Wk).T).reshape(rows, n_heads, dk)
+    k = k / np.sqrt(np.sum(k * k, axis=-1, keepdims=True) + l2_eps)
+    v = (u @ _f64(Wv).T).reshape(rows, n_heads, dv)
+    alpha = _sigmoid(u @ _f64(Wa).T)
+    beta = _sigmoid(u @ _f64(Wb).T)
+    return k, v, alpha, beta
+
+
+def gdn_recurrence(k, v, alpha, beta, S0=None):
+    """Gated delta rule over rows in order (section 2.3; R5).
+
+    ``S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T`` for every
+    head.  ``k`` [rows, H, dk], ``v`` [rows, H, dv], ``alpha``/``beta`` [rows, H];
+    ``S`` is [H, dv, dk].  ``S (I - beta k k^T)`` is evaluated as
+    ``S - beta (S k) k^T``, the same product written out.
+    """
+    k, v, alpha, beta = _f64(k), _f64(v), _f64(alpha), _f64(beta)
+    rows, nh, dk = k.shape
+    dv = v.shape[2]
+    S = np.zeros((nh, dv, dk)) if S0 is None else _f64(S0).copy()
+    for t in range(rows):
+        kt, vt = k[t], v[t]
+        a = alpha[t][:, None, None]
+        bt = beta[t][:, None, None]
+        Sk = np.einsum("hvk,hk->hv", S, kt)
+        S = a * (S - bt * Sk[:, :, None] * kt[:, None, :]) + bt * vt[:, :, None] * kt[:, None, :]
+    return S
+
+
+def gdn_state(H, A, b, g, Wk, Wv, Wa, Wb, eps: float, n_heads: int, dk: int, dv: int,
+              S0=None, layers: Optional[Sequence[int]] = None,
+              heads: Optional[Sequence[int]] = None, l2_eps: float = 1e-6):
+    """End-of-fill recurrent state of GDN late layers (sections 2.1, 2.3).
+
+    Every prefix row, in order, updates the state from its predicted input.
+    Returns [len(layers), len(heads), dv, dk].
+    """
+    Ls = range(np.shape(A)[0]) if layers is None else layers
+    hs = list(range(n_heads)) if heads is None else list(heads)
+    out = []
+    for l in Ls:
+        xh = map_apply(H, A[l], b[l])
+        k, v, a, bt = gdn_projections(xh, g[l], Wk[l], Wv[l], Wa[l], Wb[l], eps,
+                                      n_heads, dk, dv, l2_eps)
+        s0 = None if S0 is None else _f64(S0)[l][hs]
+        out.append(gdn_recurrence(k[:, hs], v[:, hs], a[:, hs], bt[:, hs], s0))
+    return np.stack(out)
+
+
+# --------------------------------------------------------------------------
+# Host-side arithmetic (section 2.5, section 2.3 / Figure 4)
+# --------------------------------------------------------------------------
+
+def speedup_ceiling(S: int, L: int, T: int, N: int):
+    """Share of exact prefill compute that remains, ``r = (S(N-T) + L T)/(L N)``,
+    section 2.5; the speedup is at most ``1/r``."""
+    return (S * (N - T) + L * T) / (L * N)
+
+
+def filled_weight_share(alpha, n_filled: int):
+    """Share of a GDN state that comes from the first ``n_filled`` rows.
+
+    Section 2.3 (terminal-state correction) and Figure 4: a row's weight in
+    the final state is the product of the gates after it.  ``alpha`` [rows].
+    """
+    a = _f64(alpha)
+    rows = a.shape[0]
+    w = np.empty(rows)
+    for t in range(rows):
+        w[t] = np.prod(a[t + 1:])
+    return w[:n_filled].sum() / w.sum()
