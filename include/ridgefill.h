@@ -1,0 +1,251 @@
+/*
+ * ridgefill.h -- C ABI of the RidgeFill late-layer cache fill for GB300 (sm_103a).
+ *
+ * Method: "RidgeFill: Training-Free Late-Layer Cache Fill for Faster Prefill"
+ * (arXiv 2611.09709).  The lower layers run exactly up to a split layer S.  For
+ * every late layer l >= S a ridge map predicts the layer's input from the split
+ * state, x_hat_l = A_l x_S + b_l (section 2.2), and the layer's own norm and
+ * key/value projections (rotary embedding on keys) write its cache for every
+ * prefix row, i.e. every row before the exact tail (sections 2.1-2.2).  A Gated
+ * DeltaNet layer instead folds the filled rows into its recurrent state
+ * (section 2.3).  The maps come from a closed-form ridge fit over running sums
+ * of one capture pass (section 2.2, "Fitting", "The penalty").
+ *
+ * Conventions shared by every call
+ *  - All tensor arguments are plain pointers to dense row-major arrays.  The
+ *    caller owns every buffer, including the workspace; the library allocates
+ *    no device memory.  Device pointers must be 16-byte aligned.
+ *  - bf16 is IEEE bfloat16 (1-8-7), f32/f64 IEEE single/double.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call is
+ *    asynchronous on it: it only enqueues work.  Argument errors are returned
+ *    synchronously and nothing is enqueued; inputs are never modified.
+ *  - A device-side wait that runs out (about two seconds) makes the kernel
+ *    record a code in a device error word and return early; read it with
+ *    ridgefill_device_error().  CUDA launch failures return RF_ERR_CUDA.
+ *  - No call writes outside the output ranges it documents.
+ *  - Not thread-safe for concurrent calls that share a workspace.
+ */
+#ifndef RIDGEFILL_H
+#define RIDGEFILL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rf_status {
+  RF_OK = 0,
+  RF_ERR_ARG = 1,        /* null pointer where one is required, or a bad value   */
+  RF_ERR_SHAPE = 2,      /* sizes the kernels do not support, or inconsistent   */
+  RF_ERR_ALIGN = 3,      /* a device pointer is not 16-byte aligned             */
+  RF_ERR_NOT_PINNED = 4, /* maps_on_host set but A is not page-locked host memory */
+  RF_ERR_CUDA = 5,       /* a CUDA call failed; see ridgefill_last_error()      */
+  RF_ERR_TIMEOUT = 6,    /* a device wait ran out (see ridgefill_device_error)  */
+  RF_ERR_NUMERIC = 7,    /* the ridge system was not positive definite          */
+  RF_ERR_WORKSPACE = 8   /* workspace pointer NULL or smaller than required     */
+} rf_status;
+
+/* ------------------------------------------------------------------------ */
+/* Attention late layers                                                     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * rf_fill_args -- one fill of the prefix rows of L late attention layers.
+ *
+ * Paper section 2.2 (map x_hat = A_l x_S + b_l; "At inference the predicted
+ * input goes through the layer's own normalization and projections ...") and
+ * section 2.1 (rows before the tail).  For every layer l, row r and kv head h:
+ *   x_hat = A_l h_r + b_l                                   (f32 accumulate)
+ *   u     = x_hat / sqrt(mean(x_hat^2) + rms_eps) * gain_l  (RMSNorm)
+ *   k     = RoPE(u Wk_l[h]^T, pos0 + r),  v = u Wv_l[h]^T
+ *   Kc[l, h, pos0 + r, :] = k,  Vc[l, h, pos0 + r, :] = v   (bf16)
+ * RoPE is rotate-half: pair (i, i + hd/2) turns by (pos0 + r) * theta^(-2i/hd).
+ *
+ * Layouts (row-major, bf16 unless noted):
+ *   H     [rows, d_in]                  split state of the rows to fill
+ *   A     [L, d_out, d_in]              maps in the paper's orientation: row j of
+ *                                       A_l produces output channel j.  Device
+ *                                       memory, or page-locked host memory when
+ *                                       maps_on_host = 1 (copied one layer at a
+ *                                       time while the previous layer computes;
+ *                                       results are bitwise those of device maps)
+ *   bias  [L, d_out] f32
+ *   gain  [L, d_out]                    RMSNorm gain; NULL means all ones
+ *   Wk,Wv [L, n_kv_heads*head_dim, d_out]  projection weights, [out, in]
+ *   Kc,Vc [L, n_kv_heads, cache_len, head_dim]  caches; only positions
+ *                                       [pos0, pos0 + rows) are written
+ * Limits: d_in % 64 == 0, d_out % 128 == 0, head_dim in {64, 128},
+ *   (n_kv_heads*head_dim) % 128 == 0, pos0 + rows <= cache_len < 2^24,
+ *   rows_per_chunk == 0 (all rows in one pass) or a multiple of 128.
+ * stage_events (optional, may be NULL): host array of three cudaEvent_t that
+ *   the call records on `stream` before the first chunk's map GEMM, between
+ *   its map GEMM and its K/V GEMM, and after its K/V GEMM (instrumentation for
+ *   per-kernel timing; the events must have been created by the caller).
+ */
+typedef struct rf_fill_args {
+  int32_t n_layers;
+  int32_t d_in;
+  int32_t d_out;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t maps_on_host;
+  int64_t rows;
+  int64_t pos0;
+  int64_t cache_len;
+  int64_t rows_per_chunk;
+  double rope_theta;
+  double rms_eps;
+  const void* H;
+  const void* A;
+  const float* bias;
+  const void* gain;
+  const void* Wk;
+  const void* Wv;
+  void* Kc;
+  void* Vc;
+  void* const* stage_events;
+} rf_fill_args;
+
+/* Bytes of device workspace ridgefill_fill needs for these arguments
+ * (0 on invalid arguments).  Holds the predicted inputs of one row chunk
+ * [L, chunk, d_out] bf16, their per-tile sums of squares, and, for host
+ * maps, two map slots. */
+size_t ridgefill_fill_workspace_size(const rf_fill_args* args);
+
+/* Enqueue the fill described above on `stream`. */
+rf_status ridgefill_fill(const rf_fill_args* args, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Gated DeltaNet late layers                                                */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * rf_gdn_args -- end-of-fill recurrent state of L late Gated DeltaNet layers.
+ *
+ * Paper section 2.3 ("every filled row updates the shared state from its
+ * predicted input") and section 2.1.  For every layer l and head h, over rows
+ * r = 0 .. rows-1 in order, from u as in rf_fill_args:
+ *   k = normalize(u Wk_l[h]^T)   (k / sqrt(sum k^2 + l2_eps))
+ *   v = u Wv_l[h]^T,  alpha = sigmoid(u . Wa_l[h]),  beta = sigmoid(u . Wb_l[h])
+ *   S <- alpha S (I - beta k k^T) + beta v k^T        (S is d_v x d_k, f32)
+ * S starts from S0 (or zero) and the final S is written.  The rows are
+ * processed in chunks of `chunk` rows with the chunk-parallel form of the
+ * same recurrence.
+ *
+ * Layouts: H, A, bias, gain as in rf_fill_args; Wk [L, n_heads*d_k, d_out],
+ *   Wv [L, n_heads*d_v, d_out], Wa/Wb [L, n_heads, d_out] (bf16);
+ *   S0 (may be NULL) and S [L, n_heads, d_v, d_k] f32.
+ * Limits: d_in % 64 == 0, d_out % 128 == 0, d_k == d_v == 128, chunk == 64,
+ *   n_heads <= 64.
+ */
+typedef struct rf_gdn_args {
+  int32_t n_layers;
+  int32_t d_in;
+  int32_t d_out;
+  int32_t n_heads;
+  int32_t d_k;
+  int32_t d_v;
+  int32_t chunk;
+  int32_t maps_on_host;
+  int64_t rows;
+  int64_t rows_per_chunk;
+  double rms_eps;
+  double l2_eps;
+  const void* H;
+  const void* A;
+  const float* bias;
+  const void* gain;
+  const void* Wk;
+  const void* Wv;
+  const void* Wa;
+  const void* Wb;
+  const float* S0;
+  float* S;
+} rf_gdn_args;
+
+size_t ridgefill_gdn_workspace_size(const rf_gdn_args* args);
+rf_status ridgefill_fill_gdn(const rf_gdn_args* args, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Ridge fit                                                                 */
+/* ------------------------------------------------------------------------ */
+
+#define RF_FIT_ACCUMULATE 1
+#define RF_FIT_SOLVE 2
+
+/*
+ * rf_fit_args -- closed-form ridge maps from running sums (section 2.2,
+ * "The ridge map", "Fitting", "The penalty").
+ *
+ * RF_FIT_ACCUMULATE adds one batch of calibration pairs to caller-owned f64
+ * running sums (products of bf16 inputs formed exactly and summed in f32
+ * within the call, then added in f64):
+ *   G += X^T X [d_in, d_in],  C += X^T Y_l (column block l of [d_in, L*d_out]),
+ *   sx += sum_rows X [d_in],  sy += sum_rows Y_l [L, d_out],  count += rows.
+ * Zero the sums before the first batch; any batch split gives the same sums.
+ *
+ * RF_FIT_SOLVE solves from the sums, centring them first:
+ *   G~ = G - n mu_S mu_S^T, C~_l = C_l - n mu_S mu_l^T,
+ *   alpha = lambda * tr(G~) / d_in,
+ *   A_l = (solve(G~ + alpha I, C~_l))^T,  b_l = mu_l - A_l mu_S.
+ * The solve equilibrates the system by its diagonal and uses a blocked
+ * Cholesky factor.  Outputs A in the fill's layout [L, d_out, d_in] (bf16
+ * and/or f32) and b [L, d_out] f32; alpha_out (device f64, may be NULL).
+ *
+ * Layouts: X [rows, d_in] bf16; Y [L, rows, d_out] bf16.
+ * Limits: d_in % 128 == 0, d_out % 128 == 0, d_in <= 16384.
+ */
+typedef struct rf_fit_args {
+  int32_t n_layers;
+  int32_t d_in;
+  int32_t d_out;
+  int32_t flags;
+  int64_t rows;
+  double lambda;
+  const void* X;
+  const void* Y;
+  double* G;
+  double* C;
+  double* sx;
+  double* sy;
+  double* count;
+  void* A_out;
+  float* A_out_f32;
+  float* b_out;
+  double* alpha_out;
+} rf_fit_args;
+
+size_t ridgefill_fit_workspace_size(const rf_fit_args* args);
+rf_status ridgefill_fit(const rf_fit_args* args, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Status and host helpers                                                   */
+/* ------------------------------------------------------------------------ */
+
+/* Static description of a status code. */
+const char* ridgefill_status_string(rf_status status);
+
+/* Message of the last error returned on the calling thread ("" if none). */
+const char* ridgefill_last_error(void);
+
+/* Synchronises `stream`, stores the device error word in *code (0 = none,
+ * otherwise the id of the wait that ran out) and clears it. */
+rf_status ridgefill_device_error(void* stream, int* code);
+
+/* Section 2.5 compute ceiling: share of exact prefill work that remains,
+ * r = (S (N - T) + L T) / (L N); the speedup is at most 1/r. */
+double ridgefill_compute_share(int32_t split, int32_t n_layers, int64_t tail, int64_t prompt);
+
+/* ABI version (incremented on any change to the structs above). */
+int32_t ridgefill_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RIDGEFILL_H */

@@ -1,0 +1,219 @@
+// abi_common.cu -- status handling, tensor-map encoding, per-device state,
+// and the map-GEMM launch shared by the attention and GDN fills.
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+#include <string>
+
+#include "abi_common.h"
+
+namespace rf {
+
+namespace {
+thread_local std::string g_last_error;
+constexpr int kMaxDevices = 64;
+__device__ int g_device_error = 0;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess) {
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+  });
+  return fn;
+}
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kMaxDevices) return -1;
+  return d;
+}
+}  // namespace
+
+rf_status fail(rf_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+rf_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(RF_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+const char* last_error_cstr() { return g_last_error.c_str(); }
+void clear_last_error() { g_last_error.clear(); }
+
+int* device_error_word() {
+  static int* ptr[kMaxDevices] = {};
+  static std::mutex mu;
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (ptr[d] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    ptr[d] = static_cast<int*>(p);
+  }
+  return ptr[d];
+}
+
+int sm_count() {
+  static int cnt[kMaxDevices] = {};
+  const int d = current_device();
+  if (d < 0) return 0;
+  if (cnt[d] == 0) {
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+    cnt[d] = c;
+  }
+  return cnt[d];
+}
+
+bool make_tmap_3d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t d0,
+                  uint64_t d1, uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0,
+                  uint32_t box1, CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  if (d2 <= 1) {
+    d2 = 1;
+    stride2 = stride1 * (d1 > 0 ? d1 : 1);
+  }
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {stride1, stride2};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = fn(tm, dtype, 3, const_cast<void*>(base), dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+HostStreamer* host_streamer() {
+  static HostStreamer hs[kMaxDevices];
+  static std::mutex mu;
+  const int d = current_device();
+  if (d < 0) {
+    fail(RF_ERR_CUDA, "no current CUDA device");
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lk(mu);
+  HostStreamer& h = hs[d];
+  if (h.copy == nullptr) {
+    cudaError_t e = cudaStreamCreateWithFlags(&h.copy, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&h.copied[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.freed[i], cudaEventDisableTiming);
+    }
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
+    if (e != cudaSuccess) {
+      cuda_fail(e, "creating the map-copy stream");
+      h.copy = nullptr;
+      return nullptr;
+    }
+  }
+  return &h;
+}
+
+rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
+  GemmParams p{};
+  p.mode = kModeMap;
+  p.k_blocks = m.d_in / kBK;
+  const bool single = m.slot_layer >= 0;
+  const uint64_t brows = single ? static_cast<uint64_t>(m.d_out)
+                                : static_cast<uint64_t>(m.n_layers) * m.d_out;
+  const uint64_t in_row = static_cast<uint64_t>(m.d_in) * 2;
+  const uint64_t out_row = static_cast<uint64_t>(m.d_out) * 2;
+  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.H, m.d_in, m.rows, 1, in_row,
+                         0, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A, m.d_in, brows, 1,
+                          in_row, 0, kBK, m.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmO[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.xhat, m.d_out, m.rows,
+                          m.n_layers, out_row, out_row * m.R, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the map GEMM");
+  p.m_tiles = static_cast<int32_t>(ceil_div(m.rows, kBM));
+  p.n_tiles = static_cast<int32_t>(brows / m.bn);
+  p.batches = 1;
+  p.bn = m.bn;
+  p.group_m = 32;
+  p.rows = static_cast<int32_t>(m.rows);
+  p.ss_stride = static_cast<int32_t>(m.R);
+  p.d_out = m.d_out;
+  p.layer_base = single ? m.slot_layer : 0;
+  p.ss_tiles = m.d_out / m.bn;
+  p.bias = m.bias;
+  p.gain = static_cast<const __nv_bfloat16*>(m.gain);
+  p.ss_part = m.ss;
+  p.err = device_error_word();
+  if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  if (grid <= 0) return RF_OK;
+  cudaError_t e = launch_gemm(p, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "map GEMM launch");
+  return RF_OK;
+}
+
+}  // namespace rf
+
+// --------------------------------------------------------------- C ABI
+namespace rf {
+const char* last_error_cstr();
+void clear_last_error();
+}
+
+extern "C" const char* ridgefill_status_string(rf_status s) {
+  switch (s) {
+    case RF_OK: return "ok";
+    case RF_ERR_ARG: return "invalid argument";
+    case RF_ERR_SHAPE: return "unsupported or inconsistent shape";
+    case RF_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case RF_ERR_NOT_PINNED: return "host maps are not page-locked";
+    case RF_ERR_CUDA: return "CUDA error";
+    case RF_ERR_TIMEOUT: return "device wait timed out";
+    case RF_ERR_NUMERIC: return "ridge system not positive definite";
+    case RF_ERR_WORKSPACE: return "workspace missing or too small";
+  }
+  return "unknown status";
+}
+
+extern "C" const char* ridgefill_last_error(void) { return rf::last_error_cstr(); }
+
+extern "C" rf_status ridgefill_device_error(void* stream, int* code) {
+  if (code == nullptr) return rf::fail(RF_ERR_ARG, "code is NULL");
+  *code = 0;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return rf::cuda_fail(e, "cudaStreamSynchronize");
+  int* w = rf::device_error_word();
+  if (w == nullptr) return rf::fail(RF_ERR_CUDA, "device error word unavailable");
+  int v = 0;
+  e = cudaMemcpy(&v, w, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return rf::cuda_fail(e, "reading the device error word");
+  if (v != 0) {
+    const int zero = 0;
+    e = cudaMemcpy(w, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return rf::cuda_fail(e, "clearing the device error word");
+  }
+  *code = v;
+  return v == 0 ? RF_OK : rf::fail(RF_ERR_TIMEOUT, "device wait ran out at site %d", v);
+}
+
+extern "C" double ridgefill_compute_share(int32_t split, int32_t n_layers, int64_t tail,
+                                          int64_t prompt) {
+  if (n_layers <= 0 || prompt <= 0) return 0.0;
+  const double S = split, L = n_layers, T = static_cast<double>(tail),
+               N = static_cast<double>(prompt);
+  return (S * (N - T) + L * T) / (L * N);
+}
+
+extern "C" int32_t ridgefill_abi_version(void) { return 1; }

@@ -1,0 +1,466 @@
+// fill_gemm.cu -- persistent, warp-specialised tcgen05 GEMM with the fill's
+// epilogues (RidgeFill, "Training-Free Late-Layer Cache Fill for Faster
+// Prefill", sections 2.2 and 2.3).
+//
+//   map mode : X_hat = H A^T + b for every late layer in one grouped GEMM over
+//              the concatenated maps [A_1; ...; A_L] (B operand [L*d_out, d_in]);
+//              the epilogue adds b, accumulates per-row sums of squares of the
+//              f32 result (one partial per tile), multiplies by the RMSNorm gain
+//              and stores bf16 X_hat [L, rows, d_out] through TMA.
+//   kv mode  : per layer, X_hat_l W^T for the K and V weights; the epilogue
+//              applies the per-row RMS scale rsqrt(ss/d + eps), RoPE on K, and
+//              stores bf16 straight into the [layer, kv_head, pos, head_dim] cache.
+//   gdn mode : per GDN layer, X_hat_l times [Wk; Wv; Wa|Wb]; the epilogue applies
+//              the RMS scale, L2-normalises k per head, and writes f32 k, v and
+//              the gates (log alpha, beta) for the state kernel.
+//
+// Roles (256 threads, one CTA per SM): warp 0 issues TMA loads into a
+// kStages-deep ring, warp 1 issues tcgen05.mma (M=128, N=bn, K=16) into one of
+// two TMEM accumulators, warp 2 owns the TMEM allocation, warps 4-7 drain the
+// accumulators (TMEM lane = tile row) while the next tile accumulates.
+#include "rf_internal.h"
+#include "sm103_ptx.cuh"
+
+namespace rf {
+
+namespace {
+
+constexpr double kTwoPi = 6.283185307179586476925286766559;
+constexpr float kTwoPiHi = static_cast<float>(kTwoPi);
+constexpr float kTwoPiLo = static_cast<float>(kTwoPi - static_cast<double>(kTwoPiHi));
+constexpr float kInvTwoPi = static_cast<float>(1.0 / kTwoPi);
+
+// cos/sin of pos * f where f = fhi + flo (a float pair of the double frequency).
+// The product is carried exactly as hi + lo (FMA two-product), reduced by
+// 2*pi split in two floats (Cody-Waite), then evaluated by sincosf.
+__device__ __forceinline__ void rope_cs(float posf, float fhi, float flo, float& c, float& s) {
+  const float ph = posf * fhi;
+  const float pe = fmaf(posf, fhi, -ph);
+  const float pl = fmaf(posf, flo, pe);
+  const float k = rintf(ph * kInvTwoPi);
+  float r = fmaf(-k, kTwoPiHi, ph);
+  r = fmaf(-k, kTwoPiLo, r);
+  r += pl;
+  sincosf(r, &s, &c);
+}
+
+__device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& m, int& n, int& b) {
+  const int per_b = p.m_tiles * p.n_tiles;
+  b = t / per_b;
+  const int r = t - b * per_b;
+  const int gsz = p.group_m * p.n_tiles;
+  const int g = r / gsz;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.m_tiles - first_m, p.group_m);
+  const int rr = r - g * gsz;
+  m = first_m + rr % gm;
+  n = rr / gm;
+}
+
+// Which B segment a tile reads and its MMA width.
+struct TileB {
+  int seg;   // tensor map index
+  int nrow;  // first B row inside the segment
+  int bn;    // MMA N
+};
+
+__device__ __forceinline__ TileB tile_b(const GemmParams& p, int n) {
+  TileB t;
+  if (p.mode == kModeMap) {
+    t.seg = 0; t.nrow = n * p.bn; t.bn = p.bn;
+  } else if (p.mode == kModeKV) {
+    const bool v = n >= p.n_k_tiles;
+    t.seg = v ? 1 : 0; t.nrow = (v ? n - p.n_k_tiles : n) * p.bn; t.bn = p.bn;
+  } else {
+    if (n < p.n_k_tiles) {
+      t.seg = 0; t.nrow = n * p.bn; t.bn = p.bn;
+    } else if (n < p.n_k_tiles + p.n_v_tiles) {
+      t.seg = 1; t.nrow = (n - p.n_k_tiles) * p.bn; t.bn = p.bn;
+    } else {
+      t.seg = 2; t.nrow = 0; t.bn = 2 * p.gdn_heads;  // Wa rows then Wb rows
+    }
+  }
+  return t;
+}
+
+// Write 32 consecutive bf16 of this lane's row into a 64-column, 32-row
+// store box laid out with the 128-byte swizzle (16-byte chunk ^= row % 8).
+__device__ __forceinline__ void stage32(uint8_t* box, int lane, int col, const uint32_t (&w)[16]) {
+  const int ch0 = col >> 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int ch = (ch0 + c) ^ (lane & 7);
+    *reinterpret_cast<uint4*>(box + lane * 128 + ch * 16) =
+        make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+  }
+}
+
+__device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
+
+// ------------------------------------------------------------------ epilogues
+__device__ __forceinline__ void map_half(const uint32_t (&r)[32], const float* bp,
+                                         const __nv_bfloat16* gp, float& ss, uint32_t (&w)[16]) {
+  const float4* b4 = reinterpret_cast<const float4*>(bp);
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    const float4 bb = __ldg(b4 + j / 4);
+    float x0 = f32(r[j]) + bb.x, x1 = f32(r[j + 1]) + bb.y;
+    float x2 = f32(r[j + 2]) + bb.z, x3 = f32(r[j + 3]) + bb.w;
+    ss = fmaf(x0, x0, ss); ss = fmaf(x1, x1, ss);
+    ss = fmaf(x2, x2, ss); ss = fmaf(x3, x3, ss);
+    if (gp != nullptr) {
+      const uint2 gg = __ldg(reinterpret_cast<const uint2*>(gp + j));
+      const float2 g01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg.x));
+      const float2 g23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gg.y));
+      x0 *= g01.x; x1 *= g01.y; x2 *= g23.x; x3 *= g23.y;
+    }
+    w[j / 2] = pack_bf16(x0, x1);
+    w[j / 2 + 1] = pack_bf16(x2, x3);
+  }
+}
+
+__device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
+                             int m, int n, uint64_t* tempty) {
+  const int gcol = n * p.bn;
+  const int l = p.layer_base + gcol / p.d_out;
+  const int j0 = gcol % p.d_out;
+  const int row = m * kBM + q * 32 + lane;
+  const int nch = p.bn / 64;
+  float ss = 0.f;
+  for (int c = 0; c < nch; ++c) {
+    uint32_t r0[32], r1[32];
+    tmem_ld32(tcol + c * 64, r0);
+    tmem_ld32(tcol + c * 64 + 32, r1);
+    tmem_wait_ld();
+    if (c == nch - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+    }
+    const int col = j0 + c * 64;
+    const float* bp = p.bias + static_cast<size_t>(l) * p.d_out + col;
+    const __nv_bfloat16* gp =
+        p.gain != nullptr ? p.gain + static_cast<size_t>(l) * p.d_out + col : nullptr;
+    uint32_t w0[16], w1[16];
+    map_half(r0, bp, gp, ss, w0);
+    map_half(r1, bp + 32, gp != nullptr ? gp + 32 : nullptr, ss, w1);
+    uint8_t* box = stg + (c & 1) * kOutBoxBytes;
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+    stage32(box, lane, 0, w0);
+    stage32(box, lane, 32, w1);
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(&p.tmO[0], smem_u32(box), col, m * kBM + q * 32, l);
+      bulk_commit();
+    }
+  }
+  if (row < p.rows) {
+    p.ss_part[(static_cast<size_t>(l) * p.ss_tiles + j0 / p.bn) * p.ss_stride + row] = ss;
+  }
+}
+
+__device__ __forceinline__ float row_rms_scale(const GemmParams& p, int l, int row) {
+  float ssum = 0.f;
+  if (row < p.rows) {
+    const float* sp = p.ss_in + static_cast<size_t>(l) * p.ss_tiles * p.ss_stride + row;
+    for (int t = 0; t < p.ss_tiles; ++t) ssum += sp[static_cast<size_t>(t) * p.ss_stride];
+  }
+  return rsqrtf(fmaf(ssum, p.inv_d, p.eps));
+}
+
+__device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
+                            int m, int n, int l, uint64_t* tempty) {
+  const int row = m * kBM + q * 32 + lane;
+  const float rs = row_rms_scale(p, l, row);
+  const float posf = static_cast<float>(p.pos_base + row);
+  const bool is_k = n < p.n_k_tiles;
+  const int hd = p.head_dim;
+  const int half = hd / 2;
+  const int hpt = p.bn / hd;
+  const int head0 = (is_k ? n : n - p.n_k_tiles) * hpt;
+  const CUtensorMap* out = &p.tmO[is_k ? 0 : 1];
+  for (int hh = 0; hh < hpt; ++hh) {
+    const uint32_t hc = tcol + hh * hd;
+    if (lane == 0) bulk_wait_read<0>();
+    __syncwarp();
+    if (is_k) {
+      for (int i0 = 0; i0 < half; i0 += 32) {
+        uint32_t a[32], b[32];
+        tmem_ld32(hc + i0, a);
+        tmem_ld32(hc + half + i0, b);
+        tmem_wait_ld();
+        uint32_t w1[16], w2[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          float c0, s0, c1, s1;
+          rope_cs(posf, p.inv_freq_hi[i0 + j], p.inv_freq_lo[i0 + j], c0, s0);
+          rope_cs(posf, p.inv_freq_hi[i0 + j + 1], p.inv_freq_lo[i0 + j + 1], c1, s1);
+          const float xa = f32(a[j]) * rs, ya = f32(b[j]) * rs;
+          const float xb = f32(a[j + 1]) * rs, yb = f32(b[j + 1]) * rs;
+          w1[j / 2] = pack_bf16(xa * c0 - ya * s0, xb * c1 - yb * s1);
+          w2[j / 2] = pack_bf16(ya * c0 + xa * s0, yb * c1 + xb * s1);
+        }
+        stage32(stg + (i0 / 64) * kOutBoxBytes, lane, i0 % 64, w1);
+        stage32(stg + ((half + i0) / 64) * kOutBoxBytes, lane, (half + i0) % 64, w2);
+      }
+    } else {
+      for (int c0 = 0; c0 < hd; c0 += 32) {
+        uint32_t a[32];
+        tmem_ld32(hc + c0, a);
+        tmem_wait_ld();
+        uint32_t w[16];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) w[j / 2] = pack_bf16(f32(a[j]) * rs, f32(a[j + 1]) * rs);
+        stage32(stg + (c0 / 64) * kOutBoxBytes, lane, c0 % 64, w);
+      }
+    }
+    if (hh == hpt - 1) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+    }
+    fence_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      for (int bx = 0; bx < hd / 64; ++bx)
+        tma_store_3d(out, smem_u32(stg + bx * kOutBoxBytes), bx * 64,
+                     p.pos_base + m * kBM + q * 32, l * p.n_kv + head0 + hh);
+      bulk_commit();
+    }
+  }
+}
+
+__device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, int q, int lane, int m, int n,
+                             int l, uint64_t* tempty) {
+  const int row = m * kBM + q * 32 + lane;
+  const float rs = row_rms_scale(p, l, row);
+  const bool valid = row < p.rows;
+  const int H = p.gdn_heads;
+  const size_t ra = static_cast<size_t>(p.gdn_rows_alloc);
+  if (n < p.n_k_tiles + p.n_v_tiles) {
+    const bool is_k = n < p.n_k_tiles;
+    const int hpt = p.bn / 128;
+    const int head0 = (is_k ? n : n - p.n_k_tiles) * hpt;
+    float* base = is_k ? p.gdn_k : p.gdn_v;
+    for (int hh = 0; hh < hpt; ++hh) {
+      const uint32_t hc = tcol + hh * 128;
+      float scale = rs;
+      if (is_k) {
+        float nrm = 0.f;
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t a[32];
+          tmem_ld32(hc + c0, a);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float x = f32(a[j]) * rs;
+            nrm = fmaf(x, x, nrm);
+          }
+        }
+        scale = rs * rsqrtf(nrm + p.l2_eps);
+      }
+      float* dst = base + ((static_cast<size_t>(l) * H + head0 + hh) * ra + row) * 128;
+      for (int c0 = 0; c0 < 128; c0 += 32) {
+        uint32_t a[32];
+        tmem_ld32(hc + c0, a);
+        tmem_wait_ld();
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float4 v = make_float4(f32(a[j]) * scale, f32(a[j + 1]) * scale,
+                                   f32(a[j + 2]) * scale, f32(a[j + 3]) * scale);
+            *reinterpret_cast<float4*>(dst + c0 + j) = v;
+          }
+        }
+      }
+    }
+  } else {
+    // gate tile: columns [0, H) are the alpha logits, [H, 2H) the beta logits
+    for (int c0 = 0; c0 < 2 * H; c0 += 16) {
+      uint32_t a[32];
+      tmem_ld32(tcol + c0, a);  // reads 32 columns; only the first 16 are used
+      tmem_wait_ld();
+      if (valid) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const int c = c0 + j;
+          const float z = f32(a[j]) * rs;
+          float val;
+          if (c < H) {
+            val = fminf(z, 0.f) - log1pf(expf(-fabsf(z)));  // log sigmoid(z)
+          } else {
+            val = 1.f / (1.f + expf(-z));                    // sigmoid(z)
+          }
+          const int which = c < H ? 0 : 1;
+          const int h = c < H ? c : c - H;
+          p.gdn_gate[((static_cast<size_t>(l) * 2 + which) * H + h) * ra + row] = val;
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tempty);
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + kStages * kABytes;
+  uint8_t* stg_all = sB + kStages * kBBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 4 * kOutWarpBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&p.tmA);
+    tma_prefetch(&p.tmB[0]);
+    if (p.mode != kModeMap) tma_prefetch(&p.tmB[1]);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = p.m_tiles * p.n_tiles * p.batches;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        int m, n, b;
+        decode_tile(t, p, m, n, b);
+        const TileB tb = tile_b(p, n);
+        const uint32_t bytes = kABytes + tb.bn * kBK * 2;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[stage], bytes);
+          tma_load_3d(smem_u32(sA + stage * kABytes), &p.tmA, &full[stage], kb * kBK, m * kBM, b);
+          uint8_t* bdst = sB + stage * kBBytes;
+          if (tb.seg < 2) {
+            tma_load_3d(smem_u32(bdst), &p.tmB[tb.seg], &full[stage], kb * kBK, tb.nrow, b);
+          } else {
+            tma_load_3d(smem_u32(bdst), &p.tmB[2], &full[stage], kb * kBK, 0, b);
+            tma_load_3d(smem_u32(bdst + p.gdn_heads * 128), &p.tmB[3], &full[stage], kb * kBK, 0, b);
+          }
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        int m, n, b;
+        decode_tile(t, p, m, n, b);
+        const TileB tb = tile_b(p, n);
+        const uint32_t idesc = idesc_bf16_f32(kBM, tb.bn);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, kErrMma)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem_base + acc * kBNMax;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err, kErrMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * kABytes));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * kBBytes));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            // advance 16 bf16 (32 B) along K inside the swizzled 128-byte row
+            mma_bf16(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) mma_commit(&tfull[acc]);
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue warpgroup
+    const int q = warp - 4;
+    uint8_t* stg = stg_all + q * kOutWarpBytes;
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      int m, n, b;
+      decode_tile(t, p, m, n, b);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, kErrEpilogue)) break;
+      tc_fence_after();
+      const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBNMax;
+      if (p.mode == kModeMap) {
+        epilogue_map(p, tcol, stg, q, lane, m, n, &tempty[acc]);
+      } else if (p.mode == kModeKV) {
+        epilogue_kv(p, tcol, stg, q, lane, m, n, b, &tempty[acc]);
+      } else {
+        epilogue_gdn(p, tcol, q, lane, m, n, b, &tempty[acc]);
+      }
+    }
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  }
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 512);
+  }
+}
+
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(rf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kGemmSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  rf_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace rf

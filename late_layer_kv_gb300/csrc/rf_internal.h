@@ -1,0 +1,100 @@
+// rf_internal.h -- shared declarations of the RidgeFill CUDA library (not ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rf {
+
+// ------------------------------------------------------------ GEMM tiling
+constexpr int kStages = 4;         // TMA -> MMA shared-memory ring depth
+constexpr int kBM = 128;           // rows per tile (one TMEM lane per row)
+constexpr int kBK = 64;            // K elements per stage (one 128-byte row)
+constexpr int kBNMax = 256;        // max columns per tile (TMEM cols per accumulator)
+constexpr int kABytes = kBM * kBK * 2;
+constexpr int kBBytes = kBNMax * kBK * 2;
+constexpr int kOutBoxBytes = 64 * 32 * 2;   // one 64-col x 32-row bf16 store box
+constexpr int kOutWarpBytes = 2 * kOutBoxBytes;
+constexpr int kGemmThreads = 256;  // warp 0 TMA, warp 1 MMA, warp 2 TMEM, warps 4-7 epilogue
+constexpr int kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 4 * kOutWarpBytes + 256;
+
+enum GemmMode : int {
+  kModeMap = 0,      // X_hat = H A^T + b (times gain), row sums of squares
+  kModeKV = 1,       // K/V projection, RMS scale, RoPE on K, cache store
+  kModeGdnProj = 2,  // GDN projections: RMS scale, k L2-norm, v, sigmoid gates
+};
+
+// Device error word sites (which wait ran out).
+enum ErrSite : int {
+  kErrProducer = 1,
+  kErrMma = 2,
+  kErrEpilogue = 3,
+  kErrGdn = 4,
+};
+
+struct GemmParams {
+  CUtensorMap tmA;     // A operand, K-major 3D {K, rows, batch}, box {64, 128, 1}
+  CUtensorMap tmB[4];  // B operand segments, K-major 3D {K, n, batch}, box {64, bn|16, 1}
+  CUtensorMap tmO[2];  // outputs, 3D, box {64, 32, 1}
+  int32_t mode;
+  int32_t k_blocks;    // K / 64
+  int32_t m_tiles;
+  int32_t n_tiles;     // tiles along N per batch entry
+  int32_t batches;     // batch entries (layers) the tile loop covers
+  int32_t bn;          // MMA N of a tile
+  int32_t group_m;     // raster group height
+  int32_t rows;        // valid rows of this launch
+  int32_t ss_stride;   // row stride of the sum-of-squares partials
+  int32_t d_out;
+  int32_t layer_base;  // map mode: layer of B row 0
+  int32_t ss_tiles;    // partials per row per layer
+  // map epilogue
+  const float* bias;
+  const __nv_bfloat16* gain;
+  float* ss_part;
+  // K/V epilogue
+  const float* ss_in;
+  int32_t n_k_tiles;
+  int32_t n_kv;
+  int32_t head_dim;
+  int32_t pos_base;
+  float inv_d;
+  float eps;
+  // GDN projection epilogue
+  float* gdn_k;        // [L, rows_alloc, H, dk] f32
+  float* gdn_v;        // [L, rows_alloc, H, dv] f32
+  float* gdn_gate;     // [L, rows_alloc, 2, H] f32 (log alpha, beta)
+  int32_t gdn_heads;
+  int32_t gdn_rows_alloc;
+  int32_t n_v_tiles;
+  float l2_eps;
+  int* err;
+  float inv_freq_hi[64];
+  float inv_freq_lo[64];
+};
+
+cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
+
+// ------------------------------------------------------------ GDN state
+struct GdnStateParams {
+  const float* k;      // [L, rows_alloc, H, dk]
+  const float* v;      // [L, rows_alloc, H, dv]
+  const float* gate;   // [L, rows_alloc, 2, H]
+  const float* S0;     // [L, H, dv, dk] or null
+  float* S;            // [L, H, dv, dk]
+  int32_t layers;
+  int32_t heads;
+  int32_t rows;        // rows of this launch
+  int32_t rows_alloc;
+  int32_t chunk;
+  int32_t first;       // 1 if S starts from S0/zero, 0 if it continues from S
+  int* err;
+};
+cudaError_t launch_gdn_state(const GdnStateParams& p, cudaStream_t stream);
+
+// ------------------------------------------------------------ fit
+struct FitParams;  // defined in fit.cu
+
+}  // namespace rf

@@ -1,0 +1,308 @@
+"""Thin Python binding of ``libridgefill.so`` (argument marshalling only).
+
+The functions take torch tensors for device memory and streams, check their
+dtype, device and layout, fill the C argument structs and call the library.
+Every step of the fill and the fit runs in the library's CUDA kernels; there
+is no fallback: if the library is missing or fails to load, these functions
+raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+_lib = None
+
+RF_FIT_ACCUMULATE = 1
+RF_FIT_SOLVE = 2
+
+STATUS = {
+    0: "RF_OK", 1: "RF_ERR_ARG", 2: "RF_ERR_SHAPE", 3: "RF_ERR_ALIGN", 4: "RF_ERR_NOT_PINNED",
+    5: "RF_ERR_CUDA", 6: "RF_ERR_TIMEOUT", 7: "RF_ERR_NUMERIC", 8: "RF_ERR_WORKSPACE",
+}
+
+_vp = ctypes.c_void_p
+
+
+class FillArgs(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("d_in", ctypes.c_int32), ("d_out", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+        ("maps_on_host", ctypes.c_int32), ("rows", ctypes.c_int64), ("pos0", ctypes.c_int64),
+        ("cache_len", ctypes.c_int64), ("rows_per_chunk", ctypes.c_int64),
+        ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_double),
+        ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
+        ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp),
+    ]
+
+
+class GdnArgs(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("d_in", ctypes.c_int32), ("d_out", ctypes.c_int32),
+        ("n_heads", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+        ("chunk", ctypes.c_int32), ("maps_on_host", ctypes.c_int32),
+        ("rows", ctypes.c_int64), ("rows_per_chunk", ctypes.c_int64),
+        ("rms_eps", ctypes.c_double), ("l2_eps", ctypes.c_double),
+        ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
+        ("Wa", _vp), ("Wb", _vp), ("S0", _vp), ("S", _vp),
+    ]
+
+
+class FitArgs(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("d_in", ctypes.c_int32), ("d_out", ctypes.c_int32),
+        ("flags", ctypes.c_int32), ("rows", ctypes.c_int64), ("lam", ctypes.c_double),
+        ("X", _vp), ("Y", _vp), ("G", _vp), ("C", _vp), ("sx", _vp), ("sy", _vp),
+        ("count", _vp), ("A_out", _vp), ("A_out_f32", _vp), ("b_out", _vp), ("alpha_out", _vp),
+    ]
+
+
+class RidgeFillError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{STATUS.get(status, status)}: {msg}")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(rebuild: bool = True) -> ctypes.CDLL:
+    """Load ``libridgefill.so`` (building it first if it is stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build() if rebuild else _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"RidgeFill CUDA library not found at {path}")
+    lib = ctypes.CDLL(path)
+    lib.ridgefill_fill_workspace_size.argtypes = [ctypes.POINTER(FillArgs)]
+    lib.ridgefill_fill_workspace_size.restype = ctypes.c_size_t
+    lib.ridgefill_fill.argtypes = [ctypes.POINTER(FillArgs), _vp, ctypes.c_size_t, _vp]
+    lib.ridgefill_fill.restype = ctypes.c_int
+    lib.ridgefill_gdn_workspace_size.argtypes = [ctypes.POINTER(GdnArgs)]
+    lib.ridgefill_gdn_workspace_size.restype = ctypes.c_size_t
+    lib.ridgefill_fill_gdn.argtypes = [ctypes.POINTER(GdnArgs), _vp, ctypes.c_size_t, _vp]
+    lib.ridgefill_fill_gdn.restype = ctypes.c_int
+    lib.ridgefill_fit_workspace_size.argtypes = [ctypes.POINTER(FitArgs)]
+    lib.ridgefill_fit_workspace_size.restype = ctypes.c_size_t
+    lib.ridgefill_fit.argtypes = [ctypes.POINTER(FitArgs), _vp, ctypes.c_size_t, _vp]
+    lib.ridgefill_fit.restype = ctypes.c_int
+    lib.ridgefill_status_string.argtypes = [ctypes.c_int]
+    lib.ridgefill_status_string.restype = ctypes.c_char_p
+    lib.ridgefill_last_error.argtypes = []
+    lib.ridgefill_last_error.restype = ctypes.c_char_p
+    lib.ridgefill_device_error.argtypes = [_vp, ctypes.POINTER(ctypes.c_int)]
+    lib.ridgefill_device_error.restype = ctypes.c_int
+    lib.ridgefill_compute_share.argtypes = [ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                            ctypes.c_int64]
+    lib.ridgefill_compute_share.restype = ctypes.c_double
+    lib.ridgefill_abi_version.argtypes = []
+    lib.ridgefill_abi_version.restype = ctypes.c_int32
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise RidgeFillError(status, load().ridgefill_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+def _stream(stream) -> int:
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _event_array(events):
+    if events is None:
+        return None
+    arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
+    return arr
+
+
+def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
+              rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
+              stage_events=None) -> FillArgs:
+    L, d_out, d_in = A.shape
+    rows = H.shape[0]
+    n_kv = Kc.shape[1]
+    cache_len = Kc.shape[2]
+    host = not A.is_cuda
+    _dev(H, "H", torch.bfloat16, (rows, d_in))
+    if host:
+        if A.dtype != torch.bfloat16 or not A.is_contiguous() or not A.is_pinned():
+            raise ValueError("host maps must be contiguous, pinned bf16")
+    else:
+        _dev(A, "A", torch.bfloat16)
+    _dev(bias, "bias", torch.float32, (L, d_out))
+    if gain is not None:
+        _dev(gain, "gain", torch.bfloat16, (L, d_out))
+    _dev(Wk, "Wk", torch.bfloat16, (L, n_kv * head_dim, d_out))
+    _dev(Wv, "Wv", torch.bfloat16, (L, n_kv * head_dim, d_out))
+    _dev(Kc, "Kc", torch.bfloat16, (L, n_kv, cache_len, head_dim))
+    _dev(Vc, "Vc", torch.bfloat16, (L, n_kv, cache_len, head_dim))
+    ev = _event_array(stage_events)
+    a = FillArgs(L, d_in, d_out, n_kv, head_dim, 1 if host else 0, rows, pos0, cache_len,
+                 rows_per_chunk, float(rope_theta), float(rms_eps), _ptr(H), _ptr(A),
+                 _ptr(bias), _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Kc), _ptr(Vc),
+                 ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None)
+    a._events_keepalive = ev
+    return a
+
+
+def fill_workspace_size(args: FillArgs) -> int:
+    return int(load().ridgefill_fill_workspace_size(ctypes.byref(args)))
+
+
+def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
+                   rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
+                   workspace: Optional[torch.Tensor] = None, stream=None,
+                   stage_events=None) -> None:
+    """Write the K/V cache of the prefix rows of every late attention layer.
+
+    ``H`` [rows, d_in] bf16, ``A`` [L, d_out, d_in] bf16 (device, or pinned host
+    memory to stream the maps), ``bias`` [L, d_out] f32, ``gain`` [L, d_out] bf16
+    or None, ``Wk``/``Wv`` [L, n_kv*hd, d_out] bf16, ``Kc``/``Vc``
+    [L, n_kv, cache_len, hd] bf16 (positions ``pos0 .. pos0+rows-1`` written).
+    ``stage_events``: optional three ``torch.cuda.Event`` recorded around the
+    first chunk's map GEMM and K/V GEMM.
+    """
+    args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
+                     rms_eps=rms_eps, pos0=pos0, rows_per_chunk=rows_per_chunk,
+                     stage_events=stage_events)
+    lib = load()
+    need = int(lib.ridgefill_fill_workspace_size(ctypes.byref(args)))
+    if need == 0:
+        _check(lib.ridgefill_fill(ctypes.byref(args), None, 0, _stream(stream)))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=H.device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    _check(lib.ridgefill_fill(ctypes.byref(args), _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
+             l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0) -> GdnArgs:
+    L, d_out, d_in = A.shape
+    rows = H.shape[0]
+    d_k = Wk.shape[1] // n_heads
+    d_v = Wv.shape[1] // n_heads
+    host = not A.is_cuda
+    _dev(H, "H", torch.bfloat16, (rows, d_in))
+    if host:
+        if A.dtype != torch.bfloat16 or not A.is_contiguous() or not A.is_pinned():
+            raise ValueError("host maps must be contiguous, pinned bf16")
+    else:
+        _dev(A, "A", torch.bfloat16)
+    _dev(bias, "bias", torch.float32, (L, d_out))
+    if gain is not None:
+        _dev(gain, "gain", torch.bfloat16, (L, d_out))
+    _dev(Wk, "Wk", torch.bfloat16, (L, n_heads * d_k, d_out))
+    _dev(Wv, "Wv", torch.bfloat16, (L, n_heads * d_v, d_out))
+    _dev(Wa, "Wa", torch.bfloat16, (L, n_heads, d_out))
+    _dev(Wb, "Wb", torch.bfloat16, (L, n_heads, d_out))
+    _dev(S, "S", torch.float32, (L, n_heads, d_v, d_k))
+    if S0 is not None:
+        _dev(S0, "S0", torch.float32, (L, n_heads, d_v, d_k))
+    return GdnArgs(L, d_in, d_out, n_heads, d_k, d_v, chunk, 1 if host else 0, rows,
+                   rows_per_chunk, float(rms_eps), float(l2_eps), _ptr(H), _ptr(A), _ptr(bias),
+                   _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Wa), _ptr(Wb), _ptr(S0), _ptr(S))
+
+
+def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
+                       l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
+                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """End-of-fill recurrent state ``S`` [L, H, dv, dk] f32 of Gated DeltaNet layers."""
+    args = gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, n_heads=n_heads, rms_eps=rms_eps,
+                    l2_eps=l2_eps, S0=S0, chunk=chunk, rows_per_chunk=rows_per_chunk)
+    lib = load()
+    need = int(lib.ridgefill_gdn_workspace_size(ctypes.byref(args)))
+    if need == 0:
+        _check(lib.ridgefill_fill_gdn(ctypes.byref(args), None, 0, _stream(stream)))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=H.device)
+    _check(lib.ridgefill_fill_gdn(ctypes.byref(args), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+class FitSums:
+    """Caller-owned f64 running sums of the ridge fit (device tensors)."""
+
+    def __init__(self, n_layers: int, d_in: int, d_out: int, device="cuda"):
+        f64 = torch.float64
+        self.n_layers, self.d_in, self.d_out = n_layers, d_in, d_out
+        self.G = torch.zeros((d_in, d_in), dtype=f64, device=device)
+        self.C = torch.zeros((d_in, n_layers * d_out), dtype=f64, device=device)
+        self.sx = torch.zeros((d_in,), dtype=f64, device=device)
+        self.sy = torch.zeros((n_layers, d_out), dtype=f64, device=device)
+        self.count = torch.zeros((1,), dtype=f64, device=device)
+
+
+def _fit_call(sums: FitSums, flags: int, X=None, Y=None, lam: float = 0.0, A_out=None,
+              A_out_f32=None, b_out=None, alpha_out=None, workspace=None, stream=None):
+    L, d_in, d_out = sums.n_layers, sums.d_in, sums.d_out
+    rows = 0
+    if X is not None:
+        rows = X.shape[0]
+        _dev(X, "X", torch.bfloat16, (rows, d_in))
+        _dev(Y, "Y", torch.bfloat16, (L, rows, d_out))
+    if A_out is not None:
+        _dev(A_out, "A_out", torch.bfloat16, (L, d_out, d_in))
+    if A_out_f32 is not None:
+        _dev(A_out_f32, "A_out_f32", torch.float32, (L, d_out, d_in))
+    if b_out is not None:
+        _dev(b_out, "b_out", torch.float32, (L, d_out))
+    args = FitArgs(L, d_in, d_out, flags, rows, float(lam), _ptr(X), _ptr(Y), _ptr(sums.G),
+                   _ptr(sums.C), _ptr(sums.sx), _ptr(sums.sy), _ptr(sums.count), _ptr(A_out),
+                   _ptr(A_out_f32), _ptr(b_out), _ptr(alpha_out))
+    lib = load()
+    need = int(lib.ridgefill_fit_workspace_size(ctypes.byref(args)))
+    if workspace is None:
+        dev = sums.G.device
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    _check(lib.ridgefill_fit(ctypes.byref(args), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ridgefill_fit_accumulate(sums: FitSums, X, Y, *, workspace=None, stream=None) -> None:
+    """Add calibration pairs ``X`` [n, d_in], ``Y`` [L, n, d_out] (bf16) to the sums."""
+    _fit_call(sums, RF_FIT_ACCUMULATE, X=X, Y=Y, workspace=workspace, stream=stream)
+
+
+def ridgefill_fit_solve(sums: FitSums, lam: float, *, A_out=None, A_out_f32=None, b_out=None,
+                        alpha_out=None, workspace=None, stream=None) -> None:
+    """Solve the ridge maps from the sums (``alpha = lam * tr(X~^T X~)/d_in``)."""
+    _fit_call(sums, RF_FIT_SOLVE, lam=lam, A_out=A_out, A_out_f32=A_out_f32, b_out=b_out,
+              alpha_out=alpha_out, workspace=workspace, stream=stream)
+
+
+def device_error(stream=None) -> int:
+    """Synchronise ``stream`` and return (and clear) the device error word."""
+    code = ctypes.c_int(0)
+    load().ridgefill_device_error(_stream(stream), ctypes.byref(code))
+    return int(code.value)
+
+
+def compute_share(split: int, n_layers: int, tail: int, prompt: int) -> float:
+    return float(load().ridgefill_compute_share(split, n_layers, tail, prompt))

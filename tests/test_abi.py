@@ -1,0 +1,77 @@
+"""CPU checks of the C ABI: the library builds, loads without a GPU, exports every
+function `include/ridgefill.h` declares, and its host helpers and struct layouts
+agree with the header."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ridgefill.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(ridgefill_\w+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), f"{n} not exported"
+    from late_layer_kv_gb300 import library_path
+    out = subprocess.run(["nm", "-D", "--defined-only", library_path()], capture_output=True,
+                         text=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}\b", out), f"{n} missing from the dynamic symbol table"
+
+
+def test_compute_share_helper_matches_printed_ceilings(lib):
+    from late_layer_kv_gb300 import compute_share
+    for N, sp in ((9216, 1.64), (16384, 1.78), (32768, 1.88)):
+        assert abs(1.0 / compute_share(24, 48, 2048, N) - sp) <= 0.005
+
+
+def _c_sizeof(struct):
+    code = f'#include "ridgefill.h"\n#include <stdio.h>\n#include <stddef.h>\nint main(void){{printf("%zu", sizeof({struct}));return 0;}}\n'
+    exe = os.path.join(tempfile.mkdtemp(prefix="rf_sizeof_"), "sizeof_" + struct)
+    r = subprocess.run(["gcc", "-x", "c", "-I", os.path.join(ROOT, "include"), "-o", exe, "-"],
+                       input=code, text=True, capture_output=True)
+    if r.returncode != 0:
+        pytest.skip("no C compiler")
+    return int(subprocess.run([exe], capture_output=True, text=True).stdout)
+
+
+def test_ctypes_structs_match_header():
+    from late_layer_kv_gb300 import ridgefill as rb
+    assert ctypes.sizeof(rb.FillArgs) == _c_sizeof("rf_fill_args")
+    assert ctypes.sizeof(rb.GdnArgs) == _c_sizeof("rf_gdn_args")
+    assert ctypes.sizeof(rb.FitArgs) == _c_sizeof("rf_fit_args")
+
+
+def test_invalid_arguments_fail_without_a_gpu(lib):
+    from late_layer_kv_gb300 import ridgefill as rb
+    a = rb.FillArgs()
+    a.n_layers = 1
+    a.d_in = 100  # not a multiple of 64
+    a.d_out = 256
+    a.n_kv_heads = 2
+    a.head_dim = 64
+    assert lib.ridgefill_fill_workspace_size(ctypes.byref(a)) == 0
+    assert lib.ridgefill_fill(ctypes.byref(a), None, 0, None) == 2  # RF_ERR_SHAPE
+    assert b"d_in" in lib.ridgefill_last_error()
+    assert lib.ridgefill_status_string(2) == b"unsupported or inconsistent shape"
+
+
+def test_workspace_size_formula(lib):
+    from late_layer_kv_gb300 import ridgefill as rb
+    a = rb.FillArgs(20, 4096, 4096, 8, 128, 0, 14336, 0, 16384, 0, 5e5, 1e-6)
+    ws = lib.ridgefill_fill_workspace_size(ctypes.byref(a))
+    xhat = 20 * 14336 * 4096 * 2
+    ss = 20 * (4096 // 256) * 14336 * 4
+    assert xhat + ss <= ws <= xhat + ss + 1024
