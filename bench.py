@@ -206,6 +206,8 @@ def run_ours(args, shape):
     stream = torch.cuda.current_stream(dev)
     steps = args.steps
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for e in sum(ev, []):
+        e.record(stream)  # torch creates the CUDA event on first record
 
     def step(i=None):
         ridgefill_fill(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc,
@@ -276,7 +278,11 @@ def run_ours(args, shape):
     e2e_value = token_layers * world / (e2e_ms / 1000.0)
 
     peaks, src = _peaks()
-    peak = float(peaks["bf16_tflops_sustained"])
+    # a timed region of a few seconds or more runs under the power cap: compare with the
+    # sustained cuBLAS figure; shorter regions with the burst figure
+    sustained = ms >= 2000.0
+    peak_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    peak = float(peaks[peak_key])
     map_flops = 2.0 * rows * L * shape.d * shape.d
     achieved = map_flops / (map_ms / 1000.0) / 1e12
     total_flops = rows * L * _flops_per_row_layer(shape)
@@ -303,7 +309,8 @@ def run_ours(args, shape):
             "roofline": {"bound": "tensor", "kernel": "map GEMM (rf_gemm_kernel, map mode)",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{src} bf16_tflops_sustained"},
+                         "peak_source": f"{src} {peak_key}",
+                         "timed_region_ms": ms},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": "token-layers/s",
                     "h2d_bytes_per_step": int(H_host.numel() * 2),
@@ -323,7 +330,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama8b_16k")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=512)
+    ap.add_argument("--cpu-rows", type=int, default=4096)
     ap.add_argument("--ref-rows", type=int, default=64)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

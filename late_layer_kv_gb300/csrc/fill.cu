@@ -137,10 +137,6 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
   for (const void* p : dev)
     if (p != nullptr && !aligned16(p)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
   if (!aligned16(a->A)) return fail(RF_ERR_ALIGN, "A is not 16-byte aligned");
-  FillPlan pl;
-  plan_fill(a, &pl);
-  if (workspace == nullptr || ws_bytes < pl.total)
-    return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes", pl.total);
   if (a->maps_on_host) {
     cudaPointerAttributes attr;
     cudaError_t e = cudaPointerGetAttributes(&attr, a->A);
@@ -149,6 +145,10 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
       return fail(RF_ERR_NOT_PINNED, "maps_on_host set but A is not page-locked host memory");
     }
   }
+  FillPlan pl;
+  plan_fill(a, &pl);
+  if (workspace == nullptr || ws_bytes < pl.total)
+    return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes", pl.total);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* xhat = ws + pl.off_xhat;

@@ -134,11 +134,11 @@ def test_bad_arguments_are_rejected():
     Kc, Vc = new_cache(1, 2, 16, 64)
     a = rb.fill_args(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc, head_dim=64,
                      rope_theta=1e4, rms_eps=1e-6)
-    ws = torch.empty(rb.fill_workspace_size(a) + 4096, dtype=torch.uint8, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
     host_map = d["A"].cpu()  # pageable, not pinned
     a.maps_on_host = 1
     a.A = host_map.data_ptr()
+    ws = torch.empty(rb.fill_workspace_size(a), dtype=torch.uint8, device="cuda")
     assert lib.ridgefill_fill(ctypes.byref(a), ws.data_ptr(), ws.numel(), s) == 4
     a.maps_on_host = 0
     a.A = d["A"].data_ptr()
