@@ -118,6 +118,30 @@ size_t ridgefill_fill_workspace_size(const rf_fill_args* args);
 rf_status ridgefill_fill(const rf_fill_args* args, void* workspace, size_t workspace_bytes,
                          void* stream);
 
+/*
+ * ridgefill_fill_noalloc -- the same fill for callers that cannot allocate
+ * device memory.  The paper has no counterpart: it is a packaging variant.
+ *
+ * Some callers have no allocator at hand (a host engine that owns every
+ * device buffer and gives plugins none, or code running after the engine has
+ * divided up all device memory).  They pass inputs and outputs exactly as for
+ * ridgefill_fill but no workspace; the scratch lives in a library-owned
+ * device array of RF_NOALLOC_SCRATCH_BYTES that every GPU loading the library
+ * holds until exit.  The call allocates nothing.
+ *  - Rows are processed in the largest 128-row multiple whose scratch fits
+ *    (rows_per_chunk, if set, caps it); results equal ridgefill_fill's.
+ *  - If one 128-row chunk does not fit (n_layers * d_out too large) the call
+ *    returns RF_ERR_WORKSPACE with the required size in ridgefill_last_error().
+ *  - maps_on_host = 1 is rejected (RF_ERR_ARG).
+ *  - The array is shared by all calls on a device and keeps the last call's
+ *    contents (nothing in it needs to start at zero); calls that overlap on
+ *    the GPU race on it, so order them on one stream.
+ *  - The first call on a device looks up the array's address with that
+ *    device current; make it before any stream capture.
+ */
+#define RF_NOALLOC_SCRATCH_BYTES (64u << 20)
+rf_status ridgefill_fill_noalloc(const rf_fill_args* args, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Gated DeltaNet late layers                                                */
 /* ------------------------------------------------------------------------ */

@@ -1,0 +1,90 @@
+// fill_noalloc.cu -- ridgefill_fill_noalloc: the attention fill without a
+// caller-provided workspace.
+//
+// Some callers have no way to obtain device memory on demand: a host engine
+// that hands out every device buffer itself and offers plugins no allocator,
+// or code that runs once the engine has divided up all of device memory.
+// Such callers can still pass their inputs and outputs, but not a workspace.
+// This entry point keeps its scratch (the predicted layer inputs of one row
+// chunk and their sums of squares) in a fixed-size array in device global
+// memory that belongs to the library.  Every GPU that loads the library holds
+// that array until the process exits.
+//
+// Notes for callers:
+//  - The array is shared by every call on a device and keeps the contents of
+//    the last call.  Nothing in it has to start at zero: each chunk writes
+//    every scratch element it later reads.  Two calls whose work overlaps on
+//    the GPU (different streams without ordering, or different host threads)
+//    race on the array; order them on one stream.
+//  - The first call on a device looks up the array's device address (once per
+//    device, with that device current); make that first call before any
+//    stream capture.
+//  - Host-memory maps (maps_on_host = 1) are not supported here: their two
+//    map slots would not fit in the array.
+//  - The call itself allocates nothing: no cudaMalloc, cudaFree or allocating
+//    library routine.
+#include <mutex>
+
+#include "abi_common.h"
+
+namespace rf {
+namespace {
+
+static __device__ __align__(256) unsigned char g_fill_scratch[RF_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDev = 64;
+
+// Device address of g_fill_scratch on the current device (host code must not
+// use the symbol itself: on the host it only names a stand-in).
+rf_status scratch_address(void** out) {
+  static void* addr[kMaxDev] = {};
+  static std::mutex mu;
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDev) return fail(RF_ERR_CUDA, "device index %d out of range", dev);
+  std::lock_guard<std::mutex> lk(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_fill_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return RF_OK;
+}
+
+}  // namespace
+}  // namespace rf
+
+using namespace rf;
+
+extern "C" rf_status ridgefill_fill_noalloc(const rf_fill_args* a, void* stream) {
+  if (a == nullptr) return fail(RF_ERR_ARG, "args is NULL");
+  if (a->maps_on_host != 0)
+    return fail(RF_ERR_ARG, "ridgefill_fill_noalloc does not stream host maps (maps_on_host = 1)");
+  rf_fill_args c = *a;
+  // largest chunk (multiple of 128 rows) whose workspace fits the static scratch
+  const int64_t want = a->rows_per_chunk > 0 ? a->rows_per_chunk
+                                             : ceil_div(a->rows > 0 ? a->rows : 1, kBM) * kBM;
+  int64_t best = 0;
+  for (int64_t r = kBM; r <= want; r += kBM) {
+    c.rows_per_chunk = r;
+    const size_t need = ridgefill_fill_workspace_size(&c);
+    if (need == 0) return ridgefill_fill(&c, nullptr, 0, stream);  // reports the argument error
+    if (need > RF_NOALLOC_SCRATCH_BYTES) break;
+    best = r;
+  }
+  if (best == 0) {
+    c.rows_per_chunk = kBM;
+    return fail(RF_ERR_WORKSPACE,
+                "ridgefill_fill_noalloc: one 128-row chunk needs %zu bytes of scratch but the "
+                "static scratch holds %zu bytes (reduce n_layers * d_out or use ridgefill_fill)",
+                ridgefill_fill_workspace_size(&c), static_cast<size_t>(RF_NOALLOC_SCRATCH_BYTES));
+  }
+  c.rows_per_chunk = best;
+  void* scratch = nullptr;
+  rf_status st = scratch_address(&scratch);
+  if (st != RF_OK) return st;
+  return ridgefill_fill(&c, scratch, RF_NOALLOC_SCRATCH_BYTES, stream);
+}
