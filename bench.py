@@ -1,14 +1,21 @@
 #!/usr/bin/env python
-"""Benchmark of the RidgeFill late-layer cache fill on GB300.
+"""Benchmark of the RidgeFill late-layer fill on GB300.
 
-One step = one ridgefill_fill call over the whole prefix of one synthetic
-prompt: the grouped map GEMM for every late layer and the K/V GEMM that writes
-the caches.  The metric is filled token-layers per second ((N - T) * L_late /
-step time), also reported as fill-stage ms and as a fraction of the bf16
-tensor peak.  With torchrun (N > 1) every rank fills its own prompt (replicas,
-no collective on the data path); the timing takes the max over ranks.
+One step = one pass of the fill over the whole prefix of one synthetic prompt
+(N - T filled rows through every late layer).  The metric is filled
+token-layers per second: (N - T) * L_late / step time.  Alongside it the line
+reports the fill-stage ms, the share of the bf16 tensor peak, per-kernel stage
+times (CUDA events recorded by the library between its launches on the
+launching stream), the roofline of the dominant kernel, an end-to-end figure
+through the public call with host buffers, and the CPU oracle's rate.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+Workloads (``--workload``):
+  llama8b_16k (default)           attention fill, maps in HBM
+  dense27b_{16k,32k,64k,120k}      27B-class dense shape, rows processed in chunks
+  hostmaps_{16k,64k}               maps in pinned host memory, streamed per layer
+  hybrid_gdn_32k                   15 Gated DeltaNet + 5 attention late layers
+With torchrun (N > 1) every rank fills its own prompt (replicas, no collective
+on the data path); the timing takes the max over ranks.
 """
 from __future__ import annotations
 
@@ -21,6 +28,7 @@ import subprocess
 import sys
 import threading
 import time
+from dataclasses import replace
 
 import numpy as np
 import torch
@@ -28,15 +36,18 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import WORKLOADS, fill_inputs, to_f64  # noqa: E402
+from synthetic import WORKLOADS, FillShape, GdnShape, fill_inputs, gdn_inputs, to_f64  # noqa: E402
 
-PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+METRIC = "filled token-layers/s (fill-stage ms and % of GB300 bf16 tensor peak alongside)"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                  "sm_max_mhz": 2070.0}
+N_SM = 152
+FP32_LANES_PER_SM = 128
 
-# DRAM bytes per launch of the map GEMM from an ncu capture, valid only for the
-# kernel source with this digest (otherwise reported as null).
+# DRAM bytes per launch of the dominant kernel from an ncu capture, valid only
+# for the kernel source with this digest (otherwise reported as null).
 PROFILED_TRAFFIC = {
-    "kernel_sha256": None,
-    "map_gemm_bytes_per_launch": None,
+    "llama8b_16k": {"kernel_sha256": None, "bytes_per_launch": None},
 }
 
 
@@ -44,8 +55,7 @@ def _peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
-            d = json.load(f)
-        return d, "measured"
+            return json.load(f), "measured"
     return PEAKS_FALLBACK, "fallback"
 
 
@@ -65,10 +75,7 @@ class ClockSampler:
          "clocks_event_reasons.sw_power_cap")
 
     def __init__(self, index: int):
-        self.index = index
-        self.proc = None
-        self.lines = []
-        self.thread = None
+        self.index, self.proc, self.lines, self.thread = index, None, [], None
 
     def start(self):
         try:
@@ -94,7 +101,7 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
@@ -103,6 +110,7 @@ class ClockSampler:
             try:
                 sm.append(float(parts[0]))
                 mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
             except ValueError:
                 continue
             for nm, v in zip(names, parts[3:7]):
@@ -110,31 +118,13 @@ class ClockSampler:
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
 def _dist():
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return world, rank, local
-
-
-def _flops_per_row_layer(shape) -> float:
-    # map d_in*d_out plus the layer's K and V projections, 2 flops per MAC
-    return 2.0 * (shape.d * shape.d + shape.d * 2 * shape.kv_width)
-
-
-def cpu_oracle_rate(shape, inp, sample_rows: int):
-    """Filled token-layers/s of the f64 oracle on a seeded row sample."""
-    import oracle
-    o = {k: to_f64(v) for k, v in inp.items()}
-    idx = np.sort(np.random.default_rng(0).choice(shape.rows, size=sample_rows, replace=False))
-    t0 = time.perf_counter()
-    oracle.fill_attention(o["H"][idx], idx, o["A"], o["b"], o["g"], o["Wk"], o["Wv"],
-                          shape.rms_eps, shape.rope_theta, shape.n_kv, shape.head_dim)
-    dt = time.perf_counter() - t0
-    return sample_rows * shape.n_layers / dt, dt
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
 def _cores():
@@ -144,15 +134,384 @@ def _cores():
     return os.cpu_count() or 1
 
 
-def run_reference(args, shape):
+def _events(n):
+    return [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+
+
+# ----------------------------------------------------------------------------- workloads
+
+class AttnWorkload:
+    """Attention late layers (ridgefill_fill); maps in HBM or in pinned host memory."""
+
+    def __init__(self, shape: FillShape, host_maps=False, rows_per_chunk=0):
+        self.shape, self.host_maps, self.rpc = shape, host_maps, rows_per_chunk
+        s = shape
+        self.token_layers = s.rows * s.n_layers
+        self.stage_names = ["map_gemm", "kv_gemm"]
+        self.stage_work = {  # algorithmic FLOP of the first chunk's launches
+            "map_gemm": 2.0 * self._chunk_rows() * s.n_layers * s.d * s.d,
+            "kv_gemm": 2.0 * self._chunk_rows() * s.n_layers * s.d * 2 * s.kv_width,
+        }
+        self.stage_bound = {"map_gemm": "tensor", "kv_gemm": "tensor"}
+        self.total_flops = 2.0 * s.rows * s.n_layers * (s.d * s.d + s.d * 2 * s.kv_width)
+
+    def _chunk_rows(self):
+        return min(self.rpc, self.shape.rows) if self.rpc else self.shape.rows
+
+    def launches_per_step(self):
+        chunks = -(-self.shape.rows // self._chunk_rows())
+        per_chunk = (self.shape.n_layers + 1) if self.host_maps else 2
+        return chunks * per_chunk
+
+    def setup(self, dev, seed):
+        from late_layer_kv_gb300 import ridgefill as rb
+        s = self.shape
+        self.inp = fill_inputs(s, seed=seed)
+        self.d = {k: v.to(dev) for k, v in self.inp.items()}
+        self.A = self.inp["A"].pin_memory() if self.host_maps else self.d["A"]
+        self.Kc = torch.zeros((s.n_layers, s.n_kv, s.N, s.head_dim), dtype=torch.bfloat16,
+                              device=dev)
+        self.Vc = torch.zeros_like(self.Kc)
+        a = rb.fill_args(self.d["H"], self.A, self.d["b"], self.d["g"], self.d["Wk"],
+                         self.d["Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
+                         rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc)
+        self.ws = torch.empty(rb.fill_workspace_size(a), dtype=torch.uint8, device=dev)
+        self.H_dev = self.d["H"]
+
+    def n_events(self):
+        return 3
+
+    def step(self, stream, ev=None):
+        from late_layer_kv_gb300 import ridgefill_fill
+        s, d = self.shape, self.d
+        ridgefill_fill(self.H_dev, self.A, d["b"], d["g"], d["Wk"], d["Wv"], self.Kc, self.Vc,
+                       head_dim=s.head_dim, rope_theta=s.rope_theta, rms_eps=s.rms_eps,
+                       rows_per_chunk=self.rpc, workspace=self.ws, stream=stream,
+                       stage_events=ev)
+
+    def stage_ms(self, ev):
+        return {"map_gemm": ev[0].elapsed_time(ev[1]), "kv_gemm": ev[1].elapsed_time(ev[2])}
+
+    # end to end: pinned H in, two cache rows per layer out
+    def e2e_buffers(self):
+        s = self.shape
+        self.H_host = self.inp["H"].pin_memory()
+        self.out_host = torch.empty((s.n_layers, s.n_kv, 2, s.head_dim),
+                                    dtype=torch.bfloat16).pin_memory()
+        self.H_dev = torch.empty_like(self.d["H"])
+        return self.H_host.numel() * 2, self.out_host.numel() * 2
+
+    def e2e_step(self, stream):
+        r = self.shape.rows
+        self.H_dev.copy_(self.H_host, non_blocking=True)
+        self.step(stream)
+        self.out_host.copy_(self.Kc[:, :, r - 2:r], non_blocking=True)
+
+    def cpu_rate(self, budget_flop):
+        import oracle
+        s = self.shape
+        per_row = s.n_layers * 2.0 * (s.d * s.d + s.d * 2 * s.kv_width)
+        n = int(max(64, min(s.rows, budget_flop / per_row)))
+        o = {k: to_f64(v) for k, v in self.inp.items()}
+        idx = np.sort(np.random.default_rng(0).choice(s.rows, size=n, replace=False))
+        t0 = time.perf_counter()
+        oracle.fill_attention(o["H"][idx], idx, o["A"], o["b"], o["g"], o["Wk"], o["Wv"],
+                              s.rms_eps, s.rope_theta, s.n_kv, s.head_dim)
+        dt = time.perf_counter() - t0
+        return (n * s.n_layers / dt, dt,
+                f"{n} seeded random prefix rows x all {s.n_layers} late layers")
+
+    def config(self):
+        s = self.shape
+        return {"workload": s.name, "d": s.d, "late_layers": s.n_layers, "N": s.N, "T": s.T,
+                "filled_rows": s.rows, "kv_heads": s.n_kv, "head_dim": s.head_dim,
+                "maps": "pinned host, streamed per layer" if self.host_maps else "hbm",
+                "rows_per_chunk": self.rpc or s.rows,
+                "l2": "inputs larger than L2 (maps %d MiB, split state %d MiB)" % (
+                    s.n_layers * s.d * s.d * 2 >> 20, s.rows * s.d * 2 >> 20)}
+
+
+class HybridWorkload:
+    """Gated DeltaNet late layers (ridgefill_fill_gdn) plus attention late layers."""
+
+    def __init__(self, shape: GdnShape):
+        self.shape = s = shape
+        La, Lg, H = s.n_attn, s.n_gdn, s.n_heads
+        kvw = s.n_kv * s.head_dim
+        self.token_layers = s.rows * (La + Lg)
+        self.stage_names = ["attn_map_gemm", "attn_kv_gemm", "gdn_map_gemm", "gdn_proj_gemm",
+                            "gdn_state"]
+        proj = H * s.d_k + H * s.d_v + 2 * H
+        self.stage_work = {
+            "attn_map_gemm": 2.0 * s.rows * La * s.d * s.d,
+            "attn_kv_gemm": 2.0 * s.rows * La * s.d * 2 * kvw,
+            "gdn_map_gemm": 2.0 * s.rows * Lg * s.d * s.d,
+            "gdn_proj_gemm": 2.0 * s.rows * Lg * s.d * proj,
+            # per row and head: dot product and rank-1 update, one FMA per state element each
+            "gdn_state": 4.0 * s.rows * Lg * H * s.d_v * s.d_k,
+        }
+        self.stage_bound = {k: "tensor" for k in self.stage_names}
+        self.stage_bound["gdn_state"] = "alu"
+        self.total_flops = sum(v for k, v in self.stage_work.items() if k != "gdn_state")
+
+    def launches_per_step(self):
+        return 5
+
+    def setup(self, dev, seed):
+        from late_layer_kv_gb300 import ridgefill as rb
+        s = self.shape
+        self.inp = gdn_inputs(s, seed=seed)
+        self.d = {k: v.to(dev) for k, v in self.inp.items()}
+        self.Kc = torch.zeros((s.n_attn, s.n_kv, s.N, s.head_dim), dtype=torch.bfloat16,
+                              device=dev)
+        self.Vc = torch.zeros_like(self.Kc)
+        self.S = torch.zeros((s.n_gdn, s.n_heads, s.d_v, s.d_k), dtype=torch.float32, device=dev)
+        d = self.d
+        a = rb.fill_args(d["H"], d["attn_A"], d["attn_b"], d["attn_g"], d["attn_Wk"],
+                         d["attn_Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
+                         rope_theta=s.rope_theta, rms_eps=s.rms_eps)
+        g = rb.gdn_args(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"], d["Wb"],
+                        self.S, n_heads=s.n_heads, rms_eps=s.rms_eps)
+        self.ws = torch.empty(max(rb.fill_workspace_size(a), rb.gdn_workspace_size(g)),
+                              dtype=torch.uint8, device=dev)
+        self.H_dev = d["H"]
+
+    def n_events(self):
+        return 7
+
+    def step(self, stream, ev=None):
+        from late_layer_kv_gb300 import ridgefill_fill, ridgefill_fill_gdn
+        s, d = self.shape, self.d
+        ridgefill_fill(self.H_dev, d["attn_A"], d["attn_b"], d["attn_g"], d["attn_Wk"],
+                       d["attn_Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
+                       rope_theta=s.rope_theta, rms_eps=s.rms_eps, workspace=self.ws,
+                       stream=stream, stage_events=None if ev is None else ev[0:3])
+        ridgefill_fill_gdn(self.H_dev, d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"],
+                           d["Wb"], self.S, n_heads=s.n_heads, rms_eps=s.rms_eps,
+                           workspace=self.ws, stream=stream,
+                           stage_events=None if ev is None else ev[3:7])
+
+    def stage_ms(self, ev):
+        pairs = [(0, 1), (1, 2), (3, 4), (4, 5), (5, 6)]
+        return {n: ev[a].elapsed_time(ev[b]) for n, (a, b) in zip(self.stage_names, pairs)}
+
+    def e2e_buffers(self):
+        self.H_host = self.inp["H"].pin_memory()
+        self.out_host = torch.empty(self.S.shape, dtype=torch.float32).pin_memory()
+        self.H_dev = torch.empty_like(self.d["H"])
+        return self.H_host.numel() * 2, self.out_host.numel() * 4
+
+    def e2e_step(self, stream):
+        self.H_dev.copy_(self.H_host, non_blocking=True)
+        self.step(stream)
+        self.out_host.copy_(self.S, non_blocking=True)
+
+    def cpu_rate(self, budget_flop):
+        """Attention layers on sampled rows, GDN layers on the first rows of one layer
+        (its state needs every earlier row); combined per token-layer in the layer mix."""
+        import oracle
+        s = self.shape
+        o = {k: to_f64(v) for k, v in self.inp.items()}
+        kvw = s.n_kv * s.head_dim
+        per_row = s.n_attn * 2.0 * (s.d * s.d + s.d * 2 * kvw)
+        na = int(max(64, min(s.rows, budget_flop / 2 / per_row)))
+        idx = np.sort(np.random.default_rng(0).choice(s.rows, size=na, replace=False))
+        t0 = time.perf_counter()
+        oracle.fill_attention(o["H"][idx], idx, o["attn_A"], o["attn_b"], o["attn_g"],
+                              o["attn_Wk"], o["attn_Wv"], s.rms_eps, s.rope_theta, s.n_kv,
+                              s.head_dim)
+        ta = (time.perf_counter() - t0) / (na * s.n_attn)
+        ng = 256
+        t0 = time.perf_counter()
+        oracle.gdn_state(o["H"][:ng], o["A"], o["b"], o["g"], o["Wk"], o["Wv"], o["Wa"], o["Wb"],
+                         s.rms_eps, s.n_heads, s.d_k, s.d_v, layers=[0])
+        tg = (time.perf_counter() - t0) / ng
+        per = (s.n_attn * ta + s.n_gdn * tg) / (s.n_attn + s.n_gdn)
+        return 1.0 / per, na * s.n_attn * ta + ng * tg, (
+            f"attention: {na} random prefix rows x {s.n_attn} layers; GDN: first {ng} rows x 1 "
+            f"layer x {s.n_heads} heads; combined per token-layer in the "
+            f"{s.n_attn}:{s.n_gdn} mix")
+
+    def config(self):
+        s = self.shape
+        return {"workload": s.name, "d": s.d, "late_layers": s.n_attn + s.n_gdn,
+                "gdn_layers": s.n_gdn, "attn_layers": s.n_attn, "gdn_heads": s.n_heads,
+                "d_k": s.d_k, "d_v": s.d_v, "N": s.N, "T": s.T, "filled_rows": s.rows,
+                "kv_heads": s.n_kv, "head_dim": s.head_dim, "maps": "hbm",
+                "l2": "inputs larger than L2 (maps %d MiB)" % (
+                    (s.n_attn + s.n_gdn) * s.d * s.d * 2 >> 20)}
+
+
+def make_workload(name, args):
+    shape = WORKLOADS[name]
+    if isinstance(shape, GdnShape):
+        if args.rows:
+            shape = replace(shape, name=f"{shape.name}_rows{args.rows}", N=args.rows + shape.T)
+        return HybridWorkload(shape)
+    if args.rows or args.layers:
+        rows = args.rows or shape.rows
+        L = args.layers or shape.n_layers
+        shape = replace(shape, name=f"{shape.name}_rows{rows}_L{L}", N=rows + shape.T, n_layers=L)
+    rpc = args.rows_per_chunk
+    if name.startswith("dense27b") and not rpc:
+        rpc = 16384  # late-layer X_hat processed in row chunks
+    return AttnWorkload(shape, host_maps=name.startswith("hostmaps"), rows_per_chunk=rpc)
+
+
+# ----------------------------------------------------------------------------- arms
+
+def h2d_rate_gbs(dev, nbytes=32 << 20, reps=20):
+    """Best-of pinned host -> device copy rate (GB/s)."""
+    src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    dst = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    best = 0.0
+    for _ in range(reps + 3):
+        e0, e1 = _events(2)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (e0.elapsed_time(e1) / 1000.0) / 1e9)
+    return best
+
+
+def run_ours(args):
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from late_layer_kv_gb300 import device_error
+    wl = make_workload(args.workload, args)
+    wl.setup(dev, seed=1001 + rank)
+    stream = torch.cuda.current_stream(dev)
+    steps = args.steps
+    ev = [_events(wl.n_events()) for _ in range(steps)]
+    for e in sum(ev, []):
+        e.record(stream)  # torch creates the CUDA event on first record
+    for _ in range(args.warmup):
+        wl.step(stream)
+    torch.cuda.synchronize()
+    assert device_error(stream) == 0, "device wait ran out during warm-up"
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0, t1 = _events(2)
+    t0.record(stream)
+    for i in range(steps):
+        wl.step(stream, ev[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop()
+    assert device_error(stream) == 0, "device wait ran out during the timed region"
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / steps
+    value = wl.token_layers * world / (ms_step / 1000.0)
+
+    peaks, src = _peaks()
+    sustained = ms >= 2000.0  # long regions run under the power cap
+    pkey = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    tpeak = float(peaks[pkey])
+    alu_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    alu_peak = N_SM * FP32_LANES_PER_SM * 2 * alu_mhz * 1e6 / 1e12
+    stages = {}
+    for name in wl.stage_names:
+        sm = float(np.mean([wl.stage_ms(e)[name] for e in ev]))
+        ach = wl.stage_work[name] / (sm / 1000.0) / 1e12
+        pk = tpeak if wl.stage_bound[name] == "tensor" else alu_peak
+        stages[name] = {"ms": sm, "achieved_tflops": ach, "bound": wl.stage_bound[name],
+                        "frac": ach / pk}
+    dom = max(stages, key=lambda k: stages[k]["ms"])
+    traffic = None
+    pt = PROFILED_TRAFFIC.get(wl.shape.name)
+    if pt and pt["kernel_sha256"] == _kernel_digest():
+        traffic = pt["bytes_per_launch"]
+    dpk = tpeak if stages[dom]["bound"] == "tensor" else alu_peak
+    roofline = {"bound": stages[dom]["bound"], "kernel": dom,
+                "achieved": stages[dom]["achieved_tflops"], "peak": dpk, "unit": "TFLOP/s",
+                "frac": stages[dom]["achieved_tflops"] / dpk, "traffic": traffic,
+                "peak_source": (f"{src} {pkey}" if stages[dom]["bound"] == "tensor" else
+                                f"{N_SM} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {alu_mhz} MHz"),
+                "timed_region_ms": ms}
+    pct = 100.0 * wl.total_flops / (ms_step / 1000.0) / 1e12 / tpeak
+
+    e2e = None
+    if not args.no_e2e:
+        bi, bo = wl.e2e_buffers()
+        for _ in range(3):
+            wl.e2e_step(stream)
+        torch.cuda.synchronize()
+        e0, e1 = _events(2)
+        e0.record(stream)
+        for _ in range(steps):
+            wl.e2e_step(stream)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / steps
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        e2e = {"value": wl.token_layers * world / (ems / 1000.0), "unit": "token-layers/s",
+               "ms_per_step": ems, "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+
+    host_link = None
+    if getattr(wl, "host_maps", False):
+        s = wl.shape
+        link = h2d_rate_gbs(dev)
+        map_bytes = s.n_layers * s.d * s.d * 2
+        mstage = stages["map_gemm"]["ms"]
+        host_link = {"h2d_gbs_measured": link, "map_bytes_per_step": map_bytes,
+                     "map_stage_gbs": map_bytes / (mstage / 1000.0) / 1e9,
+                     "note": "maps copied per layer on a side stream while the previous layer "
+                             "computes; map_stage_gbs is the rate the maps flowed through the "
+                             "map stage"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        r, dt, what = wl.cpu_rate(args.cpu_flop)
+        cpu = {"value": r, "unit": "token-layers/s", "cores": _cores(), "kind": "oracle",
+               "sample": f"{what} ({dt:.1f} s of f64 numpy work)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "token-layers/s", "n_gpus": world,
+            "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": wl.config(),
+            "fill_stage_ms": ms_step, "pct_bf16_peak": pct, "stages": stages,
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": wl.launches_per_step() * steps, "clocks": clk,
+        }
+        if host_link:
+            line["host_link"] = host_link
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_reference(args):
+    """The oracle as it stands, on the host cores, for the same metric and workload."""
     world, rank, _ = _dist()
     if rank != 0:
         return
-    inp = fill_inputs(shape, seed=1001)
-    sample = args.ref_rows
-    rates, times = [], []
+    wl = make_workload(args.workload, args)
+    wl.inp = (gdn_inputs(wl.shape, seed=1001) if isinstance(wl, HybridWorkload)
+              else fill_inputs(wl.shape, seed=1001))
+    rates, times, what = [], [], ""
     for i in range(args.warmup + args.steps):
-        r, dt = cpu_oracle_rate(shape, inp, sample)
+        r, dt, what = wl.cpu_rate(args.ref_flop)
         if i >= args.warmup:
             rates.append(r)
             times.append(dt)
@@ -162,202 +521,36 @@ def run_reference(args, shape):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * float(np.mean(times)), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": _config(shape),
+        "config": wl.config(),
         "cpu_baseline": {"value": value, "unit": "token-layers/s", "cores": _cores(),
-                         "kind": "oracle",
-                         "sample": f"{sample} seeded random prefix rows x all {shape.n_layers} "
-                                   f"late layers per step"},
+                         "kind": "oracle", "sample": what + " per step"},
         "e2e": {"value": value, "unit": "token-layers/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-METRIC = "filled token-layers/s (fill-stage ms and % of GB300 bf16 tensor peak alongside)"
-
-
-def _config(shape):
-    return {"workload": shape.name, "d": shape.d, "late_layers": shape.n_layers, "N": shape.N,
-            "T": shape.T, "filled_rows": shape.rows, "kv_heads": shape.n_kv,
-            "head_dim": shape.head_dim, "maps": "hbm",
-            "l2": "inputs larger than L2 (maps %d MiB, split state %d MiB)" % (
-                shape.n_layers * shape.d * shape.d * 2 >> 20, shape.rows * shape.d * 2 >> 20)}
-
-
-
-def _e2e(shape, inp, d, Kc, Vc, ws, stream, steps, world, dev, token_layers):
-    """The same metric through the public call with host buffers: each step copies the
-    prompt's split state H from pinned host memory and reads two cache rows per layer back."""
-    from late_layer_kv_gb300 import ridgefill_fill
-    L, rows = shape.n_layers, shape.rows
-    H_host = inp["H"].pin_memory()
-    out_host = torch.empty((L, shape.n_kv, 2, shape.head_dim), dtype=torch.bfloat16).pin_memory()
-    H_dev = torch.empty_like(d["H"])
-
-    def one():
-        H_dev.copy_(H_host, non_blocking=True)
-        ridgefill_fill(H_dev, d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc,
-                       head_dim=shape.head_dim, rope_theta=shape.rope_theta,
-                       rms_eps=shape.rms_eps, workspace=ws, stream=stream)
-        out_host.copy_(Kc[:, :, rows - 2:rows], non_blocking=True)
-
-    for _ in range(3):
-        one()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        one()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    return {"value": token_layers * world / (e2e_ms / 1000.0), "unit": "token-layers/s",
-            "ms_per_step": e2e_ms, "h2d_bytes_per_step": int(H_host.numel() * 2),
-            "d2h_bytes_per_step": int(out_host.numel() * 2)}
-
-def run_ours(args, shape):
-    world, rank, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    from late_layer_kv_gb300 import device_error, ridgefill_fill
-    from late_layer_kv_gb300 import ridgefill as rb
-
-    inp = fill_inputs(shape, seed=1001 + rank)
-    d = {k: v.to(dev) for k, v in inp.items()}
-    L, rows = shape.n_layers, shape.rows
-    Kc = torch.zeros((L, shape.n_kv, shape.N, shape.head_dim), dtype=torch.bfloat16, device=dev)
-    Vc = torch.zeros_like(Kc)
-    ws_args = rb.fill_args(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc,
-                           head_dim=shape.head_dim, rope_theta=shape.rope_theta,
-                           rms_eps=shape.rms_eps)
-    ws = torch.empty(rb.fill_workspace_size(ws_args), dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    steps = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    for e in sum(ev, []):
-        e.record(stream)  # torch creates the CUDA event on first record
-
-    def step(i=None):
-        ridgefill_fill(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc,
-                       head_dim=shape.head_dim, rope_theta=shape.rope_theta,
-                       rms_eps=shape.rms_eps, workspace=ws, stream=stream,
-                       stage_events=None if i is None else ev[i])
-
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
-    assert device_error(stream) == 0
-
-    clocks = ClockSampler(local)
-    clocks.start()
-    time.sleep(0.3)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    t0.record(stream)
-    for i in range(steps):
-        step(i)
-    t1.record(stream)
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    clk = clocks.stop()
-    assert device_error(stream) == 0
-    ms = t0.elapsed_time(t1)
-    map_ms = float(np.mean([e[0].elapsed_time(e[1]) for e in ev]))
-    kv_ms = float(np.mean([e[1].elapsed_time(e[2]) for e in ev]))
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    ms_step = ms / steps
-    token_layers = rows * L
-    value = token_layers * world / (ms_step / 1000.0)
-
-    # end to end through the public call with host buffers: pinned H in, a cache row out
-    e2e = None
-    if not args.no_e2e:
-        e2e = _e2e(shape, inp, d, Kc, Vc, ws, stream, steps, world, dev, token_layers)
-
-    peaks, src = _peaks()
-    # a timed region of a few seconds or more runs under the power cap: compare with the
-    # sustained cuBLAS figure; shorter regions with the burst figure
-    sustained = ms >= 2000.0
-    peak_key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
-    peak = float(peaks[peak_key])
-    map_flops = 2.0 * rows * L * shape.d * shape.d
-    achieved = map_flops / (map_ms / 1000.0) / 1e12
-    total_flops = rows * L * _flops_per_row_layer(shape)
-    pct = 100.0 * total_flops / (ms_step / 1000.0) / 1e12 / peak
-    traffic = None
-    if PROFILED_TRAFFIC["kernel_sha256"] == _kernel_digest():
-        traffic = PROFILED_TRAFFIC["map_gemm_bytes_per_launch"]
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        r, dt = cpu_oracle_rate(shape, inp, args.cpu_rows)
-        cpu = {"value": r, "unit": "token-layers/s", "cores": _cores(), "kind": "oracle",
-               "sample": f"{args.cpu_rows} seeded random prefix rows x all {L} late layers "
-                         f"({dt:.1f} s of f64 numpy work)"}
-
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "token-layers/s", "n_gpus": world,
-            "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": _config(shape),
-            "fill_stage_ms": ms_step, "map_gemm_ms": map_ms, "kv_gemm_ms": kv_ms,
-            "pct_bf16_peak": pct,
-            "roofline": {"bound": "tensor", "kernel": "map GEMM (rf_gemm_kernel, map mode)",
-                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "peak_source": f"{src} {peak_key}",
-                         "timed_region_ms": ms},
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": 2 * steps,
-            "clocks": clk,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
-
-
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="llama8b_16k")
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="llama8b_16k", choices=sorted(WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--cpu-rows", type=int, default=4096)
-    ap.add_argument("--ref-rows", type=int, default=64)
+    ap.add_argument("--cpu-flop", type=float, default=6e12,
+                    help="f64 work of the CPU-baseline sample (about 10-30 s on the host)")
+    ap.add_argument("--ref-flop", type=float, default=2e11,
+                    help="f64 work per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--rows", type=int, default=0, help="override the filled rows (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the late layers (profiling)")
+    ap.add_argument("--rows-per-chunk", type=int, default=0)
     args = ap.parse_args()
-    shape = WORKLOADS[args.workload]
-    if args.rows or args.layers:
-        from dataclasses import replace
-        rows = args.rows or shape.rows
-        L = args.layers or shape.n_layers
-        shape = replace(shape, name=f"{shape.name}_rows{rows}_L{L}", N=rows + shape.T,
-                        n_layers=L)
     if args.impl == "reference":
-        run_reference(args, shape)
+        run_reference(args)
     else:
-        run_ours(args, shape)
+        run_ours(args)
 
 
 if __name__ == "__main__":

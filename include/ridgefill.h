@@ -155,15 +155,18 @@ rf_status ridgefill_fill_noalloc(const rf_fill_args* args, void* stream);
  *   k = normalize(u Wk_l[h]^T)   (k / sqrt(sum k^2 + l2_eps))
  *   v = u Wv_l[h]^T,  alpha = sigmoid(u . Wa_l[h]),  beta = sigmoid(u . Wb_l[h])
  *   S <- alpha S (I - beta k k^T) + beta v k^T        (S is d_v x d_k, f32)
- * S starts from S0 (or zero) and the final S is written.  The rows are
- * processed in chunks of `chunk` rows with the chunk-parallel form of the
- * same recurrence.
+ * S starts from S0 (or zero) and the final S is written; with rows == 0 the
+ * call writes S = S0 (or zero).  The state is carried in f32; `chunk` is the
+ * row-chunk length of the state computation and must be 64.
  *
  * Layouts: H, A, bias, gain as in rf_fill_args; Wk [L, n_heads*d_k, d_out],
  *   Wv [L, n_heads*d_v, d_out], Wa/Wb [L, n_heads, d_out] (bf16);
  *   S0 (may be NULL) and S [L, n_heads, d_v, d_k] f32.
  * Limits: d_in % 64 == 0, d_out % 128 == 0, d_k == d_v == 128, chunk == 64,
- *   n_heads <= 64.
+ *   n_heads a multiple of 8 in [8, 64], rows_per_chunk 0 or a multiple of 128.
+ * stage_events (optional): host array of four cudaEvent_t recorded on `stream`
+ *   before the first chunk's map GEMM, after it, after its projection GEMM and
+ *   after its state kernel.
  */
 typedef struct rf_gdn_args {
   int32_t n_layers;
@@ -188,6 +191,7 @@ typedef struct rf_gdn_args {
   const void* Wb;
   const float* S0;
   float* S;
+  void* const* stage_events;
 } rf_gdn_args;
 
 size_t ridgefill_gdn_workspace_size(const rf_gdn_args* args);

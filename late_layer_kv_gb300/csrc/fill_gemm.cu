@@ -278,24 +278,24 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, int q, int lane
     }
   } else {
     // gate tile: columns [0, H) are the alpha logits, [H, 2H) the beta logits
-    for (int c0 = 0; c0 < 2 * H; c0 += 16) {
+    for (int c0 = 0; c0 < 2 * H; c0 += 32) {
       uint32_t a[32];
-      tmem_ld32(tcol + c0, a);  // reads 32 columns; only the first 16 are used
+      tmem_ld32(tcol + c0, a);  // columns past 2H are read but unused
       tmem_wait_ld();
       if (valid) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < 32; ++j) {
           const int c = c0 + j;
-          const float z = f32(a[j]) * rs;
-          float val;
-          if (c < H) {
-            val = fminf(z, 0.f) - log1pf(expf(-fabsf(z)));  // log sigmoid(z)
-          } else {
-            val = 1.f / (1.f + expf(-z));                    // sigmoid(z)
+          if (c < 2 * H) {
+            const float z = f32(a[j]) * rs;
+            const bool is_a = c < H;
+            // log sigmoid(z) for alpha, sigmoid(z) for beta
+            const float val = is_a ? fminf(z, 0.f) - log1pf(expf(-fabsf(z)))
+                                   : 1.f / (1.f + expf(-z));
+            const int which = is_a ? 0 : 1;
+            const int h = is_a ? c : c - H;
+            p.gdn_gate[((static_cast<size_t>(l) * 2 + which) * H + h) * ra + row] = val;
           }
-          const int which = c < H ? 0 : 1;
-          const int h = c < H ? c : c - H;
-          p.gdn_gate[((static_cast<size_t>(l) * 2 + which) * H + h) * ra + row] = val;
         }
       }
     }

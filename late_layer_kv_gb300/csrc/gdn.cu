@@ -1,0 +1,394 @@
+// gdn.cu -- ridgefill_fill_gdn: end-of-fill recurrent state of Gated DeltaNet
+// late layers (RidgeFill, "Training-Free Late-Layer Cache Fill for Faster
+// Prefill", section 2.3: every filled row updates the shared state from its
+// predicted input).
+//
+// Per row chunk: the grouped map GEMM (X_hat for every GDN layer), the GDN
+// projection GEMM (RMS scale, L2-normalised k per head, v, log alpha, beta),
+// then the state kernel, which carries S over the chunk's rows in order.
+//
+// State kernel.  For one head the recurrence
+//   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
+// is, row by row of S (index i over d_v),
+//   S_t[i,:] = alpha_t S_{t-1}[i,:] + c_t[i] k_t^T,
+//   c_t[i]   = beta_t (v_t[i] - alpha_t S_{t-1}[i,:] . k_t),
+// so the d_v rows of S evolve independently.  A CTA owns 32 rows of S of one
+// (layer, head) in registers, four threads per row with 32 columns each.  The
+// decay is applied lazily: the registers hold S / g, g being the product of
+// the gates since the last renormalisation, so a prompt row costs one FMA per
+// element for the dot product and one for the update.  k, v and the gates are
+// staged through shared memory 32 prompt rows at a time with cp.async,
+// double buffered.
+#include <cmath>
+#include <mutex>
+
+#include "abi_common.h"
+#include "sm103_ptx.cuh"
+
+namespace rf {
+namespace {
+
+constexpr int kSRows = 32;     // rows of S (d_v) per CTA
+constexpr int kGdnThreads = 128;
+constexpr int kStageRows = 32;  // prompt rows per staging buffer
+constexpr int kDk = 128;
+constexpr float kRenorm = 1e-20f;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+__global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStateParams p) {
+  __shared__ __align__(16) float sk[2][kStageRows][kDk];
+  __shared__ __align__(16) float sv[2][kStageRows][kSRows];
+  __shared__ __align__(16) float sg[2][2][kStageRows];
+
+  const int slice = blockIdx.x, h = blockIdx.y, l = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int r = tid >> 2;     // S row inside the slice
+  const int part = tid & 3;   // 32-column part of d_k
+  const int i = slice * kSRows + r;
+  const int H = p.heads;
+  const size_t ra = static_cast<size_t>(p.rows_alloc);
+  const int dv = p.dv;
+
+  const float* kbase = p.k + (static_cast<size_t>(l) * H + h) * ra * kDk;
+  const float* vbase = p.v + (static_cast<size_t>(l) * H + h) * ra * dv + slice * kSRows;
+  const float* abase = p.gate + (static_cast<size_t>(l) * 2 * H + h) * ra;
+  const float* bbase = p.gate + (static_cast<size_t>(l) * 2 * H + H + h) * ra;
+  const size_t s_off = ((static_cast<size_t>(l) * H + h) * dv + i) * kDk + part * 32;
+
+  float S[32];
+  if (p.first) {
+    if (p.S0 != nullptr) {
+#pragma unroll
+      for (int j = 0; j < 32; j += 4) {
+        const float4 x = *reinterpret_cast<const float4*>(p.S0 + s_off + j);
+        S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) S[j] = 0.f;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; j += 4) {
+      const float4 x = *reinterpret_cast<const float4*>(p.S + s_off + j);
+      S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
+    }
+  }
+  float g = 1.f;
+
+  const int nst = (p.rows + kStageRows - 1) / kStageRows;
+  auto load = [&](int st, int buf) {
+    const int t0 = st * kStageRows;
+    const int n = min(kStageRows, p.rows - t0);
+    for (int q = tid; q < n * (kDk / 4); q += kGdnThreads) {
+      const int rr = q / (kDk / 4), cc = q % (kDk / 4);
+      cp_async16(&sk[buf][rr][cc * 4], kbase + static_cast<size_t>(t0 + rr) * kDk + cc * 4);
+    }
+    for (int q = tid; q < n * (kSRows / 4); q += kGdnThreads) {
+      const int rr = q / (kSRows / 4), cc = q % (kSRows / 4);
+      cp_async16(&sv[buf][rr][cc * 4], vbase + static_cast<size_t>(t0 + rr) * dv + cc * 4);
+    }
+    if (tid < 2 * (kStageRows / 4)) {
+      const int which = tid / (kStageRows / 4), cc = tid % (kStageRows / 4);
+      if (cc * 4 < n)  // gate rows are padded to the 128-row allocation
+        cp_async16(&sg[buf][which][cc * 4], (which ? bbase : abase) + t0 + cc * 4);
+    }
+    cp_async_commit();
+  };
+
+  if (nst > 0) load(0, 0);
+  for (int st = 0; st < nst; ++st) {
+    const int buf = st & 1;
+    if (st + 1 < nst) {
+      load(st + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const int n = min(kStageRows, p.rows - st * kStageRows);
+    for (int tt = 0; tt < n; ++tt) {
+      const float a = expf(sg[buf][0][tt]);
+      const float bt = sg[buf][1][tt];
+      const float vi = sv[buf][tt][r];
+      float kk[32];
+      const float4* k4 = reinterpret_cast<const float4*>(&sk[buf][tt][part * 32]);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float4 x = k4[j];
+        kk[4 * j] = x.x; kk[4 * j + 1] = x.y; kk[4 * j + 2] = x.z; kk[4 * j + 3] = x.w;
+      }
+      float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; j += 2) {
+        d0 = fmaf(S[j], kk[j], d0);
+        d1 = fmaf(S[j + 1], kk[j + 1], d1);
+      }
+      float dot = d0 + d1;
+      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
+      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
+      // true S_{t-1} k_t = g * dot
+      const float c = bt * (vi - a * (g * dot));
+      const float gn = g * a;
+      if (gn >= kRenorm) {
+        const float s = c / gn;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[j] = fmaf(s, kk[j], S[j]);
+        g = gn;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) S[j] = fmaf(c, kk[j], gn * S[j]);
+        g = 1.f;
+      }
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    float4 x = make_float4(g * S[j], g * S[j + 1], g * S[j + 2], g * S[j + 3]);
+    *reinterpret_cast<float4*>(p.S + s_off + j) = x;
+  }
+}
+
+struct GdnPlan {
+  int bn_map = 0;
+  int64_t R = 0;
+  size_t off_xhat = 0, off_ss = 0, off_k = 0, off_v = 0, off_gate = 0, off_slots = 0, total = 0;
+};
+
+rf_status validate_gdn(const rf_gdn_args* a) {
+  if (a == nullptr) return fail(RF_ERR_ARG, "args is NULL");
+  if (a->n_layers < 1) return fail(RF_ERR_SHAPE, "n_layers must be >= 1");
+  if (a->d_in < 64 || a->d_in % 64 != 0) return fail(RF_ERR_SHAPE, "d_in must be a positive multiple of 64");
+  if (a->d_out < 128 || a->d_out % 128 != 0)
+    return fail(RF_ERR_SHAPE, "d_out must be a positive multiple of 128");
+  if (a->d_k != kDk || a->d_v != kDk) return fail(RF_ERR_SHAPE, "d_k and d_v must be 128");
+  if (a->n_heads < 8 || a->n_heads > 64 || a->n_heads % 8 != 0)
+    return fail(RF_ERR_SHAPE, "n_heads must be a multiple of 8 in [8, 64]");
+  if (a->chunk != 64) return fail(RF_ERR_SHAPE, "chunk must be 64");
+  if (a->rows < 0) return fail(RF_ERR_ARG, "rows must be >= 0");
+  if (a->rows_per_chunk < 0 || a->rows_per_chunk % 128 != 0)
+    return fail(RF_ERR_SHAPE, "rows_per_chunk must be 0 or a multiple of 128");
+  if (!(a->rms_eps >= 0.0) || !(a->l2_eps >= 0.0)) return fail(RF_ERR_ARG, "bad rms_eps or l2_eps");
+  if (a->maps_on_host != 0 && a->maps_on_host != 1) return fail(RF_ERR_ARG, "maps_on_host must be 0 or 1");
+  if (a->rows >= (int64_t(1) << 31) || static_cast<int64_t>(a->n_layers) * a->d_out >= (int64_t(1) << 31))
+    return fail(RF_ERR_SHAPE, "sizes exceed the 32-bit tile indexing");
+  return RF_OK;
+}
+
+void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
+  pl->bn_map = (a->d_out % 256 == 0) ? 256 : 128;
+  const int64_t all = ceil_div(a->rows > 0 ? a->rows : 1, kBM) * kBM;
+  pl->R = a->rows_per_chunk > 0 ? (a->rows_per_chunk < all ? a->rows_per_chunk : all) : all;
+  const size_t L = a->n_layers, d = a->d_out, R = pl->R, H = a->n_heads;
+  size_t off = 0;
+  pl->off_xhat = off;  off = align_up(off + L * R * d * 2, 256);
+  pl->off_ss = off;    off = align_up(off + L * (d / pl->bn_map) * R * 4, 256);
+  pl->off_k = off;     off = align_up(off + L * H * R * kDk * 4, 256);
+  pl->off_v = off;     off = align_up(off + L * H * R * kDk * 4, 256);
+  pl->off_gate = off;  off = align_up(off + L * 2 * H * R * 4, 256);
+  pl->off_slots = off; off = align_up(off + (a->maps_on_host ? 2 * d * static_cast<size_t>(a->d_in) * 2 : 0), 256);
+  pl->total = off;
+}
+
+rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, const void* xhat,
+                          const float* ss, float* kb, float* vb, float* gb, cudaStream_t s) {
+  GemmParams p{};
+  p.mode = kModeGdnProj;
+  p.k_blocks = a->d_out / kBK;
+  const int H = a->n_heads;
+  const uint64_t drow = static_cast<uint64_t>(a->d_out) * 2;
+  const uint64_t hk = static_cast<uint64_t>(H) * kDk;
+  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xhat, a->d_out, rc, a->n_layers,
+                         drow, drow * pl.R, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wk, a->d_out, hk,
+                          a->n_layers, drow, drow * hk, kBK, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wv, a->d_out, hk,
+                          a->n_layers, drow, drow * hk, kBK, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmB[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wa, a->d_out, H,
+                          a->n_layers, drow, drow * H, kBK, H, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmB[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wb, a->d_out, H,
+                          a->n_layers, drow, drow * H, kBK, H, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the GDN projection GEMM");
+  p.m_tiles = static_cast<int32_t>(ceil_div(rc, kBM));
+  p.n_k_tiles = H / 2;
+  p.n_v_tiles = H / 2;
+  p.n_tiles = H + 1;
+  p.batches = a->n_layers;
+  p.bn = 256;
+  p.group_m = 16;
+  p.rows = static_cast<int32_t>(rc);
+  p.ss_stride = static_cast<int32_t>(pl.R);
+  p.d_out = a->d_out;
+  p.ss_tiles = a->d_out / pl.bn_map;
+  p.ss_in = ss;
+  p.inv_d = static_cast<float>(1.0 / a->d_out);
+  p.eps = static_cast<float>(a->rms_eps);
+  p.gdn_k = kb;
+  p.gdn_v = vb;
+  p.gdn_gate = gb;
+  p.gdn_heads = H;
+  p.gdn_rows_alloc = static_cast<int32_t>(pl.R);
+  p.l2_eps = static_cast<float>(a->l2_eps);
+  p.err = device_error_word();
+  if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.batches;
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  if (grid <= 0) return RF_OK;
+  cudaError_t e = launch_gemm(p, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "GDN projection GEMM launch");
+  return RF_OK;
+}
+
+std::mutex g_gdn_host_map_mu;
+
+}  // namespace
+
+cudaError_t launch_gdn_state(const GdnStateParams& p, cudaStream_t stream) {
+  dim3 grid(p.dv / kSRows, p.heads, p.layers);
+  gdn_state_kernel<<<grid, kGdnThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace rf
+
+using namespace rf;
+
+extern "C" size_t ridgefill_gdn_workspace_size(const rf_gdn_args* a) {
+  if (validate_gdn(a) != RF_OK) return 0;
+  GdnPlan pl;
+  plan_gdn(a, &pl);
+  return pl.total;
+}
+
+extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, size_t ws_bytes,
+                                        void* stream) {
+  rf_status st = validate_gdn(a);
+  if (st != RF_OK) return st;
+  if (a->S == nullptr) return fail(RF_ERR_ARG, "S is NULL");
+  if (a->rows > 0) {
+    const void* req[] = {a->H, a->A, a->bias, a->Wk, a->Wv, a->Wa, a->Wb};
+    for (const void* q : req)
+      if (q == nullptr) return fail(RF_ERR_ARG, "a required pointer is NULL");
+  }
+  const void* dev[] = {a->H, a->bias, a->gain, a->Wk, a->Wv, a->Wa, a->Wb, a->S0, a->S, workspace};
+  for (const void* q : dev)
+    if (q != nullptr && !aligned16(q)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
+  if (a->A != nullptr && !aligned16(a->A)) return fail(RF_ERR_ALIGN, "A is not 16-byte aligned");
+  if (a->maps_on_host && a->rows > 0) {
+    cudaPointerAttributes attr;
+    cudaError_t e = cudaPointerGetAttributes(&attr, a->A);
+    if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+      cudaGetLastError();
+      return fail(RF_ERR_NOT_PINNED, "maps_on_host set but A is not page-locked host memory");
+    }
+  }
+  GdnPlan pl;
+  plan_gdn(a, &pl);
+  if (workspace == nullptr || ws_bytes < pl.total)
+    return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes", pl.total);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  void* xhat = ws + pl.off_xhat;
+  float* ss = reinterpret_cast<float*>(ws + pl.off_ss);
+  float* kb = reinterpret_cast<float*>(ws + pl.off_k);
+  float* vb = reinterpret_cast<float*>(ws + pl.off_v);
+  float* gb = reinterpret_cast<float*>(ws + pl.off_gate);
+
+  GdnStateParams sp{};
+  sp.k = kb;
+  sp.v = vb;
+  sp.gate = gb;
+  sp.S0 = a->S0;
+  sp.S = a->S;
+  sp.layers = a->n_layers;
+  sp.heads = a->n_heads;
+  sp.dv = a->d_v;
+  sp.rows_alloc = static_cast<int32_t>(pl.R);
+  sp.chunk = a->chunk;
+  sp.err = device_error_word();
+
+  if (a->rows == 0) {  // the end-of-fill state is the initial state
+    sp.rows = 0;
+    sp.first = 1;
+    cudaError_t e = launch_gdn_state(sp, s);
+    return e == cudaSuccess ? RF_OK : cuda_fail(e, "GDN state launch");
+  }
+
+  HostStreamer* hs = nullptr;
+  std::unique_lock<std::mutex> lk(g_gdn_host_map_mu, std::defer_lock);
+  const size_t map_bytes = static_cast<size_t>(a->d_out) * a->d_in * 2;
+  if (a->maps_on_host) {
+    lk.lock();
+    hs = host_streamer();
+    if (hs == nullptr) return RF_ERR_CUDA;
+    cudaError_t e = cudaEventRecord(hs->start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->copy, hs->start, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "ordering the map-copy stream");
+  }
+  cudaEvent_t const* ev = reinterpret_cast<cudaEvent_t const*>(a->stage_events);
+  auto mark = [&](int64_t start, int i) -> rf_status {
+    if (ev == nullptr || start != 0) return RF_OK;
+    cudaError_t e = cudaEventRecord(ev[i], s);
+    return e == cudaSuccess ? RF_OK : cuda_fail(e, "recording a stage event");
+  };
+  for (int64_t start = 0; start < a->rows; start += pl.R) {
+    const int64_t rc = (a->rows - start < pl.R) ? a->rows - start : pl.R;
+    if ((st = mark(start, 0)) != RF_OK) return st;
+    MapLaunch m{};
+    m.H = static_cast<const uint8_t*>(a->H) + static_cast<size_t>(start) * a->d_in * 2;
+    m.rows = rc;
+    m.d_in = a->d_in;
+    m.d_out = a->d_out;
+    m.n_layers = a->n_layers;
+    m.bn = pl.bn_map;
+    m.R = pl.R;
+    m.bias = a->bias;
+    m.gain = a->gain;
+    m.xhat = xhat;
+    m.ss = ss;
+    if (!a->maps_on_host) {
+      m.A = a->A;
+      m.slot_layer = -1;
+      if ((st = launch_map(m, s)) != RF_OK) return st;
+    } else {
+      for (int l = 0; l < a->n_layers; ++l) {
+        const int k = l & 1;
+        uint8_t* slot = ws + pl.off_slots + k * map_bytes;
+        cudaError_t e = cudaSuccess;
+        if (start > 0 || l >= 2) e = cudaStreamWaitEvent(hs->copy, hs->freed[k], 0);
+        if (e == cudaSuccess)
+          e = cudaMemcpyAsync(slot, static_cast<const uint8_t*>(a->A) + l * map_bytes, map_bytes,
+                              cudaMemcpyHostToDevice, hs->copy);
+        if (e == cudaSuccess) e = cudaEventRecord(hs->copied[k], hs->copy);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hs->copied[k], 0);
+        if (e != cudaSuccess) return cuda_fail(e, "streaming a map from host memory");
+        m.A = slot;
+        m.slot_layer = l;
+        if ((st = launch_map(m, s)) != RF_OK) return st;
+        e = cudaEventRecord(hs->freed[k], s);
+        if (e != cudaSuccess) return cuda_fail(e, "recording a map slot release");
+      }
+    }
+    if ((st = mark(start, 1)) != RF_OK) return st;
+    if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s)) != RF_OK) return st;
+    if ((st = mark(start, 2)) != RF_OK) return st;
+    sp.rows = static_cast<int32_t>(rc);
+    sp.first = start == 0 ? 1 : 0;
+    cudaError_t e = launch_gdn_state(sp, s);
+    if (e != cudaSuccess) return cuda_fail(e, "GDN state launch");
+    if ((st = mark(start, 3)) != RF_OK) return st;
+  }
+  return RF_OK;
+}

@@ -3,10 +3,6 @@
 
 using namespace rf;
 
-extern "C" size_t ridgefill_gdn_workspace_size(const rf_gdn_args*) { return 0; }
-extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args*, void*, size_t, void*) {
-  return fail(RF_ERR_SHAPE, "ridgefill_fill_gdn is not available in this build");
-}
 extern "C" size_t ridgefill_fit_workspace_size(const rf_fit_args*) { return 0; }
 extern "C" rf_status ridgefill_fit(const rf_fit_args*, void*, size_t, void*) {
   return fail(RF_ERR_SHAPE, "ridgefill_fit is not available in this build");

@@ -63,9 +63,9 @@ struct GemmParams {
   float inv_d;
   float eps;
   // GDN projection epilogue
-  float* gdn_k;        // [L, rows_alloc, H, dk] f32
-  float* gdn_v;        // [L, rows_alloc, H, dv] f32
-  float* gdn_gate;     // [L, rows_alloc, 2, H] f32 (log alpha, beta)
+  float* gdn_k;        // [L, H, rows_alloc, dk] f32
+  float* gdn_v;        // [L, H, rows_alloc, dv] f32
+  float* gdn_gate;     // [L, 2, H, rows_alloc] f32 (log alpha, beta)
   int32_t gdn_heads;
   int32_t gdn_rows_alloc;
   int32_t n_v_tiles;
@@ -79,13 +79,14 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 
 // ------------------------------------------------------------ GDN state
 struct GdnStateParams {
-  const float* k;      // [L, rows_alloc, H, dk]
-  const float* v;      // [L, rows_alloc, H, dv]
-  const float* gate;   // [L, rows_alloc, 2, H]
+  const float* k;      // [L, H, rows_alloc, dk]
+  const float* v;      // [L, H, rows_alloc, dv]
+  const float* gate;   // [L, 2, H, rows_alloc]: log alpha, then beta
   const float* S0;     // [L, H, dv, dk] or null
   float* S;            // [L, H, dv, dk]
   int32_t layers;
   int32_t heads;
+  int32_t dv;
   int32_t rows;        // rows of this launch
   int32_t rows_alloc;
   int32_t chunk;

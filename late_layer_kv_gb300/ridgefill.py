@@ -49,7 +49,7 @@ class GdnArgs(ctypes.Structure):
         ("rows", ctypes.c_int64), ("rows_per_chunk", ctypes.c_int64),
         ("rms_eps", ctypes.c_double), ("l2_eps", ctypes.c_double),
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
-        ("Wa", _vp), ("Wb", _vp), ("S0", _vp), ("S", _vp),
+        ("Wa", _vp), ("Wb", _vp), ("S0", _vp), ("S", _vp), ("stage_events", _vp),
     ]
 
 
@@ -136,7 +136,7 @@ def _stream(stream) -> int:
 def _event_array(events):
     if events is None:
         return None
-    arr = (ctypes.c_void_p * 3)(*[e.cuda_event for e in events])
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     return arr
 
 
@@ -174,6 +174,10 @@ def fill_workspace_size(args: FillArgs) -> int:
     return int(load().ridgefill_fill_workspace_size(ctypes.byref(args)))
 
 
+def gdn_workspace_size(args: GdnArgs) -> int:
+    return int(load().ridgefill_gdn_workspace_size(ctypes.byref(args)))
+
+
 def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
                    rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
                    workspace: Optional[torch.Tensor] = None, stream=None,
@@ -203,7 +207,8 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
 
 
 def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
-             l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0) -> GdnArgs:
+             l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
+             stage_events=None) -> GdnArgs:
     L, d_out, d_in = A.shape
     rows = H.shape[0]
     d_k = Wk.shape[1] // n_heads
@@ -225,23 +230,34 @@ def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: floa
     _dev(S, "S", torch.float32, (L, n_heads, d_v, d_k))
     if S0 is not None:
         _dev(S0, "S0", torch.float32, (L, n_heads, d_v, d_k))
-    return GdnArgs(L, d_in, d_out, n_heads, d_k, d_v, chunk, 1 if host else 0, rows,
-                   rows_per_chunk, float(rms_eps), float(l2_eps), _ptr(H), _ptr(A), _ptr(bias),
-                   _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Wa), _ptr(Wb), _ptr(S0), _ptr(S))
+    ev = _event_array(stage_events)
+    a = GdnArgs(L, d_in, d_out, n_heads, d_k, d_v, chunk, 1 if host else 0, rows,
+                rows_per_chunk, float(rms_eps), float(l2_eps), _ptr(H), _ptr(A), _ptr(bias),
+                _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Wa), _ptr(Wb), _ptr(S0), _ptr(S),
+                ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None)
+    a._events_keepalive = ev
+    return a
 
 
 def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
                        l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
-                       workspace: Optional[torch.Tensor] = None, stream=None) -> None:
-    """End-of-fill recurrent state ``S`` [L, H, dv, dk] f32 of Gated DeltaNet layers."""
+                       workspace: Optional[torch.Tensor] = None, stream=None,
+                       stage_events=None) -> None:
+    """End-of-fill recurrent state ``S`` [L, H, dv, dk] f32 of Gated DeltaNet layers.
+
+    ``stage_events``: optional four ``torch.cuda.Event`` recorded around the first
+    chunk's map GEMM, projection GEMM and state kernel."""
     args = gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, n_heads=n_heads, rms_eps=rms_eps,
-                    l2_eps=l2_eps, S0=S0, chunk=chunk, rows_per_chunk=rows_per_chunk)
+                    l2_eps=l2_eps, S0=S0, chunk=chunk, rows_per_chunk=rows_per_chunk,
+                    stage_events=stage_events)
     lib = load()
     need = int(lib.ridgefill_gdn_workspace_size(ctypes.byref(args)))
     if need == 0:
         _check(lib.ridgefill_fill_gdn(ctypes.byref(args), None, 0, _stream(stream)))
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=H.device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
     _check(lib.ridgefill_fill_gdn(ctypes.byref(args), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
 
