@@ -212,17 +212,21 @@ rf_status ridgefill_fill_gdn(const rf_gdn_args* args, void* workspace, size_t wo
  * RF_FIT_ACCUMULATE adds one batch of calibration pairs to caller-owned f64
  * running sums (products of bf16 inputs formed exactly and summed in f32
  * within the call, then added in f64):
- *   G += X^T X [d_in, d_in],  C += X^T Y_l (column block l of [d_in, L*d_out]),
+ *   G += X^T X [d_in, d_in],  C_l += Y_l^T X (C is [L, d_out, d_in]),
  *   sx += sum_rows X [d_in],  sy += sum_rows Y_l [L, d_out],  count += rows.
- * Zero the sums before the first batch; any batch split gives the same sums.
+ * Zero the sums before the first batch; any batch split gives the same sums
+ * up to f64 rounding.
  *
  * RF_FIT_SOLVE solves from the sums, centring them first:
- *   G~ = G - n mu_S mu_S^T, C~_l = C_l - n mu_S mu_l^T,
+ *   G~ = G - n mu_S mu_S^T, C~_l = C_l - n mu_l mu_S^T,
  *   alpha = lambda * tr(G~) / d_in,
- *   A_l = (solve(G~ + alpha I, C~_l))^T,  b_l = mu_l - A_l mu_S.
- * The solve equilibrates the system by its diagonal and uses a blocked
- * Cholesky factor.  Outputs A in the fill's layout [L, d_out, d_in] (bf16
- * and/or f32) and b [L, d_out] f32; alpha_out (device f64, may be NULL).
+ *   A_l = C~_l (G~ + alpha I)^-1,  b_l = mu_l - A_l mu_S.
+ * The system is equilibrated by its diagonal, factored by a blocked f32
+ * Cholesky and inverted; the product with C~ runs on the tensor cores with a
+ * three-term bf16 split of both operands (about 16 significant bits each).
+ * Outputs A in the fill's layout [L, d_out, d_in] (bf16 and/or f32) and b
+ * [L, d_out] f32; alpha_out (device f64, may be NULL).  A non-positive pivot
+ * is reported by ridgefill_device_error() as RF_ERR_NUMERIC.
  *
  * Layouts: X [rows, d_in] bf16; Y [L, rows, d_out] bf16.
  * Limits: d_in % 128 == 0, d_out % 128 == 0, d_in <= 16384.

@@ -205,7 +205,9 @@ extern "C" rf_status ridgefill_device_error(void* stream, int* code) {
     if (e != cudaSuccess) return rf::cuda_fail(e, "clearing the device error word");
   }
   *code = v;
-  return v == 0 ? RF_OK : rf::fail(RF_ERR_TIMEOUT, "device wait ran out at site %d", v);
+  if (v == 0) return RF_OK;
+  if (v == rf::kErrNumeric) return rf::fail(RF_ERR_NUMERIC, "ridge system not positive definite");
+  return rf::fail(RF_ERR_TIMEOUT, "device wait ran out at site %d", v);
 }
 
 extern "C" double ridgefill_compute_share(int32_t split, int32_t n_layers, int64_t tail,

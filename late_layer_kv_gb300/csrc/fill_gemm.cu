@@ -66,7 +66,7 @@ struct TileB {
 
 __device__ __forceinline__ TileB tile_b(const GemmParams& p, int n) {
   TileB t;
-  if (p.mode == kModeMap) {
+  if (p.mode == kModeMap || p.mode == kModeGram || p.mode == kModeSolve) {
     t.seg = 0; t.nrow = n * p.bn; t.bn = p.bn;
   } else if (p.mode == kModeKV) {
     const bool v = n >= p.n_k_tiles;
@@ -305,6 +305,82 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, int q, int lane
   if (lane == 0) mbar_arrive(tempty);
 }
 
+// Fit sums: this tile of [X | Y_1 .. Y_L]^T X (f32, summed over the call's rows)
+// is added into the caller's f64 sums, one output row per thread.
+__device__ void epilogue_gram(const GemmParams& p, uint32_t tcol, int q, int lane, int m, int n,
+                              uint64_t* tempty) {
+  const int r = q * 32 + lane;
+  double* dst;
+  if (m < p.gram_x_tiles) {
+    dst = p.gram_G + static_cast<size_t>(m * kBM + r) * p.gram_ld;
+  } else {
+    const int mm = m - p.gram_x_tiles;
+    const int l = mm / p.gram_y_tiles_per_layer;
+    const int o = (mm % p.gram_y_tiles_per_layer) * kBM + r;
+    dst = p.gram_C + (static_cast<size_t>(l) * p.d_out + o) * p.gram_ld;
+  }
+  dst += n * p.bn;
+  for (int c0 = 0; c0 < p.bn; c0 += 32) {
+    uint32_t a[32];
+    tmem_ld32(tcol + c0, a);
+    tmem_wait_ld();
+    if (c0 + 32 == p.bn) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+    }
+    double2* d2 = reinterpret_cast<double2*>(dst + c0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      double2 v = d2[j];
+      v.x += static_cast<double>(f32(a[2 * j]));
+      v.y += static_cast<double>(f32(a[2 * j + 1]));
+      d2[j] = v;
+    }
+  }
+}
+
+// Fit solve: out[o, i] = s_i * acc[o, i] (f32 and/or bf16) and the partial
+// sum over this tile's columns of out[o, i] * mu_x[i] (for the offsets).
+__device__ void epilogue_solve(const GemmParams& p, uint32_t tcol, int q, int lane, int m, int n,
+                               uint64_t* tempty) {
+  const int o = m * kBM + q * 32 + lane;
+  const int c_base = n * p.bn;
+  const bool valid = o < p.rows;
+  float part = 0.f;
+  for (int c0 = 0; c0 < p.bn; c0 += 32) {
+    uint32_t a[32];
+    tmem_ld32(tcol + c0, a);
+    tmem_wait_ld();
+    if (c0 + 32 == p.bn) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(tempty);
+    }
+    if (!valid) continue;
+    const int c = c_base + c0;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      v[j] = f32(a[j]) * __ldg(p.col_scale + c + j);
+      part = fmaf(v[j], __ldg(p.mu_x + c + j), part);
+    }
+    if (p.out_f32 != nullptr) {
+      float4* d4 = reinterpret_cast<float4*>(p.out_f32 + static_cast<size_t>(o) * p.out_ld + c);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    }
+    if (p.out_bf16 != nullptr) {
+      uint4* d4 = reinterpret_cast<uint4*>(p.out_bf16 + static_cast<size_t>(o) * p.out_ld + c);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        d4[j] = make_uint4(pack_bf16(v[8 * j], v[8 * j + 1]), pack_bf16(v[8 * j + 2], v[8 * j + 3]),
+                           pack_bf16(v[8 * j + 4], v[8 * j + 5]), pack_bf16(v[8 * j + 6], v[8 * j + 7]));
+    }
+  }
+  if (valid) p.bias_part[static_cast<size_t>(o) * p.n_tiles + n] = part;
+}
+
 }  // namespace
 
 __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -340,7 +416,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
   if (warp == 0 && lane == 0) {
     tma_prefetch(&p.tmA);
     tma_prefetch(&p.tmB[0]);
-    if (p.mode != kModeMap) tma_prefetch(&p.tmB[1]);
+    if (p.mode == kModeKV || p.mode == kModeGdnProj) tma_prefetch(&p.tmB[1]);
+    if (p.mode == kModeGram) tma_prefetch(&p.tmA2);
   }
   if (warp == 2) {
     tmem_alloc(tmem_slot, 512);
@@ -367,9 +444,31 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
             break;
           }
           mbar_expect_tx(&full[stage], bytes);
-          tma_load_3d(smem_u32(sA + stage * kABytes), &p.tmA, &full[stage], kb * kBK, m * kBM, b);
           uint8_t* bdst = sB + stage * kBBytes;
-          if (tb.seg < 2) {
+          if (p.mode == kModeGram) {
+            // MN-major operands: 64-wide column blocks of [rows, width] arrays, 64 rows of K
+            uint8_t* adst = sA + stage * kABytes;
+            if (m < p.gram_x_tiles) {
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_3d(smem_u32(adst + j * 8192), &p.tmA, &full[stage], m * kBM + 64 * j,
+                            kb * kBK, 0);
+            } else {
+              const int mm = m - p.gram_x_tiles;
+              const int l = mm / p.gram_y_tiles_per_layer;
+              const int m0 = (mm % p.gram_y_tiles_per_layer) * kBM;
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_3d(smem_u32(adst + j * 8192), &p.tmA2, &full[stage], m0 + 64 * j,
+                            kb * kBK, l);
+            }
+            for (int j = 0; j < tb.bn / 64; ++j)
+              tma_load_3d(smem_u32(bdst + j * 8192), &p.tmB[0], &full[stage], tb.nrow + 64 * j,
+                          kb * kBK, 0);
+          } else {
+            tma_load_3d(smem_u32(sA + stage * kABytes), &p.tmA, &full[stage], kb * kBK, m * kBM, b);
+          }
+          if (p.mode == kModeGram) {
+            // loaded above
+          } else if (tb.seg < 2) {
             tma_load_3d(smem_u32(bdst), &p.tmB[tb.seg], &full[stage], kb * kBK, tb.nrow, b);
           } else {
             tma_load_3d(smem_u32(bdst), &p.tmB[2], &full[stage], kb * kBK, 0, b);
@@ -392,7 +491,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
         int m, n, b;
         decode_tile(t, p, m, n, b);
         const TileB tb = tile_b(p, n);
-        const uint32_t idesc = idesc_bf16_f32(kBM, tb.bn);
+        const bool mn = p.mode == kModeGram;
+        const uint32_t idesc = idesc_bf16_f32(kBM, tb.bn) | (mn ? (3u << 15) : 0u);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, kErrMma)) break;
@@ -404,12 +504,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * kABytes));
-          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * kBBytes));
+          if (!mn) {
+            const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * kABytes));
+            const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * kBBytes));
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            // advance 16 bf16 (32 B) along K inside the swizzled 128-byte row
-            mma_bf16(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k) {
+              // advance 16 bf16 (32 B) along K inside the swizzled 128-byte row
+              mma_bf16(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
+          } else {
+            // MN-major: 64-element column blocks 8 KB apart, K rows 128 B apart
+            const uint64_t ad = sdesc_mnmajor_sw128(smem_u32(sA + stage * kABytes), 8192);
+            const uint64_t bd = sdesc_mnmajor_sw128(smem_u32(sB + stage * kBBytes), 8192);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              // advance 16 K rows (2048 B)
+              mma_bf16(dt, ad + 128 * k, bd + 128 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            }
           }
           mma_commit(&empty[stage]);
           if (++stage == kStages) {
@@ -437,8 +548,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
         epilogue_map(p, tcol, stg, q, lane, m, n, &tempty[acc]);
       } else if (p.mode == kModeKV) {
         epilogue_kv(p, tcol, stg, q, lane, m, n, b, &tempty[acc]);
-      } else {
+      } else if (p.mode == kModeGdnProj) {
         epilogue_gdn(p, tcol, q, lane, m, n, b, &tempty[acc]);
+      } else if (p.mode == kModeGram) {
+        epilogue_gram(p, tcol, q, lane, m, n, &tempty[acc]);
+      } else {
+        epilogue_solve(p, tcol, q, lane, m, n, &tempty[acc]);
       }
     }
     if (lane == 0) bulk_wait_all<0>();

@@ -1,0 +1,542 @@
+// fit.cu -- ridgefill_fit: the closed-form ridge maps (RidgeFill, "Training-Free
+// Late-Layer Cache Fill for Faster Prefill", section 2.2: "The ridge map",
+// "Fitting", "The penalty").
+//
+// ACCUMULATE adds one batch of calibration pairs to caller-owned f64 running
+// sums.  One tcgen05 GEMM forms [X^T X ; Y_1^T X ; ... ; Y_L^T X] over the
+// batch's rows: X and Y are read in place as MN-major operands (their rows are
+// the reduction dimension), products of bf16 inputs are exact in f32, the
+// batch is summed in f32 in TMEM and each tile is added into the f64 sums.
+// The column sums and the row count go the same way.
+//
+// SOLVE, from the sums:
+//   mu_S = sx/n, mu_l = sy_l/n, G~ = G - n mu_S mu_S^T, C~_l = C_l - n mu_l mu_S^T
+//   alpha = lambda * tr(G~) / d_in
+//   s_i = (G~_ii + alpha)^(-1/2);  G^ = diag(s) (G~ + alpha I) diag(s)   (unit diagonal)
+//   G^ = L L^T (blocked Cholesky, f32), X = L^-1 (blocked), G^-1 = X^T X
+//   A_l[o, i] = s_i sum_k (s_k C~_l[o, k]) G^-1[k, i],  b_l = mu_l - A_l mu_S
+// The last product is one tcgen05 GEMM over the split bf16 operands
+// [c_hi | c_hi | c_lo] x [g_hi | g_lo | g_hi] (K = 3 d_in), which carries about
+// 16 bits of each f32 operand.
+#include <cmath>
+
+#include "abi_common.h"
+#include "sm103_ptx.cuh"
+
+namespace rf {
+namespace {
+
+constexpr int kNB = 64;  // Cholesky / triangular-inverse block
+
+// ------------------------------------------------------------ column sums
+// out[c] += sum over rows of in[r, c] for a [rows, width] bf16 array, one
+// thread per column pair; f32 over blocks of 256 rows, then f64.
+__global__ void colsum_kernel(const __nv_bfloat16* in, int64_t rows, int width, int batches,
+                              int64_t batch_stride, double* out) {
+  const int pairs = width / 2;
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= static_cast<int64_t>(pairs) * batches) return;
+  const int b = static_cast<int>(t / pairs);
+  const int c = static_cast<int>(t % pairs) * 2;
+  const __nv_bfloat16* p = in + b * batch_stride + c;
+  double a0 = 0.0, a1 = 0.0;
+  for (int64_t r0 = 0; r0 < rows; r0 += 256) {
+    const int64_t r1 = r0 + 256 < rows ? r0 + 256 : rows;
+    float f0 = 0.f, f1 = 0.f;
+    for (int64_t r = r0; r < r1; ++r) {
+      const float2 v =
+          __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p + r * width));
+      f0 += v.x;
+      f1 += v.y;
+    }
+    a0 += f0;
+    a1 += f1;
+  }
+  out[static_cast<int64_t>(b) * width + c] += a0;
+  out[static_cast<int64_t>(b) * width + c + 1] += a1;
+}
+
+__global__ void add_count_kernel(double* count, double rows) { *count += rows; }
+
+// ------------------------------------------------------------ solve: centring
+// One block: mu_x, alpha (trace of the centred Gram), the equilibration s.
+__global__ void prep_kernel(const double* G, const double* sx, const double* count, int d,
+                            double lam, float* s_f32, float* mu_f32, double* mu_f64,
+                            double* alpha_ws, double* alpha_out) {
+  __shared__ double red[256];
+  const double n = *count;
+  double tr = 0.0;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const double mu = sx[i] / n;
+    mu_f64[i] = mu;
+    mu_f32[i] = static_cast<float>(mu);
+    tr += G[static_cast<size_t>(i) * d + i] - n * mu * mu;
+  }
+  red[threadIdx.x] = tr;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  const double alpha = lam * red[0] / d;
+  for (int i = threadIdx.x; i < d; i += blockDim.x) {
+    const double mu = sx[i] / n;
+    const double dd = G[static_cast<size_t>(i) * d + i] - n * mu * mu + alpha;
+    s_f32[i] = static_cast<float>(dd > 0.0 ? 1.0 / sqrt(dd) : 0.0);
+  }
+  if (threadIdx.x == 0) {
+    *alpha_ws = alpha;
+    if (alpha_out != nullptr) *alpha_out = alpha;
+  }
+}
+
+// G^ = diag(s) (G - n mu mu^T + alpha I) diag(s), f32 [d, d]
+__global__ void equilibrate_kernel(const double* G, const double* count, const double* mu,
+                                   const float* s, const double* alpha, int d, float* Gh) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= static_cast<int64_t>(d) * d) return;
+  const int i = static_cast<int>(t / d), j = static_cast<int>(t % d);
+  double v = G[t] - (*count) * mu[i] * mu[j];
+  if (i == j) v += *alpha;
+  Gh[t] = static_cast<float>(v * s[i] * s[j]);
+}
+
+// ------------------------------------------------------------ Cholesky (f32)
+// In-place factor of one 64x64 diagonal block (lower); a pivot <= 0 records
+// kErrNumeric in the device error word and continues with pivot 1.
+__global__ void potrf_diag_kernel(float* A, int ld, int kb, int* err) {
+  __shared__ float a[kNB][kNB + 1];
+  float* blk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
+  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x)
+    a[e / kNB][e % kNB] = blk[static_cast<size_t>(e / kNB) * ld + e % kNB];
+  __syncthreads();
+  for (int j = 0; j < kNB; ++j) {
+    if (threadIdx.x == 0) {
+      float v = a[j][j];
+      if (!(v > 0.f)) {
+        atomicCAS(err, 0, kErrNumeric);
+        v = 1.f;
+      }
+      a[j][j] = sqrtf(v);
+    }
+    __syncthreads();
+    const float piv = a[j][j];
+    for (int i = j + 1 + threadIdx.x; i < kNB; i += blockDim.x) a[i][j] /= piv;
+    __syncthreads();
+    const int m = kNB - j - 1;
+    for (int e = threadIdx.x; e < m * m; e += blockDim.x) {
+      const int i = j + 1 + e / m, k = j + 1 + e % m;
+      if (k <= i) a[i][k] -= a[i][j] * a[k][j];
+    }
+    __syncthreads();
+  }
+  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x) {
+    const int i = e / kNB, k = e % kNB;
+    blk[static_cast<size_t>(i) * ld + k] = k <= i ? a[i][k] : 0.f;
+  }
+}
+
+// Panel: A_ik <- A_ik L_kk^-T for block rows i > kb (one block row per CTA,
+// one matrix row per thread, forward substitution).
+__global__ void trsm_panel_kernel(float* A, int ld, int kb) {
+  __shared__ float L[kNB][kNB + 1];
+  __shared__ float X[kNB][kNB + 1];
+  const int ib = kb + 1 + blockIdx.x;
+  const float* lkk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
+  float* aik = A + static_cast<size_t>(ib) * kNB * ld + static_cast<size_t>(kb) * kNB;
+  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x) {
+    L[e / kNB][e % kNB] = lkk[static_cast<size_t>(e / kNB) * ld + e % kNB];
+    X[e / kNB][e % kNB] = aik[static_cast<size_t>(e / kNB) * ld + e % kNB];
+  }
+  __syncthreads();
+  if (threadIdx.x < kNB) {
+    const int r = threadIdx.x;
+    for (int c = 0; c < kNB; ++c) {
+      float s = X[r][c];
+      for (int c2 = 0; c2 < c; ++c2) s -= X[r][c2] * L[c][c2];
+      X[r][c] = s / L[c][c];
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x)
+    aik[static_cast<size_t>(e / kNB) * ld + e % kNB] = X[e / kNB][e % kNB];
+}
+
+// Inverse of each 64x64 lower diagonal block of L, in place (upper part zero).
+__global__ void trinv_diag_kernel(float* A, int ld) {
+  __shared__ float L[kNB][kNB + 1];
+  __shared__ float X[kNB][kNB + 1];
+  float* blk = A + static_cast<size_t>(blockIdx.x) * kNB * (ld + 1);
+  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x)
+    L[e / kNB][e % kNB] = blk[static_cast<size_t>(e / kNB) * ld + e % kNB];
+  __syncthreads();
+  if (threadIdx.x < kNB) {
+    const int c = threadIdx.x;
+    for (int r = 0; r < kNB; ++r) {
+      if (r < c) {
+        X[r][c] = 0.f;
+        continue;
+      }
+      float s = (r == c) ? 1.f : 0.f;
+      for (int k = c; k < r; ++k) s -= L[r][k] * X[k][c];
+      X[r][c] = s / L[r][r];
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x)
+    blk[static_cast<size_t>(e / kNB) * ld + e % kNB] = X[e / kNB][e % kNB];
+}
+
+__global__ void zero_upper_kernel(float* A, int d) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= static_cast<int64_t>(d) * d) return;
+  if (t % d > t / d) A[t] = 0.f;
+}
+
+// ------------------------------------------------------------ f32 SIMT GEMM
+// C = alpha op(A) op(B) + beta C for row-major f32 matrices; 64x64 tiles,
+// 256 threads with 4x4 outputs each.  lower_only skips tiles above the
+// diagonal; k_tri starts the K loop at max(m0, n0) (operands lower triangular
+// in K, as in X^T X with X lower); k_end_tri stops it at m0 + 64 (op(A) lower).
+struct SgemmArgs {
+  int M, N, K;
+  float alpha, beta;
+  const float* A; int lda;
+  const float* B; int ldb;
+  float* C; int ldc;
+  int lower_only, k_tri, k_end_tri;
+};
+
+template <bool TA, bool TB>
+__global__ void __launch_bounds__(256) sgemm_kernel(const SgemmArgs g) {
+  __shared__ float As[16][64 + 4];
+  __shared__ float Bs[16][64 + 4];
+  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  if (g.lower_only && n0 > m0 + 63) return;
+  const int tid = threadIdx.x;
+  const int tx = tid % 16, ty = tid / 16;
+  float acc[4][4] = {};
+  int kbeg = 0, kend = g.K;
+  if (g.k_tri) kbeg = (max(m0, n0) / 16) * 16;
+  if (g.k_end_tri) kend = min(g.K, m0 + 64);
+  for (int k0 = kbeg; k0 < kend; k0 += 16) {
+    for (int e = tid; e < 64 * 16; e += 256) {
+      int mm, kk;
+      if (TA) { kk = e / 64; mm = e % 64; } else { mm = e / 16; kk = e % 16; }
+      const int m = m0 + mm, k = k0 + kk;
+      float v = 0.f;
+      if (m < g.M && k < g.K) v = TA ? g.A[static_cast<size_t>(k) * g.lda + m]
+                                     : g.A[static_cast<size_t>(m) * g.lda + k];
+      As[kk][mm] = v;
+    }
+    for (int e = tid; e < 64 * 16; e += 256) {
+      int nn, kk;
+      if (TB) { nn = e / 16; kk = e % 16; } else { kk = e / 64; nn = e % 64; }
+      const int n = n0 + nn, k = k0 + kk;
+      float v = 0.f;
+      if (n < g.N && k < g.K) v = TB ? g.B[static_cast<size_t>(n) * g.ldb + k]
+                                     : g.B[static_cast<size_t>(k) * g.ldb + n];
+      Bs[kk][nn] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= g.M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= g.N) continue;
+      float* c = g.C + static_cast<size_t>(m) * g.ldc + n;
+      *c = g.alpha * acc[i][j] + (g.beta != 0.f ? g.beta * *c : 0.f);
+    }
+  }
+}
+
+cudaError_t sgemm(bool ta, bool tb, const SgemmArgs& g, cudaStream_t s) {
+  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  dim3 grid((g.N + 63) / 64, (g.M + 63) / 64);
+  if (!ta && !tb) sgemm_kernel<false, false><<<grid, 256, 0, s>>>(g);
+  else if (!ta && tb) sgemm_kernel<false, true><<<grid, 256, 0, s>>>(g);
+  else if (ta && !tb) sgemm_kernel<true, false><<<grid, 256, 0, s>>>(g);
+  else sgemm_kernel<true, true><<<grid, 256, 0, s>>>(g);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ split operands
+__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// B' [d, 3d] = [hi(G^-1) | lo(G^-1) | hi(G^-1)]
+__global__ void split_ginv_kernel(const float* Gi, int d, __nv_bfloat16* Bp) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= static_cast<int64_t>(d) * d) return;
+  const int64_t i = t / d, k = t % d;
+  __nv_bfloat16 hi, lo;
+  split_bf16(Gi[t], hi, lo);
+  __nv_bfloat16* row = Bp + i * 3 * d;
+  row[k] = hi;
+  row[d + k] = lo;
+  row[2 * d + k] = hi;
+}
+
+// A' [L*d_out, 3d] = [hi(c) | hi(c) | lo(c)],  c[o, k] = s_k (C[o, k] - n mu_y[o] mu_x[k])
+__global__ void split_rhs_kernel(const double* C, const double* sy, const double* count,
+                                 const double* mu_x, const float* s, int64_t rows_out, int d,
+                                 __nv_bfloat16* Ap) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= rows_out * d) return;
+  const int64_t o = t / d, k = t % d;
+  const double n = *count;
+  const double v = (C[t] - n * (sy[o] / n) * mu_x[k]) * static_cast<double>(s[k]);
+  __nv_bfloat16 hi, lo;
+  split_bf16(static_cast<float>(v), hi, lo);
+  __nv_bfloat16* row = Ap + o * 3 * d;
+  row[k] = hi;
+  row[d + k] = hi;
+  row[2 * d + k] = lo;
+}
+
+// b[o] = mu_y[o] - sum_t part[o, t]
+__global__ void bias_kernel(const double* sy, const double* count, const float* part,
+                            int n_tiles, int64_t rows_out, float* b) {
+  const int64_t o = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (o >= rows_out) return;
+  double acc = 0.0;
+  for (int t = 0; t < n_tiles; ++t) acc += part[o * n_tiles + t];
+  b[o] = static_cast<float>(sy[o] / (*count) - acc);
+}
+
+// ------------------------------------------------------------ plan
+struct FitPlan {
+  size_t off_gh = 0, off_s = 0, off_mu32 = 0, off_mu64 = 0, off_alpha = 0, off_T = 0,
+         off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0, total = 0;
+  int bn = 0;
+};
+
+rf_status validate_fit(const rf_fit_args* a) {
+  if (a == nullptr) return fail(RF_ERR_ARG, "args is NULL");
+  if (a->n_layers < 1) return fail(RF_ERR_SHAPE, "n_layers must be >= 1");
+  if (a->d_in < 128 || a->d_in % 128 != 0 || a->d_in > 16384)
+    return fail(RF_ERR_SHAPE, "d_in must be a multiple of 128 in [128, 16384]");
+  if (a->d_out < 128 || a->d_out % 128 != 0) return fail(RF_ERR_SHAPE, "d_out must be a positive multiple of 128");
+  if ((a->flags & ~(RF_FIT_ACCUMULATE | RF_FIT_SOLVE)) != 0 || a->flags == 0)
+    return fail(RF_ERR_ARG, "flags must be RF_FIT_ACCUMULATE and/or RF_FIT_SOLVE");
+  if (a->rows < 0 || a->rows >= (int64_t(1) << 31)) return fail(RF_ERR_ARG, "rows out of range");
+  if (static_cast<int64_t>(a->n_layers) * a->d_out >= (int64_t(1) << 31) / 3)
+    return fail(RF_ERR_SHAPE, "n_layers * d_out too large");
+  if ((a->flags & RF_FIT_SOLVE) && !(a->lambda >= 0.0)) return fail(RF_ERR_ARG, "lambda must be >= 0");
+  return RF_OK;
+}
+
+void plan_fit(const rf_fit_args* a, FitPlan* pl) {
+  const size_t d = a->d_in, M = static_cast<size_t>(a->n_layers) * a->d_out;
+  pl->bn = (a->d_in % 256 == 0) ? 256 : 128;
+  size_t off = 0;
+  if (a->flags & RF_FIT_SOLVE) {
+    pl->off_gh = off;    off = align_up(off + d * d * 4, 256);
+    pl->off_s = off;     off = align_up(off + d * 4, 256);
+    pl->off_mu32 = off;  off = align_up(off + d * 4, 256);
+    pl->off_mu64 = off;  off = align_up(off + d * 8, 256);
+    pl->off_alpha = off; off = align_up(off + 8, 256);
+    pl->off_T = off;     off = align_up(off + d * kNB * 4, 256);
+    pl->off_gi = off;    off = align_up(off + d * d * 4, 256);
+    pl->off_bp = off;    off = align_up(off + d * 3 * d * 2, 256);
+    pl->off_ap = off;    off = align_up(off + M * 3 * d * 2, 256);
+    pl->off_part = off;  off = align_up(off + M * (d / pl->bn) * 4, 256);
+  }
+  pl->total = off;
+}
+
+rf_status accumulate(const rf_fit_args* a, const FitPlan& pl, cudaStream_t s) {
+  const int64_t rows = a->rows;
+  if (rows == 0) return RF_OK;
+  const int L = a->n_layers, din = a->d_in, dout = a->d_out;
+  // column sums
+  {
+    const int64_t th = din / 2;
+    colsum_kernel<<<static_cast<unsigned>((th + 255) / 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(a->X), rows, din, 1, 0, a->sx);
+    const int64_t ty = static_cast<int64_t>(dout / 2) * L;
+    colsum_kernel<<<static_cast<unsigned>((ty + 255) / 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(a->Y), rows, dout, L, rows * dout, a->sy);
+    add_count_kernel<<<1, 1, 0, s>>>(a->count, static_cast<double>(rows));
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
+  }
+  GemmParams p{};
+  p.mode = kModeGram;
+  p.k_blocks = static_cast<int32_t>(ceil_div(rows, kBK));
+  const uint64_t xrow = static_cast<uint64_t>(din) * 2, yrow = static_cast<uint64_t>(dout) * 2;
+  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->X, din, rows, 1, xrow, 0,
+                         64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmA2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Y, dout, rows, L, yrow,
+                          yrow * rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+  p.tmB[0] = p.tmA;
+  if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the Gram GEMM");
+  p.gram_x_tiles = din / kBM;
+  p.gram_y_tiles_per_layer = dout / kBM;
+  p.m_tiles = p.gram_x_tiles + L * p.gram_y_tiles_per_layer;
+  p.bn = pl.bn;
+  p.n_tiles = din / pl.bn;
+  p.batches = 1;
+  p.group_m = 16;
+  p.d_out = dout;
+  p.gram_G = a->G;
+  p.gram_C = a->C;
+  p.gram_ld = din;
+  p.err = device_error_word();
+  if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  cudaError_t e = launch_gemm(p, grid, s);
+  if (e != cudaSuccess) return cuda_fail(e, "Gram GEMM launch");
+  return RF_OK;
+}
+
+rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream_t s) {
+  const int d = a->d_in;
+  const int64_t M = static_cast<int64_t>(a->n_layers) * a->d_out;
+  float* Gh = reinterpret_cast<float*>(ws + pl.off_gh);
+  float* sc = reinterpret_cast<float*>(ws + pl.off_s);
+  float* mu32 = reinterpret_cast<float*>(ws + pl.off_mu32);
+  double* mu64 = reinterpret_cast<double*>(ws + pl.off_mu64);
+  double* alpha = reinterpret_cast<double*>(ws + pl.off_alpha);
+  float* T = reinterpret_cast<float*>(ws + pl.off_T);
+  float* Gi = reinterpret_cast<float*>(ws + pl.off_gi);
+  __nv_bfloat16* Bp = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_bp);
+  __nv_bfloat16* Ap = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_ap);
+  float* part = reinterpret_cast<float*>(ws + pl.off_part);
+  int* err = device_error_word();
+  if (err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
+  const int64_t dd = static_cast<int64_t>(d) * d;
+
+  prep_kernel<<<1, 256, 0, s>>>(a->G, a->sx, a->count, d, a->lambda, sc, mu32, mu64, alpha,
+                                a->alpha_out);
+  equilibrate_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(a->G, a->count, mu64,
+                                                                              sc, alpha, d, Gh);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "fit preparation launch");
+
+  // blocked Cholesky, lower factor in place
+  const int nb = d / kNB;
+  for (int kb = 0; kb < nb; ++kb) {
+    potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb, err);
+    if (kb + 1 < nb) {
+      trsm_panel_kernel<<<nb - kb - 1, 256, 0, s>>>(Gh, d, kb);
+      const int rem = d - (kb + 1) * kNB;
+      const float* panel = Gh + static_cast<size_t>(kb + 1) * kNB * d + static_cast<size_t>(kb) * kNB;
+      float* trail = Gh + static_cast<size_t>(kb + 1) * kNB * d + static_cast<size_t>(kb + 1) * kNB;
+      SgemmArgs g{rem, rem, kNB, -1.f, 1.f, panel, d, panel, d, trail, d, 1, 0, 0};
+      if ((e = sgemm(false, true, g, s)) != cudaSuccess) return cuda_fail(e, "Cholesky update");
+    }
+  }
+  zero_upper_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gh, d);
+  // X = L^-1 in place: diagonal blocks, then block columns right to left
+  trinv_diag_kernel<<<nb, 256, 0, s>>>(Gh, d);
+  for (int j = nb - 2; j >= 0; --j) {
+    const int rem = d - (j + 1) * kNB;
+    float* col = Gh + static_cast<size_t>(j + 1) * kNB * d + static_cast<size_t>(j) * kNB;
+    const float* xjj = Gh + static_cast<size_t>(j) * kNB * d + static_cast<size_t>(j) * kNB;
+    const float* xsub = Gh + static_cast<size_t>(j + 1) * kNB * d + static_cast<size_t>(j + 1) * kNB;
+    SgemmArgs g1{rem, kNB, kNB, 1.f, 0.f, col, d, xjj, d, T, kNB, 0, 0, 0};       // T = L_sub,j X_jj
+    if ((e = sgemm(false, false, g1, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
+    SgemmArgs g2{rem, kNB, rem, -1.f, 0.f, xsub, d, T, kNB, col, d, 0, 0, 1};     // X_sub,j = -X_sub T
+    if ((e = sgemm(false, false, g2, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
+  }
+  // G^-1 = X^T X
+  SgemmArgs gi{d, d, d, 1.f, 0.f, Gh, d, Gh, d, Gi, d, 0, 1, 0};
+  if ((e = sgemm(true, false, gi, s)) != cudaSuccess) return cuda_fail(e, "inverse product");
+
+  split_ginv_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gi, d, Bp);
+  split_rhs_kernel<<<static_cast<unsigned>((M * d + 255) / 256), 256, 0, s>>>(
+      a->C, a->sy, a->count, mu64, sc, M, d, Ap);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "operand split launch");
+
+  GemmParams p{};
+  p.mode = kModeSolve;
+  p.k_blocks = 3 * d / kBK;
+  const uint64_t krow = static_cast<uint64_t>(3 * d) * 2;
+  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap, 3 * d, M, 1, krow, 0, kBK,
+                         kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, 3 * d, d, 1, krow, 0,
+                          kBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the solve GEMM");
+  p.m_tiles = static_cast<int32_t>(ceil_div(M, kBM));
+  p.bn = pl.bn;
+  p.n_tiles = d / pl.bn;
+  p.batches = 1;
+  p.group_m = 16;
+  p.rows = static_cast<int32_t>(M);
+  p.col_scale = sc;
+  p.mu_x = mu32;
+  p.out_f32 = a->A_out_f32;
+  p.out_bf16 = static_cast<__nv_bfloat16*>(a->A_out);
+  p.bias_part = part;
+  p.out_ld = d;
+  p.err = err;
+  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+  if ((e = launch_gemm(p, grid, s)) != cudaSuccess) return cuda_fail(e, "solve GEMM launch");
+  bias_kernel<<<static_cast<unsigned>((M + 255) / 256), 256, 0, s>>>(a->sy, a->count, part,
+                                                                     p.n_tiles, M, a->b_out);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "offset launch");
+  return RF_OK;
+}
+
+}  // namespace
+}  // namespace rf
+
+using namespace rf;
+
+extern "C" size_t ridgefill_fit_workspace_size(const rf_fit_args* a) {
+  if (validate_fit(a) != RF_OK) return 0;
+  FitPlan pl;
+  plan_fit(a, &pl);
+  return pl.total > 0 ? pl.total : 256;
+}
+
+extern "C" rf_status ridgefill_fit(const rf_fit_args* a, void* workspace, size_t ws_bytes,
+                                   void* stream) {
+  rf_status st = validate_fit(a);
+  if (st != RF_OK) return st;
+  const void* sums[] = {a->G, a->C, a->sx, a->sy, a->count};
+  for (const void* q : sums)
+    if (q == nullptr) return fail(RF_ERR_ARG, "a running-sum pointer is NULL");
+  if ((a->flags & RF_FIT_ACCUMULATE) && a->rows > 0 && (a->X == nullptr || a->Y == nullptr))
+    return fail(RF_ERR_ARG, "X and Y are required to accumulate");
+  if ((a->flags & RF_FIT_SOLVE) &&
+      (a->b_out == nullptr || (a->A_out == nullptr && a->A_out_f32 == nullptr)))
+    return fail(RF_ERR_ARG, "the solve needs b_out and A_out or A_out_f32");
+  const void* dev[] = {a->X, a->Y, a->G, a->C, a->A_out, a->A_out_f32, a->b_out, workspace};
+  for (const void* q : dev)
+    if (q != nullptr && !aligned16(q)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
+  FitPlan pl;
+  plan_fit(a, &pl);
+  if ((a->flags & RF_FIT_SOLVE) && (workspace == nullptr || ws_bytes < pl.total))
+    return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes", pl.total);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (a->flags & RF_FIT_ACCUMULATE) {
+    if ((st = accumulate(a, pl, s)) != RF_OK) return st;
+  }
+  if (a->flags & RF_FIT_SOLVE) {
+    if ((st = solve(a, pl, static_cast<uint8_t*>(workspace), s)) != RF_OK) return st;
+  }
+  return RF_OK;
+}

@@ -24,6 +24,8 @@ enum GemmMode : int {
   kModeMap = 0,      // X_hat = H A^T + b (times gain), row sums of squares
   kModeKV = 1,       // K/V projection, RMS scale, RoPE on K, cache store
   kModeGdnProj = 2,  // GDN projections: RMS scale, k L2-norm, v, sigmoid gates
+  kModeGram = 3,     // fit sums: [X | Y_1 .. Y_L]^T X over rows, MN-major operands, f64 add
+  kModeSolve = 4,    // fit solve: A = C~^T G^-1 (split bf16), column scale, f32/bf16 out
 };
 
 // Device error word sites (which wait ran out).
@@ -32,10 +34,12 @@ enum ErrSite : int {
   kErrMma = 2,
   kErrEpilogue = 3,
   kErrGdn = 4,
+  kErrNumeric = 7,   // the ridge system was not positive definite (Cholesky pivot <= 0)
 };
 
 struct GemmParams {
   CUtensorMap tmA;     // A operand, K-major 3D {K, rows, batch}, box {64, 128, 1}
+  CUtensorMap tmA2;    // gram mode: the Y operand, MN-major 3D {d_out, rows, L}, box {64, 64, 1}
   CUtensorMap tmB[4];  // B operand segments, K-major 3D {K, n, batch}, box {64, bn|16, 1}
   CUtensorMap tmO[2];  // outputs, 3D, box {64, 32, 1}
   int32_t mode;
@@ -70,6 +74,19 @@ struct GemmParams {
   int32_t gdn_rows_alloc;
   int32_t n_v_tiles;
   float l2_eps;
+  // gram epilogue (MN-major operands; A = X for the first gram_x_tiles M tiles, else Y)
+  int32_t gram_x_tiles;
+  int32_t gram_y_tiles_per_layer;
+  double* gram_G;      // [d_in, d_in]
+  double* gram_C;      // [L, d_out, d_in]
+  int32_t gram_ld;     // d_in
+  // solve epilogue
+  const float* col_scale;   // [N]
+  const float* mu_x;        // [N]
+  float* out_f32;           // [M, N] or null
+  __nv_bfloat16* out_bf16;  // [M, N] or null
+  float* bias_part;         // [M, n_tiles]
+  int32_t out_ld;
   int* err;
   float inv_freq_hi[64];
   float inv_freq_lo[64];

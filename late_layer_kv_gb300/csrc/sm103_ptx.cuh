@@ -174,8 +174,20 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
          (static_cast<uint64_t>(2) << 61);
 }
 
+// Shared-memory matrix descriptor: MN-major, 128-byte swizzle.  Each 128-byte
+// row holds 64 consecutive M (or N) elements of one K index; K rows are 128 B
+// apart, 8-row groups 1024 B apart (stride offset), and successive 64-element
+// M/N blocks `lbo` bytes apart (leading offset).
+__device__ __forceinline__ uint64_t sdesc_mnmajor_sw128(uint32_t saddr, uint32_t lbo) {
+  return static_cast<uint64_t>((saddr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
 // Instruction descriptor of kind::f16: f32 accumulator (bits 4-5 = 1), bf16 A
 // (bits 7-9 = 1) and B (bits 10-12 = 1), both K-major, N>>3 at bit 17, M>>4 at 24.
+// Bits 15 and 16 (set by the caller) make A and B MN-major.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
          (static_cast<uint32_t>(M >> 4) << 24);

@@ -269,7 +269,7 @@ class FitSums:
         f64 = torch.float64
         self.n_layers, self.d_in, self.d_out = n_layers, d_in, d_out
         self.G = torch.zeros((d_in, d_in), dtype=f64, device=device)
-        self.C = torch.zeros((d_in, n_layers * d_out), dtype=f64, device=device)
+        self.C = torch.zeros((n_layers, d_out, d_in), dtype=f64, device=device)
         self.sx = torch.zeros((d_in,), dtype=f64, device=device)
         self.sy = torch.zeros((n_layers, d_out), dtype=f64, device=device)
         self.count = torch.zeros((1,), dtype=f64, device=device)
@@ -297,6 +297,8 @@ def _fit_call(sums: FitSums, flags: int, X=None, Y=None, lam: float = 0.0, A_out
     if workspace is None:
         dev = sums.G.device
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    if workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
     _check(lib.ridgefill_fit(ctypes.byref(args), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)))
 

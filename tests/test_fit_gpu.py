@@ -1,0 +1,126 @@
+"""GPU parity of ridgefill_fit (running sums and closed-form solve) against the f64
+oracle.
+
+Paper: "RidgeFill: Training-Free Late-Layer Cache Fill for Faster Prefill",
+section 2.2 ("The ridge map", "Fitting": running sums one document at a time
+give the all-rows solve, "The penalty").
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from synthetic import WORKLOADS, calibration, fill_inputs, to_f64
+from tests._fill_helpers import compare, new_cache
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from late_layer_kv_gb300 import (FitSums, device_error, ridgefill_fill,  # noqa: E402
+                                 ridgefill_fit_accumulate, ridgefill_fit_solve)
+
+W_REL_FRO = 1e-3  # fitted maps: relative Frobenius error against the f64 solve
+
+
+def _rel(a, b):
+    return np.linalg.norm(np.asarray(a, np.float64) - b) / np.linalg.norm(b)
+
+
+def _gpu_fit(X, Y, lam, batches=(None,)):
+    L, n, d_out = Y.shape
+    d_in = X.shape[1]
+    sums = FitSums(L, d_in, d_out)
+    Xd, Yd = X.cuda(), Y.cuda()
+    bounds = [0] + [b for b in batches if b is not None] + [n]
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        ridgefill_fit_accumulate(sums, Xd[lo:hi].contiguous(), Yd[:, lo:hi].contiguous())
+    A32 = torch.empty((L, d_out, d_in), dtype=torch.float32, device="cuda")
+    A16 = torch.empty((L, d_out, d_in), dtype=torch.bfloat16, device="cuda")
+    b = torch.empty((L, d_out), dtype=torch.float32, device="cuda")
+    alpha = torch.zeros(1, dtype=torch.float64, device="cuda")
+    ridgefill_fit_solve(sums, lam, A_out=A16, A_out_f32=A32, b_out=b, alpha_out=alpha)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    return sums, A32.cpu().double().numpy(), A16, b.cpu().double().numpy(), float(alpha.item())
+
+
+def test_sums_match_oracle_and_split_batches():
+    cal = calibration(d=256, n_layers=3, n=1000, seed=40)
+    X, Y = cal["X"], cal["Y"]
+    sums, *_ = _gpu_fit(X, Y, 1e-3, batches=(600,))
+    n, sx, sy, G, C = oracle.fit_sums(to_f64(X), to_f64(Y))
+    assert float(sums.count.item()) == n
+    np.testing.assert_allclose(sums.sx.cpu().numpy(), sx, rtol=2e-5, atol=2e-5 * np.abs(sx).max())
+    np.testing.assert_allclose(sums.sy.cpu().numpy(), sy, rtol=2e-5, atol=2e-5 * np.abs(sy).max())
+    # f32 sums of up to 600 exact products per batch: relative error ~ sqrt(n) u, n u = 6e-5 at worst
+    assert _rel(sums.G.cpu().numpy(), G) < 2e-5
+    Cg = sums.C.cpu().numpy()                       # [L, d_out, d_in] = Y_l^T X
+    Co = C.reshape(256, 3, 256).transpose(1, 2, 0)  # oracle [d_in, L*d_out] -> [L, d_out, d_in]
+    assert _rel(Cg, Co) < 2e-5
+
+
+@pytest.mark.parametrize("d,L,n,lam", [(256, 3, 1000, 1e-3), (512, 2, 4096, 3e-2)])
+def test_solve_matches_closed_form(d, L, n, lam):
+    cal = calibration(d=d, n_layers=L, n=n, seed=41 + d)
+    X, Y = cal["X"], cal["Y"]
+    _, A32, A16, b, alpha = _gpu_fit(X, Y, lam, batches=(n // 3,))
+    Ao, bo, ao = oracle.ridge_fit(to_f64(X), to_f64(Y), lam)
+    assert abs(alpha - ao) <= 1e-5 * ao
+    for l in range(L):
+        assert _rel(A32[l], Ao[l]) <= W_REL_FRO, f"layer {l}: {_rel(A32[l], Ao[l]):.2e}"
+        assert _rel(b[l], bo[l]) <= W_REL_FRO
+        # the bf16 output is the f32 output rounded
+        np.testing.assert_array_equal(to_f64(A16[l]), to_f64(torch.from_numpy(A32[l]).float()
+                                                            .to(torch.bfloat16)))
+
+
+def test_batch_split_does_not_change_the_fit():
+    cal = calibration(d=256, n_layers=2, n=2048, seed=43)
+    _, A1, _, b1, _ = _gpu_fit(cal["X"], cal["Y"], 1e-3)
+    _, A2, _, b2, _ = _gpu_fit(cal["X"], cal["Y"], 1e-3, batches=(64, 1000, 1999))
+    # the sums differ only by f32 rounding inside each batch; the solve carries ~2^-16 of
+    # each operand (three-term bf16 split), so two batchings agree to ~1e-5
+    assert _rel(A2, A1) < 1e-4 and _rel(b2, b1) < 1e-4
+
+
+def test_noise_free_recovers_generating_map():
+    """Y = X M + c exactly (f64, then rounded to bf16 inputs) with a tiny penalty:
+    the fit returns A = M^T and b = c up to the bf16 rounding of Y."""
+    rng = np.random.default_rng(44)
+    d, n = 256, 4096
+    X = torch.from_numpy((rng.standard_normal((n, d)) * 2).astype(np.float32)).to(torch.bfloat16)
+    M = (np.eye(d) + 0.1 * rng.standard_normal((d, d)) / 16).astype(np.float64)
+    c = rng.standard_normal(d)
+    Y = torch.from_numpy((to_f64(X) @ M + c).astype(np.float32)).to(torch.bfloat16)[None]
+    _, A, _, b, _ = _gpu_fit(X, Y, 1e-9)
+    Ao, bo, _ = oracle.ridge_fit(to_f64(X), to_f64(Y), 1e-9)
+    assert _rel(A[0], Ao[0]) <= W_REL_FRO
+    assert _rel(A[0], M.T) < 5e-3          # bf16 rounding of Y limits the recovery
+    assert np.abs(b[0] - c).max() < 0.05
+
+
+def test_tiny_fit_then_fill_end_to_end():
+    """Config tiny_d256: fit six maps from 4,096 calibration rows, then fill 448 prefix
+    rows with the fitted (bf16) maps; both steps against the oracle."""
+    shape = WORKLOADS["tiny_d256"]
+    cal = calibration(d=shape.d, n_layers=shape.n_layers, n=shape.calib_rows, seed=1000)
+    _, A32, A16, b, _ = _gpu_fit(cal["X"], cal["Y"], shape.lam)
+    Ao, bo, _ = oracle.ridge_fit(to_f64(cal["X"]), to_f64(cal["Y"]), shape.lam)
+    assert _rel(A32, Ao) <= W_REL_FRO
+    inp = fill_inputs(shape, seed=1000)
+    inp["A"] = A16.cpu()
+    inp["b"] = torch.from_numpy(b.astype(np.float32))
+    d = {k: v.cuda() for k, v in inp.items()}
+    Kc, Vc = new_cache(shape.n_layers, shape.n_kv, shape.N, shape.head_dim)
+    ridgefill_fill(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc,
+                   head_dim=shape.head_dim, rope_theta=shape.rope_theta, rms_eps=shape.rms_eps)
+    torch.cuda.synchronize()
+    o = {k: to_f64(v) for k, v in inp.items()}
+    K, V = oracle.fill_attention(o["H"], np.arange(shape.rows), o["A"], o["b"], o["g"], o["Wk"],
+                                 o["Wv"], shape.rms_eps, shape.rope_theta, shape.n_kv,
+                                 shape.head_dim)
+    for l in range(shape.n_layers):
+        compare(to_f64(Kc[l, :, :shape.rows]), K[l], f"K layer {l}")
+        compare(to_f64(Vc[l, :, :shape.rows]), V[l], f"V layer {l}")
