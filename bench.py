@@ -342,7 +342,115 @@ class HybridWorkload:
                     (s.n_attn + s.n_gdn) * s.d * s.d * 2 >> 20)}
 
 
+class FitWorkload:
+    """The ridge fit of every late layer's map from calibration pairs (ridgefill_fit):
+    one accumulate call over all calibration rows, then the solve."""
+
+    metric = "ridge fit: calibration row-layers/s (accumulate + solve of every late map)"
+    unit = "row-layers/s"
+
+    def __init__(self, shape: FillShape, rows: int):
+        self.shape, self.n = shape, rows
+        s = shape
+        L, d = s.n_layers, s.d
+        self.token_layers = rows * L  # calibration row-layers per fit
+        self.stage_names = ["accumulate", "solve"]
+        self.stage_work = {"accumulate": 2.0 * rows * d * (d + L * d),
+                           "solve": 2.0 * L * d * 3 * d * d}
+        self.stage_bound = {"accumulate": "tensor", "solve": "tensor"}
+        self.total_flops = sum(self.stage_work.values())
+
+    def launches_per_step(self):
+        nb = self.shape.d // 64
+        # colsum x2, count, Gram; prep, equilibrate, Cholesky 3 per block, zero, trinv
+        # diag + 2 per block column, inverse product, 2 splits, solve GEMM, offsets
+        return 4 + 2 + (3 * nb - 2) + 1 + 1 + 2 * (nb - 1) + 1 + 2 + 1 + 1
+
+    def setup(self, dev, seed):
+        """Calibration pairs drawn on the device (torch Philox, seeded) in the
+        distributions of the synthetic generators; the maps are generated per layer."""
+        from late_layer_kv_gb300 import FitSums
+        from late_layer_kv_gb300 import ridgefill as rb
+        s, n = self.shape, self.n
+        L, d = s.n_layers, s.d
+        g = torch.Generator(device=dev).manual_seed(seed)
+        sc = torch.exp(torch.randn(d, generator=g, device=dev))
+        X = (torch.randn(n, d, generator=g, device=dev) * sc).to(torch.bfloat16)
+        Y = torch.empty((L, n, d), dtype=torch.bfloat16, device=dev)
+        Xf = X.float()
+        for l in range(L):
+            M = torch.eye(d, device=dev) + 0.1 * torch.randn(d, d, generator=g, device=dev) / d ** 0.5
+            bl = torch.randn(d, generator=g, device=dev)
+            Y[l] = (Xf @ M + bl + 0.05 * torch.randn(n, d, generator=g, device=dev)).to(torch.bfloat16)
+        self.X, self.Y = X, Y
+        self.sums = FitSums(L, d, d, device=dev)
+        self.A = torch.empty((L, d, d), dtype=torch.bfloat16, device=dev)
+        self.b = torch.empty((L, d), dtype=torch.float32, device=dev)
+        a = rb.FitArgs(L, d, d, rb.RF_FIT_SOLVE, 0, s.lam)
+        self.ws = torch.empty(int(rb.load().ridgefill_fit_workspace_size(ctypes_byref(a))),
+                              dtype=torch.uint8, device=dev)
+
+    def n_events(self):
+        return 3
+
+    def step(self, stream, ev=None):
+        from late_layer_kv_gb300 import ridgefill_fit_accumulate, ridgefill_fit_solve
+        for t in (self.sums.G, self.sums.C, self.sums.sx, self.sums.sy, self.sums.count):
+            t.zero_()
+        if ev is not None:
+            ev[0].record(stream)
+        ridgefill_fit_accumulate(self.sums, self.X, self.Y, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        ridgefill_fit_solve(self.sums, self.shape.lam, A_out=self.A, b_out=self.b,
+                            workspace=self.ws, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def stage_ms(self, ev):
+        return {"accumulate": ev[0].elapsed_time(ev[1]), "solve": ev[1].elapsed_time(ev[2])}
+
+    def e2e_buffers(self):
+        self.X_host = self.X.cpu().pin_memory()
+        self.Y_host = self.Y.cpu().pin_memory()
+        self.A_host = torch.empty(self.A.shape, dtype=torch.bfloat16).pin_memory()
+        return (self.X_host.numel() + self.Y_host.numel()) * 2, self.A_host.numel() * 2
+
+    def e2e_step(self, stream):
+        self.X.copy_(self.X_host, non_blocking=True)
+        self.Y.copy_(self.Y_host, non_blocking=True)
+        self.step(stream)
+        self.A_host.copy_(self.A, non_blocking=True)
+
+    def cpu_rate(self, budget_flop):
+        """The f64 oracle fit of one layer on a row sample of the calibration pairs."""
+        import oracle
+        d = self.shape.d
+        n = int(max(256, min(self.n, budget_flop / (4.0 * d * d))))
+        X = to_f64(self.X[:n].cpu())
+        Y = to_f64(self.Y[:1, :n].cpu())
+        t0 = time.perf_counter()
+        oracle.ridge_fit(X, Y, self.shape.lam)
+        dt = time.perf_counter() - t0
+        return n / dt, dt, f"one layer's fit from the first {n} calibration rows (row-layers/s)"
+
+    def config(self):
+        s = self.shape
+        return {"workload": s.name + "_fit", "d": s.d, "late_layers": s.n_layers,
+                "calibration_rows": self.n, "lambda": s.lam,
+                "l2": "inputs larger than L2 (calibration pairs %d MiB)" % (
+                    self.n * s.d * (s.n_layers + 1) * 2 >> 20)}
+
+
+def ctypes_byref(x):
+    import ctypes
+    return ctypes.byref(x)
+
+
 def make_workload(name, args):
+    if args.fit:
+        shape = WORKLOADS[name]
+        return FitWorkload(shape, args.fit_rows or shape.calib_rows)
     shape = WORKLOADS[name]
     if isinstance(shape, GdnShape):
         if args.rows:
@@ -463,7 +571,7 @@ def run_ours(args):
             t = torch.tensor([ems], device=dev)
             torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
             ems = float(t.item())
-        e2e = {"value": wl.token_layers * world / (ems / 1000.0), "unit": "token-layers/s",
+        e2e = {"value": wl.token_layers * world / (ems / 1000.0), "unit": getattr(wl, "unit", "token-layers/s"),
                "ms_per_step": ems, "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
 
     host_link = None
@@ -481,12 +589,12 @@ def run_ours(args):
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r, dt, what = wl.cpu_rate(args.cpu_flop)
-        cpu = {"value": r, "unit": "token-layers/s", "cores": _cores(), "kind": "oracle",
+        cpu = {"value": r, "unit": getattr(wl, "unit", "token-layers/s"), "cores": _cores(), "kind": "oracle",
                "sample": f"{what} ({dt:.1f} s of f64 numpy work)"}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": value, "unit": "token-layers/s", "n_gpus": world,
+            "metric": getattr(wl, "metric", METRIC), "value": value, "unit": getattr(wl, "unit", "token-layers/s"), "n_gpus": world,
             "steps": steps, "warmup": args.warmup, "ms_per_step": ms_step,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic", "config": wl.config(),
@@ -505,6 +613,9 @@ def run_reference(args):
     """The oracle as it stands, on the host cores, for the same metric and workload."""
     world, rank, _ = _dist()
     if rank != 0:
+        return
+    if args.fit:
+        print(json.dumps({"impl": "reference", "unavailable": "the fit line has no reference arm"}))
         return
     wl = make_workload(args.workload, args)
     wl.inp = (gdn_inputs(wl.shape, seed=1001) if isinstance(wl, HybridWorkload)
@@ -546,6 +657,9 @@ def main():
     ap.add_argument("--rows", type=int, default=0, help="override the filled rows (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the late layers (profiling)")
     ap.add_argument("--rows-per-chunk", type=int, default=0)
+    ap.add_argument("--fit", action="store_true",
+                    help="benchmark the ridge fit of the workload's maps instead of the fill")
+    ap.add_argument("--fit-rows", type=int, default=0)
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

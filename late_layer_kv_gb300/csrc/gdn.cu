@@ -12,12 +12,14 @@
 // is, row by row of S (index i over d_v),
 //   S_t[i,:] = alpha_t S_{t-1}[i,:] + c_t[i] k_t^T,
 //   c_t[i]   = beta_t (v_t[i] - alpha_t S_{t-1}[i,:] . k_t),
-// so the d_v rows of S evolve independently.  A CTA owns 32 rows of S of one
-// (layer, head) in registers, four threads per row with 32 columns each.  The
+// so the d_v rows of S evolve independently.  A CTA owns 64 rows of S of one
+// (layer, head) in registers: each thread two rows and 32 columns, taken as
+// every fourth 16-byte chunk so that the four threads of a row read k from
+// distinct shared-memory banks.  The
 // decay is applied lazily: the registers hold S / g, g being the product of
 // the gates since the last renormalisation, so a prompt row costs one FMA per
 // element for the dot product and one for the update.  k, v and the gates are
-// staged through shared memory 32 prompt rows at a time with cp.async,
+// staged through shared memory 16 prompt rows at a time with cp.async,
 // double buffered.
 #include <cmath>
 #include <mutex>
@@ -28,9 +30,9 @@
 namespace rf {
 namespace {
 
-constexpr int kSRows = 32;     // rows of S (d_v) per CTA
+constexpr int kSRows = 64;      // rows of S (d_v) per CTA, two per thread
 constexpr int kGdnThreads = 128;
-constexpr int kStageRows = 32;  // prompt rows per staging buffer
+constexpr int kStageRows = 16;  // prompt rows per staging buffer
 constexpr int kDk = 128;
 constexpr float kRenorm = 1e-20f;
 
@@ -53,9 +55,9 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStatePa
 
   const int slice = blockIdx.x, h = blockIdx.y, l = blockIdx.z;
   const int tid = threadIdx.x;
-  const int r = tid >> 2;     // S row inside the slice
-  const int part = tid & 3;   // 32-column part of d_k
-  const int i = slice * kSRows + r;
+  const int rp = tid >> 2;    // this thread owns S rows rp and rp + 32 of the slice
+  const int part = tid & 3;   // and the 16-byte column chunks part, part + 4, ..., part + 28
+  const int i0 = slice * kSRows + rp;
   const int H = p.heads;
   const size_t ra = static_cast<size_t>(p.rows_alloc);
   const int dv = p.dv;
@@ -64,26 +66,21 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStatePa
   const float* vbase = p.v + (static_cast<size_t>(l) * H + h) * ra * dv + slice * kSRows;
   const float* abase = p.gate + (static_cast<size_t>(l) * 2 * H + h) * ra;
   const float* bbase = p.gate + (static_cast<size_t>(l) * 2 * H + H + h) * ra;
-  const size_t s_off = ((static_cast<size_t>(l) * H + h) * dv + i) * kDk + part * 32;
+  const size_t row0 = ((static_cast<size_t>(l) * H + h) * dv + i0) * kDk;
+  const size_t row1 = row0 + static_cast<size_t>(32) * kDk;
 
-  float S[32];
-  if (p.first) {
-    if (p.S0 != nullptr) {
+  // S0 and S1 hold columns 4 (part + 4 q) + e at index 4 q + e
+  float S0[32], S1[32];
+  const float* src = p.first ? p.S0 : p.S;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(p.S0 + s_off + j);
-        S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-      }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 32; ++j) S[j] = 0.f;
+  for (int q = 0; q < 8; ++q) {
+    float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
+    if (src != nullptr) {
+      x0 = *reinterpret_cast<const float4*>(src + row0 + 4 * (part + 4 * q));
+      x1 = *reinterpret_cast<const float4*>(src + row1 + 4 * (part + 4 * q));
     }
-  } else {
-#pragma unroll
-    for (int j = 0; j < 32; j += 4) {
-      const float4 x = *reinterpret_cast<const float4*>(p.S + s_off + j);
-      S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
-    }
+    S0[4 * q] = x0.x; S0[4 * q + 1] = x0.y; S0[4 * q + 2] = x0.z; S0[4 * q + 3] = x0.w;
+    S1[4 * q] = x1.x; S1[4 * q + 1] = x1.y; S1[4 * q + 2] = x1.z; S1[4 * q + 3] = x1.w;
   }
   float g = 1.f;
 
@@ -121,43 +118,57 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStatePa
     for (int tt = 0; tt < n; ++tt) {
       const float a = expf(sg[buf][0][tt]);
       const float bt = sg[buf][1][tt];
-      const float vi = sv[buf][tt][r];
+      const float v0 = sv[buf][tt][rp], v1 = sv[buf][tt][rp + 32];
       float kk[32];
-      const float4* k4 = reinterpret_cast<const float4*>(&sk[buf][tt][part * 32]);
+      const float4* k4 = reinterpret_cast<const float4*>(&sk[buf][tt][0]);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float4 x = k4[j];
-        kk[4 * j] = x.x; kk[4 * j + 1] = x.y; kk[4 * j + 2] = x.z; kk[4 * j + 3] = x.w;
+      for (int q = 0; q < 8; ++q) {
+        const float4 x = k4[part + 4 * q];
+        kk[4 * q] = x.x; kk[4 * q + 1] = x.y; kk[4 * q + 2] = x.z; kk[4 * q + 3] = x.w;
       }
-      float d0 = 0.f, d1 = 0.f;
+      float e0a = 0.f, e0b = 0.f, e1a = 0.f, e1b = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; j += 2) {
-        d0 = fmaf(S[j], kk[j], d0);
-        d1 = fmaf(S[j + 1], kk[j + 1], d1);
+        e0a = fmaf(S0[j], kk[j], e0a);
+        e0b = fmaf(S0[j + 1], kk[j + 1], e0b);
+        e1a = fmaf(S1[j], kk[j], e1a);
+        e1b = fmaf(S1[j + 1], kk[j + 1], e1b);
       }
-      float dot = d0 + d1;
-      dot += __shfl_xor_sync(0xffffffffu, dot, 1);
-      dot += __shfl_xor_sync(0xffffffffu, dot, 2);
-      // true S_{t-1} k_t = g * dot
-      const float c = bt * (vi - a * (g * dot));
-      const float gn = g * a;
-      if (gn >= kRenorm) {
-        const float s = c / gn;
+      float e0 = e0a + e0b, e1 = e1a + e1b;
+      e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
+      e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
+      e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
+      e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
+      // true S_{t-1}[i,:] k_t = g * e
+      const float ag = a * g;
+      const float c0 = bt * (v0 - ag * e0);
+      const float c1 = bt * (v1 - ag * e1);
+      if (ag >= kRenorm) {
+        const float inv = 1.f / ag;
+        const float s0 = c0 * inv, s1 = c1 * inv;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[j] = fmaf(s, kk[j], S[j]);
-        g = gn;
+        for (int j = 0; j < 32; ++j) {
+          S0[j] = fmaf(s0, kk[j], S0[j]);
+          S1[j] = fmaf(s1, kk[j], S1[j]);
+        }
+        g = ag;
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) S[j] = fmaf(c, kk[j], gn * S[j]);
+        for (int j = 0; j < 32; ++j) {
+          S0[j] = fmaf(c0, kk[j], ag * S0[j]);
+          S1[j] = fmaf(c1, kk[j], ag * S1[j]);
+        }
         g = 1.f;
       }
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int j = 0; j < 32; j += 4) {
-    float4 x = make_float4(g * S[j], g * S[j + 1], g * S[j + 2], g * S[j + 3]);
-    *reinterpret_cast<float4*>(p.S + s_off + j) = x;
+  for (int q = 0; q < 8; ++q) {
+    *reinterpret_cast<float4*>(p.S + row0 + 4 * (part + 4 * q)) =
+        make_float4(g * S0[4 * q], g * S0[4 * q + 1], g * S0[4 * q + 2], g * S0[4 * q + 3]);
+    *reinterpret_cast<float4*>(p.S + row1 + 4 * (part + 4 * q)) =
+        make_float4(g * S1[4 * q], g * S1[4 * q + 1], g * S1[4 * q + 2], g * S1[4 * q + 3]);
   }
 }
 
