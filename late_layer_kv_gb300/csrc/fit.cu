@@ -29,31 +29,52 @@ namespace {
 constexpr int kNB = 64;  // Cholesky / triangular-inverse block
 
 // ------------------------------------------------------------ column sums
-// out[c] += sum over rows of in[r, c] for a [rows, width] bf16 array, one
-// thread per column pair; f32 over blocks of 256 rows, then f64.
-__global__ void colsum_kernel(const __nv_bfloat16* in, int64_t rows, int width, int batches,
-                              int64_t batch_stride, double* out) {
-  const int pairs = width / 2;
+// Partial column sums of a [batches][rows, width] bf16 array over row slabs:
+// part[slab][col_base + b*width + c] = sum of rows in the slab (f32 over 64-row
+// runs, then f64), eight columns per thread so each load is 16 bytes.
+__global__ void colsum_partial_kernel(const __nv_bfloat16* in, int64_t rows, int width,
+                                      int batches, int64_t batch_stride, int64_t slab_rows,
+                                      double* part, int64_t part_ld, int64_t col_base) {
+  const int oct = width / 8;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= static_cast<int64_t>(pairs) * batches) return;
-  const int b = static_cast<int>(t / pairs);
-  const int c = static_cast<int>(t % pairs) * 2;
+  if (t >= static_cast<int64_t>(oct) * batches) return;
+  const int b = static_cast<int>(t / oct);
+  const int c = static_cast<int>(t % oct) * 8;
+  const int64_t r_lo = static_cast<int64_t>(blockIdx.y) * slab_rows;
+  const int64_t r_hi = r_lo + slab_rows < rows ? r_lo + slab_rows : rows;
   const __nv_bfloat16* p = in + b * batch_stride + c;
-  double a0 = 0.0, a1 = 0.0;
-  for (int64_t r0 = 0; r0 < rows; r0 += 256) {
-    const int64_t r1 = r0 + 256 < rows ? r0 + 256 : rows;
-    float f0 = 0.f, f1 = 0.f;
+  double acc[8] = {};
+  for (int64_t r0 = r_lo; r0 < r_hi; r0 += 64) {
+    const int64_t r1 = r0 + 64 < r_hi ? r0 + 64 : r_hi;
+    float f[8] = {};
+#pragma unroll 4
     for (int64_t r = r0; r < r1; ++r) {
-      const float2 v =
-          __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p + r * width));
-      f0 += v.x;
-      f1 += v.y;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(p + r * width));
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+        f[2 * e] += x.x;
+        f[2 * e + 1] += x.y;
+      }
     }
-    a0 += f0;
-    a1 += f1;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] += f[e];
   }
-  out[static_cast<int64_t>(b) * width + c] += a0;
-  out[static_cast<int64_t>(b) * width + c + 1] += a1;
+  double* dst = part + blockIdx.y * part_ld + col_base + static_cast<int64_t>(b) * width + c;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) dst[e] = acc[e];
+}
+
+// out_x[c] += sum over slabs (c < nx), out_y[c - nx] += ... (fixed order).
+__global__ void colsum_reduce_kernel(const double* part, int slabs, int64_t part_ld, int64_t nx,
+                                     double* out_x, double* out_y) {
+  const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (c >= part_ld) return;
+  double s = 0.0;
+  for (int k = 0; k < slabs; ++k) s += part[k * part_ld + c];
+  if (c < nx) out_x[c] += s;
+  else out_y[c - nx] += s;
 }
 
 __global__ void add_count_kernel(double* count, double rows) { *count += rows; }
@@ -283,17 +304,28 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
-// B' [d, 3d] = [hi(G^-1) | lo(G^-1) | hi(G^-1)]
-__global__ void split_ginv_kernel(const float* Gi, int d, __nv_bfloat16* Bp) {
+// B' [d, 3d] = [hi(G^-1) | lo(G^-1) | hi(G^-1)] from the f64 inverse
+__global__ void split_ginv_kernel(const double* Gi, int d, __nv_bfloat16* Bp) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= static_cast<int64_t>(d) * d) return;
   const int64_t i = t / d, k = t % d;
-  __nv_bfloat16 hi, lo;
-  split_bf16(Gi[t], hi, lo);
+  const double v = Gi[t];
+  const __nv_bfloat16 hi = __float2bfloat16_rn(static_cast<float>(v));
+  const __nv_bfloat16 lo = __float2bfloat16_rn(static_cast<float>(v - static_cast<double>(__bfloat162float(hi))));
   __nv_bfloat16* row = Bp + i * 3 * d;
   row[k] = hi;
   row[d + k] = lo;
   row[2 * d + k] = hi;
+}
+
+// X = L^-1 (f32, lower) split into bf16 hi and lo parts
+__global__ void split2_kernel(const float* X, int64_t n, __nv_bfloat16* hi, __nv_bfloat16* lo) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n) return;
+  __nv_bfloat16 h, l;
+  split_bf16(X[t], h, l);
+  hi[t] = h;
+  lo[t] = l;
 }
 
 // A' [L*d_out, 3d] = [hi(c) | hi(c) | lo(c)],  c[o, k] = s_k (C[o, k] - n mu_y[o] mu_x[k])
@@ -326,8 +358,11 @@ __global__ void bias_kernel(const double* sy, const double* count, const float* 
 // ------------------------------------------------------------ plan
 struct FitPlan {
   size_t off_gh = 0, off_s = 0, off_mu32 = 0, off_mu64 = 0, off_alpha = 0, off_T = 0,
-         off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0, total = 0;
+         off_xhi = 0, off_xlo = 0, off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0,
+         off_cs = 0, total = 0;
   int bn = 0;
+  int slabs = 0;
+  int64_t slab_rows = 0;
 };
 
 rf_status validate_fit(const rf_fit_args* a) {
@@ -349,6 +384,12 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
   const size_t d = a->d_in, M = static_cast<size_t>(a->n_layers) * a->d_out;
   pl->bn = (a->d_in % 256 == 0) ? 256 : 128;
   size_t off = 0;
+  if (a->flags & RF_FIT_ACCUMULATE) {
+    const int64_t rows = a->rows > 0 ? a->rows : 1;
+    pl->slab_rows = ceil_div(ceil_div(rows, 64), 64) * 64;  // at most 64 slabs, 64-row runs
+    pl->slabs = static_cast<int>(ceil_div(rows, pl->slab_rows));
+    pl->off_cs = off;    off = align_up(off + static_cast<size_t>(pl->slabs) * (d + M) * 8, 256);
+  }
   if (a->flags & RF_FIT_SOLVE) {
     pl->off_gh = off;    off = align_up(off + d * d * 4, 256);
     pl->off_s = off;     off = align_up(off + d * 4, 256);
@@ -356,7 +397,9 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->off_mu64 = off;  off = align_up(off + d * 8, 256);
     pl->off_alpha = off; off = align_up(off + 8, 256);
     pl->off_T = off;     off = align_up(off + d * kNB * 4, 256);
-    pl->off_gi = off;    off = align_up(off + d * d * 4, 256);
+    pl->off_xhi = off;   off = align_up(off + d * d * 2, 256);
+    pl->off_xlo = off;   off = align_up(off + d * d * 2, 256);
+    pl->off_gi = off;    off = align_up(off + d * d * 8, 256);
     pl->off_bp = off;    off = align_up(off + d * 3 * d * 2, 256);
     pl->off_ap = off;    off = align_up(off + M * 3 * d * 2, 256);
     pl->off_part = off;  off = align_up(off + M * (d / pl->bn) * 4, 256);
@@ -364,43 +407,34 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
   pl->total = off;
 }
 
-rf_status accumulate(const rf_fit_args* a, const FitPlan& pl, cudaStream_t s) {
-  const int64_t rows = a->rows;
-  if (rows == 0) return RF_OK;
-  const int L = a->n_layers, din = a->d_in, dout = a->d_out;
-  // column sums
-  {
-    const int64_t th = din / 2;
-    colsum_kernel<<<static_cast<unsigned>((th + 255) / 256), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a->X), rows, din, 1, 0, a->sx);
-    const int64_t ty = static_cast<int64_t>(dout / 2) * L;
-    colsum_kernel<<<static_cast<unsigned>((ty + 255) / 256), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(a->Y), rows, dout, L, rows * dout, a->sy);
-    add_count_kernel<<<1, 1, 0, s>>>(a->count, static_cast<double>(rows));
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
-  }
+// Gram-mode tcgen05 GEMM: out_G[m, n] += sum_k Xa[k, m] Xb[k, n] for the d-wide
+// arrays Xa, Xb ([rows, d], MN-major), and, if Y is given, out_C[l, o, n] +=
+// sum_k Y[l, k, o] Xb[k, n].
+rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int64_t rows, int d,
+                      int dout, int bn, double* out_G, double* out_C, cudaStream_t s) {
   GemmParams p{};
   p.mode = kModeGram;
   p.k_blocks = static_cast<int32_t>(ceil_div(rows, kBK));
-  const uint64_t xrow = static_cast<uint64_t>(din) * 2, yrow = static_cast<uint64_t>(dout) * 2;
-  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->X, din, rows, 1, xrow, 0,
-                         64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_tmap_3d(&p.tmA2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Y, dout, rows, L, yrow,
-                          yrow * rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
-  p.tmB[0] = p.tmA;
+  const uint64_t xrow = static_cast<uint64_t>(d) * 2, yrow = static_cast<uint64_t>(dout) * 2;
+  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xa, d, rows, 1, xrow, 0, 64, 64,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xb, d, rows, 1, xrow, 0, 64,
+                          64, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (Y != nullptr)
+    ok = ok && make_tmap_3d(&p.tmA2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, dout, rows, L, yrow,
+                            yrow * rows, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the Gram GEMM");
-  p.gram_x_tiles = din / kBM;
+  p.gram_x_tiles = d / kBM;
   p.gram_y_tiles_per_layer = dout / kBM;
-  p.m_tiles = p.gram_x_tiles + L * p.gram_y_tiles_per_layer;
-  p.bn = pl.bn;
-  p.n_tiles = din / pl.bn;
+  p.m_tiles = p.gram_x_tiles + (Y != nullptr ? L * p.gram_y_tiles_per_layer : 0);
+  p.bn = bn;
+  p.n_tiles = d / bn;
   p.batches = 1;
   p.group_m = 16;
   p.d_out = dout;
-  p.gram_G = a->G;
-  p.gram_C = a->C;
-  p.gram_ld = din;
+  p.gram_G = out_G;
+  p.gram_C = out_C;
+  p.gram_ld = d;
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
   const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -408,6 +442,27 @@ rf_status accumulate(const rf_fit_args* a, const FitPlan& pl, cudaStream_t s) {
   cudaError_t e = launch_gemm(p, grid, s);
   if (e != cudaSuccess) return cuda_fail(e, "Gram GEMM launch");
   return RF_OK;
+}
+
+rf_status accumulate(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream_t s) {
+  const int64_t rows = a->rows;
+  if (rows == 0) return RF_OK;
+  const int L = a->n_layers, din = a->d_in, dout = a->d_out;
+  // column sums: slab partials, then a fixed-order reduction into the f64 sums
+  double* cs = reinterpret_cast<double*>(ws + pl.off_cs);
+  const int64_t ld = din + static_cast<int64_t>(L) * dout;
+  const int64_t tx = din / 8, ty = static_cast<int64_t>(dout / 8) * L;
+  colsum_partial_kernel<<<dim3(static_cast<unsigned>((tx + 127) / 128), pl.slabs), 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a->X), rows, din, 1, 0, pl.slab_rows, cs, ld, 0);
+  colsum_partial_kernel<<<dim3(static_cast<unsigned>((ty + 127) / 128), pl.slabs), 128, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a->Y), rows, dout, L, rows * dout, pl.slab_rows, cs, ld,
+      din);
+  colsum_reduce_kernel<<<static_cast<unsigned>((ld + 255) / 256), 256, 0, s>>>(cs, pl.slabs, ld,
+                                                                               din, a->sx, a->sy);
+  add_count_kernel<<<1, 1, 0, s>>>(a->count, static_cast<double>(rows));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
+  return launch_gram(a->X, a->X, a->Y, L, rows, din, dout, pl.bn, a->G, a->C, s);
 }
 
 rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream_t s) {
@@ -419,7 +474,9 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   double* mu64 = reinterpret_cast<double*>(ws + pl.off_mu64);
   double* alpha = reinterpret_cast<double*>(ws + pl.off_alpha);
   float* T = reinterpret_cast<float*>(ws + pl.off_T);
-  float* Gi = reinterpret_cast<float*>(ws + pl.off_gi);
+  double* Gi = reinterpret_cast<double*>(ws + pl.off_gi);
+  __nv_bfloat16* Xhi = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xhi);
+  __nv_bfloat16* Xlo = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xlo);
   __nv_bfloat16* Bp = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_bp);
   __nv_bfloat16* Ap = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_ap);
   float* part = reinterpret_cast<float*>(ws + pl.off_part);
@@ -460,9 +517,15 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
     SgemmArgs g2{rem, kNB, rem, -1.f, 0.f, xsub, d, T, kNB, col, d, 0, 0, 1};     // X_sub,j = -X_sub T
     if ((e = sgemm(false, false, g2, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
   }
-  // G^-1 = X^T X
-  SgemmArgs gi{d, d, d, 1.f, 0.f, Gh, d, Gh, d, Gi, d, 0, 1, 0};
-  if ((e = sgemm(true, false, gi, s)) != cudaSuccess) return cuda_fail(e, "inverse product");
+  // G^-1 = X^T X on the tensor cores: three MN-major Gram products of the bf16
+  // split of X (hi hi + hi lo + lo hi), summed in f64
+  split2_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gh, dd, Xhi, Xlo);
+  if ((e = cudaMemsetAsync(Gi, 0, static_cast<size_t>(dd) * 8, s)) != cudaSuccess)
+    return cuda_fail(e, "clearing the inverse");
+  rf_status st;
+  if ((st = launch_gram(Xhi, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
+  if ((st = launch_gram(Xhi, Xlo, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
+  if ((st = launch_gram(Xlo, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
 
   split_ginv_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gi, d, Bp);
   split_rhs_kernel<<<static_cast<unsigned>((M * d + 255) / 256), 256, 0, s>>>(
@@ -529,11 +592,11 @@ extern "C" rf_status ridgefill_fit(const rf_fit_args* a, void* workspace, size_t
     if (q != nullptr && !aligned16(q)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
   FitPlan pl;
   plan_fit(a, &pl);
-  if ((a->flags & RF_FIT_SOLVE) && (workspace == nullptr || ws_bytes < pl.total))
+  if (pl.total > 0 && (workspace == nullptr || ws_bytes < pl.total))
     return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes", pl.total);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (a->flags & RF_FIT_ACCUMULATE) {
-    if ((st = accumulate(a, pl, s)) != RF_OK) return st;
+    if ((st = accumulate(a, pl, static_cast<uint8_t*>(workspace), s)) != RF_OK) return st;
   }
   if (a->flags & RF_FIT_SOLVE) {
     if ((st = solve(a, pl, static_cast<uint8_t*>(workspace), s)) != RF_OK) return st;
