@@ -12,7 +12,7 @@
 //              stores bf16 straight into the [layer, kv_head, pos, head_dim] cache.
 //   gdn mode : per GDN layer, X_hat_l times [Wk; Wv; Wa|Wb]; the epilogue applies
 //              the RMS scale, L2-normalises k per head, and writes f32 k, v and
-//              the gates (log alpha, beta) for the state kernel.
+//              the gates (alpha, beta) for the state kernel.
 //
 // Roles (256 threads, one CTA per SM): warp 0 issues TMA loads into a
 // kStages-deep ring, warp 1 issues tcgen05.mma (M=128, N=bn, K=16) into one of
@@ -289,9 +289,8 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, int q, int lane
           if (c < 2 * H) {
             const float z = f32(a[j]) * rs;
             const bool is_a = c < H;
-            // log sigmoid(z) for alpha, sigmoid(z) for beta
-            const float val = is_a ? fminf(z, 0.f) - log1pf(expf(-fabsf(z)))
-                                   : 1.f / (1.f + expf(-z));
+            // sigmoid(z): alpha for the first H columns, beta for the next H
+            const float val = 1.f / (1.f + expf(-z));
             const int which = is_a ? 0 : 1;
             const int h = is_a ? c : c - H;
             p.gdn_gate[((static_cast<size_t>(l) * 2 + which) * H + h) * ra + row] = val;

@@ -4,7 +4,7 @@
 // predicted input).
 //
 // Per row chunk: the grouped map GEMM (X_hat for every GDN layer), the GDN
-// projection GEMM (RMS scale, L2-normalised k per head, v, log alpha, beta),
+// projection GEMM (RMS scale, L2-normalised k per head, v, alpha, beta),
 // then the state kernel, which carries S over the chunk's rows in order.
 //
 // State kernel.  For one head the recurrence
@@ -19,8 +19,8 @@
 // decay is applied lazily: the registers hold S / g, g being the product of
 // the gates since the last renormalisation, so a prompt row costs one FMA per
 // element for the dot product and one for the update.  k, v and the gates are
-// staged through shared memory 16 prompt rows at a time with cp.async,
-// double buffered.
+// staged through shared memory 16 prompt rows at a time with cp.async in a
+// four-deep ring, so the loads run three stages ahead of the arithmetic.
 #include <cmath>
 #include <mutex>
 
@@ -33,7 +33,9 @@ namespace {
 constexpr int kSRows = 64;      // rows of S (d_v) per CTA, two per thread
 constexpr int kGdnThreads = 128;
 constexpr int kStageRows = 16;  // prompt rows per staging buffer
+constexpr int kBufs = 4;        // staging ring depth (loads run kBufs - 1 stages ahead)
 constexpr int kDk = 128;
+constexpr int kStateSmem = kBufs * (kStageRows * (kDk + kSRows) + 2 * kStageRows) * 4;
 constexpr float kRenorm = 1e-20f;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
@@ -48,10 +50,24 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// d = a * b + c on two float lanes at once (one issued instruction)
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+
 __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStateParams p) {
-  __shared__ __align__(16) float sk[2][kStageRows][kDk];
-  __shared__ __align__(16) float sv[2][kStageRows][kSRows];
-  __shared__ __align__(16) float sg[2][2][kStageRows];
+  extern __shared__ __align__(16) float smem_f[];
+  float (*sk)[kStageRows][kDk] = reinterpret_cast<float (*)[kStageRows][kDk]>(smem_f);
+  float (*sv)[kStageRows][kSRows] =
+      reinterpret_cast<float (*)[kStageRows][kSRows]>(smem_f + kBufs * kStageRows * kDk);
+  float (*sg)[2][kStageRows] = reinterpret_cast<float (*)[2][kStageRows]>(
+      smem_f + kBufs * kStageRows * (kDk + kSRows));
 
   const int slice = blockIdx.x, h = blockIdx.y, l = blockIdx.z;
   const int tid = threadIdx.x;
@@ -69,8 +85,8 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStatePa
   const size_t row0 = ((static_cast<size_t>(l) * H + h) * dv + i0) * kDk;
   const size_t row1 = row0 + static_cast<size_t>(32) * kDk;
 
-  // S0 and S1 hold columns 4 (part + 4 q) + e at index 4 q + e
-  float S0[32], S1[32];
+  // S0, S1 hold columns 4 (part + 4 q) + e at pair 2 q + e / 2
+  float2 S0[16], S1[16];
   const float* src = p.first ? p.S0 : p.S;
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
@@ -79,8 +95,8 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStatePa
       x0 = *reinterpret_cast<const float4*>(src + row0 + 4 * (part + 4 * q));
       x1 = *reinterpret_cast<const float4*>(src + row1 + 4 * (part + 4 * q));
     }
-    S0[4 * q] = x0.x; S0[4 * q + 1] = x0.y; S0[4 * q + 2] = x0.z; S0[4 * q + 3] = x0.w;
-    S1[4 * q] = x1.x; S1[4 * q + 1] = x1.y; S1[4 * q + 2] = x1.z; S1[4 * q + 3] = x1.w;
+    S0[2 * q] = make_float2(x0.x, x0.y); S0[2 * q + 1] = make_float2(x0.z, x0.w);
+    S1[2 * q] = make_float2(x1.x, x1.y); S1[2 * q + 1] = make_float2(x1.z, x1.w);
   }
   float g = 1.f;
 
@@ -104,37 +120,41 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStatePa
     cp_async_commit();
   };
 
-  if (nst > 0) load(0, 0);
+  // one cp.async group per stage (empty past the end) keeps the group count uniform
+  for (int q = 0; q < kBufs - 1; ++q) {
+    if (q < nst) load(q, q);
+    else cp_async_commit();
+  }
   for (int st = 0; st < nst; ++st) {
-    const int buf = st & 1;
-    if (st + 1 < nst) {
-      load(st + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int buf = st % kBufs;
+    const int ahead = st + kBufs - 1;
+    if (ahead < nst) load(ahead, ahead % kBufs);
+    else cp_async_commit();
+    cp_async_wait<kBufs - 1>();
     __syncthreads();
     const int n = min(kStageRows, p.rows - st * kStageRows);
     for (int tt = 0; tt < n; ++tt) {
-      const float a = expf(sg[buf][0][tt]);
+      const float a = sg[buf][0][tt];
       const float bt = sg[buf][1][tt];
       const float v0 = sv[buf][tt][rp], v1 = sv[buf][tt][rp + 32];
-      float kk[32];
+      float2 kk[16];
       const float4* k4 = reinterpret_cast<const float4*>(&sk[buf][tt][0]);
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const float4 x = k4[part + 4 * q];
-        kk[4 * q] = x.x; kk[4 * q + 1] = x.y; kk[4 * q + 2] = x.z; kk[4 * q + 3] = x.w;
+        kk[2 * q] = make_float2(x.x, x.y);
+        kk[2 * q + 1] = make_float2(x.z, x.w);
       }
-      float e0a = 0.f, e0b = 0.f, e1a = 0.f, e1b = 0.f;
+      float2 e0a = make_float2(0.f, 0.f), e0b = e0a, e1a = e0a, e1b = e0a;
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) {
-        e0a = fmaf(S0[j], kk[j], e0a);
-        e0b = fmaf(S0[j + 1], kk[j + 1], e0b);
-        e1a = fmaf(S1[j], kk[j], e1a);
-        e1b = fmaf(S1[j + 1], kk[j + 1], e1b);
+      for (int j = 0; j < 16; j += 2) {
+        e0a = ffma2(S0[j], kk[j], e0a);
+        e0b = ffma2(S0[j + 1], kk[j + 1], e0b);
+        e1a = ffma2(S1[j], kk[j], e1a);
+        e1b = ffma2(S1[j + 1], kk[j + 1], e1b);
       }
-      float e0 = e0a + e0b, e1 = e1a + e1b;
+      float e0 = (e0a.x + e0a.y) + (e0b.x + e0b.y);
+      float e1 = (e1a.x + e1a.y) + (e1b.x + e1b.y);
       e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
       e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
       e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
@@ -145,18 +165,18 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStatePa
       const float c1 = bt * (v1 - ag * e1);
       if (ag >= kRenorm) {
         const float inv = 1.f / ag;
-        const float s0 = c0 * inv, s1 = c1 * inv;
+        const float2 s0 = make_float2(c0 * inv, c0 * inv), s1 = make_float2(c1 * inv, c1 * inv);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          S0[j] = fmaf(s0, kk[j], S0[j]);
-          S1[j] = fmaf(s1, kk[j], S1[j]);
+        for (int j = 0; j < 16; ++j) {
+          S0[j] = ffma2(s0, kk[j], S0[j]);
+          S1[j] = ffma2(s1, kk[j], S1[j]);
         }
         g = ag;
       } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          S0[j] = fmaf(c0, kk[j], ag * S0[j]);
-          S1[j] = fmaf(c1, kk[j], ag * S1[j]);
+        for (int j = 0; j < 16; ++j) {
+          S0[j] = make_float2(fmaf(c0, kk[j].x, ag * S0[j].x), fmaf(c0, kk[j].y, ag * S0[j].y));
+          S1[j] = make_float2(fmaf(c1, kk[j].x, ag * S1[j].x), fmaf(c1, kk[j].y, ag * S1[j].y));
         }
         g = 1.f;
       }
@@ -166,9 +186,9 @@ __global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStatePa
 #pragma unroll
   for (int q = 0; q < 8; ++q) {
     *reinterpret_cast<float4*>(p.S + row0 + 4 * (part + 4 * q)) =
-        make_float4(g * S0[4 * q], g * S0[4 * q + 1], g * S0[4 * q + 2], g * S0[4 * q + 3]);
+        make_float4(g * S0[2 * q].x, g * S0[2 * q].y, g * S0[2 * q + 1].x, g * S0[2 * q + 1].y);
     *reinterpret_cast<float4*>(p.S + row1 + 4 * (part + 4 * q)) =
-        make_float4(g * S1[4 * q], g * S1[4 * q + 1], g * S1[4 * q + 2], g * S1[4 * q + 3]);
+        make_float4(g * S1[2 * q].x, g * S1[2 * q].y, g * S1[2 * q + 1].x, g * S1[2 * q + 1].y);
   }
 }
 
@@ -267,8 +287,15 @@ std::mutex g_gdn_host_map_mu;
 }  // namespace
 
 cudaError_t launch_gdn_state(const GdnStateParams& p, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(gdn_state_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
   dim3 grid(p.dv / kSRows, p.heads, p.layers);
-  gdn_state_kernel<<<grid, kGdnThreads, 0, stream>>>(p);
+  gdn_state_kernel<<<grid, kGdnThreads, kStateSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -69,7 +69,7 @@ struct GemmParams {
   // GDN projection epilogue
   float* gdn_k;        // [L, H, rows_alloc, dk] f32
   float* gdn_v;        // [L, H, rows_alloc, dv] f32
-  float* gdn_gate;     // [L, 2, H, rows_alloc] f32 (log alpha, beta)
+  float* gdn_gate;     // [L, 2, H, rows_alloc] f32 (alpha, beta)
   int32_t gdn_heads;
   int32_t gdn_rows_alloc;
   int32_t n_v_tiles;
@@ -98,7 +98,7 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 struct GdnStateParams {
   const float* k;      // [L, H, rows_alloc, dk]
   const float* v;      // [L, H, rows_alloc, dv]
-  const float* gate;   // [L, 2, H, rows_alloc]: log alpha, then beta
+  const float* gate;   // [L, 2, H, rows_alloc]: alpha, then beta
   const float* S0;     // [L, H, dv, dk] or null
   float* S;            // [L, H, dv, dk]
   int32_t layers;
