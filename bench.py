@@ -179,7 +179,7 @@ class AttnWorkload:
         self.H_dev = self.d["H"]
 
     def n_events(self):
-        return 3
+        return 3 + (2 * self.shape.n_layers if self.host_maps else 0)
 
     def step(self, stream, ev=None):
         from late_layer_kv_gb300 import ridgefill_fill
@@ -187,7 +187,12 @@ class AttnWorkload:
         ridgefill_fill(self.H_dev, self.A, d["b"], d["g"], d["Wk"], d["Wv"], self.Kc, self.Vc,
                        head_dim=s.head_dim, rope_theta=s.rope_theta, rms_eps=s.rms_eps,
                        rows_per_chunk=self.rpc, workspace=self.ws, stream=stream,
-                       stage_events=ev)
+                       stage_events=None if ev is None else ev[:3],
+                       copy_events=None if (ev is None or not self.host_maps) else ev[3:])
+
+    def copy_ms(self, ev):
+        """Durations of the first chunk's per-layer map copies (host maps only)."""
+        return [ev[3 + 2 * l].elapsed_time(ev[4 + 2 * l]) for l in range(self.shape.n_layers)]
 
     def stage_ms(self, ev):
         return {"map_gemm": ev[0].elapsed_time(ev[1]), "kv_gemm": ev[1].elapsed_time(ev[2])}
@@ -468,6 +473,15 @@ def make_workload(name, args):
 
 # ----------------------------------------------------------------------------- arms
 
+def _copy_ms(dst, src):
+    e0, e1 = _events(2)
+    e0.record()
+    dst.copy_(src, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
 def h2d_rate_gbs(dev, nbytes=32 << 20, reps=20):
     """Best-of pinned host -> device copy rate (GB/s)."""
     src = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
@@ -580,10 +594,19 @@ def run_ours(args):
         link = h2d_rate_gbs(dev)
         map_bytes = s.n_layers * s.d * s.d * 2
         mstage = stages["map_gemm"]["ms"]
-        host_link = {"h2d_gbs_measured": link, "map_bytes_per_step": map_bytes,
+        cms = [t for e in ev for t in wl.copy_ms(e)]
+        copy_gbs = (map_bytes / s.n_layers) / (float(np.mean(cms)) / 1000.0) / 1e9
+        one = wl.A[0].view(-1)  # the maps' own pinned buffer, alone on the link
+        tmp = torch.empty_like(one, device=dev)
+        maps_buf = max(one.numel() * 2 / (t / 1000.0) / 1e9 for t in
+                       [_copy_ms(tmp, one) for _ in range(10)])
+        host_link = {"h2d_gbs_measured": link, "maps_buffer_h2d_gbs": maps_buf,
+                     "map_bytes_per_step": map_bytes,
+                     "copy_gbs": copy_gbs, "copy_frac_of_link": copy_gbs / link,
                      "map_stage_gbs": map_bytes / (mstage / 1000.0) / 1e9,
                      "note": "maps copied per layer on a side stream while the previous layer "
-                             "computes; map_stage_gbs is the rate the maps flowed through the "
+                             "computes; copy_gbs is the mean rate of those copies (events on the "
+                             "copy stream), map_stage_gbs the rate the maps flowed through the "
                              "map stage"}
 
     cpu = None

@@ -83,6 +83,9 @@ typedef enum rf_status {
  *   the call records on `stream` before the first chunk's map GEMM, between
  *   its map GEMM and its K/V GEMM, and after its K/V GEMM (instrumentation for
  *   per-kernel timing; the events must have been created by the caller).
+ * copy_events (optional, may be NULL; host maps only): host array of
+ *   2 * n_layers cudaEvent_t recorded on the library's copy stream right before
+ *   and after the first chunk's copy of map l (entries 2l and 2l + 1).
  */
 typedef struct rf_fill_args {
   int32_t n_layers;
@@ -106,12 +109,13 @@ typedef struct rf_fill_args {
   void* Kc;
   void* Vc;
   void* const* stage_events;
+  void* const* copy_events;
 } rf_fill_args;
 
 /* Bytes of device workspace ridgefill_fill needs for these arguments
  * (0 on invalid arguments).  Holds the predicted inputs of one row chunk
  * [L, chunk, d_out] bf16, their per-tile sums of squares, and, for host
- * maps, two map slots. */
+ * maps, three map slots. */
 size_t ridgefill_fill_workspace_size(const rf_fill_args* args);
 
 /* Enqueue the fill described above on `stream`. */

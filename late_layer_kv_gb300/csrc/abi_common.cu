@@ -110,7 +110,7 @@ HostStreamer* host_streamer() {
   HostStreamer& h = hs[d];
   if (h.copy == nullptr) {
     cudaError_t e = cudaStreamCreateWithFlags(&h.copy, cudaStreamNonBlocking);
-    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+    for (int i = 0; i < kMapSlots && e == cudaSuccess; ++i) {
       e = cudaEventCreateWithFlags(&h.copied[i], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.freed[i], cudaEventDisableTiming);
     }

@@ -31,11 +31,15 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Device slots for maps streamed from host memory: the copy of layer l + 2
+// can run while layer l computes and layer l + 1 waits.
+constexpr int kMapSlots = 3;
+
 // Per-device side stream and events for streaming maps from host memory.
 struct HostStreamer {
   cudaStream_t copy = nullptr;
-  cudaEvent_t copied[2] = {nullptr, nullptr};
-  cudaEvent_t freed[2] = {nullptr, nullptr};
+  cudaEvent_t copied[kMapSlots] = {};
+  cudaEvent_t freed[kMapSlots] = {};
   cudaEvent_t start = nullptr;
 };
 HostStreamer* host_streamer();  // nullptr on failure (error recorded)

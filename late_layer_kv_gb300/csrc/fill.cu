@@ -54,7 +54,7 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   pl->off_xhat = 0;
   pl->off_ss = align_up(L * pl->R * d * 2, 256);
   pl->off_slots = align_up(pl->off_ss + L * (d / pl->bn_map) * pl->R * 4, 256);
-  const size_t slots = a->maps_on_host ? 2 * d * static_cast<size_t>(a->d_in) * 2 : 0;
+  const size_t slots = a->maps_on_host ? kMapSlots * d * static_cast<size_t>(a->d_in) * 2 : 0;
   pl->total = align_up(pl->off_slots + slots, 256);
 }
 
@@ -195,13 +195,17 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
       if (st != RF_OK) return st;
     } else {
       for (int l = 0; l < a->n_layers; ++l) {
-        const int k = l & 1;
+        const int k = l % kMapSlots;
         uint8_t* slot = ws + pl.off_slots + k * map_bytes;
         cudaError_t e = cudaSuccess;
-        if (start > 0 || l >= 2) e = cudaStreamWaitEvent(hs->copy, hs->freed[k], 0);
+        cudaEvent_t const* cev = reinterpret_cast<cudaEvent_t const*>(a->copy_events);
+        if (start > 0 || l >= kMapSlots) e = cudaStreamWaitEvent(hs->copy, hs->freed[k], 0);
+        if (e == cudaSuccess && cev != nullptr && start == 0) e = cudaEventRecord(cev[2 * l], hs->copy);
         if (e == cudaSuccess)
           e = cudaMemcpyAsync(slot, static_cast<const uint8_t*>(a->A) + l * map_bytes, map_bytes,
                               cudaMemcpyHostToDevice, hs->copy);
+        if (e == cudaSuccess && cev != nullptr && start == 0)
+          e = cudaEventRecord(cev[2 * l + 1], hs->copy);
         if (e == cudaSuccess) e = cudaEventRecord(hs->copied[k], hs->copy);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hs->copied[k], 0);
         if (e != cudaSuccess) return cuda_fail(e, "streaming a map from host memory");

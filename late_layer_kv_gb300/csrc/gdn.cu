@@ -229,7 +229,7 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
   pl->off_k = off;     off = align_up(off + L * H * R * kDk * 4, 256);
   pl->off_v = off;     off = align_up(off + L * H * R * kDk * 4, 256);
   pl->off_gate = off;  off = align_up(off + L * 2 * H * R * 4, 256);
-  pl->off_slots = off; off = align_up(off + (a->maps_on_host ? 2 * d * static_cast<size_t>(a->d_in) * 2 : 0), 256);
+  pl->off_slots = off; off = align_up(off + (a->maps_on_host ? kMapSlots * d * static_cast<size_t>(a->d_in) * 2 : 0), 256);
   pl->total = off;
 }
 
@@ -402,10 +402,10 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
       if ((st = launch_map(m, s)) != RF_OK) return st;
     } else {
       for (int l = 0; l < a->n_layers; ++l) {
-        const int k = l & 1;
+        const int k = l % kMapSlots;
         uint8_t* slot = ws + pl.off_slots + k * map_bytes;
         cudaError_t e = cudaSuccess;
-        if (start > 0 || l >= 2) e = cudaStreamWaitEvent(hs->copy, hs->freed[k], 0);
+        if (start > 0 || l >= kMapSlots) e = cudaStreamWaitEvent(hs->copy, hs->freed[k], 0);
         if (e == cudaSuccess)
           e = cudaMemcpyAsync(slot, static_cast<const uint8_t*>(a->A) + l * map_bytes, map_bytes,
                               cudaMemcpyHostToDevice, hs->copy);

@@ -37,7 +37,7 @@ class FillArgs(ctypes.Structure):
         ("cache_len", ctypes.c_int64), ("rows_per_chunk", ctypes.c_int64),
         ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_double),
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
-        ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp),
+        ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp), ("copy_events", _vp),
     ]
 
 
@@ -142,7 +142,7 @@ def _event_array(events):
 
 def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
               rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
-              stage_events=None) -> FillArgs:
+              stage_events=None, copy_events=None) -> FillArgs:
     L, d_out, d_in = A.shape
     rows = H.shape[0]
     n_kv = Kc.shape[1]
@@ -162,11 +162,15 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
     _dev(Kc, "Kc", torch.bfloat16, (L, n_kv, cache_len, head_dim))
     _dev(Vc, "Vc", torch.bfloat16, (L, n_kv, cache_len, head_dim))
     ev = _event_array(stage_events)
+    cev = _event_array(copy_events)
+    if cev is not None and len(copy_events) != 2 * L:
+        raise ValueError("copy_events needs two events per layer")
     a = FillArgs(L, d_in, d_out, n_kv, head_dim, 1 if host else 0, rows, pos0, cache_len,
                  rows_per_chunk, float(rope_theta), float(rms_eps), _ptr(H), _ptr(A),
                  _ptr(bias), _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Kc), _ptr(Vc),
-                 ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None)
-    a._events_keepalive = ev
+                 ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None,
+                 ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None)
+    a._events_keepalive = (ev, cev)
     return a
 
 
@@ -181,7 +185,7 @@ def gdn_workspace_size(args: GdnArgs) -> int:
 def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
                    rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
                    workspace: Optional[torch.Tensor] = None, stream=None,
-                   stage_events=None) -> None:
+                   stage_events=None, copy_events=None) -> None:
     """Write the K/V cache of the prefix rows of every late attention layer.
 
     ``H`` [rows, d_in] bf16, ``A`` [L, d_out, d_in] bf16 (device, or pinned host
@@ -193,7 +197,7 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     """
     args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
                      rms_eps=rms_eps, pos0=pos0, rows_per_chunk=rows_per_chunk,
-                     stage_events=stage_events)
+                     stage_events=stage_events, copy_events=copy_events)
     lib = load()
     need = int(lib.ridgefill_fill_workspace_size(ctypes.byref(args)))
     if need == 0:
