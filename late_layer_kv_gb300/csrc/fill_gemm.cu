@@ -243,7 +243,7 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, int q, int lane
     const bool is_k = n < p.n_k_tiles;
     const int hpt = p.bn / 128;
     const int head0 = (is_k ? n : n - p.n_k_tiles) * hpt;
-    float* base = is_k ? p.gdn_k : p.gdn_v;
+    __nv_bfloat16* base = is_k ? p.gdn_k : p.gdn_v;
     for (int hh = 0; hh < hpt; ++hh) {
       const uint32_t hc = tcol + hh * 128;
       float scale = rs;
@@ -261,17 +261,26 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, int q, int lane
         }
         scale = rs * rsqrtf(nrm + p.l2_eps);
       }
-      float* dst = base + ((static_cast<size_t>(l) * H + head0 + hh) * ra + row) * 128;
+      // bf16 high part and the bf16 remainder: together about 16 significant bits
+      __nv_bfloat16* hi = base + ((static_cast<size_t>(l) * H + head0 + hh) * 2 * ra + row) * 128;
+      __nv_bfloat16* lo = hi + ra * 128;
       for (int c0 = 0; c0 < 128; c0 += 32) {
         uint32_t a[32];
         tmem_ld32(hc + c0, a);
         tmem_wait_ld();
         if (valid) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 4) {
-            float4 v = make_float4(f32(a[j]) * scale, f32(a[j + 1]) * scale,
-                                   f32(a[j + 2]) * scale, f32(a[j + 3]) * scale);
-            *reinterpret_cast<float4*>(dst + c0 + j) = v;
+          for (int j = 0; j < 32; j += 8) {
+            uint32_t h[4], r[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x0 = f32(a[j + 2 * e]) * scale, x1 = f32(a[j + 2 * e + 1]) * scale;
+              const __nv_bfloat162 hv = __floats2bfloat162_rn(x0, x1);
+              h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+              r[e] = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
+            }
+            *reinterpret_cast<uint4*>(hi + c0 + j) = make_uint4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<uint4*>(lo + c0 + j) = make_uint4(r[0], r[1], r[2], r[3]);
           }
         }
       }

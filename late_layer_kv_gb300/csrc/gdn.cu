@@ -4,23 +4,33 @@
 // predicted input).
 //
 // Per row chunk: the grouped map GEMM (X_hat for every GDN layer), the GDN
-// projection GEMM (RMS scale, L2-normalised k per head, v, alpha, beta),
-// then the state kernel, which carries S over the chunk's rows in order.
+// projection GEMM (RMS scale, L2-normalised k per head, v, alpha, beta; k and v
+// stored as bf16 high parts plus bf16 remainders), then the state kernel.
 //
-// State kernel.  For one head the recurrence
-//   S_t = alpha_t S_{t-1} (I - beta_t k_t k_t^T) + beta_t v_t k_t^T
-// is, row by row of S (index i over d_v),
-//   S_t[i,:] = alpha_t S_{t-1}[i,:] + c_t[i] k_t^T,
-//   c_t[i]   = beta_t (v_t[i] - alpha_t S_{t-1}[i,:] . k_t),
-// so the d_v rows of S evolve independently.  A CTA owns 64 rows of S of one
-// (layer, head) in registers: each thread two rows and 32 columns, taken as
-// every fourth 16-byte chunk so that the four threads of a row read k from
-// distinct shared-memory banks.  The
-// decay is applied lazily: the registers hold S / g, g being the product of
-// the gates since the last renormalisation, so a prompt row costs one FMA per
-// element for the dot product and one for the update.  k, v and the gates are
-// staged through shared memory 16 prompt rows at a time with cp.async in a
-// four-deep ring, so the loads run three stages ahead of the arithmetic.
+// State kernel: the recurrence S_t = a_t S_{t-1} (I - b_t k_t k_t^T) + b_t v_t k_t^T
+// in chunks of C = 64 rows on the tensor cores.  Inside a chunk, with the
+// cumulative log gates G_t = sum_{s<=t} log a_s, g_t = e^{G_t}, the rows of
+//   NEW = (I + B)^-1 (diag(b) V - diag(b g) K S_0^T),
+//   B_ts = b_t e^{G_t - G_s} k_t.k_s for s < t (else 0)
+// are the per-row innovations b_t (v_t - a_t S_{t-1} k_t), and
+//   S_C = g_C S_0 + NEW^T diag(e^{G_C - G_t}) K.
+// With T = (I + B)^-1, W = T diag(b g) K and U = T diag(b) V (the WY factors)
+// this is NEW^T = U^T - S_0 W^T, which needs S_0 only in two products per chunk.
+//
+// One CTA per (layer, head) carries S through the chunks in TMEM (f32).  Its
+// roles:
+//   warp 9      TMA producer: k, v (hi and lo) and the gates of each chunk;
+//   warp 8      MMA issuer (one thread) and TMEM owner;
+//   warps 4-7   chunk-local work for the chunk ahead: P = K K^T on the tensor
+//               cores, T by blocked inversion on the CUDA cores, then
+//               W^T = K^T (T diag(b g))^T and U^T = V^T (T diag(b))^T;
+//   warps 0-3   the serial part: NEW^T = U^T - S_0 W^T (tensor cores, added to
+//               U^T in TMEM), its decay-weighted bf16 split, S += NEW'^T K, and
+//               the bf16 split of the new S for the next chunk.
+// The chunk-local work of chunk c + 1 overlaps the serial part of chunk c.
+// Every product takes bf16 high and low parts of both operands (hi.hi + hi.lo
+// + lo.hi: about 16 significant bits); S and NEW' are A operands read from
+// TMEM, the rest come from 128-byte-swizzled shared-memory tiles.
 #include <cmath>
 #include <mutex>
 
@@ -30,165 +40,534 @@
 namespace rf {
 namespace {
 
-constexpr int kSRows = 64;      // rows of S (d_v) per CTA, two per thread
-constexpr int kGdnThreads = 128;
-constexpr int kStageRows = 16;  // prompt rows per staging buffer
-constexpr int kBufs = 4;        // staging ring depth (loads run kBufs - 1 stages ahead)
-constexpr int kDk = 128;
-constexpr int kStateSmem = kBufs * (kStageRows * (kDk + kSRows) + 2 * kStageRows) * 4;
-constexpr float kRenorm = 1e-20f;
+constexpr int kC = 64;         // rows per chunk
+constexpr int kDk = 128;       // d_k = d_v
+constexpr int kStateThreads = 320;
+constexpr int kPreBar = 1;     // named barrier of warps 4-7
 
-__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+// shared memory, from a 1024-byte aligned base
+constexpr uint32_t kBox = 8192;                     // one 64 x 64 bf16 swizzled box
+constexpr uint32_t kKV = 4 * kBox;                  // hi (2 boxes) then lo (2 boxes)
+constexpr uint32_t kOffK = 0;                       // two chunk buffers of k
+constexpr uint32_t kOffV = kOffK + 2 * kKV;         // one chunk buffer of v
+constexpr uint32_t kOffT = kOffV + kKV;             // T diag(b g) hi, lo; T diag(b) hi, lo
+constexpr uint32_t kOffW = kOffT + 4 * kBox;        // -W hi, lo: [j][t] rows (MN-major B)
+constexpr uint32_t kOffGateRaw = kOffW + 4 * kBox;  // two buffers: alpha[64], beta[64]
+constexpr uint32_t kOffGate = kOffGateRaw + 2 * 512;  // two slots: beta, b g, decay, G
+constexpr uint32_t kOffScr = kOffGate + 2 * 1024;     // B, T: [64][65] f32 each
+constexpr int kLd = 65;
+constexpr uint32_t kOffBar = kOffScr + 2 * kC * kLd * 4;
+constexpr uint32_t kStateSmem = kOffBar + 256 + 1024;
+static_assert(kStateSmem <= 232448, "state kernel shared memory");
+
+// TMEM columns
+constexpr uint32_t kColS = 0;     // S (f32, 128)
+constexpr uint32_t kColSh = 128;  // S bf16 high parts (64 columns = 128 values)
+constexpr uint32_t kColSl = 192;  // S bf16 remainders
+constexpr uint32_t kColN = 256;   // U^T, then NEW^T (f32, 64)
+constexpr uint32_t kColNh = 320;  // NEW'^T bf16 high parts (32 columns)
+constexpr uint32_t kColNl = 352;  // NEW'^T remainders
+constexpr uint32_t kColP = 384;   // P = K K^T, then W^T (f32, 64)
+
+// barriers
+enum : int {
+  kBarKFull = 0,   // 2: k + gates of a chunk landed
+  kBarKEmpty = 2,  // 2: the chunk's last product that reads k is done
+  kBarVFull = 4,
+  kBarVEmpty = 5,
+  kBarP = 6,       // P done
+  kBarUW = 7,      // U^T and W^T done
+  kBarDA = 8,      // NEW^T done
+  kBarDB = 9,      // S update done
+  kBarTops = 10,   // T operands written (4 warp arrivals)
+  kBarWop = 11,    // -W operand written
+  kBarNop = 12,    // NEW' operand written
+  kBarSops = 13,   // S operand written and S pre-scaled
+  kBarFinal = 14,
+  kNumBars = 15,
+};
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {
+  return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-// d = a * b + c on two float lanes at once (one issued instruction)
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  float2 d;
-  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
-      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
-      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
-      : "=f"(d.x), "=f"(d.y)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return d;
+// bf16 high parts and remainders of 8 values, packed two per word (lower index low)
+__device__ __forceinline__ void split8(const float (&x)[8], uint4& hi, uint4& lo) {
+  uint32_t h[4], r[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const __nv_bfloat162 hv = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+    h[e] = *reinterpret_cast<const uint32_t*>(&hv);
+    r[e] = pack_bf16(x[2 * e] - __low2float(hv), x[2 * e + 1] - __high2float(hv));
+  }
+  hi = make_uint4(h[0], h[1], h[2], h[3]);
+  lo = make_uint4(r[0], r[1], r[2], r[3]);
+}
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 hv = __floats2bfloat162_rn(x0, x1);
+  hi = *reinterpret_cast<const uint32_t*>(&hv);
+  lo = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
 }
 
-__global__ void __launch_bounds__(kGdnThreads) gdn_state_kernel(const GdnStateParams p) {
-  extern __shared__ __align__(16) float smem_f[];
-  float (*sk)[kStageRows][kDk] = reinterpret_cast<float (*)[kStageRows][kDk]>(smem_f);
-  float (*sv)[kStageRows][kSRows] =
-      reinterpret_cast<float (*)[kStageRows][kSRows]>(smem_f + kBufs * kStageRows * kDk);
-  float (*sg)[2][kStageRows] = reinterpret_cast<float (*)[2][kStageRows]>(
-      smem_f + kBufs * kStageRows * (kDk + kSRows));
+// log of the chunk's total decay: warp-wide sum of log alpha over its n rows
+__device__ __forceinline__ float chunk_log_decay(const float* alpha, int n, int lane) {
+  float s = 0.f;
+  for (int t = lane; t < n; t += 32) s += fmaxf(logf(alpha[t]), -80.f);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  return s;
+}
 
-  const int slice = blockIdx.x, h = blockIdx.y, l = blockIdx.z;
-  const int tid = threadIdx.x;
-  const int rp = tid >> 2;    // this thread owns S rows rp and rp + 32 of the slice
-  const int part = tid & 3;   // and the 16-byte column chunks part, part + 4, ..., part + 28
-  const int i0 = slice * kSRows + rp;
+// the three split terms of one product: hi.hi, hi.lo, lo.hi
+struct Split {
+  uint32_t a[3];
+  uint32_t b[3];
+};
+
+__global__ void __launch_bounds__(kStateThreads, 1)
+    gdn_state_kernel(const __grid_constant__ GdnStateParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(sm);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kOffBar);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+  float* Bs = reinterpret_cast<float*>(sm + kOffScr);
+  float* Ts = Bs + kC * kLd;
+  float* Xs = reinterpret_cast<float*>(sm + kOffT);  // scratch while T is formed
+
+  const int h = blockIdx.x, l = blockIdx.y;
   const int H = p.heads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int lh = l * H + h;
   const size_t ra = static_cast<size_t>(p.rows_alloc);
-  const int dv = p.dv;
+  const float* alpha_g = p.gate + (static_cast<size_t>(l) * 2 * H + h) * ra;
+  const float* beta_g = p.gate + (static_cast<size_t>(l) * 2 * H + H + h) * ra;
+  float* s_out = p.S + static_cast<size_t>(lh) * kDk * kDk;
+  const float* s_in = p.first ? (p.S0 != nullptr ? p.S0 + static_cast<size_t>(lh) * kDk * kDk
+                                                 : nullptr)
+                              : s_out;
+  const int nch = (p.rows + kC - 1) / kC;
 
-  const float* kbase = p.k + (static_cast<size_t>(l) * H + h) * ra * kDk;
-  const float* vbase = p.v + (static_cast<size_t>(l) * H + h) * ra * dv + slice * kSRows;
-  const float* abase = p.gate + (static_cast<size_t>(l) * 2 * H + h) * ra;
-  const float* bbase = p.gate + (static_cast<size_t>(l) * 2 * H + H + h) * ra;
-  const size_t row0 = ((static_cast<size_t>(l) * H + h) * dv + i0) * kDk;
-  const size_t row1 = row0 + static_cast<size_t>(32) * kDk;
-
-  // S0, S1 hold columns 4 (part + 4 q) + e at pair 2 q + e / 2
-  float2 S0[16], S1[16];
-  const float* src = p.first ? p.S0 : p.S;
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    float4 x0 = make_float4(0.f, 0.f, 0.f, 0.f), x1 = x0;
-    if (src != nullptr) {
-      x0 = *reinterpret_cast<const float4*>(src + row0 + 4 * (part + 4 * q));
-      x1 = *reinterpret_cast<const float4*>(src + row1 + 4 * (part + 4 * q));
-    }
-    S0[2 * q] = make_float2(x0.x, x0.y); S0[2 * q + 1] = make_float2(x0.z, x0.w);
-    S1[2 * q] = make_float2(x1.x, x1.y); S1[2 * q + 1] = make_float2(x1.z, x1.w);
+  if (tid == 0) {
+    for (int i = 0; i < kNumBars; ++i) mbar_init(&bar[i], 1);
+    mbar_init(&bar[kBarTops], 4);
+    mbar_init(&bar[kBarWop], 4);
+    mbar_init(&bar[kBarNop], 4);
+    mbar_init(&bar[kBarSops], 4);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  float g = 1.f;
-
-  const int nst = (p.rows + kStageRows - 1) / kStageRows;
-  auto load = [&](int st, int buf) {
-    const int t0 = st * kStageRows;
-    const int n = min(kStageRows, p.rows - t0);
-    for (int q = tid; q < n * (kDk / 4); q += kGdnThreads) {
-      const int rr = q / (kDk / 4), cc = q % (kDk / 4);
-      cp_async16(&sk[buf][rr][cc * 4], kbase + static_cast<size_t>(t0 + rr) * kDk + cc * 4);
-    }
-    for (int q = tid; q < n * (kSRows / 4); q += kGdnThreads) {
-      const int rr = q / (kSRows / 4), cc = q % (kSRows / 4);
-      cp_async16(&sv[buf][rr][cc * 4], vbase + static_cast<size_t>(t0 + rr) * dv + cc * 4);
-    }
-    if (tid < 2 * (kStageRows / 4)) {
-      const int which = tid / (kStageRows / 4), cc = tid % (kStageRows / 4);
-      if (cc * 4 < n)  // gate rows are padded to the 128-row allocation
-        cp_async16(&sg[buf][which][cc * 4], (which ? bbase : abase) + t0 + cc * 4);
-    }
-    cp_async_commit();
-  };
-
-  // one cp.async group per stage (empty past the end) keeps the group count uniform
-  for (int q = 0; q < kBufs - 1; ++q) {
-    if (q < nst) load(q, q);
-    else cp_async_commit();
+  if (warp == 8) {
+    tmem_alloc(tslot, 512);
+    tmem_relinquish();
   }
-  for (int st = 0; st < nst; ++st) {
-    const int buf = st % kBufs;
-    const int ahead = st + kBufs - 1;
-    if (ahead < nst) load(ahead, ahead % kBufs);
-    else cp_async_commit();
-    cp_async_wait<kBufs - 1>();
-    __syncthreads();
-    const int n = min(kStageRows, p.rows - st * kStageRows);
-    for (int tt = 0; tt < n; ++tt) {
-      const float a = sg[buf][0][tt];
-      const float bt = sg[buf][1][tt];
-      const float v0 = sv[buf][tt][rp], v1 = sv[buf][tt][rp + 32];
-      float2 kk[16];
-      const float4* k4 = reinterpret_cast<const float4*>(&sk[buf][tt][0]);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 x = k4[part + 4 * q];
-        kk[2 * q] = make_float2(x.x, x.y);
-        kk[2 * q + 1] = make_float2(x.z, x.w);
-      }
-      float2 e0a = make_float2(0.f, 0.f), e0b = e0a, e1a = e0a, e1b = e0a;
-#pragma unroll
-      for (int j = 0; j < 16; j += 2) {
-        e0a = ffma2(S0[j], kk[j], e0a);
-        e0b = ffma2(S0[j + 1], kk[j + 1], e0b);
-        e1a = ffma2(S1[j], kk[j], e1a);
-        e1b = ffma2(S1[j + 1], kk[j + 1], e1b);
-      }
-      float e0 = (e0a.x + e0a.y) + (e0b.x + e0b.y);
-      float e1 = (e1a.x + e1a.y) + (e1b.x + e1b.y);
-      e0 += __shfl_xor_sync(0xffffffffu, e0, 1);
-      e1 += __shfl_xor_sync(0xffffffffu, e1, 1);
-      e0 += __shfl_xor_sync(0xffffffffu, e0, 2);
-      e1 += __shfl_xor_sync(0xffffffffu, e1, 2);
-      // true S_{t-1}[i,:] k_t = g * e
-      const float ag = a * g;
-      const float c0 = bt * (v0 - ag * e0);
-      const float c1 = bt * (v1 - ag * e1);
-      if (ag >= kRenorm) {
-        const float inv = 1.f / ag;
-        const float2 s0 = make_float2(c0 * inv, c0 * inv), s1 = make_float2(c1 * inv, c1 * inv);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          S0[j] = ffma2(s0, kk[j], S0[j]);
-          S1[j] = ffma2(s1, kk[j], S1[j]);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tb = *tslot;
+
+  if (warp == 9) {
+    // ---------------------------------------------------------------- producer
+    if (lane == 0 && nch > 0) {
+      tma_prefetch(&p.tmK);
+      tma_prefetch(&p.tmV);
+      int loaded_k = 0, loaded_v = 0;
+      bool ok = true;
+      for (int c = 0; c < nch && ok; ++c) {
+        const int kb = c & 1;
+        if (c >= 2 && !mbar_wait(&bar[kBarKEmpty + kb], ((c - 2) >> 1) & 1, abort_flag, p.err, kErrGdn)) {
+          ok = false;
+          break;
         }
-        g = ag;
+        uint64_t* kf = &bar[kBarKFull + kb];
+        mbar_expect_tx(kf, kKV + 512);
+        for (int part = 0; part < 2; ++part)
+          for (int box = 0; box < 2; ++box)
+            tma_load_3d(sb + kOffK + kb * kKV + part * 2 * kBox + box * kBox, &p.tmK, kf, 64 * box,
+                        kC * c, 2 * lh + part);
+        bulk_load(sb + kOffGateRaw + kb * 512, alpha_g + kC * c, 256, kf);
+        bulk_load(sb + kOffGateRaw + kb * 512 + 256, beta_g + kC * c, 256, kf);
+        loaded_k = c + 1;
+        if (c >= 1 && !mbar_wait(&bar[kBarVEmpty], (c - 1) & 1, abort_flag, p.err, kErrGdn)) {
+          ok = false;
+          break;
+        }
+        uint64_t* vf = &bar[kBarVFull];
+        mbar_expect_tx(vf, kKV);
+        for (int part = 0; part < 2; ++part)
+          for (int box = 0; box < 2; ++box)
+            tma_load_3d(sb + kOffV + part * 2 * kBox + box * kBox, &p.tmV, vf, 64 * box, kC * c,
+                        2 * lh + part);
+        loaded_v = c + 1;
+      }
+      if (!ok) {  // let the copies already issued land before the CTA exits
+        for (int c = loaded_k - 2 < 0 ? 0 : loaded_k - 2; c < loaded_k; ++c)
+          mbar_drain(&bar[kBarKFull + (c & 1)], (c >> 1) & 1);
+        if (loaded_v > 0) mbar_drain(&bar[kBarVFull], (loaded_v - 1) & 1);
+      }
+    }
+  } else if (warp == 8) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0 && nch > 0) {
+      const uint32_t id_p = idesc_bf16_f32(128, 64);
+      const uint32_t id_uw = idesc_bf16_f32(128, 64) | (1u << 15);
+      const uint32_t id_da = idesc_bf16_f32(128, 64) | (1u << 16);
+      const uint32_t id_db = idesc_bf16_f32(128, 128) | (1u << 16);
+      auto wait = [&](int b, uint32_t parity) -> bool {
+        const bool ok = mbar_wait(&bar[b], parity, abort_flag, p.err, kErrGdn);
+        tc_fence_after();
+        return ok;
+      };
+      // P = K K^T: A = the k tile read as 128 K-major rows (rows 64-127 are not used)
+      auto issue_p = [&](int c) {
+        const uint32_t kt = sb + kOffK + (c & 1) * kKV;
+        const uint32_t ah[3] = {kt, kt, kt + 2 * kBox};
+        const uint32_t bh[3] = {kt, kt + 2 * kBox, kt};
+        uint32_t acc = 0;
+        for (int g = 0; g < 3; ++g)
+          for (int kblk = 0; kblk < 2; ++kblk)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = sdesc_kmajor_sw128(ah[g] + kblk * kBox + 32 * ks);
+              const uint64_t bd = sdesc_kmajor_sw128(bh[g] + kblk * kBox + 32 * ks);
+              mma_bf16(tb + kColP, ad, bd, id_p, acc);
+              acc = 1;
+            }
+        mma_commit(&bar[kBarP]);
+      };
+      // U^T = V^T (T diag(b))^T and W^T = K^T (T diag(b g))^T
+      auto issue_uw = [&](int c) {
+        const uint32_t kt = sb + kOffK + (c & 1) * kKV, vt = sb + kOffV;
+        const uint32_t tw = sb + kOffT, tu = sb + kOffT + 2 * kBox;
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t at = which == 0 ? vt : kt;
+          const uint32_t bt = which == 0 ? tu : tw;
+          const uint32_t dcol = which == 0 ? kColN : kColP;
+          const uint32_t ah[3] = {at, at, at + 2 * kBox};
+          const uint32_t bh[3] = {bt, bt + kBox, bt};
+          uint32_t acc = 0;
+          for (int g = 0; g < 3; ++g)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint64_t ad = sdesc_mnmajor_sw128(ah[g] + 2048 * ks, 8192);
+              const uint64_t bd = sdesc_kmajor_sw128(bh[g] + 32 * ks);
+              mma_bf16(tb + dcol, ad, bd, id_uw, acc);
+              acc = 1;
+            }
+        }
+        mma_commit(&bar[kBarUW]);
+        mma_commit(&bar[kBarVEmpty]);
+      };
+      bool ok = wait(kBarKFull, 0);
+      if (ok) issue_p(0);
+      ok = ok && wait(kBarTops, 0) && wait(kBarVFull, 0);
+      if (ok) issue_uw(0);
+      for (int c = 0; c < nch && ok; ++c) {
+        if (!wait(kBarWop, c & 1) || !wait(kBarSops, c & 1)) break;
+        {  // NEW^T += S_0 (-W)^T, added to U^T
+          const uint32_t wt = sb + kOffW;
+          const uint32_t ah[3] = {tb + kColSh, tb + kColSh, tb + kColSl};
+          const uint32_t bh[3] = {wt, wt + 2 * kBox, wt};
+          for (int g = 0; g < 3; ++g)
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks)
+              mma_bf16_tmem_a(tb + kColN, ah[g] + 8 * ks, sdesc_mnmajor_sw128(bh[g] + 2048 * ks, 8192),
+                              id_da, 1u);
+          mma_commit(&bar[kBarDA]);
+        }
+        if (c + 1 < nch) {
+          if (!wait(kBarKFull + ((c + 1) & 1), ((c + 1) >> 1) & 1)) break;
+          issue_p(c + 1);
+        }
+        if (!wait(kBarNop, c & 1)) break;
+        {  // S += NEW'^T K
+          const uint32_t kt = sb + kOffK + (c & 1) * kKV;
+          const uint32_t ah[3] = {tb + kColNh, tb + kColNh, tb + kColNl};
+          const uint32_t bh[3] = {kt, kt + 2 * kBox, kt};
+          for (int g = 0; g < 3; ++g)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+              mma_bf16_tmem_a(tb + kColS, ah[g] + 8 * ks, sdesc_mnmajor_sw128(bh[g] + 2048 * ks, 8192),
+                              id_db, 1u);
+          mma_commit(&bar[kBarDB]);
+          mma_commit(&bar[kBarKEmpty + (c & 1)]);
+        }
+        if (c + 1 < nch) {
+          if (!wait(kBarTops, (c + 1) & 1) || !wait(kBarVFull, (c + 1) & 1)) break;
+          issue_uw(c + 1);
+        }
+      }
+      // every MMA issued has finished before TMEM is released
+      mma_commit(&bar[kBarFinal]);
+      mbar_drain(&bar[kBarFinal], 0);
+    }
+  } else if (warp >= 4) {
+    // ---------------------------------------------------------------- chunk-local work
+    const int pt = tid - 128;  // 0..127, TMEM lane of this thread
+    const int q = warp - 4;
+    for (int c = 0; c < nch; ++c) {
+      const int kb = c & 1;
+      bool ok = mbar_wait(&bar[kBarKFull + kb], (c >> 1) & 1, abort_flag, p.err, kErrGdn);
+      if (!named_bar_all(kPreBar, 128, ok)) break;
+      float* gs = reinterpret_cast<float*>(sm + kOffGate + kb * 1024);  // beta, bg, dec, G
+      if (q == 0) {
+        const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw + kb * 512);
+        const float* gbeta = ga + 64;
+        const int n = min(kC, p.rows - kC * c);
+        float la[2], be[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int t = 2 * lane + e;
+          la[e] = t < n ? fmaxf(logf(ga[t]), -80.f) : 0.f;
+          be[e] = t < n ? gbeta[t] : 0.f;
+        }
+        const float pair = la[0] + la[1];
+        float incl = pair;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const float g0 = incl - la[1], g1 = incl;
+        const float gC = __shfl_sync(0xffffffffu, incl, 31);
+        gs[2 * lane] = be[0];
+        gs[2 * lane + 1] = be[1];
+        gs[64 + 2 * lane] = be[0] * expf(g0);
+        gs[64 + 2 * lane + 1] = be[1] * expf(g1);
+        gs[128 + 2 * lane] = expf(gC - g0);
+        gs[128 + 2 * lane + 1] = expf(gC - g1);
+        gs[192 + 2 * lane] = g0;
+        gs[192 + 2 * lane + 1] = g1;
+      }
+      ok = mbar_wait(&bar[kBarP], c & 1, abort_flag, p.err, kErrGdn);
+      if (!named_bar_all(kPreBar, 128, ok)) break;
+      tc_fence_after();
+      // B_ts = b_t e^{G_t - G_s} P_ts below the diagonal
+      if (q < 2) {
+        const int t = pt;
+        const float gt = gs[192 + t], bt = gs[t];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tmem_ld32(tb + (static_cast<uint32_t>(32 * q) << 16) + kColP + 32 * half, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int s = 32 * half + j;
+            Bs[t * kLd + s] = s < t ? bt * expf(gt - gs[192 + s]) * __uint_as_float(r[j]) : 0.f;
+          }
+        }
+      }
+      named_bar_sync(kPreBar, 128);
+      // T = (I + B)^-1, unit lower triangular, by 16 x 16 blocks: diagonal blocks
+      // by substitution, then block diagonals a - b = 1, 2, 3:
+      //   T_ab = -T_aa sum_{c=b}^{a-1} B_ac T_cb
+      if (pt < 64) {
+        const int b = pt >> 4, s = pt & 15, o = 16 * b;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+          float acc = r == s ? 1.f : 0.f;
+#pragma unroll
+          for (int k = 0; k < r; ++k) acc = fmaf(-Bs[(o + r) * kLd + o + k], x[k], acc);
+          x[r] = acc;
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) Ts[(o + r) * kLd + o + s] = x[r];
+      }
+      named_bar_sync(kPreBar, 128);
+      for (int d = 1; d < 4; ++d) {
+        const int nel = (4 - d) * 256;
+        for (int idx = pt; idx < nel; idx += 128) {
+          const int b = idx >> 8, e = idx & 255, r = e >> 4, cc = e & 15, a = b + d;
+          float acc = 0.f;
+          for (int c2 = b; c2 < a; ++c2) {
+            const float* brow = Bs + (16 * a + r) * kLd + 16 * c2;
+            const float* tcol = Ts + (16 * c2) * kLd + 16 * b + cc;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc = fmaf(brow[k], tcol[k * kLd], acc);
+          }
+          Xs[(16 * a + r) * kLd + 16 * b + cc] = acc;
+        }
+        named_bar_sync(kPreBar, 128);
+        for (int idx = pt; idx < nel; idx += 128) {
+          const int b = idx >> 8, e = idx & 255, r = e >> 4, cc = e & 15, a = b + d;
+          const float* trow = Ts + (16 * a + r) * kLd + 16 * a;
+          const float* xcol = Xs + (16 * a) * kLd + 16 * b + cc;
+          float acc = 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) acc = fmaf(trow[k], xcol[k * kLd], acc);
+          Ts[(16 * a + r) * kLd + 16 * b + cc] = -acc;
+        }
+        named_bar_sync(kPreBar, 128);
+      }
+      // T diag(b g) and T diag(b) as bf16 hi/lo K-major tiles [t][s]
+      for (int idx = pt; idx < kC * 8; idx += 128) {
+        const int t = idx >> 3, ch = idx & 7;
+        float w[8], u[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const int s = 8 * ch + e;
+          const float v = s <= t ? Ts[t * kLd + s] : 0.f;
+          w[e] = v * gs[64 + s];
+          u[e] = v * gs[s];
+        }
+        uint4 hi, lo;
+        const uint32_t off = swz(t, ch);
+        split8(w, hi, lo);
+        *reinterpret_cast<uint4*>(sm + kOffT + off) = hi;
+        *reinterpret_cast<uint4*>(sm + kOffT + kBox + off) = lo;
+        split8(u, hi, lo);
+        *reinterpret_cast<uint4*>(sm + kOffT + 2 * kBox + off) = hi;
+        *reinterpret_cast<uint4*>(sm + kOffT + 3 * kBox + off) = lo;
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarTops]);
+      // -W as the MN-major B operand: row j holds W^T[j][0..63]
+      ok = mbar_wait(&bar[kBarUW], c & 1, abort_flag, p.err, kErrGdn);
+      if (!named_bar_all(kPreBar, 128, ok)) break;
+      tc_fence_after();
+      {
+        const int j = pt;
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tmem_ld32(tb + (static_cast<uint32_t>(32 * q) << 16) + kColP + 32 * half, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int c8 = 0; c8 < 4; ++c8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[e] = -__uint_as_float(r[8 * c8 + e]);
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            const uint32_t off = swz(j, 4 * half + c8);
+            *reinterpret_cast<uint4*>(sm + kOffW + off) = hi;
+            *reinterpret_cast<uint4*>(sm + kOffW + 2 * kBox + off) = lo;
+          }
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarWop]);
+    }
+  } else {
+    // ---------------------------------------------------------------- serial part
+    const int i = tid;  // state row = TMEM lane
+    const uint32_t lrow = tb + (static_cast<uint32_t>(32 * warp) << 16);
+    const float* src = s_in != nullptr ? s_in + static_cast<size_t>(i) * kDk : nullptr;
+    float* dst = s_out + static_cast<size_t>(i) * kDk;
+    // S (f32, pre-scaled by the next chunk's decay g) and its bf16 split, 64 columns at a time
+    auto put_state = [&](const float (&s)[64], int half, float g) {
+      uint32_t r[32], hi[32], lo[32];
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(g * s[32 * cc + j]);
+        tmem_st32(lrow + kColS + 64 * half + 32 * cc, r);
+      }
+#pragma unroll
+      for (int m = 0; m < 32; ++m) split2(s[2 * m], s[2 * m + 1], hi[m], lo[m]);
+      tmem_st32(lrow + kColSh + 32 * half, hi);
+      tmem_st32(lrow + kColSl + 32 * half, lo);
+    };
+    bool ok = true;
+    if (nch == 0) {
+      for (int j = 0; j < kDk; j += 4)
+        *reinterpret_cast<float4*>(dst + j) =
+            src != nullptr ? *reinterpret_cast<const float4*>(src + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    } else {
+      ok = mbar_wait(&bar[kBarKFull], 0, abort_flag, p.err, kErrGdn);
+      if (ok) {
+        const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw);
+        const float g = expf(chunk_log_decay(ga, min(kC, p.rows), lane));
+        for (int half = 0; half < 2; ++half) {
+          float s[64];
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const float4 x = src != nullptr ? *reinterpret_cast<const float4*>(src + 64 * half + j)
+                                            : make_float4(0.f, 0.f, 0.f, 0.f);
+            s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
+          }
+          put_state(s, half, g);
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kBarSops]);
+      }
+    }
+    for (int c = 0; c < nch && ok; ++c) {
+      const int kb = c & 1;
+      if (!mbar_wait(&bar[kBarDA], c & 1, abort_flag, p.err, kErrGdn)) break;
+      tc_fence_after();
+      {  // NEW'^T[i][t] = NEW^T[i][t] e^{G_C - G_t}
+        const float* dec = reinterpret_cast<const float*>(sm + kOffGate + kb * 1024) + 128;
+        uint32_t hi[32], lo[32];
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tmem_ld32(lrow + kColN + 32 * half, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int m = 0; m < 16; ++m) {
+            const int t = 32 * half + 2 * m;
+            split2(__uint_as_float(r[2 * m]) * dec[t], __uint_as_float(r[2 * m + 1]) * dec[t + 1],
+                   hi[16 * half + m], lo[16 * half + m]);
+          }
+        }
+        tmem_st32(lrow + kColNh, hi);
+        tmem_st32(lrow + kColNl, lo);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bar[kBarNop]);
+      if (!mbar_wait(&bar[kBarDB], c & 1, abort_flag, p.err, kErrGdn)) break;
+      tc_fence_after();
+      if (c + 1 == nch) {
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t r[32];
+          tmem_ld32(lrow + kColS + 32 * cc, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int j = 0; j < 32; j += 4)
+            *reinterpret_cast<float4*>(dst + 32 * cc + j) =
+                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
+                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+        }
       } else {
+        const int kn = (c + 1) & 1;
+        if (!mbar_wait(&bar[kBarKFull + kn], ((c + 1) >> 1) & 1, abort_flag, p.err, kErrGdn)) break;
+        const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw + kn * 512);
+        const float g = expf(chunk_log_decay(ga, min(kC, p.rows - kC * (c + 1)), lane));
+        for (int half = 0; half < 2; ++half) {
+          float s[64];
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          S0[j] = make_float2(fmaf(c0, kk[j].x, ag * S0[j].x), fmaf(c0, kk[j].y, ag * S0[j].y));
-          S1[j] = make_float2(fmaf(c1, kk[j].x, ag * S1[j].x), fmaf(c1, kk[j].y, ag * S1[j].y));
+          for (int cc = 0; cc < 2; ++cc) {
+            uint32_t r[32];
+            tmem_ld32(lrow + kColS + 64 * half + 32 * cc, r);
+            tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s[32 * cc + j] = __uint_as_float(r[j]);
+          }
+          put_state(s, half, g);
         }
-        g = 1.f;
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kBarSops]);
       }
     }
-    __syncthreads();
   }
-#pragma unroll
-  for (int q = 0; q < 8; ++q) {
-    *reinterpret_cast<float4*>(p.S + row0 + 4 * (part + 4 * q)) =
-        make_float4(g * S0[2 * q].x, g * S0[2 * q].y, g * S0[2 * q + 1].x, g * S0[2 * q + 1].y);
-    *reinterpret_cast<float4*>(p.S + row1 + 4 * (part + 4 * q)) =
-        make_float4(g * S1[2 * q].x, g * S1[2 * q].y, g * S1[2 * q + 1].x, g * S1[2 * q + 1].y);
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tb, 512);
   }
 }
 
@@ -234,7 +613,8 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
 }
 
 rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, const void* xhat,
-                          const float* ss, float* kb, float* vb, float* gb, cudaStream_t s) {
+                          const float* ss, __nv_bfloat16* kb, __nv_bfloat16* vb, float* gb,
+                          cudaStream_t s) {
   GemmParams p{};
   p.mode = kModeGdnProj;
   p.k_blocks = a->d_out / kBK;
@@ -294,8 +674,8 @@ cudaError_t launch_gdn_state(const GdnStateParams& p, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  dim3 grid(p.dv / kSRows, p.heads, p.layers);
-  gdn_state_kernel<<<grid, kGdnThreads, kStateSmem, stream>>>(p);
+  dim3 grid(p.heads, p.layers);
+  gdn_state_kernel<<<grid, kStateThreads, kStateSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -340,22 +720,29 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* xhat = ws + pl.off_xhat;
   float* ss = reinterpret_cast<float*>(ws + pl.off_ss);
-  float* kb = reinterpret_cast<float*>(ws + pl.off_k);
-  float* vb = reinterpret_cast<float*>(ws + pl.off_v);
+  __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_k);
+  __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_v);
   float* gb = reinterpret_cast<float*>(ws + pl.off_gate);
 
   GdnStateParams sp{};
-  sp.k = kb;
-  sp.v = vb;
   sp.gate = gb;
   sp.S0 = a->S0;
   sp.S = a->S;
   sp.layers = a->n_layers;
   sp.heads = a->n_heads;
-  sp.dv = a->d_v;
   sp.rows_alloc = static_cast<int32_t>(pl.R);
-  sp.chunk = a->chunk;
   sp.err = device_error_word();
+  if (sp.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
+  // k and v of one launch as {d_k, rows, L*H*2} (hi/lo planes of each layer and head)
+  auto state_maps = [&](int64_t rc) -> bool {
+    const uint64_t row_b = static_cast<uint64_t>(kDk) * 2;
+    const uint64_t plane_b = row_b * pl.R;
+    const uint64_t planes = static_cast<uint64_t>(a->n_layers) * a->n_heads * 2;
+    return make_tmap_3d(&sp.tmK, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kb, kDk, rc, planes, row_b,
+                        plane_b, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B) &&
+           make_tmap_3d(&sp.tmV, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, vb, kDk, rc, planes, row_b,
+                        plane_b, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B);
+  };
 
   if (a->rows == 0) {  // the end-of-fill state is the initial state
     sp.rows = 0;
@@ -424,6 +811,7 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     if ((st = mark(start, 2)) != RF_OK) return st;
     sp.rows = static_cast<int32_t>(rc);
     sp.first = start == 0 ? 1 : 0;
+    if (!state_maps(rc)) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the GDN state");
     cudaError_t e = launch_gdn_state(sp, s);
     if (e != cudaSuccess) return cuda_fail(e, "GDN state launch");
     if ((st = mark(start, 3)) != RF_OK) return st;

@@ -67,8 +67,8 @@ struct GemmParams {
   float inv_d;
   float eps;
   // GDN projection epilogue
-  float* gdn_k;        // [L, H, rows_alloc, dk] f32
-  float* gdn_v;        // [L, H, rows_alloc, dv] f32
+  __nv_bfloat16* gdn_k;  // [L, H, 2, rows_alloc, dk]: bf16 high part, then the low remainder
+  __nv_bfloat16* gdn_v;  // [L, H, 2, rows_alloc, dv], same split
   float* gdn_gate;     // [L, 2, H, rows_alloc] f32 (alpha, beta)
   int32_t gdn_heads;
   int32_t gdn_rows_alloc;
@@ -96,17 +96,15 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 
 // ------------------------------------------------------------ GDN state
 struct GdnStateParams {
-  const float* k;      // [L, H, rows_alloc, dk]
-  const float* v;      // [L, H, rows_alloc, dv]
+  CUtensorMap tmK;     // k hi/lo, 3D {dk, rows, L*H*2}, box {64, 64, 1}, 128-byte swizzle
+  CUtensorMap tmV;     // v hi/lo, same layout
   const float* gate;   // [L, 2, H, rows_alloc]: alpha, then beta
   const float* S0;     // [L, H, dv, dk] or null
   float* S;            // [L, H, dv, dk]
   int32_t layers;
   int32_t heads;
-  int32_t dv;
   int32_t rows;        // rows of this launch
   int32_t rows_alloc;
-  int32_t chunk;
   int32_t first;       // 1 if S starts from S0/zero, 0 if it continues from S
   int* err;
 };
