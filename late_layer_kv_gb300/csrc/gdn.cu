@@ -19,18 +19,23 @@
 //
 // One CTA per (layer, head) carries S through the chunks in TMEM (f32).  Its
 // roles:
-//   warp 9      TMA producer: k, v (hi and lo) and the gates of each chunk;
+//   warp 9      TMA producers: lane 0 streams k (hi and lo) and the gates into
+//               three chunk buffers, lane 1 streams v into one;
 //   warp 8      MMA issuer (one thread) and TMEM owner;
-//   warps 4-7   chunk-local work for the chunk ahead: P = K K^T on the tensor
-//               cores, T by blocked inversion on the CUDA cores, then
-//               W^T = K^T (T diag(b g))^T and U^T = V^T (T diag(b))^T;
-//   warps 0-3   the serial part: NEW^T = U^T - S_0 W^T (tensor cores, added to
-//               U^T in TMEM), its decay-weighted bf16 split, S += NEW'^T K, and
-//               the bf16 split of the new S for the next chunk.
-// The chunk-local work of chunk c + 1 overlaps the serial part of chunk c.
-// Every product takes bf16 high and low parts of both operands (hi.hi + hi.lo
-// + lo.hi: about 16 significant bits); S and NEW' are A operands read from
-// TMEM, the rest come from 128-byte-swizzled shared-memory tiles.
+//   warps 4-7   chunk-local work: B from P = K K^T (tensor cores), T = (I + B)^-1
+//               by 16 x 16 diagonal blocks and a recursive 2 x 2 block inverse
+//               (CUDA cores, in place), and the T operands of U^T, W^T;
+//   warps 0-3   the serial part: the -W operand, NEW^T = U^T - S_0 W^T (tensor
+//               cores, added to U^T in TMEM), its decay-weighted bf16 split,
+//               S += NEW'^T K, and the bf16 split of the new S for the next chunk.
+// The issuer sends P of the next chunk as soon as its keys have landed and the
+// previous P has been read, so the chunk-local work of chunk c + 1 overlaps the
+// serial part of chunk c.  Every product takes bf16 high and low parts of both
+// operands (hi.hi + hi.lo + lo.hi, about 16 significant bits; P also lo.lo);
+// S and NEW' are A operands read from TMEM, the rest come from
+// 128-byte-swizzled shared-memory tiles.  Where the operand shared by two split
+// terms allows, the terms are one N = 128 product whose two 64-column halves are
+// summed afterwards.
 #include <cmath>
 #include <mutex>
 
@@ -47,16 +52,17 @@ constexpr int kPreBar = 1;     // named barrier of warps 4-7
 
 // shared memory, from a 1024-byte aligned base
 constexpr uint32_t kBox = 8192;                     // one 64 x 64 bf16 swizzled box
-constexpr uint32_t kKV = 4 * kBox;                  // hi (2 boxes) then lo (2 boxes)
-constexpr uint32_t kOffK = 0;                       // two chunk buffers of k
-constexpr uint32_t kOffV = kOffK + 2 * kKV;         // one chunk buffer of v
+constexpr uint32_t kKV = 4 * kBox;                  // hi, lo of columns 0-63, then of 64-127
+constexpr int kKBufs = 3;                           // chunk buffers of k (and its gates)
+constexpr uint32_t kOffK = 0;
+constexpr uint32_t kOffV = kOffK + kKBufs * kKV;    // one chunk buffer of v
 constexpr uint32_t kOffT = kOffV + kKV;             // T diag(b g) hi, lo; T diag(b) hi, lo
 constexpr uint32_t kOffW = kOffT + 4 * kBox;        // -W hi, lo: [j][t] rows (MN-major B)
-constexpr uint32_t kOffGateRaw = kOffW + 4 * kBox;  // two buffers: alpha[64], beta[64]
-constexpr uint32_t kOffGate = kOffGateRaw + 2 * 512;  // two slots: beta, b g, decay, G
-constexpr uint32_t kOffScr = kOffGate + 2 * 1024;     // B, T: [64][65] f32 each
-constexpr int kLd = 65;
-constexpr uint32_t kOffBar = kOffScr + 2 * kC * kLd * 4;
+constexpr uint32_t kOffGateRaw = kOffW + 4 * kBox;  // per k buffer: alpha[64], beta[64]
+constexpr uint32_t kOffGate = kOffGateRaw + kKBufs * 512;  // three slots: beta, b g, decay, G2
+constexpr uint32_t kOffScr = kOffGate + 3 * 1024;          // B, then T in place: [64][68] f32
+constexpr int kLd = 68;  // 16-byte rows; 8 consecutive rows cover all banks
+constexpr uint32_t kOffBar = kOffScr + kC * kLd * 4;
 constexpr uint32_t kStateSmem = kOffBar + 256 + 1024;
 static_assert(kStateSmem <= 232448, "state kernel shared memory");
 
@@ -64,28 +70,33 @@ static_assert(kStateSmem <= 232448, "state kernel shared memory");
 constexpr uint32_t kColS = 0;     // S (f32, 128)
 constexpr uint32_t kColSh = 128;  // S bf16 high parts (64 columns = 128 values)
 constexpr uint32_t kColSl = 192;  // S bf16 remainders
-constexpr uint32_t kColN = 256;   // U^T, then NEW^T (f32, 64)
-constexpr uint32_t kColNh = 320;  // NEW'^T bf16 high parts (32 columns)
-constexpr uint32_t kColNl = 352;  // NEW'^T remainders
-constexpr uint32_t kColP = 384;   // P = K K^T, then W^T (f32, 64)
+constexpr uint32_t kColN = 256;   // U^T, then NEW^T, as two 64-column parts to be summed
+constexpr uint32_t kColNh = 256;  // NEW'^T bf16 high parts (32 columns, over the read NEW^T)
+constexpr uint32_t kColNl = 320;  // NEW'^T remainders (over the read second part)
+constexpr uint32_t kColP = 384;   // P = K K^T (f32, 64; rows 0-63)
+constexpr uint32_t kColW = 448;   // W^T (f32, 64)
 
 // barriers
 enum : int {
-  kBarKFull = 0,   // 2: k + gates of a chunk landed
-  kBarKEmpty = 2,  // 2: the chunk's last product that reads k is done
-  kBarVFull = 4,
-  kBarVEmpty = 5,
-  kBarP = 6,       // P done
-  kBarUW = 7,      // U^T and W^T done
-  kBarDA = 8,      // NEW^T done
-  kBarDB = 9,      // S update done
-  kBarTops = 10,   // T operands written (4 warp arrivals)
-  kBarWop = 11,    // -W operand written
-  kBarNop = 12,    // NEW' operand written
-  kBarSops = 13,   // S operand written and S pre-scaled
-  kBarFinal = 14,
-  kNumBars = 15,
+  kBarKFull = 0,   // 3: k + gates of a chunk landed
+  kBarKEmpty = 3,  // 3: the chunk's last product that reads k is done
+  kBarVFull = 6,
+  kBarVEmpty = 7,
+  kBarP = 8,       // P done
+  kBarUW = 9,      // U^T and W^T done
+  kBarDA = 10,     // NEW^T done
+  kBarDB = 11,     // S update done
+  kBarTops = 12,   // T operands written (4 warp arrivals)
+  kBarWop = 13,    // -W operand written (4 warp arrivals)
+  kBarNop = 14,    // NEW' operand written (4 warp arrivals)
+  kBarSops = 15,   // S operand written and S pre-scaled (4 warp arrivals)
+  kBarFinal = 16,
+  kBarPfree = 17,  // P read out of TMEM (4 warp arrivals)
+  kNumBars = 18,
 };
+
+// gates are kept in log2 units; a gate below 2^-115 counts as 2^-115
+constexpr float kMinLog2Gate = -115.f;
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {
   return static_cast<uint32_t>(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -109,20 +120,45 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
   lo = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
 }
 
-// log of the chunk's total decay: warp-wide sum of log alpha over its n rows
-__device__ __forceinline__ float chunk_log_decay(const float* alpha, int n, int lane) {
+// log2 of the chunk's total decay: warp-wide sum of log2 alpha over its n rows
+__device__ __forceinline__ float chunk_log2_decay(const float* alpha, int n, int lane) {
   float s = 0.f;
-  for (int t = lane; t < n; t += 32) s += fmaxf(logf(alpha[t]), -80.f);
+  for (int t = lane; t < n; t += 32) s += fmaxf(log2f(alpha[t]), kMinLog2Gate);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
   return s;
 }
 
-// the three split terms of one product: hi.hi, hi.lo, lo.hi
-struct Split {
-  uint32_t a[3];
-  uint32_t b[3];
-};
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ float4 fma4(float a, float4 b, float4 c) {
+  return make_float4(fmaf(a, b.x, c.x), fmaf(a, b.y, c.y), fmaf(a, b.z, c.z), fmaf(a, b.w, c.w));
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 2 x 4 tile (rows r and r + 8, columns 4 cg .. 4 cg + 3) of the product of
+// the 16 x (16 n) row panel at A (stride kLd) and the (16 n) x 16 column panel at B.
+template <int N>
+__device__ __forceinline__ void tile_product(const float* A, const float* B, int r, int cg,
+                                             float4& y0, float4& y1) {
+  y0 = make_float4(0.f, 0.f, 0.f, 0.f);
+  y1 = y0;
+#pragma unroll
+  for (int k = 0; k < 16 * N; k += 4) {
+    const float4 a0 = ld4(A + r * kLd + k), a1 = ld4(A + (r + 8) * kLd + k);
+    const float a0v[4] = {a0.x, a0.y, a0.z, a0.w}, a1v[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      const float4 bv = ld4(B + (k + kk) * kLd + 4 * cg);
+      y0 = fma4(a0v[kk], bv, y0);
+      y1 = fma4(a1v[kk], bv, y1);
+    }
+  }
+}
 
 __global__ void __launch_bounds__(kStateThreads, 1)
     gdn_state_kernel(const __grid_constant__ GdnStateParams p) {
@@ -134,7 +170,6 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bar + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   float* Bs = reinterpret_cast<float*>(sm + kOffScr);
-  float* Ts = Bs + kC * kLd;
   float* Xs = reinterpret_cast<float*>(sm + kOffT);  // scratch while T is formed
 
   const int h = blockIdx.x, l = blockIdx.y;
@@ -156,6 +191,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     mbar_init(&bar[kBarWop], 4);
     mbar_init(&bar[kBarNop], 4);
     mbar_init(&bar[kBarSops], 4);
+    mbar_init(&bar[kBarPfree], 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -170,14 +206,16 @@ __global__ void __launch_bounds__(kStateThreads, 1)
 
   if (warp == 9) {
     // ---------------------------------------------------------------- producer
+    // lane 0 streams k (and the gates), lane 1 streams v: k runs ahead by its
+    // three buffers, v by one
     if (lane == 0 && nch > 0) {
       tma_prefetch(&p.tmK);
-      tma_prefetch(&p.tmV);
-      int loaded_k = 0, loaded_v = 0;
+      int loaded = 0;
       bool ok = true;
-      for (int c = 0; c < nch && ok; ++c) {
-        const int kb = c & 1;
-        if (c >= 2 && !mbar_wait(&bar[kBarKEmpty + kb], ((c - 2) >> 1) & 1, abort_flag, p.err, kErrGdn)) {
+      for (int c = 0; c < nch; ++c) {
+        const int kb = c % kKBufs;
+        if (c >= kKBufs &&
+            !mbar_wait(&bar[kBarKEmpty + kb], ((c - kKBufs) / kKBufs) & 1, abort_flag, p.err, kErrGdn)) {
           ok = false;
           break;
         }
@@ -185,11 +223,20 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         mbar_expect_tx(kf, kKV + 512);
         for (int part = 0; part < 2; ++part)
           for (int box = 0; box < 2; ++box)
-            tma_load_3d(sb + kOffK + kb * kKV + part * 2 * kBox + box * kBox, &p.tmK, kf, 64 * box,
+            tma_load_3d(sb + kOffK + kb * kKV + box * 2 * kBox + part * kBox, &p.tmK, kf, 64 * box,
                         kC * c, 2 * lh + part);
         bulk_load(sb + kOffGateRaw + kb * 512, alpha_g + kC * c, 256, kf);
         bulk_load(sb + kOffGateRaw + kb * 512 + 256, beta_g + kC * c, 256, kf);
-        loaded_k = c + 1;
+        loaded = c + 1;
+      }
+      if (!ok)  // let the copies already issued land before the CTA exits
+        for (int c = loaded - kKBufs < 0 ? 0 : loaded - kKBufs; c < loaded; ++c)
+          mbar_drain(&bar[kBarKFull + c % kKBufs], (c / kKBufs) & 1);
+    } else if (lane == 1 && nch > 0) {
+      tma_prefetch(&p.tmV);
+      int loaded = 0;
+      bool ok = true;
+      for (int c = 0; c < nch; ++c) {
         if (c >= 1 && !mbar_wait(&bar[kBarVEmpty], (c - 1) & 1, abort_flag, p.err, kErrGdn)) {
           ok = false;
           break;
@@ -198,105 +245,120 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         mbar_expect_tx(vf, kKV);
         for (int part = 0; part < 2; ++part)
           for (int box = 0; box < 2; ++box)
-            tma_load_3d(sb + kOffV + part * 2 * kBox + box * kBox, &p.tmV, vf, 64 * box, kC * c,
+            tma_load_3d(sb + kOffV + box * 2 * kBox + part * kBox, &p.tmV, vf, 64 * box, kC * c,
                         2 * lh + part);
-        loaded_v = c + 1;
+        loaded = c + 1;
       }
-      if (!ok) {  // let the copies already issued land before the CTA exits
-        for (int c = loaded_k - 2 < 0 ? 0 : loaded_k - 2; c < loaded_k; ++c)
-          mbar_drain(&bar[kBarKFull + (c & 1)], (c >> 1) & 1);
-        if (loaded_v > 0) mbar_drain(&bar[kBarVFull], (loaded_v - 1) & 1);
-      }
+      if (!ok && loaded > 0) mbar_drain(&bar[kBarVFull], (loaded - 1) & 1);
     }
   } else if (warp == 8) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0 && nch > 0) {
       const uint32_t id_p = idesc_bf16_f32(128, 64);
       const uint32_t id_uw = idesc_bf16_f32(128, 64) | (1u << 15);
+      const uint32_t id_u2 = idesc_bf16_f32(128, 128) | (1u << 15);
       const uint32_t id_da = idesc_bf16_f32(128, 64) | (1u << 16);
+      const uint32_t id_da2 = idesc_bf16_f32(128, 128) | (1u << 16);
       const uint32_t id_db = idesc_bf16_f32(128, 128) | (1u << 16);
-      auto wait = [&](int b, uint32_t parity) -> bool {
-        const bool ok = mbar_wait(&bar[b], parity, abort_flag, p.err, kErrGdn);
-        tc_fence_after();
-        return ok;
-      };
-      // P = K K^T: A = the k tile read as 128 K-major rows (rows 64-127 are not used)
+      // descriptors of shared-memory offset 0; an operand at byte offset `o` adds o >> 4
+      const uint64_t dk = sdesc_kmajor_sw128(sb);
+      const uint64_t dm = sdesc_mnmajor_sw128(sb, 2 * kBox);  // 64-column blocks 16 KB apart
+      int p_next = 0;  // next chunk whose P = K K^T is still to be issued
+      // P = K K^T with A = [K_hi; K_lo] (128 K-major rows: a box of high parts and
+      // the box of remainders after it) and B = K_hi, then K_lo: rows 0-63 of the
+      // result hold K_hi K^T, rows 64-127 K_lo K^T; their sum is P.
       auto issue_p = [&](int c) {
-        const uint32_t kt = sb + kOffK + (c & 1) * kKV;
-        const uint32_t ah[3] = {kt, kt, kt + 2 * kBox};
-        const uint32_t bh[3] = {kt, kt + 2 * kBox, kt};
-        uint32_t acc = 0;
-        for (int g = 0; g < 3; ++g)
+        const uint64_t kd = dk + ((kOffK + (c % kKBufs) * kKV) >> 4);
+#pragma unroll
+        for (int g = 0; g < 2; ++g)
+#pragma unroll
           for (int kblk = 0; kblk < 2; ++kblk)
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = sdesc_kmajor_sw128(ah[g] + kblk * kBox + 32 * ks);
-              const uint64_t bd = sdesc_kmajor_sw128(bh[g] + kblk * kBox + 32 * ks);
-              mma_bf16(tb + kColP, ad, bd, id_p, acc);
-              acc = 1;
+              const uint32_t o = (kblk * 2 * kBox + 32 * ks) >> 4;
+              mma_bf16(tb + kColP, kd + o, kd + o + (g == 1 ? kBox >> 4 : 0), id_p,
+                       (g | kblk | ks) != 0 ? 1u : 0u);
             }
         mma_commit(&bar[kBarP]);
       };
-      // U^T = V^T (T diag(b))^T and W^T = K^T (T diag(b g))^T
+      // P of the next chunk needs only its keys and the P columns (free once the
+      // previous P has been read out); it is issued while waiting for anything else.
+      auto try_p = [&]() {
+        if (p_next < nch && (p_next == 0 || mbar_poll(&bar[kBarPfree], (p_next - 1) & 1)) &&
+            mbar_poll(&bar[kBarKFull + p_next % kKBufs], (p_next / kKBufs) & 1)) {
+          tc_fence_after();
+          issue_p(p_next);
+          ++p_next;
+        }
+      };
+      auto wait = [&](int b, uint32_t parity) -> bool {
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          if (mbar_test_for(&bar[b], parity, 200)) break;
+          try_p();
+          if (*abort_flag) return false;
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicCAS(p.err, 0, kErrGdn);
+            return false;
+          }
+        }
+        tc_fence_after();
+        return true;
+      };
+      // U^T = V^T (T diag(b))^T into two 64-column parts (V_hi [T_hi | T_lo]^T as one
+      // N = 128 product, plus V_lo T_hi^T on the first part) and
+      // W^T = K^T (T diag(b g))^T (three split terms)
       auto issue_uw = [&](int c) {
-        const uint32_t kt = sb + kOffK + (c & 1) * kKV, vt = sb + kOffV;
-        const uint32_t tw = sb + kOffT, tu = sb + kOffT + 2 * kBox;
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t at = which == 0 ? vt : kt;
-          const uint32_t bt = which == 0 ? tu : tw;
-          const uint32_t dcol = which == 0 ? kColN : kColP;
-          const uint32_t ah[3] = {at, at, at + 2 * kBox};
-          const uint32_t bh[3] = {bt, bt + kBox, bt};
-          uint32_t acc = 0;
-          for (int g = 0; g < 3; ++g)
+        const uint64_t vd = dm + (kOffV >> 4);
+        const uint64_t kd = dm + ((kOffK + (c % kKBufs) * kKV) >> 4);
+        const uint64_t tu = dk + ((kOffT + 2 * kBox) >> 4), tw = dk + (kOffT >> 4);
 #pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint64_t ad = sdesc_mnmajor_sw128(ah[g] + 2048 * ks, 8192);
-              const uint64_t bd = sdesc_kmajor_sw128(bh[g] + 32 * ks);
-              mma_bf16(tb + dcol, ad, bd, id_uw, acc);
-              acc = 1;
-            }
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tb + kColN, vd + ((2048 * ks) >> 4), tu + ((32 * ks) >> 4), id_u2, ks != 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          mma_bf16(tb + kColN, vd + (kBox >> 4) + ((2048 * ks) >> 4), tu + ((32 * ks) >> 4), id_uw, 1u);
+#pragma unroll
+        for (int g = 0; g < 3; ++g) {
+          const uint64_t ad = kd + (g == 2 ? kBox >> 4 : 0);
+          const uint64_t bd = tw + (g == 1 ? kBox >> 4 : 0);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_bf16(tb + kColW, ad + ((2048 * ks) >> 4), bd + ((32 * ks) >> 4), id_uw,
+                     (g | ks) != 0 ? 1u : 0u);
         }
         mma_commit(&bar[kBarUW]);
         mma_commit(&bar[kBarVEmpty]);
       };
-      bool ok = wait(kBarKFull, 0);
-      if (ok) issue_p(0);
-      ok = ok && wait(kBarTops, 0) && wait(kBarVFull, 0);
-      if (ok) issue_uw(0);
+      bool ok = true;
       for (int c = 0; c < nch && ok; ++c) {
+        if (!wait(kBarTops, c & 1) || !wait(kBarVFull, c & 1)) break;
+        issue_uw(c);
         if (!wait(kBarWop, c & 1) || !wait(kBarSops, c & 1)) break;
-        {  // NEW^T += S_0 (-W)^T, added to U^T
-          const uint32_t wt = sb + kOffW;
-          const uint32_t ah[3] = {tb + kColSh, tb + kColSh, tb + kColSl};
-          const uint32_t bh[3] = {wt, wt + 2 * kBox, wt};
-          for (int g = 0; g < 3; ++g)
+        {  // NEW^T += S_0 (-W)^T on U^T: S_hi [-W_hi | -W_lo]^T (N = 128) and S_lo (-W_hi)^T
+          const uint64_t wd = dm + (kOffW >> 4);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              mma_bf16_tmem_a(tb + kColN, ah[g] + 8 * ks, sdesc_mnmajor_sw128(bh[g] + 2048 * ks, 8192),
-                              id_da, 1u);
+          for (int ks = 0; ks < 8; ++ks)
+            mma_bf16_tmem_a(tb + kColN, tb + kColSh + 8 * ks, wd + ((2048 * ks) >> 4), id_da2, 1u);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks)
+            mma_bf16_tmem_a(tb + kColN, tb + kColSl + 8 * ks, wd + ((2048 * ks) >> 4), id_da, 1u);
           mma_commit(&bar[kBarDA]);
-        }
-        if (c + 1 < nch) {
-          if (!wait(kBarKFull + ((c + 1) & 1), ((c + 1) >> 1) & 1)) break;
-          issue_p(c + 1);
         }
         if (!wait(kBarNop, c & 1)) break;
         {  // S += NEW'^T K
-          const uint32_t kt = sb + kOffK + (c & 1) * kKV;
-          const uint32_t ah[3] = {tb + kColNh, tb + kColNh, tb + kColNl};
-          const uint32_t bh[3] = {kt, kt + 2 * kBox, kt};
-          for (int g = 0; g < 3; ++g)
+          const uint64_t kd = dm + ((kOffK + (c % kKBufs) * kKV) >> 4);
+#pragma unroll
+          for (int g = 0; g < 3; ++g) {
+            const uint32_t at = tb + (g == 2 ? kColNl : kColNh);
+            const uint64_t bd = kd + (g == 1 ? kBox >> 4 : 0);
 #pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-              mma_bf16_tmem_a(tb + kColS, ah[g] + 8 * ks, sdesc_mnmajor_sw128(bh[g] + 2048 * ks, 8192),
-                              id_db, 1u);
+              mma_bf16_tmem_a(tb + kColS, at + 8 * ks, bd + ((2048 * ks) >> 4), id_db, 1u);
+          }
           mma_commit(&bar[kBarDB]);
-          mma_commit(&bar[kBarKEmpty + (c & 1)]);
-        }
-        if (c + 1 < nch) {
-          if (!wait(kBarTops, (c + 1) & 1) || !wait(kBarVFull, (c + 1) & 1)) break;
-          issue_uw(c + 1);
+          mma_commit(&bar[kBarKEmpty + c % kKBufs]);
         }
       }
       // every MMA issued has finished before TMEM is released
@@ -307,111 +369,174 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     // ---------------------------------------------------------------- chunk-local work
     const int pt = tid - 128;  // 0..127, TMEM lane of this thread
     const int q = warp - 4;
-    for (int c = 0; c < nch; ++c) {
-      const int kb = c & 1;
-      bool ok = mbar_wait(&bar[kBarKFull + kb], (c >> 1) & 1, abort_flag, p.err, kErrGdn);
-      if (!named_bar_all(kPreBar, 128, ok)) break;
-      float* gs = reinterpret_cast<float*>(sm + kOffGate + kb * 1024);  // beta, bg, dec, G
-      if (q == 0) {
-        const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw + kb * 512);
-        const float* gbeta = ga + 64;
-        const int n = min(kC, p.rows - kC * c);
-        float la[2], be[2];
+    const uint32_t lrow = tb + (static_cast<uint32_t>(32 * q) << 16);
+    // Software pipeline over chunks: the front of chunk c + 1 (gates, B, the
+    // diagonal blocks of T) runs while the products U^T, W^T of chunk c are on
+    // the tensor cores; the rest of T needs the T-operand tiles they read.
+    auto gates = [&](int c, float* gs) {
+      const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw + (c % kKBufs) * 512);
+      const float* gbeta = ga + 64;
+      const int n = min(kC, p.rows - kC * c);
+      float la[2], be[2];
 #pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int t = 2 * lane + e;
-          la[e] = t < n ? fmaxf(logf(ga[t]), -80.f) : 0.f;
-          be[e] = t < n ? gbeta[t] : 0.f;
-        }
-        const float pair = la[0] + la[1];
-        float incl = pair;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const float g0 = incl - la[1], g1 = incl;
-        const float gC = __shfl_sync(0xffffffffu, incl, 31);
-        gs[2 * lane] = be[0];
-        gs[2 * lane + 1] = be[1];
-        gs[64 + 2 * lane] = be[0] * expf(g0);
-        gs[64 + 2 * lane + 1] = be[1] * expf(g1);
-        gs[128 + 2 * lane] = expf(gC - g0);
-        gs[128 + 2 * lane + 1] = expf(gC - g1);
-        gs[192 + 2 * lane] = g0;
-        gs[192 + 2 * lane + 1] = g1;
+      for (int e = 0; e < 2; ++e) {
+        const int t = 2 * lane + e;
+        la[e] = t < n ? fmaxf(log2f(ga[t]), kMinLog2Gate) : 0.f;
+        be[e] = t < n ? gbeta[t] : 0.f;
       }
-      ok = mbar_wait(&bar[kBarP], c & 1, abort_flag, p.err, kErrGdn);
-      if (!named_bar_all(kPreBar, 128, ok)) break;
-      tc_fence_after();
-      // B_ts = b_t e^{G_t - G_s} P_ts below the diagonal
-      if (q < 2) {
-        const int t = pt;
-        const float gt = gs[192 + t], bt = gs[t];
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tmem_ld32(tb + (static_cast<uint32_t>(32 * q) << 16) + kColP + 32 * half, r);
-          tmem_wait_ld();
+      const float pair = la[0] + la[1];
+      float incl = pair;
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int s = 32 * half + j;
-            Bs[t * kLd + s] = s < t ? bt * expf(gt - gs[192 + s]) * __uint_as_float(r[j]) : 0.f;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const float g0 = incl - la[1], g1 = incl;
+      const float gC = __shfl_sync(0xffffffffu, incl, 31);
+      gs[2 * lane] = be[0];
+      gs[2 * lane + 1] = be[1];
+      gs[64 + 2 * lane] = be[0] * exp2f(g0);
+      gs[64 + 2 * lane + 1] = be[1] * exp2f(g1);
+      gs[128 + 2 * lane] = exp2f(gC - g0);
+      gs[128 + 2 * lane + 1] = exp2f(gC - g1);
+      gs[192 + 2 * lane] = g0;
+      gs[192 + 2 * lane + 1] = g1;
+    };
+    // gates, B and the diagonal blocks of T for chunk c
+    auto front = [&](int c) -> bool {
+      bool ok = mbar_wait(&bar[kBarKFull + c % kKBufs], (c / kKBufs) & 1, abort_flag, p.err, kErrGdn);
+      if (!named_bar_all(kPreBar, 128, ok)) return false;
+      float* gs = reinterpret_cast<float*>(sm + kOffGate + (c % 3) * 1024);  // beta, bg, dec, G2
+      if (c == 0 && q == 0) gates(0, gs);  // later chunks: computed during the previous chunk
+      ok = mbar_wait(&bar[kBarP], c & 1, abort_flag, p.err, kErrGdn);
+      if (!named_bar_all(kPreBar, 128, ok)) return false;
+      tc_fence_after();
+      // B_ts = b_t 2^{G2_t - G2_s} P_ts below the diagonal.  Lane t < 64 holds
+      // (K_hi K^T)[t], lane 64 + t (K_lo K^T)[t]: warps 4-5 finish columns 0-31 and
+      // warps 6-7 columns 32-63, each first leaving the other half in B's row.
+      {
+        const int t = pt & 63;
+        const bool lowq = q < 2;
+        const int own = lowq ? 0 : 32;  // columns this thread finishes
+        uint32_t r[2][32];
+        tmem_ld32(lrow + kColP, r[0]);
+        tmem_ld32(lrow + kColP + 32, r[1]);
+        tmem_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kBarPfree]);
+        uint32_t keep[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) keep[j] = lowq ? r[0][j] : r[1][j];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = __uint_as_float(lowq ? r[1][j + e] : r[0][j + e]);
+          st4(Bs + t * kLd + (32 - own) + j, make_float4(v[0], v[1], v[2], v[3]));
+        }
+        named_bar_sync(kPreBar, 128);
+        const float gt = gs[192 + t], bt = gs[t];
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          const int s0 = own + j;
+          const float4 other = ld4(Bs + t * kLd + s0);
+          const float4 gsv = ld4(gs + 192 + s0);
+          const float ov[4] = {other.x, other.y, other.z, other.w};
+          const float g4[4] = {gsv.x, gsv.y, gsv.z, gsv.w};
+          float v[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float pts = __uint_as_float(keep[j + e]) + ov[e];
+            v[e] = s0 + e < t ? bt * ex2(gt - g4[e]) * pts : 0.f;
           }
+          st4(Bs + t * kLd + s0, make_float4(v[0], v[1], v[2], v[3]));
         }
       }
       named_bar_sync(kPreBar, 128);
-      // T = (I + B)^-1, unit lower triangular, by 16 x 16 blocks: diagonal blocks
-      // by substitution, then block diagonals a - b = 1, 2, 3:
-      //   T_ab = -T_aa sum_{c=b}^{a-1} B_ac T_cb
+      // T = (I + B)^-1, unit lower triangular: the 16 x 16 diagonal blocks by substitution
       if (pt < 64) {
         const int b = pt >> 4, s = pt & 15, o = 16 * b;
         float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
+          float brow[16];
+#pragma unroll
+          for (int k4 = 0; k4 < 16; k4 += 4) {
+            const float4 v = ld4(Bs + (o + r) * kLd + o + k4);
+            brow[k4] = v.x; brow[k4 + 1] = v.y; brow[k4 + 2] = v.z; brow[k4 + 3] = v.w;
+          }
           float acc = r == s ? 1.f : 0.f;
 #pragma unroll
-          for (int k = 0; k < r; ++k) acc = fmaf(-Bs[(o + r) * kLd + o + k], x[k], acc);
+          for (int k = 0; k < r; ++k) acc = fmaf(-brow[k], x[k], acc);
           x[r] = acc;
         }
+        named_bar_sync(kPreBar + 1, 64);  // all columns are computed before B_bb is overwritten
 #pragma unroll
-        for (int r = 0; r < 16; ++r) Ts[(o + r) * kLd + o + s] = x[r];
+        for (int r = 0; r < 16; ++r) Bs[(o + r) * kLd + o + s] = x[r];
       }
       named_bar_sync(kPreBar, 128);
-      for (int d = 1; d < 4; ++d) {
-        const int nel = (4 - d) * 256;
-        for (int idx = pt; idx < nel; idx += 128) {
-          const int b = idx >> 8, e = idx & 255, r = e >> 4, cc = e & 15, a = b + d;
-          float acc = 0.f;
-          for (int c2 = b; c2 < a; ++c2) {
-            const float* brow = Bs + (16 * a + r) * kLd + 16 * c2;
-            const float* tcol = Ts + (16 * c2) * kLd + 16 * b + cc;
-#pragma unroll
-            for (int k = 0; k < 16; ++k) acc = fmaf(brow[k], tcol[k * kLd], acc);
-          }
-          Xs[(16 * a + r) * kLd + 16 * b + cc] = acc;
+      return true;
+    };
+    // the rest of T, then T diag(b g) and T diag(b) as bf16 hi/lo K-major tiles [t][s]
+    auto back = [&](int c) -> bool {
+      const float* gs = reinterpret_cast<const float*>(sm + kOffGate + (c % 3) * 1024);
+      if (c > 0) {  // the T-operand area (scratch X here) is free once U^T, W^T of c - 1 are done
+        const bool ok = mbar_wait(&bar[kBarUW], (c - 1) & 1, abort_flag, p.err, kErrGdn);
+        if (!named_bar_all(kPreBar, 128, ok)) return false;
+      }
+      // warp 6, idle in the first block step below, prepares the next chunk's gates
+      // (read again only after the next chunk's keys are waited for by every warp)
+      if (q == 2 && c + 1 < nch &&
+          mbar_wait(&bar[kBarKFull + (c + 1) % kKBufs], ((c + 1) / kKBufs) & 1, abort_flag, p.err,
+                    kErrGdn))
+        gates(c + 1, reinterpret_cast<float*>(sm + kOffGate + ((c + 1) % 3) * 1024));
+      {
+        // 32 x 32 halves: T_10 = -T_11 B_10 T_00 and T_32 = -T_33 B_32 T_22
+        const int r = (pt & 31) >> 2, cg = pt & 3;
+        const int a = pt < 32 ? 1 : 3, b = a - 1;
+        float4 y0, y1;
+        if (pt < 64) {
+          tile_product<1>(Bs + (16 * a) * kLd + 16 * b, Bs + (16 * b) * kLd + 16 * b, r, cg, y0, y1);
+          st4(Xs + (16 * a + r) * kLd + 16 * b + 4 * cg, y0);
+          st4(Xs + (16 * a + r + 8) * kLd + 16 * b + 4 * cg, y1);
         }
         named_bar_sync(kPreBar, 128);
-        for (int idx = pt; idx < nel; idx += 128) {
-          const int b = idx >> 8, e = idx & 255, r = e >> 4, cc = e & 15, a = b + d;
-          const float* trow = Ts + (16 * a + r) * kLd + 16 * a;
-          const float* xcol = Xs + (16 * a) * kLd + 16 * b + cc;
-          float acc = 0.f;
-#pragma unroll
-          for (int k = 0; k < 16; ++k) acc = fmaf(trow[k], xcol[k * kLd], acc);
-          Ts[(16 * a + r) * kLd + 16 * b + cc] = -acc;
+        if (pt < 64) {
+          tile_product<1>(Bs + (16 * a) * kLd + 16 * a, Xs + (16 * a) * kLd + 16 * b, r, cg, y0, y1);
+          st4(Bs + (16 * a + r) * kLd + 16 * b + 4 * cg, make_float4(-y0.x, -y0.y, -y0.z, -y0.w));
+          st4(Bs + (16 * a + r + 8) * kLd + 16 * b + 4 * cg, make_float4(-y1.x, -y1.y, -y1.z, -y1.w));
         }
+        named_bar_sync(kPreBar, 128);
+        // the 64 x 64 whole: T[32:64, 0:32] = -T[32:64, 32:64] B[32:64, 0:32] T[0:32, 0:32]
+        const int blk = pt >> 5, a2 = 2 + (blk >> 1), b2 = blk & 1;
+        tile_product<2>(Bs + (16 * a2) * kLd, Bs + 16 * b2, r, cg, y0, y1);
+        st4(Xs + (16 * a2 + r) * kLd + 16 * b2 + 4 * cg, y0);
+        st4(Xs + (16 * a2 + r + 8) * kLd + 16 * b2 + 4 * cg, y1);
+        named_bar_sync(kPreBar, 128);
+        tile_product<2>(Bs + (16 * a2) * kLd + 32, Xs + 32 * kLd + 16 * b2, r, cg, y0, y1);
+        st4(Bs + (16 * a2 + r) * kLd + 16 * b2 + 4 * cg, make_float4(-y0.x, -y0.y, -y0.z, -y0.w));
+        st4(Bs + (16 * a2 + r + 8) * kLd + 16 * b2 + 4 * cg, make_float4(-y1.x, -y1.y, -y1.z, -y1.w));
         named_bar_sync(kPreBar, 128);
       }
-      // T diag(b g) and T diag(b) as bf16 hi/lo K-major tiles [t][s]
-      for (int idx = pt; idx < kC * 8; idx += 128) {
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const int idx = pt + 128 * m;
         const int t = idx >> 3, ch = idx & 7;
         float w[8], u[8];
+        {
+          const float4 t0 = ld4(Bs + t * kLd + 8 * ch), t1 = ld4(Bs + t * kLd + 8 * ch + 4);
+          const float4 w0 = ld4(gs + 64 + 8 * ch), w1 = ld4(gs + 64 + 8 * ch + 4);
+          const float4 u0 = ld4(gs + 8 * ch), u1 = ld4(gs + 8 * ch + 4);
+          const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+          const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+          const float uv[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int s = 8 * ch + e;
-          const float v = s <= t ? Ts[t * kLd + s] : 0.f;
-          w[e] = v * gs[64 + s];
-          u[e] = v * gs[s];
+          for (int e = 0; e < 8; ++e) {
+            const float v = 8 * ch + e <= t ? tv[e] : 0.f;
+            w[e] = v * wv[e];
+            u[e] = v * uv[e];
+          }
         }
         uint4 hi, lo;
         const uint32_t off = swz(t, ch);
@@ -426,33 +551,13 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kBarTops]);
-      // -W as the MN-major B operand: row j holds W^T[j][0..63]
-      ok = mbar_wait(&bar[kBarUW], c & 1, abort_flag, p.err, kErrGdn);
-      if (!named_bar_all(kPreBar, 128, ok)) break;
-      tc_fence_after();
-      {
-        const int j = pt;
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tmem_ld32(tb + (static_cast<uint32_t>(32 * q) << 16) + kColP + 32 * half, r);
-          tmem_wait_ld();
-#pragma unroll
-          for (int c8 = 0; c8 < 4; ++c8) {
-            float x[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = -__uint_as_float(r[8 * c8 + e]);
-            uint4 hi, lo;
-            split8(x, hi, lo);
-            const uint32_t off = swz(j, 4 * half + c8);
-            *reinterpret_cast<uint4*>(sm + kOffW + off) = hi;
-            *reinterpret_cast<uint4*>(sm + kOffW + 2 * kBox + off) = lo;
-          }
-        }
+      return true;
+    };
+    if (nch > 0 && front(0)) {
+      for (int c = 0; c < nch; ++c) {
+        if (!back(c)) break;
+        if (c + 1 < nch && !front(c + 1)) break;
       }
-      fence_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bar[kBarWop]);
     }
   } else {
     // ---------------------------------------------------------------- serial part
@@ -460,19 +565,21 @@ __global__ void __launch_bounds__(kStateThreads, 1)
     const uint32_t lrow = tb + (static_cast<uint32_t>(32 * warp) << 16);
     const float* src = s_in != nullptr ? s_in + static_cast<size_t>(i) * kDk : nullptr;
     float* dst = s_out + static_cast<size_t>(i) * kDk;
-    // S (f32, pre-scaled by the next chunk's decay g) and its bf16 split, 64 columns at a time
-    auto put_state = [&](const float (&s)[64], int half, float g) {
-      uint32_t r[32], hi[32], lo[32];
+    // 64 columns of S: the bf16 split (operand of the next chunk) and S times the
+    // next chunk's total decay g (the accumulator the next update adds to)
+    auto put_state = [&](uint32_t (&r)[2][32], int half, float g) {
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
+        uint32_t hi[16], lo[16];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(g * s[32 * cc + j]);
-        tmem_st32(lrow + kColS + 64 * half + 32 * cc, r);
+        for (int m = 0; m < 16; ++m)
+          split2(__uint_as_float(r[cc][2 * m]), __uint_as_float(r[cc][2 * m + 1]), hi[m], lo[m]);
+        tmem_st16(lrow + kColSh + 32 * half + 16 * cc, hi);
+        tmem_st16(lrow + kColSl + 32 * half + 16 * cc, lo);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[cc][j] = __float_as_uint(g * __uint_as_float(r[cc][j]));
+        tmem_st32(lrow + kColS + 64 * half + 32 * cc, r[cc]);
       }
-#pragma unroll
-      for (int m = 0; m < 32; ++m) split2(s[2 * m], s[2 * m + 1], hi[m], lo[m]);
-      tmem_st32(lrow + kColSh + 32 * half, hi);
-      tmem_st32(lrow + kColSl + 32 * half, lo);
     };
     bool ok = true;
     if (nch == 0) {
@@ -483,16 +590,19 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       ok = mbar_wait(&bar[kBarKFull], 0, abort_flag, p.err, kErrGdn);
       if (ok) {
         const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw);
-        const float g = expf(chunk_log_decay(ga, min(kC, p.rows), lane));
+        const float g = exp2f(chunk_log2_decay(ga, min(kC, p.rows), lane));
         for (int half = 0; half < 2; ++half) {
-          float s[64];
+          uint32_t r[2][32];
 #pragma unroll
           for (int j = 0; j < 64; j += 4) {
             const float4 x = src != nullptr ? *reinterpret_cast<const float4*>(src + 64 * half + j)
                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-            s[j] = x.x; s[j + 1] = x.y; s[j + 2] = x.z; s[j + 3] = x.w;
+            r[j >> 5][j & 31] = __float_as_uint(x.x);
+            r[j >> 5][(j & 31) + 1] = __float_as_uint(x.y);
+            r[j >> 5][(j & 31) + 2] = __float_as_uint(x.z);
+            r[j >> 5][(j & 31) + 3] = __float_as_uint(x.w);
           }
-          put_state(s, half, g);
+          put_state(r, half, g);
         }
         tmem_wait_st();
         tc_fence_before();
@@ -501,59 +611,87 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       }
     }
     for (int c = 0; c < nch && ok; ++c) {
-      const int kb = c & 1;
+      {  // -W as the MN-major B operand of NEW^T: row j holds W^T[j][0..63]
+        if (!mbar_wait(&bar[kBarUW], c & 1, abort_flag, p.err, kErrGdn)) break;
+        tc_fence_after();
+        uint32_t r[2][32];
+        tmem_ld32(lrow + kColW, r[0]);
+        tmem_ld32(lrow + kColW + 32, r[1]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          float x[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) x[e] = -__uint_as_float(r[c8 >> 2][8 * (c8 & 3) + e]);
+          uint4 hi, lo;
+          split8(x, hi, lo);
+          const uint32_t off = swz(i, c8);
+          *reinterpret_cast<uint4*>(sm + kOffW + off) = hi;
+          *reinterpret_cast<uint4*>(sm + kOffW + 2 * kBox + off) = lo;
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bar[kBarWop]);
+      }
       if (!mbar_wait(&bar[kBarDA], c & 1, abort_flag, p.err, kErrGdn)) break;
       tc_fence_after();
-      {  // NEW'^T[i][t] = NEW^T[i][t] e^{G_C - G_t}
-        const float* dec = reinterpret_cast<const float*>(sm + kOffGate + kb * 1024) + 128;
-        uint32_t hi[32], lo[32];
+      {  // NEW'^T[i][t] = NEW^T[i][t] 2^{G2_C - G2_t}
+        const float* dec = reinterpret_cast<const float*>(sm + kOffGate + (c % 3) * 1024) + 128;
+        // t in [32 half, 32 half + 32): both parts are read before the split of the
+        // same t range overwrites them
+#pragma unroll
         for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tmem_ld32(lrow + kColN + 32 * half, r);
+          uint32_t r0[32], r1[32];
+          tmem_ld32(lrow + kColN + 32 * half, r0);
+          tmem_ld32(lrow + kColN + 64 + 32 * half, r1);
           tmem_wait_ld();
+          uint32_t hi[16], lo[16];
 #pragma unroll
           for (int m = 0; m < 16; ++m) {
             const int t = 32 * half + 2 * m;
-            split2(__uint_as_float(r[2 * m]) * dec[t], __uint_as_float(r[2 * m + 1]) * dec[t + 1],
-                   hi[16 * half + m], lo[16 * half + m]);
+            const float y0 = (__uint_as_float(r0[2 * m]) + __uint_as_float(r1[2 * m])) * dec[t];
+            const float y1 = (__uint_as_float(r0[2 * m + 1]) + __uint_as_float(r1[2 * m + 1])) * dec[t + 1];
+            split2(y0, y1, hi[m], lo[m]);
           }
+          tmem_st16(lrow + kColNh + 16 * half, hi);
+          tmem_st16(lrow + kColNl + 16 * half, lo);
         }
-        tmem_st32(lrow + kColNh, hi);
-        tmem_st32(lrow + kColNl, lo);
         tmem_wait_st();
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bar[kBarNop]);
+      // the next chunk's total decay, while the update runs
+      float g = 1.f;
+      if (c + 1 < nch) {
+        const int kn = (c + 1) % kKBufs;
+        if (!mbar_wait(&bar[kBarKFull + kn], ((c + 1) / kKBufs) & 1, abort_flag, p.err, kErrGdn)) break;
+        const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw + kn * 512);
+        g = exp2f(chunk_log2_decay(ga, min(kC, p.rows - kC * (c + 1)), lane));
+      }
       if (!mbar_wait(&bar[kBarDB], c & 1, abort_flag, p.err, kErrGdn)) break;
       tc_fence_after();
       if (c + 1 == nch) {
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t r[32];
-          tmem_ld32(lrow + kColS + 32 * cc, r);
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[2][32];
+          tmem_ld32(lrow + kColS + 64 * half, r[0]);
+          tmem_ld32(lrow + kColS + 64 * half + 32, r[1]);
           tmem_wait_ld();
 #pragma unroll
-          for (int j = 0; j < 32; j += 4)
-            *reinterpret_cast<float4*>(dst + 32 * cc + j) =
-                make_float4(__uint_as_float(r[j]), __uint_as_float(r[j + 1]),
-                            __uint_as_float(r[j + 2]), __uint_as_float(r[j + 3]));
+          for (int j = 0; j < 64; j += 4)
+            *reinterpret_cast<float4*>(dst + 64 * half + j) =
+                make_float4(__uint_as_float(r[j >> 5][j & 31]), __uint_as_float(r[j >> 5][(j & 31) + 1]),
+                            __uint_as_float(r[j >> 5][(j & 31) + 2]),
+                            __uint_as_float(r[j >> 5][(j & 31) + 3]));
         }
       } else {
-        const int kn = (c + 1) & 1;
-        if (!mbar_wait(&bar[kBarKFull + kn], ((c + 1) >> 1) & 1, abort_flag, p.err, kErrGdn)) break;
-        const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw + kn * 512);
-        const float g = expf(chunk_log_decay(ga, min(kC, p.rows - kC * (c + 1)), lane));
         for (int half = 0; half < 2; ++half) {
-          float s[64];
-#pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint32_t r[32];
-            tmem_ld32(lrow + kColS + 64 * half + 32 * cc, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) s[32 * cc + j] = __uint_as_float(r[j]);
-          }
-          put_state(s, half, g);
+          uint32_t r[2][32];
+          tmem_ld32(lrow + kColS + 64 * half, r[0]);
+          tmem_ld32(lrow + kColS + 64 * half + 32, r[1]);
+          tmem_wait_ld();
+          put_state(r, half, g);
         }
         tmem_wait_st();
         tc_fence_before();
