@@ -171,9 +171,8 @@ __device__ __forceinline__ float row_rms_scale(const GemmParams& p, int l, int r
 }
 
 __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
-                            int m, int n, int l, uint64_t* tempty) {
+                            int m, int n, int l, float rs, uint64_t* tempty) {
   const int row = m * kBM + q * 32 + lane;
-  const float rs = row_rms_scale(p, l, row);
   const float posf = static_cast<float>(p.pos_base + row);
   const bool is_k = n < p.n_k_tiles;
   const int hd = p.head_dim;
@@ -232,60 +231,74 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
   }
 }
 
-__device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, int q, int lane, int m, int n,
-                             int l, uint64_t* tempty) {
+// GDN projections: k (L2-normalised per head) and v as bf16 high parts plus
+// bf16 remainders, staged per 64-column half and stored by TMA into the
+// [L, H, 2, rows, 128] planes; the gate tile stores sigmoid(alpha), sigmoid(beta).
+__device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
+                             int m, int n, int l, float rs, uint64_t* tempty) {
   const int row = m * kBM + q * 32 + lane;
-  const float rs = row_rms_scale(p, l, row);
-  const bool valid = row < p.rows;
   const int H = p.gdn_heads;
-  const size_t ra = static_cast<size_t>(p.gdn_rows_alloc);
   if (n < p.n_k_tiles + p.n_v_tiles) {
     const bool is_k = n < p.n_k_tiles;
     const int hpt = p.bn / 128;
     const int head0 = (is_k ? n : n - p.n_k_tiles) * hpt;
-    __nv_bfloat16* base = is_k ? p.gdn_k : p.gdn_v;
+    const CUtensorMap* out = &p.tmO[is_k ? 0 : 1];
     for (int hh = 0; hh < hpt; ++hh) {
       const uint32_t hc = tcol + hh * 128;
       float scale = rs;
       if (is_k) {
         float nrm = 0.f;
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t a[32];
+        for (int c0 = 0; c0 < 128; c0 += 64) {
+          uint32_t a[32], b[32];
           tmem_ld32(hc + c0, a);
+          tmem_ld32(hc + c0 + 32, b);
           tmem_wait_ld();
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float x = f32(a[j]) * rs;
+            const float x = f32(a[j]) * rs, y = f32(b[j]) * rs;
             nrm = fmaf(x, x, nrm);
+            nrm = fmaf(y, y, nrm);
           }
         }
         scale = rs * rsqrtf(nrm + p.l2_eps);
       }
-      // bf16 high part and the bf16 remainder: together about 16 significant bits
-      __nv_bfloat16* hi = base + ((static_cast<size_t>(l) * H + head0 + hh) * 2 * ra + row) * 128;
-      __nv_bfloat16* lo = hi + ra * 128;
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t a[32];
-        tmem_ld32(hc + c0, a);
-        tmem_wait_ld();
-        if (valid) {
+      const int plane = (l * H + head0 + hh) * 2;
+      for (int bx = 0; bx < 2; ++bx) {
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint32_t h[4], r[4];
+        for (int c = 0; c < 2; ++c) {
+          uint32_t a[32];
+          tmem_ld32(hc + 64 * bx + 32 * c, a);
+          tmem_wait_ld();
+          uint32_t wh[16], wl[16];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float x0 = f32(a[j + 2 * e]) * scale, x1 = f32(a[j + 2 * e + 1]) * scale;
-              const __nv_bfloat162 hv = __floats2bfloat162_rn(x0, x1);
-              h[e] = *reinterpret_cast<const uint32_t*>(&hv);
-              r[e] = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
-            }
-            *reinterpret_cast<uint4*>(hi + c0 + j) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4*>(lo + c0 + j) = make_uint4(r[0], r[1], r[2], r[3]);
+          for (int j = 0; j < 32; j += 2) {
+            const float x0 = f32(a[j]) * scale, x1 = f32(a[j + 1]) * scale;
+            const __nv_bfloat162 hv = __floats2bfloat162_rn(x0, x1);
+            wh[j / 2] = *reinterpret_cast<const uint32_t*>(&hv);
+            wl[j / 2] = pack_bf16(x0 - __low2float(hv), x1 - __high2float(hv));
           }
+          stage32(stg, lane, 32 * c, wh);
+          stage32(stg + kOutBoxBytes, lane, 32 * c, wl);
+        }
+        if (hh == hpt - 1 && bx == 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(out, smem_u32(stg), 64 * bx, m * kBM + q * 32, plane);
+          tma_store_3d(out, smem_u32(stg + kOutBoxBytes), 64 * bx, m * kBM + q * 32, plane + 1);
+          bulk_commit();
         }
       }
     }
   } else {
+    const bool valid = row < p.rows;
+    const size_t ra = static_cast<size_t>(p.gdn_rows_alloc);
     // gate tile: columns [0, H) are the alpha logits, [H, 2H) the beta logits
     for (int c0 = 0; c0 < 2 * H; c0 += 32) {
       uint32_t a[32];
@@ -307,10 +320,10 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, int q, int lane
         }
       }
     }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty);
   }
-  tc_fence_before();
-  __syncwarp();
-  if (lane == 0) mbar_arrive(tempty);
 }
 
 // Fit sums: this tile of [X | Y_1 .. Y_L]^T X (f32, summed over the call's rows)
@@ -549,15 +562,19 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
       decode_tile(t, p, m, n, b);
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
+      // the row's RMS scale (from the sum-of-squares partials) is loaded before
+      // the accumulator is waited for
+      float rs = 1.f;
+      if (p.mode == kModeKV || p.mode == kModeGdnProj) rs = row_rms_scale(p, b, m * kBM + q * 32 + lane);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBNMax;
       if (p.mode == kModeMap) {
         epilogue_map(p, tcol, stg, q, lane, m, n, &tempty[acc]);
       } else if (p.mode == kModeKV) {
-        epilogue_kv(p, tcol, stg, q, lane, m, n, b, &tempty[acc]);
+        epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, &tempty[acc]);
       } else if (p.mode == kModeGdnProj) {
-        epilogue_gdn(p, tcol, q, lane, m, n, b, &tempty[acc]);
+        epilogue_gdn(p, tcol, stg, q, lane, m, n, b, rs, &tempty[acc]);
       } else if (p.mode == kModeGram) {
         epilogue_gram(p, tcol, q, lane, m, n, &tempty[acc]);
       } else {

@@ -769,6 +769,13 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
                           a->n_layers, drow, drow * H, kBK, H, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_tmap_3d(&p.tmB[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wb, a->d_out, H,
                           a->n_layers, drow, drow * H, kBK, H, CU_TENSOR_MAP_SWIZZLE_128B);
+  // outputs: k and v planes {d_k, rows, L*H*2} (high part, then remainder, per layer and head)
+  const uint64_t prow = static_cast<uint64_t>(kDk) * 2, pplane = prow * pl.R;
+  const uint64_t planes = static_cast<uint64_t>(a->n_layers) * H * 2;
+  ok = ok && make_tmap_3d(&p.tmO[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, kb, kDk, rc, planes, prow,
+                          pplane, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmO[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, vb, kDk, rc, planes, prow,
+                          pplane, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the GDN projection GEMM");
   p.m_tiles = static_cast<int32_t>(ceil_div(rc, kBM));
   p.n_k_tiles = H / 2;
