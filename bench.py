@@ -46,8 +46,12 @@ FP32_LANES_PER_SM = 128
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture, valid only
 # for the kernel source with this digest (otherwise reported as null).
+# dram__bytes_read.sum + dram__bytes_write.sum of one full-size map-GEMM launch
+# (ncu, one pass; profiles/fill_launches_llama8b_16k.md), valid while the
+# library sources hash to kernel_sha256.
 PROFILED_TRAFFIC = {
-    "llama8b_16k": {"kernel_sha256": None, "bytes_per_launch": None},
+    "llama8b_16k": {"kernel_sha256": "510babdf25013b7783000ffb55bb274cd8e9103f1542ff3e9a07cc97052bd66f",
+                    "bytes_per_launch": 2831165952 + 2344527616},
 }
 
 
@@ -61,8 +65,10 @@ def _peaks():
 
 def _kernel_digest() -> str:
     h = hashlib.sha256()
-    for f in ("fill_gemm.cu", "sm103_ptx.cuh", "rf_internal.h"):
-        with open(os.path.join(ROOT, "late_layer_kv_gb300", "csrc", f), "rb") as fh:
+    csrc = os.path.join(ROOT, "late_layer_kv_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
             h.update(fh.read())
     return h.hexdigest()
 
