@@ -123,16 +123,17 @@ __global__ void equilibrate_kernel(const double* G, const double* count, const d
 }
 
 // ------------------------------------------------------------ Cholesky (f32)
-// In-place factor of one 64x64 diagonal block (lower); a pivot <= 0 records
-// kErrNumeric in the device error word and continues with pivot 1.
-__global__ void potrf_diag_kernel(float* A, int ld, int kb, int* err) {
+// In-place factor of one 64x64 diagonal block (lower), right-looking, one row
+// per thread (64 threads); a pivot <= 0 records kErrNumeric in the device error
+// word and continues with pivot 1.
+__global__ void __launch_bounds__(kNB) potrf_diag_kernel(float* A, int ld, int kb, int* err) {
   __shared__ float a[kNB][kNB + 1];
   float* blk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
-  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x)
-    a[e / kNB][e % kNB] = blk[static_cast<size_t>(e / kNB) * ld + e % kNB];
+  const int i = threadIdx.x;
+  for (int k = 0; k < kNB; ++k) a[i][k] = blk[static_cast<size_t>(i) * ld + k];
   __syncthreads();
   for (int j = 0; j < kNB; ++j) {
-    if (threadIdx.x == 0) {
+    if (i == j) {
       float v = a[j][j];
       if (!(v > 0.f)) {
         atomicCAS(err, 0, kErrNumeric);
@@ -141,20 +142,15 @@ __global__ void potrf_diag_kernel(float* A, int ld, int kb, int* err) {
       a[j][j] = sqrtf(v);
     }
     __syncthreads();
-    const float piv = a[j][j];
-    for (int i = j + 1 + threadIdx.x; i < kNB; i += blockDim.x) a[i][j] /= piv;
+    if (i > j) a[i][j] /= a[j][j];
     __syncthreads();
-    const int m = kNB - j - 1;
-    for (int e = threadIdx.x; e < m * m; e += blockDim.x) {
-      const int i = j + 1 + e / m, k = j + 1 + e % m;
-      if (k <= i) a[i][k] -= a[i][j] * a[k][j];
+    if (i > j) {
+      const float lij = a[i][j];
+      for (int k = j + 1; k <= i; ++k) a[i][k] = fmaf(-lij, a[k][j], a[i][k]);
     }
-    __syncthreads();
   }
-  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x) {
-    const int i = e / kNB, k = e % kNB;
-    blk[static_cast<size_t>(i) * ld + k] = k <= i ? a[i][k] : 0.f;
-  }
+  __syncthreads();
+  for (int k = 0; k < kNB; ++k) blk[static_cast<size_t>(i) * ld + k] = k <= i ? a[i][k] : 0.f;
 }
 
 // Panel: A_ik <- A_ik L_kk^-T for block rows i > kb (one block row per CTA,
@@ -217,15 +213,18 @@ __global__ void zero_upper_kernel(float* A, int d) {
 // ------------------------------------------------------------ f32 SIMT GEMM
 // C = alpha op(A) op(B) + beta C for row-major f32 matrices; 64x64 tiles,
 // 256 threads with 4x4 outputs each.  lower_only skips tiles above the
-// diagonal; k_tri starts the K loop at max(m0, n0) (operands lower triangular
-// in K, as in X^T X with X lower); k_end_tri stops it at m0 + 64 (op(A) lower).
+// diagonal; k_from_n starts the K loop at the tile's first column (op(B) lower
+// triangular); k_end_tri stops it at m0 + 64 (op(A) lower).  A batch of
+// `batch` products (grid z) steps the three operands by sa, sb, sc elements.
 struct SgemmArgs {
   int M, N, K;
   float alpha, beta;
   const float* A; int lda;
   const float* B; int ldb;
   float* C; int ldc;
-  int lower_only, k_tri, k_end_tri;
+  int lower_only, k_from_n, k_end_tri;
+  int batch = 1;
+  int64_t sa = 0, sb = 0, sc = 0;
 };
 
 template <bool TA, bool TB>
@@ -234,11 +233,14 @@ __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmArgs g) {
   __shared__ float Bs[16][64 + 4];
   const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
   if (g.lower_only && n0 > m0 + 63) return;
+  const float* __restrict__ Ag = g.A + blockIdx.z * g.sa;
+  const float* __restrict__ Bg = g.B + blockIdx.z * g.sb;
+  float* Cg = g.C + blockIdx.z * g.sc;
   const int tid = threadIdx.x;
   const int tx = tid % 16, ty = tid / 16;
   float acc[4][4] = {};
   int kbeg = 0, kend = g.K;
-  if (g.k_tri) kbeg = (max(m0, n0) / 16) * 16;
+  if (g.k_from_n) kbeg = (n0 / 16) * 16;
   if (g.k_end_tri) kend = min(g.K, m0 + 64);
   for (int k0 = kbeg; k0 < kend; k0 += 16) {
     for (int e = tid; e < 64 * 16; e += 256) {
@@ -246,8 +248,8 @@ __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmArgs g) {
       if (TA) { kk = e / 64; mm = e % 64; } else { mm = e / 16; kk = e % 16; }
       const int m = m0 + mm, k = k0 + kk;
       float v = 0.f;
-      if (m < g.M && k < g.K) v = TA ? g.A[static_cast<size_t>(k) * g.lda + m]
-                                     : g.A[static_cast<size_t>(m) * g.lda + k];
+      if (m < g.M && k < g.K) v = TA ? Ag[static_cast<size_t>(k) * g.lda + m]
+                                     : Ag[static_cast<size_t>(m) * g.lda + k];
       As[kk][mm] = v;
     }
     for (int e = tid; e < 64 * 16; e += 256) {
@@ -255,8 +257,8 @@ __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmArgs g) {
       if (TB) { nn = e / 16; kk = e % 16; } else { kk = e / 64; nn = e % 64; }
       const int n = n0 + nn, k = k0 + kk;
       float v = 0.f;
-      if (n < g.N && k < g.K) v = TB ? g.B[static_cast<size_t>(n) * g.ldb + k]
-                                     : g.B[static_cast<size_t>(k) * g.ldb + n];
+      if (n < g.N && k < g.K) v = TB ? Bg[static_cast<size_t>(n) * g.ldb + k]
+                                     : Bg[static_cast<size_t>(k) * g.ldb + n];
       Bs[kk][nn] = v;
     }
     __syncthreads();
@@ -282,7 +284,7 @@ __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmArgs g) {
     for (int j = 0; j < 4; ++j) {
       const int n = n0 + tx * 4 + j;
       if (n >= g.N) continue;
-      float* c = g.C + static_cast<size_t>(m) * g.ldc + n;
+      float* c = Cg + static_cast<size_t>(m) * g.ldc + n;
       *c = g.alpha * acc[i][j] + (g.beta != 0.f ? g.beta * *c : 0.f);
     }
   }
@@ -290,7 +292,7 @@ __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmArgs g) {
 
 cudaError_t sgemm(bool ta, bool tb, const SgemmArgs& g, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
-  dim3 grid((g.N + 63) / 64, (g.M + 63) / 64);
+  dim3 grid((g.N + 63) / 64, (g.M + 63) / 64, g.batch);
   if (!ta && !tb) sgemm_kernel<false, false><<<grid, 256, 0, s>>>(g);
   else if (!ta && tb) sgemm_kernel<false, true><<<grid, 256, 0, s>>>(g);
   else if (ta && !tb) sgemm_kernel<true, false><<<grid, 256, 0, s>>>(g);
@@ -335,10 +337,10 @@ __global__ void split_rhs_kernel(const double* C, const double* sy, const double
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (t >= rows_out * d) return;
   const int64_t o = t / d, k = t % d;
-  const double n = *count;
-  const double v = (C[t] - n * (sy[o] / n) * mu_x[k]) * static_cast<double>(s[k]);
+  // n mu_y[o] mu_x[k] = sy[o] mu_x[k]
+  const float v = static_cast<float>(fma(-sy[o], mu_x[k], C[t])) * s[k];
   __nv_bfloat16 hi, lo;
-  split_bf16(static_cast<float>(v), hi, lo);
+  split_bf16(v, hi, lo);
   __nv_bfloat16* row = Ap + o * 3 * d;
   row[k] = hi;
   row[d + k] = hi;
@@ -357,7 +359,7 @@ __global__ void bias_kernel(const double* sy, const double* count, const float* 
 
 // ------------------------------------------------------------ plan
 struct FitPlan {
-  size_t off_gh = 0, off_s = 0, off_mu32 = 0, off_mu64 = 0, off_alpha = 0, off_T = 0,
+  size_t off_gh = 0, off_s = 0, off_mu32 = 0, off_mu64 = 0, off_alpha = 0,
          off_xhi = 0, off_xlo = 0, off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0,
          off_cs = 0, total = 0;
   int bn = 0;
@@ -396,7 +398,6 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->off_mu32 = off;  off = align_up(off + d * 4, 256);
     pl->off_mu64 = off;  off = align_up(off + d * 8, 256);
     pl->off_alpha = off; off = align_up(off + 8, 256);
-    pl->off_T = off;     off = align_up(off + d * kNB * 4, 256);
     pl->off_xhi = off;   off = align_up(off + d * d * 2, 256);
     pl->off_xlo = off;   off = align_up(off + d * d * 2, 256);
     pl->off_gi = off;    off = align_up(off + d * d * 8, 256);
@@ -473,7 +474,6 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   float* mu32 = reinterpret_cast<float*>(ws + pl.off_mu32);
   double* mu64 = reinterpret_cast<double*>(ws + pl.off_mu64);
   double* alpha = reinterpret_cast<double*>(ws + pl.off_alpha);
-  float* T = reinterpret_cast<float*>(ws + pl.off_T);
   double* Gi = reinterpret_cast<double*>(ws + pl.off_gi);
   __nv_bfloat16* Xhi = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xhi);
   __nv_bfloat16* Xlo = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xlo);
@@ -494,7 +494,7 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   // blocked Cholesky, lower factor in place
   const int nb = d / kNB;
   for (int kb = 0; kb < nb; ++kb) {
-    potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb, err);
+    potrf_diag_kernel<<<1, kNB, 0, s>>>(Gh, d, kb, err);
     if (kb + 1 < nb) {
       trsm_panel_kernel<<<nb - kb - 1, 256, 0, s>>>(Gh, d, kb);
       const int rem = d - (kb + 1) * kNB;
@@ -505,17 +505,33 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
     }
   }
   zero_upper_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gh, d);
-  // X = L^-1 in place: diagonal blocks, then block columns right to left
+  // X = L^-1 in place: the 64 x 64 diagonal blocks, then recursive doubling:
+  // blocks [s1 | s2] of size s (already inverted) merge as
+  //   X_21 = -X_22 (L_21 X_11),
+  // every pair of a level in one batched product (the scratch T is the X_hi/X_lo
+  // area, free until the split below)
   trinv_diag_kernel<<<nb, 256, 0, s>>>(Gh, d);
-  for (int j = nb - 2; j >= 0; --j) {
-    const int rem = d - (j + 1) * kNB;
-    float* col = Gh + static_cast<size_t>(j + 1) * kNB * d + static_cast<size_t>(j) * kNB;
-    const float* xjj = Gh + static_cast<size_t>(j) * kNB * d + static_cast<size_t>(j) * kNB;
-    const float* xsub = Gh + static_cast<size_t>(j + 1) * kNB * d + static_cast<size_t>(j + 1) * kNB;
-    SgemmArgs g1{rem, kNB, kNB, 1.f, 0.f, col, d, xjj, d, T, kNB, 0, 0, 0};       // T = L_sub,j X_jj
-    if ((e = sgemm(false, false, g1, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
-    SgemmArgs g2{rem, kNB, rem, -1.f, 0.f, xsub, d, T, kNB, col, d, 0, 0, 1};     // X_sub,j = -X_sub T
-    if ((e = sgemm(false, false, g2, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
+  float* T = reinterpret_cast<float*>(Xhi);
+  for (int sz = kNB; sz < d; sz *= 2) {
+    const int full = d / (2 * sz);        // pairs with both halves of size sz
+    const int rest = d - full * 2 * sz;   // a last pair [sz | rest - sz] if rest > sz
+    for (int part = 0; part < 2; ++part) {
+      const int cnt = part == 0 ? full : (rest > sz ? 1 : 0);
+      if (cnt == 0) continue;
+      const int b0 = part == 0 ? 0 : full * 2 * sz;
+      const int s2 = part == 0 ? sz : rest - sz;
+      const int64_t step = 2 * static_cast<int64_t>(sz) * (d + 1);
+      const float* l21 = Gh + static_cast<size_t>(b0 + sz) * d + b0;
+      const float* x11 = Gh + static_cast<size_t>(b0) * d + b0;
+      const float* x22 = Gh + static_cast<size_t>(b0 + sz) * d + b0 + sz;
+      float* x21 = Gh + static_cast<size_t>(b0 + sz) * d + b0;
+      SgemmArgs g1{s2, sz, sz, 1.f, 0.f, l21, d, x11, d, T, sz, 0, 1, 0};   // T = L_21 X_11
+      g1.batch = cnt; g1.sa = step; g1.sb = step; g1.sc = static_cast<int64_t>(sz) * sz;
+      if ((e = sgemm(false, false, g1, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
+      SgemmArgs g2{s2, sz, s2, -1.f, 0.f, x22, d, T, sz, x21, d, 0, 0, 1};  // X_21 = -X_22 T
+      g2.batch = cnt; g2.sa = step; g2.sb = static_cast<int64_t>(sz) * sz; g2.sc = step;
+      if ((e = sgemm(false, false, g2, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
+    }
   }
   // G^-1 = X^T X on the tensor cores: three MN-major Gram products of the bf16
   // split of X (hi hi + hi lo + lo hi), summed in f64

@@ -61,7 +61,10 @@ def test_sums_match_oracle_and_split_batches():
     assert _rel(Cg, Co) < 2e-5
 
 
-@pytest.mark.parametrize("d,L,n,lam", [(256, 3, 1000, 1e-3), (512, 2, 4096, 3e-2)])
+# d = 384 and 640 are not powers of two: the blocked inverse then merges a last,
+# shorter block pair
+@pytest.mark.parametrize("d,L,n,lam", [(256, 3, 1000, 1e-3), (512, 2, 4096, 3e-2),
+                                       (384, 2, 2000, 1e-3), (640, 2, 3000, 1e-2)])
 def test_solve_matches_closed_form(d, L, n, lam):
     cal = calibration(d=d, n_layers=L, n=n, seed=41 + d)
     X, Y = cal["X"], cal["Y"]
