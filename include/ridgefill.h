@@ -260,6 +260,23 @@ rf_status ridgefill_fit(const rf_fit_args* args, void* workspace, size_t workspa
                         void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Workspace sizes through one entry                                         */
+/* ------------------------------------------------------------------------ */
+
+/* Which call ridgefill_workspace_size answers for. */
+typedef enum {
+  RF_CALL_FILL = 0,      /* args is a const rf_fill_args*  (ridgefill_fill)     */
+  RF_CALL_FILL_GDN = 1,  /* args is a const rf_gdn_args*   (ridgefill_fill_gdn) */
+  RF_CALL_FIT = 2        /* args is a const rf_fit_args*   (ridgefill_fit)      */
+} rf_call;
+
+/* Bytes of device workspace the call `which` needs for `args`: the same value
+ * as ridgefill_fill_workspace_size, ridgefill_gdn_workspace_size or
+ * ridgefill_fit_workspace_size.  0 for an unknown `which`, a NULL `args` or
+ * arguments the call would reject (the reason is in ridgefill_last_error). */
+size_t ridgefill_workspace_size(int32_t which, const void* args);
+
+/* ------------------------------------------------------------------------ */
 /* Status and host helpers                                                   */
 /* ------------------------------------------------------------------------ */
 

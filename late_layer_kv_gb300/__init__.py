@@ -15,4 +15,5 @@ from .ridgefill import (  # noqa: F401
     ridgefill_fill_gdn,
     ridgefill_fit_accumulate,
     ridgefill_fit_solve,
+    ridgefill_workspace_size,
 )

@@ -93,6 +93,8 @@ def load(rebuild: bool = True) -> ctypes.CDLL:
     lib.ridgefill_fit_workspace_size.restype = ctypes.c_size_t
     lib.ridgefill_fit.argtypes = [ctypes.POINTER(FitArgs), _vp, ctypes.c_size_t, _vp]
     lib.ridgefill_fit.restype = ctypes.c_int
+    lib.ridgefill_workspace_size.argtypes = [ctypes.c_int32, _vp]
+    lib.ridgefill_workspace_size.restype = ctypes.c_size_t
     lib.ridgefill_status_string.argtypes = [ctypes.c_int]
     lib.ridgefill_status_string.restype = ctypes.c_char_p
     lib.ridgefill_last_error.argtypes = []
@@ -172,6 +174,14 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
                  ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None)
     a._events_keepalive = (ev, cev)
     return a
+
+
+RF_CALL_FILL, RF_CALL_FILL_GDN, RF_CALL_FIT = 0, 1, 2
+
+
+def ridgefill_workspace_size(which: int, args) -> int:
+    """Workspace bytes of call `which` (RF_CALL_*) for an argument struct; 0 if rejected."""
+    return int(load().ridgefill_workspace_size(which, ctypes.cast(ctypes.byref(args), _vp)))
 
 
 def fill_workspace_size(args: FillArgs) -> int:

@@ -75,3 +75,25 @@ def test_workspace_size_formula(lib):
     xhat = 20 * 14336 * 4096 * 2
     ss = 20 * (4096 // 256) * 14336 * 4
     assert xhat + ss <= ws <= xhat + ss + 1024
+
+
+def test_generic_workspace_size_matches_each_call(lib):
+    """ridgefill_workspace_size(which, args) answers as the per-call size functions."""
+    from late_layer_kv_gb300 import ridgefill as rb
+    lib.ridgefill_workspace_size.argtypes = [ctypes.c_int32, ctypes.c_void_p]
+    lib.ridgefill_workspace_size.restype = ctypes.c_size_t
+    fa = rb.FillArgs(20, 4096, 4096, 8, 128, 0, 14336, 0, 16384, 0, 5e5, 1e-6)
+    ga = rb.GdnArgs()
+    ga.n_layers, ga.d_in, ga.d_out, ga.n_heads, ga.d_k, ga.d_v, ga.chunk = 15, 4096, 4096, 16, 128, 128, 64
+    ga.rows, ga.rms_eps, ga.l2_eps = 28672, 1e-6, 1e-6
+    ta = rb.FitArgs()
+    ta.n_layers, ta.d_in, ta.d_out, ta.flags, ta.rows = 20, 4096, 4096, 3, 65536
+    setattr(ta, "lambda", 1e-3)
+    pairs = [(0, fa, lib.ridgefill_fill_workspace_size), (1, ga, lib.ridgefill_gdn_workspace_size),
+             (2, ta, lib.ridgefill_fit_workspace_size)]
+    for which, args, single in pairs:
+        ws = lib.ridgefill_workspace_size(which, ctypes.cast(ctypes.byref(args), ctypes.c_void_p))
+        assert ws > 0 and ws == single(ctypes.byref(args))
+    assert lib.ridgefill_workspace_size(7, ctypes.cast(ctypes.byref(fa), ctypes.c_void_p)) == 0
+    assert b"unknown call" in lib.ridgefill_last_error()
+    assert lib.ridgefill_workspace_size(0, None) == 0
