@@ -135,8 +135,9 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   const uint64_t out_row = static_cast<uint64_t>(m.d_out) * 2;
   bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.H, m.d_in, m.rows, 1, in_row,
                          0, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  // B boxes of bn / 2 rows: each CTA of a pair stages half of a tile's columns
   ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A, m.d_in, brows, 1,
-                          in_row, 0, kBK, m.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+                          in_row, 0, kBK, m.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_tmap_3d(&p.tmO[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.xhat, m.d_out, m.rows,
                           m.n_layers, out_row, out_row * m.R, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the map GEMM");
@@ -155,10 +156,10 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   p.ss_part = m.ss;
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
-  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  if (grid <= 0) return RF_OK;
-  cudaError_t e = launch_gemm(p, grid, s);
+  const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+  const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  if (pairs <= 0) return RF_OK;
+  cudaError_t e = launch_gemm2(p, pairs, s);
   if (e != cudaSuccess) return cuda_fail(e, "map GEMM launch");
   return RF_OK;
 }

@@ -58,6 +58,9 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   pl->total = align_up(pl->off_slots + slots, 256);
 }
 
+// K/V GEMM on CTA pairs (true) or single CTAs
+constexpr bool kKvPairs = true;
+
 rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, int64_t rc,
                     const void* xhat, const float* ss, cudaStream_t s) {
   GemmParams p{};
@@ -69,10 +72,12 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   const uint64_t pos_end = static_cast<uint64_t>(a->pos0 + start + rc);
   bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xhat, a->d_out, rc,
                          a->n_layers, drow, drow * pl.R, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  // pair kernel: B boxes of bn / 2 rows (each CTA of a pair stages half of a tile's columns)
+  const uint32_t bbox = kKvPairs ? pl.bn_kv / 2 : pl.bn_kv;
   ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wk, a->d_out, kvw,
-                          a->n_layers, drow, drow * kvw, kBK, pl.bn_kv, CU_TENSOR_MAP_SWIZZLE_128B);
+                          a->n_layers, drow, drow * kvw, kBK, bbox, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wv, a->d_out, kvw,
-                          a->n_layers, drow, drow * kvw, kBK, pl.bn_kv, CU_TENSOR_MAP_SWIZZLE_128B);
+                          a->n_layers, drow, drow * kvw, kBK, bbox, CU_TENSOR_MAP_SWIZZLE_128B);
   const uint64_t planes = static_cast<uint64_t>(a->n_layers) * a->n_kv_heads;
   const uint64_t plane_bytes = static_cast<uint64_t>(a->cache_len) * hd * 2;
   ok = ok && make_tmap_3d(&p.tmO[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Kc, hd, pos_end, planes,
@@ -103,10 +108,18 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   }
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
-  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.batches;
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  if (grid <= 0) return RF_OK;
-  cudaError_t e = launch_gemm(p, grid, s);
+  cudaError_t e;
+  if (kKvPairs) {
+    const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles * p.batches;
+    const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+    if (pairs <= 0) return RF_OK;
+    e = launch_gemm2(p, pairs, s);
+  } else {
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.batches;
+    const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+    if (grid <= 0) return RF_OK;
+    e = launch_gemm(p, grid, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "K/V GEMM launch");
   return RF_OK;
 }

@@ -120,7 +120,7 @@ __device__ __forceinline__ void map_half(const uint32_t (&r)[32], const float* b
 }
 
 __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
-                             int m, int n, uint64_t* tempty) {
+                             int m, int n, uint32_t tempty) {
   const int gcol = n * p.bn;
   const int l = p.layer_base + gcol / p.d_out;
   const int j0 = gcol % p.d_out;
@@ -135,7 +135,7 @@ __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
     if (c == nch - 1) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
+      if (lane == 0) mbar_arrive_cl(tempty);
     }
     const int col = j0 + c * 64;
     const float* bp = p.bias + static_cast<size_t>(l) * p.d_out + col;
@@ -171,7 +171,7 @@ __device__ __forceinline__ float row_rms_scale(const GemmParams& p, int l, int r
 }
 
 __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
-                            int m, int n, int l, float rs, uint64_t* tempty) {
+                            int m, int n, int l, float rs, uint32_t tempty) {
   const int row = m * kBM + q * 32 + lane;
   const float posf = static_cast<float>(p.pos_base + row);
   const bool is_k = n < p.n_k_tiles;
@@ -218,7 +218,7 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
     if (hh == hpt - 1) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
+      if (lane == 0) mbar_arrive_cl(tempty);
     }
     fence_async_smem();
     __syncwarp();
@@ -235,7 +235,7 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
 // bf16 remainders, staged per 64-column half and stored by TMA into the
 // [L, H, 2, rows, 128] planes; the gate tile stores sigmoid(alpha), sigmoid(beta).
 __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
-                             int m, int n, int l, float rs, uint64_t* tempty) {
+                             int m, int n, int l, float rs, uint32_t tempty) {
   const int row = m * kBM + q * 32 + lane;
   const int H = p.gdn_heads;
   if (n < p.n_k_tiles + p.n_v_tiles) {
@@ -285,7 +285,7 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
         if (hh == hpt - 1 && bx == 1) {
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(tempty);
+          if (lane == 0) mbar_arrive_cl(tempty);
         }
         fence_async_smem();
         __syncwarp();
@@ -322,14 +322,14 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
     }
     tc_fence_before();
     __syncwarp();
-    if (lane == 0) mbar_arrive(tempty);
+    if (lane == 0) mbar_arrive_cl(tempty);
   }
 }
 
 // Fit sums: this tile of [X | Y_1 .. Y_L]^T X (f32, summed over the call's rows)
 // is added into the caller's f64 sums, one output row per thread.
 __device__ void epilogue_gram(const GemmParams& p, uint32_t tcol, int q, int lane, int m, int n,
-                              uint64_t* tempty) {
+                              uint32_t tempty) {
   const int r = q * 32 + lane;
   double* dst;
   if (m < p.gram_x_tiles) {
@@ -348,7 +348,7 @@ __device__ void epilogue_gram(const GemmParams& p, uint32_t tcol, int q, int lan
     if (c0 + 32 == p.bn) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
+      if (lane == 0) mbar_arrive_cl(tempty);
     }
     double2* d2 = reinterpret_cast<double2*>(dst + c0);
 #pragma unroll
@@ -364,7 +364,7 @@ __device__ void epilogue_gram(const GemmParams& p, uint32_t tcol, int q, int lan
 // Fit solve: out[o, i] = s_i * acc[o, i] (f32 and/or bf16) and the partial
 // sum over this tile's columns of out[o, i] * mu_x[i] (for the offsets).
 __device__ void epilogue_solve(const GemmParams& p, uint32_t tcol, int q, int lane, int m, int n,
-                               uint64_t* tempty) {
+                               uint32_t tempty) {
   const int o = m * kBM + q * 32 + lane;
   const int c_base = n * p.bn;
   const bool valid = o < p.rows;
@@ -376,7 +376,7 @@ __device__ void epilogue_solve(const GemmParams& p, uint32_t tcol, int q, int la
     if (c0 + 32 == p.bn) {
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(tempty);
+      if (lane == 0) mbar_arrive_cl(tempty);
     }
     if (!valid) continue;
     const int c = c_base + c0;
@@ -570,15 +570,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
       tc_fence_after();
       const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBNMax;
       if (p.mode == kModeMap) {
-        epilogue_map(p, tcol, stg, q, lane, m, n, &tempty[acc]);
+        epilogue_map(p, tcol, stg, q, lane, m, n, smem_u32(&tempty[acc]));
       } else if (p.mode == kModeKV) {
-        epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, &tempty[acc]);
+        epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, smem_u32(&tempty[acc]));
       } else if (p.mode == kModeGdnProj) {
-        epilogue_gdn(p, tcol, stg, q, lane, m, n, b, rs, &tempty[acc]);
+        epilogue_gdn(p, tcol, stg, q, lane, m, n, b, rs, smem_u32(&tempty[acc]));
       } else if (p.mode == kModeGram) {
-        epilogue_gram(p, tcol, q, lane, m, n, &tempty[acc]);
+        epilogue_gram(p, tcol, q, lane, m, n, smem_u32(&tempty[acc]));
       } else {
-        epilogue_solve(p, tcol, q, lane, m, n, &tempty[acc]);
+        epilogue_solve(p, tcol, q, lane, m, n, smem_u32(&tempty[acc]));
       }
     }
     if (lane == 0) bulk_wait_all<0>();
@@ -589,6 +589,212 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem_base, 512);
   }
+}
+
+// ------------------------------------------------------------------ CTA pairs
+// Map and K/V modes on CTA pairs (clusters of 2): the pair computes a 256-row x
+// bn-column tile with tcgen05.mma.cta_group::2.  Each CTA stages its 128 rows
+// of A and its bn / 2 rows of B (up to 32 KB a stage, six stages); the MMA of CTA 0 reads
+// both CTAs' halves and writes each CTA's 128 accumulator rows into its own
+// TMEM.  Loads of both CTAs complete on CTA 0's `full` barrier; CTA 0's commits
+// release both CTAs' stages and accumulators; both CTAs' epilogues release the
+// accumulator on CTA 0's `tempty` barrier.
+constexpr int kStages2 = 6;
+constexpr int kHalfBytes = 128 * kBK * 2;  // 128 rows x 64 K of bf16
+
+namespace {
+
+__device__ __forceinline__ void decode_pair(int t, const GemmParams& p, int& mp, int& n, int& b) {
+  const int m_pairs = (p.m_tiles + 1) / 2;
+  const int gp = p.group_m / 2 > 0 ? p.group_m / 2 : 1;
+  const int per_b = m_pairs * p.n_tiles;
+  b = t / per_b;
+  const int r = t - b * per_b;
+  const int gsz = gp * p.n_tiles;
+  const int g = r / gsz;
+  const int first = g * gp;
+  const int gm = min(m_pairs - first, gp);
+  const int rr = r - g * gsz;
+  mp = first + rr % gm;
+  n = rr / gm;
+}
+
+}  // namespace
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    rf_gemm2_kernel(const __grid_constant__ GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = sA + kStages2 * kHalfBytes;
+  uint8_t* stg_all = sB + kStages2 * kHalfBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 4 * kOutWarpBytes);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages2;
+  uint64_t* tfull = bars + 2 * kStages2;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* fin = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages2; ++s) {
+      mbar_init(&full[s], 2);   // both CTAs' producers
+      mbar_init(&empty[s], 1);  // CTA 0's commit
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(fin, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch(&p.tmA);
+    tma_prefetch(&p.tmB[0]);
+    if (p.mode == kModeKV) tma_prefetch(&p.tmB[1]);
+  }
+  if (warp == 2) {
+    tmem_alloc_pair(tmem_slot, 512);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // both CTAs' barriers are initialised and their TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int total = ((p.m_tiles + 1) / 2) * p.n_tiles * p.batches;
+  const uint32_t full0 = cluster_addr(smem_u32(full), 0);
+  const uint32_t tempty0 = cluster_addr(smem_u32(tempty), 0);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer of this CTA's halves
+      uint32_t stage = 0, phase = 0;
+      int issued[kStages2];
+      for (int s = 0; s < kStages2; ++s) issued[s] = -1;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        int mp, n, b;
+        decode_pair(t, p, mp, n, b);
+        const int m = 2 * mp + static_cast<int>(rank);
+        const TileB tb = tile_b(p, n);
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrProducer)) {
+            ok = false;
+            break;
+          }
+          const uint32_t fb = full0 + 8 * stage;
+          const int half = tb.bn / 2;  // B rows (tile columns) this CTA stages
+          if (rank == 0) mbar_expect_tx(&full[stage], kHalfBytes + half * kBK * 2);
+          else mbar_expect_tx_cl(fb, kHalfBytes + half * kBK * 2);
+          tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, kb * kBK, m * kBM, b);
+          tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[tb.seg], fb, kb * kBK,
+                           tb.nrow + half * static_cast<int>(rank), b);
+          issued[stage] = static_cast<int>(phase);
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (!ok && rank == 0)  // let the copies counted on this CTA's barriers land
+        for (int s = 0; s < kStages2; ++s)
+          if (issued[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued[s]));
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (CTA 0 only)
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs, ++it) {
+        int mp, n, b;
+        decode_pair(t, p, mp, n, b);
+        const TileB tb = tile_b(p, n);
+        const uint32_t idesc = idesc_bf16_f32(2 * kBM, tb.bn);
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, kErrMma)) break;
+        tc_fence_after();
+        const uint32_t dt = tmem_base + acc * kBNMax;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err, kErrMma)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * kHalfBytes));
+          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * kHalfBytes));
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16_pair(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          mma_commit_pair(&empty[stage], 3);
+          if (++stage == kStages2) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) mma_commit_pair(&tfull[acc], 3);
+      }
+      // every MMA issued has finished before TMEM is released
+      mma_commit_pair(fin, 1);
+      mbar_drain(fin, 0);
+    }
+  } else if (warp >= 4) {
+    // ---------------- epilogue warpgroup (both CTAs)
+    const int q = warp - 4;
+    uint8_t* stg = stg_all + q * kOutWarpBytes;
+    int it = 0;
+    for (int t = pair; t < total; t += npairs, ++it) {
+      int mp, n, b;
+      decode_pair(t, p, mp, n, b);
+      const int m = 2 * mp + static_cast<int>(rank);
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      float rs = 1.f;
+      if (p.mode == kModeKV) rs = row_rms_scale(p, b, m * kBM + q * 32 + lane);
+      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, kErrEpilogue)) break;
+      tc_fence_after();
+      const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBNMax;
+      if (m >= p.m_tiles) {  // the second half of a last, odd row tile: nothing to store
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cl(tempty0 + 8 * acc);
+      } else if (p.mode == kModeMap) {
+        epilogue_map(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
+      } else {
+        epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
+      }
+    }
+    if (lane == 0) bulk_wait_all<0>();
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no pair MMA, commit or remote arrival targets either CTA any more
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, 512);
+  }
+}
+
+cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kGemmSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  rf_gemm2_kernel<<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {

@@ -93,6 +93,8 @@ struct GemmParams {
 };
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
+// map and K/V modes on CTA pairs (B tensor maps with 128-row boxes); `pairs` clusters of 2
+cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream);
 
 // ------------------------------------------------------------ GDN state
 struct GdnStateParams {
