@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
 }
 
 // ------------------------------------------------------------------ CTA pairs
-// Map and K/V modes on CTA pairs (clusters of 2): the pair computes a 256-row x
+// Map, K/V and GDN projection modes on CTA pairs (clusters of 2): the pair computes a 256-row x
 // bn-column tile with tcgen05.mma.cta_group::2.  Each CTA stages its 128 rows
 // of A and its bn / 2 rows of B (up to 32 KB a stage, six stages); the MMA of CTA 0 reads
 // both CTAs' halves and writes each CTA's 128 accumulator rows into its own
@@ -659,7 +659,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch(&p.tmA);
     tma_prefetch(&p.tmB[0]);
-    if (p.mode == kModeKV) tma_prefetch(&p.tmB[1]);
+    if (p.mode == kModeKV || p.mode == kModeGdnProj) tma_prefetch(&p.tmB[1]);
+    if (p.mode == kModeGdnProj) {
+      tma_prefetch(&p.tmB[2]);
+      tma_prefetch(&p.tmB[3]);
+    }
   }
   if (warp == 2) {
     tmem_alloc_pair(tmem_slot, 512);
@@ -695,8 +699,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (rank == 0) mbar_expect_tx(&full[stage], kHalfBytes + half * kBK * 2);
           else mbar_expect_tx_cl(fb, kHalfBytes + half * kBK * 2);
           tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, kb * kBK, m * kBM, b);
-          tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[tb.seg], fb, kb * kBK,
-                           tb.nrow + half * static_cast<int>(rank), b);
+          if (tb.seg < 2)
+            tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[tb.seg], fb, kb * kBK,
+                             tb.nrow + half * static_cast<int>(rank), b);
+          else  // GDN gate tile: CTA 0 stages the alpha weights, CTA 1 the beta weights
+            tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[2 + rank], fb, kb * kBK, 0, b);
           issued[stage] = static_cast<int>(phase);
           if (++stage == kStages2) {
             stage = 0;
@@ -759,7 +766,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       float rs = 1.f;
-      if (p.mode == kModeKV) rs = row_rms_scale(p, b, m * kBM + q * 32 + lane);
+      if (p.mode == kModeKV || p.mode == kModeGdnProj) rs = row_rms_scale(p, b, m * kBM + q * 32 + lane);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBNMax;
@@ -769,8 +776,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) mbar_arrive_cl(tempty0 + 8 * acc);
       } else if (p.mode == kModeMap) {
         epilogue_map(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
-      } else {
+      } else if (p.mode == kModeKV) {
         epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
+      } else {
+        epilogue_gdn(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
       }
     }
     if (lane == 0) bulk_wait_all<0>();

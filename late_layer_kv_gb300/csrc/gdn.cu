@@ -761,10 +761,12 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
   const uint64_t hk = static_cast<uint64_t>(H) * kDk;
   bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xhat, a->d_out, rc, a->n_layers,
                          drow, drow * pl.R, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  // B boxes of half a tile's columns: each CTA of a pair stages one half (the gate
+  // tile's halves are the H rows of w_a and of w_b)
   ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wk, a->d_out, hk,
-                          a->n_layers, drow, drow * hk, kBK, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+                          a->n_layers, drow, drow * hk, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wv, a->d_out, hk,
-                          a->n_layers, drow, drow * hk, kBK, 256, CU_TENSOR_MAP_SWIZZLE_128B);
+                          a->n_layers, drow, drow * hk, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_tmap_3d(&p.tmB[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wa, a->d_out, H,
                           a->n_layers, drow, drow * H, kBK, H, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_tmap_3d(&p.tmB[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wb, a->d_out, H,
@@ -799,10 +801,10 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
   p.l2_eps = static_cast<float>(a->l2_eps);
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
-  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.batches;
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  if (grid <= 0) return RF_OK;
-  cudaError_t e = launch_gemm(p, grid, s);
+  const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles * p.batches;
+  const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  if (pairs <= 0) return RF_OK;
+  cudaError_t e = launch_gemm2(p, pairs, s);
   if (e != cudaSuccess) return cuda_fail(e, "GDN projection GEMM launch");
   return RF_OK;
 }

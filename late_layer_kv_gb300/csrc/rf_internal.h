@@ -93,7 +93,8 @@ struct GemmParams {
 };
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
-// map and K/V modes on CTA pairs (B tensor maps with 128-row boxes); `pairs` clusters of 2
+// map, K/V and GDN projection modes on CTA pairs (B tensor maps with boxes of half a
+// tile's columns); `pairs` clusters of 2
 cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream);
 
 // ------------------------------------------------------------ GDN state
