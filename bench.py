@@ -50,8 +50,8 @@ FP32_LANES_PER_SM = 128
 # (ncu, one pass; profiles/fill_launches_llama8b_16k.md), valid while the
 # library sources hash to kernel_sha256.
 PROFILED_TRAFFIC = {
-    "llama8b_16k": {"kernel_sha256": "510babdf25013b7783000ffb55bb274cd8e9103f1542ff3e9a07cc97052bd66f",
-                    "bytes_per_launch": 2831165952 + 2344527616},
+    "llama8b_16k": {"kernel_sha256": "1f18ba1329d9959ce992c4954320b44dbdec42463f447544bae6bb4ce4bf98d6",
+                    "bytes_per_launch": 8223792640 + 2361430784},
 }
 
 
