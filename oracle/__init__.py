@@ -13,6 +13,7 @@ from .ridgefill import (  # noqa: F401
     late_layer_kv,
     map_apply,
     fill_attention,
+    kv_rescale,
     gdn_projections,
     gdn_recurrence,
     gdn_state,

@@ -30,6 +30,8 @@ Readings where the paper is silent (each applied below):
   convolution; ``k`` is L2-normalised with ``k / sqrt(sum k^2 + 1e-6)``; state
   ``S`` is ``d_v x d_k`` and starts at zero unless given.
 * R6 rows: every prefix row is filled; the tail is not touched.
+* R16 value/key rescale: "the ratio of the exact value norm to the predicted
+  one, averaged over the c rows" is the mean of the per-row ratios.
 
 Parity status: every function below is pinned by a test in ``tests/`` that
 does not re-evaluate its own formula (closed forms, exact rational
@@ -177,6 +179,35 @@ def fill_attention(H, pos, A, b, g, Wk, Wv, eps: float, theta: float, n_kv: int,
         Ks.append(k)
         Vs.append(v)
     return np.stack(Ks), np.stack(Vs)
+
+
+def kv_rescale(H_tail, X_true, A, b, g, W, eps: float, n_kv: int, hd: int):
+    """Per-layer, per-kv-head scale of the value (or key) rescale, section 2.3
+    "Value rescale" (and the key scale of section 6.6).
+
+    The first ``c`` tail rows go through the layer's norm and projection ``W``
+    ([L, n_kv*hd, d_out]: W_v for values, W_k for keys) twice: from their true
+    late-layer inputs ``X_true`` [L, c, d_out] and from the map's prediction
+    ``A h + b`` of their split states ``H_tail`` [c, d_in].  The scale of a head
+    is the mean over the rows of ||exact|| / ||predicted|| (R16: the per-row
+    ratio averaged; rows whose predicted norm is 0 are left out, and a head
+    with no such row keeps scale 1).  The rotary embedding preserves key norms,
+    so it does not enter.  Returns [L, n_kv].
+    """
+    L = np.shape(A)[0]
+    out = np.ones((L, n_kv))
+    for l in range(L):
+        W_l = _f64(W[l])
+        pred = rms_norm(map_apply(H_tail, A[l], b[l]), g[l], eps) @ W_l.T
+        true = rms_norm(X_true[l], g[l], eps) @ W_l.T
+        for h in range(n_kv):
+            cols = slice(h * hd, (h + 1) * hd)
+            n_pred = np.sqrt(np.sum(pred[:, cols] ** 2, axis=1))
+            n_true = np.sqrt(np.sum(true[:, cols] ** 2, axis=1))
+            ok = n_pred > 0
+            if ok.any():
+                out[l, h] = np.mean(n_true[ok] / n_pred[ok])
+    return out
 
 
 # --------------------------------------------------------------------------
