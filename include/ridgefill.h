@@ -147,6 +147,65 @@ rf_status ridgefill_fill(const rf_fill_args* args, void* workspace, size_t works
 rf_status ridgefill_fill_noalloc(const rf_fill_args* args, void* stream);
 
 /* ------------------------------------------------------------------------ */
+/* Value / key rescale of the filled rows                                    */
+/* ------------------------------------------------------------------------ */
+/*
+ * ridgefill_rescale -- RidgeFill section 2.3 "Value rescale" (and the key
+ * scale of section 6.6).  In every late attention layer the first c tail
+ * rows go through the layer's norm and value (or key) projection twice: from
+ * their true late-layer inputs and from the map's prediction of the same
+ * rows.  For each kv head, the mean over the c rows of
+ * ||exact projection|| / ||predicted projection|| (rows whose predicted norm
+ * is 0 are left out; a head with none keeps 1) is the head's scale, and the
+ * filled rows' values (or keys) in the cache are multiplied by it.  Keys are
+ * scaled after the rotary embedding, which preserves their norm.
+ *
+ *  which       RF_RESCALE_VALUES or RF_RESCALE_KEYS.
+ *  tail_rows   c >= 1, the measured rows.
+ *  rows, pos0  the filled rows scaled in place: cache positions
+ *              [pos0, pos0 + rows) of every layer and kv head.
+ *  H_tail      [c, d_in] bf16, split states of the c tail rows (device).
+ *  X_true      [L, c, d_out] bf16, their true inputs to each late layer.
+ *  A, bias, gain, Wk, Wv, Kc, Vc, cache_len, rms_eps: as in rf_fill_args
+ *              (maps resident in device memory).
+ *  scale       optional [L, n_kv_heads] f32 output of the scales (device).
+ * All pointers 16-byte aligned.  Asynchronous on `stream`; the cache rows
+ * outside [pos0, pos0 + rows) and every other input are left unchanged.
+ */
+#define RF_RESCALE_VALUES 1
+#define RF_RESCALE_KEYS 2
+typedef struct {
+  int32_t n_layers;
+  int32_t d_in;
+  int32_t d_out;
+  int32_t n_kv_heads;
+  int32_t head_dim;
+  int32_t which;
+  int64_t tail_rows;
+  int64_t rows;
+  int64_t pos0;
+  int64_t cache_len;
+  double rms_eps;
+  const void* H_tail;
+  const void* X_true;
+  const void* A;
+  const float* bias;
+  const void* gain;
+  const void* Wk;
+  const void* Wv;
+  void* Kc;
+  void* Vc;
+  float* scale;
+} rf_rescale_args;
+
+/* Workspace bytes ridgefill_rescale needs (0 on invalid arguments): the
+ * predicted and true inputs of the c rows, their sums of squares, four scratch
+ * [L, n_kv, c, head_dim] bf16 projections and the scales. */
+size_t ridgefill_rescale_workspace_size(const rf_rescale_args* args);
+rf_status ridgefill_rescale(const rf_rescale_args* args, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/* ------------------------------------------------------------------------ */
 /* Gated DeltaNet late layers                                                */
 /* ------------------------------------------------------------------------ */
 
@@ -267,12 +326,13 @@ rf_status ridgefill_fit(const rf_fit_args* args, void* workspace, size_t workspa
 typedef enum {
   RF_CALL_FILL = 0,      /* args is a const rf_fill_args*  (ridgefill_fill)     */
   RF_CALL_FILL_GDN = 1,  /* args is a const rf_gdn_args*   (ridgefill_fill_gdn) */
-  RF_CALL_FIT = 2        /* args is a const rf_fit_args*   (ridgefill_fit)      */
+  RF_CALL_FIT = 2,       /* args is a const rf_fit_args*   (ridgefill_fit)      */
+  RF_CALL_RESCALE = 3    /* args is a const rf_rescale_args* (ridgefill_rescale) */
 } rf_call;
 
 /* Bytes of device workspace the call `which` needs for `args`: the same value
- * as ridgefill_fill_workspace_size, ridgefill_gdn_workspace_size or
- * ridgefill_fit_workspace_size.  0 for an unknown `which`, a NULL `args` or
+ * as ridgefill_fill_workspace_size, ridgefill_gdn_workspace_size,
+ * ridgefill_fit_workspace_size or ridgefill_rescale_workspace_size.  0 for an unknown `which`, a NULL `args` or
  * arguments the call would reject (the reason is in ridgefill_last_error). */
 size_t ridgefill_workspace_size(int32_t which, const void* args);
 

@@ -15,5 +15,8 @@ from .ridgefill import (  # noqa: F401
     ridgefill_fill_gdn,
     ridgefill_fit_accumulate,
     ridgefill_fit_solve,
+    ridgefill_rescale,
+    RF_RESCALE_KEYS,
+    RF_RESCALE_VALUES,
     ridgefill_workspace_size,
 )

@@ -219,7 +219,7 @@ extern "C" double ridgefill_compute_share(int32_t split, int32_t n_layers, int64
   return (S * (N - T) + L * T) / (L * N);
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 1; }
+extern "C" int32_t ridgefill_abi_version(void) { return 2; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {
@@ -230,6 +230,8 @@ extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
     case RF_CALL_FILL: return ridgefill_fill_workspace_size(static_cast<const rf_fill_args*>(args));
     case RF_CALL_FILL_GDN: return ridgefill_gdn_workspace_size(static_cast<const rf_gdn_args*>(args));
     case RF_CALL_FIT: return ridgefill_fit_workspace_size(static_cast<const rf_fit_args*>(args));
+    case RF_CALL_RESCALE:
+      return ridgefill_rescale_workspace_size(static_cast<const rf_rescale_args*>(args));
     default:
       rf::fail(RF_ERR_ARG, "unknown call %d", static_cast<int>(which));
       return 0;

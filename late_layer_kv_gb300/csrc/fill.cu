@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "abi_common.h"
+#include "sm103_ptx.cuh"
 
 namespace rf {
 namespace {
@@ -234,6 +235,269 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     st = launch_kv(a, pl, start, rc, xhat, ss, s);
     if (st != RF_OK) return st;
     if ((st = mark(start, 2)) != RF_OK) return st;
+  }
+  return RF_OK;
+}
+
+// ------------------------------------------------------------------ value / key rescale
+// RidgeFill section 2.3 "Value rescale" and the key scale of section 6.6: the
+// c tail rows are projected from the map's prediction (map GEMM + K/V GEMM into
+// scratch caches) and from their true inputs (g * x and its sums of squares,
+// then the same K/V GEMM); the per-head mean of the norm ratios scales the
+// filled rows of the cache in place.
+namespace rf {
+namespace {
+
+struct RescalePlan {
+  FillPlan fp;  // the predicted rows' fill plan (R = c rounded up to 128)
+  size_t off_xp = 0, off_ssp = 0, off_xt = 0, off_sst = 0, off_cache = 0, off_scale = 0, total = 0;
+  size_t cache_bytes = 0;  // one [L, n_kv, R, hd] bf16 scratch projection
+};
+
+rf_status validate_rescale(const rf_rescale_args* a) {
+  if (a == nullptr) return fail(RF_ERR_ARG, "args is NULL");
+  if (a->which != RF_RESCALE_VALUES && a->which != RF_RESCALE_KEYS)
+    return fail(RF_ERR_ARG, "which must be RF_RESCALE_VALUES or RF_RESCALE_KEYS");
+  if (a->tail_rows < 1 || a->tail_rows >= (int64_t(1) << 24))
+    return fail(RF_ERR_ARG, "tail_rows must be in [1, 2^24)");
+  rf_fill_args f{};
+  f.n_layers = a->n_layers;
+  f.d_in = a->d_in;
+  f.d_out = a->d_out;
+  f.n_kv_heads = a->n_kv_heads;
+  f.head_dim = a->head_dim;
+  f.rows = a->rows;
+  f.pos0 = a->pos0;
+  f.cache_len = a->cache_len;
+  f.rope_theta = 1e4;
+  f.rms_eps = a->rms_eps;
+  return validate_fill(&f);
+}
+
+void plan_rescale(const rf_rescale_args* a, RescalePlan* pl) {
+  rf_fill_args f{};
+  f.n_layers = a->n_layers;
+  f.d_in = a->d_in;
+  f.d_out = a->d_out;
+  f.n_kv_heads = a->n_kv_heads;
+  f.head_dim = a->head_dim;
+  f.rows = a->tail_rows;
+  plan_fill(&f, &pl->fp);
+  const size_t L = a->n_layers, d = a->d_out, R = pl->fp.R;
+  size_t off = 0;
+  pl->off_xp = off;    off = align_up(off + L * R * d * 2, 256);
+  pl->off_ssp = off;   off = align_up(off + L * (d / pl->fp.bn_map) * R * 4, 256);
+  pl->off_xt = off;    off = align_up(off + L * R * d * 2, 256);
+  pl->off_sst = off;   off = align_up(off + L * R * 4, 256);
+  pl->cache_bytes = align_up(L * a->n_kv_heads * R * a->head_dim * 2, 256);
+  pl->off_cache = off; off += 4 * pl->cache_bytes;  // K, V predicted; K, V true
+  pl->off_scale = off; off = align_up(off + L * a->n_kv_heads * 4, 256);
+  pl->total = off;
+}
+
+// One warp per (layer, row): ss = sum x^2 of the true input and xhat = bf16(g x).
+__global__ void true_input_kernel(const __nv_bfloat16* X, const __nv_bfloat16* g, int L, int64_t c,
+                                  int d, int64_t R, __nv_bfloat16* xhat, float* ss) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= static_cast<int64_t>(L) * c) return;
+  const int l = static_cast<int>(w / c);
+  const int64_t r = w % c;
+  const __nv_bfloat16* src = X + (static_cast<size_t>(l) * c + r) * d;
+  __nv_bfloat16* dst = xhat + (static_cast<size_t>(l) * R + r) * d;
+  const __nv_bfloat16* gl = g != nullptr ? g + static_cast<size_t>(l) * d : nullptr;
+  float acc = 0.f;
+  for (int j = 8 * lane; j < d; j += 256) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(src + j);
+    uint4 gv = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);  // bf16 1.0 pairs
+    if (gl != nullptr) gv = *reinterpret_cast<const uint4*>(gl + j);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[e]));
+      const float2 g2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[e]));
+      acc = fmaf(x2.x, x2.x, acc);
+      acc = fmaf(x2.y, x2.y, acc);
+      out[e] = pack_bf16(x2.x * g2.x, x2.y * g2.y);
+    }
+    *reinterpret_cast<uint4*>(dst + j) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (lane == 0) ss[static_cast<size_t>(l) * R + r] = acc;
+}
+
+__device__ __forceinline__ float row_sq(const __nv_bfloat16* p, int hd) {
+  float s = 0.f;
+  for (int j = 0; j < hd; j += 8) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p + j);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      s = fmaf(f.x, f.x, s);
+      s = fmaf(f.y, f.y, s);
+    }
+  }
+  return s;
+}
+
+// One CTA per (layer, kv head): the mean over rows of |true| / |predicted|.
+__global__ void __launch_bounds__(256) rescale_ratio_kernel(const __nv_bfloat16* pred,
+                                                            const __nv_bfloat16* truth, int64_t R,
+                                                            int64_t c, int hd, float* scale_ws,
+                                                            float* scale_out) {
+  __shared__ float s_sum[256];
+  __shared__ int s_cnt[256];
+  const size_t plane = blockIdx.x;
+  float sum = 0.f;
+  int cnt = 0;
+  for (int64_t r = threadIdx.x; r < c; r += blockDim.x) {
+    const float np = row_sq(pred + (plane * R + r) * hd, hd);
+    const float nt = row_sq(truth + (plane * R + r) * hd, hd);
+    if (np > 0.f) {
+      sum += sqrtf(nt) / sqrtf(np);
+      ++cnt;
+    }
+  }
+  s_sum[threadIdx.x] = sum;
+  s_cnt[threadIdx.x] = cnt;
+  __syncthreads();
+  for (int o = blockDim.x / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) {
+      s_sum[threadIdx.x] += s_sum[threadIdx.x + o];
+      s_cnt[threadIdx.x] += s_cnt[threadIdx.x + o];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const float sc = s_cnt[0] > 0 ? s_sum[0] / static_cast<float>(s_cnt[0]) : 1.f;
+    scale_ws[plane] = sc;
+    if (scale_out != nullptr) scale_out[plane] = sc;
+  }
+}
+
+// cache[plane, pos0 + r, :] *= scale[plane] for r < rows (8 bf16 per thread step)
+__global__ void rescale_apply_kernel(__nv_bfloat16* cache, const float* scale, int64_t planes,
+                                     int64_t cache_len, int64_t pos0, int64_t rows, int hd) {
+  const int64_t per_plane = rows * (hd / 8);
+  const int64_t total = planes * per_plane;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t plane = i / per_plane, rem = i % per_plane;
+    const int64_t r = rem / (hd / 8), c8 = rem % (hd / 8);
+    uint4* p = reinterpret_cast<uint4*>(cache + (plane * cache_len + pos0 + r) * hd + 8 * c8);
+    const float sc = scale[plane];
+    uint4 v = *p;
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+      w[e] = pack_bf16(f.x * sc, f.y * sc);
+    }
+    *p = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+}  // namespace
+}  // namespace rf
+
+extern "C" size_t ridgefill_rescale_workspace_size(const rf_rescale_args* a) {
+  if (rf::validate_rescale(a) != RF_OK) return 0;
+  rf::RescalePlan pl;
+  rf::plan_rescale(a, &pl);
+  return pl.total;
+}
+
+extern "C" rf_status ridgefill_rescale(const rf_rescale_args* a, void* workspace, size_t ws_bytes,
+                                       void* stream) {
+  using namespace rf;
+  rf_status st = validate_rescale(a);
+  if (st != RF_OK) return st;
+  const void* req[] = {a->H_tail, a->X_true, a->A, a->bias, a->Wk, a->Wv, a->Kc, a->Vc};
+  for (const void* p : req)
+    if (p == nullptr) return fail(RF_ERR_ARG, "a required pointer is NULL");
+  const void* dev[] = {a->H_tail, a->X_true, a->A, a->bias, a->gain, a->Wk,
+                       a->Wv,     a->Kc,     a->Vc, a->scale, workspace};
+  for (const void* p : dev)
+    if (p != nullptr && !aligned16(p)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
+  RescalePlan pl;
+  plan_rescale(a, &pl);
+  if (workspace == nullptr || ws_bytes < pl.total)
+    return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes", pl.total);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const int64_t c = a->tail_rows, R = pl.fp.R;
+  uint8_t* kp = ws + pl.off_cache;
+  uint8_t* vp = kp + pl.cache_bytes;
+  uint8_t* kt = vp + pl.cache_bytes;
+  uint8_t* vt = kt + pl.cache_bytes;
+  float* scale = reinterpret_cast<float*>(ws + pl.off_scale);
+
+  // predicted rows: map GEMM, then the K/V GEMM into scratch caches
+  MapLaunch m{};
+  m.H = a->H_tail;
+  m.A = a->A;
+  m.rows = c;
+  m.d_in = a->d_in;
+  m.d_out = a->d_out;
+  m.n_layers = a->n_layers;
+  m.slot_layer = -1;
+  m.bn = pl.fp.bn_map;
+  m.R = R;
+  m.bias = a->bias;
+  m.gain = a->gain;
+  m.xhat = ws + pl.off_xp;
+  m.ss = reinterpret_cast<float*>(ws + pl.off_ssp);
+  if ((st = launch_map(m, s)) != RF_OK) return st;
+  rf_fill_args f{};
+  f.n_layers = a->n_layers;
+  f.d_in = a->d_in;
+  f.d_out = a->d_out;
+  f.n_kv_heads = a->n_kv_heads;
+  f.head_dim = a->head_dim;
+  f.rows = c;
+  f.pos0 = 0;
+  f.cache_len = R;
+  f.rope_theta = 1e4;  // both projections rotate alike; norms do not depend on it
+  f.rms_eps = a->rms_eps;
+  f.Wk = a->Wk;
+  f.Wv = a->Wv;
+  f.Kc = kp;
+  f.Vc = vp;
+  if ((st = launch_kv(&f, pl.fp, 0, c, ws + pl.off_xp, m.ss, s)) != RF_OK) return st;
+
+  // true rows: g * x and sums of squares (one partial per row), then the same K/V GEMM
+  const int64_t warps = static_cast<int64_t>(a->n_layers) * c;
+  true_input_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a->X_true), static_cast<const __nv_bfloat16*>(a->gain),
+      a->n_layers, c, a->d_out, R, reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xt),
+      reinterpret_cast<float*>(ws + pl.off_sst));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "true-input kernel launch");
+  FillPlan fp1 = pl.fp;
+  fp1.bn_map = a->d_out;  // one sum-of-squares partial per row
+  f.Kc = kt;
+  f.Vc = vt;
+  if ((st = launch_kv(&f, fp1, 0, c, ws + pl.off_xt, reinterpret_cast<float*>(ws + pl.off_sst), s)) !=
+      RF_OK)
+    return st;
+
+  // scales, then the filled rows of the cache in place
+  const bool values = a->which == RF_RESCALE_VALUES;
+  const int64_t planes = static_cast<int64_t>(a->n_layers) * a->n_kv_heads;
+  rescale_ratio_kernel<<<static_cast<unsigned>(planes), 256, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(values ? vp : kp),
+      reinterpret_cast<const __nv_bfloat16*>(values ? vt : kt), R, c, a->head_dim, scale, a->scale);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rescale ratio launch");
+  if (a->rows > 0) {
+    const int64_t work = planes * a->rows * (a->head_dim / 8);
+    const int64_t blocks = (work + 255) / 256 < 8 * sm_count() ? (work + 255) / 256 : 8 * sm_count();
+    rescale_apply_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        static_cast<__nv_bfloat16*>(values ? a->Vc : a->Kc), scale, planes, a->cache_len, a->pos0,
+        a->rows, a->head_dim);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rescale apply launch");
   }
   return RF_OK;
 }

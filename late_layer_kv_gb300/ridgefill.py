@@ -62,6 +62,20 @@ class FitArgs(ctypes.Structure):
     ]
 
 
+class RescaleArgs(ctypes.Structure):
+    _fields_ = [
+        ("n_layers", ctypes.c_int32), ("d_in", ctypes.c_int32), ("d_out", ctypes.c_int32),
+        ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("which", ctypes.c_int32),
+        ("tail_rows", ctypes.c_int64), ("rows", ctypes.c_int64), ("pos0", ctypes.c_int64),
+        ("cache_len", ctypes.c_int64), ("rms_eps", ctypes.c_double),
+        ("H_tail", _vp), ("X_true", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp),
+        ("Wk", _vp), ("Wv", _vp), ("Kc", _vp), ("Vc", _vp), ("scale", _vp),
+    ]
+
+
+RF_RESCALE_VALUES, RF_RESCALE_KEYS = 1, 2
+
+
 class RidgeFillError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"{STATUS.get(status, status)}: {msg}")
@@ -93,6 +107,10 @@ def load(rebuild: bool = True) -> ctypes.CDLL:
     lib.ridgefill_fit_workspace_size.restype = ctypes.c_size_t
     lib.ridgefill_fit.argtypes = [ctypes.POINTER(FitArgs), _vp, ctypes.c_size_t, _vp]
     lib.ridgefill_fit.restype = ctypes.c_int
+    lib.ridgefill_rescale_workspace_size.argtypes = [ctypes.POINTER(RescaleArgs)]
+    lib.ridgefill_rescale_workspace_size.restype = ctypes.c_size_t
+    lib.ridgefill_rescale.argtypes = [ctypes.POINTER(RescaleArgs), _vp, ctypes.c_size_t, _vp]
+    lib.ridgefill_rescale.restype = ctypes.c_int
     lib.ridgefill_workspace_size.argtypes = [ctypes.c_int32, _vp]
     lib.ridgefill_workspace_size.restype = ctypes.c_size_t
     lib.ridgefill_status_string.argtypes = [ctypes.c_int]
@@ -176,7 +194,7 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
     return a
 
 
-RF_CALL_FILL, RF_CALL_FILL_GDN, RF_CALL_FIT = 0, 1, 2
+RF_CALL_FILL, RF_CALL_FILL_GDN, RF_CALL_FIT, RF_CALL_RESCALE = 0, 1, 2, 3
 
 
 def ridgefill_workspace_size(which: int, args) -> int:
@@ -274,6 +292,45 @@ def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms
         raise ValueError(f"workspace needs {need} bytes")
     _check(lib.ridgefill_fill_gdn(ctypes.byref(args), _ptr(workspace),
                                   workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def rescale_args(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, *, which: int, head_dim: int,
+                 rms_eps: float, rows: int, pos0: int = 0, scale=None) -> RescaleArgs:
+    L, d_out, d_in = A.shape
+    c = H_tail.shape[0]
+    if X_true.shape != (L, c, d_out):
+        raise ValueError("X_true must be [L, tail_rows, d_out]")
+    n_kv = Kc.shape[1]
+    a = RescaleArgs()
+    a.n_layers, a.d_in, a.d_out, a.n_kv_heads, a.head_dim = L, d_in, d_out, n_kv, head_dim
+    a.which, a.tail_rows, a.rows, a.pos0, a.cache_len = which, c, rows, pos0, Kc.shape[2]
+    a.rms_eps = rms_eps
+    a.H_tail, a.X_true, a.A, a.bias = _ptr(H_tail), _ptr(X_true), _ptr(A), _ptr(bias)
+    a.gain = _ptr(gain) if gain is not None else None
+    a.Wk, a.Wv, a.Kc, a.Vc = _ptr(Wk), _ptr(Wv), _ptr(Kc), _ptr(Vc)
+    a.scale = _ptr(scale) if scale is not None else None
+    return a
+
+
+def ridgefill_rescale(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, *, which: int, head_dim: int,
+                      rms_eps: float, rows: int, pos0: int = 0, scale=None,
+                      workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Value (or key) rescale of the filled cache rows [pos0, pos0 + rows), section 2.3.
+
+    ``H_tail`` [c, d_in] bf16 and ``X_true`` [L, c, d_out] bf16 are the split states and
+    the true late-layer inputs of the first c tail rows; ``scale`` an optional
+    [L, n_kv] f32 output of the per-head scales.  Other arguments as for
+    :func:`ridgefill_fill`."""
+    args = rescale_args(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, which=which,
+                        head_dim=head_dim, rms_eps=rms_eps, rows=rows, pos0=pos0, scale=scale)
+    lib = load()
+    need = int(lib.ridgefill_rescale_workspace_size(ctypes.byref(args)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=H_tail.device)
+    elif workspace.numel() * workspace.element_size() < need:
+        raise ValueError(f"workspace needs {need} bytes")
+    _check(lib.ridgefill_rescale(ctypes.byref(args), _ptr(workspace),
+                                 workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 class FitSums:

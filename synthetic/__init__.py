@@ -11,6 +11,7 @@ from .workloads import (  # noqa: F401
     normal,
     channel_scales,
     fill_inputs,
+    tail_inputs,
     gdn_inputs,
     calibration,
     to_f64,

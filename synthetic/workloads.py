@@ -33,6 +33,7 @@ _THREADS = max(1, min(32, os.cpu_count() or 1))
 # tensor ids used in keys (stable; never renumber)
 _ID_SCALES, _ID_H, _ID_A, _ID_B, _ID_GAIN, _ID_WK, _ID_WV = 1, 2, 3, 4, 5, 6, 7
 _ID_WA, _ID_WB, _ID_X, _ID_YG, _ID_YB, _ID_YN = 8, 9, 10, 11, 12, 13
+_ID_TAILH, _ID_TAILX, _ID_TAILS = 14, 15, 16
 
 
 def normal(shape: Sequence[int], key: Tuple[int, ...]) -> np.ndarray:
@@ -231,6 +232,20 @@ def fill_inputs(shape: FillShape, seed: int, layer_ids: Optional[Sequence[int]] 
                                scale=1.0 / math.sqrt(d))),
     }
     return out
+
+
+def tail_inputs(shape: FillShape, seed: int, c: int) -> Dict[str, torch.Tensor]:
+    """Rows of the exact tail for the value/key rescale, as CPU tensors.
+
+    ``H_tail`` [c, d] bf16 split states drawn like ``H`` (same per-channel
+    scales), and ``X_true`` [L, c, d] bf16 standing in for the true late-layer
+    inputs: ``N(0, 1)`` per entry times per-layer, per-channel scales
+    ``exp(N(0, 1))`` of their own.
+    """
+    L, d = shape.n_layers, shape.d
+    xt = np.stack([normal((c, d), (seed, _ID_TAILX, l)) *
+                   np.exp(normal((d,), (seed, _ID_TAILS, l)))[None, :] for l in range(L)])
+    return {"H_tail": _split_state(c, d, seed, _ID_TAILH), "X_true": _bf16(xt.astype(np.float32))}
 
 
 def gdn_inputs(shape: GdnShape, seed: int, rows: Optional[int] = None,

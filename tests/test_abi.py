@@ -52,6 +52,7 @@ def test_ctypes_structs_match_header():
     assert ctypes.sizeof(rb.FillArgs) == _c_sizeof("rf_fill_args")
     assert ctypes.sizeof(rb.GdnArgs) == _c_sizeof("rf_gdn_args")
     assert ctypes.sizeof(rb.FitArgs) == _c_sizeof("rf_fit_args")
+    assert ctypes.sizeof(rb.RescaleArgs) == _c_sizeof("rf_rescale_args")
 
 
 def test_invalid_arguments_fail_without_a_gpu(lib):
@@ -87,10 +88,12 @@ def test_generic_workspace_size_matches_each_call(lib):
     ga.n_layers, ga.d_in, ga.d_out, ga.n_heads, ga.d_k, ga.d_v, ga.chunk = 15, 4096, 4096, 16, 128, 128, 64
     ga.rows, ga.rms_eps, ga.l2_eps = 28672, 1e-6, 1e-6
     ta = rb.FitArgs()
-    ta.n_layers, ta.d_in, ta.d_out, ta.flags, ta.rows = 20, 4096, 4096, 3, 65536
-    setattr(ta, "lambda", 1e-3)
+    ta.n_layers, ta.d_in, ta.d_out, ta.flags, ta.rows, ta.lam = 20, 4096, 4096, 3, 65536, 1e-3
+    ra = rb.RescaleArgs()
+    ra.n_layers, ra.d_in, ra.d_out, ra.n_kv_heads, ra.head_dim, ra.which = 20, 4096, 4096, 8, 128, 1
+    ra.tail_rows, ra.rows, ra.pos0, ra.cache_len, ra.rms_eps = 512, 14336, 0, 16384, 1e-6
     pairs = [(0, fa, lib.ridgefill_fill_workspace_size), (1, ga, lib.ridgefill_gdn_workspace_size),
-             (2, ta, lib.ridgefill_fit_workspace_size)]
+             (2, ta, lib.ridgefill_fit_workspace_size), (3, ra, lib.ridgefill_rescale_workspace_size)]
     for which, args, single in pairs:
         ws = lib.ridgefill_workspace_size(which, ctypes.cast(ctypes.byref(args), ctypes.c_void_p))
         assert ws > 0 and ws == single(ctypes.byref(args))
