@@ -36,7 +36,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import WORKLOADS, FillShape, GdnShape, fill_inputs, gdn_inputs, to_f64  # noqa: E402
+from synthetic import (WORKLOADS, FillShape, GdnShape, fill_inputs, gdn_inputs,  # noqa: E402
+                       tail_inputs, to_f64)
 
 METRIC = "filled token-layers/s (fill-stage ms and % of GB300 bf16 tensor peak alongside)"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
@@ -149,8 +150,11 @@ def _events(n):
 class AttnWorkload:
     """Attention late layers (ridgefill_fill); maps in HBM or in pinned host memory."""
 
-    def __init__(self, shape: FillShape, host_maps=False, rows_per_chunk=0):
+    def __init__(self, shape: FillShape, host_maps=False, rows_per_chunk=0, rescale_rows=0):
         self.shape, self.host_maps, self.rpc = shape, host_maps, rows_per_chunk
+        self.c = rescale_rows
+        if self.c and host_maps:
+            raise ValueError("the rescale needs the maps resident in device memory")
         s = shape
         self.token_layers = s.rows * s.n_layers
         self.stage_names = ["map_gemm", "kv_gemm"]
@@ -160,6 +164,15 @@ class AttnWorkload:
         }
         self.stage_bound = {"map_gemm": "tensor", "kv_gemm": "tensor"}
         self.total_flops = 2.0 * s.rows * s.n_layers * (s.d * s.d + s.d * 2 * s.kv_width)
+        if self.c:
+            # value rescale before the fill: the c tail rows' map GEMM and one value
+            # projection of the 2c stacked predicted and true rows; the fill applies
+            # the per-head scales as it writes the values
+            self.stage_names.append("value_rescale")
+            self.stage_work["value_rescale"] = 2.0 * self.c * s.n_layers * (
+                s.d * s.d + 2 * s.d * s.kv_width)
+            self.stage_bound["value_rescale"] = "tensor"
+            self.total_flops += self.stage_work["value_rescale"]
 
     def _chunk_rows(self):
         return min(self.rpc, self.shape.rows) if self.rpc else self.shape.rows
@@ -167,7 +180,8 @@ class AttnWorkload:
     def launches_per_step(self):
         chunks = -(-self.shape.rows // self._chunk_rows())
         per_chunk = (self.shape.n_layers + 1) if self.host_maps else 2
-        return chunks * per_chunk
+        # rescale: map GEMM, true-input norm, value GEMM, ratio
+        return chunks * per_chunk + (4 if self.c else 0)
 
     def setup(self, dev, seed):
         from late_layer_kv_gb300 import ridgefill as rb
@@ -183,25 +197,48 @@ class AttnWorkload:
                          rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc)
         self.ws = torch.empty(rb.fill_workspace_size(a), dtype=torch.uint8, device=dev)
         self.H_dev = self.d["H"]
+        if self.c:
+            t = {k: v.to(dev) for k, v in tail_inputs(s, seed=seed, c=self.c).items()}
+            self.tail = t
+            self.scale = torch.empty((s.n_layers, s.n_kv), dtype=torch.float32, device=dev)
+            ra = rb.rescale_args(t["H_tail"], t["X_true"], self.A, self.d["b"], self.d["g"],
+                                 self.d["Wk"], self.d["Wv"], self.Kc, self.Vc,
+                                 which=rb.RF_RESCALE_VALUES, head_dim=s.head_dim,
+                                 rms_eps=s.rms_eps, rows=0, scale=self.scale)
+            self.rws = torch.empty(max(1, rb.load().ridgefill_rescale_workspace_size(
+                ctypes_byref(ra))), dtype=torch.uint8, device=dev)
 
     def n_events(self):
-        return 3 + (2 * self.shape.n_layers if self.host_maps else 0)
+        return 3 + (2 * self.shape.n_layers if self.host_maps else 0) + (1 if self.c else 0)
 
     def step(self, stream, ev=None):
         from late_layer_kv_gb300 import ridgefill_fill
         s, d = self.shape, self.d
+        if self.c:
+            from late_layer_kv_gb300 import RF_RESCALE_VALUES, ridgefill_rescale
+            t = self.tail
+            if ev is not None:
+                ev[-1].record(stream)
+            ridgefill_rescale(t["H_tail"], t["X_true"], self.A, d["b"], d["g"], d["Wk"], d["Wv"],
+                              self.Kc, self.Vc, which=RF_RESCALE_VALUES, head_dim=s.head_dim,
+                              rms_eps=s.rms_eps, rows=0, scale=self.scale,
+                              workspace=self.rws, stream=stream)
         ridgefill_fill(self.H_dev, self.A, d["b"], d["g"], d["Wk"], d["Wv"], self.Kc, self.Vc,
                        head_dim=s.head_dim, rope_theta=s.rope_theta, rms_eps=s.rms_eps,
                        rows_per_chunk=self.rpc, workspace=self.ws, stream=stream,
                        stage_events=None if ev is None else ev[:3],
-                       copy_events=None if (ev is None or not self.host_maps) else ev[3:])
+                       copy_events=None if (ev is None or not self.host_maps) else
+                       ev[3:3 + 2 * s.n_layers], v_scale=self.scale if self.c else None)
 
     def copy_ms(self, ev):
         """Durations of the first chunk's per-layer map copies (host maps only)."""
         return [ev[3 + 2 * l].elapsed_time(ev[4 + 2 * l]) for l in range(self.shape.n_layers)]
 
     def stage_ms(self, ev):
-        return {"map_gemm": ev[0].elapsed_time(ev[1]), "kv_gemm": ev[1].elapsed_time(ev[2])}
+        out = {"map_gemm": ev[0].elapsed_time(ev[1]), "kv_gemm": ev[1].elapsed_time(ev[2])}
+        if self.c:
+            out["value_rescale"] = ev[-1].elapsed_time(ev[0])
+        return out
 
     # end to end: pinned H in, two cache rows per layer out
     def e2e_buffers(self):
@@ -210,11 +247,18 @@ class AttnWorkload:
         self.out_host = torch.empty((s.n_layers, s.n_kv, 2, s.head_dim),
                                     dtype=torch.bfloat16).pin_memory()
         self.H_dev = torch.empty_like(self.d["H"])
-        return self.H_host.numel() * 2, self.out_host.numel() * 2
+        bi = self.H_host.numel() * 2
+        if self.c:  # the tail rows' split states and true inputs come from the host too
+            self.tail_host = {k: v.cpu().pin_memory() for k, v in self.tail.items()}
+            bi += sum(v.numel() * 2 for v in self.tail_host.values())
+        return bi, self.out_host.numel() * 2
 
     def e2e_step(self, stream):
         r = self.shape.rows
         self.H_dev.copy_(self.H_host, non_blocking=True)
+        if self.c:
+            for k, v in self.tail_host.items():
+                self.tail[k].copy_(v, non_blocking=True)
         self.step(stream)
         self.out_host.copy_(self.Kc[:, :, r - 2:r], non_blocking=True)
 
@@ -238,6 +282,7 @@ class AttnWorkload:
                 "filled_rows": s.rows, "kv_heads": s.n_kv, "head_dim": s.head_dim,
                 "maps": "pinned host, streamed per layer" if self.host_maps else "hbm",
                 "rows_per_chunk": self.rpc or s.rows,
+                "value_rescale_tail_rows": self.c,
                 "l2": "inputs larger than L2 (maps %d MiB, split state %d MiB)" % (
                     s.n_layers * s.d * s.d * 2 >> 20, s.rows * s.d * 2 >> 20)}
 
@@ -474,7 +519,8 @@ def make_workload(name, args):
     rpc = args.rows_per_chunk
     if name.startswith("dense27b") and not rpc:
         rpc = 16384  # late-layer X_hat processed in row chunks
-    return AttnWorkload(shape, host_maps=name.startswith("hostmaps"), rows_per_chunk=rpc)
+    return AttnWorkload(shape, host_maps=name.startswith("hostmaps"), rows_per_chunk=rpc,
+                        rescale_rows=args.rescale)
 
 
 # ----------------------------------------------------------------------------- arms
@@ -689,6 +735,8 @@ def main():
     ap.add_argument("--fit", action="store_true",
                     help="benchmark the ridge fit of the workload's maps instead of the fill")
     ap.add_argument("--fit-rows", type=int, default=0)
+    ap.add_argument("--rescale", type=int, default=0, metavar="C",
+                    help="also apply the value rescale from C exact tail rows each step")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

@@ -86,6 +86,11 @@ typedef enum rf_status {
  * copy_events (optional, may be NULL; host maps only): host array of
  *   2 * n_layers cudaEvent_t recorded on the library's copy stream right before
  *   and after the first chunk's copy of map l (entries 2l and 2l + 1).
+ * k_scale, v_scale (optional, may be NULL): [L, n_kv_heads] f32 device arrays.
+ *   When set, every key (value) of head h in layer l is multiplied by
+ *   k_scale[l, h] (v_scale[l, h]) before its rounding to bf16: the value or
+ *   key rescale of section 2.3 folded into the fill, with the scales from
+ *   ridgefill_rescale called with rows = 0.
  */
 typedef struct rf_fill_args {
   int32_t n_layers;
@@ -110,6 +115,8 @@ typedef struct rf_fill_args {
   void* Vc;
   void* const* stage_events;
   void* const* copy_events;
+  const float* k_scale;
+  const float* v_scale;
 } rf_fill_args;
 
 /* Bytes of device workspace ridgefill_fill needs for these arguments
@@ -161,9 +168,13 @@ rf_status ridgefill_fill_noalloc(const rf_fill_args* args, void* stream);
  * scaled after the rotary embedding, which preserves their norm.
  *
  *  which       RF_RESCALE_VALUES or RF_RESCALE_KEYS.
- *  tail_rows   c >= 1, the measured rows.
+ *  tail_rows   c in [1, 2^23), the measured rows.
  *  rows, pos0  the filled rows scaled in place: cache positions
- *              [pos0, pos0 + rows) of every layer and kv head.
+ *              [pos0, pos0 + rows) of every layer and kv head.  rows = 0
+ *              computes the scales only; passed to ridgefill_fill as
+ *              v_scale (k_scale) they are applied as the fill writes the
+ *              rows, which saves the read and write of the filled rows here
+ *              and rounds each value once instead of twice.
  *  H_tail      [c, d_in] bf16, split states of the c tail rows (device).
  *  X_true      [L, c, d_out] bf16, their true inputs to each late layer.
  *  A, bias, gain, Wk, Wv, Kc, Vc, cache_len, rms_eps: as in rf_fill_args
@@ -199,8 +210,9 @@ typedef struct {
 } rf_rescale_args;
 
 /* Workspace bytes ridgefill_rescale needs (0 on invalid arguments): the
- * predicted and true inputs of the c rows, their sums of squares, four scratch
- * [L, n_kv, c, head_dim] bf16 projections and the scales. */
+ * predicted and true inputs of the c rows stacked [L, 2c, d_out] bf16, their
+ * sums of squares, the scaled projection of both [L, n_kv, 2c, head_dim] bf16
+ * and the scales. */
 size_t ridgefill_rescale_workspace_size(const rf_rescale_args* args);
 rf_status ridgefill_rescale(const rf_rescale_args* args, void* workspace, size_t workspace_bytes,
                             void* stream);

@@ -219,7 +219,7 @@ extern "C" double ridgefill_compute_share(int32_t split, int32_t n_layers, int64
   return (S * (N - T) + L * T) / (L * N);
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 2; }
+extern "C" int32_t ridgefill_abi_version(void) { return 3; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {

@@ -62,8 +62,9 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
 // K/V GEMM on CTA pairs (true) or single CTAs
 constexpr bool kKvPairs = true;
 
+// `only`: 0 = keys and values, RF_RESCALE_KEYS / RF_RESCALE_VALUES = that half alone
 rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, int64_t rc,
-                    const void* xhat, const float* ss, cudaStream_t s) {
+                    const void* xhat, const float* ss, cudaStream_t s, int only = 0) {
   GemmParams p{};
   p.mode = kModeKV;
   p.k_blocks = a->d_out / kBK;
@@ -87,8 +88,8 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
                           hd * 2, plane_bytes, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K/V GEMM");
   p.m_tiles = static_cast<int32_t>(ceil_div(rc, kBM));
-  p.n_k_tiles = kvw / pl.bn_kv;
-  p.n_tiles = 2 * p.n_k_tiles;
+  p.n_k_tiles = only == RF_RESCALE_VALUES ? 0 : kvw / pl.bn_kv;
+  p.n_tiles = only == 0 ? 2 * p.n_k_tiles : kvw / pl.bn_kv;
   p.batches = a->n_layers;
   p.bn = pl.bn_kv;
   p.group_m = 16;
@@ -102,6 +103,8 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   p.pos_base = static_cast<int32_t>(a->pos0 + start);
   p.inv_d = static_cast<float>(1.0 / a->d_out);
   p.eps = static_cast<float>(a->rms_eps);
+  p.k_scale = a->k_scale;
+  p.v_scale = a->v_scale;
   for (int i = 0; i < a->head_dim / 2; ++i) {
     const double f = std::pow(a->rope_theta, -2.0 * i / a->head_dim);
     p.inv_freq_hi[i] = static_cast<float>(f);
@@ -249,17 +252,17 @@ namespace rf {
 namespace {
 
 struct RescalePlan {
-  FillPlan fp;  // the predicted rows' fill plan (R = c rounded up to 128)
-  size_t off_xp = 0, off_ssp = 0, off_xt = 0, off_sst = 0, off_cache = 0, off_scale = 0, total = 0;
-  size_t cache_bytes = 0;  // one [L, n_kv, R, hd] bf16 scratch projection
+  FillPlan fp;     // fill plan of the c predicted rows (map tile widths)
+  int64_t R2 = 0;  // rows of the stacked buffers: predicted rows [0, c), true rows [c, 2c)
+  size_t off_x = 0, off_ss = 0, off_cache = 0, off_scale = 0, total = 0;
 };
 
 rf_status validate_rescale(const rf_rescale_args* a) {
   if (a == nullptr) return fail(RF_ERR_ARG, "args is NULL");
   if (a->which != RF_RESCALE_VALUES && a->which != RF_RESCALE_KEYS)
     return fail(RF_ERR_ARG, "which must be RF_RESCALE_VALUES or RF_RESCALE_KEYS");
-  if (a->tail_rows < 1 || a->tail_rows >= (int64_t(1) << 24))
-    return fail(RF_ERR_ARG, "tail_rows must be in [1, 2^24)");
+  if (a->tail_rows < 1 || a->tail_rows >= (int64_t(1) << 23))
+    return fail(RF_ERR_ARG, "tail_rows must be in [1, 2^23)");
   rf_fill_args f{};
   f.n_layers = a->n_layers;
   f.d_in = a->d_in;
@@ -283,28 +286,28 @@ void plan_rescale(const rf_rescale_args* a, RescalePlan* pl) {
   f.head_dim = a->head_dim;
   f.rows = a->tail_rows;
   plan_fill(&f, &pl->fp);
-  const size_t L = a->n_layers, d = a->d_out, R = pl->fp.R;
+  pl->R2 = ceil_div(2 * a->tail_rows, kBM) * kBM;
+  const size_t L = a->n_layers, d = a->d_out, R2 = pl->R2;
   size_t off = 0;
-  pl->off_xp = off;    off = align_up(off + L * R * d * 2, 256);
-  pl->off_ssp = off;   off = align_up(off + L * (d / pl->fp.bn_map) * R * 4, 256);
-  pl->off_xt = off;    off = align_up(off + L * R * d * 2, 256);
-  pl->off_sst = off;   off = align_up(off + L * R * 4, 256);
-  pl->cache_bytes = align_up(L * a->n_kv_heads * R * a->head_dim * 2, 256);
-  pl->off_cache = off; off += 4 * pl->cache_bytes;  // K, V predicted; K, V true
+  pl->off_x = off;     off = align_up(off + L * R2 * d * 2, 256);
+  pl->off_ss = off;    off = align_up(off + L * (d / pl->fp.bn_map) * R2 * 4, 256);
+  pl->off_cache = off; off = align_up(off + L * a->n_kv_heads * R2 * a->head_dim * 2, 256);
   pl->off_scale = off; off = align_up(off + L * a->n_kv_heads * 4, 256);
   pl->total = off;
 }
 
-// One warp per (layer, row): ss = sum x^2 of the true input and xhat = bf16(g x).
+// One warp per (layer, true row r): X_hat row c + r = bf16(g x) and its sum of
+// squares as the row's first partial (the other partials zero), in the layout
+// the map GEMM gives the predicted rows.
 __global__ void true_input_kernel(const __nv_bfloat16* X, const __nv_bfloat16* g, int L, int64_t c,
-                                  int d, int64_t R, __nv_bfloat16* xhat, float* ss) {
+                                  int d, int64_t R2, int ss_tiles, __nv_bfloat16* xhat, float* ss) {
   const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (w >= static_cast<int64_t>(L) * c) return;
   const int l = static_cast<int>(w / c);
   const int64_t r = w % c;
   const __nv_bfloat16* src = X + (static_cast<size_t>(l) * c + r) * d;
-  __nv_bfloat16* dst = xhat + (static_cast<size_t>(l) * R + r) * d;
+  __nv_bfloat16* dst = xhat + (static_cast<size_t>(l) * R2 + c + r) * d;
   const __nv_bfloat16* gl = g != nullptr ? g + static_cast<size_t>(l) * d : nullptr;
   float acc = 0.f;
   for (int j = 8 * lane; j < d; j += 256) {
@@ -325,7 +328,8 @@ __global__ void true_input_kernel(const __nv_bfloat16* X, const __nv_bfloat16* g
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) ss[static_cast<size_t>(l) * R + r] = acc;
+  for (int t = lane; t < ss_tiles; t += 32)
+    ss[(static_cast<size_t>(l) * ss_tiles + t) * R2 + c + r] = t == 0 ? acc : 0.f;
 }
 
 __device__ __forceinline__ float row_sq(const __nv_bfloat16* p, int hd) {
@@ -343,9 +347,9 @@ __device__ __forceinline__ float row_sq(const __nv_bfloat16* p, int hd) {
   return s;
 }
 
-// One CTA per (layer, kv head): the mean over rows of |true| / |predicted|.
-__global__ void __launch_bounds__(256) rescale_ratio_kernel(const __nv_bfloat16* pred,
-                                                            const __nv_bfloat16* truth, int64_t R,
+// One CTA per (layer, kv head) of the stacked projections (predicted rows
+// [0, c), true rows [c, 2c)): the mean over rows of |true| / |predicted|.
+__global__ void __launch_bounds__(256) rescale_ratio_kernel(const __nv_bfloat16* proj, int64_t R2,
                                                             int64_t c, int hd, float* scale_ws,
                                                             float* scale_out) {
   __shared__ float s_sum[256];
@@ -354,8 +358,8 @@ __global__ void __launch_bounds__(256) rescale_ratio_kernel(const __nv_bfloat16*
   float sum = 0.f;
   int cnt = 0;
   for (int64_t r = threadIdx.x; r < c; r += blockDim.x) {
-    const float np = row_sq(pred + (plane * R + r) * hd, hd);
-    const float nt = row_sq(truth + (plane * R + r) * hd, hd);
+    const float np = row_sq(proj + (plane * R2 + r) * hd, hd);
+    const float nt = row_sq(proj + (plane * R2 + c + r) * hd, hd);
     if (np > 0.f) {
       sum += sqrtf(nt) / sqrtf(np);
       ++cnt;
@@ -428,14 +432,13 @@ extern "C" rf_status ridgefill_rescale(const rf_rescale_args* a, void* workspace
     return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes", pl.total);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  const int64_t c = a->tail_rows, R = pl.fp.R;
-  uint8_t* kp = ws + pl.off_cache;
-  uint8_t* vp = kp + pl.cache_bytes;
-  uint8_t* kt = vp + pl.cache_bytes;
-  uint8_t* vt = kt + pl.cache_bytes;
+  const int64_t c = a->tail_rows, R2 = pl.R2;
+  const int ss_tiles = a->d_out / pl.fp.bn_map;
+  float* ss = reinterpret_cast<float*>(ws + pl.off_ss);
+  uint8_t* proj = ws + pl.off_cache;
   float* scale = reinterpret_cast<float*>(ws + pl.off_scale);
 
-  // predicted rows: map GEMM, then the K/V GEMM into scratch caches
+  // predicted rows: the map GEMM writes X_hat rows [0, c) of every layer
   MapLaunch m{};
   m.H = a->H_tail;
   m.A = a->A;
@@ -445,51 +448,44 @@ extern "C" rf_status ridgefill_rescale(const rf_rescale_args* a, void* workspace
   m.n_layers = a->n_layers;
   m.slot_layer = -1;
   m.bn = pl.fp.bn_map;
-  m.R = R;
+  m.R = R2;
   m.bias = a->bias;
   m.gain = a->gain;
-  m.xhat = ws + pl.off_xp;
-  m.ss = reinterpret_cast<float*>(ws + pl.off_ssp);
+  m.xhat = ws + pl.off_x;
+  m.ss = ss;
   if ((st = launch_map(m, s)) != RF_OK) return st;
+  // true rows: rows [c, 2c) from g * x
+  const int64_t warps = static_cast<int64_t>(a->n_layers) * c;
+  true_input_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(a->X_true), static_cast<const __nv_bfloat16*>(a->gain),
+      a->n_layers, c, a->d_out, R2, ss_tiles, reinterpret_cast<__nv_bfloat16*>(ws + pl.off_x), ss);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "true-input kernel launch");
+  // one K/V GEMM over the 2c stacked rows, the scaled projection only, into scratch
   rf_fill_args f{};
   f.n_layers = a->n_layers;
   f.d_in = a->d_in;
   f.d_out = a->d_out;
   f.n_kv_heads = a->n_kv_heads;
   f.head_dim = a->head_dim;
-  f.rows = c;
+  f.rows = 2 * c;
   f.pos0 = 0;
-  f.cache_len = R;
-  f.rope_theta = 1e4;  // both projections rotate alike; norms do not depend on it
+  f.cache_len = R2;
+  f.rope_theta = 1e4;  // keys of both inputs rotate alike; the norms do not depend on it
   f.rms_eps = a->rms_eps;
   f.Wk = a->Wk;
   f.Wv = a->Wv;
-  f.Kc = kp;
-  f.Vc = vp;
-  if ((st = launch_kv(&f, pl.fp, 0, c, ws + pl.off_xp, m.ss, s)) != RF_OK) return st;
-
-  // true rows: g * x and sums of squares (one partial per row), then the same K/V GEMM
-  const int64_t warps = static_cast<int64_t>(a->n_layers) * c;
-  true_input_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(a->X_true), static_cast<const __nv_bfloat16*>(a->gain),
-      a->n_layers, c, a->d_out, R, reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xt),
-      reinterpret_cast<float*>(ws + pl.off_sst));
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "true-input kernel launch");
-  FillPlan fp1 = pl.fp;
-  fp1.bn_map = a->d_out;  // one sum-of-squares partial per row
-  f.Kc = kt;
-  f.Vc = vt;
-  if ((st = launch_kv(&f, fp1, 0, c, ws + pl.off_xt, reinterpret_cast<float*>(ws + pl.off_sst), s)) !=
-      RF_OK)
-    return st;
+  f.Kc = proj;
+  f.Vc = proj;
+  FillPlan fp2 = pl.fp;
+  fp2.R = R2;  // row stride of the partial sums
+  if ((st = launch_kv(&f, fp2, 0, 2 * c, ws + pl.off_x, ss, s, a->which)) != RF_OK) return st;
 
   // scales, then the filled rows of the cache in place
   const bool values = a->which == RF_RESCALE_VALUES;
   const int64_t planes = static_cast<int64_t>(a->n_layers) * a->n_kv_heads;
   rescale_ratio_kernel<<<static_cast<unsigned>(planes), 256, 0, s>>>(
-      reinterpret_cast<const __nv_bfloat16*>(values ? vp : kp),
-      reinterpret_cast<const __nv_bfloat16*>(values ? vt : kt), R, c, a->head_dim, scale, a->scale);
+      reinterpret_cast<const __nv_bfloat16*>(proj), R2, c, a->head_dim, scale, a->scale);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rescale ratio launch");
   if (a->rows > 0) {
     const int64_t work = planes * a->rows * (a->head_dim / 8);

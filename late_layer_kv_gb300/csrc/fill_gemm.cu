@@ -180,8 +180,11 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
   const int hpt = p.bn / hd;
   const int head0 = (is_k ? n : n - p.n_k_tiles) * hpt;
   const CUtensorMap* out = &p.tmO[is_k ? 0 : 1];
+  const float* hscale = is_k ? p.k_scale : p.v_scale;
   for (int hh = 0; hh < hpt; ++hh) {
     const uint32_t hc = tcol + hh * hd;
+    // the head's rescale factor folds into the row's RMS scale (both multiply the row)
+    const float rh = hscale != nullptr ? rs * hscale[l * p.n_kv + head0 + hh] : rs;
     if (lane == 0) bulk_wait_read<0>();
     __syncwarp();
     if (is_k) {
@@ -196,8 +199,8 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
           float c0, s0, c1, s1;
           rope_cs(posf, p.inv_freq_hi[i0 + j], p.inv_freq_lo[i0 + j], c0, s0);
           rope_cs(posf, p.inv_freq_hi[i0 + j + 1], p.inv_freq_lo[i0 + j + 1], c1, s1);
-          const float xa = f32(a[j]) * rs, ya = f32(b[j]) * rs;
-          const float xb = f32(a[j + 1]) * rs, yb = f32(b[j + 1]) * rs;
+          const float xa = f32(a[j]) * rh, ya = f32(b[j]) * rh;
+          const float xb = f32(a[j + 1]) * rh, yb = f32(b[j + 1]) * rh;
           w1[j / 2] = pack_bf16(xa * c0 - ya * s0, xb * c1 - yb * s1);
           w2[j / 2] = pack_bf16(ya * c0 + xa * s0, yb * c1 + xb * s1);
         }
@@ -211,7 +214,7 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
         tmem_wait_ld();
         uint32_t w[16];
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) w[j / 2] = pack_bf16(f32(a[j]) * rs, f32(a[j + 1]) * rs);
+        for (int j = 0; j < 32; j += 2) w[j / 2] = pack_bf16(f32(a[j]) * rh, f32(a[j + 1]) * rh);
         stage32(stg + (c0 / 64) * kOutBoxBytes, lane, c0 % 64, w);
       }
     }

@@ -66,6 +66,8 @@ struct GemmParams {
   int32_t pos_base;
   float inv_d;
   float eps;
+  const float* k_scale;  // [L, n_kv] per-head key scale, or null
+  const float* v_scale;  // [L, n_kv] per-head value scale, or null
   // GDN projection epilogue
   __nv_bfloat16* gdn_k;  // [L, H, 2, rows_alloc, dk]: bf16 high part, then the low remainder
   __nv_bfloat16* gdn_v;  // [L, H, 2, rows_alloc, dv], same split

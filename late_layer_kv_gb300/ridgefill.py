@@ -38,6 +38,7 @@ class FillArgs(ctypes.Structure):
         ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_double),
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp), ("copy_events", _vp),
+        ("k_scale", _vp), ("v_scale", _vp),
     ]
 
 
@@ -162,7 +163,7 @@ def _event_array(events):
 
 def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
               rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
-              stage_events=None, copy_events=None) -> FillArgs:
+              stage_events=None, copy_events=None, k_scale=None, v_scale=None) -> FillArgs:
     L, d_out, d_in = A.shape
     rows = H.shape[0]
     n_kv = Kc.shape[1]
@@ -181,6 +182,9 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
     _dev(Wv, "Wv", torch.bfloat16, (L, n_kv * head_dim, d_out))
     _dev(Kc, "Kc", torch.bfloat16, (L, n_kv, cache_len, head_dim))
     _dev(Vc, "Vc", torch.bfloat16, (L, n_kv, cache_len, head_dim))
+    for t, name in ((k_scale, "k_scale"), (v_scale, "v_scale")):
+        if t is not None:
+            _dev(t, name, torch.float32, (L, n_kv))
     ev = _event_array(stage_events)
     cev = _event_array(copy_events)
     if cev is not None and len(copy_events) != 2 * L:
@@ -189,7 +193,8 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
                  rows_per_chunk, float(rope_theta), float(rms_eps), _ptr(H), _ptr(A),
                  _ptr(bias), _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Kc), _ptr(Vc),
                  ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None,
-                 ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None)
+                 ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None,
+                 _ptr(k_scale), _ptr(v_scale))
     a._events_keepalive = (ev, cev)
     return a
 
@@ -213,7 +218,7 @@ def gdn_workspace_size(args: GdnArgs) -> int:
 def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
                    rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
                    workspace: Optional[torch.Tensor] = None, stream=None,
-                   stage_events=None, copy_events=None) -> None:
+                   stage_events=None, copy_events=None, k_scale=None, v_scale=None) -> None:
     """Write the K/V cache of the prefix rows of every late attention layer.
 
     ``H`` [rows, d_in] bf16, ``A`` [L, d_out, d_in] bf16 (device, or pinned host
@@ -221,11 +226,14 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     or None, ``Wk``/``Wv`` [L, n_kv*hd, d_out] bf16, ``Kc``/``Vc``
     [L, n_kv, cache_len, hd] bf16 (positions ``pos0 .. pos0+rows-1`` written).
     ``stage_events``: optional three ``torch.cuda.Event`` recorded around the
-    first chunk's map GEMM and K/V GEMM.
+    first chunk's map GEMM and K/V GEMM.  ``k_scale``/``v_scale``: optional
+    [L, n_kv] f32 per-head factors applied to the keys / values before rounding
+    (the rescale of section 2.3 folded into the fill).
     """
     args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
                      rms_eps=rms_eps, pos0=pos0, rows_per_chunk=rows_per_chunk,
-                     stage_events=stage_events, copy_events=copy_events)
+                     stage_events=stage_events, copy_events=copy_events, k_scale=k_scale,
+                     v_scale=v_scale)
     lib = load()
     need = int(lib.ridgefill_fill_workspace_size(ctypes.byref(args)))
     if need == 0:

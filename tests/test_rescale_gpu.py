@@ -10,7 +10,7 @@ import torch
 
 import oracle
 from synthetic import WORKLOADS, fill_inputs, tail_inputs, to_f64
-from tests._fill_helpers import SENTINEL, oracle_inputs
+from tests._fill_helpers import SENTINEL, compare, new_cache, oracle_inputs, to_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -18,7 +18,7 @@ if not torch.cuda.is_available():
     pytest.skip("needs a CUDA GPU", allow_module_level=True)
 
 from late_layer_kv_gb300 import (  # noqa: E402
-    RF_RESCALE_KEYS, RF_RESCALE_VALUES, device_error, ridgefill_rescale)
+    RF_RESCALE_KEYS, RF_RESCALE_VALUES, device_error, ridgefill_fill, ridgefill_rescale)
 
 # The scale is a mean of norm ratios of bf16-rounded projections (one rounding of
 # g * x_hat and one of the stored projection, each ~2^-9 per element and
@@ -105,3 +105,60 @@ def test_full_size_scales_sampled_layers():
     ref = _oracle_scale(shape, inp, tail, RF_RESCALE_VALUES, layers=layers)
     np.testing.assert_allclose(s[layers].double().numpy(), ref, rtol=SCALE_RTOL)
     _check_apply(Vc, V, s, 4096, 0)
+
+
+@pytest.mark.parametrize("which", [RF_RESCALE_VALUES, RF_RESCALE_KEYS])
+def test_scales_only_then_fused_fill(which):
+    """rows = 0 leaves the caches alone; the scales passed to the fill multiply the
+    filled values (keys) of each head, the other half unchanged."""
+    shape = WORKLOADS["tiny_d256"]
+    inp = fill_inputs(shape, seed=74)
+    tail = tail_inputs(shape, seed=74, c=150)
+    d = to_cuda(inp)
+    t = to_cuda(tail)
+    Kc, Vc = new_cache(shape.n_layers, shape.n_kv, shape.N, shape.head_dim)
+    scale = torch.full((shape.n_layers, shape.n_kv), float("nan"), device="cuda")
+    ridgefill_rescale(t["H_tail"], t["X_true"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc,
+                      which=which, head_dim=shape.head_dim, rms_eps=shape.rms_eps, rows=0,
+                      scale=scale)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    assert bool((Kc == SENTINEL).all()) and bool((Vc == SENTINEL).all()), "rows = 0 wrote the cache"
+    ref = _oracle_scale(shape, inp, tail, which)
+    np.testing.assert_allclose(scale.cpu().double().numpy(), ref, rtol=SCALE_RTOL)
+    kw = {"v_scale": scale} if which == RF_RESCALE_VALUES else {"k_scale": scale}
+    ridgefill_fill(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc,
+                   head_dim=shape.head_dim, rope_theta=shape.rope_theta, rms_eps=shape.rms_eps,
+                   **kw)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    o = oracle_inputs(inp)
+    rows = shape.rows
+    K, V = oracle.fill_attention(o["H"], np.arange(rows), o["A"], o["b"], o["g"], o["Wk"],
+                                 o["Wv"], shape.rms_eps, shape.rope_theta, shape.n_kv,
+                                 shape.head_dim)
+    if which == RF_RESCALE_VALUES:
+        V = V * ref[:, :, None, None]
+    else:
+        K = K * ref[:, :, None, None]
+    gk, gv = to_f64(Kc[:, :, :rows]), to_f64(Vc[:, :, :rows])
+    for l in range(shape.n_layers):
+        compare(gk[l], K[l], f"K layer {l}")
+        compare(gv[l], V[l], f"V layer {l}")
+    assert bool((Kc[:, :, rows:] == SENTINEL).all()) and bool((Vc[:, :, rows:] == SENTINEL).all())
+
+
+def test_unit_scales_are_bitwise_the_plain_fill():
+    shape = WORKLOADS["tiny_d256"]
+    inp = fill_inputs(shape, seed=75)
+    d = to_cuda(inp)
+    ones = torch.ones((shape.n_layers, shape.n_kv), device="cuda")
+    out = []
+    for kw in ({}, {"k_scale": ones, "v_scale": ones}):
+        Kc, Vc = new_cache(shape.n_layers, shape.n_kv, shape.N, shape.head_dim)
+        ridgefill_fill(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc,
+                       head_dim=shape.head_dim, rope_theta=shape.rope_theta,
+                       rms_eps=shape.rms_eps, **kw)
+        out.append((Kc, Vc))
+    torch.cuda.synchronize()
+    assert torch.equal(out[0][0], out[1][0]) and torch.equal(out[0][1], out[1][1])
