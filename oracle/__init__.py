@@ -19,4 +19,7 @@ from .ridgefill import (  # noqa: F401
     gdn_state,
     speedup_ceiling,
     filled_weight_share,
+    quantize_map,
+    dequantize_map,
+    Q8_GROUP,
 )

@@ -32,6 +32,11 @@ Readings where the paper is silent (each applied below):
 * R6 rows: every prefix row is filled; the tail is not touched.
 * R16 value/key rescale: "the ratio of the exact value norm to the predicted
   one, averaged over the c rows" is the mean of the per-row ratios.
+* R18 int8 maps: symmetric absmax groups of 128 consecutive weights of a row,
+  scale ``s = bf16(absmax / 127)``, code ``q = rint(a / s)`` (ties to even,
+  clamped to [-127, 127]); an all-zero group has ``s = 0``, ``q = 0``.  The
+  two divisions that decide ``s`` and ``q`` are IEEE float32 operations, the
+  precision of the kernel that makes the codes; everything after is float64.
 
 Parity status: every function below is pinned by a test in ``tests/`` that
 does not re-evaluate its own formula (closed forms, exact rational
@@ -295,3 +300,44 @@ def filled_weight_share(alpha, n_filled: int):
     for t in range(rows):
         w[t] = np.prod(a[t + 1:])
     return w[:n_filled].sum() / w.sum()
+
+
+# --------------------------------------------------------------------------
+# int8 maps  (section 2.2 "Size and cost"; section 4.2 map format)
+# --------------------------------------------------------------------------
+
+Q8_GROUP = 128  # weights of a row that share one scale
+
+
+def _to_bf16(x):
+    """Round float32 values to the nearest bfloat16 (ties to even); float32 out."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
+    return u.astype(np.uint32).view(np.float32)
+
+
+def quantize_map(A):
+    """int8 codes and bf16 scales of maps ``A`` [..., d_out, d_in] (R18).
+
+    Section 2.2 ("Size and cost") and section 4.2 store the maps as int8 with
+    one scale per 128 weights of each row.  Returns ``q`` [..., d_out, d_in]
+    int8 and ``s`` [..., d_out, d_in / 128] (bf16 values held in float32).
+    """
+    a = np.asarray(A, dtype=np.float32)
+    d_in = a.shape[-1]
+    assert d_in % Q8_GROUP == 0
+    g = a.reshape(a.shape[:-1] + (d_in // Q8_GROUP, Q8_GROUP))
+    amax = np.abs(g).max(axis=-1)
+    s = _to_bf16(amax / np.float32(127.0))
+    safe = np.where(s > 0, s, np.float32(1.0))
+    q = np.rint(g / safe[..., None])
+    q = np.where(s[..., None] > 0, np.clip(q, -127, 127), 0)
+    return q.reshape(a.shape).astype(np.int8), s
+
+
+def dequantize_map(q, s):
+    """The weights ``q * s`` the int8 maps stand for, float64 [..., d_out, d_in]."""
+    qq = np.asarray(q, dtype=np.float64)
+    d_in = qq.shape[-1]
+    g = qq.reshape(qq.shape[:-1] + (d_in // Q8_GROUP, Q8_GROUP))
+    return (g * _f64(s)[..., None]).reshape(qq.shape)
