@@ -150,9 +150,11 @@ def _events(n):
 class AttnWorkload:
     """Attention late layers (ridgefill_fill); maps in HBM or in pinned host memory."""
 
-    def __init__(self, shape: FillShape, host_maps=False, rows_per_chunk=0, rescale_rows=0):
+    def __init__(self, shape: FillShape, host_maps=False, rows_per_chunk=0, rescale_rows=0,
+                 int8_maps=False):
         self.shape, self.host_maps, self.rpc = shape, host_maps, rows_per_chunk
         self.c = rescale_rows
+        self.q8 = int8_maps
         if self.c and host_maps:
             raise ValueError("the rescale needs the maps resident in device memory")
         s = shape
@@ -188,13 +190,22 @@ class AttnWorkload:
         s = self.shape
         self.inp = fill_inputs(s, seed=seed)
         self.d = {k: v.to(dev) for k, v in self.inp.items()}
-        self.A = self.inp["A"].pin_memory() if self.host_maps else self.d["A"]
+        self.A_scale = None
+        if self.q8:  # int8 maps with one bf16 scale per 128 weights, made on the device
+            from late_layer_kv_gb300 import ridgefill_quantize_maps
+            q, sc = ridgefill_quantize_maps(self.d["A"])
+            torch.cuda.synchronize()
+            self.d["A"], self.A_scale = q, sc
+            if self.host_maps:
+                self.A_scale = sc.cpu().pin_memory()
+        self.A = self.d["A"].cpu().pin_memory() if self.host_maps else self.d["A"]
         self.Kc = torch.zeros((s.n_layers, s.n_kv, s.N, s.head_dim), dtype=torch.bfloat16,
                               device=dev)
         self.Vc = torch.zeros_like(self.Kc)
         a = rb.fill_args(self.d["H"], self.A, self.d["b"], self.d["g"], self.d["Wk"],
                          self.d["Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
-                         rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc)
+                         rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc,
+                         A_scale=self.A_scale)
         self.ws = torch.empty(rb.fill_workspace_size(a), dtype=torch.uint8, device=dev)
         self.H_dev = self.d["H"]
         if self.c:
@@ -204,7 +215,8 @@ class AttnWorkload:
             ra = rb.rescale_args(t["H_tail"], t["X_true"], self.A, self.d["b"], self.d["g"],
                                  self.d["Wk"], self.d["Wv"], self.Kc, self.Vc,
                                  which=rb.RF_RESCALE_VALUES, head_dim=s.head_dim,
-                                 rms_eps=s.rms_eps, rows=0, scale=self.scale)
+                                 rms_eps=s.rms_eps, rows=0, scale=self.scale,
+                                 A_scale=self.A_scale)
             self.rws = torch.empty(max(1, rb.load().ridgefill_rescale_workspace_size(
                 ctypes_byref(ra))), dtype=torch.uint8, device=dev)
 
@@ -222,13 +234,14 @@ class AttnWorkload:
             ridgefill_rescale(t["H_tail"], t["X_true"], self.A, d["b"], d["g"], d["Wk"], d["Wv"],
                               self.Kc, self.Vc, which=RF_RESCALE_VALUES, head_dim=s.head_dim,
                               rms_eps=s.rms_eps, rows=0, scale=self.scale,
-                              workspace=self.rws, stream=stream)
+                              workspace=self.rws, stream=stream, A_scale=self.A_scale)
         ridgefill_fill(self.H_dev, self.A, d["b"], d["g"], d["Wk"], d["Wv"], self.Kc, self.Vc,
                        head_dim=s.head_dim, rope_theta=s.rope_theta, rms_eps=s.rms_eps,
                        rows_per_chunk=self.rpc, workspace=self.ws, stream=stream,
                        stage_events=None if ev is None else ev[:3],
                        copy_events=None if (ev is None or not self.host_maps) else
-                       ev[3:3 + 2 * s.n_layers], v_scale=self.scale if self.c else None)
+                       ev[3:3 + 2 * s.n_layers], v_scale=self.scale if self.c else None,
+                       A_scale=self.A_scale)
 
     def copy_ms(self, ev):
         """Durations of the first chunk's per-layer map copies (host maps only)."""
@@ -281,6 +294,7 @@ class AttnWorkload:
         return {"workload": s.name, "d": s.d, "late_layers": s.n_layers, "N": s.N, "T": s.T,
                 "filled_rows": s.rows, "kv_heads": s.n_kv, "head_dim": s.head_dim,
                 "maps": "pinned host, streamed per layer" if self.host_maps else "hbm",
+                "map_format": "int8, one bf16 scale per 128 weights" if self.q8 else "bf16",
                 "rows_per_chunk": self.rpc or s.rows,
                 "value_rescale_tail_rows": self.c,
                 "l2": "inputs larger than L2 (maps %d MiB, split state %d MiB)" % (
@@ -520,7 +534,7 @@ def make_workload(name, args):
     if name.startswith("dense27b") and not rpc:
         rpc = 16384  # late-layer X_hat processed in row chunks
     return AttnWorkload(shape, host_maps=name.startswith("hostmaps"), rows_per_chunk=rpc,
-                        rescale_rows=args.rescale)
+                        rescale_rows=args.rescale, int8_maps=args.int8_maps)
 
 
 # ----------------------------------------------------------------------------- arms
@@ -644,13 +658,15 @@ def run_ours(args):
     if getattr(wl, "host_maps", False):
         s = wl.shape
         link = h2d_rate_gbs(dev)
-        map_bytes = s.n_layers * s.d * s.d * 2
+        # bytes per layer on the link: bf16 maps, or int8 codes plus bf16 scales
+        layer_bytes = s.d * s.d * 2 if not wl.q8 else s.d * s.d + s.d * (s.d // 128) * 2
+        map_bytes = s.n_layers * layer_bytes
         mstage = stages["map_gemm"]["ms"]
         cms = [t for e in ev for t in wl.copy_ms(e)]
-        copy_gbs = (map_bytes / s.n_layers) / (float(np.mean(cms)) / 1000.0) / 1e9
+        copy_gbs = layer_bytes / (float(np.mean(cms)) / 1000.0) / 1e9
         one = wl.A[0].view(-1)  # the maps' own pinned buffer, alone on the link
         tmp = torch.empty_like(one, device=dev)
-        maps_buf = max(one.numel() * 2 / (t / 1000.0) / 1e9 for t in
+        maps_buf = max(one.numel() * one.element_size() / (t / 1000.0) / 1e9 for t in
                        [_copy_ms(tmp, one) for _ in range(10)])
         host_link = {"h2d_gbs_measured": link, "maps_buffer_h2d_gbs": maps_buf,
                      "map_bytes_per_step": map_bytes,
@@ -735,6 +751,8 @@ def main():
     ap.add_argument("--fit", action="store_true",
                     help="benchmark the ridge fit of the workload's maps instead of the fill")
     ap.add_argument("--fit-rows", type=int, default=0)
+    ap.add_argument("--int8-maps", action="store_true",
+                    help="maps as int8 codes with one bf16 scale per 128 weights")
     ap.add_argument("--rescale", type=int, default=0, metavar="C",
                     help="also apply the value rescale from C exact tail rows each step")
     args = ap.parse_args()

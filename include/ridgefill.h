@@ -86,6 +86,14 @@ typedef enum rf_status {
  * copy_events (optional, may be NULL; host maps only): host array of
  *   2 * n_layers cudaEvent_t recorded on the library's copy stream right before
  *   and after the first chunk's copy of map l (entries 2l and 2l + 1).
+ * A_scale (optional, may be NULL): int8 maps.  When set, A holds int8 codes
+ *   q [L, d_out, d_in] and A_scale the bf16 scales s [L, d_out, d_in / 128],
+ *   one per 128 consecutive weights of a row (sections 2.2 "Size and cost"
+ *   and 4.2); the map's weight is q * s, rounded once to bf16 as the GEMM
+ *   stages it (the product has at most 16 significant bits).  d_in must be a
+ *   multiple of 128.  Device memory, or page-locked host memory with
+ *   maps_on_host = 1 (then both arrays are streamed, half the bytes of bf16
+ *   maps).  ridgefill_quantize_maps makes them.
  * k_scale, v_scale (optional, may be NULL): [L, n_kv_heads] f32 device arrays.
  *   When set, every key (value) of head h in layer l is multiplied by
  *   k_scale[l, h] (v_scale[l, h]) before its rounding to bf16: the value or
@@ -117,6 +125,7 @@ typedef struct rf_fill_args {
   void* const* copy_events;
   const float* k_scale;
   const float* v_scale;
+  const void* A_scale;
 } rf_fill_args;
 
 /* Bytes of device workspace ridgefill_fill needs for these arguments
@@ -177,8 +186,8 @@ rf_status ridgefill_fill_noalloc(const rf_fill_args* args, void* stream);
  *              and rounds each value once instead of twice.
  *  H_tail      [c, d_in] bf16, split states of the c tail rows (device).
  *  X_true      [L, c, d_out] bf16, their true inputs to each late layer.
- *  A, bias, gain, Wk, Wv, Kc, Vc, cache_len, rms_eps: as in rf_fill_args
- *              (maps resident in device memory).
+ *  A, A_scale, bias, gain, Wk, Wv, Kc, Vc, cache_len, rms_eps: as in
+ *              rf_fill_args (maps resident in device memory).
  *  scale       optional [L, n_kv_heads] f32 output of the scales (device).
  * All pointers 16-byte aligned.  Asynchronous on `stream`; the cache rows
  * outside [pos0, pos0 + rows) and every other input are left unchanged.
@@ -207,6 +216,7 @@ typedef struct {
   void* Kc;
   void* Vc;
   float* scale;
+  const void* A_scale;
 } rf_rescale_args;
 
 /* Workspace bytes ridgefill_rescale needs (0 on invalid arguments): the
@@ -216,6 +226,35 @@ typedef struct {
 size_t ridgefill_rescale_workspace_size(const rf_rescale_args* args);
 rf_status ridgefill_rescale(const rf_rescale_args* args, void* workspace, size_t workspace_bytes,
                             void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* int8 maps                                                                 */
+/* ------------------------------------------------------------------------ */
+/*
+ * ridgefill_quantize_maps -- the int8 map format of sections 2.2 ("Size and
+ * cost") and 4.2: int8 codes with one bf16 scale per 128 consecutive weights
+ * of each map row.  For every group a[0..127] of a row:
+ *   s = bf16(max|a| / 127)   (float32 division, then rounding to nearest even)
+ *   q = clamp(rint(a / s), -127, 127)   (float32 division, ties to even)
+ * and a group of zeros gets s = 0, q = 0.
+ *
+ *  A       [n_maps, d_out, d_in] f32 (src_bf16 = 0) or bf16 (src_bf16 = 1)
+ *  q       [n_maps, d_out, d_in] int8 (output)
+ *  scale   [n_maps, d_out, d_in / 128] bf16 (output)
+ * All device memory, 16-byte aligned; d_in a multiple of 128.  Asynchronous
+ * on `stream`; the int8 maps then go to rf_fill_args.A / A_scale.
+ */
+typedef struct {
+  int32_t n_maps;
+  int32_t d_out;
+  int32_t d_in;
+  int32_t src_bf16;
+  const void* A;
+  void* q;
+  void* scale;
+} rf_quantize_args;
+
+rf_status ridgefill_quantize_maps(const rf_quantize_args* args, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Gated DeltaNet late layers                                                */
@@ -242,6 +281,7 @@ rf_status ridgefill_rescale(const rf_rescale_args* args, void* workspace, size_t
  * stage_events (optional): host array of four cudaEvent_t recorded on `stream`
  *   before the first chunk's map GEMM, after it, after its projection GEMM and
  *   after its state kernel.
+ * A_scale (optional): int8 maps, as in rf_fill_args.
  */
 typedef struct rf_gdn_args {
   int32_t n_layers;
@@ -267,6 +307,7 @@ typedef struct rf_gdn_args {
   const float* S0;
   float* S;
   void* const* stage_events;
+  const void* A_scale;
 } rf_gdn_args;
 
 size_t ridgefill_gdn_workspace_size(const rf_gdn_args* args);

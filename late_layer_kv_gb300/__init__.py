@@ -15,7 +15,9 @@ from .ridgefill import (  # noqa: F401
     ridgefill_fill_gdn,
     ridgefill_fit_accumulate,
     ridgefill_fit_solve,
+    ridgefill_quantize_maps,
     ridgefill_rescale,
+    Q8_GROUP,
     RF_RESCALE_KEYS,
     RF_RESCALE_VALUES,
     ridgefill_workspace_size,

@@ -133,11 +133,18 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
                                 : static_cast<uint64_t>(m.n_layers) * m.d_out;
   const uint64_t in_row = static_cast<uint64_t>(m.d_in) * 2;
   const uint64_t out_row = static_cast<uint64_t>(m.d_out) * 2;
+  const bool q8 = m.A_scale != nullptr;
   bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.H, m.d_in, m.rows, 1, in_row,
                          0, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   // B boxes of bn / 2 rows: each CTA of a pair stages half of a tile's columns
-  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A, m.d_in, brows, 1,
-                          in_row, 0, kBK, m.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (q8) {
+    p.q8 = static_cast<const int8_t*>(m.A);
+    p.q8_scale = static_cast<const __nv_bfloat16*>(m.A_scale);
+    p.q8_ld = m.d_in;
+  } else {
+    ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A, m.d_in, brows, 1,
+                            in_row, 0, kBK, m.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+  }
   ok = ok && make_tmap_3d(&p.tmO[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.xhat, m.d_out, m.rows,
                           m.n_layers, out_row, out_row * m.R, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the map GEMM");
@@ -159,8 +166,44 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
   const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
   if (pairs <= 0) return RF_OK;
-  cudaError_t e = launch_gemm2(p, pairs, s);
+  cudaError_t e = q8 ? launch_gemm2_q8(p, pairs, s) : launch_gemm2(p, pairs, s);
   if (e != cudaSuccess) return cuda_fail(e, "map GEMM launch");
+  return RF_OK;
+}
+
+size_t map_slot_bytes(int d_out, int d_in, bool q8) {
+  const size_t n = static_cast<size_t>(d_out) * d_in;
+  if (!q8) return n * 2;
+  return align_up(n, 256) + align_up(static_cast<size_t>(d_out) * (d_in / kQ8Group) * 2, 256);
+}
+
+cudaError_t copy_map_layer(uint8_t* slot, const void* A, const void* A_scale, int l, int d_out,
+                           int d_in, cudaStream_t copy, const void** dA, const void** dS) {
+  const size_t n = static_cast<size_t>(d_out) * d_in;
+  if (A_scale == nullptr) {
+    *dA = slot;
+    *dS = nullptr;
+    return cudaMemcpyAsync(slot, static_cast<const uint8_t*>(A) + l * n * 2, n * 2,
+                           cudaMemcpyHostToDevice, copy);
+  }
+  const size_t sb = static_cast<size_t>(d_out) * (d_in / kQ8Group) * 2;
+  uint8_t* sslot = slot + align_up(n, 256);
+  *dA = slot;
+  *dS = sslot;
+  cudaError_t e = cudaMemcpyAsync(slot, static_cast<const uint8_t*>(A) + l * n, n,
+                                  cudaMemcpyHostToDevice, copy);
+  if (e != cudaSuccess) return e;
+  return cudaMemcpyAsync(sslot, static_cast<const uint8_t*>(A_scale) + l * sb, sb,
+                         cudaMemcpyHostToDevice, copy);
+}
+
+rf_status check_pinned(const void* ptr, const char* what) {
+  cudaPointerAttributes attr;
+  cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
+  if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return fail(RF_ERR_NOT_PINNED, "maps_on_host set but %s is not page-locked host memory", what);
+  }
   return RF_OK;
 }
 
@@ -219,7 +262,7 @@ extern "C" double ridgefill_compute_share(int32_t split, int32_t n_layers, int64
   return (S * (N - T) + L * T) / (L * N);
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 3; }
+extern "C" int32_t ridgefill_abi_version(void) { return 4; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {

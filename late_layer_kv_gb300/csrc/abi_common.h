@@ -49,7 +49,8 @@ HostStreamer* host_streamer();  // nullptr on failure (error recorded)
 // map is at A).  Writes X_hat [L, R, d_out] and the sums-of-squares partials.
 struct MapLaunch {
   const void* H;
-  const void* A;
+  const void* A;        // bf16 maps, or int8 codes when A_scale is set
+  const void* A_scale;  // bf16 [maps' rows, d_in / 128] for int8 maps, else null
   int64_t rows;
   int32_t d_in, d_out, n_layers;
   int32_t slot_layer;
@@ -61,5 +62,15 @@ struct MapLaunch {
   float* ss;
 };
 rf_status launch_map(const MapLaunch& m, cudaStream_t s);
+
+// One layer's map in a device slot: bf16 [d_out, d_in], or (q8) int8 codes
+// followed at a 256-byte boundary by the bf16 scales [d_out, d_in / 128].
+size_t map_slot_bytes(int d_out, int d_in, bool q8);
+// Enqueue on `copy` the host-to-device copy of layer l's map (and scales) into
+// `slot`; *dA and *dS receive the slot's code (or bf16) and scale pointers.
+cudaError_t copy_map_layer(uint8_t* slot, const void* A, const void* A_scale, int l, int d_out,
+                           int d_in, cudaStream_t copy, const void** dA, const void** dS);
+// RF_OK if p is page-locked host memory, else RF_ERR_NOT_PINNED with `what` in the message.
+rf_status check_pinned(const void* p, const char* what);
 
 }  // namespace rf

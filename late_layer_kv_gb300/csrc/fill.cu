@@ -42,6 +42,8 @@ rf_status validate_fill(const rf_fill_args* a) {
       a->rows >= (int64_t(1) << 31))
     return fail(RF_ERR_SHAPE, "sizes exceed the 32-bit tile indexing");
   if (a->maps_on_host != 0 && a->maps_on_host != 1) return fail(RF_ERR_ARG, "maps_on_host must be 0 or 1");
+  if (a->A_scale != nullptr && a->d_in % kQ8Group != 0)
+    return fail(RF_ERR_SHAPE, "int8 maps need d_in to be a multiple of 128");
   return RF_OK;
 }
 
@@ -55,7 +57,8 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   pl->off_xhat = 0;
   pl->off_ss = align_up(L * pl->R * d * 2, 256);
   pl->off_slots = align_up(pl->off_ss + L * (d / pl->bn_map) * pl->R * 4, 256);
-  const size_t slots = a->maps_on_host ? kMapSlots * d * static_cast<size_t>(a->d_in) * 2 : 0;
+  const size_t slots =
+      a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0;
   pl->total = align_up(pl->off_slots + slots, 256);
 }
 
@@ -154,13 +157,11 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
   for (const void* p : dev)
     if (p != nullptr && !aligned16(p)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
   if (!aligned16(a->A)) return fail(RF_ERR_ALIGN, "A is not 16-byte aligned");
+  if (a->A_scale != nullptr && !aligned16(a->A_scale))
+    return fail(RF_ERR_ALIGN, "A_scale is not 16-byte aligned");
   if (a->maps_on_host) {
-    cudaPointerAttributes attr;
-    cudaError_t e = cudaPointerGetAttributes(&attr, a->A);
-    if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
-      cudaGetLastError();
-      return fail(RF_ERR_NOT_PINNED, "maps_on_host set but A is not page-locked host memory");
-    }
+    if ((st = check_pinned(a->A, "A")) != RF_OK) return st;
+    if (a->A_scale != nullptr && (st = check_pinned(a->A_scale, "A_scale")) != RF_OK) return st;
   }
   FillPlan pl;
   plan_fill(a, &pl);
@@ -170,7 +171,7 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* xhat = ws + pl.off_xhat;
   float* ss = reinterpret_cast<float*>(ws + pl.off_ss);
-  const size_t map_bytes = static_cast<size_t>(a->d_out) * a->d_in * 2;
+  const size_t slot_bytes = map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr);
 
   HostStreamer* hs = nullptr;
   std::unique_lock<std::mutex> lk(g_host_map_mu, std::defer_lock);
@@ -207,26 +208,26 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     m.ss = ss;
     if (!a->maps_on_host) {
       m.A = a->A;
+      m.A_scale = a->A_scale;
       m.slot_layer = -1;
       st = launch_map(m, s);
       if (st != RF_OK) return st;
     } else {
       for (int l = 0; l < a->n_layers; ++l) {
         const int k = l % kMapSlots;
-        uint8_t* slot = ws + pl.off_slots + k * map_bytes;
+        uint8_t* slot = ws + pl.off_slots + k * slot_bytes;
         cudaError_t e = cudaSuccess;
         cudaEvent_t const* cev = reinterpret_cast<cudaEvent_t const*>(a->copy_events);
         if (start > 0 || l >= kMapSlots) e = cudaStreamWaitEvent(hs->copy, hs->freed[k], 0);
         if (e == cudaSuccess && cev != nullptr && start == 0) e = cudaEventRecord(cev[2 * l], hs->copy);
         if (e == cudaSuccess)
-          e = cudaMemcpyAsync(slot, static_cast<const uint8_t*>(a->A) + l * map_bytes, map_bytes,
-                              cudaMemcpyHostToDevice, hs->copy);
+          e = copy_map_layer(slot, a->A, a->A_scale, l, a->d_out, a->d_in, hs->copy, &m.A,
+                             &m.A_scale);
         if (e == cudaSuccess && cev != nullptr && start == 0)
           e = cudaEventRecord(cev[2 * l + 1], hs->copy);
         if (e == cudaSuccess) e = cudaEventRecord(hs->copied[k], hs->copy);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hs->copied[k], 0);
         if (e != cudaSuccess) return cuda_fail(e, "streaming a map from host memory");
-        m.A = slot;
         m.slot_layer = l;
         st = launch_map(m, s);
         if (st != RF_OK) return st;
@@ -274,6 +275,7 @@ rf_status validate_rescale(const rf_rescale_args* a) {
   f.cache_len = a->cache_len;
   f.rope_theta = 1e4;
   f.rms_eps = a->rms_eps;
+  f.A_scale = a->A_scale;
   return validate_fill(&f);
 }
 
@@ -422,8 +424,8 @@ extern "C" rf_status ridgefill_rescale(const rf_rescale_args* a, void* workspace
   const void* req[] = {a->H_tail, a->X_true, a->A, a->bias, a->Wk, a->Wv, a->Kc, a->Vc};
   for (const void* p : req)
     if (p == nullptr) return fail(RF_ERR_ARG, "a required pointer is NULL");
-  const void* dev[] = {a->H_tail, a->X_true, a->A, a->bias, a->gain, a->Wk,
-                       a->Wv,     a->Kc,     a->Vc, a->scale, workspace};
+  const void* dev[] = {a->H_tail, a->X_true, a->A,  a->A_scale, a->bias, a->gain,
+                       a->Wk,     a->Wv,     a->Kc, a->Vc,      a->scale, workspace};
   for (const void* p : dev)
     if (p != nullptr && !aligned16(p)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
   RescalePlan pl;
@@ -442,6 +444,7 @@ extern "C" rf_status ridgefill_rescale(const rf_rescale_args* a, void* workspace
   MapLaunch m{};
   m.H = a->H_tail;
   m.A = a->A;
+  m.A_scale = a->A_scale;
   m.rows = c;
   m.d_in = a->d_in;
   m.d_out = a->d_out;

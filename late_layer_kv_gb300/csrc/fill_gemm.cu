@@ -622,9 +622,67 @@ __device__ __forceinline__ void decode_pair(int t, const GemmParams& p, int& mp,
   n = rr / gm;
 }
 
+// ---- int8 maps: one converter thread's share of a CTA's B half-tile per stage
+// (rows crow + 32 i of the half, 16 codes at column chunk cch of the 64-wide K block)
+struct Q8Regs {
+  uint4 v[4];
+  uint32_t s[4];  // bf16 bits of each row's scale
+};
+
+__device__ __forceinline__ void q8_fetch(const GemmParams& p, int brow0, int kb, int crow, int cch,
+                                         int nr, Q8Regs& r) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i < nr) {
+      const size_t row = static_cast<size_t>(brow0 + crow + 32 * i);
+      r.v[i] = __ldg(reinterpret_cast<const uint4*>(p.q8 + row * p.q8_ld + kb * kBK + cch * 16));
+      r.s[i] = __ldg(reinterpret_cast<const unsigned short*>(p.q8_scale) +
+                     row * (p.q8_ld / kQ8Group) + (kb * kBK) / kQ8Group);
+    }
+  }
+}
+
+// bf16(q * s) of 16 codes: each byte b becomes the float 2^23 + (b ^ 0x80) by a
+// byte permute, minus 2^23 + 128 gives q exactly, times s is exact in f32 (at
+// most 16 significant bits), and the pack rounds once to bf16.
+__device__ __forceinline__ void q8_dequant16(uint4 v, float sc, uint32_t (&w)[8]) {
+  const uint32_t x[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
+                         v.w ^ 0x80808080u};
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float f0 = __uint_as_float(__byte_perm(x[e], 0x4B000000u, 0x7440)) - 8388736.f;
+    const float f1 = __uint_as_float(__byte_perm(x[e], 0x4B000000u, 0x7441)) - 8388736.f;
+    const float f2 = __uint_as_float(__byte_perm(x[e], 0x4B000000u, 0x7442)) - 8388736.f;
+    const float f3 = __uint_as_float(__byte_perm(x[e], 0x4B000000u, 0x7443)) - 8388736.f;
+    w[2 * e] = pack_bf16(f0 * sc, f1 * sc);
+    w[2 * e + 1] = pack_bf16(f2 * sc, f3 * sc);
+  }
+}
+
+// Write the dequantised rows into the stage in the layout a 128-byte-swizzled TMA
+// box {64, rows} gives (row r at r * 128 bytes, 16-byte chunk c at c ^ (r % 8)).
+__device__ __forceinline__ void q8_store(uint8_t* sb, int crow, int cch, int nr, const Q8Regs& r) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i < nr) {
+      const int row = crow + 32 * i;
+      uint32_t w[8];
+      q8_dequant16(r.v[i], __uint_as_float(r.s[i] << 16), w);
+      uint8_t* rp = sb + row * 128;
+      *reinterpret_cast<uint4*>(rp + (((2 * cch) ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(rp + (((2 * cch + 1) ^ (row & 7)) * 16)) =
+          make_uint4(w[4], w[5], w[6], w[7]);
+    }
+  }
+}
+
 }  // namespace
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+// kQ8: map mode with int8 maps; warps 8-11 dequantise this CTA's B half-tile of each
+// stage into shared memory and arrive on CTA 0's `full` barrier (released at
+// cluster scope; the MMA acquires at cluster scope before reading both halves).
+template <bool kQ8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8 : kGemmThreads, 1)
     rf_gemm2_kernel(const __grid_constant__ GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -648,7 +706,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages2; ++s) {
-      mbar_init(&full[s], 2);   // both CTAs' producers
+      // both CTAs' producers (+ both CTAs' four converter warps)
+      mbar_init(&full[s], kQ8 ? 10 : 2);
       mbar_init(&empty[s], 1);  // CTA 0's commit
     }
     for (int a = 0; a < 2; ++a) {
@@ -661,7 +720,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch(&p.tmA);
-    tma_prefetch(&p.tmB[0]);
+    if (!kQ8) tma_prefetch(&p.tmB[0]);
     if (p.mode == kModeKV || p.mode == kModeGdnProj) tma_prefetch(&p.tmB[1]);
     if (p.mode == kModeGdnProj) {
       tma_prefetch(&p.tmB[2]);
@@ -699,10 +758,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
           const uint32_t fb = full0 + 8 * stage;
           const int half = tb.bn / 2;  // B rows (tile columns) this CTA stages
-          if (rank == 0) mbar_expect_tx(&full[stage], kHalfBytes + half * kBK * 2);
-          else mbar_expect_tx_cl(fb, kHalfBytes + half * kBK * 2);
+          const uint32_t tx = kQ8 ? kHalfBytes : kHalfBytes + half * kBK * 2;
+          if (rank == 0) mbar_expect_tx(&full[stage], tx);
+          else mbar_expect_tx_cl(fb, tx);
           tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, kb * kBK, m * kBM, b);
-          if (tb.seg < 2)
+          if (kQ8) {
+            // B comes from the converter warps
+          } else if (tb.seg < 2)
             tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[tb.seg], fb, kb * kBK,
                              tb.nrow + half * static_cast<int>(rank), b);
           else  // GDN gate tile: CTA 0 stages the alpha weights, CTA 1 the beta weights
@@ -735,7 +797,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_after();
         const uint32_t dt = tmem_base + acc * kBNMax;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.err, kErrMma)) {
+          const bool got = kQ8 ? mbar_wait_acq_cluster(&full[stage], phase, abort_flag, p.err, kErrMma)
+                               : mbar_wait(&full[stage], phase, abort_flag, p.err, kErrMma);
+          if (!got) {
             ok = false;
             break;
           }
@@ -757,7 +821,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       mma_commit_pair(fin, 1);
       mbar_drain(fin, 0);
     }
-  } else if (warp >= 4) {
+  } else if (warp >= 4 && warp < 8) {
     // ---------------- epilogue warpgroup (both CTAs)
     const int q = warp - 4;
     uint8_t* stg = stg_all + q * kOutWarpBytes;
@@ -769,7 +833,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const int acc = it & 1;
       const uint32_t acc_phase = (it >> 1) & 1;
       float rs = 1.f;
-      if (p.mode == kModeKV || p.mode == kModeGdnProj) rs = row_rms_scale(p, b, m * kBM + q * 32 + lane);
+      if (!kQ8 && (p.mode == kModeKV || p.mode == kModeGdnProj))
+        rs = row_rms_scale(p, b, m * kBM + q * 32 + lane);
       if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, kErrEpilogue)) break;
       tc_fence_after();
       const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBNMax;
@@ -777,7 +842,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cl(tempty0 + 8 * acc);
-      } else if (p.mode == kModeMap) {
+      } else if (kQ8 || p.mode == kModeMap) {
         epilogue_map(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
       } else if (p.mode == kModeKV) {
         epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
@@ -787,6 +852,49 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     }
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
+  } else if (kQ8 && warp >= 8) {
+    // ---------------- int8 converters: this CTA's B half of every stage
+    const int ct = static_cast<int>(threadIdx.x) - 256;
+    const int crow = ct >> 2, cch = ct & 3;
+    uint32_t stage = 0, phase = 0;
+    int t = pair, kb = 0;
+    int brow0 = 0, nr = 0;
+    auto tile_rows = [&](int tt) {
+      int mp, n, b;
+      decode_pair(tt, p, mp, n, b);
+      const TileB tb = tile_b(p, n);
+      brow0 = tb.nrow + (tb.bn / 2) * static_cast<int>(rank);
+      nr = tb.bn / 64;  // rows of the half / 32
+    };
+    Q8Regs cur, nxt;
+    if (t < total) {
+      tile_rows(t);
+      q8_fetch(p, brow0, kb, crow, cch, nr, cur);
+    }
+    int cur_nr = nr;
+    while (t < total) {
+      // codes of the next stage are in flight while this one converts
+      int t2 = t, kb2 = kb + 1;
+      if (kb2 == p.k_blocks) {
+        kb2 = 0;
+        t2 += npairs;
+        if (t2 < total) tile_rows(t2);
+      }
+      if (t2 < total) q8_fetch(p, brow0, kb2, crow, cch, nr, nxt);
+      if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrConvert)) break;
+      q8_store(sB + stage * kHalfBytes, crow, cch, cur_nr, cur);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cl(full0 + 8 * stage);
+      cur = nxt;
+      cur_nr = nr;
+      t = t2;
+      kb = kb2;
+      if (++stage == kStages2) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -800,12 +908,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
 cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGemmSmem);
+    cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
     if (e != cudaSuccess) return e;
     configured = true;
   }
-  rf_gemm2_kernel<<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(p);
+  rf_gemm2_kernel<false><<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream) {
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<true>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  rf_gemm2_kernel<true><<<2 * pairs, kGemmThreadsQ8, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

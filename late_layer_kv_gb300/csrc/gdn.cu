@@ -732,6 +732,8 @@ rf_status validate_gdn(const rf_gdn_args* a) {
   if (a->maps_on_host != 0 && a->maps_on_host != 1) return fail(RF_ERR_ARG, "maps_on_host must be 0 or 1");
   if (a->rows >= (int64_t(1) << 31) || static_cast<int64_t>(a->n_layers) * a->d_out >= (int64_t(1) << 31))
     return fail(RF_ERR_SHAPE, "sizes exceed the 32-bit tile indexing");
+  if (a->A_scale != nullptr && a->d_in % kQ8Group != 0)
+    return fail(RF_ERR_SHAPE, "int8 maps need d_in to be a multiple of 128");
   return RF_OK;
 }
 
@@ -746,7 +748,8 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
   pl->off_k = off;     off = align_up(off + L * H * R * kDk * 4, 256);
   pl->off_v = off;     off = align_up(off + L * H * R * kDk * 4, 256);
   pl->off_gate = off;  off = align_up(off + L * 2 * H * R * 4, 256);
-  pl->off_slots = off; off = align_up(off + (a->maps_on_host ? kMapSlots * d * static_cast<size_t>(a->d_in) * 2 : 0), 256);
+  pl->off_slots = off;
+  off = align_up(off + (a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0), 256);
   pl->total = off;
 }
 
@@ -851,13 +854,11 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
   for (const void* q : dev)
     if (q != nullptr && !aligned16(q)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
   if (a->A != nullptr && !aligned16(a->A)) return fail(RF_ERR_ALIGN, "A is not 16-byte aligned");
+  if (a->A_scale != nullptr && !aligned16(a->A_scale))
+    return fail(RF_ERR_ALIGN, "A_scale is not 16-byte aligned");
   if (a->maps_on_host && a->rows > 0) {
-    cudaPointerAttributes attr;
-    cudaError_t e = cudaPointerGetAttributes(&attr, a->A);
-    if (e != cudaSuccess || attr.type != cudaMemoryTypeHost) {
-      cudaGetLastError();
-      return fail(RF_ERR_NOT_PINNED, "maps_on_host set but A is not page-locked host memory");
-    }
+    if ((st = check_pinned(a->A, "A")) != RF_OK) return st;
+    if (a->A_scale != nullptr && (st = check_pinned(a->A_scale, "A_scale")) != RF_OK) return st;
   }
   GdnPlan pl;
   plan_gdn(a, &pl);
@@ -900,7 +901,7 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
 
   HostStreamer* hs = nullptr;
   std::unique_lock<std::mutex> lk(g_gdn_host_map_mu, std::defer_lock);
-  const size_t map_bytes = static_cast<size_t>(a->d_out) * a->d_in * 2;
+  const size_t slot_bytes = map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr);
   if (a->maps_on_host) {
     lk.lock();
     hs = host_streamer();
@@ -932,21 +933,21 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     m.ss = ss;
     if (!a->maps_on_host) {
       m.A = a->A;
+      m.A_scale = a->A_scale;
       m.slot_layer = -1;
       if ((st = launch_map(m, s)) != RF_OK) return st;
     } else {
       for (int l = 0; l < a->n_layers; ++l) {
         const int k = l % kMapSlots;
-        uint8_t* slot = ws + pl.off_slots + k * map_bytes;
+        uint8_t* slot = ws + pl.off_slots + k * slot_bytes;
         cudaError_t e = cudaSuccess;
         if (start > 0 || l >= kMapSlots) e = cudaStreamWaitEvent(hs->copy, hs->freed[k], 0);
         if (e == cudaSuccess)
-          e = cudaMemcpyAsync(slot, static_cast<const uint8_t*>(a->A) + l * map_bytes, map_bytes,
-                              cudaMemcpyHostToDevice, hs->copy);
+          e = copy_map_layer(slot, a->A, a->A_scale, l, a->d_out, a->d_in, hs->copy, &m.A,
+                             &m.A_scale);
         if (e == cudaSuccess) e = cudaEventRecord(hs->copied[k], hs->copy);
         if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hs->copied[k], 0);
         if (e != cudaSuccess) return cuda_fail(e, "streaming a map from host memory");
-        m.A = slot;
         m.slot_layer = l;
         if ((st = launch_map(m, s)) != RF_OK) return st;
         e = cudaEventRecord(hs->freed[k], s);

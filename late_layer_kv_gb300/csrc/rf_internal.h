@@ -18,6 +18,8 @@ constexpr int kBBytes = kBNMax * kBK * 2;
 constexpr int kOutBoxBytes = 64 * 32 * 2;   // one 64-col x 32-row bf16 store box
 constexpr int kOutWarpBytes = 2 * kOutBoxBytes;
 constexpr int kGemmThreads = 256;  // warp 0 TMA, warp 1 MMA, warp 2 TMEM, warps 4-7 epilogue
+constexpr int kGemmThreadsQ8 = 384;  // int8 maps: warps 8-11 convert the B operand
+constexpr int kQ8Group = 128;        // map weights of a row that share one bf16 scale
 constexpr int kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 4 * kOutWarpBytes + 256;
 
 enum GemmMode : int {
@@ -34,6 +36,7 @@ enum ErrSite : int {
   kErrMma = 2,
   kErrEpilogue = 3,
   kErrGdn = 4,
+  kErrConvert = 5,   // int8-map converter warps
   kErrNumeric = 7,   // the ridge system was not positive definite (Cholesky pivot <= 0)
 };
 
@@ -54,6 +57,11 @@ struct GemmParams {
   int32_t d_out;
   int32_t layer_base;  // map mode: layer of B row 0
   int32_t ss_tiles;    // partials per row per layer
+  // int8 maps (map mode on CTA pairs): codes [B rows, q8_ld] and bf16 scales
+  // [B rows, q8_ld / 128]; the converter warps write bf16(q * s) into the B stages
+  const int8_t* q8;
+  const __nv_bfloat16* q8_scale;
+  int32_t q8_ld;
   // map epilogue
   const float* bias;
   const __nv_bfloat16* gain;
@@ -98,6 +106,8 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 // map, K/V and GDN projection modes on CTA pairs (B tensor maps with boxes of half a
 // tile's columns); `pairs` clusters of 2
 cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream);
+// map mode on CTA pairs with int8 maps (p.q8, p.q8_scale); tmB unused
+cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream);
 
 // ------------------------------------------------------------ GDN state
 struct GdnStateParams {

@@ -97,6 +97,36 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
   }
 }
 
+// try_wait with acquire at cluster scope: the phase was completed by arrivals
+// that released writes of the peer CTA (generic stores into its shared memory)
+__device__ __forceinline__ bool mbar_test_acq_cluster(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait with cluster-scope acquire
+__device__ __forceinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t parity,
+                                                      volatile int* abort_flag, int* err, int site) {
+  if (mbar_test_acq_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_test_acq_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, site);
+      return false;
+    }
+  }
+}
+
 // Wait for phase `parity` of `bar` until the time limit only (used to drain
 // copies and MMAs still in flight after another role gave up).
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {

@@ -38,7 +38,7 @@ class FillArgs(ctypes.Structure):
         ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_double),
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp), ("copy_events", _vp),
-        ("k_scale", _vp), ("v_scale", _vp),
+        ("k_scale", _vp), ("v_scale", _vp), ("A_scale", _vp),
     ]
 
 
@@ -51,6 +51,7 @@ class GdnArgs(ctypes.Structure):
         ("rms_eps", ctypes.c_double), ("l2_eps", ctypes.c_double),
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Wa", _vp), ("Wb", _vp), ("S0", _vp), ("S", _vp), ("stage_events", _vp),
+        ("A_scale", _vp),
     ]
 
 
@@ -70,11 +71,19 @@ class RescaleArgs(ctypes.Structure):
         ("tail_rows", ctypes.c_int64), ("rows", ctypes.c_int64), ("pos0", ctypes.c_int64),
         ("cache_len", ctypes.c_int64), ("rms_eps", ctypes.c_double),
         ("H_tail", _vp), ("X_true", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp),
-        ("Wk", _vp), ("Wv", _vp), ("Kc", _vp), ("Vc", _vp), ("scale", _vp),
+        ("Wk", _vp), ("Wv", _vp), ("Kc", _vp), ("Vc", _vp), ("scale", _vp), ("A_scale", _vp),
+    ]
+
+
+class QuantizeArgs(ctypes.Structure):
+    _fields_ = [
+        ("n_maps", ctypes.c_int32), ("d_out", ctypes.c_int32), ("d_in", ctypes.c_int32),
+        ("src_bf16", ctypes.c_int32), ("A", _vp), ("q", _vp), ("scale", _vp),
     ]
 
 
 RF_RESCALE_VALUES, RF_RESCALE_KEYS = 1, 2
+Q8_GROUP = 128  # map weights of a row sharing one bf16 scale
 
 
 class RidgeFillError(RuntimeError):
@@ -112,6 +121,8 @@ def load(rebuild: bool = True) -> ctypes.CDLL:
     lib.ridgefill_rescale_workspace_size.restype = ctypes.c_size_t
     lib.ridgefill_rescale.argtypes = [ctypes.POINTER(RescaleArgs), _vp, ctypes.c_size_t, _vp]
     lib.ridgefill_rescale.restype = ctypes.c_int
+    lib.ridgefill_quantize_maps.argtypes = [ctypes.POINTER(QuantizeArgs), _vp]
+    lib.ridgefill_quantize_maps.restype = ctypes.c_int
     lib.ridgefill_workspace_size.argtypes = [ctypes.c_int32, _vp]
     lib.ridgefill_workspace_size.restype = ctypes.c_size_t
     lib.ridgefill_status_string.argtypes = [ctypes.c_int]
@@ -149,6 +160,26 @@ def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
+def _check_maps(A, A_scale) -> bool:
+    """Maps are bf16 [L, d_out, d_in], or int8 codes with bf16 scales
+    [L, d_out, d_in / 128] when ``A_scale`` is given; device tensors, or pinned
+    host tensors to stream.  Returns whether they live in host memory."""
+    host = not A.is_cuda
+    L, d_out, d_in = A.shape
+    items = [(A, "A", torch.int8 if A_scale is not None else torch.bfloat16, None)]
+    if A_scale is not None:
+        items.append((A_scale, "A_scale", torch.bfloat16, (L, d_out, d_in // Q8_GROUP)))
+    for t, name, dt, shape in items:
+        if host:
+            if t.is_cuda or t.dtype != dt or not t.is_contiguous() or not t.is_pinned():
+                raise ValueError(f"host {name} must be contiguous, pinned {dt}")
+            if shape is not None and tuple(t.shape) != shape:
+                raise ValueError(f"{name} must have shape {shape}")
+        else:
+            _dev(t, name, dt, shape)
+    return host
+
+
 def _stream(stream) -> int:
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -163,18 +194,14 @@ def _event_array(events):
 
 def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
               rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
-              stage_events=None, copy_events=None, k_scale=None, v_scale=None) -> FillArgs:
+              stage_events=None, copy_events=None, k_scale=None, v_scale=None,
+              A_scale=None) -> FillArgs:
     L, d_out, d_in = A.shape
     rows = H.shape[0]
     n_kv = Kc.shape[1]
     cache_len = Kc.shape[2]
-    host = not A.is_cuda
     _dev(H, "H", torch.bfloat16, (rows, d_in))
-    if host:
-        if A.dtype != torch.bfloat16 or not A.is_contiguous() or not A.is_pinned():
-            raise ValueError("host maps must be contiguous, pinned bf16")
-    else:
-        _dev(A, "A", torch.bfloat16)
+    host = _check_maps(A, A_scale)
     _dev(bias, "bias", torch.float32, (L, d_out))
     if gain is not None:
         _dev(gain, "gain", torch.bfloat16, (L, d_out))
@@ -194,7 +221,7 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
                  _ptr(bias), _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Kc), _ptr(Vc),
                  ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None,
                  ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None,
-                 _ptr(k_scale), _ptr(v_scale))
+                 _ptr(k_scale), _ptr(v_scale), _ptr(A_scale))
     a._events_keepalive = (ev, cev)
     return a
 
@@ -218,7 +245,8 @@ def gdn_workspace_size(args: GdnArgs) -> int:
 def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
                    rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
                    workspace: Optional[torch.Tensor] = None, stream=None,
-                   stage_events=None, copy_events=None, k_scale=None, v_scale=None) -> None:
+                   stage_events=None, copy_events=None, k_scale=None, v_scale=None,
+                   A_scale=None) -> None:
     """Write the K/V cache of the prefix rows of every late attention layer.
 
     ``H`` [rows, d_in] bf16, ``A`` [L, d_out, d_in] bf16 (device, or pinned host
@@ -228,12 +256,14 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     ``stage_events``: optional three ``torch.cuda.Event`` recorded around the
     first chunk's map GEMM and K/V GEMM.  ``k_scale``/``v_scale``: optional
     [L, n_kv] f32 per-head factors applied to the keys / values before rounding
-    (the rescale of section 2.3 folded into the fill).
+    (the rescale of section 2.3 folded into the fill).  ``A_scale``: with int8
+    maps ``A`` [L, d_out, d_in], their bf16 scales [L, d_out, d_in / 128]
+    (section 2.2 "Size and cost"; see :func:`ridgefill_quantize_maps`).
     """
     args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
                      rms_eps=rms_eps, pos0=pos0, rows_per_chunk=rows_per_chunk,
                      stage_events=stage_events, copy_events=copy_events, k_scale=k_scale,
-                     v_scale=v_scale)
+                     v_scale=v_scale, A_scale=A_scale)
     lib = load()
     need = int(lib.ridgefill_fill_workspace_size(ctypes.byref(args)))
     if need == 0:
@@ -248,18 +278,13 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
 
 def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
              l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
-             stage_events=None) -> GdnArgs:
+             stage_events=None, A_scale=None) -> GdnArgs:
     L, d_out, d_in = A.shape
     rows = H.shape[0]
     d_k = Wk.shape[1] // n_heads
     d_v = Wv.shape[1] // n_heads
-    host = not A.is_cuda
     _dev(H, "H", torch.bfloat16, (rows, d_in))
-    if host:
-        if A.dtype != torch.bfloat16 or not A.is_contiguous() or not A.is_pinned():
-            raise ValueError("host maps must be contiguous, pinned bf16")
-    else:
-        _dev(A, "A", torch.bfloat16)
+    host = _check_maps(A, A_scale)
     _dev(bias, "bias", torch.float32, (L, d_out))
     if gain is not None:
         _dev(gain, "gain", torch.bfloat16, (L, d_out))
@@ -274,7 +299,7 @@ def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: floa
     a = GdnArgs(L, d_in, d_out, n_heads, d_k, d_v, chunk, 1 if host else 0, rows,
                 rows_per_chunk, float(rms_eps), float(l2_eps), _ptr(H), _ptr(A), _ptr(bias),
                 _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Wa), _ptr(Wb), _ptr(S0), _ptr(S),
-                ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None)
+                ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None, _ptr(A_scale))
     a._events_keepalive = ev
     return a
 
@@ -282,14 +307,15 @@ def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: floa
 def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
                        l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
                        workspace: Optional[torch.Tensor] = None, stream=None,
-                       stage_events=None) -> None:
+                       stage_events=None, A_scale=None) -> None:
     """End-of-fill recurrent state ``S`` [L, H, dv, dk] f32 of Gated DeltaNet layers.
 
     ``stage_events``: optional four ``torch.cuda.Event`` recorded around the first
-    chunk's map GEMM, projection GEMM and state kernel."""
+    chunk's map GEMM, projection GEMM and state kernel.  ``A_scale``: int8 maps, as
+    for :func:`ridgefill_fill`."""
     args = gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, n_heads=n_heads, rms_eps=rms_eps,
                     l2_eps=l2_eps, S0=S0, chunk=chunk, rows_per_chunk=rows_per_chunk,
-                    stage_events=stage_events)
+                    stage_events=stage_events, A_scale=A_scale)
     lib = load()
     need = int(lib.ridgefill_gdn_workspace_size(ctypes.byref(args)))
     if need == 0:
@@ -303,8 +329,11 @@ def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms
 
 
 def rescale_args(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, *, which: int, head_dim: int,
-                 rms_eps: float, rows: int, pos0: int = 0, scale=None) -> RescaleArgs:
+                 rms_eps: float, rows: int, pos0: int = 0, scale=None,
+                 A_scale=None) -> RescaleArgs:
     L, d_out, d_in = A.shape
+    if _check_maps(A, A_scale):
+        raise ValueError("the rescale needs the maps in device memory")
     c = H_tail.shape[0]
     if X_true.shape != (L, c, d_out):
         raise ValueError("X_true must be [L, tail_rows, d_out]")
@@ -317,12 +346,14 @@ def rescale_args(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, *, which: int, h
     a.gain = _ptr(gain) if gain is not None else None
     a.Wk, a.Wv, a.Kc, a.Vc = _ptr(Wk), _ptr(Wv), _ptr(Kc), _ptr(Vc)
     a.scale = _ptr(scale) if scale is not None else None
+    a.A_scale = _ptr(A_scale)
     return a
 
 
 def ridgefill_rescale(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, *, which: int, head_dim: int,
                       rms_eps: float, rows: int, pos0: int = 0, scale=None,
-                      workspace: Optional[torch.Tensor] = None, stream=None) -> None:
+                      workspace: Optional[torch.Tensor] = None, stream=None,
+                      A_scale=None) -> None:
     """Value (or key) rescale of the filled cache rows [pos0, pos0 + rows), section 2.3.
 
     ``H_tail`` [c, d_in] bf16 and ``X_true`` [L, c, d_out] bf16 are the split states and
@@ -330,7 +361,8 @@ def ridgefill_rescale(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, *, which: i
     [L, n_kv] f32 output of the per-head scales.  Other arguments as for
     :func:`ridgefill_fill`."""
     args = rescale_args(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, which=which,
-                        head_dim=head_dim, rms_eps=rms_eps, rows=rows, pos0=pos0, scale=scale)
+                        head_dim=head_dim, rms_eps=rms_eps, rows=rows, pos0=pos0, scale=scale,
+                        A_scale=A_scale)
     lib = load()
     need = int(lib.ridgefill_rescale_workspace_size(ctypes.byref(args)))
     if workspace is None:
@@ -339,6 +371,28 @@ def ridgefill_rescale(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, *, which: i
         raise ValueError(f"workspace needs {need} bytes")
     _check(lib.ridgefill_rescale(ctypes.byref(args), _ptr(workspace),
                                  workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ridgefill_quantize_maps(A, q=None, scale=None, stream=None):
+    """int8 codes and bf16 scales of maps ``A`` [L, d_out, d_in] (f32 or bf16, device):
+    one scale per 128 weights of a row, section 2.2 ("Size and cost").  Returns
+    ``(q, scale)``: [L, d_out, d_in] int8 and [L, d_out, d_in / 128] bf16."""
+    if A.dim() != 3:
+        raise ValueError("A must be [L, d_out, d_in]")
+    L, d_out, d_in = A.shape
+    if A.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("A must be float32 or bfloat16")
+    _dev(A, "A", A.dtype)
+    if q is None:
+        q = torch.empty((L, d_out, d_in), dtype=torch.int8, device=A.device)
+    if scale is None:
+        scale = torch.empty((L, d_out, d_in // Q8_GROUP), dtype=torch.bfloat16, device=A.device)
+    _dev(q, "q", torch.int8, (L, d_out, d_in))
+    _dev(scale, "scale", torch.bfloat16, (L, d_out, d_in // Q8_GROUP))
+    args = QuantizeArgs(L, d_out, d_in, 1 if A.dtype == torch.bfloat16 else 0, _ptr(A), _ptr(q),
+                        _ptr(scale))
+    _check(load().ridgefill_quantize_maps(ctypes.byref(args), _stream(stream)))
+    return q, scale
 
 
 class FitSums:

@@ -53,6 +53,7 @@ def test_ctypes_structs_match_header():
     assert ctypes.sizeof(rb.GdnArgs) == _c_sizeof("rf_gdn_args")
     assert ctypes.sizeof(rb.FitArgs) == _c_sizeof("rf_fit_args")
     assert ctypes.sizeof(rb.RescaleArgs) == _c_sizeof("rf_rescale_args")
+    assert ctypes.sizeof(rb.QuantizeArgs) == _c_sizeof("rf_quantize_args")
 
 
 def test_invalid_arguments_fail_without_a_gpu(lib):
