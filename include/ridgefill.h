@@ -87,11 +87,12 @@ typedef enum rf_status {
  *   2 * n_layers cudaEvent_t recorded on the library's copy stream right before
  *   and after the first chunk's copy of map l (entries 2l and 2l + 1).
  * A_scale (optional, may be NULL): int8 maps.  When set, A holds int8 codes
- *   q [L, d_out, d_in] and A_scale the bf16 scales s [L, d_out, d_in / 128],
- *   one per 128 consecutive weights of a row (sections 2.2 "Size and cost"
- *   and 4.2); the map's weight is q * s, rounded once to bf16 as the GEMM
- *   stages it (the product has at most 16 significant bits).  d_in must be a
- *   multiple of 128.  Device memory, or page-locked host memory with
+ *   q [L, d_out, d_in] and A_scale the bf16 scales, one per 128 consecutive
+ *   weights of a row (sections 2.2 "Size and cost" and 4.2), stored group-major
+ *   [L, d_in / 128, d_out]: the scale of weights 128g .. 128g + 127 of row j
+ *   is A_scale[l, g, j].  The map's weight is q * s, rounded once to bf16 as
+ *   the GEMM stages it (the product has at most 16 significant bits).  d_in
+ *   must be a multiple of 128.  Device memory, or page-locked host memory with
  *   maps_on_host = 1 (then both arrays are streamed, half the bytes of bf16
  *   maps).  ridgefill_quantize_maps makes them.
  * k_scale, v_scale (optional, may be NULL): [L, n_kv_heads] f32 device arrays.
@@ -240,7 +241,8 @@ rf_status ridgefill_rescale(const rf_rescale_args* args, void* workspace, size_t
  *
  *  A       [n_maps, d_out, d_in] f32 (src_bf16 = 0) or bf16 (src_bf16 = 1)
  *  q       [n_maps, d_out, d_in] int8 (output)
- *  scale   [n_maps, d_out, d_in / 128] bf16 (output)
+ *  scale   [n_maps, d_in / 128, d_out] bf16 (output), group-major: the
+ *          scale of weights 128g .. 128g + 127 of row j is scale[l, g, j]
  * All device memory, 16-byte aligned; d_in a multiple of 128.  Asynchronous
  * on `stream`; the int8 maps then go to rf_fill_args.A / A_scale.
  */

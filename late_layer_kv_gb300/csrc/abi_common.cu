@@ -138,6 +138,16 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
                          0, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   // B boxes of bn / 2 rows: each CTA of a pair stages half of a tile's columns
   if (q8) {
+    // codes {d_in, B rows} int8 in boxes {64, bn / 2}; scales [layers, d_in / 128, d_out]
+    // bf16 in boxes {bn / 2} (one 128-weight group of a half tile's rows)
+    const uint64_t groups = static_cast<uint64_t>(m.d_in / kQ8Group);
+    const uint64_t slayers = single ? 1 : static_cast<uint64_t>(m.n_layers);
+    ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.A, m.d_in, brows, 1,
+                            static_cast<uint64_t>(m.d_in), 0, kBK, m.bn / 2,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
+    ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A_scale, m.d_out, groups,
+                            slayers, out_row, out_row * groups, m.bn / 2, 1,
+                            CU_TENSOR_MAP_SWIZZLE_NONE);
     p.q8 = static_cast<const int8_t*>(m.A);
     p.q8_scale = static_cast<const __nv_bfloat16*>(m.A_scale);
     p.q8_ld = m.d_in;
@@ -186,7 +196,7 @@ cudaError_t copy_map_layer(uint8_t* slot, const void* A, const void* A_scale, in
     return cudaMemcpyAsync(slot, static_cast<const uint8_t*>(A) + l * n * 2, n * 2,
                            cudaMemcpyHostToDevice, copy);
   }
-  const size_t sb = static_cast<size_t>(d_out) * (d_in / kQ8Group) * 2;
+  const size_t sb = static_cast<size_t>(d_out) * (d_in / kQ8Group) * 2;  // [d_in / 128, d_out]
   uint8_t* sslot = slot + align_up(n, 256);
   *dA = slot;
   *dS = sslot;

@@ -50,7 +50,7 @@ HostStreamer* host_streamer();  // nullptr on failure (error recorded)
 struct MapLaunch {
   const void* H;
   const void* A;        // bf16 maps, or int8 codes when A_scale is set
-  const void* A_scale;  // bf16 [maps' rows, d_in / 128] for int8 maps, else null
+  const void* A_scale;  // bf16 [layers, d_in / 128, d_out] for int8 maps, else null
   int64_t rows;
   int32_t d_in, d_out, n_layers;
   int32_t slot_layer;
@@ -64,7 +64,7 @@ struct MapLaunch {
 rf_status launch_map(const MapLaunch& m, cudaStream_t s);
 
 // One layer's map in a device slot: bf16 [d_out, d_in], or (q8) int8 codes
-// followed at a 256-byte boundary by the bf16 scales [d_out, d_in / 128].
+// followed at a 256-byte boundary by the bf16 scales [d_in / 128, d_out].
 size_t map_slot_bytes(int d_out, int d_in, bool q8);
 // Enqueue on `copy` the host-to-device copy of layer l's map (and scales) into
 // `slot`; *dA and *dS receive the slot's code (or bf16) and scale pointers.

@@ -622,25 +622,22 @@ __device__ __forceinline__ void decode_pair(int t, const GemmParams& p, int& mp,
   n = rr / gm;
 }
 
-// ---- int8 maps: one converter thread's share of a CTA's B half-tile per stage
-// (rows crow + 32 i of the half, 16 codes at column chunk cch of the 64-wide K block)
-struct Q8Regs {
-  uint4 v[4];
-  uint32_t s[4];  // bf16 bits of each row's scale
-};
-
-__device__ __forceinline__ void q8_fetch(const GemmParams& p, int brow0, int kb, int crow, int cch,
-                                         int nr, Q8Regs& r) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (i < nr) {
-      const size_t row = static_cast<size_t>(brow0 + crow + 32 * i);
-      r.v[i] = __ldg(reinterpret_cast<const uint4*>(p.q8 + row * p.q8_ld + kb * kBK + cch * 16));
-      r.s[i] = __ldg(reinterpret_cast<const unsigned short*>(p.q8_scale) +
-                     row * (p.q8_ld / kQ8Group) + (kb * kBK) / kQ8Group);
-    }
-  }
-}
+// ---- int8 maps.  A third ring ("raw", kRawStages deep) holds this CTA's half of
+// each B tile as int8 codes (box {64, bn / 2}, no swizzle: row r at r * 64 bytes)
+// and the rows' bf16 scales of the stage's 128-weight group (box {bn / 2}); a
+// producer thread (warp 3) fills it by TMA and the converter warps turn it into
+// the bf16 stage the MMA reads.
+constexpr int kRawBytes = 128 * kBK;      // int8 codes of a half tile
+constexpr int kRawScaleBytes = 128 * 2;   // bf16 scales of its rows
+constexpr int kStagesQ8 = 4;              // bf16 MMA stages with int8 maps
+constexpr int kRawStages = 7;
+// scale ring padded so the epilogue's 128-byte-swizzled staging stays 1024-byte aligned
+constexpr int kRawScaleRegion = (kRawStages * kRawScaleBytes + 1023) / 1024 * 1024;
+static_assert(1024 + kStages2 * 2 * kHalfBytes + 4 * kOutWarpBytes + 8 * (2 * kStages2 + 5) + 8 <=
+                  kGemmSmem, "pair GEMM shared memory");
+static_assert(1024 + kStagesQ8 * 2 * kHalfBytes + kRawStages * kRawBytes + kRawScaleRegion +
+                      4 * kOutWarpBytes + 8 * (2 * kStagesQ8 + 5 + 2 * kRawStages) + 8 <=
+                  kGemmSmem, "int8 pair GEMM shared memory");
 
 // bf16(q * s) of 16 codes: each byte b becomes the float 2^23 + (b ^ 0x80) by a
 // byte permute, minus 2^23 + 128 gives q exactly, times s is exact in f32 (at
@@ -659,15 +656,19 @@ __device__ __forceinline__ void q8_dequant16(uint4 v, float sc, uint32_t (&w)[8]
   }
 }
 
-// Write the dequantised rows into the stage in the layout a 128-byte-swizzled TMA
-// box {64, rows} gives (row r at r * 128 bytes, 16-byte chunk c at c ^ (r % 8)).
-__device__ __forceinline__ void q8_store(uint8_t* sb, int crow, int cch, int nr, const Q8Regs& r) {
+// Converter thread (crow, cch): rows crow + 32 i of the half tile, the 16 codes of
+// column chunk cch; writes them as bf16 in the layout a 128-byte-swizzled TMA box
+// {64, rows} gives (row r at r * 128 bytes, 16-byte chunk c at c ^ (r % 8)).
+__device__ __forceinline__ void q8_convert(const uint8_t* raw, const uint8_t* rsc, uint8_t* sb,
+                                           int crow, int cch, int nr) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     if (i < nr) {
       const int row = crow + 32 * i;
+      const uint4 v = *reinterpret_cast<const uint4*>(raw + row * kBK + cch * 16);
+      const uint32_t sbits = *reinterpret_cast<const uint16_t*>(rsc + row * 2);
       uint32_t w[8];
-      q8_dequant16(r.v[i], __uint_as_float(r.s[i] << 16), w);
+      q8_dequant16(v, __uint_as_float(sbits << 16), w);
       uint8_t* rp = sb + row * 128;
       *reinterpret_cast<uint4*>(rp + (((2 * cch) ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4*>(rp + (((2 * cch + 1) ^ (row & 7)) * 16)) =
@@ -678,25 +679,31 @@ __device__ __forceinline__ void q8_store(uint8_t* sb, int crow, int cch, int nr,
 
 }  // namespace
 
-// kQ8: map mode with int8 maps; warps 8-11 dequantise this CTA's B half-tile of each
-// stage into shared memory and arrive on CTA 0's `full` barrier (released at
-// cluster scope; the MMA acquires at cluster scope before reading both halves).
+// kQ8: map mode with int8 maps (tmB[0]: codes {d_in, B rows, 1} uint8; tmB[1]: scales
+// {d_out, d_in / 128, layers} bf16).  Warps 8-11 dequantise this CTA's B half of each
+// stage into shared memory and arrive on CTA 0's `full` barrier (released at cluster
+// scope; the MMA acquires at cluster scope before reading both halves).
 template <bool kQ8>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8 : kGemmThreads, 1)
     rf_gemm2_kernel(const __grid_constant__ GemmParams p) {
+  constexpr int kS = kQ8 ? kStagesQ8 : kStages2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = sA + kStages2 * kHalfBytes;
-  uint8_t* stg_all = sB + kStages2 * kHalfBytes;
+  uint8_t* sB = sA + kS * kHalfBytes;
+  uint8_t* sRaw = sB + kS * kHalfBytes;                           // kQ8 only
+  uint8_t* sRawScale = sRaw + (kQ8 ? kRawStages * kRawBytes : 0);  // kQ8 only
+  uint8_t* stg_all = sRawScale + (kQ8 ? kRawScaleRegion : 0);
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 4 * kOutWarpBytes);
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages2;
-  uint64_t* tfull = bars + 2 * kStages2;
+  uint64_t* empty = bars + kS;
+  uint64_t* tfull = bars + 2 * kS;
   uint64_t* tempty = tfull + 2;
   uint64_t* fin = tempty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+  uint64_t* raw_full = fin + 1;                            // kQ8 only
+  uint64_t* raw_empty = raw_full + (kQ8 ? kRawStages : 0);  // kQ8 only
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_empty + (kQ8 ? kRawStages : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -705,7 +712,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages2; ++s) {
+    for (int s = 0; s < kS; ++s) {
       // both CTAs' producers (+ both CTAs' four converter warps)
       mbar_init(&full[s], kQ8 ? 10 : 2);
       mbar_init(&empty[s], 1);  // CTA 0's commit
@@ -715,14 +722,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       mbar_init(&tempty[a], 8);  // four epilogue warps in each CTA
     }
     mbar_init(fin, 1);
+    if (kQ8) {
+      for (int s = 0; s < kRawStages; ++s) {
+        mbar_init(&raw_full[s], 1);   // this CTA's raw producer (+ its copies' bytes)
+        mbar_init(&raw_empty[s], 4);  // this CTA's converter warps
+      }
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch(&p.tmA);
-    if (!kQ8) tma_prefetch(&p.tmB[0]);
-    if (p.mode == kModeKV || p.mode == kModeGdnProj) tma_prefetch(&p.tmB[1]);
-    if (p.mode == kModeGdnProj) {
+    tma_prefetch(&p.tmB[0]);
+    if (kQ8 || p.mode == kModeKV || p.mode == kModeGdnProj) tma_prefetch(&p.tmB[1]);
+    if (!kQ8 && p.mode == kModeGdnProj) {
       tma_prefetch(&p.tmB[2]);
       tma_prefetch(&p.tmB[3]);
     }
@@ -743,8 +756,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
     if (lane == 0) {
       // ---------------- TMA producer of this CTA's halves
       uint32_t stage = 0, phase = 0;
-      int issued[kStages2];
-      for (int s = 0; s < kStages2; ++s) issued[s] = -1;
+      int issued[kS];
+      for (int s = 0; s < kS; ++s) issued[s] = -1;
       bool ok = true;
       for (int t = pair; t < total && ok; t += npairs) {
         int mp, n, b;
@@ -770,14 +783,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
           else  // GDN gate tile: CTA 0 stages the alpha weights, CTA 1 the beta weights
             tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[2 + rank], fb, kb * kBK, 0, b);
           issued[stage] = static_cast<int>(phase);
-          if (++stage == kStages2) {
+          if (++stage == kS) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
       if (!ok && rank == 0)  // let the copies counted on this CTA's barriers land
-        for (int s = 0; s < kStages2; ++s)
+        for (int s = 0; s < kS; ++s)
           if (issued[s] >= 0) mbar_drain(&full[s], static_cast<uint32_t>(issued[s]));
     }
   } else if (warp == 1) {
@@ -810,7 +823,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
           for (int k = 0; k < kBK / 16; ++k)
             mma_bf16_pair(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
           mma_commit_pair(&empty[stage], 3);
-          if (++stage == kStages2) {
+          if (++stage == kS) {
             stage = 0;
             phase ^= 1;
           }
@@ -820,6 +833,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       // every MMA issued has finished before TMEM is released
       mma_commit_pair(fin, 1);
       mbar_drain(fin, 0);
+    }
+  } else if (kQ8 && warp == 3) {
+    if (lane == 0) {
+      // ---------------- int8 producer: this CTA's codes and scales of every stage
+      uint32_t rs = 0, rphase = 0;
+      int issued[kRawStages];
+      for (int s = 0; s < kRawStages; ++s) issued[s] = -1;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        int mp, n, b;
+        decode_pair(t, p, mp, n, b);
+        const TileB tb = tile_b(p, n);
+        const int half = tb.bn / 2;
+        const int brow0 = tb.nrow + half * static_cast<int>(rank);
+        const int l = brow0 / p.d_out, j0 = brow0 - l * p.d_out;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          if (!mbar_wait(&raw_empty[rs], rphase ^ 1, abort_flag, p.err, kErrProducer)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&raw_full[rs], half * (kBK + 2));
+          tma_load_3d(smem_u32(sRaw + rs * kRawBytes), &p.tmB[0], &raw_full[rs], kb * kBK, brow0, 0);
+          tma_load_3d(smem_u32(sRawScale + rs * kRawScaleBytes), &p.tmB[1], &raw_full[rs], j0,
+                      (kb * kBK) / kQ8Group, l);
+          issued[rs] = static_cast<int>(rphase);
+          if (++rs == kRawStages) {
+            rs = 0;
+            rphase ^= 1;
+          }
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < kRawStages; ++s)
+          if (issued[s] >= 0) mbar_drain(&raw_full[s], static_cast<uint32_t>(issued[s]));
     }
   } else if (warp >= 4 && warp < 8) {
     // ---------------- epilogue warpgroup (both CTAs)
@@ -853,46 +900,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
   } else if (kQ8 && warp >= 8) {
-    // ---------------- int8 converters: this CTA's B half of every stage
+    // ---------------- int8 converters: raw stage -> bf16 B stage of this CTA
     const int ct = static_cast<int>(threadIdx.x) - 256;
     const int crow = ct >> 2, cch = ct & 3;
-    uint32_t stage = 0, phase = 0;
-    int t = pair, kb = 0;
-    int brow0 = 0, nr = 0;
-    auto tile_rows = [&](int tt) {
+    uint32_t stage = 0, phase = 0, rs = 0, rphase = 0;
+    bool ok = true;
+    for (int t = pair; t < total && ok; t += npairs) {
       int mp, n, b;
-      decode_pair(tt, p, mp, n, b);
-      const TileB tb = tile_b(p, n);
-      brow0 = tb.nrow + (tb.bn / 2) * static_cast<int>(rank);
-      nr = tb.bn / 64;  // rows of the half / 32
-    };
-    Q8Regs cur, nxt;
-    if (t < total) {
-      tile_rows(t);
-      q8_fetch(p, brow0, kb, crow, cch, nr, cur);
-    }
-    int cur_nr = nr;
-    while (t < total) {
-      // codes of the next stage are in flight while this one converts
-      int t2 = t, kb2 = kb + 1;
-      if (kb2 == p.k_blocks) {
-        kb2 = 0;
-        t2 += npairs;
-        if (t2 < total) tile_rows(t2);
-      }
-      if (t2 < total) q8_fetch(p, brow0, kb2, crow, cch, nr, nxt);
-      if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrConvert)) break;
-      q8_store(sB + stage * kHalfBytes, crow, cch, cur_nr, cur);
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cl(full0 + 8 * stage);
-      cur = nxt;
-      cur_nr = nr;
-      t = t2;
-      kb = kb2;
-      if (++stage == kStages2) {
-        stage = 0;
-        phase ^= 1;
+      decode_pair(t, p, mp, n, b);
+      const int nr = tile_b(p, n).bn / 64;  // rows of the half / 32
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!mbar_wait(&raw_full[rs], rphase, abort_flag, p.err, kErrConvert) ||
+            !mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrConvert)) {
+          ok = false;
+          break;
+        }
+        q8_convert(sRaw + rs * kRawBytes, sRawScale + rs * kRawScaleBytes,
+                   sB + stage * kHalfBytes, crow, cch, nr);
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_cl(full0 + 8 * stage);
+          mbar_arrive(&raw_empty[rs]);
+        }
+        if (++stage == kS) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++rs == kRawStages) {
+          rs = 0;
+          rphase ^= 1;
+        }
       }
     }
   }

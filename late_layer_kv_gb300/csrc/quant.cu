@@ -12,9 +12,11 @@ namespace {
 // One warp per group of 128 weights (lane i holds weights 4i .. 4i + 3):
 // s = bf16(max|a| / 127), q = clamp(rint(a / s), -127, 127), both divisions in
 // IEEE float32 (round to nearest), rint ties to even; a zero group gets s = q = 0.
+// The scale of group gi of map row j in layer l is stored at [l, gi, j].
 template <bool kBf16>
 __global__ void __launch_bounds__(256) quantize_kernel(const void* A, uint32_t* q,
-                                                       __nv_bfloat16* scale, int64_t groups) {
+                                                       __nv_bfloat16* scale, int64_t groups,
+                                                       int d_out, int G) {
   const int lane = threadIdx.x & 31;
   const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
   for (int64_t g = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; g < groups;
@@ -44,7 +46,11 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* A, uint32_t* 
       }
     }
     q[g * 32 + lane] = packed;
-    if (lane == 0) scale[g] = sb;
+    if (lane == 0) {
+      const int64_t row = g / G, gi = g - row * G;  // row = l * d_out + j
+      const int64_t l = row / d_out, j = row - l * d_out;
+      scale[(l * G + gi) * d_out + j] = sb;
+    }
   }
 }
 
@@ -68,8 +74,9 @@ extern "C" rf_status ridgefill_quantize_maps(const rf_quantize_args* a, void* st
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto* q = static_cast<uint32_t*>(a->q);
   auto* sc = static_cast<__nv_bfloat16*>(a->scale);
-  if (a->src_bf16) quantize_kernel<true><<<blocks, 256, 0, s>>>(a->A, q, sc, groups);
-  else quantize_kernel<false><<<blocks, 256, 0, s>>>(a->A, q, sc, groups);
+  const int G = a->d_in / kQ8Group;
+  if (a->src_bf16) quantize_kernel<true><<<blocks, 256, 0, s>>>(a->A, q, sc, groups, a->d_out, G);
+  else quantize_kernel<false><<<blocks, 256, 0, s>>>(a->A, q, sc, groups, a->d_out, G);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "quantize launch");
   return RF_OK;

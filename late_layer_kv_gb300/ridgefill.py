@@ -161,14 +161,14 @@ def _dev(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
 
 
 def _check_maps(A, A_scale) -> bool:
-    """Maps are bf16 [L, d_out, d_in], or int8 codes with bf16 scales
-    [L, d_out, d_in / 128] when ``A_scale`` is given; device tensors, or pinned
+    """Maps are bf16 [L, d_out, d_in], or int8 codes with group-major bf16 scales
+    [L, d_in / 128, d_out] when ``A_scale`` is given; device tensors, or pinned
     host tensors to stream.  Returns whether they live in host memory."""
     host = not A.is_cuda
     L, d_out, d_in = A.shape
     items = [(A, "A", torch.int8 if A_scale is not None else torch.bfloat16, None)]
     if A_scale is not None:
-        items.append((A_scale, "A_scale", torch.bfloat16, (L, d_out, d_in // Q8_GROUP)))
+        items.append((A_scale, "A_scale", torch.bfloat16, (L, d_in // Q8_GROUP, d_out)))
     for t, name, dt, shape in items:
         if host:
             if t.is_cuda or t.dtype != dt or not t.is_contiguous() or not t.is_pinned():
@@ -257,7 +257,7 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     first chunk's map GEMM and K/V GEMM.  ``k_scale``/``v_scale``: optional
     [L, n_kv] f32 per-head factors applied to the keys / values before rounding
     (the rescale of section 2.3 folded into the fill).  ``A_scale``: with int8
-    maps ``A`` [L, d_out, d_in], their bf16 scales [L, d_out, d_in / 128]
+    maps ``A`` [L, d_out, d_in], their bf16 scales [L, d_in / 128, d_out]
     (section 2.2 "Size and cost"; see :func:`ridgefill_quantize_maps`).
     """
     args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
@@ -376,7 +376,8 @@ def ridgefill_rescale(H_tail, X_true, A, bias, gain, Wk, Wv, Kc, Vc, *, which: i
 def ridgefill_quantize_maps(A, q=None, scale=None, stream=None):
     """int8 codes and bf16 scales of maps ``A`` [L, d_out, d_in] (f32 or bf16, device):
     one scale per 128 weights of a row, section 2.2 ("Size and cost").  Returns
-    ``(q, scale)``: [L, d_out, d_in] int8 and [L, d_out, d_in / 128] bf16."""
+    ``(q, scale)``: [L, d_out, d_in] int8 and [L, d_in / 128, d_out] bf16 (the scale
+    of weights 128g .. 128g + 127 of row j at [l, g, j])."""
     if A.dim() != 3:
         raise ValueError("A must be [L, d_out, d_in]")
     L, d_out, d_in = A.shape
@@ -386,9 +387,9 @@ def ridgefill_quantize_maps(A, q=None, scale=None, stream=None):
     if q is None:
         q = torch.empty((L, d_out, d_in), dtype=torch.int8, device=A.device)
     if scale is None:
-        scale = torch.empty((L, d_out, d_in // Q8_GROUP), dtype=torch.bfloat16, device=A.device)
+        scale = torch.empty((L, d_in // Q8_GROUP, d_out), dtype=torch.bfloat16, device=A.device)
     _dev(q, "q", torch.int8, (L, d_out, d_in))
-    _dev(scale, "scale", torch.bfloat16, (L, d_out, d_in // Q8_GROUP))
+    _dev(scale, "scale", torch.bfloat16, (L, d_in // Q8_GROUP, d_out))
     args = QuantizeArgs(L, d_out, d_in, 1 if A.dtype == torch.bfloat16 else 0, _ptr(A), _ptr(q),
                         _ptr(scale))
     _check(load().ridgefill_quantize_maps(ctypes.byref(args), _stream(stream)))

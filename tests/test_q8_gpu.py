@@ -24,10 +24,15 @@ from late_layer_kv_gb300 import (  # noqa: E402
     ridgefill_rescale)
 
 
+def _rowmajor(s):
+    """Group-major scales [L, G, d_out] as [L, d_out, G] (the oracle's layout)."""
+    return s.transpose(1, 2).contiguous()
+
+
 def _bf16_of_codes(q, s):
     """bf16(q * s) per weight (q * s is exact in f32), as CPU bf16."""
     L, d_out, d_in = q.shape
-    w = q.float().reshape(L, d_out, d_in // 128, 128) * s.float()[..., None]
+    w = q.float().reshape(L, d_out, d_in // 128, 128) * _rowmajor(s).float()[..., None]
     return w.reshape(L, d_out, d_in).to(torch.bfloat16)
 
 
@@ -49,7 +54,7 @@ def test_quantizer_bitwise_equals_oracle(src):
     q, s = _quantize(A)
     q_ref, s_ref = oracle.quantize_map(A.float().numpy())
     assert np.array_equal(q.numpy(), q_ref)
-    assert np.array_equal(s.float().numpy(), s_ref)
+    assert np.array_equal(_rowmajor(s).float().numpy(), s_ref)
 
 
 def _fill(shape, d, A, A_scale=None, host=False, rows_per_chunk=0):
@@ -80,7 +85,7 @@ def test_int8_fill_matches_oracle_and_bf16_path(shape):
     Kb, Vb = _fill(shape, d, _bf16_of_codes(q.cpu(), s.cpu()).cuda())
     assert torch.equal(K8, Kb) and torch.equal(V8, Vb)
     o = oracle_inputs(inp)
-    Aq = oracle.dequantize_map(q.cpu().numpy(), s.cpu().float().numpy())
+    Aq = oracle.dequantize_map(q.cpu().numpy(), _rowmajor(s.cpu()).float().numpy())
     rows = shape.rows
     K, V = oracle.fill_attention(o["H"], np.arange(rows), Aq, o["b"], o["g"], o["Wk"], o["Wv"],
                                  shape.rms_eps, shape.rope_theta, shape.n_kv, shape.head_dim)
