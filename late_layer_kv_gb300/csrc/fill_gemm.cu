@@ -639,20 +639,22 @@ static_assert(1024 + kStagesQ8 * 2 * kHalfBytes + kRawStages * kRawBytes + kRawS
                       4 * kOutWarpBytes + 8 * (2 * kStagesQ8 + 5 + 2 * kRawStages) + 8 <=
                   kGemmSmem, "int8 pair GEMM shared memory");
 
-// bf16(q * s) of 16 codes: each byte b becomes the float 2^23 + (b ^ 0x80) by a
-// byte permute, minus 2^23 + 128 gives q exactly, times s is exact in f32 (at
-// most 16 significant bits), and the pack rounds once to bf16.
-__device__ __forceinline__ void q8_dequant16(uint4 v, float sc, uint32_t (&w)[8]) {
+// bf16(q * s) of 16 codes.  A byte permute turns u = b ^ 0x80 = q + 128 into the
+// float 2^15 + u (bits 0x47 : 00 : u : 00); one FMA with c = -(2^15 + 128) s, which
+// f32 holds exactly (9 x 8 significant bits), gives (2^15 + u) s + c = q s exactly
+// before its rounding, and q s (at most 16 significant bits) survives it; the pack
+// rounds once to bf16.
+__device__ __forceinline__ void q8_dequant16(uint4 v, float sc, float c, uint32_t (&w)[8]) {
   const uint32_t x[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
                          v.w ^ 0x80808080u};
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float f0 = __uint_as_float(__byte_perm(x[e], 0x4B000000u, 0x7440)) - 8388736.f;
-    const float f1 = __uint_as_float(__byte_perm(x[e], 0x4B000000u, 0x7441)) - 8388736.f;
-    const float f2 = __uint_as_float(__byte_perm(x[e], 0x4B000000u, 0x7442)) - 8388736.f;
-    const float f3 = __uint_as_float(__byte_perm(x[e], 0x4B000000u, 0x7443)) - 8388736.f;
-    w[2 * e] = pack_bf16(f0 * sc, f1 * sc);
-    w[2 * e + 1] = pack_bf16(f2 * sc, f3 * sc);
+    const float f0 = fmaf(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7504)), sc, c);
+    const float f1 = fmaf(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7514)), sc, c);
+    const float f2 = fmaf(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7524)), sc, c);
+    const float f3 = fmaf(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7534)), sc, c);
+    w[2 * e] = pack_bf16(f0, f1);
+    w[2 * e + 1] = pack_bf16(f2, f3);
   }
 }
 
@@ -666,9 +668,9 @@ __device__ __forceinline__ void q8_convert(const uint8_t* raw, const uint8_t* rs
     if (i < nr) {
       const int row = crow + 32 * i;
       const uint4 v = *reinterpret_cast<const uint4*>(raw + row * kBK + cch * 16);
-      const uint32_t sbits = *reinterpret_cast<const uint16_t*>(rsc + row * 2);
+      const float sc = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rsc + row * 2)) << 16);
       uint32_t w[8];
-      q8_dequant16(v, __uint_as_float(sbits << 16), w);
+      q8_dequant16(v, sc, -32896.f * sc, w);
       uint8_t* rp = sb + row * 128;
       *reinterpret_cast<uint4*>(rp + (((2 * cch) ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
       *reinterpret_cast<uint4*>(rp + (((2 * cch + 1) ^ (row & 7)) * 16)) =
@@ -920,7 +922,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         fence_async_smem();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_cl(full0 + 8 * stage);
+          if (rank == 0) {
+            mbar_arrive(&full[stage]);  // release at CTA scope; the MMA issuer is in this CTA
+          } else {
+            // this CTA's shared-memory writes, released to the peer's MMA issuer
+            fence_release_smem_cluster();
+            mbar_arrive_relaxed_cl(full0 + 8 * stage);
+          }
           mbar_arrive(&raw_empty[rs]);
         }
         if (++stage == kS) {

@@ -268,6 +268,16 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t saddr, uint32_t rank) 
 __device__ __forceinline__ void mbar_arrive_cl(uint32_t addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
 }
+// release fence restricted to this CTA's shared memory, at cluster scope: orders the
+// thread's prior shared::cta accesses (and those it has observed) before its later
+// arrivals on a peer CTA's mbarrier, without ordering global memory
+__device__ __forceinline__ void fence_release_smem_cluster() {
+  asm volatile("fence.release.sync_restrict::shared::cta.cluster;" ::: "memory");
+}
+// relaxed arrive on an mbarrier given by its shared::cluster address
+__device__ __forceinline__ void mbar_arrive_relaxed_cl(uint32_t addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
+}
 // arrive and add expected transaction bytes on an mbarrier of this or the peer
 // CTA; relaxed: the bytes themselves are counted by the copies' complete_tx
 __device__ __forceinline__ void mbar_expect_tx_cl(uint32_t addr, uint32_t bytes) {
