@@ -631,6 +631,8 @@ constexpr int kRawBytes = 128 * kBK;      // int8 codes of a half tile
 constexpr int kRawScaleBytes = 128 * 2;   // bf16 scales of its rows
 constexpr int kStagesQ8 = 4;              // bf16 MMA stages with int8 maps
 constexpr int kRawStages = 7;
+constexpr int kConvGroups = 2;            // converter warp groups taking alternate stages
+static_assert(kStagesQ8 % kConvGroups == 0, "each converter group keeps to its own MMA stages");
 // scale ring padded so the epilogue's 128-byte-swizzled staging stays 1024-byte aligned
 constexpr int kRawScaleRegion = (kRawStages * kRawScaleBytes + 1023) / 1024 * 1024;
 static_assert(1024 + kStages2 * 2 * kHalfBytes + 4 * kOutWarpBytes + 8 * (2 * kStages2 + 5) + 8 <=
@@ -902,43 +904,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
     if (lane == 0) bulk_wait_all<0>();
     __syncwarp();
   } else if (kQ8 && warp >= 8) {
-    // ---------------- int8 converters: raw stage -> bf16 B stage of this CTA
-    const int ct = static_cast<int>(threadIdx.x) - 256;
+    // ---------------- int8 converters: raw stage -> bf16 B stage of this CTA.  Two
+    // groups of four warps take alternate stages, so one group's waits and fences
+    // overlap the other's conversion.
+    const int cg = (warp - 8) >> 2;
+    const int ct = static_cast<int>(threadIdx.x) - 256 - 128 * cg;
     const int crow = ct >> 2, cch = ct & 3;
-    uint32_t stage = 0, phase = 0, rs = 0, rphase = 0;
-    bool ok = true;
-    for (int t = pair; t < total && ok; t += npairs) {
-      int mp, n, b;
-      decode_pair(t, p, mp, n, b);
-      const int nr = tile_b(p, n).bn / 64;  // rows of the half / 32
-      for (int kb = 0; kb < p.k_blocks; ++kb) {
-        if (!mbar_wait(&raw_full[rs], rphase, abort_flag, p.err, kErrConvert) ||
-            !mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrConvert)) {
-          ok = false;
-          break;
+    const int nr = p.bn / 64;  // rows of the half tile / 32 (map mode: one tile width)
+    const int my_tiles = pair < total ? (total - pair + npairs - 1) / npairs : 0;
+    const int jobs = my_tiles * p.k_blocks;
+    for (int j = cg; j < jobs; j += kConvGroups) {
+      const uint32_t stage = static_cast<uint32_t>(j % kS), phase = static_cast<uint32_t>(j / kS) & 1u;
+      const uint32_t rs = static_cast<uint32_t>(j % kRawStages);
+      const uint32_t rphase = static_cast<uint32_t>(j / kRawStages) & 1u;
+      if (!mbar_wait(&raw_full[rs], rphase, abort_flag, p.err, kErrConvert) ||
+          !mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrConvert))
+        break;
+      q8_convert(sRaw + rs * kRawBytes, sRawScale + rs * kRawScaleBytes,
+                 sB + stage * kHalfBytes, crow, cch, nr);
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        if (rank == 0) {
+          mbar_arrive(&full[stage]);  // release at CTA scope; the MMA issuer is in this CTA
+        } else {
+          // this CTA's shared-memory writes, released to the peer's MMA issuer
+          fence_release_smem_cluster();
+          mbar_arrive_relaxed_cl(full0 + 8 * stage);
         }
-        q8_convert(sRaw + rs * kRawBytes, sRawScale + rs * kRawScaleBytes,
-                   sB + stage * kHalfBytes, crow, cch, nr);
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          if (rank == 0) {
-            mbar_arrive(&full[stage]);  // release at CTA scope; the MMA issuer is in this CTA
-          } else {
-            // this CTA's shared-memory writes, released to the peer's MMA issuer
-            fence_release_smem_cluster();
-            mbar_arrive_relaxed_cl(full0 + 8 * stage);
-          }
-          mbar_arrive(&raw_empty[rs]);
-        }
-        if (++stage == kS) {
-          stage = 0;
-          phase ^= 1;
-        }
-        if (++rs == kRawStages) {
-          rs = 0;
-          rphase ^= 1;
-        }
+        mbar_arrive(&raw_empty[rs]);
       }
     }
   }

@@ -18,7 +18,7 @@ constexpr int kBBytes = kBNMax * kBK * 2;
 constexpr int kOutBoxBytes = 64 * 32 * 2;   // one 64-col x 32-row bf16 store box
 constexpr int kOutWarpBytes = 2 * kOutBoxBytes;
 constexpr int kGemmThreads = 256;  // warp 0 TMA, warp 1 MMA, warp 2 TMEM, warps 4-7 epilogue
-constexpr int kGemmThreadsQ8 = 384;  // int8 maps: warps 8-11 convert the B operand
+constexpr int kGemmThreadsQ8 = 512;  // int8 maps: warps 8-15 convert the B operand
 constexpr int kQ8Group = 128;        // map weights of a row that share one bf16 scale
 constexpr int kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 4 * kOutWarpBytes + 256;
 
