@@ -632,7 +632,6 @@ constexpr int kRawScaleBytes = 128 * 2;   // bf16 scales of its rows
 constexpr int kStagesQ8 = 4;              // bf16 MMA stages with int8 maps
 constexpr int kRawStages = 7;
 constexpr int kConvGroups = 2;            // converter warp groups taking alternate stages
-static_assert(kStagesQ8 % kConvGroups == 0, "each converter group keeps to its own MMA stages");
 // scale ring padded so the epilogue's 128-byte-swizzled staging stays 1024-byte aligned
 constexpr int kRawScaleRegion = (kRawStages * kRawScaleBytes + 1023) / 1024 * 1024;
 static_assert(1024 + kStages2 * 2 * kHalfBytes + 4 * kOutWarpBytes + 8 * (2 * kStages2 + 5) + 8 <=
