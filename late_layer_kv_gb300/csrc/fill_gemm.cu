@@ -648,14 +648,17 @@ static_assert(1024 + kStagesQ8 * 2 * kHalfBytes + kRawStages * kRawBytes + kRawS
 __device__ __forceinline__ void q8_dequant16(uint4 v, float sc, float c, uint32_t (&w)[8]) {
   const uint32_t x[4] = {v.x ^ 0x80808080u, v.y ^ 0x80808080u, v.z ^ 0x80808080u,
                          v.w ^ 0x80808080u};
+  const float2 s2 = make_float2(sc, sc), c2 = make_float2(c, c);
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float f0 = fmaf(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7504)), sc, c);
-    const float f1 = fmaf(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7514)), sc, c);
-    const float f2 = fmaf(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7524)), sc, c);
-    const float f3 = fmaf(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7534)), sc, c);
-    w[2 * e] = pack_bf16(f0, f1);
-    w[2 * e + 1] = pack_bf16(f2, f3);
+    const float2 f01 = __ffma2_rn(make_float2(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7504)),
+                                              __uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7514))),
+                                  s2, c2);
+    const float2 f23 = __ffma2_rn(make_float2(__uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7524)),
+                                              __uint_as_float(__byte_perm(x[e], 0x47000000u, 0x7534))),
+                                  s2, c2);
+    w[2 * e] = pack_bf16(f01.x, f01.y);
+    w[2 * e + 1] = pack_bf16(f23.x, f23.y);
   }
 }
 
