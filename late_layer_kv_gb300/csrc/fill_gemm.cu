@@ -18,6 +18,9 @@
 // kStages-deep ring, warp 1 issues tcgen05.mma (M=128, N=bn, K=16) into one of
 // two TMEM accumulators, warp 2 owns the TMEM allocation, warps 4-7 drain the
 // accumulators (TMEM lane = tile row) while the next tile accumulates.
+// rf_gemm2_kernel runs the map, K/V and GDN modes on CTA pairs (M=256); its
+// int8-map variant (section 2.2 "Size and cost") adds warp 3 loading int8 codes
+// and scales and warps 8-15 dequantising them into the MMA stages.
 #include "rf_internal.h"
 #include "sm103_ptx.cuh"
 
