@@ -19,6 +19,10 @@ from .ridgefill import (  # noqa: F401
     gdn_state,
     speedup_ceiling,
     filled_weight_share,
+    filled_share,
+    gdn_rho,
+    terminal_correction,
+    layer_inputs,
     quantize_map,
     dequantize_map,
     Q8_GROUP,

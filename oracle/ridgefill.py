@@ -32,6 +32,13 @@ Readings where the paper is silent (each applied below):
 * R6 rows: every prefix row is filled; the tail is not touched.
 * R16 value/key rescale: "the ratio of the exact value norm to the predicted
   one, averaged over the c rows" is the mean of the per-row ratios.
+* R19 exact prefix rows (section 2.4): an exact row's late-layer input is its
+  true input, given; in an attention layer the fill does not write its row, in
+  a GDN layer it enters the state in prompt order with its true input.
+* R20 rho (section 2.3, terminal-state correction): the weight of row t in the
+  state at the end of the prefix is the product of the gates of the rows after
+  it; rho is taken per layer and head (the gates are per head; Delta M is per
+  value head), over the prefix rows only.
 * R18 int8 maps: symmetric absmax groups of 128 consecutive weights of a row,
   scale ``s = bf16(absmax / 127)``, code ``q = rint(a / s)`` (ties to even,
   clamped to [-127, 127]); an all-zero group has ``s = 0``, ``q = 0``.  The
@@ -258,19 +265,32 @@ def gdn_recurrence(k, v, alpha, beta, S0=None):
     return S
 
 
+def layer_inputs(H, A_l, b_l, exact_idx=None, X_exact_l=None):
+    """Every prefix row's input to one late layer (sections 2.2 and 2.4, R19):
+    the map's prediction ``A h + b``, except that the exact rows ``exact_idx``
+    take their true inputs ``X_exact_l`` [len(exact_idx), d_out]."""
+    x = map_apply(H, A_l, b_l)
+    if exact_idx is not None and len(exact_idx) > 0:
+        x[np.asarray(exact_idx)] = _f64(X_exact_l)
+    return x
+
+
 def gdn_state(H, A, b, g, Wk, Wv, Wa, Wb, eps: float, n_heads: int, dk: int, dv: int,
               S0=None, layers: Optional[Sequence[int]] = None,
-              heads: Optional[Sequence[int]] = None, l2_eps: float = 1e-6):
+              heads: Optional[Sequence[int]] = None, l2_eps: float = 1e-6,
+              exact_idx=None, X_exact=None):
     """End-of-fill recurrent state of GDN late layers (sections 2.1, 2.3).
 
-    Every prefix row, in order, updates the state from its predicted input.
+    Every prefix row, in order, updates the state from its input: the map's
+    prediction, or for the exact rows ``exact_idx`` their true inputs
+    ``X_exact`` [L, len(exact_idx), d_out] (section 2.4, R19).
     Returns [len(layers), len(heads), dv, dk].
     """
     Ls = range(np.shape(A)[0]) if layers is None else layers
     hs = list(range(n_heads)) if heads is None else list(heads)
     out = []
     for l in Ls:
-        xh = map_apply(H, A[l], b[l])
+        xh = layer_inputs(H, A[l], b[l], exact_idx, None if X_exact is None else X_exact[l])
         k, v, a, bt = gdn_projections(xh, g[l], Wk[l], Wv[l], Wa[l], Wb[l], eps,
                                       n_heads, dk, dv, l2_eps)
         s0 = None if S0 is None else _f64(S0)[l][hs]
@@ -286,6 +306,46 @@ def speedup_ceiling(S: int, L: int, T: int, N: int):
     """Share of exact prefill compute that remains, ``r = (S(N-T) + L T)/(L N)``,
     section 2.5; the speedup is at most ``1/r``."""
     return (S * (N - T) + L * T) / (L * N)
+
+
+def filled_share(alpha, filled):
+    """rho of section 2.3 (terminal-state correction, R20): the filled rows'
+    total weight over all rows' total weight, where a row's weight in the state
+    at the end of the rows is the product of the gates after it.
+
+    ``alpha`` [rows] gates of one head, ``filled`` [rows] bool.  The suffix
+    products are a reversed cumulative product (a library primitive).
+    """
+    a = _f64(alpha)
+    f = np.asarray(filled, dtype=bool)
+    # w[t] = prod(a[t+1:]): reverse cumulative product, shifted by one
+    after = np.concatenate([np.cumprod(a[::-1])[::-1][1:], [1.0]])
+    return after[f].sum() / after.sum()
+
+
+def gdn_rho(H, A, b, g, Wa, eps: float, n_heads: int, exact_idx=None, X_exact=None,
+            layers: Optional[Sequence[int]] = None):
+    """rho [len(layers), n_heads] of GDN late layers at the end of the prefix:
+    per head, ``filled_share`` of the gates the layer computes from every
+    prefix row's input (R19, R20)."""
+    Ls = range(np.shape(A)[0]) if layers is None else layers
+    rows = np.shape(H)[0]
+    filled = np.ones(rows, dtype=bool)
+    if exact_idx is not None:
+        filled[np.asarray(exact_idx, dtype=np.int64)] = False
+    out = []
+    for l in Ls:
+        x = layer_inputs(H, A[l], b[l], exact_idx, None if X_exact is None else X_exact[l])
+        alpha = _sigmoid(rms_norm(x, g[l], eps) @ _f64(Wa[l]).T)  # [rows, H] (R5)
+        out.append([filled_share(alpha[:, h], filled) for h in range(n_heads)])
+    return np.asarray(out)
+
+
+def terminal_correction(S, rho, delta_M):
+    """The state after the terminal-state correction of section 2.3,
+    ``S + rho Delta M``, once per layer and head (``S``, ``delta_M``
+    [L, H, dv, dk]; ``rho`` [L, H])."""
+    return _f64(S) + _f64(rho)[:, :, None, None] * _f64(delta_M)
 
 
 def filled_weight_share(alpha, n_filled: int):
