@@ -95,6 +95,15 @@ typedef enum rf_status {
  *   must be a multiple of 128.  Device memory, or page-locked host memory with
  *   maps_on_host = 1 (then both arrays are streamed, half the bytes of bf16
  *   maps).  ridgefill_quantize_maps makes them.
+ * row_idx, h_rows (optional; row_idx may be NULL): exact prefix rows (section
+ *   2.4).  When row_idx is set, H is [h_rows, d_in], the split states of every
+ *   prefix row, and fill row r (0 <= r < rows) is prefix row row_idx[r]: its
+ *   split state is H[row_idx[r]] and its keys and values go to cache position
+ *   pos0 + row_idx[r], with RoPE at that position.  Positions not listed are
+ *   not written (the exact rows the model computes).  row_idx is device int32
+ *   [rows], 4-byte aligned, entries distinct and in [0, h_rows) (an entry
+ *   outside is skipped and reported by ridgefill_device_error as
+ *   RF_ERR_ARG); pos0 + h_rows <= cache_len.
  * k_scale, v_scale (optional, may be NULL): [L, n_kv_heads] f32 device arrays.
  *   When set, every key (value) of head h in layer l is multiplied by
  *   k_scale[l, h] (v_scale[l, h]) before its rounding to bf16: the value or
@@ -127,6 +136,8 @@ typedef struct rf_fill_args {
   const float* k_scale;
   const float* v_scale;
   const void* A_scale;
+  const int32_t* row_idx;
+  int64_t h_rows;
 } rf_fill_args;
 
 /* Bytes of device workspace ridgefill_fill needs for these arguments
@@ -284,6 +295,18 @@ rf_status ridgefill_quantize_maps(const rf_quantize_args* args, void* stream);
  *   before the first chunk's map GEMM, after it, after its projection GEMM and
  *   after its state kernel.
  * A_scale (optional): int8 maps, as in rf_fill_args.
+ * exact_idx, n_exact, X_exact (optional): exact prefix rows (section 2.4).
+ *   Rows exact_idx[e] (device int32 [n_exact], 4-byte aligned, strictly
+ *   increasing, in [0, rows)) enter the state in prompt order from their true
+ *   inputs X_exact[l, e, :] ([L, n_exact, d_out] bf16) instead of the map's
+ *   prediction; H still holds every prefix row.  An entry outside [0, rows) is
+ *   skipped and reported by ridgefill_device_error as RF_ERR_ARG.
+ * rho (optional): [L, n_heads] f32 output, section 2.3's share of the state at
+ *   the end of the prefix that comes from filled rows: a row's weight is the
+ *   product of the gates alpha of the rows after it, and rho is the filled
+ *   rows' total weight over all rows' (1 with no exact rows, 0 with rows = 0).
+ * delta_M (optional): [L, n_heads, d_v, d_k] f32, the terminal-state
+ *   correction of section 2.3: S += rho * delta_M once, after the last row.
  */
 typedef struct rf_gdn_args {
   int32_t n_layers;
@@ -310,6 +333,11 @@ typedef struct rf_gdn_args {
   float* S;
   void* const* stage_events;
   const void* A_scale;
+  const int32_t* exact_idx;
+  int64_t n_exact;
+  const void* X_exact;
+  float* rho;
+  const float* delta_M;
 } rf_gdn_args;
 
 size_t ridgefill_gdn_workspace_size(const rf_gdn_args* args);
@@ -402,7 +430,9 @@ const char* ridgefill_status_string(rf_status status);
 const char* ridgefill_last_error(void);
 
 /* Synchronises `stream`, stores the device error word in *code (0 = none,
- * otherwise the id of the wait that ran out) and clears it. */
+ * otherwise the id of the wait that ran out, 7 for a non-positive Cholesky
+ * pivot, 6 for an out-of-range row index) and clears it.  The status is
+ * RF_ERR_TIMEOUT, RF_ERR_NUMERIC or RF_ERR_ARG accordingly. */
 rf_status ridgefill_device_error(void* stream, int* code);
 
 /* Section 2.5 compute ceiling: share of exact prefill work that remains,

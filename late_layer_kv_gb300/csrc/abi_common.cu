@@ -261,6 +261,7 @@ extern "C" rf_status ridgefill_device_error(void* stream, int* code) {
   *code = v;
   if (v == 0) return RF_OK;
   if (v == rf::kErrNumeric) return rf::fail(RF_ERR_NUMERIC, "ridge system not positive definite");
+  if (v == rf::kErrIndex) return rf::fail(RF_ERR_ARG, "a row index list entry was out of range");
   return rf::fail(RF_ERR_TIMEOUT, "device wait ran out at site %d", v);
 }
 
@@ -272,7 +273,7 @@ extern "C" double ridgefill_compute_share(int32_t split, int32_t n_layers, int64
   return (S * (N - T) + L * T) / (L * N);
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 4; }
+extern "C" int32_t ridgefill_abi_version(void) { return 5; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {

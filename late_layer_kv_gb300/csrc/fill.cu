@@ -18,7 +18,7 @@ namespace {
 struct FillPlan {
   int bn_map = 0, bn_kv = 0;
   int64_t R = 0;  // rows per chunk
-  size_t off_xhat = 0, off_ss = 0, off_slots = 0, total = 0;
+  size_t off_xhat = 0, off_ss = 0, off_slots = 0, off_gather = 0, total = 0;
 };
 
 rf_status validate_fill(const rf_fill_args* a) {
@@ -32,6 +32,12 @@ rf_status validate_fill(const rf_fill_args* a) {
   if ((static_cast<int64_t>(a->n_kv_heads) * a->head_dim) % 128 != 0)
     return fail(RF_ERR_SHAPE, "n_kv_heads * head_dim must be a multiple of 128");
   if (a->rows < 0 || a->pos0 < 0) return fail(RF_ERR_ARG, "rows and pos0 must be >= 0");
+  if (a->row_idx != nullptr) {
+    if (a->h_rows < a->rows || a->h_rows >= (int64_t(1) << 31))
+      return fail(RF_ERR_SHAPE, "with row_idx, h_rows must be >= rows and < 2^31");
+    if (a->cache_len < a->pos0 + a->h_rows)
+      return fail(RF_ERR_SHAPE, "pos0 + h_rows exceeds cache_len");
+  }
   if (a->cache_len < a->pos0 + a->rows) return fail(RF_ERR_SHAPE, "pos0 + rows exceeds cache_len");
   if (a->cache_len >= (int64_t(1) << 24)) return fail(RF_ERR_SHAPE, "cache_len must be < 2^24");
   if (a->rows_per_chunk < 0 || a->rows_per_chunk % 128 != 0)
@@ -59,11 +65,29 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   pl->off_slots = align_up(pl->off_ss + L * (d / pl->bn_map) * pl->R * 4, 256);
   const size_t slots =
       a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0;
-  pl->total = align_up(pl->off_slots + slots, 256);
+  pl->off_gather = align_up(pl->off_slots + slots, 256);
+  const size_t gather = a->row_idx != nullptr ? static_cast<size_t>(pl->R) * a->d_in * 2 : 0;
+  pl->total = align_up(pl->off_gather + gather, 256);
 }
 
 // K/V GEMM on CTA pairs (true) or single CTAs
 constexpr bool kKvPairs = true;
+
+// Exact prefix rows (section 2.4): the split states of the listed rows
+// idx[0 .. rc) gathered into a dense [rc, d_in] block for the map GEMM; one
+// warp per row, an entry outside [0, h_rows) gives a zero row and an error code.
+__global__ void gather_rows_kernel(const __nv_bfloat16* H, const int32_t* idx, int64_t rc,
+                                   int64_t h_rows, int d_in, __nv_bfloat16* out, int* err) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= rc) return;
+  const int64_t src = idx[w];
+  const bool ok = src >= 0 && src < h_rows;
+  if (!ok && lane == 0) atomicCAS(err, 0, kErrIndex);
+  const uint4* s = reinterpret_cast<const uint4*>(H + (ok ? src : 0) * d_in);
+  uint4* d = reinterpret_cast<uint4*>(out + w * d_in);
+  for (int j = lane; j < d_in / 8; j += 32) d[j] = ok ? s[j] : make_uint4(0, 0, 0, 0);
+}
 
 // `only`: 0 = keys and values, RF_RESCALE_KEYS / RF_RESCALE_VALUES = that half alone
 rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, int64_t rc,
@@ -108,6 +132,14 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   p.eps = static_cast<float>(a->rms_eps);
   p.k_scale = a->k_scale;
   p.v_scale = a->v_scale;
+  if (a->row_idx != nullptr) {
+    p.kv_rows = a->row_idx + start;
+    p.kv_pos0 = static_cast<int32_t>(a->pos0);
+    p.kv_hrows = static_cast<int32_t>(a->h_rows);
+    p.kv_cache[0] = static_cast<__nv_bfloat16*>(a->Kc);
+    p.kv_cache[1] = static_cast<__nv_bfloat16*>(a->Vc);
+    p.cache_len = a->cache_len;
+  }
   for (int i = 0; i < a->head_dim / 2; ++i) {
     const double f = std::pow(a->rope_theta, -2.0 * i / a->head_dim);
     p.inv_freq_hi[i] = static_cast<float>(f);
@@ -159,6 +191,8 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
   if (!aligned16(a->A)) return fail(RF_ERR_ALIGN, "A is not 16-byte aligned");
   if (a->A_scale != nullptr && !aligned16(a->A_scale))
     return fail(RF_ERR_ALIGN, "A_scale is not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(a->row_idx) & 3u) != 0)
+    return fail(RF_ERR_ALIGN, "row_idx is not 4-byte aligned");
   if (a->maps_on_host) {
     if ((st = check_pinned(a->A, "A")) != RF_OK) return st;
     if (a->A_scale != nullptr && (st = check_pinned(a->A_scale, "A_scale")) != RF_OK) return st;
@@ -196,6 +230,15 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     const int64_t rc = (a->rows - start < pl.R) ? a->rows - start : pl.R;
     MapLaunch m{};
     m.H = static_cast<const uint8_t*>(a->H) + static_cast<size_t>(start) * a->d_in * 2;
+    if (a->row_idx != nullptr) {  // the chunk's listed rows, gathered
+      void* hc = ws + pl.off_gather;
+      gather_rows_kernel<<<static_cast<unsigned>((rc * 32 + 255) / 256), 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(a->H), a->row_idx + start, rc, a->h_rows, a->d_in,
+          static_cast<__nv_bfloat16*>(hc), device_error_word());
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "row gather launch");
+      m.H = hc;
+    }
     m.rows = rc;
     m.d_in = a->d_in;
     m.d_out = a->d_out;

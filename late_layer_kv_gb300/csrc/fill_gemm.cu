@@ -173,10 +173,30 @@ __device__ __forceinline__ float row_rms_scale(const GemmParams& p, int l, int r
   return rsqrtf(fmaf(ssum, p.inv_d, p.eps));
 }
 
+// 32 bf16 (16 words) of one row straight to global memory
+__device__ __forceinline__ void store32(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) d[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
 __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
                             int m, int n, int l, float rs, uint32_t tempty) {
   const int row = m * kBM + q * 32 + lane;
-  const float posf = static_cast<float>(p.pos_base + row);
+  // rows listed by index (exact prefix rows skipped) are stored one by one
+  const bool direct = p.kv_rows != nullptr;
+  int pos = p.pos_base + row;
+  bool keep = true;
+  if (direct) {
+    keep = row < p.rows;
+    const int idx = keep ? p.kv_rows[row] : 0;
+    if (keep && (idx < 0 || idx >= p.kv_hrows)) {
+      keep = false;
+      atomicCAS(p.err, 0, kErrIndex);
+    }
+    pos = p.kv_pos0 + idx;
+  }
+  const float posf = static_cast<float>(pos);
   const bool is_k = n < p.n_k_tiles;
   const int hd = p.head_dim;
   const int half = hd / 2;
@@ -188,7 +208,11 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
     const uint32_t hc = tcol + hh * hd;
     // the head's rescale factor folds into the row's RMS scale (both multiply the row)
     const float rh = hscale != nullptr ? rs * hscale[l * p.n_kv + head0 + hh] : rs;
-    if (lane == 0) bulk_wait_read<0>();
+    __nv_bfloat16* drow =
+        direct ? p.kv_cache[is_k ? 0 : 1] +
+                     ((static_cast<int64_t>(l) * p.n_kv + head0 + hh) * p.cache_len + pos) * hd
+               : nullptr;
+    if (!direct && lane == 0) bulk_wait_read<0>();
     __syncwarp();
     if (is_k) {
       for (int i0 = 0; i0 < half; i0 += 32) {
@@ -207,8 +231,15 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
           w1[j / 2] = pack_bf16(xa * c0 - ya * s0, xb * c1 - yb * s1);
           w2[j / 2] = pack_bf16(ya * c0 + xa * s0, yb * c1 + xb * s1);
         }
-        stage32(stg + (i0 / 64) * kOutBoxBytes, lane, i0 % 64, w1);
-        stage32(stg + ((half + i0) / 64) * kOutBoxBytes, lane, (half + i0) % 64, w2);
+        if (direct) {
+          if (keep) {
+            store32(drow + i0, w1);
+            store32(drow + half + i0, w2);
+          }
+        } else {
+          stage32(stg + (i0 / 64) * kOutBoxBytes, lane, i0 % 64, w1);
+          stage32(stg + ((half + i0) / 64) * kOutBoxBytes, lane, (half + i0) % 64, w2);
+        }
       }
     } else {
       for (int c0 = 0; c0 < hd; c0 += 32) {
@@ -218,7 +249,11 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
         uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 32; j += 2) w[j / 2] = pack_bf16(f32(a[j]) * rh, f32(a[j + 1]) * rh);
-        stage32(stg + (c0 / 64) * kOutBoxBytes, lane, c0 % 64, w);
+        if (direct) {
+          if (keep) store32(drow + c0, w);
+        } else {
+          stage32(stg + (c0 / 64) * kOutBoxBytes, lane, c0 % 64, w);
+        }
       }
     }
     if (hh == hpt - 1) {
@@ -226,6 +261,7 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
       __syncwarp();
       if (lane == 0) mbar_arrive_cl(tempty);
     }
+    if (direct) continue;
     fence_async_smem();
     __syncwarp();
     if (lane == 0) {

@@ -709,10 +709,135 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   }
 }
 
+// ---------------------------------------------------------------- exact rows and rho
+// Exact prefix rows (section 2.4): row exact_idx[e] takes its true input X_exact[l, e]
+// in place of the map's prediction: bf16(g x) into X_hat and its sum of squares as the
+// row's first partial (the others zero), after the map GEMM of the row's chunk.
+__global__ void exact_input_kernel(const __nv_bfloat16* X, const __nv_bfloat16* g,
+                                   const int32_t* idx, int64_t n_exact, int L, int d,
+                                   int64_t start, int64_t rc, int64_t rows, int64_t R,
+                                   int ss_tiles, __nv_bfloat16* xhat, float* ss, int* err) {
+  const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= static_cast<int64_t>(L) * n_exact) return;
+  const int l = static_cast<int>(w / n_exact);
+  const int64_t e = w % n_exact;
+  const int64_t t = idx[e];
+  if (t < 0 || t >= rows) {
+    if (lane == 0) atomicCAS(err, 0, kErrIndex);
+    return;
+  }
+  if (t < start || t >= start + rc) return;
+  const int64_t r = t - start;
+  const __nv_bfloat16* src = X + (static_cast<size_t>(l) * n_exact + e) * d;
+  __nv_bfloat16* dst = xhat + (static_cast<size_t>(l) * R + r) * d;
+  const __nv_bfloat16* gl = g != nullptr ? g + static_cast<size_t>(l) * d : nullptr;
+  float acc = 0.f;
+  for (int j = 8 * lane; j < d; j += 256) {
+    const uint4 xv = *reinterpret_cast<const uint4*>(src + j);
+    uint4 gv = make_uint4(0x3f803f80u, 0x3f803f80u, 0x3f803f80u, 0x3f803f80u);  // bf16 1.0 pairs
+    if (gl != nullptr) gv = *reinterpret_cast<const uint4*>(gl + j);
+    const uint32_t xw[4] = {xv.x, xv.y, xv.z, xv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const float2 x2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&xw[q]));
+      const float2 g2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&gw[q]));
+      acc = fmaf(x2.x, x2.x, acc);
+      acc = fmaf(x2.y, x2.y, acc);
+      out[q] = pack_bf16(x2.x * g2.x, x2.y * g2.y);
+    }
+    *reinterpret_cast<uint4*>(dst + j) = make_uint4(out[0], out[1], out[2], out[3]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  for (int j = lane; j < ss_tiles; j += 32)
+    ss[(static_cast<size_t>(l) * ss_tiles + j) * R + r] = j == 0 ? acc : 0.f;
+}
+
+// rho of section 2.3 (terminal-state correction), one CTA per (layer, head) and
+// row chunk.  A row's weight in the state at the end of the rows is the product
+// of the gates after it.  Each thread runs over a segment of rows with
+//   den <- den * alpha_t + 1,  num <- num * alpha_t + [row t filled],  P <- P * alpha_t
+// (weights relative to the segment's end), the segments combine in row order
+// ((n, d, P)_a then (n, d, P)_b gives (n_a P_b + n_b, d_a P_b + d_b, P_a P_b)), and
+// the chunk's result extends the sums carried from earlier chunks.  f64 throughout.
+constexpr int kRhoThreads = 1024;
+
+__global__ void __launch_bounds__(kRhoThreads) rho_chunk_kernel(
+    const float* gate, int H, int64_t R, int64_t rc, int64_t start, const int32_t* exact_idx,
+    int64_t n_exact, double* acc, int first) {
+  __shared__ double s_n[kRhoThreads], s_d[kRhoThreads], s_p[kRhoThreads];
+  const int lh = blockIdx.x;
+  const int l = lh / H, h = lh - l * H;
+  const float* alpha = gate + (static_cast<size_t>(l) * 2 * H + h) * R;  // alpha plane of (l, h)
+  const int64_t seg = (rc + kRhoThreads - 1) / kRhoThreads;
+  const int64_t a = threadIdx.x * seg;
+  const int64_t b = a + seg < rc ? a + seg : rc;
+  // first exact row at or after prompt row start + a (exact_idx ascending)
+  int64_t lo = 0, hi = n_exact;
+  while (lo < hi) {
+    const int64_t mid = (lo + hi) >> 1;
+    if (exact_idx[mid] < start + a) lo = mid + 1;
+    else hi = mid;
+  }
+  double num = 0.0, den = 0.0, P = 1.0;
+  for (int64_t t = a; t < b; ++t) {
+    const double al = alpha[t];
+    bool exact = false;
+    if (lo < n_exact && exact_idx[lo] == start + t) {
+      exact = true;
+      ++lo;
+    }
+    den = fma(den, al, 1.0);
+    num = fma(num, al, exact ? 0.0 : 1.0);
+    P *= al;
+  }
+  s_n[threadIdx.x] = num;
+  s_d[threadIdx.x] = den;
+  s_p[threadIdx.x] = P;
+  __syncthreads();
+  for (int stride = 1; stride < kRhoThreads; stride <<= 1) {
+    const int i = static_cast<int>(threadIdx.x);
+    if ((i & (2 * stride - 1)) == 0) {
+      const int j = i + stride;  // the later segment
+      s_n[i] = fma(s_n[i], s_p[j], s_n[j]);
+      s_d[i] = fma(s_d[i], s_p[j], s_d[j]);
+      s_p[i] *= s_p[j];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    double* c = acc + 2 * static_cast<size_t>(lh);
+    if (first) {
+      c[0] = s_n[0];
+      c[1] = s_d[0];
+    } else {
+      c[0] = fma(c[0], s_p[0], s_n[0]);
+      c[1] = fma(c[1], s_p[0], s_d[0]);
+    }
+  }
+}
+
+// rho = filled / all weight (0 with no rows), written to `rho` if set; with
+// delta_M set, the terminal-state correction S += rho * delta_M of the (layer, head).
+__global__ void __launch_bounds__(256) rho_finish_kernel(const double* acc, int empty, float* rho,
+                                                         const float* delta_M, float* S, int dvdk) {
+  const size_t lh = blockIdx.x;
+  const double d = acc != nullptr ? acc[2 * lh + 1] : 0.0;
+  const float r = (empty || !(d > 0.0)) ? 0.f : static_cast<float>(acc[2 * lh] / d);
+  if (rho != nullptr && threadIdx.x == 0) rho[lh] = r;
+  if (delta_M == nullptr) return;
+  float* s = S + lh * dvdk;
+  const float* m = delta_M + lh * dvdk;
+  for (int i = threadIdx.x; i < dvdk; i += blockDim.x) s[i] = fmaf(r, m[i], s[i]);
+}
+
 struct GdnPlan {
   int bn_map = 0;
   int64_t R = 0;
-  size_t off_xhat = 0, off_ss = 0, off_k = 0, off_v = 0, off_gate = 0, off_slots = 0, total = 0;
+  size_t off_xhat = 0, off_ss = 0, off_k = 0, off_v = 0, off_gate = 0, off_slots = 0, off_rho = 0,
+         total = 0;
 };
 
 rf_status validate_gdn(const rf_gdn_args* a) {
@@ -734,6 +859,9 @@ rf_status validate_gdn(const rf_gdn_args* a) {
     return fail(RF_ERR_SHAPE, "sizes exceed the 32-bit tile indexing");
   if (a->A_scale != nullptr && a->d_in % kQ8Group != 0)
     return fail(RF_ERR_SHAPE, "int8 maps need d_in to be a multiple of 128");
+  if (a->n_exact < 0 || a->n_exact > a->rows) return fail(RF_ERR_ARG, "n_exact must be in [0, rows]");
+  if (a->n_exact > 0 && (a->exact_idx == nullptr || a->X_exact == nullptr))
+    return fail(RF_ERR_ARG, "n_exact > 0 needs exact_idx and X_exact");
   return RF_OK;
 }
 
@@ -750,6 +878,7 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
   pl->off_gate = off;  off = align_up(off + L * 2 * H * R * 4, 256);
   pl->off_slots = off;
   off = align_up(off + (a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0), 256);
+  pl->off_rho = off;   off = align_up(off + L * H * 2 * sizeof(double), 256);
   pl->total = off;
 }
 
@@ -856,6 +985,11 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
   if (a->A != nullptr && !aligned16(a->A)) return fail(RF_ERR_ALIGN, "A is not 16-byte aligned");
   if (a->A_scale != nullptr && !aligned16(a->A_scale))
     return fail(RF_ERR_ALIGN, "A_scale is not 16-byte aligned");
+  const void* dev2[] = {a->X_exact, a->rho, a->delta_M};
+  for (const void* q : dev2)
+    if (q != nullptr && !aligned16(q)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
+  if ((reinterpret_cast<uintptr_t>(a->exact_idx) & 3u) != 0)
+    return fail(RF_ERR_ALIGN, "exact_idx is not 4-byte aligned");
   if (a->maps_on_host && a->rows > 0) {
     if ((st = check_pinned(a->A, "A")) != RF_OK) return st;
     if (a->A_scale != nullptr && (st = check_pinned(a->A_scale, "A_scale")) != RF_OK) return st;
@@ -892,11 +1026,19 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
                         plane_b, 64, kC, CU_TENSOR_MAP_SWIZZLE_128B);
   };
 
-  if (a->rows == 0) {  // the end-of-fill state is the initial state
+  const int LH = a->n_layers * a->n_heads;
+  const bool want_rho = a->rho != nullptr || a->delta_M != nullptr;
+  double* rho_acc = reinterpret_cast<double*>(ws + pl.off_rho);
+  if (a->rows == 0) {  // the end-of-fill state is the initial state; no filled rows: rho = 0
     sp.rows = 0;
     sp.first = 1;
     cudaError_t e = launch_gdn_state(sp, s);
-    return e == cudaSuccess ? RF_OK : cuda_fail(e, "GDN state launch");
+    if (e != cudaSuccess) return cuda_fail(e, "GDN state launch");
+    if (a->rho != nullptr) {
+      rho_finish_kernel<<<LH, 256, 0, s>>>(nullptr, 1, a->rho, nullptr, a->S, kDk * kDk);
+      if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rho launch");
+    }
+    return RF_OK;
   }
 
   HostStreamer* hs = nullptr;
@@ -954,8 +1096,23 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
         if (e != cudaSuccess) return cuda_fail(e, "recording a map slot release");
       }
     }
+    if (a->n_exact > 0) {  // exact rows of this chunk take their true inputs
+      const int64_t warps = static_cast<int64_t>(a->n_layers) * a->n_exact;
+      exact_input_kernel<<<static_cast<unsigned>((warps * 32 + 255) / 256), 256, 0, s>>>(
+          static_cast<const __nv_bfloat16*>(a->X_exact), static_cast<const __nv_bfloat16*>(a->gain),
+          a->exact_idx, a->n_exact, a->n_layers, a->d_out, start, rc, a->rows, pl.R,
+          a->d_out / pl.bn_map, static_cast<__nv_bfloat16*>(xhat), ss, device_error_word());
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "exact-row input launch");
+    }
     if ((st = mark(start, 1)) != RF_OK) return st;
     if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s)) != RF_OK) return st;
+    if (want_rho) {
+      rho_chunk_kernel<<<LH, kRhoThreads, 0, s>>>(gb, a->n_heads, pl.R, rc, start, a->exact_idx,
+                                                  a->n_exact, rho_acc, start == 0 ? 1 : 0);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "rho launch");
+    }
     if ((st = mark(start, 2)) != RF_OK) return st;
     sp.rows = static_cast<int32_t>(rc);
     sp.first = start == 0 ? 1 : 0;
@@ -963,6 +1120,11 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     cudaError_t e = launch_gdn_state(sp, s);
     if (e != cudaSuccess) return cuda_fail(e, "GDN state launch");
     if ((st = mark(start, 3)) != RF_OK) return st;
+  }
+  if (want_rho) {  // rho, and the terminal-state correction on the final state
+    rho_finish_kernel<<<LH, 256, 0, s>>>(rho_acc, 0, a->rho, a->delta_M, a->S, kDk * kDk);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "rho launch");
   }
   return RF_OK;
 }

@@ -37,6 +37,7 @@ enum ErrSite : int {
   kErrEpilogue = 3,
   kErrGdn = 4,
   kErrConvert = 5,   // int8-map converter warps
+  kErrIndex = 6,     // a row index list entry was out of range (the row was skipped)
   kErrNumeric = 7,   // the ridge system was not positive definite (Cholesky pivot <= 0)
 };
 
@@ -76,6 +77,13 @@ struct GemmParams {
   float eps;
   const float* k_scale;  // [L, n_kv] per-head key scale, or null
   const float* v_scale;  // [L, n_kv] per-head value scale, or null
+  // exact prefix rows: when kv_rows is set, tile row r goes to cache position
+  // kv_pos0 + kv_rows[r] (kv_rows[r] in [0, kv_hrows)), stored row by row
+  const int32_t* kv_rows;
+  int32_t kv_pos0;
+  int32_t kv_hrows;
+  __nv_bfloat16* kv_cache[2];  // K, V caches [L, n_kv, cache_len, head_dim]
+  int64_t cache_len;
   // GDN projection epilogue
   __nv_bfloat16* gdn_k;  // [L, H, 2, rows_alloc, dk]: bf16 high part, then the low remainder
   __nv_bfloat16* gdn_v;  // [L, H, 2, rows_alloc, dv], same split

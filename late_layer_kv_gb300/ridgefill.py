@@ -38,7 +38,8 @@ class FillArgs(ctypes.Structure):
         ("rope_theta", ctypes.c_double), ("rms_eps", ctypes.c_double),
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp), ("copy_events", _vp),
-        ("k_scale", _vp), ("v_scale", _vp), ("A_scale", _vp),
+        ("k_scale", _vp), ("v_scale", _vp), ("A_scale", _vp), ("row_idx", _vp),
+        ("h_rows", ctypes.c_int64),
     ]
 
 
@@ -51,7 +52,8 @@ class GdnArgs(ctypes.Structure):
         ("rms_eps", ctypes.c_double), ("l2_eps", ctypes.c_double),
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Wa", _vp), ("Wb", _vp), ("S0", _vp), ("S", _vp), ("stage_events", _vp),
-        ("A_scale", _vp),
+        ("A_scale", _vp), ("exact_idx", _vp), ("n_exact", ctypes.c_int64), ("X_exact", _vp),
+        ("rho", _vp), ("delta_M", _vp),
     ]
 
 
@@ -195,12 +197,15 @@ def _event_array(events):
 def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
               rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
               stage_events=None, copy_events=None, k_scale=None, v_scale=None,
-              A_scale=None) -> FillArgs:
+              A_scale=None, row_idx=None) -> FillArgs:
     L, d_out, d_in = A.shape
-    rows = H.shape[0]
+    rows = H.shape[0] if row_idx is None else row_idx.shape[0]
+    h_rows = H.shape[0] if row_idx is not None else 0
+    if row_idx is not None:
+        _dev(row_idx, "row_idx", torch.int32, (rows,))
     n_kv = Kc.shape[1]
     cache_len = Kc.shape[2]
-    _dev(H, "H", torch.bfloat16, (rows, d_in))
+    _dev(H, "H", torch.bfloat16, (H.shape[0], d_in))
     host = _check_maps(A, A_scale)
     _dev(bias, "bias", torch.float32, (L, d_out))
     if gain is not None:
@@ -221,7 +226,7 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
                  _ptr(bias), _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Kc), _ptr(Vc),
                  ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None,
                  ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None,
-                 _ptr(k_scale), _ptr(v_scale), _ptr(A_scale))
+                 _ptr(k_scale), _ptr(v_scale), _ptr(A_scale), _ptr(row_idx), h_rows)
     a._events_keepalive = (ev, cev)
     return a
 
@@ -246,7 +251,7 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
                    rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
                    workspace: Optional[torch.Tensor] = None, stream=None,
                    stage_events=None, copy_events=None, k_scale=None, v_scale=None,
-                   A_scale=None) -> None:
+                   A_scale=None, row_idx=None) -> None:
     """Write the K/V cache of the prefix rows of every late attention layer.
 
     ``H`` [rows, d_in] bf16, ``A`` [L, d_out, d_in] bf16 (device, or pinned host
@@ -258,12 +263,15 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     [L, n_kv] f32 per-head factors applied to the keys / values before rounding
     (the rescale of section 2.3 folded into the fill).  ``A_scale``: with int8
     maps ``A`` [L, d_out, d_in], their bf16 scales [L, d_in / 128, d_out]
-    (section 2.2 "Size and cost"; see :func:`ridgefill_quantize_maps`).
+    (section 2.2 "Size and cost"; see :func:`ridgefill_quantize_maps`).  ``row_idx``:
+    optional int32 [rows] prefix rows to fill (section 2.4): ``H`` then holds every
+    prefix row, row ``row_idx[r]`` is filled at position ``pos0 + row_idx[r]`` and the
+    unlisted (exact) rows are left alone.
     """
     args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
                      rms_eps=rms_eps, pos0=pos0, rows_per_chunk=rows_per_chunk,
                      stage_events=stage_events, copy_events=copy_events, k_scale=k_scale,
-                     v_scale=v_scale, A_scale=A_scale)
+                     v_scale=v_scale, A_scale=A_scale, row_idx=row_idx)
     lib = load()
     need = int(lib.ridgefill_fill_workspace_size(ctypes.byref(args)))
     if need == 0:
@@ -278,7 +286,8 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
 
 def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
              l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
-             stage_events=None, A_scale=None) -> GdnArgs:
+             stage_events=None, A_scale=None, exact_idx=None, X_exact=None, rho=None,
+             delta_M=None) -> GdnArgs:
     L, d_out, d_in = A.shape
     rows = H.shape[0]
     d_k = Wk.shape[1] // n_heads
@@ -295,11 +304,22 @@ def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: floa
     _dev(S, "S", torch.float32, (L, n_heads, d_v, d_k))
     if S0 is not None:
         _dev(S0, "S0", torch.float32, (L, n_heads, d_v, d_k))
+    n_exact = 0
+    if exact_idx is not None:
+        n_exact = exact_idx.shape[0]
+        _dev(exact_idx, "exact_idx", torch.int32, (n_exact,))
+        _dev(X_exact, "X_exact", torch.bfloat16, (L, n_exact, d_out))
+    if rho is not None:
+        _dev(rho, "rho", torch.float32, (L, n_heads))
+    if delta_M is not None:
+        _dev(delta_M, "delta_M", torch.float32, (L, n_heads, d_v, d_k))
     ev = _event_array(stage_events)
     a = GdnArgs(L, d_in, d_out, n_heads, d_k, d_v, chunk, 1 if host else 0, rows,
                 rows_per_chunk, float(rms_eps), float(l2_eps), _ptr(H), _ptr(A), _ptr(bias),
                 _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Wa), _ptr(Wb), _ptr(S0), _ptr(S),
-                ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None, _ptr(A_scale))
+                ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None, _ptr(A_scale),
+                _ptr(exact_idx), n_exact, _ptr(X_exact) if n_exact else None, _ptr(rho),
+                _ptr(delta_M))
     a._events_keepalive = ev
     return a
 
@@ -307,15 +327,20 @@ def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: floa
 def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
                        l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
                        workspace: Optional[torch.Tensor] = None, stream=None,
-                       stage_events=None, A_scale=None) -> None:
+                       stage_events=None, A_scale=None, exact_idx=None, X_exact=None,
+                       rho=None, delta_M=None) -> None:
     """End-of-fill recurrent state ``S`` [L, H, dv, dk] f32 of Gated DeltaNet layers.
 
     ``stage_events``: optional four ``torch.cuda.Event`` recorded around the first
     chunk's map GEMM, projection GEMM and state kernel.  ``A_scale``: int8 maps, as
-    for :func:`ridgefill_fill`."""
+    for :func:`ridgefill_fill`.  ``exact_idx`` (int32 [n]) and ``X_exact`` ([L, n, d_out]
+    bf16): exact prefix rows and their true inputs (section 2.4).  ``rho``: optional
+    [L, H] f32 output of the filled rows' share of the state; ``delta_M``: optional
+    [L, H, dv, dk] f32 terminal-state correction ``S += rho * delta_M`` (section 2.3)."""
     args = gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, n_heads=n_heads, rms_eps=rms_eps,
                     l2_eps=l2_eps, S0=S0, chunk=chunk, rows_per_chunk=rows_per_chunk,
-                    stage_events=stage_events, A_scale=A_scale)
+                    stage_events=stage_events, A_scale=A_scale, exact_idx=exact_idx,
+                    X_exact=X_exact, rho=rho, delta_M=delta_M)
     lib = load()
     need = int(lib.ridgefill_gdn_workspace_size(ctypes.byref(args)))
     if need == 0:

@@ -12,6 +12,8 @@ from .workloads import (  # noqa: F401
     channel_scales,
     fill_inputs,
     tail_inputs,
+    exact_rows,
+    true_inputs,
     gdn_inputs,
     calibration,
     to_f64,

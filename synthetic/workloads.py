@@ -34,6 +34,7 @@ _THREADS = max(1, min(32, os.cpu_count() or 1))
 _ID_SCALES, _ID_H, _ID_A, _ID_B, _ID_GAIN, _ID_WK, _ID_WV = 1, 2, 3, 4, 5, 6, 7
 _ID_WA, _ID_WB, _ID_X, _ID_YG, _ID_YB, _ID_YN = 8, 9, 10, 11, 12, 13
 _ID_TAILH, _ID_TAILX, _ID_TAILS = 14, 15, 16
+_ID_EXACT, _ID_XEX, _ID_XEXS = 17, 18, 19
 
 
 def normal(shape: Sequence[int], key: Tuple[int, ...]) -> np.ndarray:
@@ -246,6 +247,22 @@ def tail_inputs(shape: FillShape, seed: int, c: int) -> Dict[str, torch.Tensor]:
     xt = np.stack([normal((c, d), (seed, _ID_TAILX, l)) *
                    np.exp(normal((d,), (seed, _ID_TAILS, l)))[None, :] for l in range(L)])
     return {"H_tail": _split_state(c, d, seed, _ID_TAILH), "X_true": _bf16(xt.astype(np.float32))}
+
+
+def exact_rows(rows: int, frac: float, seed: int) -> torch.Tensor:
+    """A seeded set of exact prefix rows: about ``frac`` of ``rows``, drawn
+    uniformly without replacement, as sorted int32 indices (CPU)."""
+    n = int(round(frac * rows))
+    pick = np.argsort(normal((rows,), (seed, _ID_EXACT)))[:n]
+    return torch.from_numpy(np.sort(pick).astype(np.int32))
+
+
+def true_inputs(n_layers: int, n: int, d: int, seed: int) -> torch.Tensor:
+    """Stand-ins for ``n`` rows' true late-layer inputs, [n_layers, n, d] bf16:
+    ``N(0, 1)`` times per-layer, per-channel scales ``exp(N(0, 1))``."""
+    x = np.stack([normal((n, d), (seed, _ID_XEX, l)) *
+                  np.exp(normal((d,), (seed, _ID_XEXS, l)))[None, :] for l in range(n_layers)])
+    return _bf16(x.astype(np.float32))
 
 
 def gdn_inputs(shape: GdnShape, seed: int, rows: Optional[int] = None,
