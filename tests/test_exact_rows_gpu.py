@@ -136,7 +136,7 @@ def test_gdn_exact_rows_state_and_rho(rows_per_chunk):
             compare(S[l, h].double().numpy(), ref[l, h], f"S layer {l} head {h}")
     rref = oracle.gdn_rho(o["H"], o["A"], o["b"], o["g"], o["Wa"], shape.rms_eps, 8,
                           exact_idx=ex, X_exact=to_f64(X))
-    assert np.abs(rref - 1).max() > 0.05 and rref.min() > 0.05  # a case that tells rho apart
+    assert np.ptp(rref) > 0.3  # heads whose filled share differs widely
     np.testing.assert_allclose(rho.double().numpy(), rref, rtol=0, atol=RHO_ATOL)
 
 
