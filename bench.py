@@ -36,8 +36,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import (WORKLOADS, FillShape, GdnShape, fill_inputs, gdn_inputs,  # noqa: E402
-                       tail_inputs, to_f64)
+from synthetic import (WORKLOADS, FillShape, GdnShape, exact_rows, fill_inputs,  # noqa: E402
+                       gdn_inputs, tail_inputs, to_f64, true_inputs)
 
 METRIC = "filled token-layers/s (fill-stage ms and % of GB300 bf16 tensor peak alongside)"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
@@ -151,21 +151,24 @@ class AttnWorkload:
     """Attention late layers (ridgefill_fill); maps in HBM or in pinned host memory."""
 
     def __init__(self, shape: FillShape, host_maps=False, rows_per_chunk=0, rescale_rows=0,
-                 int8_maps=False):
+                 int8_maps=False, exact_frac=0.0):
         self.shape, self.host_maps, self.rpc = shape, host_maps, rows_per_chunk
         self.c = rescale_rows
         self.q8 = int8_maps
+        self.exact_frac = exact_frac
         if self.c and host_maps:
             raise ValueError("the rescale needs the maps resident in device memory")
         s = shape
-        self.token_layers = s.rows * s.n_layers
+        # with exact prefix rows (section 2.4) only the other rows are filled
+        self.n_fill = s.rows - int(round(exact_frac * s.rows))
+        self.token_layers = self.n_fill * s.n_layers
         self.stage_names = ["map_gemm", "kv_gemm"]
         self.stage_work = {  # algorithmic FLOP of the first chunk's launches
             "map_gemm": 2.0 * self._chunk_rows() * s.n_layers * s.d * s.d,
             "kv_gemm": 2.0 * self._chunk_rows() * s.n_layers * s.d * 2 * s.kv_width,
         }
         self.stage_bound = {"map_gemm": "tensor", "kv_gemm": "tensor"}
-        self.total_flops = 2.0 * s.rows * s.n_layers * (s.d * s.d + s.d * 2 * s.kv_width)
+        self.total_flops = 2.0 * self.n_fill * s.n_layers * (s.d * s.d + s.d * 2 * s.kv_width)
         if self.c:
             # value rescale before the fill: the c tail rows' map GEMM and one value
             # projection of the 2c stacked predicted and true rows; the fill applies
@@ -177,11 +180,12 @@ class AttnWorkload:
             self.total_flops += self.stage_work["value_rescale"]
 
     def _chunk_rows(self):
-        return min(self.rpc, self.shape.rows) if self.rpc else self.shape.rows
+        return min(self.rpc, self.n_fill) if self.rpc else self.n_fill
 
     def launches_per_step(self):
-        chunks = -(-self.shape.rows // self._chunk_rows())
+        chunks = -(-self.n_fill // self._chunk_rows())
         per_chunk = (self.shape.n_layers + 1) if self.host_maps else 2
+        per_chunk += 1 if self.exact_frac else 0  # the row gather
         # rescale: map GEMM, true-input norm, value GEMM, ratio
         return chunks * per_chunk + (4 if self.c else 0)
 
@@ -206,6 +210,16 @@ class AttnWorkload:
                          self.d["Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
                          rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc,
                          A_scale=self.A_scale)
+        self.row_idx = None
+        if self.exact_frac:
+            keep = np.ones(s.rows, bool)
+            keep[exact_rows(s.rows, self.exact_frac, seed=seed).numpy()] = False
+            self.row_idx = torch.from_numpy(np.nonzero(keep)[0].astype(np.int32)).to(dev)
+            assert self.row_idx.numel() == self.n_fill
+            a = rb.fill_args(self.d["H"], self.A, self.d["b"], self.d["g"], self.d["Wk"],
+                             self.d["Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
+                             rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc,
+                             A_scale=self.A_scale, row_idx=self.row_idx)
         self.ws = torch.empty(rb.fill_workspace_size(a), dtype=torch.uint8, device=dev)
         self.H_dev = self.d["H"]
         if self.c:
@@ -241,7 +255,7 @@ class AttnWorkload:
                        stage_events=None if ev is None else ev[:3],
                        copy_events=None if (ev is None or not self.host_maps) else
                        ev[3:3 + 2 * s.n_layers], v_scale=self.scale if self.c else None,
-                       A_scale=self.A_scale)
+                       A_scale=self.A_scale, row_idx=self.row_idx)
 
     def copy_ms(self, ev):
         """Durations of the first chunk's per-layer map copies (host maps only)."""
@@ -297,6 +311,7 @@ class AttnWorkload:
                 "map_format": "int8, one bf16 scale per 128 weights" if self.q8 else "bf16",
                 "rows_per_chunk": self.rpc or s.rows,
                 "value_rescale_tail_rows": self.c,
+                "exact_prefix_rows": s.rows - self.n_fill,
                 "l2": "inputs larger than L2 (maps %d MiB, split state %d MiB)" % (
                     s.n_layers * s.d * s.d * 2 >> 20, s.rows * s.d * 2 >> 20)}
 
@@ -304,17 +319,20 @@ class AttnWorkload:
 class HybridWorkload:
     """Gated DeltaNet late layers (ridgefill_fill_gdn) plus attention late layers."""
 
-    def __init__(self, shape: GdnShape):
+    def __init__(self, shape: GdnShape, exact_frac=0.0):
         self.shape = s = shape
         La, Lg, H = s.n_attn, s.n_gdn, s.n_heads
         kvw = s.n_kv * s.head_dim
-        self.token_layers = s.rows * (La + Lg)
+        self.exact_frac = exact_frac
+        self.n_exact = int(round(exact_frac * s.rows))
+        # filled token-layers: exact rows still enter the GDN state but are not filled
+        self.token_layers = (s.rows - self.n_exact) * (La + Lg)
         self.stage_names = ["attn_map_gemm", "attn_kv_gemm", "gdn_map_gemm", "gdn_proj_gemm",
                             "gdn_state"]
         proj = H * s.d_k + H * s.d_v + 2 * H
         self.stage_work = {
-            "attn_map_gemm": 2.0 * s.rows * La * s.d * s.d,
-            "attn_kv_gemm": 2.0 * s.rows * La * s.d * 2 * kvw,
+            "attn_map_gemm": 2.0 * (s.rows - self.n_exact) * La * s.d * s.d,
+            "attn_kv_gemm": 2.0 * (s.rows - self.n_exact) * La * s.d * 2 * kvw,
             "gdn_map_gemm": 2.0 * s.rows * Lg * s.d * s.d,
             "gdn_proj_gemm": 2.0 * s.rows * Lg * s.d * proj,
             # per row and head: dot product and rank-1 update, one FMA per state element each
@@ -325,7 +343,8 @@ class HybridWorkload:
         self.total_flops = sum(v for k, v in self.stage_work.items() if k != "gdn_state")
 
     def launches_per_step(self):
-        return 5
+        # attention map + K/V (+ gather), GDN map, projection, state (+ exact input, rho, finish)
+        return 5 + (4 if self.exact_frac else 0)
 
     def setup(self, dev, seed):
         from late_layer_kv_gb300 import ridgefill as rb
@@ -342,6 +361,24 @@ class HybridWorkload:
                          rope_theta=s.rope_theta, rms_eps=s.rms_eps)
         g = rb.gdn_args(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"], d["Wb"],
                         self.S, n_heads=s.n_heads, rms_eps=s.rms_eps)
+        self.row_idx = self.exact_idx = self.X_exact = self.rho = self.dM = None
+        if self.exact_frac:
+            ex = exact_rows(s.rows, self.exact_frac, seed=seed)
+            keep = np.ones(s.rows, bool)
+            keep[ex.numpy()] = False
+            self.row_idx = torch.from_numpy(np.nonzero(keep)[0].astype(np.int32)).to(dev)
+            self.exact_idx = ex.to(dev)
+            self.X_exact = true_inputs(s.n_gdn, self.n_exact, s.d, seed=seed).to(dev)
+            self.rho = torch.empty((s.n_gdn, s.n_heads), dtype=torch.float32, device=dev)
+            gen = torch.Generator(device=dev).manual_seed(seed)
+            self.dM = 1e-3 * torch.randn((s.n_gdn, s.n_heads, s.d_v, s.d_k), generator=gen,
+                                         device=dev)
+            a = rb.fill_args(d["H"], d["attn_A"], d["attn_b"], d["attn_g"], d["attn_Wk"],
+                             d["attn_Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
+                             rope_theta=s.rope_theta, rms_eps=s.rms_eps, row_idx=self.row_idx)
+            g = rb.gdn_args(d["H"], d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"], d["Wb"],
+                            self.S, n_heads=s.n_heads, rms_eps=s.rms_eps, exact_idx=self.exact_idx,
+                            X_exact=self.X_exact, rho=self.rho, delta_M=self.dM)
         self.ws = torch.empty(max(rb.fill_workspace_size(a), rb.gdn_workspace_size(g)),
                               dtype=torch.uint8, device=dev)
         self.H_dev = d["H"]
@@ -355,11 +392,14 @@ class HybridWorkload:
         ridgefill_fill(self.H_dev, d["attn_A"], d["attn_b"], d["attn_g"], d["attn_Wk"],
                        d["attn_Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
                        rope_theta=s.rope_theta, rms_eps=s.rms_eps, workspace=self.ws,
-                       stream=stream, stage_events=None if ev is None else ev[0:3])
+                       stream=stream, stage_events=None if ev is None else ev[0:3],
+                       row_idx=self.row_idx)
         ridgefill_fill_gdn(self.H_dev, d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"],
                            d["Wb"], self.S, n_heads=s.n_heads, rms_eps=s.rms_eps,
                            workspace=self.ws, stream=stream,
-                           stage_events=None if ev is None else ev[3:7])
+                           stage_events=None if ev is None else ev[3:7],
+                           exact_idx=self.exact_idx, X_exact=self.X_exact, rho=self.rho,
+                           delta_M=self.dM)
 
     def stage_ms(self, ev):
         pairs = [(0, 1), (1, 2), (3, 4), (4, 5), (5, 6)]
@@ -406,7 +446,9 @@ class HybridWorkload:
         s = self.shape
         return {"workload": s.name, "d": s.d, "late_layers": s.n_attn + s.n_gdn,
                 "gdn_layers": s.n_gdn, "attn_layers": s.n_attn, "gdn_heads": s.n_heads,
-                "d_k": s.d_k, "d_v": s.d_v, "N": s.N, "T": s.T, "filled_rows": s.rows,
+                "d_k": s.d_k, "d_v": s.d_v, "N": s.N, "T": s.T, "filled_rows": s.rows - self.n_exact,
+                "exact_prefix_rows": self.n_exact,
+                "terminal_correction": bool(self.exact_frac),
                 "kv_heads": s.n_kv, "head_dim": s.head_dim, "maps": "hbm",
                 "l2": "inputs larger than L2 (maps %d MiB)" % (
                     (s.n_attn + s.n_gdn) * s.d * s.d * 2 >> 20)}
@@ -525,7 +567,7 @@ def make_workload(name, args):
     if isinstance(shape, GdnShape):
         if args.rows:
             shape = replace(shape, name=f"{shape.name}_rows{args.rows}", N=args.rows + shape.T)
-        return HybridWorkload(shape)
+        return HybridWorkload(shape, exact_frac=args.exact_frac)
     if args.rows or args.layers:
         rows = args.rows or shape.rows
         L = args.layers or shape.n_layers
@@ -534,7 +576,8 @@ def make_workload(name, args):
     if name.startswith("dense27b") and not rpc:
         rpc = 16384  # late-layer X_hat processed in row chunks
     return AttnWorkload(shape, host_maps=name.startswith("hostmaps"), rows_per_chunk=rpc,
-                        rescale_rows=args.rescale, int8_maps=args.int8_maps)
+                        rescale_rows=args.rescale, int8_maps=args.int8_maps,
+                        exact_frac=args.exact_frac)
 
 
 # ----------------------------------------------------------------------------- arms
@@ -751,6 +794,9 @@ def main():
     ap.add_argument("--fit", action="store_true",
                     help="benchmark the ridge fit of the workload's maps instead of the fill")
     ap.add_argument("--fit-rows", type=int, default=0)
+    ap.add_argument("--exact-frac", type=float, default=0.0,
+                    help="share of prefix rows run exactly (skipped by the fill; GDN layers take "
+                         "their true inputs and apply the terminal-state correction)")
     ap.add_argument("--int8-maps", action="store_true",
                     help="maps as int8 codes with one bf16 scale per 128 weights")
     ap.add_argument("--rescale", type=int, default=0, metavar="C",
