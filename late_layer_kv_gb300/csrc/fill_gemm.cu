@@ -779,6 +779,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   if (warp == 0 && lane == 0) {
     tma_prefetch(&p.tmA);
     tma_prefetch(&p.tmB[0]);
+    if (!kQ8 && p.mode == kModeGram && p.m_tiles > p.gram_x_tiles) tma_prefetch(&p.tmA2);
     if (kQ8 || p.mode == kModeKV || p.mode == kModeGdnProj) tma_prefetch(&p.tmB[1]);
     if (!kQ8 && p.mode == kModeGdnProj) {
       tma_prefetch(&p.tmB[2]);
@@ -819,9 +820,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
           const uint32_t tx = kQ8 ? kHalfBytes : kHalfBytes + half * kBK * 2;
           if (rank == 0) mbar_expect_tx(&full[stage], tx);
           else mbar_expect_tx_cl(fb, tx);
-          tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, kb * kBK, m * kBM, b);
-          if (kQ8) {
-            // B comes from the converter warps
+          if (!kQ8 && p.mode == kModeGram) {
+            // MN-major operands: 64-wide column blocks of [rows, width] arrays, 64 rows of K;
+            // A: this CTA's 128 columns of [X | Y_1 .. Y_L], B: its half of the X columns
+            uint8_t* adst = sA + stage * kHalfBytes;
+            // (the empty second half of an odd last row tile reads past X: zero fill)
+            if (m < p.gram_x_tiles || m >= p.m_tiles) {
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_3d_pair(smem_u32(adst + j * 8192), &p.tmA, fb, m * kBM + 64 * j,
+                                 kb * kBK, 0);
+            } else {
+              const int mm = m - p.gram_x_tiles;
+              const int l = mm / p.gram_y_tiles_per_layer;
+              const int m0 = (mm % p.gram_y_tiles_per_layer) * kBM;
+              for (int j = 0; j < kBM / 64; ++j)
+                tma_load_3d_pair(smem_u32(adst + j * 8192), &p.tmA2, fb, m0 + 64 * j, kb * kBK, l);
+            }
+            for (int j = 0; j < half / 64; ++j)
+              tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes + j * 8192), &p.tmB[0], fb,
+                               tb.nrow + half * static_cast<int>(rank) + 64 * j, kb * kBK, 0);
+          } else {
+            tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, kb * kBK, m * kBM, b);
+          }
+          if (kQ8 || p.mode == kModeGram) {
+            // B comes from the converter warps, or was loaded above
           } else if (tb.seg < 2)
             tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[tb.seg], fb, kb * kBK,
                              tb.nrow + half * static_cast<int>(rank), b);
@@ -848,7 +870,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         int mp, n, b;
         decode_pair(t, p, mp, n, b);
         const TileB tb = tile_b(p, n);
-        const uint32_t idesc = idesc_bf16_f32(2 * kBM, tb.bn);
+        const bool mn = !kQ8 && p.mode == kModeGram;
+        const uint32_t idesc = idesc_bf16_f32(2 * kBM, tb.bn) | (mn ? (3u << 15) : 0u);
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, kErrMma)) break;
@@ -862,11 +885,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
             break;
           }
           tc_fence_after();
-          const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * kHalfBytes));
-          const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * kHalfBytes));
+          if (!mn) {
+            const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * kHalfBytes));
+            const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * kHalfBytes));
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16_pair(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16_pair(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          } else {
+            // MN-major: 64-element column blocks 8 KB apart, K rows 128 B apart
+            const uint64_t ad = sdesc_mnmajor_sw128(smem_u32(sA + stage * kHalfBytes), 8192);
+            const uint64_t bd = sdesc_mnmajor_sw128(smem_u32(sB + stage * kHalfBytes), 8192);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k)  // advance 16 K rows (2048 B)
+              mma_bf16_pair(dt, ad + 128 * k, bd + 128 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          }
           mma_commit_pair(&empty[stage], 3);
           if (++stage == kS) {
             stage = 0;
@@ -938,6 +970,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         epilogue_map(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
       } else if (p.mode == kModeKV) {
         epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
+      } else if (p.mode == kModeGram) {
+        epilogue_gram(p, tcol, q, lane, m, n, tempty0 + 8 * acc);
       } else {
         epilogue_gdn(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
       }

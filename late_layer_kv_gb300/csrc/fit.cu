@@ -411,6 +411,10 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
 // Gram-mode tcgen05 GEMM: out_G[m, n] += sum_k Xa[k, m] Xb[k, n] for the d-wide
 // arrays Xa, Xb ([rows, d], MN-major), and, if Y is given, out_C[l, o, n] +=
 // sum_k Y[l, k, o] Xb[k, n].
+// Gram products on CTA pairs (M = 256: each CTA stages 128 columns of [X | Y] and half of
+// the tile's X columns) or on single CTAs
+constexpr bool kGramPairs = true;
+
 rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int64_t rows, int d,
                       int dout, int bn, double* out_G, double* out_C, cudaStream_t s) {
   GemmParams p{};
@@ -438,9 +442,18 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   p.gram_ld = d;
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
-  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  cudaError_t e = launch_gemm(p, grid, s);
+  cudaError_t e;
+  if (kGramPairs) {
+    const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+    const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+    if (pairs <= 0) return RF_OK;
+    e = launch_gemm2(p, pairs, s);
+  } else {
+    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
+    const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
+    if (grid <= 0) return RF_OK;
+    e = launch_gemm(p, grid, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "Gram GEMM launch");
   return RF_OK;
 }
