@@ -816,7 +816,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
           if (paced && kb % p.sync_k == 0) {
             // wait until every producer of the previous epoch has issued it
             const int e = wave * p.sync_epochs + kb / p.sync_k;
-            if (e > 0 && e <= p.sync_count) {
+            if (e > 0) {
               const int pw = (e - 1) / p.sync_epochs;  // wave of epoch e - 1
               const int left = total - pw * npairs;
               const int need = 2 * (left < npairs ? left : npairs);
@@ -869,10 +869,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
             stage = 0;
             phase ^= 1;
           }
-          if (paced && ((kb + 1) % p.sync_k == 0 || kb + 1 == p.k_blocks)) {
-            const int e = wave * p.sync_epochs + kb / p.sync_k;
-            if (e < p.sync_count) atomicAdd(p.sync + e, 1);
-          }
+          if (paced && ((kb + 1) % p.sync_k == 0 || kb + 1 == p.k_blocks))
+            atomicAdd(p.sync + wave * p.sync_epochs + kb / p.sync_k, 1);
         }
       }
       if (!ok && rank == 0)  // let the copies counted on this CTA's barriers land
@@ -1049,27 +1047,6 @@ cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream) {
   }
   rf_gemm2_kernel<false><<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
-}
-
-int gemm2_resident_pairs() {
-  static int cached = -1;
-  if (cached >= 0) return cached;
-  if (cudaFuncSetAttribute(rf_gemm2_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kGemmSmem) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(2, 1, 1);
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmem;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, rf_gemm2_kernel<false>, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  cached = n;
-  return n;
 }
 
 cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream) {

@@ -428,18 +428,10 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
 // the tile's X columns) or on single CTAs
 constexpr bool kGramPairs = true;
 
-// Persistent pair grid of a Gram launch: at most one cluster per two SMs, and no more than
-// can be resident at once (the pacing waits on every cluster of the grid).
-int64_t gram_pairs(int64_t tiles) {
-  int64_t pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
-  const int64_t res = gemm2_resident_pairs();
-  return res > 0 && pairs > res ? res : pairs;
-}
-
 int64_t gram_sync_ints(int64_t m_tiles, int64_t n_tiles, int64_t rows) {
   if (!kGramPairs) return 0;
   const int64_t tiles = (m_tiles + 1) / 2 * n_tiles;
-  const int64_t pairs = gram_pairs(tiles);
+  const int64_t pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
   if (pairs <= 0) return 0;
   const int64_t waves = ceil_div(tiles, pairs);
   return waves * ceil_div(ceil_div(rows > 0 ? rows : 1, kBK), kGramSyncK);
@@ -477,17 +469,15 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   cudaError_t e;
   if (kGramPairs) {
     const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
-    const int pairs = static_cast<int>(gram_pairs(tiles));
+    const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
     if (pairs <= 0) return RF_OK;
     const int64_t need = gram_sync_ints(p.m_tiles, p.n_tiles, rows);
-    // paced only when the whole grid is known to be resident at once
-    if (sync != nullptr && need > 0 && need <= sync_ints && gemm2_resident_pairs() >= pairs) {
+    if (sync != nullptr && need > 0 && need <= sync_ints) {
       if ((e = cudaMemsetAsync(sync, 0, static_cast<size_t>(need) * 4, s)) != cudaSuccess)
         return cuda_fail(e, "clearing the Gram pacing counters");
       p.sync = sync;
       p.sync_k = kGramSyncK;
       p.sync_epochs = static_cast<int32_t>(ceil_div(p.k_blocks, kGramSyncK));
-      p.sync_count = static_cast<int32_t>(need);
     }
     e = launch_gemm2(p, pairs, s);
   } else {

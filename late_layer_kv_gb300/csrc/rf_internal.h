@@ -112,7 +112,6 @@ struct GemmParams {
   int* sync;
   int32_t sync_k;
   int32_t sync_epochs;  // epochs per tile
-  int32_t sync_count;   // counters available (an epoch beyond them is not paced)
   float inv_freq_hi[64];
   float inv_freq_lo[64];
 };
@@ -123,9 +122,6 @@ cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream);
 // map mode on CTA pairs with int8 maps (p.q8, p.q8_scale); tmB unused
 cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream);
-// Clusters of the pair kernel (bf16 operands) that can be resident at once on this device
-// (0 if the query fails); a paced launch must not exceed it.
-int gemm2_resident_pairs();
 
 // ------------------------------------------------------------ GDN state
 struct GdnStateParams {
