@@ -805,27 +805,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       int issued[kS];
       for (int s = 0; s < kS; ++s) issued[s] = -1;
       bool ok = true;
-      const bool paced = !kQ8 && p.sync != nullptr;
-      int wave = 0;
-      for (int t = pair; t < total && ok; t += npairs, ++wave) {
+      for (int t = pair; t < total && ok; t += npairs) {
         int mp, n, b;
         decode_pair(t, p, mp, n, b);
         const int m = 2 * mp + static_cast<int>(rank);
         const TileB tb = tile_b(p, n);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (paced && kb % p.sync_k == 0) {
-            // wait until every producer of the previous epoch has issued it
-            const int e = wave * p.sync_epochs + kb / p.sync_k;
-            if (e > 0) {
-              const int pw = (e - 1) / p.sync_epochs;  // wave of epoch e - 1
-              const int left = total - pw * npairs;
-              const int need = 2 * (left < npairs ? left : npairs);
-              if (!counter_wait(p.sync + (e - 1), need, abort_flag, p.err, kErrProducer)) {
-                ok = false;
-                break;
-              }
-            }
-          }
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrProducer)) {
             ok = false;
             break;
@@ -869,8 +854,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
             stage = 0;
             phase ^= 1;
           }
-          if (paced && ((kb + 1) % p.sync_k == 0 || kb + 1 == p.k_blocks))
-            atomicAdd(p.sync + wave * p.sync_epochs + kb / p.sync_k, 1);
         }
       }
       if (!ok && rank == 0)  // let the copies counted on this CTA's barriers land

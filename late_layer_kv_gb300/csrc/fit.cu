@@ -358,18 +358,10 @@ __global__ void bias_kernel(const double* sy, const double* count, const float* 
 }
 
 // ------------------------------------------------------------ plan
-// k-blocks per pacing epoch of the Gram products on CTA pairs
-constexpr int kGramSyncK = 64;
-
-// Pacing counters one Gram launch needs: waves of the persistent pair grid times
-// epochs per tile (0 when the products run on single CTAs).
-int64_t gram_sync_ints(int64_t m_tiles, int64_t n_tiles, int64_t rows);
-
 struct FitPlan {
   size_t off_gh = 0, off_s = 0, off_mu32 = 0, off_mu64 = 0, off_alpha = 0,
          off_xhi = 0, off_xlo = 0, off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0,
-         off_cs = 0, off_sync = 0, total = 0;
-  int64_t sync_ints = 0;
+         off_cs = 0, total = 0;
   int bn = 0;
   int slabs = 0;
   int64_t slab_rows = 0;
@@ -399,8 +391,6 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->slab_rows = ceil_div(ceil_div(rows, 64), 64) * 64;  // at most 64 slabs, 64-row runs
     pl->slabs = static_cast<int>(ceil_div(rows, pl->slab_rows));
     pl->off_cs = off;    off = align_up(off + static_cast<size_t>(pl->slabs) * (d + M) * 8, 256);
-    const int64_t n = gram_sync_ints(d / 128 + M / 128, d / pl->bn, rows);
-    pl->sync_ints = n > pl->sync_ints ? n : pl->sync_ints;
   }
   if (a->flags & RF_FIT_SOLVE) {
     pl->off_gh = off;    off = align_up(off + d * d * 4, 256);
@@ -414,10 +404,7 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->off_bp = off;    off = align_up(off + d * 3 * d * 2, 256);
     pl->off_ap = off;    off = align_up(off + M * 3 * d * 2, 256);
     pl->off_part = off;  off = align_up(off + M * (d / pl->bn) * 4, 256);
-    const int64_t n = gram_sync_ints(d / 128, d / pl->bn, static_cast<int64_t>(d));
-    pl->sync_ints = n > pl->sync_ints ? n : pl->sync_ints;
   }
-  pl->off_sync = off;    off = align_up(off + static_cast<size_t>(pl->sync_ints) * 4, 256);
   pl->total = off;
 }
 
@@ -428,19 +415,8 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
 // the tile's X columns) or on single CTAs
 constexpr bool kGramPairs = true;
 
-int64_t gram_sync_ints(int64_t m_tiles, int64_t n_tiles, int64_t rows) {
-  if (!kGramPairs) return 0;
-  const int64_t tiles = (m_tiles + 1) / 2 * n_tiles;
-  const int64_t pairs = tiles < sm_count() / 2 ? tiles : sm_count() / 2;
-  if (pairs <= 0) return 0;
-  const int64_t waves = ceil_div(tiles, pairs);
-  return waves * ceil_div(ceil_div(rows > 0 ? rows : 1, kBK), kGramSyncK);
-}
-
-// `sync`: sync_ints zeroed-before-use pacing counters in the workspace (see GemmParams)
 rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int64_t rows, int d,
-                      int dout, int bn, double* out_G, double* out_C, int* sync,
-                      int64_t sync_ints, cudaStream_t s) {
+                      int dout, int bn, double* out_G, double* out_C, cudaStream_t s) {
   GemmParams p{};
   p.mode = kModeGram;
   p.k_blocks = static_cast<int32_t>(ceil_div(rows, kBK));
@@ -471,14 +447,6 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
     const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
     const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
     if (pairs <= 0) return RF_OK;
-    const int64_t need = gram_sync_ints(p.m_tiles, p.n_tiles, rows);
-    if (sync != nullptr && need > 0 && need <= sync_ints) {
-      if ((e = cudaMemsetAsync(sync, 0, static_cast<size_t>(need) * 4, s)) != cudaSuccess)
-        return cuda_fail(e, "clearing the Gram pacing counters");
-      p.sync = sync;
-      p.sync_k = kGramSyncK;
-      p.sync_epochs = static_cast<int32_t>(ceil_div(p.k_blocks, kGramSyncK));
-    }
     e = launch_gemm2(p, pairs, s);
   } else {
     const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
@@ -508,8 +476,7 @@ rf_status accumulate(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaS
   add_count_kernel<<<1, 1, 0, s>>>(a->count, static_cast<double>(rows));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
-  return launch_gram(a->X, a->X, a->Y, L, rows, din, dout, pl.bn, a->G, a->C,
-                     reinterpret_cast<int*>(ws + pl.off_sync), pl.sync_ints, s);
+  return launch_gram(a->X, a->X, a->Y, L, rows, din, dout, pl.bn, a->G, a->C, s);
 }
 
 rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream_t s) {
@@ -585,13 +552,9 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   if ((e = cudaMemsetAsync(Gi, 0, static_cast<size_t>(dd) * 8, s)) != cudaSuccess)
     return cuda_fail(e, "clearing the inverse");
   rf_status st;
-  int* sync = reinterpret_cast<int*>(ws + pl.off_sync);
-  if ((st = launch_gram(Xhi, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, sync, pl.sync_ints, s)) != RF_OK)
-    return st;
-  if ((st = launch_gram(Xhi, Xlo, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, sync, pl.sync_ints, s)) != RF_OK)
-    return st;
-  if ((st = launch_gram(Xlo, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, sync, pl.sync_ints, s)) != RF_OK)
-    return st;
+  if ((st = launch_gram(Xhi, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
+  if ((st = launch_gram(Xhi, Xlo, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
+  if ((st = launch_gram(Xlo, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
 
   split_ginv_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gi, d, Bp);
   split_rhs_kernel<<<static_cast<unsigned>((M * d + 255) / 256), 256, 0, s>>>(

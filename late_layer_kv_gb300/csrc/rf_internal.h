@@ -106,12 +106,6 @@ struct GemmParams {
   float* bias_part;         // [M, n_tiles]
   int32_t out_ld;
   int* err;
-  // pacing of the Gram products on CTA pairs: every producer finishes issuing epoch
-  // e (sync_k k-blocks of one tile) before any starts epoch e + 1, so that tiles that
-  // share operand slabs read them from L2 together; counters zeroed before the launch
-  int* sync;
-  int32_t sync_k;
-  int32_t sync_epochs;  // epochs per tile
   float inv_freq_hi[64];
   float inv_freq_lo[64];
 };

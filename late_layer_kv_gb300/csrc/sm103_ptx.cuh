@@ -127,24 +127,6 @@ __device__ __forceinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t pa
   }
 }
 
-// Bounded wait until the global counter *ctr reaches `need` (pacing between CTAs
-// that are all resident: a persistent grid of one CTA per SM).
-__device__ __forceinline__ bool counter_wait(const int* ctr, int need, volatile int* abort_flag,
-                                             int* err, int site) {
-  if (*reinterpret_cast<const volatile int*>(ctr) >= need) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-    __nanosleep(64);
-    if (*reinterpret_cast<const volatile int*>(ctr) >= need) return true;
-    if (*abort_flag) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      *abort_flag = 1;
-      atomicCAS(err, 0, site);
-      return false;
-    }
-  }
-}
-
 // Wait for phase `parity` of `bar` until the time limit only (used to drain
 // copies and MMAs still in flight after another role gave up).
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {
