@@ -140,6 +140,22 @@ def _dist():
             int(os.environ.get("LOCAL_RANK", "0")))
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's ``x`` (timed regions end when the slowest replica
+    does); ``x`` itself with one rank."""
+    if world <= 1:
+        return float(x)
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units all replicas processed per second over the slowest replica's time."""
+    return units_per_rank * world / (ms / 1000.0)
+
+
 def _cores():
     for v in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
         if os.environ.get(v):
@@ -648,13 +664,9 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop()
     assert device_error(stream) == 0, "device wait ran out during the timed region"
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     ms_step = ms / steps
-    value = wl.token_layers * world / (ms_step / 1000.0)
+    value = whole_job_rate(wl.token_layers, world, ms_step)
 
     peaks, src = _peaks()
     sustained = ms >= 2000.0  # long regions run under the power cap
@@ -695,12 +707,8 @@ def run_ours(args):
             wl.e2e_step(stream)
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / steps
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
-        e2e = {"value": wl.token_layers * world / (ems / 1000.0), "unit": getattr(wl, "unit", "token-layers/s"),
+        ems = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
+        e2e = {"value": whole_job_rate(wl.token_layers, world, ems), "unit": getattr(wl, "unit", "token-layers/s"),
                "ms_per_step": ems, "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
 
     host_link = None
