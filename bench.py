@@ -259,7 +259,7 @@ class AttnWorkload:
     def n_events(self):
         return 3 + (2 * self.shape.n_layers if self.host_maps else 0) + (1 if self.c else 0)
 
-    def step(self, stream, ev=None):
+    def step(self, stream, ev=None, H=None, ws=None):
         from late_layer_kv_gb300 import ridgefill_fill
         s, d = self.shape, self.d
         if self.c:
@@ -271,9 +271,10 @@ class AttnWorkload:
                               self.Kc, self.Vc, which=RF_RESCALE_VALUES, head_dim=s.head_dim,
                               rms_eps=s.rms_eps, rows=0, scale=self.scale,
                               workspace=self.rws, stream=stream, A_scale=self.A_scale)
-        ridgefill_fill(self.H_dev, self.A, d["b"], d["g"], d["Wk"], d["Wv"], self.Kc, self.Vc,
-                       head_dim=s.head_dim, rope_theta=s.rope_theta, rms_eps=s.rms_eps,
-                       rows_per_chunk=self.rpc, workspace=self.ws, stream=stream,
+        ridgefill_fill(self.H_dev if H is None else H, self.A, d["b"], d["g"], d["Wk"], d["Wv"],
+                       self.Kc, self.Vc, head_dim=s.head_dim, rope_theta=s.rope_theta,
+                       rms_eps=s.rms_eps, rows_per_chunk=self.rpc,
+                       workspace=self.ws if ws is None else ws, stream=stream,
                        stage_events=None if ev is None else ev[:3],
                        copy_events=None if (ev is None or not self.host_maps) else
                        ev[3:3 + 2 * s.n_layers], v_scale=self.scale if self.c else None,
@@ -291,11 +292,23 @@ class AttnWorkload:
 
     # end to end: pinned H in, two cache rows per layer out
     def e2e_buffers(self):
+        from late_layer_kv_gb300 import ridgefill as rb
         s = self.shape
         self.H_host = self.inp["H"].pin_memory()
         self.out_host = torch.empty((s.n_layers, s.n_kv, 2, s.head_dim),
                                     dtype=torch.bfloat16).pin_memory()
-        self.H_dev = torch.empty_like(self.d["H"])
+        # the fill reads the pinned split state itself, its copy overlapped with the map GEMM
+        # (with a row list the rows are copied first, then gathered)
+        self.h_from_host = self.row_idx is None
+        if self.h_from_host:
+            a = rb.fill_args(self.H_host, self.A, self.d["b"], self.d["g"], self.d["Wk"],
+                             self.d["Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
+                             rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc,
+                             A_scale=self.A_scale)
+            self.ws_e2e = torch.empty(rb.fill_workspace_size(a), dtype=torch.uint8,
+                                      device=self.Kc.device)
+        else:
+            self.H_dev = torch.empty_like(self.d["H"])
         bi = self.H_host.numel() * 2
         if self.c:  # the tail rows' split states and true inputs come from the host too
             self.tail_host = {k: v.cpu().pin_memory() for k, v in self.tail.items()}
@@ -304,11 +317,14 @@ class AttnWorkload:
 
     def e2e_step(self, stream):
         r = self.shape.rows
-        self.H_dev.copy_(self.H_host, non_blocking=True)
         if self.c:
             for k, v in self.tail_host.items():
                 self.tail[k].copy_(v, non_blocking=True)
-        self.step(stream)
+        if self.h_from_host:
+            self.step(stream, H=self.H_host, ws=self.ws_e2e)
+        else:
+            self.H_dev.copy_(self.H_host, non_blocking=True)
+            self.step(stream)
         self.out_host.copy_(self.Kc[:, :, r - 2:r], non_blocking=True)
 
     def cpu_rate(self, budget_flop):

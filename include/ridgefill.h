@@ -104,6 +104,11 @@ typedef enum rf_status {
  *   [rows], 4-byte aligned, entries distinct and in [0, h_rows) (an entry
  *   outside is skipped and reported by ridgefill_device_error as
  *   RF_ERR_ARG); pos0 + h_rows <= cache_len.
+ * h_on_host (0 or 1): H is page-locked host memory.  The call copies it into
+ *   the workspace in groups of 4096 rows on the library's copy stream and the
+ *   map GEMM starts on each group as soon as it has landed (a flag set by a
+ *   stream memory write), so the copy overlaps the fill; later work on
+ *   `stream` is ordered after the copy.  Not with row_idx.
  * k_scale, v_scale (optional, may be NULL): [L, n_kv_heads] f32 device arrays.
  *   When set, every key (value) of head h in layer l is multiplied by
  *   k_scale[l, h] (v_scale[l, h]) before its rounding to bf16: the value or
@@ -138,6 +143,8 @@ typedef struct rf_fill_args {
   const void* A_scale;
   const int32_t* row_idx;
   int64_t h_rows;
+  int32_t h_on_host;
+  int32_t reserved0;
 } rf_fill_args;
 
 /* Bytes of device workspace ridgefill_fill needs for these arguments

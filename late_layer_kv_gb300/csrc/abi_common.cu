@@ -98,6 +98,20 @@ bool make_tmap_3d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, 
   return r == CUDA_SUCCESS;
 }
 
+StreamWrite32 stream_write32() {
+  static StreamWrite32 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuStreamWriteValue32", &p, 11070, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<StreamWrite32>(p);
+  });
+  return fn;
+}
+
 HostStreamer* host_streamer() {
   static HostStreamer hs[kMaxDevices];
   static std::mutex mu;
@@ -115,6 +129,7 @@ HostStreamer* host_streamer() {
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.freed[i], cudaEventDisableTiming);
     }
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.h_done, cudaEventDisableTiming);
     if (e != cudaSuccess) {
       cuda_fail(e, "creating the map-copy stream");
       h.copy = nullptr;
@@ -168,6 +183,10 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   p.d_out = m.d_out;
   p.layer_base = single ? m.slot_layer : 0;
   p.ss_tiles = m.d_out / m.bn;
+  p.h_ready = m.h_ready;
+  p.h_gen = m.h_gen;
+  p.h_group_rows = kHostRowGroup;
+  p.h_row_base = static_cast<int32_t>(m.h_row_base);
   p.bias = m.bias;
   p.gain = static_cast<const __nv_bfloat16*>(m.gain);
   p.ss_part = m.ss;
@@ -273,7 +292,7 @@ extern "C" double ridgefill_compute_share(int32_t split, int32_t n_layers, int64
   return (S * (N - T) + L * T) / (L * N);
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 5; }
+extern "C" int32_t ridgefill_abi_version(void) { return 6; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {

@@ -41,7 +41,19 @@ struct HostStreamer {
   cudaEvent_t copied[kMapSlots] = {};
   cudaEvent_t freed[kMapSlots] = {};
   cudaEvent_t start = nullptr;
+  cudaEvent_t h_done = nullptr;  // split state copied from host memory
+  uint32_t h_gen = 0;            // value that marks this call's row groups ready
 };
+
+// Stream write of a 32-bit value by the GPU's front end, no SM involved: marks a
+// host-to-device copy done for a kernel that is already running.  nullptr if the
+// driver does not offer it.
+using StreamWrite32 = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
+StreamWrite32 stream_write32();
+
+// Rows of split state per ready flag when H streams from host memory (a multiple
+// of the pair GEMM's 256-row tiles; one raster group of the map GEMM).
+constexpr int kHostRowGroup = 4096;
 HostStreamer* host_streamer();  // nullptr on failure (error recorded)
 
 // The map GEMM over `rows` split-state rows starting at H (grouped over all
@@ -56,6 +68,9 @@ struct MapLaunch {
   int32_t slot_layer;
   int32_t bn;
   int64_t R;  // allocated rows of X_hat / partial buffers
+  const uint32_t* h_ready;  // split state streamed from host memory: ready flags, or null
+  uint32_t h_gen;
+  int64_t h_row_base;       // row of H's first row in the flags' numbering
   const float* bias;
   const void* gain;
   void* xhat;

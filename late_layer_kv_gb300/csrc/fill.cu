@@ -18,7 +18,8 @@ namespace {
 struct FillPlan {
   int bn_map = 0, bn_kv = 0;
   int64_t R = 0;  // rows per chunk
-  size_t off_xhat = 0, off_ss = 0, off_slots = 0, off_gather = 0, total = 0;
+  size_t off_xhat = 0, off_ss = 0, off_slots = 0, off_gather = 0, off_hdev = 0, off_hflags = 0,
+         total = 0;
 };
 
 rf_status validate_fill(const rf_fill_args* a) {
@@ -50,6 +51,9 @@ rf_status validate_fill(const rf_fill_args* a) {
   if (a->maps_on_host != 0 && a->maps_on_host != 1) return fail(RF_ERR_ARG, "maps_on_host must be 0 or 1");
   if (a->A_scale != nullptr && a->d_in % kQ8Group != 0)
     return fail(RF_ERR_SHAPE, "int8 maps need d_in to be a multiple of 128");
+  if (a->h_on_host != 0 && a->h_on_host != 1) return fail(RF_ERR_ARG, "h_on_host must be 0 or 1");
+  if (a->h_on_host && a->row_idx != nullptr)
+    return fail(RF_ERR_ARG, "h_on_host cannot be combined with row_idx");
   return RF_OK;
 }
 
@@ -67,7 +71,11 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
       a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0;
   pl->off_gather = align_up(pl->off_slots + slots, 256);
   const size_t gather = a->row_idx != nullptr ? static_cast<size_t>(pl->R) * a->d_in * 2 : 0;
-  pl->total = align_up(pl->off_gather + gather, 256);
+  pl->off_hdev = align_up(pl->off_gather + gather, 256);
+  const size_t rows = a->h_on_host ? static_cast<size_t>(a->rows) : 0;
+  pl->off_hflags = align_up(pl->off_hdev + rows * a->d_in * 2, 256);
+  const size_t groups = a->h_on_host ? ceil_div(a->rows, kHostRowGroup) : 0;
+  pl->total = align_up(pl->off_hflags + groups * 4, 256);
 }
 
 // K/V GEMM on CTA pairs (true) or single CTAs
@@ -197,6 +205,7 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     if ((st = check_pinned(a->A, "A")) != RF_OK) return st;
     if (a->A_scale != nullptr && (st = check_pinned(a->A_scale, "A_scale")) != RF_OK) return st;
   }
+  if (a->h_on_host && (st = check_pinned(a->H, "H")) != RF_OK) return st;
   FillPlan pl;
   plan_fill(a, &pl);
   if (workspace == nullptr || ws_bytes < pl.total)
@@ -209,10 +218,47 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
 
   HostStreamer* hs = nullptr;
   std::unique_lock<std::mutex> lk(g_host_map_mu, std::defer_lock);
-  if (a->maps_on_host) {
+  if (a->maps_on_host || a->h_on_host) {
     lk.lock();
     hs = host_streamer();
     if (hs == nullptr) return RF_ERR_CUDA;
+  }
+  // split state in host memory: copied in row groups on the copy stream; each group's
+  // flag is set by a stream write once its rows have landed, and the map GEMM's
+  // producers wait on the flags, so the copy overlaps the GEMM.  Without stream
+  // writes the map GEMM waits for the whole copy.
+  const uint8_t* h_base = static_cast<const uint8_t*>(a->H);
+  uint32_t* h_flags = nullptr;
+  uint32_t h_gen = 0;
+  bool h_overlap = false;
+  if (a->h_on_host) {
+    h_flags = reinterpret_cast<uint32_t*>(ws + pl.off_hflags);
+    h_gen = ++hs->h_gen == 0 ? ++hs->h_gen : hs->h_gen;
+    const int64_t groups = ceil_div(a->rows, kHostRowGroup);
+    StreamWrite32 wr = stream_write32();
+    h_overlap = wr != nullptr;
+    for (int64_t g = 0; g < groups && h_overlap; ++g)  // clear the flags, in order on `s`
+      h_overlap = wr(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(h_flags + g), 0,
+                     0) == CUDA_SUCCESS;
+    cudaError_t e = cudaEventRecord(hs->start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->copy, hs->start, 0);
+    for (int64_t g = 0; g < groups && e == cudaSuccess; ++g) {
+      const int64_t r0 = g * kHostRowGroup;
+      const int64_t nr = a->rows - r0 < kHostRowGroup ? a->rows - r0 : kHostRowGroup;
+      const size_t off = static_cast<size_t>(r0) * a->d_in * 2;
+      e = cudaMemcpyAsync(ws + pl.off_hdev + off, h_base + off, static_cast<size_t>(nr) * a->d_in * 2,
+                          cudaMemcpyHostToDevice, hs->copy);
+      if (e == cudaSuccess && h_overlap &&
+          wr(reinterpret_cast<CUstream>(hs->copy), reinterpret_cast<CUdeviceptr>(h_flags + g), h_gen,
+             0) != CUDA_SUCCESS)
+        e = cudaErrorUnknown;
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(hs->h_done, hs->copy);
+    if (e == cudaSuccess && !h_overlap) e = cudaStreamWaitEvent(s, hs->h_done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "streaming the split state from host memory");
+    h_base = ws + pl.off_hdev;
+  }
+  if (a->maps_on_host) {
     // the copy stream starts after work already queued on `s` (earlier users of the slots)
     cudaError_t e = cudaEventRecord(hs->start, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->copy, hs->start, 0);
@@ -229,7 +275,12 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     if ((st = mark(start, 0)) != RF_OK) return st;
     const int64_t rc = (a->rows - start < pl.R) ? a->rows - start : pl.R;
     MapLaunch m{};
-    m.H = static_cast<const uint8_t*>(a->H) + static_cast<size_t>(start) * a->d_in * 2;
+    m.H = h_base + static_cast<size_t>(start) * a->d_in * 2;
+    if (h_overlap) {
+      m.h_ready = h_flags;
+      m.h_gen = h_gen;
+      m.h_row_base = start;
+    }
     if (a->row_idx != nullptr) {  // the chunk's listed rows, gathered
       void* hc = ws + pl.off_gather;
       gather_rows_kernel<<<static_cast<unsigned>((rc * 32 + 255) / 256), 256, 0, s>>>(
@@ -282,6 +333,10 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     st = launch_kv(a, pl, start, rc, xhat, ss, s);
     if (st != RF_OK) return st;
     if ((st = mark(start, 2)) != RF_OK) return st;
+  }
+  if (a->h_on_host) {  // later work on `s` (and the caller's reuse of H) follows the copy
+    cudaError_t e = cudaStreamWaitEvent(s, hs->h_done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "ordering after the split-state copy");
   }
   return RF_OK;
 }

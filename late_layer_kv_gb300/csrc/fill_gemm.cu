@@ -805,11 +805,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       int issued[kS];
       for (int s = 0; s < kS; ++s) issued[s] = -1;
       bool ok = true;
+      int h_seen = -1;  // last split-state row group known to be in device memory
       for (int t = pair; t < total && ok; t += npairs) {
         int mp, n, b;
         decode_pair(t, p, mp, n, b);
         const int m = 2 * mp + static_cast<int>(rank);
         const TileB tb = tile_b(p, n);
+        if (p.h_ready != nullptr && m * kBM < p.rows) {
+          const int g = (p.h_row_base + m * kBM) / p.h_group_rows;
+          if (g != h_seen) {
+            if (!flag_wait(p.h_ready + g, p.h_gen, abort_flag, p.err, kErrHostRows)) break;
+            fence_acq_rel_gpu();
+            h_seen = g;
+          }
+        }
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrProducer)) {
             ok = false;

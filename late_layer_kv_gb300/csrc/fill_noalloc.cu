@@ -63,6 +63,8 @@ extern "C" rf_status ridgefill_fill_noalloc(const rf_fill_args* a, void* stream)
   if (a == nullptr) return fail(RF_ERR_ARG, "args is NULL");
   if (a->maps_on_host != 0)
     return fail(RF_ERR_ARG, "ridgefill_fill_noalloc does not stream host maps (maps_on_host = 1)");
+  if (a->h_on_host != 0)
+    return fail(RF_ERR_ARG, "ridgefill_fill_noalloc does not stream a host split state (h_on_host = 1)");
   rf_fill_args c = *a;
   // largest chunk (multiple of 128 rows) whose workspace fits the static scratch
   const int64_t want = a->rows_per_chunk > 0 ? a->rows_per_chunk

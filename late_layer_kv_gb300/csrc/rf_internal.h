@@ -38,6 +38,7 @@ enum ErrSite : int {
   kErrGdn = 4,
   kErrConvert = 5,   // int8-map converter warps
   kErrIndex = 6,     // a row index list entry was out of range (the row was skipped)
+  kErrHostRows = 8,  // a split-state row group copied from host memory never arrived
   kErrNumeric = 7,   // the ridge system was not positive definite (Cholesky pivot <= 0)
 };
 
@@ -63,6 +64,12 @@ struct GemmParams {
   const int8_t* q8;
   const __nv_bfloat16* q8_scale;
   int32_t q8_ld;
+  // split state streamed from host memory (map mode): rows of group g = row / h_group_rows
+  // (row counted from h_row_base) may be read once h_ready[g] == h_gen
+  const uint32_t* h_ready;
+  uint32_t h_gen;
+  int32_t h_group_rows;
+  int32_t h_row_base;
   // map epilogue
   const float* bias;
   const __nv_bfloat16* gain;

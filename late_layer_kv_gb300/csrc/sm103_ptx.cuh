@@ -127,6 +127,28 @@ __device__ __forceinline__ bool mbar_wait_acq_cluster(uint64_t* bar, uint32_t pa
   }
 }
 
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Bounded wait until the 32-bit word *f, written by a stream operation outside the
+// SMs (a copy engine's flag), equals `want`.
+__device__ __forceinline__ bool flag_wait(const uint32_t* f, uint32_t want, volatile int* abort_flag,
+                                          int* err, int site) {
+  if (*reinterpret_cast<const volatile uint32_t*>(f) == want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    __nanosleep(128);
+    if (*reinterpret_cast<const volatile uint32_t*>(f) == want) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(err, 0, site);
+      return false;
+    }
+  }
+}
+
 // Wait for phase `parity` of `bar` until the time limit only (used to drain
 // copies and MMAs still in flight after another role gave up).
 __device__ __forceinline__ bool mbar_drain(uint64_t* bar, uint32_t parity) {

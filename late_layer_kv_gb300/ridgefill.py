@@ -39,7 +39,7 @@ class FillArgs(ctypes.Structure):
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp), ("copy_events", _vp),
         ("k_scale", _vp), ("v_scale", _vp), ("A_scale", _vp), ("row_idx", _vp),
-        ("h_rows", ctypes.c_int64),
+        ("h_rows", ctypes.c_int64), ("h_on_host", ctypes.c_int32), ("reserved0", ctypes.c_int32),
     ]
 
 
@@ -205,7 +205,14 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
         _dev(row_idx, "row_idx", torch.int32, (rows,))
     n_kv = Kc.shape[1]
     cache_len = Kc.shape[2]
-    _dev(H, "H", torch.bfloat16, (H.shape[0], d_in))
+    h_host = not H.is_cuda
+    if h_host:
+        if H.dtype != torch.bfloat16 or not H.is_contiguous() or not H.is_pinned():
+            raise ValueError("host H must be contiguous, pinned bf16")
+        if tuple(H.shape) != (H.shape[0], d_in):
+            raise ValueError("H must be [rows, d_in]")
+    else:
+        _dev(H, "H", torch.bfloat16, (H.shape[0], d_in))
     host = _check_maps(A, A_scale)
     _dev(bias, "bias", torch.float32, (L, d_out))
     if gain is not None:
@@ -226,7 +233,8 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
                  _ptr(bias), _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Kc), _ptr(Vc),
                  ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None,
                  ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None,
-                 _ptr(k_scale), _ptr(v_scale), _ptr(A_scale), _ptr(row_idx), h_rows)
+                 _ptr(k_scale), _ptr(v_scale), _ptr(A_scale), _ptr(row_idx), h_rows,
+                 1 if h_host else 0, 0)
     a._events_keepalive = (ev, cev)
     return a
 
@@ -266,7 +274,8 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     (section 2.2 "Size and cost"; see :func:`ridgefill_quantize_maps`).  ``row_idx``:
     optional int32 [rows] prefix rows to fill (section 2.4): ``H`` then holds every
     prefix row, row ``row_idx[r]`` is filled at position ``pos0 + row_idx[r]`` and the
-    unlisted (exact) rows are left alone.
+    unlisted (exact) rows are left alone.  ``H`` may be a pinned host tensor: it is
+    then copied by the library, overlapped with the map GEMM.
     """
     args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
                      rms_eps=rms_eps, pos0=pos0, rows_per_chunk=rows_per_chunk,
@@ -277,7 +286,7 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     if need == 0:
         _check(lib.ridgefill_fill(ctypes.byref(args), None, 0, _stream(stream)))
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=H.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=Kc.device)
     elif workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace needs {need} bytes")
     _check(lib.ridgefill_fill(ctypes.byref(args), _ptr(workspace),

@@ -169,3 +169,26 @@ def test_full_size_sampled_rows(name):
         compare(gv[l], V[l], f"V layer {l}")
     tail = Kc[:, :, rows:]
     assert bool((tail == SENTINEL).all()) and bool((Vc[:, :, rows:] == SENTINEL).all())
+
+
+def test_host_split_state_bitwise_equal_device():
+    """H in pinned host memory: the library copies it in row groups overlapped with the
+    map GEMM; the caches are bitwise those of a device-resident H (several 4096-row
+    groups, chunked rows, and host maps as well)."""
+    shape = FillShape("hostH", d=512, n_layers=3, n_kv=4, head_dim=128, rope_theta=5e5,
+                      rms_eps=1e-6, N=9000 + 100, T=100)
+    inp = fill_inputs(shape, seed=12)
+    d = to_cuda(inp)
+    H_host = inp["H"].pin_memory()
+    out = []
+    for H, A, rpc in ((d["H"], d["A"], 0), (H_host, d["A"], 0), (H_host, d["A"], 4096),
+                      (H_host, inp["A"].pin_memory(), 0)):
+        Kc, Vc = new_cache(shape.n_layers, shape.n_kv, shape.N, shape.head_dim)
+        ridgefill_fill(H, A, d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc, head_dim=shape.head_dim,
+                       rope_theta=shape.rope_theta, rms_eps=shape.rms_eps, rows_per_chunk=rpc)
+        out.append((Kc, Vc))
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    K0, V0 = out[0]
+    for K, V in out[1:]:
+        assert torch.equal(K, K0) and torch.equal(V, V0)
