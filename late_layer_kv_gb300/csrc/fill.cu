@@ -19,7 +19,7 @@ struct FillPlan {
   int bn_map = 0, bn_kv = 0;
   int64_t R = 0;  // rows per chunk
   size_t off_xhat = 0, off_ss = 0, off_slots = 0, off_gather = 0, off_hdev = 0, off_hflags = 0,
-         total = 0;
+         off_rope = 0, total = 0;
 };
 
 rf_status validate_fill(const rf_fill_args* a) {
@@ -75,11 +75,43 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   const size_t rows = a->h_on_host ? static_cast<size_t>(a->rows) : 0;
   pl->off_hflags = align_up(pl->off_hdev + rows * a->d_in * 2, 256);
   const size_t groups = a->h_on_host ? ceil_div(a->rows, kHostRowGroup) : 0;
-  pl->total = align_up(pl->off_hflags + groups * 4, 256);
+  pl->off_rope = align_up(pl->off_hflags + groups * 4, 256);
+  const size_t rope = static_cast<size_t>(a->head_dim / 2) * pl->R * 8;  // (cos, sin) f32 pairs
+  pl->total = align_up(pl->off_rope + rope, 256);
 }
 
 // K/V GEMM on CTA pairs (true) or single CTAs
 constexpr bool kKvPairs = true;
+
+// RoPE angles of one row chunk (rotate-half pairs, frequency f_i = theta^(-2i/hd)):
+// tab[i * ld + r] = (cos, sin) of (pos0 + position of row r) * f_i.  The angle is
+// formed and reduced modulo 2 pi in f64, then its cos and sin taken in f32.
+struct RopeFreqs {
+  double f[64];
+};
+
+__global__ void rope_table_kernel(float2* tab, int64_t ld, int half, int64_t rc, int64_t pos0,
+                                  int64_t start, const int32_t* row_idx, int64_t h_rows,
+                                  const __grid_constant__ RopeFreqs fr) {
+  const int64_t n = static_cast<int64_t>(half) * rc;
+  for (int64_t k = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; k < n;
+       k += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int i = static_cast<int>(k / rc);
+    const int64_t r = k - i * rc;
+    int64_t pos = start + r;
+    if (row_idx != nullptr) {
+      const int64_t idx = row_idx[start + r];
+      pos = idx >= 0 && idx < h_rows ? idx : 0;  // out-of-range rows are skipped anyway
+    }
+    constexpr double kTwoPiD = 6.283185307179586476925286766559;
+    const double ang = static_cast<double>(pos0 + pos) * fr.f[i];
+    const double q = rint(ang * (1.0 / kTwoPiD));
+    const double red = fma(-q, kTwoPiD, ang);  // |red| <= pi, error ~ q * 2.4e-16
+    float s, c;
+    sincosf(static_cast<float>(red), &s, &c);
+    tab[i * ld + r] = make_float2(c, s);
+  }
+}
 
 // Exact prefix rows (section 2.4): the split states of the listed rows
 // idx[0 .. rc) gathered into a dense [rc, d_in] block for the map GEMM; one
@@ -99,7 +131,8 @@ __global__ void gather_rows_kernel(const __nv_bfloat16* H, const int32_t* idx, i
 
 // `only`: 0 = keys and values, RF_RESCALE_KEYS / RF_RESCALE_VALUES = that half alone
 rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, int64_t rc,
-                    const void* xhat, const float* ss, cudaStream_t s, int only = 0) {
+                    const void* xhat, const float* ss, cudaStream_t s, int only = 0,
+                    const float2* rope_tab = nullptr) {
   GemmParams p{};
   p.mode = kModeKV;
   p.k_blocks = a->d_out / kBK;
@@ -140,6 +173,8 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   p.eps = static_cast<float>(a->rms_eps);
   p.k_scale = a->k_scale;
   p.v_scale = a->v_scale;
+  p.rope_tab = rope_tab;
+  p.rope_ld = pl.R;
   if (a->row_idx != nullptr) {
     p.kv_rows = a->row_idx + start;
     p.kv_pos0 = static_cast<int32_t>(a->pos0);
@@ -330,7 +365,19 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
       }
     }
     if ((st = mark(start, 1)) != RF_OK) return st;
-    st = launch_kv(a, pl, start, rc, xhat, ss, s);
+    // the chunk's RoPE angles, then the K/V GEMM
+    float2* tab = reinterpret_cast<float2*>(ws + pl.off_rope);
+    {
+      RopeFreqs fr{};
+      for (int i = 0; i < a->head_dim / 2; ++i) fr.f[i] = std::pow(a->rope_theta, -2.0 * i / a->head_dim);
+      const int64_t n = static_cast<int64_t>(a->head_dim / 2) * rc;
+      const int64_t blocks = (n + 255) / 256 < 4 * sm_count() ? (n + 255) / 256 : 4 * sm_count();
+      rope_table_kernel<<<static_cast<unsigned>(blocks > 0 ? blocks : 1), 256, 0, s>>>(
+          tab, pl.R, a->head_dim / 2, rc, a->pos0, start, a->row_idx, a->h_rows, fr);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "RoPE table launch");
+    }
+    st = launch_kv(a, pl, start, rc, xhat, ss, s, 0, tab);
     if (st != RF_OK) return st;
     if ((st = mark(start, 2)) != RF_OK) return st;
   }

@@ -224,8 +224,14 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
 #pragma unroll
         for (int j = 0; j < 32; j += 2) {
           float c0, s0, c1, s1;
-          rope_cs(posf, p.inv_freq_hi[i0 + j], p.inv_freq_lo[i0 + j], c0, s0);
-          rope_cs(posf, p.inv_freq_hi[i0 + j + 1], p.inv_freq_lo[i0 + j + 1], c1, s1);
+          if (p.rope_tab != nullptr) {  // frequency-major: a warp reads 32 consecutive rows
+            const float2 t0 = p.rope_tab[(i0 + j) * p.rope_ld + row];
+            const float2 t1 = p.rope_tab[(i0 + j + 1) * p.rope_ld + row];
+            c0 = t0.x; s0 = t0.y; c1 = t1.x; s1 = t1.y;
+          } else {
+            rope_cs(posf, p.inv_freq_hi[i0 + j], p.inv_freq_lo[i0 + j], c0, s0);
+            rope_cs(posf, p.inv_freq_hi[i0 + j + 1], p.inv_freq_lo[i0 + j + 1], c1, s1);
+          }
           const float xa = f32(a[j]) * rh, ya = f32(b[j]) * rh;
           const float xb = f32(a[j + 1]) * rh, yb = f32(b[j + 1]) * rh;
           w1[j / 2] = pack_bf16(xa * c0 - ya * s0, xb * c1 - yb * s1);

@@ -89,6 +89,10 @@ struct GemmParams {
   const int32_t* kv_rows;
   int32_t kv_pos0;
   int32_t kv_hrows;
+  // RoPE angles of this launch's rows: rope_tab[i * rope_ld + row] = (cos, sin) of
+  // frequency i at the row's position; null: computed in the epilogue
+  const float2* rope_tab;
+  int64_t rope_ld;
   __nv_bfloat16* kv_cache[2];  // K, V caches [L, n_kv, cache_len, head_dim]
   int64_t cache_len;
   // GDN projection epilogue

@@ -76,7 +76,8 @@ def test_workspace_size_formula(lib):
     ws = lib.ridgefill_fill_workspace_size(ctypes.byref(a))
     xhat = 20 * 14336 * 4096 * 2
     ss = 20 * (4096 // 256) * 14336 * 4
-    assert xhat + ss <= ws <= xhat + ss + 1024
+    rope = 64 * 14336 * 8  # (cos, sin) f32 pairs of the chunk's positions
+    assert xhat + ss + rope <= ws <= xhat + ss + rope + 1024
 
 
 def test_generic_workspace_size_matches_each_call(lib):
