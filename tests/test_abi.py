@@ -102,3 +102,56 @@ def test_generic_workspace_size_matches_each_call(lib):
     assert lib.ridgefill_workspace_size(7, ctypes.cast(ctypes.byref(fa), ctypes.c_void_p)) == 0
     assert b"unknown call" in lib.ridgefill_last_error()
     assert lib.ridgefill_workspace_size(0, None) == 0
+
+
+def _fill_ok(rb):
+    a = rb.FillArgs()
+    a.n_layers, a.d_in, a.d_out, a.n_kv_heads, a.head_dim = 2, 256, 256, 2, 64
+    a.rows, a.cache_len, a.rope_theta, a.rms_eps = 100, 128, 1e4, 1e-6
+    return a
+
+
+def test_new_argument_checks_fail_without_a_gpu(lib):
+    """Argument errors of the exact-row, int8, host split-state, quantizer, rescale and
+    GDN options are reported before anything is enqueued (no device needed)."""
+    from late_layer_kv_gb300 import ridgefill as rb
+    RF_ERR_ARG, RF_ERR_SHAPE = 1, 2
+    a = _fill_ok(rb)
+    assert lib.ridgefill_fill_workspace_size(ctypes.byref(a)) > 0
+    idx = (ctypes.c_int32 * 4)(0, 1, 2, 3)
+    a.row_idx = ctypes.cast(idx, ctypes.c_void_p)
+    a.h_rows = 50  # fewer prefix rows than rows to fill
+    assert lib.ridgefill_fill(ctypes.byref(a), None, 0, None) == RF_ERR_SHAPE
+    a.h_rows, a.cache_len = 200, 128  # positions past the cache
+    assert lib.ridgefill_fill(ctypes.byref(a), None, 0, None) == RF_ERR_SHAPE
+    a.cache_len, a.h_on_host = 256, 1  # host split state with a row list
+    assert lib.ridgefill_fill(ctypes.byref(a), None, 0, None) == RF_ERR_ARG
+    a = _fill_ok(rb)
+    a.h_on_host = 2
+    assert lib.ridgefill_fill(ctypes.byref(a), None, 0, None) == RF_ERR_ARG
+    a = _fill_ok(rb)
+    a.d_in, a.A_scale = 192, 16  # int8 maps need d_in % 128 == 0
+    assert lib.ridgefill_fill(ctypes.byref(a), None, 0, None) == RF_ERR_SHAPE
+
+    q = rb.QuantizeArgs(1, 256, 192, 0, None, None, None)  # d_in not a multiple of 128
+    assert lib.ridgefill_quantize_maps(ctypes.byref(q), None) == RF_ERR_SHAPE
+    q = rb.QuantizeArgs(1, 256, 256, 0, None, None, None)
+    assert lib.ridgefill_quantize_maps(ctypes.byref(q), None) == RF_ERR_ARG
+    q = rb.QuantizeArgs(1, 256, 256, 3, 16, 16, 16)
+    assert lib.ridgefill_quantize_maps(ctypes.byref(q), None) == RF_ERR_ARG
+
+    r = rb.RescaleArgs()
+    r.n_layers, r.d_in, r.d_out, r.n_kv_heads, r.head_dim = 2, 256, 256, 2, 64
+    r.which, r.tail_rows, r.rows, r.cache_len, r.rms_eps = 3, 10, 0, 128, 1e-6
+    assert lib.ridgefill_rescale(ctypes.byref(r), None, 0, None) == RF_ERR_ARG  # bad `which`
+    r.which, r.tail_rows = 1, 0
+    assert lib.ridgefill_rescale(ctypes.byref(r), None, 0, None) == RF_ERR_ARG  # no tail rows
+
+    g = rb.GdnArgs()
+    g.n_layers, g.d_in, g.d_out, g.n_heads, g.d_k, g.d_v, g.chunk = 1, 256, 256, 8, 128, 128, 64
+    g.rows, g.rms_eps, g.l2_eps = 100, 1e-6, 1e-6
+    g.S = 16
+    g.n_exact = 101  # more exact rows than rows
+    assert lib.ridgefill_fill_gdn(ctypes.byref(g), None, 0, None) == RF_ERR_ARG
+    g.n_exact = 5  # exact rows without their indices and inputs
+    assert lib.ridgefill_fill_gdn(ctypes.byref(g), None, 0, None) == RF_ERR_ARG
