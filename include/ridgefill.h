@@ -446,6 +446,15 @@ rf_status ridgefill_device_error(void* stream, int* code);
  * r = (S (N - T) + L T) / (L N); the speedup is at most 1/r. */
 double ridgefill_compute_share(int32_t split, int32_t n_layers, int64_t tail, int64_t prompt);
 
+/* Failure-detection self-check.  Launches one small kernel whose bounded device
+ * wait, the same helper the fill kernels use, runs out: which = 0 waits on an
+ * mbarrier that nothing arrives at, which = 1 on a device flag that nothing
+ * sets.  After about two seconds the wait records code 20 + which in the
+ * device error word and the kernel returns; ridgefill_device_error() then
+ * reports RF_ERR_TIMEOUT with that code, and the context stays usable.  For
+ * tests of the error path.  Asynchronous on `stream`. */
+rf_status ridgefill_wait_selftest(int32_t which, void* stream);
+
 /* ABI version (incremented on any change to the structs above). */
 int32_t ridgefill_abi_version(void);
 

@@ -21,4 +21,5 @@ from .ridgefill import (  # noqa: F401
     RF_RESCALE_KEYS,
     RF_RESCALE_VALUES,
     ridgefill_workspace_size,
+    wait_selftest,
 )

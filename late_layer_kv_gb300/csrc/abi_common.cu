@@ -6,6 +6,7 @@
 #include <string>
 
 #include "abi_common.h"
+#include "sm103_ptx.cuh"
 
 namespace rf {
 
@@ -13,6 +14,7 @@ namespace {
 thread_local std::string g_last_error;
 constexpr int kMaxDevices = 64;
 __device__ int g_device_error = 0;
+__device__ uint32_t g_probe_flag = 0;  // never written: the flag ridgefill_wait_selftest waits on
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -292,7 +294,43 @@ extern "C" double ridgefill_compute_share(int32_t split, int32_t n_layers, int64
   return (S * (N - T) + L * T) / (L * N);
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 6; }
+namespace rf {
+namespace {
+// One warp; lane 0 waits, with the kernels' own bounded helpers, on an mbarrier that
+// nothing arrives at (which = 0) or a device word that nothing sets (which = 1).
+__global__ void wait_probe_kernel(int which, const uint32_t* word, int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (which == 0) mbar_wait(&bar, 0, &abort_flag, err, kErrProbe);
+    else flag_wait(word, 1u, &abort_flag, err, kErrProbe + 1);
+  }
+}
+}  // namespace
+}  // namespace rf
+
+extern "C" rf_status ridgefill_wait_selftest(int32_t which, void* stream) {
+  using namespace rf;
+  if (which != 0 && which != 1) return fail(RF_ERR_ARG, "which must be 0 or 1");
+  int* err = device_error_word();
+  if (err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
+  void* flag = nullptr;
+  if (cudaGetSymbolAddress(&flag, g_probe_flag) != cudaSuccess)
+    return fail(RF_ERR_CUDA, "probe flag unavailable");
+  wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      which, static_cast<const uint32_t*>(flag), err);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test launch");
+  return RF_OK;
+}
+
+extern "C" int32_t ridgefill_abi_version(void) { return 7; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {

@@ -39,6 +39,7 @@ enum ErrSite : int {
   kErrConvert = 5,   // int8-map converter warps
   kErrIndex = 6,     // a row index list entry was out of range (the row was skipped)
   kErrHostRows = 8,  // a split-state row group copied from host memory never arrived
+  kErrProbe = 20,    // ridgefill_wait_selftest: + 0 mbarrier wait, + 1 flag wait
   kErrNumeric = 7,   // the ridge system was not positive definite (Cholesky pivot <= 0)
 };
 

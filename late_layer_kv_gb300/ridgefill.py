@@ -125,6 +125,8 @@ def load(rebuild: bool = True) -> ctypes.CDLL:
     lib.ridgefill_rescale.restype = ctypes.c_int
     lib.ridgefill_quantize_maps.argtypes = [ctypes.POINTER(QuantizeArgs), _vp]
     lib.ridgefill_quantize_maps.restype = ctypes.c_int
+    lib.ridgefill_wait_selftest.argtypes = [ctypes.c_int32, _vp]
+    lib.ridgefill_wait_selftest.restype = ctypes.c_int
     lib.ridgefill_workspace_size.argtypes = [ctypes.c_int32, _vp]
     lib.ridgefill_workspace_size.restype = ctypes.c_size_t
     lib.ridgefill_status_string.argtypes = [ctypes.c_int]
@@ -488,6 +490,12 @@ def device_error(stream=None) -> int:
     code = ctypes.c_int(0)
     load().ridgefill_device_error(_stream(stream), ctypes.byref(code))
     return int(code.value)
+
+
+def wait_selftest(which: int, stream=None) -> None:
+    """Enqueue a kernel whose bounded device wait runs out (0: mbarrier, 1: flag); read
+    the outcome with :func:`device_error` (code 20 + which)."""
+    _check(load().ridgefill_wait_selftest(int(which), _stream(stream)))
 
 
 def compute_share(split: int, n_layers: int, tail: int, prompt: int) -> float:
