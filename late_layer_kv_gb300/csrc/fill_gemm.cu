@@ -707,24 +707,30 @@ __device__ __forceinline__ void q8_dequant16(uint4 v, float sc, float c, uint32_
   }
 }
 
-// Converter thread (crow, cch): rows crow + 32 i of the half tile, the 16 codes of
-// column chunk cch; writes them as bf16 in the layout a 128-byte-swizzled TMA box
-// {64, rows} gives (row r at r * 128 bytes, 16-byte chunk c at c ^ (r % 8)).
+// Converter thread (crow, cch): rows crow + 32 i (i < NR) of the half tile, the 16 codes
+// of column chunk cch; writes them as bf16 in the layout a 128-byte-swizzled TMA box
+// {64, rows} gives (row r at r * 128 bytes, 16-byte chunk c at c ^ (r % 8)).  All
+// shared-memory loads are issued before any conversion so their latencies overlap.
+template <int NR>
 __device__ __forceinline__ void q8_convert(const uint8_t* raw, const uint8_t* rsc, uint8_t* sb,
-                                           int crow, int cch, int nr) {
+                                           int crow, int cch) {
+  uint4 v[NR];
+  float sc[NR];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    if (i < nr) {
-      const int row = crow + 32 * i;
-      const uint4 v = *reinterpret_cast<const uint4*>(raw + row * kBK + cch * 16);
-      const float sc = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rsc + row * 2)) << 16);
-      uint32_t w[8];
-      q8_dequant16(v, sc, -32896.f * sc, w);
-      uint8_t* rp = sb + row * 128;
-      *reinterpret_cast<uint4*>(rp + (((2 * cch) ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
-      *reinterpret_cast<uint4*>(rp + (((2 * cch + 1) ^ (row & 7)) * 16)) =
-          make_uint4(w[4], w[5], w[6], w[7]);
-    }
+  for (int i = 0; i < NR; ++i) {
+    const int row = crow + 32 * i;
+    v[i] = *reinterpret_cast<const uint4*>(raw + row * kBK + cch * 16);
+    sc[i] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rsc + row * 2)) << 16);
+  }
+#pragma unroll
+  for (int i = 0; i < NR; ++i) {
+    const int row = crow + 32 * i;
+    uint32_t w[8];
+    q8_dequant16(v[i], sc[i], -32896.f * sc[i], w);
+    uint8_t* rp = sb + row * 128;
+    *reinterpret_cast<uint4*>(rp + (((2 * cch) ^ (row & 7)) * 16)) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4*>(rp + (((2 * cch + 1) ^ (row & 7)) * 16)) =
+        make_uint4(w[4], w[5], w[6], w[7]);
   }
 }
 
@@ -1010,8 +1016,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       if (!mbar_wait(&raw_full[rs], rphase, abort_flag, p.err, kErrConvert) ||
           !mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrConvert))
         break;
-      q8_convert(sRaw + rs * kRawBytes, sRawScale + rs * kRawScaleBytes,
-                 sB + stage * kHalfBytes, crow, cch, nr);
+      if (nr == 4)
+        q8_convert<4>(sRaw + rs * kRawBytes, sRawScale + rs * kRawScaleBytes,
+                      sB + stage * kHalfBytes, crow, cch);
+      else
+        q8_convert<2>(sRaw + rs * kRawBytes, sRawScale + rs * kRawScaleBytes,
+                      sB + stage * kHalfBytes, crow, cch);
       fence_async_smem();
       __syncwarp();
       if (lane == 0) {
