@@ -122,6 +122,8 @@ __device__ __forceinline__ void map_half(const uint32_t (&r)[32], const float* b
   }
 }
 
+// kBoxes: staging boxes per warp (2: double-buffered stores; 1 frees shared memory)
+template <int kBoxes = 2>
 __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
                              int m, int n, uint32_t tempty) {
   const int gcol = n * p.bn;
@@ -147,8 +149,8 @@ __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
     uint32_t w0[16], w1[16];
     map_half(r0, bp, gp, ss, w0);
     map_half(r1, bp + 32, gp != nullptr ? gp + 32 : nullptr, ss, w1);
-    uint8_t* box = stg + (c & 1) * kOutBoxBytes;
-    if (lane == 0) bulk_wait_read<1>();
+    uint8_t* box = stg + (c % kBoxes) * kOutBoxBytes;
+    if (lane == 0) bulk_wait_read<kBoxes - 1>();
     __syncwarp();
     stage32(box, lane, 0, w0);
     stage32(box, lane, 32, w1);
@@ -675,14 +677,15 @@ __device__ __forceinline__ void decode_pair(int t, const GemmParams& p, int& mp,
 constexpr int kRawBytes = 128 * kBK;      // int8 codes of a half tile
 constexpr int kRawScaleBytes = 128 * 2;   // bf16 scales of its rows
 constexpr int kStagesQ8 = 4;              // bf16 MMA stages with int8 maps
-constexpr int kRawStages = 7;
+constexpr int kRawStages = 9;
+constexpr int kOutBoxesQ8 = 1;            // one store box per epilogue warp (map mode)
 constexpr int kConvGroups = 2;            // converter warp groups taking alternate stages
 // scale ring padded so the epilogue's 128-byte-swizzled staging stays 1024-byte aligned
 constexpr int kRawScaleRegion = (kRawStages * kRawScaleBytes + 1023) / 1024 * 1024;
 static_assert(1024 + kStages2 * 2 * kHalfBytes + 4 * kOutWarpBytes + 8 * (2 * kStages2 + 5) + 8 <=
                   kGemmSmem, "pair GEMM shared memory");
 static_assert(1024 + kStagesQ8 * 2 * kHalfBytes + kRawStages * kRawBytes + kRawScaleRegion +
-                      4 * kOutWarpBytes + 8 * (2 * kStagesQ8 + 5 + 2 * kRawStages) + 8 <=
+                      4 * kOutBoxesQ8 * kOutBoxBytes + 8 * (2 * kStagesQ8 + 5 + 2 * kRawStages) + 8 <=
                   kGemmSmem, "int8 pair GEMM shared memory");
 
 // bf16(q * s) of 16 codes.  A byte permute turns u = b ^ 0x80 = q + 128 into the
@@ -752,7 +755,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   uint8_t* sRaw = sB + kS * kHalfBytes;                           // kQ8 only
   uint8_t* sRawScale = sRaw + (kQ8 ? kRawStages * kRawBytes : 0);  // kQ8 only
   uint8_t* stg_all = sRawScale + (kQ8 ? kRawScaleRegion : 0);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 4 * kOutWarpBytes);
+  constexpr int kStgWarpBytes = kQ8 ? kOutBoxesQ8 * kOutBoxBytes : kOutWarpBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 4 * kStgWarpBytes);
   uint64_t* full = bars;
   uint64_t* empty = bars + kS;
   uint64_t* tfull = bars + 2 * kS;
@@ -969,7 +973,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   } else if (warp >= 4 && warp < 8) {
     // ---------------- epilogue warpgroup (both CTAs)
     const int q = warp - 4;
-    uint8_t* stg = stg_all + q * kOutWarpBytes;
+    uint8_t* stg = stg_all + q * kStgWarpBytes;
     int it = 0;
     for (int t = pair; t < total; t += npairs, ++it) {
       int mp, n, b;
@@ -987,7 +991,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cl(tempty0 + 8 * acc);
-      } else if (kQ8 || p.mode == kModeMap) {
+      } else if (kQ8) {
+        epilogue_map<kOutBoxesQ8>(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
+      } else if (p.mode == kModeMap) {
         epilogue_map(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
       } else if (p.mode == kModeKV) {
         epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
