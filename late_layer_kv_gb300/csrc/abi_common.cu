@@ -155,12 +155,13 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
                          0, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   // B boxes of bn / 2 rows: each CTA of a pair stages half of a tile's columns
   if (q8) {
-    // codes {d_in, B rows} int8 in boxes {64, bn / 2}; scales [layers, d_in / 128, d_out]
-    // bf16 in boxes {bn / 2} (one 128-weight group of a half tile's rows)
+    // codes {d_in, B rows} int8 in boxes {128, bn / 2} (two k-blocks, one scale group);
+    // scales [layers, d_in / 128, d_out] bf16 in boxes {bn / 2} (one 128-weight group of a
+    // half tile's rows)
     const uint64_t groups = static_cast<uint64_t>(m.d_in / kQ8Group);
     const uint64_t slayers = single ? 1 : static_cast<uint64_t>(m.n_layers);
     ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.A, m.d_in, brows, 1,
-                            static_cast<uint64_t>(m.d_in), 0, kBK, m.bn / 2,
+                            static_cast<uint64_t>(m.d_in), 0, 2 * kBK, m.bn / 2,
                             CU_TENSOR_MAP_SWIZZLE_NONE);
     ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A_scale, m.d_out, groups,
                             slayers, out_row, out_row * groups, m.bn / 2, 1,

@@ -674,10 +674,12 @@ __device__ __forceinline__ void decode_pair(int t, const GemmParams& p, int& mp,
 // and the rows' bf16 scales of the stage's 128-weight group (box {bn / 2}); a
 // producer thread (warp 3) fills it by TMA and the converter warps turn it into
 // the bf16 stage the MMA reads.
-constexpr int kRawBytes = 128 * kBK;      // int8 codes of a half tile
+constexpr int kRawK = 2;                  // k-blocks per raw stage (128-byte code rows)
+constexpr int kRawRow = kRawK * kBK;      // bytes of one row of codes in a raw stage
+constexpr int kRawBytes = 128 * kRawRow;  // int8 codes of a half tile, kRawK k-blocks
 constexpr int kRawScaleBytes = 128 * 2;   // bf16 scales of its rows
 constexpr int kStagesQ8 = 4;              // bf16 MMA stages with int8 maps
-constexpr int kRawStages = 9;
+constexpr int kRawStages = 4;
 constexpr int kOutBoxesQ8 = 1;            // one store box per epilogue warp (map mode)
 constexpr int kConvGroups = 2;            // converter warp groups taking alternate stages
 // scale ring padded so the epilogue's 128-byte-swizzled staging stays 1024-byte aligned
@@ -722,7 +724,7 @@ __device__ __forceinline__ void q8_convert(const uint8_t* raw, const uint8_t* rs
 #pragma unroll
   for (int i = 0; i < NR; ++i) {
     const int row = crow + 32 * i;
-    v[i] = *reinterpret_cast<const uint4*>(raw + row * kBK + cch * 16);
+    v[i] = *reinterpret_cast<const uint4*>(raw + row * kRawRow + cch * 16);
     sc[i] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rsc + row * 2)) << 16);
   }
 #pragma unroll
@@ -786,7 +788,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
     if (kQ8) {
       for (int s = 0; s < kRawStages; ++s) {
         mbar_init(&raw_full[s], 1);   // this CTA's raw producer (+ its copies' bytes)
-        mbar_init(&raw_empty[s], 4);  // this CTA's converter warps
+        mbar_init(&raw_empty[s], 4 * kRawK);  // four converter warps per k-block of the stage
       }
     }
     *abort_flag = 0;
@@ -950,12 +952,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         const int half = tb.bn / 2;
         const int brow0 = tb.nrow + half * static_cast<int>(rank);
         const int l = brow0 / p.d_out, j0 = brow0 - l * p.d_out;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < p.k_blocks; kb += kRawK) {  // k_blocks is even (d_in % 128 == 0)
           if (!mbar_wait(&raw_empty[rs], rphase ^ 1, abort_flag, p.err, kErrProducer)) {
             ok = false;
             break;
           }
-          mbar_expect_tx(&raw_full[rs], half * (kBK + 2));
+          mbar_expect_tx(&raw_full[rs], half * (kRawRow + 2));
           tma_load_3d(smem_u32(sRaw + rs * kRawBytes), &p.tmB[0], &raw_full[rs], kb * kBK, brow0, 0);
           tma_load_3d(smem_u32(sRawScale + rs * kRawScaleBytes), &p.tmB[1], &raw_full[rs], j0,
                       (kb * kBK) / kQ8Group, l);
@@ -1017,16 +1019,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
     const int jobs = my_tiles * p.k_blocks;
     for (int j = cg; j < jobs; j += kConvGroups) {
       const uint32_t stage = static_cast<uint32_t>(j % kS), phase = static_cast<uint32_t>(j / kS) & 1u;
-      const uint32_t rs = static_cast<uint32_t>(j % kRawStages);
-      const uint32_t rphase = static_cast<uint32_t>(j / kRawStages) & 1u;
+      const int rj = j / kRawK;  // raw stage job: kRawK consecutive k-blocks share one
+      const uint32_t rs = static_cast<uint32_t>(rj % kRawStages);
+      const uint32_t rphase = static_cast<uint32_t>(rj / kRawStages) & 1u;
+      const int sub = (j % kRawK) * kBK;  // byte offset of this k-block inside each code row
       if (!mbar_wait(&raw_full[rs], rphase, abort_flag, p.err, kErrConvert) ||
           !mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrConvert))
         break;
       if (nr == 4)
-        q8_convert<4>(sRaw + rs * kRawBytes, sRawScale + rs * kRawScaleBytes,
+        q8_convert<4>(sRaw + rs * kRawBytes + sub, sRawScale + rs * kRawScaleBytes,
                       sB + stage * kHalfBytes, crow, cch);
       else
-        q8_convert<2>(sRaw + rs * kRawBytes, sRawScale + rs * kRawScaleBytes,
+        q8_convert<2>(sRaw + rs * kRawBytes + sub, sRawScale + rs * kRawScaleBytes,
                       sB + stage * kHalfBytes, crow, cch);
       fence_async_smem();
       __syncwarp();
