@@ -162,7 +162,7 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
     const uint64_t slayers = single ? 1 : static_cast<uint64_t>(m.n_layers);
     ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.A, m.d_in, brows, 1,
                             static_cast<uint64_t>(m.d_in), 0, 2 * kBK, m.bn / 2,
-                            CU_TENSOR_MAP_SWIZZLE_NONE);
+                            CU_TENSOR_MAP_SWIZZLE_128B);
     ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A_scale, m.d_out, groups,
                             slayers, out_row, out_row * groups, m.bn / 2, 1,
                             CU_TENSOR_MAP_SWIZZLE_NONE);

@@ -713,18 +713,20 @@ __device__ __forceinline__ void q8_dequant16(uint4 v, float sc, float c, uint32_
 }
 
 // Converter thread (crow, cch): rows crow + 32 i (i < NR) of the half tile, the 16 codes
-// of column chunk cch; writes them as bf16 in the layout a 128-byte-swizzled TMA box
-// {64, rows} gives (row r at r * 128 bytes, 16-byte chunk c at c ^ (r % 8)).  All
-// shared-memory loads are issued before any conversion so their latencies overlap.
+// of column chunk cch of the k-block at byte `sub` of each 128-byte code row (the raw
+// stage is a 128-byte-swizzled box: chunk c of row r at c ^ (r % 8), so a warp's eight
+// rows spread over all banks); writes them as bf16 in the same swizzled layout of a
+// {64, rows} box.  All shared-memory loads are issued before any conversion.
 template <int NR>
-__device__ __forceinline__ void q8_convert(const uint8_t* raw, const uint8_t* rsc, uint8_t* sb,
-                                           int crow, int cch) {
+__device__ __forceinline__ void q8_convert(const uint8_t* raw, int sub, const uint8_t* rsc,
+                                           uint8_t* sb, int crow, int cch) {
   uint4 v[NR];
   float sc[NR];
 #pragma unroll
   for (int i = 0; i < NR; ++i) {
     const int row = crow + 32 * i;
-    v[i] = *reinterpret_cast<const uint4*>(raw + row * kRawRow + cch * 16);
+    v[i] = *reinterpret_cast<const uint4*>(raw + row * kRawRow +
+                                           (((sub >> 4) + cch) ^ (row & 7)) * 16);
     sc[i] = __uint_as_float(static_cast<uint32_t>(*reinterpret_cast<const uint16_t*>(rsc + row * 2)) << 16);
   }
 #pragma unroll
@@ -1027,10 +1029,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
           !mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrConvert))
         break;
       if (nr == 4)
-        q8_convert<4>(sRaw + rs * kRawBytes + sub, sRawScale + rs * kRawScaleBytes,
+        q8_convert<4>(sRaw + rs * kRawBytes, sub, sRawScale + rs * kRawScaleBytes,
                       sB + stage * kHalfBytes, crow, cch);
       else
-        q8_convert<2>(sRaw + rs * kRawBytes + sub, sRawScale + rs * kRawScaleBytes,
+        q8_convert<2>(sRaw + rs * kRawBytes, sub, sRawScale + rs * kRawScaleBytes,
                       sB + stage * kHalfBytes, crow, cch);
       fence_async_smem();
       __syncwarp();
