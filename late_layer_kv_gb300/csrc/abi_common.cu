@@ -186,6 +186,11 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   p.d_out = m.d_out;
   p.layer_base = single ? m.slot_layer : 0;
   p.ss_tiles = m.d_out / m.bn;
+  if (m.out_rows != nullptr) {
+    p.map_rows = m.out_rows;
+    p.map_out = static_cast<__nv_bfloat16*>(m.xhat);
+    p.map_ld = m.R;
+  }
   p.h_ready = m.h_ready;
   p.h_gen = m.h_gen;
   p.h_group_rows = kHostRowGroup;

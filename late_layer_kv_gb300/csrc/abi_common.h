@@ -68,6 +68,7 @@ struct MapLaunch {
   int32_t slot_layer;
   int32_t bn;
   int64_t R;  // allocated rows of X_hat / partial buffers
+  const int32_t* out_rows;  // X_hat row of each GEMM row (rows left out are not written), or null
   const uint32_t* h_ready;  // split state streamed from host memory: ready flags, or null
   uint32_t h_gen;
   int64_t h_row_base;       // row of H's first row in the flags' numbering
@@ -77,6 +78,11 @@ struct MapLaunch {
   float* ss;
 };
 rf_status launch_map(const MapLaunch& m, cudaStream_t s);
+
+// Gather the split-state rows H[idx[0 .. rc)] ([h_rows, d_in] bf16) into a dense [rc, d_in]
+// block; an index outside [0, h_rows) gives a zero row and a device error code.
+rf_status launch_gather_rows(const void* H, const int32_t* idx, int64_t rc, int64_t h_rows,
+                             int d_in, void* out, cudaStream_t s);
 
 // One layer's map in a device slot: bf16 [d_out, d_in], or (q8) int8 codes
 // followed at a 256-byte boundary by the bf16 scales [d_in / 128, d_out].

@@ -209,6 +209,17 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
 std::mutex g_host_map_mu;
 
 }  // namespace
+
+rf_status launch_gather_rows(const void* H, const int32_t* idx, int64_t rc, int64_t h_rows,
+                             int d_in, void* out, cudaStream_t s) {
+  if (rc <= 0) return RF_OK;
+  gather_rows_kernel<<<static_cast<unsigned>((rc * 32 + 255) / 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(H), idx, rc, h_rows, d_in,
+      static_cast<__nv_bfloat16*>(out), device_error_word());
+  cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? RF_OK : cuda_fail(e, "row gather launch");
+}
+
 }  // namespace rf
 
 using namespace rf;
@@ -318,11 +329,8 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     }
     if (a->row_idx != nullptr) {  // the chunk's listed rows, gathered
       void* hc = ws + pl.off_gather;
-      gather_rows_kernel<<<static_cast<unsigned>((rc * 32 + 255) / 256), 256, 0, s>>>(
-          static_cast<const __nv_bfloat16*>(a->H), a->row_idx + start, rc, a->h_rows, a->d_in,
-          static_cast<__nv_bfloat16*>(hc), device_error_word());
-      cudaError_t e = cudaGetLastError();
-      if (e != cudaSuccess) return cuda_fail(e, "row gather launch");
+      if ((st = launch_gather_rows(a->H, a->row_idx + start, rc, a->h_rows, a->d_in, hc, s)) != RF_OK)
+        return st;
       m.H = hc;
     }
     m.rows = rc;

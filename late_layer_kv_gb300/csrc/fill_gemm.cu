@@ -100,6 +100,14 @@ __device__ __forceinline__ void stage32(uint8_t* box, int lane, int col, const u
 
 __device__ __forceinline__ float f32(uint32_t u) { return __uint_as_float(u); }
 
+// 32 bf16 (16 words) of one row straight to global memory
+__device__ __forceinline__ void store32(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) d[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+
 // ------------------------------------------------------------------ epilogues
 __device__ __forceinline__ void map_half(const uint32_t (&r)[32], const float* bp,
                                          const __nv_bfloat16* gp, float& ss, uint32_t (&w)[16]) {
@@ -122,8 +130,9 @@ __device__ __forceinline__ void map_half(const uint32_t (&r)[32], const float* b
   }
 }
 
-// kBoxes: staging boxes per warp (2: double-buffered stores; 1 frees shared memory)
-template <int kBoxes = 2>
+// kBoxes: staging boxes per warp (2: double-buffered stores; 1 frees shared memory);
+// kDirect: rows listed in p.map_rows, stored one by one (no staging)
+template <int kBoxes = 2, bool kDirect = false>
 __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
                              int m, int n, uint32_t tempty) {
   const int gcol = n * p.bn;
@@ -131,6 +140,9 @@ __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
   const int j0 = gcol % p.d_out;
   const int row = m * kBM + q * 32 + lane;
   const int nch = p.bn / 64;
+  // rows listed by index (exact rows left out of the GEMM) are stored one by one
+  constexpr bool direct = kDirect;
+  const int orow = direct ? (row < p.rows ? p.map_rows[row] : -1) : row;
   float ss = 0.f;
   for (int c = 0; c < nch; ++c) {
     uint32_t r0[32], r1[32];
@@ -149,6 +161,14 @@ __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
     uint32_t w0[16], w1[16];
     map_half(r0, bp, gp, ss, w0);
     map_half(r1, bp + 32, gp != nullptr ? gp + 32 : nullptr, ss, w1);
+    if constexpr (direct) {
+      if (orow >= 0 && orow < p.map_ld) {
+        __nv_bfloat16* dst = p.map_out + (static_cast<int64_t>(l) * p.map_ld + orow) * p.d_out + col;
+        store32(dst, w0);
+        store32(dst + 32, w1);
+      }
+      continue;
+    }
     uint8_t* box = stg + (c % kBoxes) * kOutBoxBytes;
     if (lane == 0) bulk_wait_read<kBoxes - 1>();
     __syncwarp();
@@ -161,8 +181,8 @@ __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
       bulk_commit();
     }
   }
-  if (row < p.rows) {
-    p.ss_part[(static_cast<size_t>(l) * p.ss_tiles + j0 / p.bn) * p.ss_stride + row] = ss;
+  if (row < p.rows && orow >= 0 && (!direct || orow < p.map_ld)) {
+    p.ss_part[(static_cast<size_t>(l) * p.ss_tiles + j0 / p.bn) * p.ss_stride + orow] = ss;
   }
 }
 
@@ -173,13 +193,6 @@ __device__ __forceinline__ float row_rms_scale(const GemmParams& p, int l, int r
     for (int t = 0; t < p.ss_tiles; ++t) ssum += sp[static_cast<size_t>(t) * p.ss_stride];
   }
   return rsqrtf(fmaf(ssum, p.inv_d, p.eps));
-}
-
-// 32 bf16 (16 words) of one row straight to global memory
-__device__ __forceinline__ void store32(__nv_bfloat16* dst, const uint32_t (&w)[16]) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int c = 0; c < 4; ++c) d[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
 __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, int q, int lane,
@@ -998,7 +1011,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       } else if (kQ8) {
         epilogue_map<kOutBoxesQ8>(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
       } else if (p.mode == kModeMap) {
-        epilogue_map(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
+        if (p.map_rows != nullptr) epilogue_map<2, true>(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
+        else epilogue_map(p, tcol, stg, q, lane, m, n, tempty0 + 8 * acc);
       } else if (p.mode == kModeKV) {
         epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
       } else if (p.mode == kModeGram) {

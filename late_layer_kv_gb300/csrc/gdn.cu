@@ -755,6 +755,25 @@ __global__ void exact_input_kernel(const __nv_bfloat16* X, const __nv_bfloat16* 
     ss[(static_cast<size_t>(l) * ss_tiles + j) * R + r] = j == 0 ? acc : 0.f;
 }
 
+// The filled rows: the rows of [0, rows) not in exact_idx (ascending), in order.
+// fill[t - #(exact rows before t)] = t for every filled row t.
+__global__ void complement_kernel(const int32_t* exact_idx, int64_t n_exact, int64_t rows,
+                                  int32_t* fill) {
+  const int64_t n_fill = rows - n_exact;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < rows;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    int64_t lo = 0, hi = n_exact;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi) >> 1;
+      if (exact_idx[mid] < t) lo = mid + 1;
+      else hi = mid;
+    }
+    const bool exact = lo < n_exact && exact_idx[lo] == t;
+    const int64_t k = t - lo;
+    if (!exact && k >= 0 && k < n_fill) fill[k] = static_cast<int32_t>(t);
+  }
+}
+
 // rho of section 2.3 (terminal-state correction), one CTA per (layer, head) and
 // row chunk.  A row's weight in the state at the end of the rows is the product
 // of the gates after it.  Each thread runs over a segment of rows with
@@ -837,7 +856,8 @@ struct GdnPlan {
   int bn_map = 0;
   int64_t R = 0;
   size_t off_xhat = 0, off_ss = 0, off_k = 0, off_v = 0, off_gate = 0, off_slots = 0, off_rho = 0,
-         total = 0;
+         off_fill = 0, off_hc = 0, total = 0;
+  bool compact = false;  // map only the filled rows (exact rows, one row chunk, bf16 maps)
 };
 
 rf_status validate_gdn(const rf_gdn_args* a) {
@@ -879,6 +899,12 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
   pl->off_slots = off;
   off = align_up(off + (a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0), 256);
   pl->off_rho = off;   off = align_up(off + L * H * 2 * sizeof(double), 256);
+  pl->compact = a->n_exact > 0 && pl->R >= a->rows && a->A_scale == nullptr;
+  if (pl->compact) {
+    const size_t n_fill = static_cast<size_t>(a->rows - a->n_exact);
+    pl->off_fill = off; off = align_up(off + static_cast<size_t>(a->rows) * 4, 256);
+    pl->off_hc = off;   off = align_up(off + n_fill * a->d_in * 2, 256);
+  }
   pl->total = off;
 }
 
@@ -1064,6 +1090,20 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     MapLaunch m{};
     m.H = static_cast<const uint8_t*>(a->H) + static_cast<size_t>(start) * a->d_in * 2;
     m.rows = rc;
+    if (pl.compact) {  // map only the filled rows; their X_hat rows land at their positions
+      int32_t* fill = reinterpret_cast<int32_t*>(ws + pl.off_fill);
+      const int64_t blocks = (a->rows + 255) / 256 < 4 * sm_count() ? (a->rows + 255) / 256 : 4 * sm_count();
+      complement_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(a->exact_idx, a->n_exact,
+                                                                    a->rows, fill);
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return cuda_fail(e, "filled-row list launch");
+      const int64_t n_fill = a->rows - a->n_exact;
+      if ((st = launch_gather_rows(a->H, fill, n_fill, a->rows, a->d_in, ws + pl.off_hc, s)) != RF_OK)
+        return st;
+      m.H = ws + pl.off_hc;
+      m.rows = n_fill;
+      m.out_rows = fill;
+    }
     m.d_in = a->d_in;
     m.d_out = a->d_out;
     m.n_layers = a->n_layers;
@@ -1073,7 +1113,9 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     m.gain = a->gain;
     m.xhat = xhat;
     m.ss = ss;
-    if (!a->maps_on_host) {
+    if (m.rows == 0) {
+      // every row of the chunk is exact: no map GEMM
+    } else if (!a->maps_on_host) {
       m.A = a->A;
       m.A_scale = a->A_scale;
       m.slot_layer = -1;

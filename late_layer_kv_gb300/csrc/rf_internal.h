@@ -71,7 +71,11 @@ struct GemmParams {
   uint32_t h_gen;
   int32_t h_group_rows;
   int32_t h_row_base;
-  // map epilogue
+  // map epilogue; with map_rows set, tile row r is stored as X_hat row map_rows[r] (row by
+  // row, straight from registers) into map_out [L, map_ld, d_out]
+  const int32_t* map_rows;
+  __nv_bfloat16* map_out;
+  int64_t map_ld;
   const float* bias;
   const __nv_bfloat16* gain;
   float* ss_part;

@@ -162,3 +162,39 @@ def test_terminal_state_correction():
     assert torch.equal(rho, rho2)
     want = oracle.terminal_correction(S1.double().numpy(), rho.double().numpy(), dM.double().numpy())
     np.testing.assert_allclose(S2.double().numpy(), want, rtol=1e-6, atol=1e-6)
+
+
+def test_gdn_all_rows_exact_and_int8_maps():
+    """Every prefix row exact (no map GEMM at all) and exact rows with int8 maps (mapped
+    in full, then overwritten) both follow the oracle."""
+    shape = _gdn_shape(N=200)
+    inp = gdn_inputs(shape, seed=97)
+    o = {k: to_f64(v) for k, v in inp.items()}
+    every = torch.arange(shape.rows, dtype=torch.int32)
+    X = true_inputs(2, shape.rows, 256, seed=97)
+    S, rho = _gdn(shape, inp, every, X, rho=True)
+    ref = oracle.gdn_state(o["H"], o["A"], o["b"], o["g"], o["Wk"], o["Wv"], o["Wa"], o["Wb"],
+                           shape.rms_eps, 8, 128, 128, exact_idx=every.numpy(), X_exact=to_f64(X))
+    for l in range(2):
+        for h in range(8):
+            compare(S[l, h].double().numpy(), ref[l, h], f"S layer {l} head {h}")
+    assert bool((rho == 0.0).all())
+
+    from late_layer_kv_gb300 import ridgefill_quantize_maps
+    exact = exact_rows(shape.rows, 0.3, seed=97)
+    Xe = true_inputs(2, len(exact), 256, seed=98)
+    d = {k: v.cuda() for k, v in inp.items()}
+    q, s = ridgefill_quantize_maps(d["A"])
+    out = []
+    for A, A_scale in ((q, s), (None, None)):
+        if A is None:  # bf16 maps equal to bf16(q * s), compacted path
+            w = q.cpu().float().reshape(2, 256, 2, 128) * s.cpu().float().transpose(1, 2)[..., None]
+            A = w.reshape(2, 256, 256).to(torch.bfloat16).cuda()
+        St = torch.empty((2, 8, 128, 128), device="cuda")
+        ridgefill_fill_gdn(d["H"], A, d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"], d["Wb"], St,
+                           n_heads=8, rms_eps=shape.rms_eps, exact_idx=exact.cuda(),
+                           X_exact=Xe.cuda(), A_scale=A_scale)
+        out.append(St)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    assert torch.equal(out[0], out[1])  # full-map-then-overwrite == compacted, bit for bit
