@@ -206,7 +206,8 @@ class AttnWorkload:
 
     def launches_per_step(self):
         chunks = -(-self.n_fill // self._chunk_rows())
-        per_chunk = (self.shape.n_layers + 1) if self.host_maps else 2
+        # map GEMM (one per layer with host maps), RoPE table, K/V GEMM
+        per_chunk = (self.shape.n_layers + 2) if self.host_maps else 3
         per_chunk += 1 if self.exact_frac else 0  # the row gather
         # rescale: map GEMM, true-input norm, value GEMM, ratio
         return chunks * per_chunk + (4 if self.c else 0)
@@ -371,7 +372,8 @@ class HybridWorkload:
         self.stage_work = {
             "attn_map_gemm": 2.0 * (s.rows - self.n_exact) * La * s.d * s.d,
             "attn_kv_gemm": 2.0 * (s.rows - self.n_exact) * La * s.d * 2 * kvw,
-            "gdn_map_gemm": 2.0 * s.rows * Lg * s.d * s.d,
+            # with exact rows the GDN map GEMM runs on the filled rows only
+            "gdn_map_gemm": 2.0 * (s.rows - self.n_exact) * Lg * s.d * s.d,
             "gdn_proj_gemm": 2.0 * s.rows * Lg * s.d * proj,
             # per row and head: dot product and rank-1 update, one FMA per state element each
             "gdn_state": 4.0 * s.rows * Lg * H * s.d_v * s.d_k,
@@ -381,8 +383,9 @@ class HybridWorkload:
         self.total_flops = sum(v for k, v in self.stage_work.items() if k != "gdn_state")
 
     def launches_per_step(self):
-        # attention map + K/V (+ gather), GDN map, projection, state (+ exact input, rho, finish)
-        return 5 + (4 if self.exact_frac else 0)
+        # attention map + K/V + RoPE table (+ gather), GDN map, projection, state (+ filled-row
+        # list, gather, exact input, rho, finish)
+        return 6 + (6 if self.exact_frac else 0)
 
     def setup(self, dev, seed):
         from late_layer_kv_gb300 import ridgefill as rb
