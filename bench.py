@@ -51,8 +51,8 @@ FP32_LANES_PER_SM = 128
 # (ncu, one pass; profiles/fill_launches_llama8b_16k.md), valid while the
 # library sources hash to kernel_sha256.
 PROFILED_TRAFFIC = {
-    "llama8b_16k": {"kernel_sha256": "6253e08240ad23a77477fc9225abb8c22ccd97d4320a13878927c665b7d7d621",
-                    "bytes_per_launch": 7499728896 + 2357863168},
+    "llama8b_16k": {"kernel_sha256": "2aa20fb2c123f5198a5bc2b4d3d8d451ce87bc0c98e5adb0c727d01304e36422",
+                    "bytes_per_launch": 7293371904 + 2353405184},
 }
 
 
