@@ -427,17 +427,19 @@ class HybridWorkload:
     def n_events(self):
         return 7
 
-    def step(self, stream, ev=None):
+    def step(self, stream, ev=None, H=None, ws=None):
         from late_layer_kv_gb300 import ridgefill_fill, ridgefill_fill_gdn
         s, d = self.shape, self.d
-        ridgefill_fill(self.H_dev, d["attn_A"], d["attn_b"], d["attn_g"], d["attn_Wk"],
+        Hx = self.H_dev if H is None else H
+        wsx = self.ws if ws is None else ws
+        ridgefill_fill(Hx, d["attn_A"], d["attn_b"], d["attn_g"], d["attn_Wk"],
                        d["attn_Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
-                       rope_theta=s.rope_theta, rms_eps=s.rms_eps, workspace=self.ws,
+                       rope_theta=s.rope_theta, rms_eps=s.rms_eps, workspace=wsx,
                        stream=stream, stage_events=None if ev is None else ev[0:3],
                        row_idx=self.row_idx)
-        ridgefill_fill_gdn(self.H_dev, d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"],
+        ridgefill_fill_gdn(Hx, d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"],
                            d["Wb"], self.S, n_heads=s.n_heads, rms_eps=s.rms_eps,
-                           workspace=self.ws, stream=stream,
+                           workspace=wsx, stream=stream,
                            stage_events=None if ev is None else ev[3:7],
                            exact_idx=self.exact_idx, X_exact=self.X_exact, rho=self.rho,
                            delta_M=self.dM)
@@ -447,14 +449,33 @@ class HybridWorkload:
         return {n: ev[a].elapsed_time(ev[b]) for n, (a, b) in zip(self.stage_names, pairs)}
 
     def e2e_buffers(self):
+        from late_layer_kv_gb300 import ridgefill as rb
+        s, d = self.shape, self.d
         self.H_host = self.inp["H"].pin_memory()
         self.out_host = torch.empty(self.S.shape, dtype=torch.float32).pin_memory()
+        # each call reads the pinned split state itself, its copy overlapped with its map
+        # GEMM (two copies of H per step); with a row list H is copied once, first
+        self.h_from_host = self.row_idx is None
+        if self.h_from_host:
+            a = rb.fill_args(self.H_host, d["attn_A"], d["attn_b"], d["attn_g"], d["attn_Wk"],
+                             d["attn_Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
+                             rope_theta=s.rope_theta, rms_eps=s.rms_eps)
+            g = rb.gdn_args(self.H_host, d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"],
+                            d["Wb"], self.S, n_heads=s.n_heads, rms_eps=s.rms_eps,
+                            exact_idx=self.exact_idx, X_exact=self.X_exact, rho=self.rho,
+                            delta_M=self.dM)
+            self.ws_e2e = torch.empty(max(rb.fill_workspace_size(a), rb.gdn_workspace_size(g)),
+                                      dtype=torch.uint8, device=self.S.device)
+            return 2 * self.H_host.numel() * 2, self.out_host.numel() * 4
         self.H_dev = torch.empty_like(self.d["H"])
         return self.H_host.numel() * 2, self.out_host.numel() * 4
 
     def e2e_step(self, stream):
-        self.H_dev.copy_(self.H_host, non_blocking=True)
-        self.step(stream)
+        if self.h_from_host:
+            self.step(stream, H=self.H_host, ws=self.ws_e2e)
+        else:
+            self.H_dev.copy_(self.H_host, non_blocking=True)
+            self.step(stream)
         self.out_host.copy_(self.S, non_blocking=True)
 
     def cpu_rate(self, budget_flop):

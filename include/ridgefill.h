@@ -314,6 +314,9 @@ rf_status ridgefill_quantize_maps(const rf_quantize_args* args, void* stream);
  *   rows' total weight over all rows' (1 with no exact rows, 0 with rows = 0).
  * delta_M (optional): [L, n_heads, d_v, d_k] f32, the terminal-state
  *   correction of section 2.3: S += rho * delta_M once, after the last row.
+ * h_on_host (0 or 1): H is page-locked host memory, streamed as for
+ *   rf_fill_args.h_on_host (with exact rows and one row chunk the copy
+ *   completes before the filled rows are gathered).
  */
 typedef struct rf_gdn_args {
   int32_t n_layers;
@@ -345,6 +348,8 @@ typedef struct rf_gdn_args {
   const void* X_exact;
   float* rho;
   const float* delta_M;
+  int32_t h_on_host;
+  int32_t reserved0;
 } rf_gdn_args;
 
 size_t ridgefill_gdn_workspace_size(const rf_gdn_args* args);

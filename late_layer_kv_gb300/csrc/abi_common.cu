@@ -114,6 +114,48 @@ StreamWrite32 stream_write32() {
   return fn;
 }
 
+std::mutex& host_stream_mutex() {
+  static std::mutex mu;
+  return mu;
+}
+
+size_t host_rows_bytes(int64_t rows, int d_in, size_t* flags_off) {
+  const size_t data = align_up(static_cast<size_t>(rows) * d_in * 2, 256);
+  *flags_off = data;
+  return data + align_up(static_cast<size_t>(ceil_div(rows, kHostRowGroup)) * 4, 256);
+}
+
+rf_status stream_host_rows(HostStreamer* hs, const void* H, int64_t rows, int d_in, uint8_t* dev,
+                           uint32_t* flags, cudaStream_t s, HostRows* out) {
+  out->flags = flags;
+  out->gen = ++hs->h_gen == 0 ? ++hs->h_gen : hs->h_gen;
+  const int64_t groups = ceil_div(rows, kHostRowGroup);
+  StreamWrite32 wr = stream_write32();
+  out->overlap = wr != nullptr;
+  for (int64_t g = 0; g < groups && out->overlap; ++g)  // clear the flags, in order on `s`
+    out->overlap = wr(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(flags + g), 0,
+                      0) == CUDA_SUCCESS;
+  const uint8_t* src = static_cast<const uint8_t*>(H);
+  cudaError_t e = cudaEventRecord(hs->start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->copy, hs->start, 0);
+  for (int64_t g = 0; g < groups && e == cudaSuccess; ++g) {
+    const int64_t r0 = g * kHostRowGroup;
+    const int64_t nr = rows - r0 < kHostRowGroup ? rows - r0 : kHostRowGroup;
+    const size_t off = static_cast<size_t>(r0) * d_in * 2;
+    e = cudaMemcpyAsync(dev + off, src + off, static_cast<size_t>(nr) * d_in * 2,
+                        cudaMemcpyHostToDevice, hs->copy);
+    if (e == cudaSuccess && out->overlap &&
+        wr(reinterpret_cast<CUstream>(hs->copy), reinterpret_cast<CUdeviceptr>(flags + g), out->gen,
+           0) != CUDA_SUCCESS)
+      e = cudaErrorUnknown;
+  }
+  if (e == cudaSuccess) e = cudaEventRecord(hs->h_done, hs->copy);
+  if (e == cudaSuccess && !out->overlap) e = cudaStreamWaitEvent(s, hs->h_done, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "streaming the split state from host memory");
+  out->base = dev;
+  return RF_OK;
+}
+
 HostStreamer* host_streamer() {
   static HostStreamer hs[kMaxDevices];
   static std::mutex mu;
@@ -336,7 +378,7 @@ extern "C" rf_status ridgefill_wait_selftest(int32_t which, void* stream) {
   return RF_OK;
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 7; }
+extern "C" int32_t ridgefill_abi_version(void) { return 8; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {

@@ -6,6 +6,8 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/ridgefill.h"
 #include "rf_internal.h"
 
@@ -54,7 +56,27 @@ StreamWrite32 stream_write32();
 // Rows of split state per ready flag when H streams from host memory (a multiple
 // of the pair GEMM's 256-row tiles; one raster group of the map GEMM).
 constexpr int kHostRowGroup = 4096;
+
+// Split state in page-locked host memory, streamed into device memory `dev` in groups of
+// kHostRowGroup rows on the copy stream.  Each group's flag (flags[g], in device memory)
+// is set to `gen` by a stream write once its rows have landed, so a map GEMM given the
+// flags can start on a group as soon as it is there; the flags are cleared on `s` first.
+// Without stream writes `s` waits for the whole copy (overlap false).  hs->h_done is
+// recorded after the last group.
+struct HostRows {
+  const uint8_t* base = nullptr;  // device copy of H
+  uint32_t* flags = nullptr;
+  uint32_t gen = 0;
+  bool overlap = false;
+};
+rf_status stream_host_rows(HostStreamer* hs, const void* H, int64_t rows, int d_in, uint8_t* dev,
+                           uint32_t* flags, cudaStream_t s, HostRows* out);
+// Bytes of device memory stream_host_rows needs: rows and ready flags (offsets 0 and the
+// returned flags offset).
+size_t host_rows_bytes(int64_t rows, int d_in, size_t* flags_off);
 HostStreamer* host_streamer();  // nullptr on failure (error recorded)
+// Held by a call for as long as it enqueues work on the copy stream (maps or split state).
+std::mutex& host_stream_mutex();
 
 // The map GEMM over `rows` split-state rows starting at H (grouped over all
 // maps in A when `slot_layer` < 0, else the single layer `slot_layer` whose

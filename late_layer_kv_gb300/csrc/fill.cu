@@ -72,10 +72,10 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   pl->off_gather = align_up(pl->off_slots + slots, 256);
   const size_t gather = a->row_idx != nullptr ? static_cast<size_t>(pl->R) * a->d_in * 2 : 0;
   pl->off_hdev = align_up(pl->off_gather + gather, 256);
-  const size_t rows = a->h_on_host ? static_cast<size_t>(a->rows) : 0;
-  pl->off_hflags = align_up(pl->off_hdev + rows * a->d_in * 2, 256);
-  const size_t groups = a->h_on_host ? ceil_div(a->rows, kHostRowGroup) : 0;
-  pl->off_rope = align_up(pl->off_hflags + groups * 4, 256);
+  size_t hflags = 0;
+  const size_t hbytes = a->h_on_host ? host_rows_bytes(a->rows, a->d_in, &hflags) : 0;
+  pl->off_hflags = pl->off_hdev + hflags;
+  pl->off_rope = align_up(pl->off_hdev + hbytes, 256);
   const size_t rope = static_cast<size_t>(a->head_dim / 2) * pl->R * 8;  // (cos, sin) f32 pairs
   pl->total = align_up(pl->off_rope + rope, 256);
 }
@@ -206,8 +206,6 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   return RF_OK;
 }
 
-std::mutex g_host_map_mu;
-
 }  // namespace
 
 rf_status launch_gather_rows(const void* H, const int32_t* idx, int64_t rc, int64_t h_rows,
@@ -263,46 +261,20 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
   const size_t slot_bytes = map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr);
 
   HostStreamer* hs = nullptr;
-  std::unique_lock<std::mutex> lk(g_host_map_mu, std::defer_lock);
+  std::unique_lock<std::mutex> lk(host_stream_mutex(), std::defer_lock);
   if (a->maps_on_host || a->h_on_host) {
     lk.lock();
     hs = host_streamer();
     if (hs == nullptr) return RF_ERR_CUDA;
   }
-  // split state in host memory: copied in row groups on the copy stream; each group's
-  // flag is set by a stream write once its rows have landed, and the map GEMM's
-  // producers wait on the flags, so the copy overlaps the GEMM.  Without stream
-  // writes the map GEMM waits for the whole copy.
+  // split state in host memory: streamed in row groups, overlapped with the map GEMM
   const uint8_t* h_base = static_cast<const uint8_t*>(a->H);
-  uint32_t* h_flags = nullptr;
-  uint32_t h_gen = 0;
-  bool h_overlap = false;
+  HostRows hr;
   if (a->h_on_host) {
-    h_flags = reinterpret_cast<uint32_t*>(ws + pl.off_hflags);
-    h_gen = ++hs->h_gen == 0 ? ++hs->h_gen : hs->h_gen;
-    const int64_t groups = ceil_div(a->rows, kHostRowGroup);
-    StreamWrite32 wr = stream_write32();
-    h_overlap = wr != nullptr;
-    for (int64_t g = 0; g < groups && h_overlap; ++g)  // clear the flags, in order on `s`
-      h_overlap = wr(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(h_flags + g), 0,
-                     0) == CUDA_SUCCESS;
-    cudaError_t e = cudaEventRecord(hs->start, s);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->copy, hs->start, 0);
-    for (int64_t g = 0; g < groups && e == cudaSuccess; ++g) {
-      const int64_t r0 = g * kHostRowGroup;
-      const int64_t nr = a->rows - r0 < kHostRowGroup ? a->rows - r0 : kHostRowGroup;
-      const size_t off = static_cast<size_t>(r0) * a->d_in * 2;
-      e = cudaMemcpyAsync(ws + pl.off_hdev + off, h_base + off, static_cast<size_t>(nr) * a->d_in * 2,
-                          cudaMemcpyHostToDevice, hs->copy);
-      if (e == cudaSuccess && h_overlap &&
-          wr(reinterpret_cast<CUstream>(hs->copy), reinterpret_cast<CUdeviceptr>(h_flags + g), h_gen,
-             0) != CUDA_SUCCESS)
-        e = cudaErrorUnknown;
-    }
-    if (e == cudaSuccess) e = cudaEventRecord(hs->h_done, hs->copy);
-    if (e == cudaSuccess && !h_overlap) e = cudaStreamWaitEvent(s, hs->h_done, 0);
-    if (e != cudaSuccess) return cuda_fail(e, "streaming the split state from host memory");
-    h_base = ws + pl.off_hdev;
+    if ((st = stream_host_rows(hs, a->H, a->rows, a->d_in, ws + pl.off_hdev,
+                               reinterpret_cast<uint32_t*>(ws + pl.off_hflags), s, &hr)) != RF_OK)
+      return st;
+    h_base = hr.base;
   }
   if (a->maps_on_host) {
     // the copy stream starts after work already queued on `s` (earlier users of the slots)
@@ -322,9 +294,9 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     const int64_t rc = (a->rows - start < pl.R) ? a->rows - start : pl.R;
     MapLaunch m{};
     m.H = h_base + static_cast<size_t>(start) * a->d_in * 2;
-    if (h_overlap) {
-      m.h_ready = h_flags;
-      m.h_gen = h_gen;
+    if (hr.overlap) {
+      m.h_ready = hr.flags;
+      m.h_gen = hr.gen;
       m.h_row_base = start;
     }
     if (a->row_idx != nullptr) {  // the chunk's listed rows, gathered

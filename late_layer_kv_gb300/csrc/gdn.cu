@@ -856,7 +856,7 @@ struct GdnPlan {
   int bn_map = 0;
   int64_t R = 0;
   size_t off_xhat = 0, off_ss = 0, off_k = 0, off_v = 0, off_gate = 0, off_slots = 0, off_rho = 0,
-         off_fill = 0, off_hc = 0, total = 0;
+         off_fill = 0, off_hc = 0, off_hdev = 0, off_hflags = 0, total = 0;
   bool compact = false;  // map only the filled rows (exact rows, one row chunk, bf16 maps)
 };
 
@@ -882,6 +882,7 @@ rf_status validate_gdn(const rf_gdn_args* a) {
   if (a->n_exact < 0 || a->n_exact > a->rows) return fail(RF_ERR_ARG, "n_exact must be in [0, rows]");
   if (a->n_exact > 0 && (a->exact_idx == nullptr || a->X_exact == nullptr))
     return fail(RF_ERR_ARG, "n_exact > 0 needs exact_idx and X_exact");
+  if (a->h_on_host != 0 && a->h_on_host != 1) return fail(RF_ERR_ARG, "h_on_host must be 0 or 1");
   return RF_OK;
 }
 
@@ -899,6 +900,12 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
   pl->off_slots = off;
   off = align_up(off + (a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0), 256);
   pl->off_rho = off;   off = align_up(off + L * H * 2 * sizeof(double), 256);
+  if (a->h_on_host) {
+    size_t fo = 0;
+    pl->off_hdev = off;
+    off = align_up(off + host_rows_bytes(a->rows, a->d_in, &fo), 256);
+    pl->off_hflags = pl->off_hdev + fo;
+  }
   pl->compact = a->n_exact > 0 && pl->R >= a->rows && a->A_scale == nullptr;
   if (pl->compact) {
     const size_t n_fill = static_cast<size_t>(a->rows - a->n_exact);
@@ -967,7 +974,6 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
   return RF_OK;
 }
 
-std::mutex g_gdn_host_map_mu;
 
 }  // namespace
 
@@ -1016,6 +1022,7 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     if (q != nullptr && !aligned16(q)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(a->exact_idx) & 3u) != 0)
     return fail(RF_ERR_ALIGN, "exact_idx is not 4-byte aligned");
+  if (a->h_on_host && a->rows > 0 && (st = check_pinned(a->H, "H")) != RF_OK) return st;
   if (a->maps_on_host && a->rows > 0) {
     if ((st = check_pinned(a->A, "A")) != RF_OK) return st;
     if (a->A_scale != nullptr && (st = check_pinned(a->A_scale, "A_scale")) != RF_OK) return st;
@@ -1068,12 +1075,28 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
   }
 
   HostStreamer* hs = nullptr;
-  std::unique_lock<std::mutex> lk(g_gdn_host_map_mu, std::defer_lock);
+  std::unique_lock<std::mutex> lk(host_stream_mutex(), std::defer_lock);
   const size_t slot_bytes = map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr);
-  if (a->maps_on_host) {
+  if (a->maps_on_host || a->h_on_host) {
     lk.lock();
     hs = host_streamer();
     if (hs == nullptr) return RF_ERR_CUDA;
+  }
+  // split state in host memory: streamed in row groups, overlapped with the map GEMM (with
+  // exact rows compacted, the gather waits for the whole copy)
+  const uint8_t* h_base = static_cast<const uint8_t*>(a->H);
+  HostRows hr;
+  if (a->h_on_host) {
+    if ((st = stream_host_rows(hs, a->H, a->rows, a->d_in, ws + pl.off_hdev,
+                               reinterpret_cast<uint32_t*>(ws + pl.off_hflags), s, &hr)) != RF_OK)
+      return st;
+    h_base = hr.base;
+    if (pl.compact && hr.overlap) {
+      cudaError_t e = cudaStreamWaitEvent(s, hs->h_done, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "ordering after the split-state copy");
+    }
+  }
+  if (a->maps_on_host) {
     cudaError_t e = cudaEventRecord(hs->start, s);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->copy, hs->start, 0);
     if (e != cudaSuccess) return cuda_fail(e, "ordering the map-copy stream");
@@ -1088,8 +1111,13 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     const int64_t rc = (a->rows - start < pl.R) ? a->rows - start : pl.R;
     if ((st = mark(start, 0)) != RF_OK) return st;
     MapLaunch m{};
-    m.H = static_cast<const uint8_t*>(a->H) + static_cast<size_t>(start) * a->d_in * 2;
+    m.H = h_base + static_cast<size_t>(start) * a->d_in * 2;
     m.rows = rc;
+    if (hr.overlap && !pl.compact) {
+      m.h_ready = hr.flags;
+      m.h_gen = hr.gen;
+      m.h_row_base = start;
+    }
     if (pl.compact) {  // map only the filled rows; their X_hat rows land at their positions
       int32_t* fill = reinterpret_cast<int32_t*>(ws + pl.off_fill);
       const int64_t blocks = (a->rows + 255) / 256 < 4 * sm_count() ? (a->rows + 255) / 256 : 4 * sm_count();
@@ -1098,7 +1126,7 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) return cuda_fail(e, "filled-row list launch");
       const int64_t n_fill = a->rows - a->n_exact;
-      if ((st = launch_gather_rows(a->H, fill, n_fill, a->rows, a->d_in, ws + pl.off_hc, s)) != RF_OK)
+      if ((st = launch_gather_rows(h_base, fill, n_fill, a->rows, a->d_in, ws + pl.off_hc, s)) != RF_OK)
         return st;
       m.H = ws + pl.off_hc;
       m.rows = n_fill;
@@ -1162,6 +1190,10 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     cudaError_t e = launch_gdn_state(sp, s);
     if (e != cudaSuccess) return cuda_fail(e, "GDN state launch");
     if ((st = mark(start, 3)) != RF_OK) return st;
+  }
+  if (a->h_on_host) {  // later work on `s` (and the caller's reuse of H) follows the copy
+    cudaError_t e = cudaStreamWaitEvent(s, hs->h_done, 0);
+    if (e != cudaSuccess) return cuda_fail(e, "ordering after the split-state copy");
   }
   if (want_rho) {  // rho, and the terminal-state correction on the final state
     rho_finish_kernel<<<LH, 256, 0, s>>>(rho_acc, 0, a->rho, a->delta_M, a->S, kDk * kDk);

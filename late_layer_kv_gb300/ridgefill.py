@@ -53,7 +53,7 @@ class GdnArgs(ctypes.Structure):
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Wa", _vp), ("Wb", _vp), ("S0", _vp), ("S", _vp), ("stage_events", _vp),
         ("A_scale", _vp), ("exact_idx", _vp), ("n_exact", ctypes.c_int64), ("X_exact", _vp),
-        ("rho", _vp), ("delta_M", _vp),
+        ("rho", _vp), ("delta_M", _vp), ("h_on_host", ctypes.c_int32), ("reserved0", ctypes.c_int32),
     ]
 
 
@@ -303,7 +303,14 @@ def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: floa
     rows = H.shape[0]
     d_k = Wk.shape[1] // n_heads
     d_v = Wv.shape[1] // n_heads
-    _dev(H, "H", torch.bfloat16, (rows, d_in))
+    h_host = not H.is_cuda
+    if h_host:
+        if H.dtype != torch.bfloat16 or not H.is_contiguous() or not H.is_pinned():
+            raise ValueError("host H must be contiguous, pinned bf16")
+        if tuple(H.shape) != (rows, d_in):
+            raise ValueError("H must be [rows, d_in]")
+    else:
+        _dev(H, "H", torch.bfloat16, (rows, d_in))
     host = _check_maps(A, A_scale)
     _dev(bias, "bias", torch.float32, (L, d_out))
     if gain is not None:
@@ -330,7 +337,7 @@ def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: floa
                 _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Wa), _ptr(Wb), _ptr(S0), _ptr(S),
                 ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None, _ptr(A_scale),
                 _ptr(exact_idx), n_exact, _ptr(X_exact) if n_exact else None, _ptr(rho),
-                _ptr(delta_M))
+                _ptr(delta_M), 1 if h_host else 0, 0)
     a._events_keepalive = ev
     return a
 
@@ -357,7 +364,7 @@ def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms
     if need == 0:
         _check(lib.ridgefill_fill_gdn(ctypes.byref(args), None, 0, _stream(stream)))
     if workspace is None:
-        workspace = torch.empty(need, dtype=torch.uint8, device=H.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=S.device)
     elif workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace needs {need} bytes")
     _check(lib.ridgefill_fill_gdn(ctypes.byref(args), _ptr(workspace),

@@ -101,3 +101,26 @@ def test_full_size_hybrid_sampled_heads():
     for l, h in ((0, 0), (shape.n_gdn - 1, shape.n_heads - 1)):
         ref = _oracle(shape, gdn, layers=[l], heads=[h])
         compare(got[l, h], ref[0, 0], f"full-size S layer {l} head {h}")
+
+
+def test_host_split_state_bitwise_equal_device():
+    """H in pinned host memory (streamed in row groups overlapped with the map GEMM) gives
+    the state of a device-resident H, with and without row chunks and exact rows."""
+    from synthetic import exact_rows, true_inputs
+    shape = _shape(N=9000)
+    inp = gdn_inputs(shape, seed=39)
+    d = {k: v.cuda() for k, v in inp.items()}
+    H_host = inp["H"].pin_memory()
+    ex = exact_rows(shape.rows, 0.2, seed=39)
+    X = true_inputs(2, len(ex), 256, seed=39).cuda()
+    for rpc, exact in ((0, False), (4096, False), (0, True)):
+        out = []
+        for H in (d["H"], H_host):
+            S = torch.empty((2, 8, 128, 128), device="cuda")
+            ridgefill_fill_gdn(H, d["A"], d["b"], d["g"], d["Wk"], d["Wv"], d["Wa"], d["Wb"], S,
+                               n_heads=8, rms_eps=shape.rms_eps, rows_per_chunk=rpc,
+                               exact_idx=ex.cuda() if exact else None, X_exact=X if exact else None)
+            out.append(S)
+        torch.cuda.synchronize()
+        assert device_error() == 0
+        assert torch.equal(out[0], out[1]), (rpc, exact)
