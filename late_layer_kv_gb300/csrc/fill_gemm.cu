@@ -1072,37 +1072,31 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
 }
 
 cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // set on every launch: the attribute belongs to the current device, and the call is
+  // cheap next to the kernel
+  cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<false>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
   rf_gemm2_kernel<false><<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<true>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // set on every launch: the attribute belongs to the current device, and the call is
+  // cheap next to the kernel
+  cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<true>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
+  if (e != cudaSuccess) return e;
   rf_gemm2_kernel<true><<<2 * pairs, kGemmThreadsQ8, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(rf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kGemmSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // set on every launch: the attribute belongs to the current device, and the call is
+  // cheap next to the kernel
+  cudaError_t e = cudaFuncSetAttribute(rf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kGemmSmem);
+  if (e != cudaSuccess) return e;
   rf_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
 }

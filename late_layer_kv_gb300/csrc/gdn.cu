@@ -978,13 +978,11 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
 }  // namespace
 
 cudaError_t launch_gdn_state(const GdnStateParams& p, cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(gdn_state_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  // set on every launch: the attribute belongs to the current device, and the call is
+  // cheap next to the kernel
+  cudaError_t e = cudaFuncSetAttribute(gdn_state_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kStateSmem);
+  if (e != cudaSuccess) return e;
   dim3 grid(p.heads, p.layers);
   gdn_state_kernel<<<grid, kStateThreads, kStateSmem, stream>>>(p);
   return cudaGetLastError();
