@@ -664,6 +664,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
 // accumulator on CTA 0's `tempty` barrier.
 constexpr int kStages2 = 6;
 constexpr int kHalfBytes = 128 * kBK * 2;  // 128 rows x 64 K of bf16
+// Wide Gram tiles (bn = kGramWideCols): the pair accumulates 256 x 512 in both TMEM halves with two
+// N = 256 MMAs per K step that share one A stage.  A stage then holds this CTA's A half and
+// its two B quarters (48 KB), four stages in the space of the six narrow ones.
+constexpr int kWideStageBytes = 3 * kHalfBytes;
+constexpr int kStagesWide = 4;
+static_assert(kStagesWide * kWideStageBytes <= kStages2 * 2 * kHalfBytes, "wide Gram stages");
 
 namespace {
 
@@ -834,6 +840,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer of this CTA's halves
+      const bool wide = !kQ8 && p.mode == kModeGram && p.bn == kGramWideCols;
+      const uint32_t nst = wide ? kStagesWide : kS;
       uint32_t stage = 0, phase = 0;
       int issued[kS];
       for (int s = 0; s < kS; ++s) issued[s] = -1;
@@ -864,8 +872,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
           else mbar_expect_tx_cl(fb, tx);
           if (!kQ8 && p.mode == kModeGram) {
             // MN-major operands: 64-wide column blocks of [rows, width] arrays, 64 rows of K;
-            // A: this CTA's 128 columns of [X | Y_1 .. Y_L], B: its half of the X columns
-            uint8_t* adst = sA + stage * kHalfBytes;
+            // A: this CTA's 128 columns of [X | Y_1 .. Y_L], B: its half of the X columns of
+            // each N <= 256 MMA (a wide tile's second MMA starts 256 columns on)
+            uint8_t* adst = wide ? sA + stage * kWideStageBytes : sA + stage * kHalfBytes;
+            uint8_t* bdst = wide ? adst + kHalfBytes : sB + stage * kHalfBytes;
+            const int nmma = tb.bn < 256 ? tb.bn : 256;
+            const int bpm = nmma / 128;  // 64-column boxes per MMA in this CTA's half
             // (the empty second half of an odd last row tile reads past X: zero fill)
             if (m < p.gram_x_tiles || m >= p.m_tiles) {
               for (int j = 0; j < kBM / 64; ++j)
@@ -879,8 +891,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
                 tma_load_3d_pair(smem_u32(adst + j * 8192), &p.tmA2, fb, m0 + 64 * j, kb * kBK, l);
             }
             for (int j = 0; j < half / 64; ++j)
-              tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes + j * 8192), &p.tmB[0], fb,
-                               tb.nrow + half * static_cast<int>(rank) + 64 * j, kb * kBK, 0);
+              tma_load_3d_pair(smem_u32(bdst + j * 8192), &p.tmB[0], fb,
+                               tb.nrow + (j / bpm) * nmma + (nmma / 2) * static_cast<int>(rank) +
+                                   64 * (j % bpm),
+                               kb * kBK, 0);
           } else {
             tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, kb * kBK, m * kBM, b);
           }
@@ -892,7 +906,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
           else  // GDN gate tile: CTA 0 stages the alpha weights, CTA 1 the beta weights
             tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[2 + rank], fb, kb * kBK, 0, b);
           issued[stage] = static_cast<int>(phase);
-          if (++stage == kS) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1;
           }
@@ -905,6 +919,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (CTA 0 only)
+      const bool wide = !kQ8 && p.mode == kModeGram && p.bn == kGramWideCols;
+      const uint32_t nst = wide ? kStagesWide : kS;
       uint32_t stage = 0, phase = 0;
       int it = 0;
       bool ok = true;
@@ -913,9 +929,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         decode_pair(t, p, mp, n, b);
         const TileB tb = tile_b(p, n);
         const bool mn = !kQ8 && p.mode == kModeGram;
-        const uint32_t idesc = idesc_bf16_f32(2 * kBM, tb.bn) | (mn ? (3u << 15) : 0u);
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
+        const uint32_t idesc =
+            idesc_bf16_f32(2 * kBM, wide ? 256 : tb.bn) | (mn ? (3u << 15) : 0u);
+        // a wide tile takes both accumulators: one buffer, its phase flips every tile
+        const int acc = wide ? 0 : it & 1;
+        const uint32_t acc_phase = wide ? it & 1 : (it >> 1) & 1;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, kErrMma)) break;
         tc_fence_after();
         const uint32_t dt = tmem_base + acc * kBNMax;
@@ -933,16 +951,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)
               mma_bf16_pair(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-          } else {
+          } else if (!wide) {
             // MN-major: 64-element column blocks 8 KB apart, K rows 128 B apart
             const uint64_t ad = sdesc_mnmajor_sw128(smem_u32(sA + stage * kHalfBytes), 8192);
             const uint64_t bd = sdesc_mnmajor_sw128(smem_u32(sB + stage * kHalfBytes), 8192);
 #pragma unroll
             for (int k = 0; k < kBK / 16; ++k)  // advance 16 K rows (2048 B)
               mma_bf16_pair(dt, ad + 128 * k, bd + 128 * k, idesc, (kb | k) != 0 ? 1u : 0u);
+          } else {
+            // wide: the same A stage against the two B quarters, into TMEM columns 0-255
+            // and 256-511
+            const uint32_t sa = smem_u32(sA + stage * kWideStageBytes);
+            const uint64_t ad = sdesc_mnmajor_sw128(sa, 8192);
+            const uint64_t bd0 = sdesc_mnmajor_sw128(sa + kHalfBytes, 8192);
+            const uint64_t bd1 = sdesc_mnmajor_sw128(sa + 2 * kHalfBytes, 8192);
+#pragma unroll
+            for (int k = 0; k < kBK / 16; ++k) {
+              const uint32_t accum = (kb | k) != 0 ? 1u : 0u;
+              mma_bf16_pair(dt, ad + 128 * k, bd0 + 128 * k, idesc, accum);
+              mma_bf16_pair(dt + 256, ad + 128 * k, bd1 + 128 * k, idesc, accum);
+            }
           }
           mma_commit_pair(&empty[stage], 3);
-          if (++stage == kS) {
+          if (++stage == nst) {
             stage = 0;
             phase ^= 1;
           }
@@ -996,8 +1027,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       int mp, n, b;
       decode_pair(t, p, mp, n, b);
       const int m = 2 * mp + static_cast<int>(rank);
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
+      const bool wide = !kQ8 && p.mode == kModeGram && p.bn == kGramWideCols;
+      const int acc = wide ? 0 : it & 1;
+      const uint32_t acc_phase = wide ? it & 1 : (it >> 1) & 1;
       float rs = 1.f;
       if (!kQ8 && (p.mode == kModeKV || p.mode == kModeGdnProj))
         rs = row_rms_scale(p, b, m * kBM + q * 32 + lane);

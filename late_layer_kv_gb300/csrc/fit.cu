@@ -432,8 +432,10 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   p.gram_x_tiles = d / kBM;
   p.gram_y_tiles_per_layer = dout / kBM;
   p.m_tiles = p.gram_x_tiles + (Y != nullptr ? L * p.gram_y_tiles_per_layer : 0);
-  p.bn = bn;
-  p.n_tiles = d / bn;
+  // pairs take 512-column tiles where d allows: each A stage then feeds two MMAs, which
+  // halves the A reads per flop
+  p.bn = (kGramPairs && d % kGramWideCols == 0) ? kGramWideCols : bn;
+  p.n_tiles = d / p.bn;
   p.batches = 1;
   p.group_m = 16;
   p.d_out = dout;

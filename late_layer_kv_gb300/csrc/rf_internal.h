@@ -13,6 +13,7 @@ constexpr int kStages = 4;         // TMA -> MMA shared-memory ring depth
 constexpr int kBM = 128;           // rows per tile (one TMEM lane per row)
 constexpr int kBK = 64;            // K elements per stage (one 128-byte row)
 constexpr int kBNMax = 256;        // max columns per tile (TMEM cols per accumulator)
+constexpr int kGramWideCols = 512; // Gram tiles on CTA pairs: both accumulators, one tile
 constexpr int kABytes = kBM * kBK * 2;
 constexpr int kBBytes = kBNMax * kBK * 2;
 constexpr int kOutBoxBytes = 64 * 32 * 2;   // one 64-col x 32-row bf16 store box

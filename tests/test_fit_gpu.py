@@ -46,10 +46,15 @@ def _gpu_fit(X, Y, lam, batches=(None,)):
     return sums, A32.cpu().double().numpy(), A16, b.cpu().double().numpy(), float(alpha.item())
 
 
-def test_sums_match_oracle_and_split_batches():
-    cal = calibration(d=256, n_layers=3, n=1000, seed=40)
-    X, Y = cal["X"], cal["Y"]
-    sums, *_ = _gpu_fit(X, Y, 1e-3, batches=(600,))
+# d = 256 takes 256-column Gram tiles; d = 512 and 1024 take 512-column tiles (one and two
+# column tiles), d_out = 384 leaves the last CTA pair half empty, and 777 rows end in a
+# ragged 64-row block
+@pytest.mark.parametrize("d,L,n,d_out,cut", [(256, 3, 1000, 256, 600), (1024, 2, 777, 1024, 320),
+                                             (512, 1, 300, 384, 128)])
+def test_sums_match_oracle_and_split_batches(d, L, n, d_out, cut):
+    cal = calibration(d=d, n_layers=L, n=n, seed=40 + d)
+    X, Y = cal["X"], cal["Y"][:, :, :d_out].contiguous()
+    sums, *_ = _gpu_fit(X, Y, 1e-3, batches=(cut,))
     n, sx, sy, G, C = oracle.fit_sums(to_f64(X), to_f64(Y))
     assert float(sums.count.item()) == n
     np.testing.assert_allclose(sums.sx.cpu().numpy(), sx, rtol=2e-5, atol=2e-5 * np.abs(sx).max())
@@ -57,7 +62,7 @@ def test_sums_match_oracle_and_split_batches():
     # f32 sums of up to 600 exact products per batch: relative error ~ sqrt(n) u, n u = 6e-5 at worst
     assert _rel(sums.G.cpu().numpy(), G) < 2e-5
     Cg = sums.C.cpu().numpy()                       # [L, d_out, d_in] = Y_l^T X
-    Co = C.reshape(256, 3, 256).transpose(1, 2, 0)  # oracle [d_in, L*d_out] -> [L, d_out, d_in]
+    Co = C.reshape(d, L, d_out).transpose(1, 2, 0)  # oracle [d_in, L*d_out] -> [L, d_out, d_in]
     assert _rel(Cg, Co) < 2e-5
 
 
