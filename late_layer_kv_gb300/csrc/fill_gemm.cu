@@ -1049,6 +1049,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
       } else if (p.mode == kModeGram) {
         epilogue_gram(p, tcol, q, lane, m, n, tempty0 + 8 * acc);
+      } else if (p.mode == kModeSolve) {
+        epilogue_solve(p, tcol, q, lane, m, n, tempty0 + 8 * acc);
       } else {
         epilogue_gdn(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
       }

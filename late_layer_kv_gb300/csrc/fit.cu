@@ -123,60 +123,110 @@ __global__ void equilibrate_kernel(const double* G, const double* count, const d
 }
 
 // ------------------------------------------------------------ Cholesky (f32)
-// In-place factor of one 64x64 diagonal block (lower), right-looking, one row
-// per thread (64 threads); a pivot <= 0 records kErrNumeric in the device error
-// word and continues with pivot 1.
-__global__ void __launch_bounds__(kNB) potrf_diag_kernel(float* A, int ld, int kb, int* err) {
+// One 64x64 diagonal block: the lower factor L_kk in place (zeros above) and its
+// inverse into Linv [64, 64] (lower), both right-looking in one sweep over the
+// columns j: the pivot, column j of L and row j of L^-1 scaled by its reciprocal,
+// then the rank-1 updates of the trailing lower triangle and of the rows of L^-1
+// below j.  A pivot <= 0 records kErrNumeric in the device error word and
+// continues with pivot 1.  256 threads as 16 x 16; each step's loops cover only
+// the cells that change, so the work shrinks with the triangle.
+__global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int kb, int* err,
+                                                         float* Linv) {
   __shared__ float a[kNB][kNB + 1];
+  __shared__ float x[kNB][kNB + 1];
+  __shared__ float rpiv;
   float* blk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
-  const int i = threadIdx.x;
-  for (int k = 0; k < kNB; ++k) a[i][k] = blk[static_cast<size_t>(i) * ld + k];
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  {
+    float v[16];  // all loads in flight before the shared-memory stores
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = tid + 256 * q;
+      v[q] = blk[static_cast<size_t>(e / kNB) * ld + e % kNB];
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = tid + 256 * q, r = e / kNB, c = e % kNB;
+      a[r][c] = v[q];
+      x[r][c] = r == c ? 1.f : 0.f;
+    }
+  }
   __syncthreads();
   for (int j = 0; j < kNB; ++j) {
-    if (i == j) {
+    if (tid == 0) {
       float v = a[j][j];
       if (!(v > 0.f)) {
         atomicCAS(err, 0, kErrNumeric);
         v = 1.f;
       }
-      a[j][j] = sqrtf(v);
+      const float p = sqrtf(v);
+      a[j][j] = p;
+      rpiv = 1.f / p;
     }
     __syncthreads();
-    if (i > j) a[i][j] /= a[j][j];
-    __syncthreads();
-    if (i > j) {
-      const float lij = a[i][j];
-      for (int k = j + 1; k <= i; ++k) a[i][k] = fmaf(-lij, a[k][j], a[i][k]);
+    if (tid < kNB) {
+      const float r = rpiv;
+      if (tid > j) a[tid][j] *= r;  // column j of L
+      else x[j][tid] *= r;          // row j of L^-1 (columns <= j) is final
     }
+    __syncthreads();
+    for (int i = j + 1 + ty; i < kNB; i += 16) {
+      const float li = a[i][j];
+      for (int k = j + 1 + tx; k <= i; k += 16) a[i][k] = fmaf(-li, a[k][j], a[i][k]);
+      for (int c = tx; c <= j; c += 16) x[i][c] = fmaf(-li, x[j][c], x[i][c]);
+    }
+    __syncthreads();
   }
-  __syncthreads();
-  for (int k = 0; k < kNB; ++k) blk[static_cast<size_t>(i) * ld + k] = k <= i ? a[i][k] : 0.f;
+#pragma unroll 4
+  for (int q = 0; q < 16; ++q) {
+    const int e = tid + 256 * q, r = e / kNB, c = e % kNB;
+    blk[static_cast<size_t>(r) * ld + c] = c <= r ? a[r][c] : 0.f;
+    Linv[e] = c <= r ? x[r][c] : 0.f;
+  }
 }
 
-// Panel: A_ik <- A_ik L_kk^-T for block rows i > kb (one block row per CTA,
-// one matrix row per thread, forward substitution).
-__global__ void trsm_panel_kernel(float* A, int ld, int kb) {
-  __shared__ float L[kNB][kNB + 1];
+// Panel: A_ik <- A_ik L_kk^-T = A_ik Linv^T for block rows i > kb (one 64x64 block
+// per CTA; 256 threads with 4 x 4 outputs each).
+__global__ void __launch_bounds__(256) trsm_panel_kernel(float* A, int ld, int kb,
+                                                         const float* Linv) {
   __shared__ float X[kNB][kNB + 1];
+  __shared__ __align__(16) float Lt[kNB][kNB + 4];  // Lt[k][c] = Linv[c][k]
   const int ib = kb + 1 + blockIdx.x;
-  const float* lkk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
   float* aik = A + static_cast<size_t>(ib) * kNB * ld + static_cast<size_t>(kb) * kNB;
-  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x) {
-    L[e / kNB][e % kNB] = lkk[static_cast<size_t>(e / kNB) * ld + e % kNB];
-    X[e / kNB][e % kNB] = aik[static_cast<size_t>(e / kNB) * ld + e % kNB];
-  }
-  __syncthreads();
-  if (threadIdx.x < kNB) {
-    const int r = threadIdx.x;
-    for (int c = 0; c < kNB; ++c) {
-      float s = X[r][c];
-      for (int c2 = 0; c2 < c; ++c2) s -= X[r][c2] * L[c][c2];
-      X[r][c] = s / L[c][c];
+  {
+    float xv[16], lv[16];  // all loads in flight before the shared-memory stores
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = threadIdx.x + 256 * q;
+      xv[q] = aik[static_cast<size_t>(e / kNB) * ld + e % kNB];
+      lv[q] = Linv[e];
+    }
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = threadIdx.x + 256 * q;
+      X[e / kNB][e % kNB] = xv[q];
+      Lt[e % kNB][e / kNB] = lv[q];
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x)
-    aik[static_cast<size_t>(e / kNB) * ld + e % kNB] = X[e / kNB][e % kNB];
+  const int r0 = (threadIdx.x / 16) * 4, c0 = (threadIdx.x % 16) * 4;
+  float acc[4][4] = {};
+  for (int k = 0; k < c0 + 4; ++k) {  // Linv[c][k] = 0 for k > c
+    const float4 l = *reinterpret_cast<const float4*>(&Lt[k][c0]);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float xv = X[r0 + u][k];
+      acc[u][0] = fmaf(xv, l.x, acc[u][0]);
+      acc[u][1] = fmaf(xv, l.y, acc[u][1]);
+      acc[u][2] = fmaf(xv, l.z, acc[u][2]);
+      acc[u][3] = fmaf(xv, l.w, acc[u][3]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    float4* dst = reinterpret_cast<float4*>(aik + static_cast<size_t>(r0 + u) * ld + c0);
+    *dst = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+  }
 }
 
 // Inverse of each 64x64 lower diagonal block of L, in place (upper part zero).
@@ -211,11 +261,11 @@ __global__ void zero_upper_kernel(float* A, int d) {
 }
 
 // ------------------------------------------------------------ f32 SIMT GEMM
-// C = alpha op(A) op(B) + beta C for row-major f32 matrices; 64x64 tiles,
-// 256 threads with 4x4 outputs each.  lower_only skips tiles above the
-// diagonal; k_from_n starts the K loop at the tile's first column (op(B) lower
-// triangular); k_end_tri stops it at m0 + 64 (op(A) lower).  A batch of
-// `batch` products (grid z) steps the three operands by sa, sb, sc elements.
+// C = alpha op(A) op(B) + beta C for row-major f32 matrices.  lower_only skips
+// tiles wholly above the diagonal; k_from_n starts the K loop at the tile's first
+// column (op(B) lower triangular); k_end_tri stops it after the tile's last row
+// (op(A) lower).  A batch of `batch` products (grid z) steps the three operands
+// by sa, sb, sc elements.
 struct SgemmArgs {
   int M, N, K;
   float alpha, beta;
@@ -227,76 +277,114 @@ struct SgemmArgs {
   int64_t sa = 0, sb = 0, sc = 0;
 };
 
-template <bool TA, bool TB>
+// 128 x 128 tiles, 256 threads with 8 x 8 outputs each (rows ty*4 + {0..3} and
+// 64 + ty*4 + {0..3}, likewise the columns, so a warp's shared-memory reads are
+// contiguous); K in steps of 8, the next step's tiles loaded into registers while
+// the current one is multiplied (two shared-memory buffers, one barrier a step).
+// op(A) = A (row-major [M, lda]); op(B) = B^T ([N, ldb]) if TB, else B ([K, ldb]).
+// M, N and K are multiples of 8; every pointer and leading dimension keeps rows
+// 16-byte aligned.
+constexpr int kSgT = 128, kSgK = 8;
+
+template <bool TB>
 __global__ void __launch_bounds__(256) sgemm_kernel(const SgemmArgs g) {
-  __shared__ float As[16][64 + 4];
-  __shared__ float Bs[16][64 + 4];
-  const int m0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
-  if (g.lower_only && n0 > m0 + 63) return;
+  __shared__ __align__(16) float As[2][kSgK][kSgT + 4];
+  __shared__ __align__(16) float Bs[2][kSgK][kSgT + 4];
+  const int m0 = blockIdx.y * kSgT, n0 = blockIdx.x * kSgT;
+  if (g.lower_only && n0 > m0 + kSgT - 1) return;
   const float* __restrict__ Ag = g.A + blockIdx.z * g.sa;
   const float* __restrict__ Bg = g.B + blockIdx.z * g.sb;
   float* Cg = g.C + blockIdx.z * g.sc;
   const int tid = threadIdx.x;
   const int tx = tid % 16, ty = tid / 16;
-  float acc[4][4] = {};
   int kbeg = 0, kend = g.K;
-  if (g.k_from_n) kbeg = (n0 / 16) * 16;
-  if (g.k_end_tri) kend = min(g.K, m0 + 64);
-  for (int k0 = kbeg; k0 < kend; k0 += 16) {
-    for (int e = tid; e < 64 * 16; e += 256) {
-      int mm, kk;
-      if (TA) { kk = e / 64; mm = e % 64; } else { mm = e / 16; kk = e % 16; }
-      const int m = m0 + mm, k = k0 + kk;
-      float v = 0.f;
-      if (m < g.M && k < g.K) v = TA ? Ag[static_cast<size_t>(k) * g.lda + m]
-                                     : Ag[static_cast<size_t>(m) * g.lda + k];
-      As[kk][mm] = v;
+  if (g.k_from_n) kbeg = n0;
+  if (g.k_end_tri) kend = min(g.K, m0 + kSgT);
+  // loader roles: A (and B^T) tile rows tid / 2, four K at (tid % 2) * 4; B tile row
+  // tid / 32 of K, four columns at (tid % 32) * 4
+  const int ar = tid / 2, ak = (tid % 2) * 4;
+  const int bk = tid / 32, bc = (tid % 32) * 4;
+  auto load = [&](int k0, float4& av, float4& bv) {
+    av = make_float4(0.f, 0.f, 0.f, 0.f);
+    bv = av;
+    if (m0 + ar < g.M)
+      av = *reinterpret_cast<const float4*>(Ag + static_cast<size_t>(m0 + ar) * g.lda + k0 + ak);
+    if (TB) {
+      if (n0 + ar < g.N)
+        bv = *reinterpret_cast<const float4*>(Bg + static_cast<size_t>(n0 + ar) * g.ldb + k0 + ak);
+    } else if (n0 + bc < g.N) {
+      bv = *reinterpret_cast<const float4*>(Bg + static_cast<size_t>(k0 + bk) * g.ldb + n0 + bc);
     }
-    for (int e = tid; e < 64 * 16; e += 256) {
-      int nn, kk;
-      if (TB) { nn = e / 16; kk = e % 16; } else { kk = e / 64; nn = e % 64; }
-      const int n = n0 + nn, k = k0 + kk;
-      float v = 0.f;
-      if (n < g.N && k < g.K) v = TB ? Bg[static_cast<size_t>(n) * g.ldb + k]
-                                     : Bg[static_cast<size_t>(k) * g.ldb + n];
-      Bs[kk][nn] = v;
+  };
+  auto store = [&](int buf, const float4& av, const float4& bv) {
+    As[buf][ak + 0][ar] = av.x;
+    As[buf][ak + 1][ar] = av.y;
+    As[buf][ak + 2][ar] = av.z;
+    As[buf][ak + 3][ar] = av.w;
+    if (TB) {
+      Bs[buf][ak + 0][ar] = bv.x;
+      Bs[buf][ak + 1][ar] = bv.y;
+      Bs[buf][ak + 2][ar] = bv.z;
+      Bs[buf][ak + 3][ar] = bv.w;
+    } else {
+      *reinterpret_cast<float4*>(&Bs[buf][bk][bc]) = bv;
     }
+  };
+  float acc[8][8] = {};
+  if (kbeg < kend) {
+    float4 av, bv;
+    load(kbeg, av, bv);
+    store(0, av, bv);
     __syncthreads();
+    int buf = 0;
+    for (int k0 = kbeg; k0 < kend; k0 += kSgK) {
+      const bool more = k0 + kSgK < kend;
+      if (more) load(k0 + kSgK, av, bv);
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk) {
-      float a[4], b[4];
+      for (int kk = 0; kk < kSgK; ++kk) {
+        float a[8], b[8];
+        *reinterpret_cast<float4*>(&a[0]) = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
+        *reinterpret_cast<float4*>(&a[4]) = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
+        *reinterpret_cast<float4*>(&b[0]) = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
+        *reinterpret_cast<float4*>(&b[4]) = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+      }
+      if (more) store(buf ^ 1, av, bv);
+      __syncthreads();
+      buf ^= 1;
     }
-    __syncthreads();
   }
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int m = m0 + ty * 4 + i;
+  for (int i = 0; i < 8; ++i) {
+    const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
     if (m >= g.M) continue;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int n = n0 + tx * 4 + j;
+    for (int h = 0; h < 2; ++h) {
+      const int n = n0 + h * 64 + tx * 4;
       if (n >= g.N) continue;
-      float* c = Cg + static_cast<size_t>(m) * g.ldc + n;
-      *c = g.alpha * acc[i][j] + (g.beta != 0.f ? g.beta * *c : 0.f);
+      float4* c = reinterpret_cast<float4*>(Cg + static_cast<size_t>(m) * g.ldc + n);
+      float4 o = make_float4(g.alpha * acc[i][4 * h], g.alpha * acc[i][4 * h + 1],
+                             g.alpha * acc[i][4 * h + 2], g.alpha * acc[i][4 * h + 3]);
+      if (g.beta != 0.f) {
+        const float4 cv = *c;
+        o.x = fmaf(g.beta, cv.x, o.x);
+        o.y = fmaf(g.beta, cv.y, o.y);
+        o.z = fmaf(g.beta, cv.z, o.z);
+        o.w = fmaf(g.beta, cv.w, o.w);
+      }
+      *c = o;
     }
   }
 }
 
-cudaError_t sgemm(bool ta, bool tb, const SgemmArgs& g, cudaStream_t s) {
+cudaError_t sgemm(bool tb, const SgemmArgs& g, cudaStream_t s) {
   if (g.M <= 0 || g.N <= 0) return cudaSuccess;
-  dim3 grid((g.N + 63) / 64, (g.M + 63) / 64, g.batch);
-  if (!ta && !tb) sgemm_kernel<false, false><<<grid, 256, 0, s>>>(g);
-  else if (!ta && tb) sgemm_kernel<false, true><<<grid, 256, 0, s>>>(g);
-  else if (ta && !tb) sgemm_kernel<true, false><<<grid, 256, 0, s>>>(g);
-  else sgemm_kernel<true, true><<<grid, 256, 0, s>>>(g);
+  dim3 grid((g.N + kSgT - 1) / kSgT, (g.M + kSgT - 1) / kSgT, g.batch);
+  if (tb) sgemm_kernel<true><<<grid, 256, 0, s>>>(g);
+  else sgemm_kernel<false><<<grid, 256, 0, s>>>(g);
   return cudaGetLastError();
 }
 
@@ -330,21 +418,38 @@ __global__ void split2_kernel(const float* X, int64_t n, __nv_bfloat16* hi, __nv
   lo[t] = l;
 }
 
-// A' [L*d_out, 3d] = [hi(c) | hi(c) | lo(c)],  c[o, k] = s_k (C[o, k] - n mu_y[o] mu_x[k])
+// A' [L*d_out, 3d] = [hi(c) | hi(c) | lo(c)],  c[o, k] = s_k (C[o, k] - n mu_y[o] mu_x[k]);
+// eight consecutive k per thread (d is a multiple of 128): 64-byte reads of C,
+// 16-byte stores of each part
 __global__ void split_rhs_kernel(const double* C, const double* sy, const double* count,
                                  const double* mu_x, const float* s, int64_t rows_out, int d,
                                  __nv_bfloat16* Ap) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= rows_out * d) return;
-  const int64_t o = t / d, k = t % d;
-  // n mu_y[o] mu_x[k] = sy[o] mu_x[k]
-  const float v = static_cast<float>(fma(-sy[o], mu_x[k], C[t])) * s[k];
-  __nv_bfloat16 hi, lo;
-  split_bf16(v, hi, lo);
+  const int g = d / 8;
+  if (t >= rows_out * g) return;
+  const int64_t o = t / g;
+  const int k0 = static_cast<int>(t % g) * 8;
+  const double2* c2 = reinterpret_cast<const double2*>(C + o * d + k0);
+  const double syo = sy[o];  // n mu_y[o] mu_x[k] = sy[o] mu_x[k]
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const double2 c = c2[j];
+    const float v0 = static_cast<float>(fma(-syo, mu_x[k0 + 2 * j], c.x)) * s[k0 + 2 * j];
+    const float v1 = static_cast<float>(fma(-syo, mu_x[k0 + 2 * j + 1], c.y)) * s[k0 + 2 * j + 1];
+    __nv_bfloat16 h0, l0, h1, l1;
+    split_bf16(v0, h0, l0);
+    split_bf16(v1, h1, l1);
+    hw[j] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
+            (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
+    lw[j] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
+            (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+  }
   __nv_bfloat16* row = Ap + o * 3 * d;
-  row[k] = hi;
-  row[d + k] = hi;
-  row[2 * d + k] = lo;
+  const uint4 h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  *reinterpret_cast<uint4*>(row + k0) = h;
+  *reinterpret_cast<uint4*>(row + d + k0) = h;
+  *reinterpret_cast<uint4*>(row + 2 * d + k0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
 }
 
 // b[o] = mu_y[o] - sum_t part[o, t]
@@ -361,7 +466,7 @@ __global__ void bias_kernel(const double* sy, const double* count, const float* 
 struct FitPlan {
   size_t off_gh = 0, off_s = 0, off_mu32 = 0, off_mu64 = 0, off_alpha = 0,
          off_xhi = 0, off_xlo = 0, off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0,
-         off_cs = 0, total = 0;
+         off_cs = 0, off_linv = 0, total = 0;
   int bn = 0;
   int slabs = 0;
   int64_t slab_rows = 0;
@@ -398,6 +503,7 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->off_mu32 = off;  off = align_up(off + d * 4, 256);
     pl->off_mu64 = off;  off = align_up(off + d * 8, 256);
     pl->off_alpha = off; off = align_up(off + 8, 256);
+    pl->off_linv = off;  off = align_up(off + kNB * kNB * 4, 256);
     pl->off_xhi = off;   off = align_up(off + d * d * 2, 256);
     pl->off_xlo = off;   off = align_up(off + d * d * 2, 256);
     pl->off_gi = off;    off = align_up(off + d * d * 8, 256);
@@ -432,9 +538,11 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   p.gram_x_tiles = d / kBM;
   p.gram_y_tiles_per_layer = dout / kBM;
   p.m_tiles = p.gram_x_tiles + (Y != nullptr ? L * p.gram_y_tiles_per_layer : 0);
-  // pairs take 512-column tiles where d allows: each A stage then feeds two MMAs, which
-  // halves the A reads per flop
-  p.bn = (kGramPairs && d % kGramWideCols == 0) ? kGramWideCols : bn;
+  // pairs take 512-column tiles where d allows and the tiles fill eight waves: each A
+  // stage then feeds two MMAs, which halves the A reads per flop
+  const int64_t wide_tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * (d / kGramWideCols);
+  const bool wide = kGramPairs && d % kGramWideCols == 0 && wide_tiles >= 8 * (sm_count() / 2);
+  p.bn = wide ? kGramWideCols : bn;
   p.n_tiles = d / p.bn;
   p.batches = 1;
   p.group_m = 16;
@@ -508,15 +616,16 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
 
   // blocked Cholesky, lower factor in place
   const int nb = d / kNB;
+  float* linv = reinterpret_cast<float*>(ws + pl.off_linv);
   for (int kb = 0; kb < nb; ++kb) {
-    potrf_diag_kernel<<<1, kNB, 0, s>>>(Gh, d, kb, err);
+    potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb, err, linv);
     if (kb + 1 < nb) {
-      trsm_panel_kernel<<<nb - kb - 1, 256, 0, s>>>(Gh, d, kb);
+      trsm_panel_kernel<<<nb - kb - 1, 256, 0, s>>>(Gh, d, kb, linv);
       const int rem = d - (kb + 1) * kNB;
       const float* panel = Gh + static_cast<size_t>(kb + 1) * kNB * d + static_cast<size_t>(kb) * kNB;
       float* trail = Gh + static_cast<size_t>(kb + 1) * kNB * d + static_cast<size_t>(kb + 1) * kNB;
       SgemmArgs g{rem, rem, kNB, -1.f, 1.f, panel, d, panel, d, trail, d, 1, 0, 0};
-      if ((e = sgemm(false, true, g, s)) != cudaSuccess) return cuda_fail(e, "Cholesky update");
+      if ((e = sgemm(true, g, s)) != cudaSuccess) return cuda_fail(e, "Cholesky update");
     }
   }
   zero_upper_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gh, d);
@@ -542,10 +651,10 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
       float* x21 = Gh + static_cast<size_t>(b0 + sz) * d + b0;
       SgemmArgs g1{s2, sz, sz, 1.f, 0.f, l21, d, x11, d, T, sz, 0, 1, 0};   // T = L_21 X_11
       g1.batch = cnt; g1.sa = step; g1.sb = step; g1.sc = static_cast<int64_t>(sz) * sz;
-      if ((e = sgemm(false, false, g1, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
+      if ((e = sgemm(false, g1, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
       SgemmArgs g2{s2, sz, s2, -1.f, 0.f, x22, d, T, sz, x21, d, 0, 0, 1};  // X_21 = -X_22 T
       g2.batch = cnt; g2.sa = step; g2.sb = static_cast<int64_t>(sz) * sz; g2.sc = step;
-      if ((e = sgemm(false, false, g2, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
+      if ((e = sgemm(false, g2, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
     }
   }
   // G^-1 = X^T X on the tensor cores: three MN-major Gram products of the bf16
@@ -559,7 +668,7 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   if ((st = launch_gram(Xlo, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
 
   split_ginv_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gi, d, Bp);
-  split_rhs_kernel<<<static_cast<unsigned>((M * d + 255) / 256), 256, 0, s>>>(
+  split_rhs_kernel<<<static_cast<unsigned>((M * (d / 8) + 255) / 256), 256, 0, s>>>(
       a->C, a->sy, a->count, mu64, sc, M, d, Ap);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "operand split launch");
 
@@ -569,8 +678,9 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   const uint64_t krow = static_cast<uint64_t>(3 * d) * 2;
   bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap, 3 * d, M, 1, krow, 0, kBK,
                          kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  // on CTA pairs: each CTA stages half of the tile's B rows
   ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, 3 * d, d, 1, krow, 0,
-                          kBK, pl.bn, CU_TENSOR_MAP_SWIZZLE_128B);
+                          kBK, pl.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the solve GEMM");
   p.m_tiles = static_cast<int32_t>(ceil_div(M, kBM));
   p.bn = pl.bn;
@@ -585,9 +695,9 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   p.bias_part = part;
   p.out_ld = d;
   p.err = err;
-  const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-  const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-  if ((e = launch_gemm(p, grid, s)) != cudaSuccess) return cuda_fail(e, "solve GEMM launch");
+  const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+  const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  if ((e = launch_gemm2(p, pairs, s)) != cudaSuccess) return cuda_fail(e, "solve GEMM launch");
   bias_kernel<<<static_cast<unsigned>((M + 255) / 256), 256, 0, s>>>(a->sy, a->count, part,
                                                                      p.n_tiles, M, a->b_out);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "offset launch");
