@@ -126,63 +126,94 @@ __global__ void equilibrate_kernel(const double* G, const double* count, const d
 // One 64x64 diagonal block: the lower factor L_kk in place (zeros above) and its
 // inverse into Linv [64, 64] (lower), both right-looking in one sweep over the
 // columns j: the pivot, column j of L and row j of L^-1 scaled by its reciprocal,
-// then the rank-1 updates of the trailing lower triangle and of the rows of L^-1
-// below j.  A pivot <= 0 records kErrNumeric in the device error word and
-// continues with pivot 1.  256 threads as 16 x 16; each step's loops cover only
-// the cells that change, so the work shrinks with the triangle.
+// then the rank-1 updates a_ik -= l_ij l_kj and x_ic -= l_ij x_jc.  A pivot <= 0
+// records kErrNumeric in the device error word and continues with pivot 1.
+// 256 threads, ti = tid % 16, tk = tid / 16, all cells in registers: thread
+// (ti, tk) keeps a_ik for rows i = ti + 16u and columns k = tk + 16v, and x_ic
+// transposed, rows i = tk + 16v and columns c = ti + 16u, so column j of L and
+// row j of L^-1 both sit in the sixteen threads tk = j % 16 (half a warp).  They
+// take the pivot's square root and reciprocal themselves and publish the column
+// and the row through shared memory with zeros outside i > j and c <= j.  The
+// updates then need no masks: the zeros leave every other cell unchanged, and
+// only the (never read) upper triangle of a takes stray updates.  The owner of
+// the next diagonal cell publishes it after the update: two barriers a step.
 __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int kb, int* err,
                                                          float* Linv) {
-  __shared__ float a[kNB][kNB + 1];
-  __shared__ float x[kNB][kNB + 1];
-  __shared__ float rpiv;
+  __shared__ float col[kNB];   // l_ij for i > j, else 0
+  __shared__ float xrow[kNB];  // x_jc for c <= j, else 0
+  __shared__ float diag;       // a_jj before its square root
   float* blk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
-  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
-  {
-    float v[16];  // all loads in flight before the shared-memory stores
+  const int tid = threadIdx.x, ti = tid & 15, tk = tid >> 4;
+  float a[4][4], x[4][4];
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int e = tid + 256 * q;
-      v[q] = blk[static_cast<size_t>(e / kNB) * ld + e % kNB];
-    }
+  for (int u = 0; u < 4; ++u)
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int e = tid + 256 * q, r = e / kNB, c = e % kNB;
-      a[r][c] = v[q];
-      x[r][c] = r == c ? 1.f : 0.f;
+    for (int v = 0; v < 4; ++v) {
+      a[u][v] = blk[static_cast<size_t>(ti + 16 * u) * ld + tk + 16 * v];
+      x[v][u] = (tk + 16 * v == ti + 16 * u) ? 1.f : 0.f;
     }
-  }
+  if (tid == 0) diag = a[0][0];
   __syncthreads();
-  for (int j = 0; j < kNB; ++j) {
-    if (tid == 0) {
-      float v = a[j][j];
-      if (!(v > 0.f)) {
-        atomicCAS(err, 0, kErrNumeric);
-        v = 1.f;
+  // j = 16 jw + jt with jw unrolled, so every register index below is static
+#pragma unroll
+  for (int jw = 0; jw < 4; ++jw) {
+    for (int jt = 0; jt < 16; ++jt) {
+      const int j = 16 * jw + jt;
+      if (tk == jt) {  // column j of L (a[u][jw]) and row j of L^-1 (x[jw][u])
+        float v = diag;
+        if (!(v > 0.f)) {
+          if (ti == 0) atomicCAS(err, 0, kErrNumeric);
+          v = 1.f;
+        }
+        const float p = sqrtf(v), r = 1.f / p;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int i = ti + 16 * u;  // row of a, column of x
+          float lv = 0.f, xv = 0.f;
+          if (i > j) {
+            a[u][jw] *= r;
+            lv = a[u][jw];
+          } else {
+            if (i == j) a[u][jw] = p;
+            x[jw][u] *= r;
+            xv = x[jw][u];
+          }
+          col[i] = lv;
+          xrow[i] = xv;
+        }
       }
-      const float p = sqrtf(v);
-      a[j][j] = p;
-      rpiv = 1.f / p;
+      __syncthreads();
+      float ci[4], xr[4], ck[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        ci[u] = col[ti + 16 * u];
+        xr[u] = xrow[ti + 16 * u];
+        ck[u] = col[tk + 16 * u];
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          a[u][v] = fmaf(-ci[u], ck[v], a[u][v]);
+          x[v][u] = fmaf(-ck[v], xr[u], x[v][u]);
+        }
+      // the owner of the next diagonal cell publishes it
+      const int jn = (j + 1) & 15;
+      if (ti == jn && tk == jn) {
+        if (jt < 15) diag = a[jw][jw];
+        else if (jw < 3) diag = a[jw < 3 ? jw + 1 : 3][jw < 3 ? jw + 1 : 3];
+      }
+      __syncthreads();
     }
-    __syncthreads();
-    if (tid < kNB) {
-      const float r = rpiv;
-      if (tid > j) a[tid][j] *= r;  // column j of L
-      else x[j][tid] *= r;          // row j of L^-1 (columns <= j) is final
-    }
-    __syncthreads();
-    for (int i = j + 1 + ty; i < kNB; i += 16) {
-      const float li = a[i][j];
-      for (int k = j + 1 + tx; k <= i; k += 16) a[i][k] = fmaf(-li, a[k][j], a[i][k]);
-      for (int c = tx; c <= j; c += 16) x[i][c] = fmaf(-li, x[j][c], x[i][c]);
-    }
-    __syncthreads();
   }
-#pragma unroll 4
-  for (int q = 0; q < 16; ++q) {
-    const int e = tid + 256 * q, r = e / kNB, c = e % kNB;
-    blk[static_cast<size_t>(r) * ld + c] = c <= r ? a[r][c] : 0.f;
-    Linv[e] = c <= r ? x[r][c] : 0.f;
-  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      const int i = ti + 16 * u, k = tk + 16 * v;
+      blk[static_cast<size_t>(i) * ld + k] = k <= i ? a[u][v] : 0.f;
+      Linv[k * kNB + i] = i <= k ? x[v][u] : 0.f;  // x cell: row k, column i
+    }
 }
 
 // Panel: A_ik <- A_ik L_kk^-T = A_ik Linv^T for block rows i > kb (one 64x64 block
