@@ -46,11 +46,12 @@ def _gpu_fit(X, Y, lam, batches=(None,)):
     return sums, A32.cpu().double().numpy(), A16, b.cpu().double().numpy(), float(alpha.item())
 
 
-# d = 256 takes 256-column Gram tiles; d = 512 and 1024 take 512-column tiles (one and two
-# column tiles), d_out = 384 leaves the last CTA pair half empty, and 777 rows end in a
-# ragged 64-row block
+# Gram tiles: 256 columns (d = 256, and small products at d = 512 and 1024); 512 columns on
+# clusters of two CTA pairs once the tiles fill eight waves of pairs (d = 1024 with 201 layers
+# of d_out = 384: an odd row-tile count leaves the last pair of the last cluster half empty);
+# 777 and 300 rows end in ragged 64-row blocks
 @pytest.mark.parametrize("d,L,n,d_out,cut", [(256, 3, 1000, 256, 600), (1024, 2, 777, 1024, 320),
-                                             (512, 1, 300, 384, 128)])
+                                             (512, 1, 300, 384, 128), (1024, 201, 300, 384, 100)])
 def test_sums_match_oracle_and_split_batches(d, L, n, d_out, cut):
     cal = calibration(d=d, n_layers=L, n=n, seed=40 + d)
     X, Y = cal["X"], cal["Y"][:, :, :d_out].contiguous()
