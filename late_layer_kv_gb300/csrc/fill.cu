@@ -80,9 +80,6 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   pl->total = align_up(pl->off_rope + rope, 256);
 }
 
-// K/V GEMM on CTA pairs (true) or single CTAs
-constexpr bool kKvPairs = true;
-
 // RoPE angles of one row chunk (rotate-half pairs, frequency f_i = theta^(-2i/hd)):
 // tab[i * ld + r] = (cos, sin) of (pos0 + position of row r) * f_i.  The angle is
 // formed and reduced modulo 2 pi in f64, then its cos and sin taken in f32.
@@ -143,7 +140,7 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xhat, a->d_out, rc,
                          a->n_layers, drow, drow * pl.R, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   // pair kernel: B boxes of bn / 2 rows (each CTA of a pair stages half of a tile's columns)
-  const uint32_t bbox = kKvPairs ? pl.bn_kv / 2 : pl.bn_kv;
+  const uint32_t bbox = pl.bn_kv / 2;  // each CTA of a pair stages half of the B rows
   ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wk, a->d_out, kvw,
                           a->n_layers, drow, drow * kvw, kBK, bbox, CU_TENSOR_MAP_SWIZZLE_128B);
   ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wv, a->d_out, kvw,
@@ -190,18 +187,10 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   }
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
-  cudaError_t e;
-  if (kKvPairs) {
-    const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles * p.batches;
-    const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
-    if (pairs <= 0) return RF_OK;
-    e = launch_gemm2(p, pairs, s);
-  } else {
-    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles * p.batches;
-    const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-    if (grid <= 0) return RF_OK;
-    e = launch_gemm(p, grid, s);
-  }
+  const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles * p.batches;
+  const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  if (pairs <= 0) return RF_OK;
+  const cudaError_t e = launch_gemm2(p, pairs, s);
   if (e != cudaSuccess) return cuda_fail(e, "K/V GEMM launch");
   return RF_OK;
 }

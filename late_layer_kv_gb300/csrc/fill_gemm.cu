@@ -47,18 +47,6 @@ __device__ __forceinline__ void rope_cs(float posf, float fhi, float flo, float&
   sincosf(r, &s, &c);
 }
 
-__device__ __forceinline__ void decode_tile(int t, const GemmParams& p, int& m, int& n, int& b) {
-  const int per_b = p.m_tiles * p.n_tiles;
-  b = t / per_b;
-  const int r = t - b * per_b;
-  const int gsz = p.group_m * p.n_tiles;
-  const int g = r / gsz;
-  const int first_m = g * p.group_m;
-  const int gm = min(p.m_tiles - first_m, p.group_m);
-  const int rr = r - g * gsz;
-  m = first_m + rr % gm;
-  n = rr / gm;
-}
 
 // Which B segment a tile reads and its MMA width.
 struct TileB {
@@ -467,195 +455,8 @@ __device__ void epilogue_solve(const GemmParams& p, uint32_t tcol, int q, int la
 
 }  // namespace
 
-__global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_constant__ GemmParams p) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;
-  uint8_t* sB = sA + kStages * kABytes;
-  uint8_t* stg_all = sB + kStages * kBBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stg_all + 4 * kOutWarpBytes);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
-    }
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    tma_prefetch(&p.tmA);
-    tma_prefetch(&p.tmB[0]);
-    if (p.mode == kModeKV || p.mode == kModeGdnProj) tma_prefetch(&p.tmB[1]);
-    if (p.mode == kModeGram) tma_prefetch(&p.tmA2);
-  }
-  if (warp == 2) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  const int total = p.m_tiles * p.n_tiles * p.batches;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      // ---------------- TMA producer
-      uint32_t stage = 0, phase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        int m, n, b;
-        decode_tile(t, p, m, n, b);
-        const TileB tb = tile_b(p, n);
-        const uint32_t bytes = kABytes + tb.bn * kBK * 2;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrProducer)) {
-            ok = false;
-            break;
-          }
-          mbar_expect_tx(&full[stage], bytes);
-          uint8_t* bdst = sB + stage * kBBytes;
-          if (p.mode == kModeGram) {
-            // MN-major operands: 64-wide column blocks of [rows, width] arrays, 64 rows of K
-            uint8_t* adst = sA + stage * kABytes;
-            if (m < p.gram_x_tiles) {
-              for (int j = 0; j < kBM / 64; ++j)
-                tma_load_3d(smem_u32(adst + j * 8192), &p.tmA, &full[stage], m * kBM + 64 * j,
-                            kb * kBK, 0);
-            } else {
-              const int mm = m - p.gram_x_tiles;
-              const int l = mm / p.gram_y_tiles_per_layer;
-              const int m0 = (mm % p.gram_y_tiles_per_layer) * kBM;
-              for (int j = 0; j < kBM / 64; ++j)
-                tma_load_3d(smem_u32(adst + j * 8192), &p.tmA2, &full[stage], m0 + 64 * j,
-                            kb * kBK, l);
-            }
-            for (int j = 0; j < tb.bn / 64; ++j)
-              tma_load_3d(smem_u32(bdst + j * 8192), &p.tmB[0], &full[stage], tb.nrow + 64 * j,
-                          kb * kBK, 0);
-          } else {
-            tma_load_3d(smem_u32(sA + stage * kABytes), &p.tmA, &full[stage], kb * kBK, m * kBM, b);
-          }
-          if (p.mode == kModeGram) {
-            // loaded above
-          } else if (tb.seg < 2) {
-            tma_load_3d(smem_u32(bdst), &p.tmB[tb.seg], &full[stage], kb * kBK, tb.nrow, b);
-          } else {
-            tma_load_3d(smem_u32(bdst), &p.tmB[2], &full[stage], kb * kBK, 0, b);
-            tma_load_3d(smem_u32(bdst + p.gdn_heads * 128), &p.tmB[3], &full[stage], kb * kBK, 0, b);
-          }
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ---------------- MMA issuer
-      uint32_t stage = 0, phase = 0;
-      int it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        int m, n, b;
-        decode_tile(t, p, m, n, b);
-        const TileB tb = tile_b(p, n);
-        const bool mn = p.mode == kModeGram;
-        const uint32_t idesc = idesc_bf16_f32(kBM, tb.bn) | (mn ? (3u << 15) : 0u);
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, kErrMma)) break;
-        tc_fence_after();
-        const uint32_t dt = tmem_base + acc * kBNMax;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.err, kErrMma)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (!mn) {
-            const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * kABytes));
-            const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * kBBytes));
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              // advance 16 bf16 (32 B) along K inside the swizzled 128-byte row
-              mma_bf16(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-            }
-          } else {
-            // MN-major: 64-element column blocks 8 KB apart, K rows 128 B apart
-            const uint64_t ad = sdesc_mnmajor_sw128(smem_u32(sA + stage * kABytes), 8192);
-            const uint64_t bd = sdesc_mnmajor_sw128(smem_u32(sB + stage * kBBytes), 8192);
-#pragma unroll
-            for (int k = 0; k < kBK / 16; ++k) {
-              // advance 16 K rows (2048 B)
-              mma_bf16(dt, ad + 128 * k, bd + 128 * k, idesc, (kb | k) != 0 ? 1u : 0u);
-            }
-          }
-          mma_commit(&empty[stage]);
-          if (++stage == kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
-        }
-        if (ok) mma_commit(&tfull[acc]);
-      }
-    }
-  } else if (warp >= 4) {
-    // ---------------- epilogue warpgroup
-    const int q = warp - 4;
-    uint8_t* stg = stg_all + q * kOutWarpBytes;
-    int it = 0;
-    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      int m, n, b;
-      decode_tile(t, p, m, n, b);
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
-      // the row's RMS scale (from the sum-of-squares partials) is loaded before
-      // the accumulator is waited for
-      float rs = 1.f;
-      if (p.mode == kModeKV || p.mode == kModeGdnProj) rs = row_rms_scale(p, b, m * kBM + q * 32 + lane);
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, kErrEpilogue)) break;
-      tc_fence_after();
-      const uint32_t tcol = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kBNMax;
-      if (p.mode == kModeMap) {
-        epilogue_map(p, tcol, stg, q, lane, m, n, smem_u32(&tempty[acc]));
-      } else if (p.mode == kModeKV) {
-        epilogue_kv(p, tcol, stg, q, lane, m, n, b, rs, smem_u32(&tempty[acc]));
-      } else if (p.mode == kModeGdnProj) {
-        epilogue_gdn(p, tcol, stg, q, lane, m, n, b, rs, smem_u32(&tempty[acc]));
-      } else if (p.mode == kModeGram) {
-        epilogue_gram(p, tcol, q, lane, m, n, smem_u32(&tempty[acc]));
-      } else {
-        epilogue_solve(p, tcol, q, lane, m, n, smem_u32(&tempty[acc]));
-      }
-    }
-    if (lane == 0) bulk_wait_all<0>();
-    __syncwarp();
-  }
-  __syncthreads();
-  if (warp == 2) {
-    tc_fence_after();
-    tmem_dealloc(tmem_base, 512);
-  }
-}
-
 // ------------------------------------------------------------------ CTA pairs
-// Map, K/V and GDN projection modes on CTA pairs (clusters of 2): the pair computes a 256-row x
+// Every mode runs on CTA pairs (clusters of 2): the pair computes a 256-row x
 // bn-column tile with tcgen05.mma.cta_group::2.  Each CTA stages its 128 rows
 // of A and its bn / 2 rows of B (up to 32 KB a stage, six stages); the MMA of CTA 0 reads
 // both CTAs' halves and writes each CTA's 128 accumulator rows into its own
@@ -664,8 +465,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1) rf_gemm_kernel(const __grid_c
 // accumulator on CTA 0's `tempty` barrier.
 constexpr int kStages2 = 6;
 constexpr int kHalfBytes = 128 * kBK * 2;  // 128 rows x 64 K of bf16
-// Wide Gram tiles (bn = kGramWideCols): the pair accumulates 256 x 512 in both TMEM halves with two
-// N = 256 MMAs per K step that share one A stage.  A stage then holds this CTA's A half and
+// Wide Gram tiles (bn = kGramWideCols): the pair accumulates 256 x 512 in both TMEM
+// halves with two N = 256 MMAs per K step that share one A stage.  A stage then holds this CTA's A half and
 // its two B quarters (48 KB), four stages in the space of the six narrow ones.
 constexpr int kWideStageBytes = 3 * kHalfBytes;
 constexpr int kStagesWide = 4;
@@ -1176,14 +977,5 @@ cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream)
   return cudaGetLastError();
 }
 
-cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream) {
-  // set on every launch: the attribute belongs to the current device, and the call is
-  // cheap next to the kernel
-  cudaError_t e = cudaFuncSetAttribute(rf_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kGemmSmem);
-  if (e != cudaSuccess) return e;
-  rf_gemm_kernel<<<grid, kGemmThreads, kGemmSmem, stream>>>(p);
-  return cudaGetLastError();
-}
 
 }  // namespace rf

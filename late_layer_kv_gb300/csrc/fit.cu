@@ -549,8 +549,7 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
 // arrays Xa, Xb ([rows, d], MN-major), and, if Y is given, out_C[l, o, n] +=
 // sum_k Y[l, k, o] Xb[k, n].
 // Gram products on CTA pairs (M = 256: each CTA stages 128 columns of [X | Y] and half of
-// the tile's X columns) or on single CTAs
-constexpr bool kGramPairs = true;
+// the tile's X columns).
 
 rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int64_t rows, int d,
                       int dout, int bn, double* out_G, double* out_C, cudaStream_t s) {
@@ -572,7 +571,7 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   // pairs take 512-column tiles where d allows and the tiles fill eight waves: each A
   // stage then feeds two MMAs, which halves the A reads per flop
   const int64_t wide_tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * (d / kGramWideCols);
-  const bool wide = kGramPairs && d % kGramWideCols == 0 && wide_tiles >= 8 * (sm_count() / 2);
+  const bool wide = d % kGramWideCols == 0 && wide_tiles >= 8 * (sm_count() / 2);
   p.bn = wide ? kGramWideCols : bn;
   p.n_tiles = d / p.bn;
   p.batches = 1;
@@ -583,23 +582,18 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   p.gram_ld = d;
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
-  cudaError_t e;
   const int max_cl4 = wide ? gemm2_cl4_max_clusters() : 0;
-  if (kGramPairs && max_cl4 > 0) {
+  cudaError_t e;
+  if (max_cl4 > 0) {
     // two pairs per cluster share each B panel; as many clusters as can be resident
     const int64_t tiles = static_cast<int64_t>((p.m_tiles + 3) / 4) * p.n_tiles;
     const int clusters = static_cast<int>(tiles < max_cl4 ? tiles : max_cl4);
     e = launch_gemm2_cl4(p, clusters, s);
-  } else if (kGramPairs) {
+  } else {
     const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
     const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
     if (pairs <= 0) return RF_OK;
     e = launch_gemm2(p, pairs, s);
-  } else {
-    const int64_t tiles = static_cast<int64_t>(p.m_tiles) * p.n_tiles;
-    const int grid = static_cast<int>(tiles < sm_count() ? tiles : sm_count());
-    if (grid <= 0) return RF_OK;
-    e = launch_gemm(p, grid, s);
   }
   if (e != cudaSuccess) return cuda_fail(e, "Gram GEMM launch");
   return RF_OK;

@@ -9,19 +9,18 @@
 namespace rf {
 
 // ------------------------------------------------------------ GEMM tiling
-constexpr int kStages = 4;         // TMA -> MMA shared-memory ring depth
-constexpr int kBM = 128;           // rows per tile (one TMEM lane per row)
+constexpr int kBM = 128;           // rows per CTA (one TMEM lane per row)
 constexpr int kBK = 64;            // K elements per stage (one 128-byte row)
 constexpr int kBNMax = 256;        // max columns per tile (TMEM cols per accumulator)
 constexpr int kGramWideCols = 512; // Gram tiles on CTA pairs: both accumulators, one tile
-constexpr int kABytes = kBM * kBK * 2;
-constexpr int kBBytes = kBNMax * kBK * 2;
 constexpr int kOutBoxBytes = 64 * 32 * 2;   // one 64-col x 32-row bf16 store box
 constexpr int kOutWarpBytes = 2 * kOutBoxBytes;
 constexpr int kGemmThreads = 256;  // warp 0 TMA, warp 1 MMA, warp 2 TMEM, warps 4-7 epilogue
 constexpr int kGemmThreadsQ8 = 512;  // int8 maps: warps 8-15 convert the B operand
 constexpr int kQ8Group = 128;        // map weights of a row that share one bf16 scale
-constexpr int kGemmSmem = 1024 + kStages * (kABytes + kBBytes) + 4 * kOutWarpBytes + 256;
+// dynamic shared memory of the pair GEMM kernels (the stage rings, epilogue staging,
+// barriers and 1 KB of alignment slack), within the 227 KB a CTA may use
+constexpr int kGemmSmem = 1024 + 4 * (kBM * kBK * 2 + kBNMax * kBK * 2) + 4 * kOutWarpBytes + 256;
 
 enum GemmMode : int {
   kModeMap = 0,      // X_hat = H A^T + b (times gain), row sums of squares
@@ -127,9 +126,8 @@ struct GemmParams {
   float inv_freq_lo[64];
 };
 
-cudaError_t launch_gemm(const GemmParams& p, int grid, cudaStream_t stream);
-// map, K/V and GDN projection modes on CTA pairs (B tensor maps with boxes of half a
-// tile's columns); `pairs` clusters of 2
+// every mode on CTA pairs (B tensor maps with boxes of half a tile's columns); `pairs`
+// clusters of 2
 cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream);
 // map mode on CTA pairs with int8 maps (p.q8, p.q8_scale); tmB unused
 cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream);
