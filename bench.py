@@ -45,14 +45,18 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 N_SM = 152
 FP32_LANES_PER_SM = 128
 
-# DRAM bytes per launch of the dominant kernel from an ncu capture, valid only
-# for the kernel source with this digest (otherwise reported as null).
-# dram__bytes_read.sum + dram__bytes_write.sum of one full-size map-GEMM launch
-# (ncu, one pass; profiles/fill_launches_llama8b_16k.md), valid while the
-# library sources hash to kernel_sha256.
+# DRAM bytes per launch of the dominant kernel from an ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum, one pass, full size), keyed by the bench line's workload and valid
+# only while the library sources that define that kernel hash to kernel_sha256 (otherwise
+# reported as null).  Captures: profiles/fill_launches_llama8b_16k.md (map GEMM) and
+# profiles/fit_launches_llama8b_rows65536.md (Gram accumulate).
 PROFILED_TRAFFIC = {
-    "llama8b_16k": {"kernel_sha256": "2aa20fb2c123f5198a5bc2b4d3d8d451ce87bc0c98e5adb0c727d01304e36422",
+    "llama8b_16k": {"sources": "fill",
+                    "kernel_sha256": "2aa20fb2c123f5198a5bc2b4d3d8d451ce87bc0c98e5adb0c727d01304e36422",
                     "bytes_per_launch": 7293371904 + 2353405184},
+    "hostmaps_16k_fit": {"sources": "fit",
+                         "kernel_sha256": "49521073e68f04a1613fa7e5547e6a7f1ed2836fe6852ffcaf9d0641549625d8",
+                         "bytes_per_launch": 105417109760 + 2812521728},
 }
 
 
@@ -64,16 +68,20 @@ def _peaks():
     return PEAKS_FALLBACK, "fallback"
 
 
-# Sources that define the attention fill's map GEMM and its launch: the recorded
-# traffic stays valid while these are unchanged.
-_FILL_SOURCES = ("abi_common.cu", "abi_common.h", "fill.cu", "fill_gemm.cu", "rf_internal.h",
-                 "sm103_ptx.cuh")
+# Sources that define each profiled kernel and its launch: the recorded traffic stays valid
+# while these are unchanged.
+_SOURCES = {
+    "fill": ("abi_common.cu", "abi_common.h", "fill.cu", "fill_gemm.cu", "rf_internal.h",
+             "sm103_ptx.cuh"),
+    "fit": ("abi_common.cu", "abi_common.h", "fit.cu", "fill_gemm.cu", "rf_internal.h",
+            "sm103_ptx.cuh"),
+}
 
 
-def _kernel_digest() -> str:
+def _kernel_digest(which: str = "fill") -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "late_layer_kv_gb300", "csrc")
-    for f in _FILL_SOURCES:
+    for f in _SOURCES[which]:
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(f.encode())
             h.update(fh.read())
@@ -723,8 +731,8 @@ def run_ours(args):
                         "frac": ach / pk}
     dom = max(stages, key=lambda k: stages[k]["ms"])
     traffic = None
-    pt = PROFILED_TRAFFIC.get(wl.shape.name)
-    if pt and pt["kernel_sha256"] == _kernel_digest():
+    pt = PROFILED_TRAFFIC.get(wl.config()["workload"])
+    if pt and pt["kernel_sha256"] == _kernel_digest(pt["sources"]):
         traffic = pt["bytes_per_launch"]
     dpk = tpeak if stages[dom]["bound"] == "tensor" else alu_peak
     roofline = {"bound": stages[dom]["bound"], "kernel": dom,
