@@ -592,16 +592,46 @@ class FitWorkload:
     def stage_ms(self, ev):
         return {"accumulate": ev[0].elapsed_time(ev[1]), "solve": ev[1].elapsed_time(ev[2])}
 
+    # e2e: the calibration pairs come from pinned host memory in row batches, each copied
+    # on a side stream into one of two device buffers while the previous batch is added to
+    # the sums (the running sums are additive over batches); then the solve, and the maps
+    # are read back.
+    E2E_BATCHES = 8
+
     def e2e_buffers(self):
+        s, n = self.shape, self.n
         self.X_host = self.X.cpu().pin_memory()
         self.Y_host = self.Y.cpu().pin_memory()
         self.A_host = torch.empty(self.A.shape, dtype=torch.bfloat16).pin_memory()
+        nbat = self.E2E_BATCHES if n % self.E2E_BATCHES == 0 else 1
+        self.rb = n // nbat
+        dev = self.X.device
+        self.Xb = [torch.empty((self.rb, s.d), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+        self.Yb = [torch.empty((s.n_layers, self.rb, s.d), dtype=torch.bfloat16, device=dev)
+                   for _ in range(2)]
+        self.cstream = torch.cuda.Stream(dev)
+        self.copied = [torch.cuda.Event() for _ in range(2)]
+        self.used = [torch.cuda.Event() for _ in range(2)]
         return (self.X_host.numel() + self.Y_host.numel()) * 2, self.A_host.numel() * 2
 
     def e2e_step(self, stream):
-        self.X.copy_(self.X_host, non_blocking=True)
-        self.Y.copy_(self.Y_host, non_blocking=True)
-        self.step(stream)
+        from late_layer_kv_gb300 import ridgefill_fit_accumulate, ridgefill_fit_solve
+        for t in (self.sums.G, self.sums.C, self.sums.sx, self.sums.sy, self.sums.count):
+            t.zero_()
+        rb = self.rb
+        for i, r0 in enumerate(range(0, self.n, rb)):
+            k = i % 2
+            self.cstream.wait_event(self.used[k])  # buffer k's previous batch was added
+            with torch.cuda.stream(self.cstream):
+                self.Xb[k].copy_(self.X_host[r0:r0 + rb], non_blocking=True)
+                for l in range(self.shape.n_layers):
+                    self.Yb[k][l].copy_(self.Y_host[l, r0:r0 + rb], non_blocking=True)
+                self.copied[k].record(self.cstream)
+            stream.wait_event(self.copied[k])
+            ridgefill_fit_accumulate(self.sums, self.Xb[k], self.Yb[k], stream=stream)
+            self.used[k].record(stream)
+        ridgefill_fit_solve(self.sums, self.shape.lam, A_out=self.A, b_out=self.b,
+                            workspace=self.ws, stream=stream)
         self.A_host.copy_(self.A, non_blocking=True)
 
     def cpu_rate(self, budget_flop):
