@@ -67,6 +67,26 @@ def test_sums_match_oracle_and_split_batches(d, L, n, d_out, cut):
     assert _rel(Cg, Co) < 2e-5
 
 
+def test_tiny_batches_add_exactly_what_they_hold():
+    """Batches of 0, 1, 63 and 65 rows (none, part of one 64-row block, one row past it) on
+    the clustered 512-column Gram path: the sums are those of the rows given."""
+    cal = calibration(d=1024, n_layers=201, n=129, seed=47)
+    X, Y = cal["X"], cal["Y"][:, :, :384].contiguous()
+    sums = FitSums(201, 1024, 384)
+    Xd, Yd = X.cuda(), Y.cuda()
+    bounds = [0, 0, 1, 64, 129]  # an empty batch, then 1, 63 and 65 rows
+    for lo, hi in zip(bounds[:-1], bounds[1:]):
+        ridgefill_fit_accumulate(sums, Xd[lo:hi].contiguous(), Yd[:, lo:hi].contiguous())
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    n, sx, sy, G, C = oracle.fit_sums(to_f64(X), to_f64(Y))
+    assert float(sums.count.item()) == n
+    np.testing.assert_allclose(sums.sx.cpu().numpy(), sx, rtol=1e-6, atol=1e-6 * np.abs(sx).max())
+    np.testing.assert_allclose(sums.sy.cpu().numpy(), sy, rtol=1e-6, atol=1e-6 * np.abs(sy).max())
+    assert _rel(sums.G.cpu().numpy(), G) < 1e-5
+    assert _rel(sums.C.cpu().numpy(), C.reshape(1024, 201, 384).transpose(1, 2, 0)) < 1e-5
+
+
 # d = 384 and 640 are not powers of two: the blocked inverse then merges a last,
 # shorter block pair
 @pytest.mark.parametrize("d,L,n,lam", [(256, 3, 1000, 1e-3), (512, 2, 4096, 3e-2),
