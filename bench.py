@@ -52,8 +52,8 @@ FP32_LANES_PER_SM = 128
 # profiles/fit_launches_llama8b_rows65536.md (Gram accumulate).
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "2aa20fb2c123f5198a5bc2b4d3d8d451ce87bc0c98e5adb0c727d01304e36422",
-                    "bytes_per_launch": 7293371904 + 2353405184},
+                    "kernel_sha256": "8a59e5fbe62497eb97bb9035ddf9d768cb55933cd22b4ebcbb423989c6d89882",
+                    "bytes_per_launch": 6729319424 + 2360831744},
     "hostmaps_16k_fit": {"sources": "fit",
                          "kernel_sha256": "49521073e68f04a1613fa7e5547e6a7f1ed2836fe6852ffcaf9d0641549625d8",
                          "bytes_per_launch": 105417109760 + 2812521728},
