@@ -950,7 +950,7 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
   p.n_tiles = H + 1;
   p.batches = a->n_layers;
   p.bn = 256;
-  p.group_m = 16;
+  p.group_m = 2;  // one pair row tile per group: every column tile of a row panel in turn
   p.rows = static_cast<int32_t>(rc);
   p.ss_stride = static_cast<int32_t>(pl.R);
   p.d_out = a->d_out;
