@@ -543,10 +543,21 @@ class FitWorkload:
         self.total_flops = sum(self.stage_work.values())
 
     def launches_per_step(self):
-        nb = self.shape.d // 64
-        # colsum x2, count, Gram; prep, equilibrate, Cholesky 3 per block, zero, trinv
-        # diag + 2 per block column, inverse product, 2 splits, solve GEMM, offsets
-        return 4 + 2 + (3 * nb - 2) + 1 + 1 + 2 * (nb - 1) + 1 + 2 + 1 + 1
+        d = self.shape.d
+        nb = d // 64
+        # triangular inverse by recursive doubling: two batched products per part of a level
+        inv, sz = 0, 64
+        while sz < d:
+            full = d // (2 * sz)
+            rest = d - full * 2 * sz
+            inv += 2 * ((1 if full > 0 else 0) + (1 if rest > sz else 0))
+            sz *= 2
+        # accumulate: two column-sum passes, their reduction, the count, the Gram products;
+        # solve: preparation, equilibration, Cholesky (diagonal block, panel, trailing
+        # update per block column), zero fill, diagonal-block inverses, the doubling
+        # products, the bf16 split, three G^-1 products, two operand splits, the solve GEMM,
+        # the offsets
+        return 5 + 2 + (3 * nb - 2) + 2 + inv + 1 + 3 + 2 + 1 + 1
 
     def setup(self, dev, seed):
         """Calibration pairs drawn on the device (torch Philox, seeded) in the
