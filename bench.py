@@ -36,8 +36,8 @@ import torch
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from synthetic import (WORKLOADS, FillShape, GdnShape, exact_rows, fill_inputs,  # noqa: E402
-                       gdn_inputs, tail_inputs, to_f64, true_inputs)
+from synthetic import (WORKLOADS, FillShape, GdnShape, calibration_device,  # noqa: E402
+                       exact_rows, fill_inputs, gdn_inputs, tail_inputs, to_f64, true_inputs)
 
 METRIC = "filled token-layers/s (fill-stage ms and % of GB300 bf16 tensor peak alongside)"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
@@ -560,22 +560,13 @@ class FitWorkload:
         return 5 + 2 + (3 * nb - 2) + 2 + inv + 1 + 3 + 2 + 1 + 1
 
     def setup(self, dev, seed):
-        """Calibration pairs drawn on the device (torch Philox, seeded) in the
-        distributions of the synthetic generators; the maps are generated per layer."""
+        """Calibration pairs drawn on the device (synthetic.calibration_device)."""
         from late_layer_kv_gb300 import FitSums
         from late_layer_kv_gb300 import ridgefill as rb
         s, n = self.shape, self.n
         L, d = s.n_layers, s.d
-        g = torch.Generator(device=dev).manual_seed(seed)
-        sc = torch.exp(torch.randn(d, generator=g, device=dev))
-        X = (torch.randn(n, d, generator=g, device=dev) * sc).to(torch.bfloat16)
-        Y = torch.empty((L, n, d), dtype=torch.bfloat16, device=dev)
-        Xf = X.float()
-        for l in range(L):
-            M = torch.eye(d, device=dev) + 0.1 * torch.randn(d, d, generator=g, device=dev) / d ** 0.5
-            bl = torch.randn(d, generator=g, device=dev)
-            Y[l] = (Xf @ M + bl + 0.05 * torch.randn(n, d, generator=g, device=dev)).to(torch.bfloat16)
-        self.X, self.Y = X, Y
+        cal = calibration_device(d, L, n, seed, dev)
+        self.X, self.Y = cal["X"], cal["Y"]
         self.sums = FitSums(L, d, d, device=dev)
         self.A = torch.empty((L, d, d), dtype=torch.bfloat16, device=dev)
         self.b = torch.empty((L, d), dtype=torch.float32, device=dev)

@@ -16,5 +16,6 @@ from .workloads import (  # noqa: F401
     true_inputs,
     gdn_inputs,
     calibration,
+    calibration_device,
     to_f64,
 )

@@ -326,3 +326,22 @@ def calibration(d: int, n_layers: int, n: int, seed: int, device: str = "cpu",
         Ms.append(torch.from_numpy(g))
         bs.append(torch.from_numpy(bg))
     return {"X": X, "Y": Y, "M": torch.stack(Ms), "bgen": torch.stack(bs)}
+
+
+def calibration_device(d: int, n_layers: int, n: int, seed: int, device) -> Dict[str, torch.Tensor]:
+    """Full-size calibration pairs drawn on the device (torch's Philox generator, seeded),
+    in the distributions of :func:`calibration`: ``X`` [n, d] bf16 = N(0,1) times
+    per-channel LogNormal(0,1) scales, ``Y`` [L, n, d] bf16 = X (I + 0.1 G_l/sqrt(d)) + b_l
+    + 0.05 N(0,1).  For sizes whose host generation would take minutes (the full fit
+    workload); the bytes depend on the seed and the device's generator, not on numpy."""
+    g = torch.Generator(device=device).manual_seed(seed)
+    sc = torch.exp(torch.randn(d, generator=g, device=device))
+    X = (torch.randn(n, d, generator=g, device=device) * sc).to(torch.bfloat16)
+    Y = torch.empty((n_layers, n, d), dtype=torch.bfloat16, device=device)
+    Xf = X.float()
+    for l in range(n_layers):
+        M = torch.eye(d, device=device) + 0.1 * torch.randn(d, d, generator=g, device=device) / d ** 0.5
+        bl = torch.randn(d, generator=g, device=device)
+        Y[l] = (Xf @ M + bl + 0.05 * torch.randn(n, d, generator=g, device=device)).to(torch.bfloat16)
+    return {"X": X, "Y": Y}
+

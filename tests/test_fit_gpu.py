@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from synthetic import WORKLOADS, calibration, fill_inputs, to_f64
+from synthetic import WORKLOADS, calibration, calibration_device, fill_inputs, to_f64
 from tests._fill_helpers import compare, new_cache
 
 pytestmark = pytest.mark.gpu
@@ -85,6 +85,41 @@ def test_tiny_batches_add_exactly_what_they_hold():
     np.testing.assert_allclose(sums.sy.cpu().numpy(), sy, rtol=1e-6, atol=1e-6 * np.abs(sy).max())
     assert _rel(sums.G.cpu().numpy(), G) < 1e-5
     assert _rel(sums.C.cpu().numpy(), C.reshape(1024, 201, 384).transpose(1, 2, 0)) < 1e-5
+
+
+def test_full_size_sums_sampled():
+    """The fit workload at full size (d = 4096, 20 layers, 65,536 calibration rows), on the
+    clustered Gram path the bench times: the sums of 64 sampled X columns and 64 sampled
+    output channels of every layer against the oracle's sums of those columns over every
+    row."""
+    shape = WORKLOADS["hostmaps_16k"]
+    d, L, n = shape.d, shape.n_layers, shape.calib_rows
+    cal = calibration_device(d, L, n, seed=1003, device="cuda")
+    X, Y = cal["X"], cal["Y"]
+    sums = FitSums(L, d, d)
+    ridgefill_fit_accumulate(sums, X, Y)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    rng = np.random.default_rng(11)
+    ci = np.sort(rng.choice(d, 64, replace=False))  # X columns
+    co = np.sort(rng.choice(d, 64, replace=False))  # output channels of each layer
+    ti, to = torch.from_numpy(ci).cuda(), torch.from_numpy(co).cuda()
+    Xs = X[:, ti].cpu()
+    Ys = Y[:, :, to].cpu()
+    del X, Y, cal
+    torch.cuda.empty_cache()
+    nn, sx, sy, G, C = oracle.fit_sums(to_f64(Xs), to_f64(Ys))  # C: [64, L * 64]
+    assert float(sums.count.item()) == nn == n
+    Gg = sums.G[ti][:, ti].cpu().numpy()
+    Cg = sums.C[:, to][:, :, ti].cpu().numpy()               # [L, 64 outputs, 64 inputs]
+    Co = C.reshape(64, L, 64).transpose(1, 2, 0)
+    # each entry is 4096 f32 accumulations of 16-product MMA steps: at most 4096 * 2^-24
+    # = 2.4e-4 of its magnitude even if every rounding went the same way
+    assert _rel(Gg, G) < 5e-4
+    assert _rel(Cg, Co) < 5e-4
+    np.testing.assert_allclose(sums.sx[ti].cpu().numpy(), sx, rtol=1e-6, atol=1e-6 * np.abs(sx).max())
+    np.testing.assert_allclose(sums.sy[:, to].cpu().numpy(), sy, rtol=1e-6,
+                               atol=1e-6 * np.abs(sy).max())
 
 
 # d = 384 and 640 are not powers of two: the blocked inverse then merges a last,
