@@ -122,6 +122,42 @@ def test_full_size_sums_sampled():
                                atol=1e-6 * np.abs(sy).max())
 
 
+def test_full_size_fit_sampled():
+    """The whole fit at full size (d = 4096, 20 layers, 65,536 rows: the clustered Gram, the
+    blocked Cholesky and the split-bf16 solve the bench runs): eight output channels of the
+    first and the last layer against the oracle's ridge fit of those channels.  A channel's
+    map row and offset depend only on X and on its own column of Y, so the oracle fits the
+    sampled columns alone."""
+    shape = WORKLOADS["hostmaps_16k"]
+    d, L, n = shape.d, shape.n_layers, shape.calib_rows
+    cal = calibration_device(d, L, n, seed=1004, device="cuda")
+    X, Y = cal["X"], cal["Y"]
+    sums = FitSums(L, d, d)
+    ridgefill_fit_accumulate(sums, X, Y)
+    A32 = torch.empty((L, d, d), dtype=torch.float32, device="cuda")
+    b = torch.empty((L, d), dtype=torch.float32, device="cuda")
+    alpha = torch.zeros(1, dtype=torch.float64, device="cuda")
+    ridgefill_fit_solve(sums, shape.lam, A_out_f32=A32, b_out=b, alpha_out=alpha)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    js = torch.from_numpy(np.sort(np.random.default_rng(13).choice(d, 8, replace=False))).cuda()
+    layers = torch.tensor([0, L - 1], device="cuda")
+    Ys = Y[layers][:, :, js].cpu()
+    Ag = A32[layers][:, js].cpu().double().numpy()   # [2, 8, d_in]
+    bg = b[layers][:, js].cpu().double().numpy()
+    Xh = X.cpu()
+    del X, Y, cal, A32
+    torch.cuda.empty_cache()
+    Ao, bo, ao = oracle.ridge_fit(to_f64(Xh), to_f64(Ys), shape.lam)
+    # alpha = lam tr(X~^T X~) / d_in takes the Gram diagonal, summed over the 65,536 rows of
+    # the one batch in f32 on the tensor cores (4096 accumulation steps a sum; measured
+    # 3e-4 low, against at most 4096 * 2^-23 = 4.9e-4 with every step truncated)
+    assert abs(float(alpha.item()) - ao) <= 1e-3 * ao
+    for i in range(2):
+        assert _rel(Ag[i], Ao[i]) <= W_REL_FRO, f"layer {i}: {_rel(Ag[i], Ao[i]):.2e}"
+        assert _rel(bg[i], bo[i]) <= W_REL_FRO
+
+
 # d = 384 and 640 are not powers of two: the blocked inverse then merges a last,
 # shorter block pair
 @pytest.mark.parametrize("d,L,n,lam", [(256, 3, 1000, 1e-3), (512, 2, 4096, 3e-2),
