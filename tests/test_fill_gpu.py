@@ -79,6 +79,17 @@ def test_no_gain_and_rows_below_one_tile():
     _check_all(shape, inp, Kc, Vc, gain=False)
 
 
+def test_empty_prefix_writes_nothing():
+    """No prefix rows (N = T): the call succeeds and leaves the whole cache untouched."""
+    shape = FillShape("empty", d=256, n_layers=2, n_kv=2, head_dim=128, rope_theta=1e4,
+                      rms_eps=1e-6, N=64, T=64)
+    inp = fill_inputs(shape, seed=10)
+    assert inp["H"].shape[0] == 0
+    Kc, Vc = _run(shape, inp, pos0=5, cache_len=64)
+    for C in (Kc, Vc):
+        assert bool((C == SENTINEL).all())
+
+
 def test_chunked_equals_unchunked_bitwise():
     shape = FillShape("mid", d=512, n_layers=2, n_kv=2, head_dim=128, rope_theta=5e5,
                       rms_eps=1e-6, N=700, T=0)
