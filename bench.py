@@ -52,10 +52,10 @@ FP32_LANES_PER_SM = 128
 # profiles/fit_launches_llama8b_rows65536.md (Gram accumulate).
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "8a59e5fbe62497eb97bb9035ddf9d768cb55933cd22b4ebcbb423989c6d89882",
+                    "kernel_sha256": "e9bf7038d43cb0db3c43fd6cc174fcc3a029817f3870074ea0de7225a8cfa6b4",
                     "bytes_per_launch": 6729319424 + 2360831744},
     "hostmaps_16k_fit": {"sources": "fit",
-                         "kernel_sha256": "49521073e68f04a1613fa7e5547e6a7f1ed2836fe6852ffcaf9d0641549625d8",
+                         "kernel_sha256": "2050d832798692dacd2845baba91bdb17d1f15a8318dbe4e7d460b6e6a3f7d9c",
                          "bytes_per_launch": 105417109760 + 2812521728},
 }
 

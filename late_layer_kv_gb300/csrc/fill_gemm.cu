@@ -574,10 +574,10 @@ __device__ __forceinline__ void q8_convert(const uint8_t* raw, int sub, const ui
 // {d_out, d_in / 128, layers} bf16).  Warps 8-11 dequantise this CTA's B half of each
 // stage into shared memory and arrive on CTA 0's `full` barrier (released at cluster
 // scope; the MMA acquires at cluster scope before reading both halves).
-// kCl = 4 (Gram mode, 512-column tiles): two CTA pairs per cluster take row tiles 2 mu and
-// 2 mu + 1 of the same column tile; each pair stages half of the B boxes of every stage and
-// multicasts them to the same CTA half of the other pair, so the shared B panel is read once
-// for both, and each pair's MMA commit frees the stage in all four CTAs.
+// kCl = 4 (Gram mode, 512-column tiles): two CTA pairs per cluster take pair row tiles 2 mu
+// and 2 mu + 1 of the same column tile; each pair loads half of the B boxes of every stage and
+// multicasts them to the same CTA half of both pairs, so the shared B panel is read once for
+// both, and each pair's MMA commit frees the stage in all four CTAs.
 template <bool kQ8, int kCl>
 __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8 : kGemmThreads, 1)
     rf_gemm2_kernel(const __grid_constant__ GemmParams p) {
