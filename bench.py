@@ -52,10 +52,10 @@ FP32_LANES_PER_SM = 128
 # profiles/fit_launches_llama8b_rows65536.md (Gram accumulate).
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "e9bf7038d43cb0db3c43fd6cc174fcc3a029817f3870074ea0de7225a8cfa6b4",
-                    "bytes_per_launch": 6729319424 + 2360831744},
+                    "kernel_sha256": "aa86148999b065f39db41d9a2f4654a9b47c80b4fd060bc2316213083986559a",
+                    "bytes_per_launch": 5977021184 + 2355833600},
     "hostmaps_16k_fit": {"sources": "fit",
-                         "kernel_sha256": "2050d832798692dacd2845baba91bdb17d1f15a8318dbe4e7d460b6e6a3f7d9c",
+                         "kernel_sha256": "0a0ecec19fb9f53a59245684cb362ba321539c25f635453a491cbbc91db633b5",
                          "bytes_per_launch": 105417109760 + 2812521728},
 }
 

@@ -114,6 +114,12 @@ typedef enum rf_status {
  *   k_scale[l, h] (v_scale[l, h]) before its rounding to bf16: the value or
  *   key rescale of section 2.3 folded into the fill, with the scales from
  *   ridgefill_rescale called with rows = 0.
+ * q8_group_layers (int8 maps in device memory; ignored otherwise): 0 or k > 0
+ *   writes bf16(q * s) of 4 (or k) layers at a time into the workspace and runs
+ *   the bf16 map GEMM on them (workspace grows by that many bf16 maps);
+ *   -1 converts the codes inside the map GEMM's shared-memory stages instead
+ *   (no extra workspace, bound by shared-memory bandwidth, about 9 % slower).
+ *   Both give bitwise the same results.
  */
 typedef struct rf_fill_args {
   int32_t n_layers;
@@ -144,7 +150,7 @@ typedef struct rf_fill_args {
   const int32_t* row_idx;
   int64_t h_rows;
   int32_t h_on_host;
-  int32_t reserved0;
+  int32_t q8_group_layers;
 } rf_fill_args;
 
 /* Bytes of device workspace ridgefill_fill needs for these arguments
@@ -317,6 +323,7 @@ rf_status ridgefill_quantize_maps(const rf_quantize_args* args, void* stream);
  * h_on_host (0 or 1): H is page-locked host memory, streamed as for
  *   rf_fill_args.h_on_host (with exact rows and one row chunk the copy
  *   completes before the filled rows are gathered).
+ * q8_group_layers: as rf_fill_args.q8_group_layers.
  */
 typedef struct rf_gdn_args {
   int32_t n_layers;
@@ -349,7 +356,7 @@ typedef struct rf_gdn_args {
   float* rho;
   const float* delta_M;
   int32_t h_on_host;
-  int32_t reserved0;
+  int32_t q8_group_layers;
 } rf_gdn_args;
 
 size_t ridgefill_gdn_workspace_size(const rf_gdn_args* args);

@@ -188,7 +188,8 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   p.mode = kModeMap;
   p.k_blocks = m.d_in / kBK;
   const bool single = m.slot_layer >= 0;
-  const uint64_t brows = single ? static_cast<uint64_t>(m.d_out)
+  const int slot_layers = m.slot_count > 0 ? m.slot_count : 1;
+  const uint64_t brows = single ? static_cast<uint64_t>(slot_layers) * m.d_out
                                 : static_cast<uint64_t>(m.n_layers) * m.d_out;
   const uint64_t in_row = static_cast<uint64_t>(m.d_in) * 2;
   const uint64_t out_row = static_cast<uint64_t>(m.d_out) * 2;
@@ -201,7 +202,7 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
     // scales [layers, d_in / 128, d_out] bf16 in boxes {bn / 2} (one 128-weight group of a
     // half tile's rows)
     const uint64_t groups = static_cast<uint64_t>(m.d_in / kQ8Group);
-    const uint64_t slayers = single ? 1 : static_cast<uint64_t>(m.n_layers);
+    const uint64_t slayers = single ? static_cast<uint64_t>(slot_layers) : static_cast<uint64_t>(m.n_layers);
     ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_UINT8, m.A, m.d_in, brows, 1,
                             static_cast<uint64_t>(m.d_in), 0, 2 * kBK, m.bn / 2,
                             CU_TENSOR_MAP_SWIZZLE_128B);
@@ -248,6 +249,33 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   cudaError_t e = q8 ? launch_gemm2_q8(p, pairs, s) : launch_gemm2(p, pairs, s);
   if (e != cudaSuccess) return cuda_fail(e, "map GEMM launch");
   return RF_OK;
+}
+
+rf_status launch_map_q8_groups(MapLaunch m, int group, void* dq, cudaStream_t s) {
+  const void* codes = m.A;
+  const void* scales = m.A_scale;
+  const size_t lc = static_cast<size_t>(m.d_out) * m.d_in;         // codes per layer
+  const size_t ls = static_cast<size_t>(m.d_in / kQ8Group) * m.d_out;  // scales per layer
+  for (int l0 = 0; l0 < m.n_layers; l0 += group) {
+    const int g = m.n_layers - l0 < group ? m.n_layers - l0 : group;
+    const cudaError_t e = launch_dequant_maps(static_cast<const int8_t*>(codes) + l0 * lc,
+                                              static_cast<const __nv_bfloat16*>(scales) + l0 * ls,
+                                              g, m.d_out, m.d_in, dq, s);
+    if (e != cudaSuccess) return cuda_fail(e, "int8 map dequantisation");
+    m.A = dq;
+    m.A_scale = nullptr;
+    m.slot_layer = l0;
+    m.slot_count = g;
+    const rf_status st = launch_map(m, s);
+    if (st != RF_OK) return st;
+  }
+  return RF_OK;
+}
+
+int q8_group(int option, bool q8, bool maps_on_host, int n_layers) {
+  if (!q8 || maps_on_host || option < 0) return 0;
+  const int k = option > 0 ? option : 4;
+  return k < n_layers ? k : n_layers;
 }
 
 size_t map_slot_bytes(int d_out, int d_in, bool q8) {
@@ -378,7 +406,7 @@ extern "C" rf_status ridgefill_wait_selftest(int32_t which, void* stream) {
   return RF_OK;
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 8; }
+extern "C" int32_t ridgefill_abi_version(void) { return 9; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {

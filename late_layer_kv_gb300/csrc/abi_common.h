@@ -88,6 +88,7 @@ struct MapLaunch {
   int64_t rows;
   int32_t d_in, d_out, n_layers;
   int32_t slot_layer;
+  int32_t slot_count;  // layers in the slot (0: one)
   int32_t bn;
   int64_t R;  // allocated rows of X_hat / partial buffers
   const int32_t* out_rows;  // X_hat row of each GEMM row (rows left out are not written), or null
@@ -100,6 +101,17 @@ struct MapLaunch {
   float* ss;
 };
 rf_status launch_map(const MapLaunch& m, cudaStream_t s);
+// bf16(q * s) of `layers` int8 maps (codes [layers, d_out, d_in], scales
+// [layers, d_in / 128, d_out]) into out [layers, d_out, d_in]
+cudaError_t launch_dequant_maps(const void* q, const void* scale, int layers, int d_out, int d_in,
+                                void* out, cudaStream_t s);
+// The map GEMM of resident int8 maps (m.A codes, m.A_scale scales, every layer) run as
+// `group` layers at a time: their bf16(q * s) into `dq` (group * d_out * d_in bf16), then
+// the bf16 GEMM of those layers
+rf_status launch_map_q8_groups(MapLaunch m, int group, void* dq, cudaStream_t s);
+// Layers per group of the resident int8 map GEMM for a q8_group_layers option (0 when the
+// codes are converted inside the GEMM, or the maps are not int8 in device memory)
+int q8_group(int option, bool q8, bool maps_on_host, int n_layers);
 
 // Gather the split-state rows H[idx[0 .. rc)] ([h_rows, d_in] bf16) into a dense [rc, d_in]
 // block; an index outside [0, h_rows) gives a zero row and a device error code.

@@ -18,6 +18,8 @@ namespace {
 struct FillPlan {
   int bn_map = 0, bn_kv = 0;
   int64_t R = 0;  // rows per chunk
+  int dq_layers = 0;
+  size_t off_dq = 0;
   size_t off_xhat = 0, off_ss = 0, off_slots = 0, off_gather = 0, off_hdev = 0, off_hflags = 0,
          off_rope = 0, total = 0;
 };
@@ -51,6 +53,7 @@ rf_status validate_fill(const rf_fill_args* a) {
   if (a->maps_on_host != 0 && a->maps_on_host != 1) return fail(RF_ERR_ARG, "maps_on_host must be 0 or 1");
   if (a->A_scale != nullptr && a->d_in % kQ8Group != 0)
     return fail(RF_ERR_SHAPE, "int8 maps need d_in to be a multiple of 128");
+  if (a->q8_group_layers < -1) return fail(RF_ERR_ARG, "q8_group_layers must be >= -1");
   if (a->h_on_host != 0 && a->h_on_host != 1) return fail(RF_ERR_ARG, "h_on_host must be 0 or 1");
   if (a->h_on_host && a->row_idx != nullptr)
     return fail(RF_ERR_ARG, "h_on_host cannot be combined with row_idx");
@@ -77,7 +80,10 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   pl->off_hflags = pl->off_hdev + hflags;
   pl->off_rope = align_up(pl->off_hdev + hbytes, 256);
   const size_t rope = static_cast<size_t>(a->head_dim / 2) * pl->R * 8;  // (cos, sin) f32 pairs
-  pl->total = align_up(pl->off_rope + rope, 256);
+  pl->off_dq = align_up(pl->off_rope + rope, 256);
+  pl->dq_layers = q8_group(a->q8_group_layers, a->A_scale != nullptr, a->maps_on_host != 0,
+                           a->n_layers);
+  pl->total = align_up(pl->off_dq + static_cast<size_t>(pl->dq_layers) * a->d_out * a->d_in * 2, 256);
 }
 
 // RoPE angles of one row chunk (rotate-half pairs, frequency f_i = theta^(-2i/hd)):
@@ -304,7 +310,12 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     m.gain = a->gain;
     m.xhat = xhat;
     m.ss = ss;
-    if (!a->maps_on_host) {
+    if (!a->maps_on_host && pl.dq_layers > 0) {
+      // int8 maps: bf16(q s) of a few layers at a time, then the bf16 GEMM on them
+      m.A = a->A;
+      m.A_scale = a->A_scale;
+      if ((st = launch_map_q8_groups(m, pl.dq_layers, ws + pl.off_dq, s)) != RF_OK) return st;
+    } else if (!a->maps_on_host) {
       m.A = a->A;
       m.A_scale = a->A_scale;
       m.slot_layer = -1;

@@ -66,6 +66,9 @@ extern "C" rf_status ridgefill_fill_noalloc(const rf_fill_args* a, void* stream)
   if (a->h_on_host != 0)
     return fail(RF_ERR_ARG, "ridgefill_fill_noalloc does not stream a host split state (h_on_host = 1)");
   rf_fill_args c = *a;
+  // int8 maps: the codes are converted inside the map GEMM unless the caller asked for layer
+  // groups (whose bf16 copies would take most of the fixed scratch)
+  if (c.A_scale != nullptr && c.q8_group_layers == 0) c.q8_group_layers = -1;
   // largest chunk (multiple of 128 rows) whose workspace fits the static scratch
   const int64_t want = a->rows_per_chunk > 0 ? a->rows_per_chunk
                                              : ceil_div(a->rows > 0 ? a->rows : 1, kBM) * kBM;

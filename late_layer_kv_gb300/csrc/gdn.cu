@@ -856,8 +856,9 @@ struct GdnPlan {
   int bn_map = 0;
   int64_t R = 0;
   size_t off_xhat = 0, off_ss = 0, off_k = 0, off_v = 0, off_gate = 0, off_slots = 0, off_rho = 0,
-         off_fill = 0, off_hc = 0, off_hdev = 0, off_hflags = 0, total = 0;
-  bool compact = false;  // map only the filled rows (exact rows, one row chunk, bf16 maps)
+         off_fill = 0, off_hc = 0, off_hdev = 0, off_hflags = 0, off_dq = 0, total = 0;
+  int dq_layers = 0;     // resident int8 maps: layers dequantised ahead of the bf16 GEMM
+  bool compact = false;  // map only the filled rows (exact rows, one row chunk, bf16 GEMM)
 };
 
 rf_status validate_gdn(const rf_gdn_args* a) {
@@ -883,6 +884,7 @@ rf_status validate_gdn(const rf_gdn_args* a) {
   if (a->n_exact > 0 && (a->exact_idx == nullptr || a->X_exact == nullptr))
     return fail(RF_ERR_ARG, "n_exact > 0 needs exact_idx and X_exact");
   if (a->h_on_host != 0 && a->h_on_host != 1) return fail(RF_ERR_ARG, "h_on_host must be 0 or 1");
+  if (a->q8_group_layers < -1) return fail(RF_ERR_ARG, "q8_group_layers must be >= -1");
   return RF_OK;
 }
 
@@ -906,7 +908,15 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
     off = align_up(off + host_rows_bytes(a->rows, a->d_in, &fo), 256);
     pl->off_hflags = pl->off_hdev + fo;
   }
-  pl->compact = a->n_exact > 0 && pl->R >= a->rows && a->A_scale == nullptr;
+  pl->dq_layers = q8_group(a->q8_group_layers, a->A_scale != nullptr, a->maps_on_host != 0,
+                           a->n_layers);
+  if (pl->dq_layers > 0) {
+    pl->off_dq = off;
+    off = align_up(off + static_cast<size_t>(pl->dq_layers) * a->d_out * a->d_in * 2, 256);
+  }
+  // the compacted map GEMM writes rows by index: the bf16 GEMM only (not the in-GEMM int8
+  // conversion)
+  pl->compact = a->n_exact > 0 && pl->R >= a->rows && (a->A_scale == nullptr || pl->dq_layers > 0);
   if (pl->compact) {
     const size_t n_fill = static_cast<size_t>(a->rows - a->n_exact);
     pl->off_fill = off; off = align_up(off + static_cast<size_t>(a->rows) * 4, 256);
@@ -1141,6 +1151,10 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     m.ss = ss;
     if (m.rows == 0) {
       // every row of the chunk is exact: no map GEMM
+    } else if (!a->maps_on_host && pl.dq_layers > 0) {
+      m.A = a->A;
+      m.A_scale = a->A_scale;
+      if ((st = launch_map_q8_groups(m, pl.dq_layers, ws + pl.off_dq, s)) != RF_OK) return st;
     } else if (!a->maps_on_host) {
       m.A = a->A;
       m.A_scale = a->A_scale;

@@ -54,7 +54,47 @@ __global__ void __launch_bounds__(256) quantize_kernel(const void* A, uint32_t* 
   }
 }
 
+// bf16(q * s) of layers [0, layers) of int8 maps: 16 codes a thread (one 16-byte load, two
+// 16-byte stores); q * s is exact in f32 (8 by 8 significant bits), so the one rounding gives
+// the bf16 value the in-GEMM converters produce.
+__global__ void __launch_bounds__(256) dequant_maps_kernel(const uint4* q, const __nv_bfloat16* scale,
+                                                           int64_t n16, int d_out, int d_in,
+                                                           uint4* out) {
+  const int64_t per_row = d_in / 16;
+  const int G = d_in / kQ8Group;
+  for (int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; t < n16;
+       t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t row = t / per_row;  // l * d_out + j
+    const int i16 = static_cast<int>(t - row * per_row);
+    const int64_t l = row / d_out, j = row - l * d_out;
+    const float sc = __bfloat162float(scale[(l * G + (i16 * 16) / kQ8Group) * d_out + j]);
+    const uint4 v = __ldg(q + t);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int b0 = static_cast<int8_t>(w[e] & 0xFFu), b1 = static_cast<int8_t>((w[e] >> 8) & 0xFFu);
+      const int b2 = static_cast<int8_t>((w[e] >> 16) & 0xFFu), b3 = static_cast<int8_t>(w[e] >> 24);
+      o[2 * e] = pack_bf16(static_cast<float>(b0) * sc, static_cast<float>(b1) * sc);
+      o[2 * e + 1] = pack_bf16(static_cast<float>(b2) * sc, static_cast<float>(b3) * sc);
+    }
+    out[2 * t] = make_uint4(o[0], o[1], o[2], o[3]);
+    out[2 * t + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_dequant_maps(const void* q, const void* scale, int layers, int d_out, int d_in,
+                                void* out, cudaStream_t s) {
+  const int64_t n16 = static_cast<int64_t>(layers) * d_out * (d_in / 16);
+  const int64_t blocks = (n16 + 255) / 256 < 8 * sm_count() ? (n16 + 255) / 256 : 8 * sm_count();
+  dequant_maps_kernel<<<static_cast<unsigned>(blocks > 0 ? blocks : 1), 256, 0, s>>>(
+      static_cast<const uint4*>(q), static_cast<const __nv_bfloat16*>(scale), n16, d_out, d_in,
+      static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
 }  // namespace rf
 
 extern "C" rf_status ridgefill_quantize_maps(const rf_quantize_args* a, void* stream) {

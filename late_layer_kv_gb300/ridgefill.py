@@ -39,7 +39,8 @@ class FillArgs(ctypes.Structure):
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp), ("copy_events", _vp),
         ("k_scale", _vp), ("v_scale", _vp), ("A_scale", _vp), ("row_idx", _vp),
-        ("h_rows", ctypes.c_int64), ("h_on_host", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("h_rows", ctypes.c_int64), ("h_on_host", ctypes.c_int32),
+        ("q8_group_layers", ctypes.c_int32),
     ]
 
 
@@ -53,7 +54,8 @@ class GdnArgs(ctypes.Structure):
         ("H", _vp), ("A", _vp), ("bias", _vp), ("gain", _vp), ("Wk", _vp), ("Wv", _vp),
         ("Wa", _vp), ("Wb", _vp), ("S0", _vp), ("S", _vp), ("stage_events", _vp),
         ("A_scale", _vp), ("exact_idx", _vp), ("n_exact", ctypes.c_int64), ("X_exact", _vp),
-        ("rho", _vp), ("delta_M", _vp), ("h_on_host", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("rho", _vp), ("delta_M", _vp), ("h_on_host", ctypes.c_int32),
+        ("q8_group_layers", ctypes.c_int32),
     ]
 
 
@@ -92,6 +94,10 @@ class RidgeFillError(RuntimeError):
     def __init__(self, status: int, msg: str):
         super().__init__(f"{STATUS.get(status, status)}: {msg}")
         self.status = status
+
+
+# the argument structs below match include/ridgefill.h at this version
+ABI_VERSION = 9
 
 
 def library_path() -> str:
@@ -140,6 +146,9 @@ def load(rebuild: bool = True) -> ctypes.CDLL:
     lib.ridgefill_compute_share.restype = ctypes.c_double
     lib.ridgefill_abi_version.argtypes = []
     lib.ridgefill_abi_version.restype = ctypes.c_int32
+    if lib.ridgefill_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"{path} has ABI version {lib.ridgefill_abi_version()}, this binding "
+                           f"expects {ABI_VERSION}: rebuild the library")
     _lib = lib
     return lib
 
@@ -199,7 +208,7 @@ def _event_array(events):
 def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
               rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
               stage_events=None, copy_events=None, k_scale=None, v_scale=None,
-              A_scale=None, row_idx=None) -> FillArgs:
+              A_scale=None, row_idx=None, q8_group_layers: int = 0) -> FillArgs:
     L, d_out, d_in = A.shape
     rows = H.shape[0] if row_idx is None else row_idx.shape[0]
     h_rows = H.shape[0] if row_idx is not None else 0
@@ -236,7 +245,7 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
                  ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None,
                  ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None,
                  _ptr(k_scale), _ptr(v_scale), _ptr(A_scale), _ptr(row_idx), h_rows,
-                 1 if h_host else 0, 0)
+                 1 if h_host else 0, int(q8_group_layers))
     a._events_keepalive = (ev, cev)
     return a
 
@@ -261,7 +270,7 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
                    rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
                    workspace: Optional[torch.Tensor] = None, stream=None,
                    stage_events=None, copy_events=None, k_scale=None, v_scale=None,
-                   A_scale=None, row_idx=None) -> None:
+                   A_scale=None, row_idx=None, q8_group_layers: int = 0) -> None:
     """Write the K/V cache of the prefix rows of every late attention layer.
 
     ``H`` [rows, d_in] bf16, ``A`` [L, d_out, d_in] bf16 (device, or pinned host
@@ -277,12 +286,16 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     optional int32 [rows] prefix rows to fill (section 2.4): ``H`` then holds every
     prefix row, row ``row_idx[r]`` is filled at position ``pos0 + row_idx[r]`` and the
     unlisted (exact) rows are left alone.  ``H`` may be a pinned host tensor: it is
-    then copied by the library, overlapped with the map GEMM.
+    then copied by the library, overlapped with the map GEMM.  ``q8_group_layers``:
+    resident int8 maps are dequantised 4 (or this many) layers at a time into the
+    workspace ahead of the bf16 map GEMM; -1 converts them inside the GEMM instead
+    (no extra workspace, slower; bitwise the same results).
     """
     args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
                      rms_eps=rms_eps, pos0=pos0, rows_per_chunk=rows_per_chunk,
                      stage_events=stage_events, copy_events=copy_events, k_scale=k_scale,
-                     v_scale=v_scale, A_scale=A_scale, row_idx=row_idx)
+                     v_scale=v_scale, A_scale=A_scale, row_idx=row_idx,
+                     q8_group_layers=q8_group_layers)
     lib = load()
     need = int(lib.ridgefill_fill_workspace_size(ctypes.byref(args)))
     if need == 0:
@@ -298,7 +311,7 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
 def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: float,
              l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
              stage_events=None, A_scale=None, exact_idx=None, X_exact=None, rho=None,
-             delta_M=None) -> GdnArgs:
+             delta_M=None, q8_group_layers: int = 0) -> GdnArgs:
     L, d_out, d_in = A.shape
     rows = H.shape[0]
     d_k = Wk.shape[1] // n_heads
@@ -337,7 +350,7 @@ def gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms_eps: floa
                 _ptr(gain), _ptr(Wk), _ptr(Wv), _ptr(Wa), _ptr(Wb), _ptr(S0), _ptr(S),
                 ctypes.cast(ev, ctypes.c_void_p) if ev is not None else None, _ptr(A_scale),
                 _ptr(exact_idx), n_exact, _ptr(X_exact) if n_exact else None, _ptr(rho),
-                _ptr(delta_M), 1 if h_host else 0, 0)
+                _ptr(delta_M), 1 if h_host else 0, int(q8_group_layers))
     a._events_keepalive = ev
     return a
 
@@ -346,7 +359,7 @@ def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms
                        l2_eps: float = 1e-6, S0=None, chunk: int = 64, rows_per_chunk: int = 0,
                        workspace: Optional[torch.Tensor] = None, stream=None,
                        stage_events=None, A_scale=None, exact_idx=None, X_exact=None,
-                       rho=None, delta_M=None) -> None:
+                       rho=None, delta_M=None, q8_group_layers: int = 0) -> None:
     """End-of-fill recurrent state ``S`` [L, H, dv, dk] f32 of Gated DeltaNet layers.
 
     ``stage_events``: optional four ``torch.cuda.Event`` recorded around the first
@@ -354,11 +367,12 @@ def ridgefill_fill_gdn(H, A, bias, gain, Wk, Wv, Wa, Wb, S, *, n_heads: int, rms
     for :func:`ridgefill_fill`.  ``exact_idx`` (int32 [n]) and ``X_exact`` ([L, n, d_out]
     bf16): exact prefix rows and their true inputs (section 2.4).  ``rho``: optional
     [L, H] f32 output of the filled rows' share of the state; ``delta_M``: optional
-    [L, H, dv, dk] f32 terminal-state correction ``S += rho * delta_M`` (section 2.3)."""
+    [L, H, dv, dk] f32 terminal-state correction ``S += rho * delta_M`` (section 2.3).
+    ``q8_group_layers``: as for :func:`ridgefill_fill`."""
     args = gdn_args(H, A, bias, gain, Wk, Wv, Wa, Wb, S, n_heads=n_heads, rms_eps=rms_eps,
                     l2_eps=l2_eps, S0=S0, chunk=chunk, rows_per_chunk=rows_per_chunk,
                     stage_events=stage_events, A_scale=A_scale, exact_idx=exact_idx,
-                    X_exact=X_exact, rho=rho, delta_M=delta_M)
+                    X_exact=X_exact, rho=rho, delta_M=delta_M, q8_group_layers=q8_group_layers)
     lib = load()
     need = int(lib.ridgefill_gdn_workspace_size(ctypes.byref(args)))
     if need == 0:

@@ -57,14 +57,14 @@ def test_quantizer_bitwise_equals_oracle(src):
     assert np.array_equal(_rowmajor(s).float().numpy(), s_ref)
 
 
-def _fill(shape, d, A, A_scale=None, host=False, rows_per_chunk=0):
+def _fill(shape, d, A, A_scale=None, host=False, rows_per_chunk=0, group=0):
     Kc, Vc = new_cache(shape.n_layers, shape.n_kv, shape.N, shape.head_dim)
     if host:
         A = A.cpu().pin_memory()
         A_scale = None if A_scale is None else A_scale.cpu().pin_memory()
     ridgefill_fill(d["H"], A, d["b"], d["g"], d["Wk"], d["Wv"], Kc, Vc, head_dim=shape.head_dim,
                    rope_theta=shape.rope_theta, rms_eps=shape.rms_eps, A_scale=A_scale,
-                   rows_per_chunk=rows_per_chunk)
+                   rows_per_chunk=rows_per_chunk, q8_group_layers=group)
     torch.cuda.synchronize()
     assert device_error() == 0
     return Kc, Vc
@@ -151,3 +151,44 @@ def test_int8_gdn_and_rescale_bitwise_equal_bf16_path():
     torch.cuda.synchronize()
     assert device_error() == 0
     assert torch.equal(scales[0], scales[1])
+
+
+def test_int8_layer_groups_bitwise_equal_in_gemm_conversion():
+    """Resident int8 maps dequantised a few layers at a time ahead of the bf16 GEMM (the
+    default groups of 4, and groups of 1, 2 and 5 over 6 layers, with a ragged last group)
+    give bitwise the caches of the conversion inside the GEMM (q8_group_layers = -1), also
+    over row chunks."""
+    shape = FillShape("q8_groups", d=512, n_layers=6, n_kv=4, head_dim=128, rope_theta=5e5,
+                      rms_eps=1e-6, N=700, T=100)
+    d = to_cuda(fill_inputs(shape, seed=86))
+    q, s = ridgefill_quantize_maps(d["A"])
+    K0, V0 = _fill(shape, d, q, s, group=-1)
+    for group, rpc in ((0, 0), (1, 0), (2, 256), (5, 0)):
+        K, V = _fill(shape, d, q, s, rows_per_chunk=rpc, group=group)
+        assert torch.equal(K, K0) and torch.equal(V, V0), f"group {group}, chunk {rpc}"
+
+
+def test_int8_gdn_layer_groups_with_exact_rows():
+    """GDN fill with resident int8 maps: the grouped dequantisation (which also lets the map
+    GEMM skip the exact rows) gives bitwise the state and rho of the in-GEMM conversion."""
+    from synthetic import exact_rows, true_inputs
+    gs = GdnShape("q8_gdn_groups", d=256, layer_kinds=("gdn",) * 3, n_heads=8, d_k=128, d_v=128,
+                  chunk=64, n_kv=2, head_dim=128, rope_theta=1e4, rms_eps=1e-6, N=400, T=0)
+    gd = {k: v.cuda() for k, v in gdn_inputs(gs, seed=87).items()}
+    q, s = ridgefill_quantize_maps(gd["A"])
+    rows = gs.N - gs.T
+    idx = exact_rows(rows, 0.3, seed=87).to(torch.int32).cuda()
+    X = true_inputs(3, idx.numel(), 256, seed=87).cuda()
+    out = []
+    for group in (-1, 0, 2):
+        S = torch.empty((3, 8, 128, 128), dtype=torch.float32, device="cuda")
+        rho = torch.empty((3, 8), dtype=torch.float32, device="cuda")
+        ridgefill_fill_gdn(gd["H"], q, gd["b"], gd["g"], gd["Wk"], gd["Wv"], gd["Wa"], gd["Wb"], S,
+                           n_heads=8, rms_eps=gs.rms_eps, A_scale=s, exact_idx=idx, X_exact=X,
+                           rho=rho, q8_group_layers=group)
+        out.append((S, rho))
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    for S, rho in out[1:]:
+        assert torch.equal(S, out[0][0]) and torch.equal(rho, out[0][1])
+
