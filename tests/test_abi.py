@@ -47,6 +47,35 @@ def _c_sizeof(struct):
     return int(subprocess.run([exe], capture_output=True, text=True).stdout)
 
 
+def _c_offsets(struct, fields):
+    body = "".join(f'printf("%zu\\n", offsetof({struct}, {f}));' for f in fields)
+    code = (f'#include "ridgefill.h"\n#include <stdio.h>\n#include <stddef.h>\n'
+            f'int main(void){{{body}return 0;}}\n')
+    exe = os.path.join(tempfile.mkdtemp(prefix="rf_offsetof_"), "offsetof_" + struct)
+    r = subprocess.run(["gcc", "-x", "c", "-I", os.path.join(ROOT, "include"), "-o", exe, "-"],
+                       input=code, text=True, capture_output=True)
+    assert r.returncode == 0, r.stderr
+    return [int(x) for x in subprocess.run([exe], capture_output=True, text=True).stdout.split()]
+
+
+def test_ctypes_field_offsets_match_header():
+    """Every field of the binding's structs sits at the header's offset, under the header's
+    name."""
+    from late_layer_kv_gb300 import ridgefill as rb
+    for cls, struct in ((rb.FillArgs, "rf_fill_args"), (rb.GdnArgs, "rf_gdn_args"),
+                        (rb.FitArgs, "rf_fit_args"), (rb.RescaleArgs, "rf_rescale_args"),
+                        (rb.QuantizeArgs, "rf_quantize_args")):
+        names = [f[0] for f in cls._fields_]
+        header_names = {"lam": "lambda"}  # a Python keyword in the binding
+        offs = _c_offsets(struct, [header_names.get(n, n) for n in names])
+        assert offs == [getattr(cls, n).offset for n in names], struct
+
+
+def test_abi_version_matches_binding(lib):
+    from late_layer_kv_gb300 import ridgefill as rb
+    assert lib.ridgefill_abi_version() == rb.ABI_VERSION
+
+
 def test_ctypes_structs_match_header():
     from late_layer_kv_gb300 import ridgefill as rb
     assert ctypes.sizeof(rb.FillArgs) == _c_sizeof("rf_fill_args")
