@@ -181,10 +181,11 @@ class AttnWorkload:
     """Attention late layers (ridgefill_fill); maps in HBM or in pinned host memory."""
 
     def __init__(self, shape: FillShape, host_maps=False, rows_per_chunk=0, rescale_rows=0,
-                 int8_maps=False, exact_frac=0.0):
+                 int8_maps=False, exact_frac=0.0, q8_group=0):
         self.shape, self.host_maps, self.rpc = shape, host_maps, rows_per_chunk
         self.c = rescale_rows
         self.q8 = int8_maps
+        self.q8_group = q8_group
         self.exact_frac = exact_frac
         if self.c and host_maps:
             raise ValueError("the rescale needs the maps resident in device memory")
@@ -240,7 +241,7 @@ class AttnWorkload:
         a = rb.fill_args(self.d["H"], self.A, self.d["b"], self.d["g"], self.d["Wk"],
                          self.d["Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
                          rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc,
-                         A_scale=self.A_scale)
+                         A_scale=self.A_scale, q8_group_layers=self.q8_group)
         self.row_idx = None
         if self.exact_frac:
             keep = np.ones(s.rows, bool)
@@ -250,7 +251,8 @@ class AttnWorkload:
             a = rb.fill_args(self.d["H"], self.A, self.d["b"], self.d["g"], self.d["Wk"],
                              self.d["Wv"], self.Kc, self.Vc, head_dim=s.head_dim,
                              rope_theta=s.rope_theta, rms_eps=s.rms_eps, rows_per_chunk=self.rpc,
-                             A_scale=self.A_scale, row_idx=self.row_idx)
+                             A_scale=self.A_scale, row_idx=self.row_idx,
+                             q8_group_layers=self.q8_group)
         self.ws = torch.empty(rb.fill_workspace_size(a), dtype=torch.uint8, device=dev)
         self.H_dev = self.d["H"]
         if self.c:
@@ -287,7 +289,7 @@ class AttnWorkload:
                        stage_events=None if ev is None else ev[:3],
                        copy_events=None if (ev is None or not self.host_maps) else
                        ev[3:3 + 2 * s.n_layers], v_scale=self.scale if self.c else None,
-                       A_scale=self.A_scale, row_idx=self.row_idx)
+                       A_scale=self.A_scale, row_idx=self.row_idx, q8_group_layers=self.q8_group)
 
     def copy_ms(self, ev):
         """Durations of the first chunk's per-layer map copies (host maps only)."""
@@ -356,6 +358,9 @@ class AttnWorkload:
                 "filled_rows": s.rows, "kv_heads": s.n_kv, "head_dim": s.head_dim,
                 "maps": "pinned host, streamed per layer" if self.host_maps else "hbm",
                 "map_format": "int8, one bf16 scale per 128 weights" if self.q8 else "bf16",
+                "int8_path": (None if not self.q8 else
+                              "converted inside the GEMM" if (self.q8_group < 0 or self.host_maps)
+                              else f"dequantised {self.q8_group or 4} layers at a time"),
                 "rows_per_chunk": self.rpc or s.rows,
                 "value_rescale_tail_rows": self.c,
                 "exact_prefix_rows": s.rows - self.n_fill,
@@ -679,6 +684,7 @@ def make_workload(name, args):
         rpc = 16384  # late-layer X_hat processed in row chunks
     return AttnWorkload(shape, host_maps=name.startswith("hostmaps"), rows_per_chunk=rpc,
                         rescale_rows=args.rescale, int8_maps=args.int8_maps,
+                        q8_group=args.q8_group,
                         exact_frac=args.exact_frac)
 
 
@@ -897,6 +903,9 @@ def main():
                          "their true inputs and apply the terminal-state correction)")
     ap.add_argument("--int8-maps", action="store_true",
                     help="maps as int8 codes with one bf16 scale per 128 weights")
+    ap.add_argument("--q8-group", type=int, default=0, metavar="K",
+                    help="resident int8 maps: layers dequantised at a time ahead of the bf16 "
+                         "GEMM (0: the library's 4; -1: converted inside the GEMM)")
     ap.add_argument("--rescale", type=int, default=0, metavar="C",
                     help="also apply the value rescale from C exact tail rows each step")
     args = ap.parse_args()
