@@ -52,10 +52,10 @@ FP32_LANES_PER_SM = 128
 # profiles/fit_launches_llama8b_rows65536.md (Gram accumulate).
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "aa86148999b065f39db41d9a2f4654a9b47c80b4fd060bc2316213083986559a",
+                    "kernel_sha256": "d7e39f3da74229b752c94c267b93e566a620e262b4a5146ab9330825cd4fe11c",
                     "bytes_per_launch": 5977021184 + 2355833600},
     "hostmaps_16k_fit": {"sources": "fit",
-                         "kernel_sha256": "0a0ecec19fb9f53a59245684cb362ba321539c25f635453a491cbbc91db633b5",
+                         "kernel_sha256": "cb0e95d5757c38beab7723f7dc9196a150f9888fd3bdad58b33824d5d259b984",
                          "bytes_per_launch": 105417109760 + 2812521728},
 }
 

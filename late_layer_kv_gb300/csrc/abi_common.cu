@@ -172,6 +172,9 @@ HostStreamer* host_streamer() {
       e = cudaEventCreateWithFlags(&h.copied[i], cudaEventDisableTiming);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.freed[i], cudaEventDisableTiming);
     }
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.side, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.side_start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.side_done, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.h_done, cudaEventDisableTiming);
     if (e != cudaSuccess) {

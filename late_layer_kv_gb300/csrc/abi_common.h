@@ -40,6 +40,9 @@ constexpr int kMapSlots = 3;
 // Per-device side stream and events for streaming maps from host memory.
 struct HostStreamer {
   cudaStream_t copy = nullptr;
+  cudaStream_t side = nullptr;       // small kernels beside a persistent GEMM (fit column sums)
+  cudaEvent_t side_start = nullptr;
+  cudaEvent_t side_done = nullptr;
   cudaEvent_t copied[kMapSlots] = {};
   cudaEvent_t freed[kMapSlots] = {};
   cudaEvent_t start = nullptr;

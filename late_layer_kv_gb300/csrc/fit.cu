@@ -19,6 +19,7 @@
 // [c_hi | c_hi | c_lo] x [g_hi | g_lo | g_hi] (K = 3 d_in), which carries about
 // 16 bits of each f32 operand.
 #include <cmath>
+#include <mutex>
 
 #include "abi_common.h"
 #include "sm103_ptx.cuh"
@@ -603,21 +604,36 @@ rf_status accumulate(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaS
   const int64_t rows = a->rows;
   if (rows == 0) return RF_OK;
   const int L = a->n_layers, din = a->d_in, dout = a->d_out;
+  HostStreamer* hs = host_streamer();
+  if (hs == nullptr) return RF_ERR_CUDA;
+  // one caller at a time on the device's side stream and its events
+  std::lock_guard<std::mutex> lk(host_stream_mutex());
+  // the Gram products first, on `s`; the column sums, HBM-bound, then run beside them on the
+  // side stream, in the few SMs (and the issue slots) the persistent GEMM leaves
+  cudaError_t e = cudaEventRecord(hs->side_start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->side, hs->side_start, 0);
+  if (e != cudaSuccess) return cuda_fail(e, "ordering the column sums");
+  rf_status st = launch_gram(a->X, a->X, a->Y, L, rows, din, dout, pl.bn, a->G, a->C, s);
+  if (st != RF_OK) return st;
   // column sums: slab partials, then a fixed-order reduction into the f64 sums
+  cudaStream_t cs_stream = hs->side;
   double* cs = reinterpret_cast<double*>(ws + pl.off_cs);
   const int64_t ld = din + static_cast<int64_t>(L) * dout;
   const int64_t tx = din / 8, ty = static_cast<int64_t>(dout / 8) * L;
-  colsum_partial_kernel<<<dim3(static_cast<unsigned>((tx + 127) / 128), pl.slabs), 128, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(a->X), rows, din, 1, 0, pl.slab_rows, cs, ld, 0);
-  colsum_partial_kernel<<<dim3(static_cast<unsigned>((ty + 127) / 128), pl.slabs), 128, 0, s>>>(
-      static_cast<const __nv_bfloat16*>(a->Y), rows, dout, L, rows * dout, pl.slab_rows, cs, ld,
-      din);
-  colsum_reduce_kernel<<<static_cast<unsigned>((ld + 255) / 256), 256, 0, s>>>(cs, pl.slabs, ld,
-                                                                               din, a->sx, a->sy);
-  add_count_kernel<<<1, 1, 0, s>>>(a->count, static_cast<double>(rows));
-  cudaError_t e = cudaGetLastError();
+  colsum_partial_kernel<<<dim3(static_cast<unsigned>((tx + 127) / 128), pl.slabs), 128, 0,
+                          cs_stream>>>(static_cast<const __nv_bfloat16*>(a->X), rows, din, 1, 0,
+                                       pl.slab_rows, cs, ld, 0);
+  colsum_partial_kernel<<<dim3(static_cast<unsigned>((ty + 127) / 128), pl.slabs), 128, 0,
+                          cs_stream>>>(static_cast<const __nv_bfloat16*>(a->Y), rows, dout, L,
+                                       rows * dout, pl.slab_rows, cs, ld, din);
+  colsum_reduce_kernel<<<static_cast<unsigned>((ld + 255) / 256), 256, 0, cs_stream>>>(
+      cs, pl.slabs, ld, din, a->sx, a->sy);
+  add_count_kernel<<<1, 1, 0, cs_stream>>>(a->count, static_cast<double>(rows));
+  e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaEventRecord(hs->side_done, cs_stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hs->side_done, 0);
   if (e != cudaSuccess) return cuda_fail(e, "column-sum launch");
-  return launch_gram(a->X, a->X, a->Y, L, rows, din, dout, pl.bn, a->G, a->C, s);
+  return RF_OK;
 }
 
 rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream_t s) {
