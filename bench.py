@@ -50,13 +50,18 @@ FP32_LANES_PER_SM = 128
 # only while the library sources that define that kernel hash to kernel_sha256 (otherwise
 # reported as null).  Captures: profiles/fill_launches_llama8b_16k.md (map GEMM) and
 # profiles/fit_launches_llama8b_rows65536.md (Gram accumulate).
+# The fit depends only on d, the number of maps and the calibration rows, which the Llama-8B
+# fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
+_FIT_LLAMA8B = {"sources": "fit",
+                "kernel_sha256": "cb0e95d5757c38beab7723f7dc9196a150f9888fd3bdad58b33824d5d259b984",
+                "bytes_per_launch": 105417109760 + 2812521728}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
                     "kernel_sha256": "d7e39f3da74229b752c94c267b93e566a620e262b4a5146ab9330825cd4fe11c",
                     "bytes_per_launch": 5977021184 + 2355833600},
-    "hostmaps_16k_fit": {"sources": "fit",
-                         "kernel_sha256": "cb0e95d5757c38beab7723f7dc9196a150f9888fd3bdad58b33824d5d259b984",
-                         "bytes_per_launch": 105417109760 + 2812521728},
+    "llama8b_16k_fit": _FIT_LLAMA8B,
+    "hostmaps_16k_fit": _FIT_LLAMA8B,
+    "hostmaps_64k_fit": _FIT_LLAMA8B,
 }
 
 
