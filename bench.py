@@ -53,7 +53,7 @@ FP32_LANES_PER_SM = 128
 # The fit depends only on d, the number of maps and the calibration rows, which the Llama-8B
 # fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
 _FIT_LLAMA8B = {"sources": "fit",
-                "kernel_sha256": "cb0e95d5757c38beab7723f7dc9196a150f9888fd3bdad58b33824d5d259b984",
+                "kernel_sha256": "c2bfcf9009a383123195d1a207ee52288dadb380ea9123bf2b227ac499869780",
                 "bytes_per_launch": 105417109760 + 2812521728}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",

@@ -661,19 +661,45 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fit preparation launch");
 
-  // blocked Cholesky, lower factor in place
+  // blocked Cholesky, lower factor in place, with a look-ahead of one block column:
+  // after the panel of step kb, block column kb+1 is updated on `s` and the rest of
+  // the trailing matrix on the side stream, so the next diagonal factor and panel run
+  // beside the large update.  The two parts write disjoint blocks and every element
+  // takes the same sum as one whole update; the skipped blocks above the diagonal are
+  // never read.
   const int nb = d / kNB;
   float* linv = reinterpret_cast<float*>(ws + pl.off_linv);
-  for (int kb = 0; kb < nb; ++kb) {
-    potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb, err, linv);
-    if (kb + 1 < nb) {
+  HostStreamer* hs = host_streamer();
+  if (hs == nullptr) return RF_ERR_CUDA;
+  {
+    // one caller at a time on the device's side stream and its events
+    std::lock_guard<std::mutex> lk(host_stream_mutex());
+    for (int kb = 0; kb < nb; ++kb) {
+      potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb, err, linv);
+      if (kb + 1 == nb) break;
       trsm_panel_kernel<<<nb - kb - 1, 256, 0, s>>>(Gh, d, kb, linv);
+      // block column kb+1 was last written by step kb-1's trailing update
+      if (kb > 0 && (e = cudaStreamWaitEvent(s, hs->side_done, 0)) != cudaSuccess)
+        return cuda_fail(e, "Cholesky look-ahead");
+      if ((e = cudaEventRecord(hs->side_start, s)) == cudaSuccess)
+        e = cudaStreamWaitEvent(hs->side, hs->side_start, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "Cholesky look-ahead");
       const int rem = d - (kb + 1) * kNB;
       const float* panel = Gh + static_cast<size_t>(kb + 1) * kNB * d + static_cast<size_t>(kb) * kNB;
       float* trail = Gh + static_cast<size_t>(kb + 1) * kNB * d + static_cast<size_t>(kb + 1) * kNB;
-      SgemmArgs g{rem, rem, kNB, -1.f, 1.f, panel, d, panel, d, trail, d, 1, 0, 0};
+      if (rem > kNB) {
+        const size_t skip = static_cast<size_t>(kNB) * d;
+        SgemmArgs g{rem - kNB, rem - kNB, kNB, -1.f, 1.f, panel + skip, d, panel + skip, d,
+                    trail + skip + kNB, d, 1, 0, 0};
+        if ((e = sgemm(true, g, hs->side)) != cudaSuccess) return cuda_fail(e, "Cholesky update");
+      }
+      if ((e = cudaEventRecord(hs->side_done, hs->side)) != cudaSuccess)
+        return cuda_fail(e, "Cholesky look-ahead");
+      SgemmArgs g{rem, kNB, kNB, -1.f, 1.f, panel, d, panel, d, trail, d, 0, 0, 0};
       if ((e = sgemm(true, g, s)) != cudaSuccess) return cuda_fail(e, "Cholesky update");
     }
+    if (nb > 1 && (e = cudaStreamWaitEvent(s, hs->side_done, 0)) != cudaSuccess)
+      return cuda_fail(e, "Cholesky look-ahead");
   }
   zero_upper_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gh, d);
   // X = L^-1 in place: the 64 x 64 diagonal blocks, then recursive doubling:
