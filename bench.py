@@ -54,7 +54,7 @@ FP32_LANES_PER_SM = 128
 # fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
 _FIT_LLAMA8B = {"sources": "fit",
                 "kernel_sha256": "c2bfcf9009a383123195d1a207ee52288dadb380ea9123bf2b227ac499869780",
-                "bytes_per_launch": 105417109760 + 2812521728}
+                "bytes_per_launch": 92237788416 + 2804967936}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
                     "kernel_sha256": "d7e39f3da74229b752c94c267b93e566a620e262b4a5146ab9330825cd4fe11c",
@@ -563,11 +563,12 @@ class FitWorkload:
             inv += 2 * ((1 if full > 0 else 0) + (1 if rest > sz else 0))
             sz *= 2
         # accumulate: two column-sum passes, their reduction, the count, the Gram products;
-        # solve: preparation, equilibration, Cholesky (diagonal block, panel, trailing
-        # update per block column), zero fill, diagonal-block inverses, the doubling
-        # products, the bf16 split, three G^-1 products, two operand splits, the solve GEMM,
-        # the offsets
-        return 5 + 2 + (3 * nb - 2) + 2 + inv + 1 + 3 + 2 + 1 + 1
+        # solve: preparation, equilibration, Cholesky (per block column the diagonal block,
+        # then panel, next-column update and, while more columns remain, the rest of the
+        # trailing update), zero fill, diagonal-block inverses, the doubling products, the
+        # bf16 split, three G^-1 products, two operand splits, the solve GEMM, the offsets
+        chol = nb + 2 * (nb - 1) + max(0, nb - 2)
+        return 5 + 2 + chol + 2 + inv + 1 + 3 + 2 + 1 + 1
 
     def setup(self, dev, seed):
         """Calibration pairs drawn on the device (synthetic.calibration_device)."""
