@@ -48,8 +48,8 @@ FP32_LANES_PER_SM = 128
 # DRAM bytes per launch of the dominant kernel from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum, one pass, full size), keyed by the bench line's workload and valid
 # only while the library sources that define that kernel hash to kernel_sha256 (otherwise
-# reported as null).  Captures: profiles/fill_launches_llama8b_16k.md (map GEMM) and
-# profiles/fit_launches_llama8b_rows65536.md (Gram accumulate).
+# reported as null).  The map GEMM's figure comes from a capture of the default fill, the
+# Gram accumulate's from a capture of the full fit.
 # The fit depends only on d, the number of maps and the calibration rows, which the Llama-8B
 # fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
 _FIT_LLAMA8B = {"sources": "fit",

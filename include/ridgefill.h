@@ -177,12 +177,13 @@ rf_status ridgefill_fill(const rf_fill_args* args, void* workspace, size_t works
  *    (rows_per_chunk, if set, caps it); results equal ridgefill_fill's.
  *  - If one 128-row chunk does not fit (n_layers * d_out too large) the call
  *    returns RF_ERR_WORKSPACE with the required size in ridgefill_last_error().
- *  - maps_on_host = 1 is rejected (RF_ERR_ARG).
+ *  - maps_on_host = 1 and h_on_host = 1 are rejected (RF_ERR_ARG).
  *  - The array is shared by all calls on a device and keeps the last call's
  *    contents (nothing in it needs to start at zero); calls that overlap on
  *    the GPU race on it, so order them on one stream.
- *  - The first call on a device looks up the array's address with that
- *    device current; make it before any stream capture.
+ *  - The first call on a device (and the first after its context changed)
+ *    looks up the array's address with that device current; make it before
+ *    any stream capture.
  */
 #define RF_NOALLOC_SCRATCH_BYTES (64u << 20)
 rf_status ridgefill_fill_noalloc(const rf_fill_args* args, void* stream);

@@ -474,16 +474,12 @@ static_assert(kStagesWide * kWideStageBytes <= kStages2 * 2 * kHalfBytes, "wide 
 
 namespace {
 
-// Tile t of a cluster of kCl CTAs: a unit of kCl / 2 consecutive pair row tiles (mu) that
-// share the column tile n, in batch b; grouped raster over units.
-template <int kCl>
-__device__ __forceinline__ int units_m(const GemmParams& p) {
-  return ((p.m_tiles + 1) / 2 + kCl / 2 - 1) / (kCl / 2);
-}
-template <int kCl>
+// Tile t of the pair grid: pair row tile mu (row tiles 2 mu and 2 mu + 1, one per CTA) of
+// column tile n, in batch b; grouped raster over pair row tiles.
+__device__ __forceinline__ int units_m(const GemmParams& p) { return (p.m_tiles + 1) / 2; }
 __device__ __forceinline__ void decode_unit(int t, const GemmParams& p, int& mu, int& n, int& b) {
-  const int m_units = units_m<kCl>(p);
-  const int gp = p.group_m / kCl > 0 ? p.group_m / kCl : 1;
+  const int m_units = units_m(p);
+  const int gp = p.group_m / 2 > 0 ? p.group_m / 2 : 1;
   const int per_b = m_units * p.n_tiles;
   b = t / per_b;
   const int r = t - b * per_b;
@@ -574,14 +570,9 @@ __device__ __forceinline__ void q8_convert(const uint8_t* raw, int sub, const ui
 // {d_out, d_in / 128, layers} bf16).  Warps 8-11 dequantise this CTA's B half of each
 // stage into shared memory and arrive on CTA 0's `full` barrier (released at cluster
 // scope; the MMA acquires at cluster scope before reading both halves).
-// kCl = 4 (Gram mode, 512-column tiles): two CTA pairs per cluster take pair row tiles 2 mu
-// and 2 mu + 1 of the same column tile; each pair loads half of the B boxes of every stage and
-// multicasts them to the same CTA half of both pairs, so the shared B panel is read once for
-// both, and each pair's MMA commit frees the stage in all four CTAs.
-template <bool kQ8, int kCl>
-__global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8 : kGemmThreads, 1)
+template <bool kQ8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8 : kGemmThreads, 1)
     rf_gemm2_kernel(const __grid_constant__ GemmParams p) {
-  static_assert(kCl == 2 || (kCl == 4 && !kQ8), "clusters of one or two CTA pairs");
   constexpr int kS = kQ8 ? kStagesQ8 : kStages2;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -605,17 +596,14 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const uint32_t crank = cluster_ctarank();
-  const uint32_t rank = crank & 1u;  // position in the CTA pair
-  const uint32_t sub = crank >> 1;   // pair within the cluster
-  const uint32_t lead = crank & ~1u;  // this pair's MMA CTA
-  const int cl = blockIdx.x / kCl, ncl = gridDim.x / kCl;
+  const uint32_t rank = cluster_ctarank();  // position in the CTA pair
+  const int cl = blockIdx.x / 2, ncl = gridDim.x / 2;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kS; ++s) {
       // both CTAs' producers (+ both CTAs' four converter warps)
       mbar_init(&full[s], kQ8 ? 10 : 2);
-      mbar_init(&empty[s], kCl / 2);  // the commit of each pair's MMA CTA
+      mbar_init(&empty[s], 1);  // the commit of the pair's MMA CTA
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
@@ -649,9 +637,9 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
   cluster_sync();  // both CTAs' barriers are initialised and their TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = units_m<kCl>(p) * p.n_tiles * p.batches;
-  const uint32_t full0 = cluster_addr(smem_u32(full), lead);
-  const uint32_t tempty0 = cluster_addr(smem_u32(tempty), lead);
+  const int total = units_m(p) * p.n_tiles * p.batches;
+  const uint32_t full0 = cluster_addr(smem_u32(full), 0);
+  const uint32_t tempty0 = cluster_addr(smem_u32(tempty), 0);
 
   if (warp == 0) {
     if (lane == 0) {
@@ -665,8 +653,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
       int h_seen = -1;  // last split-state row group known to be in device memory
       for (int t = cl; t < total && ok; t += ncl) {
         int mu, n, b;
-        decode_unit<kCl>(t, p, mu, n, b);
-        const int m = 2 * (mu * (kCl / 2) + static_cast<int>(sub)) + static_cast<int>(rank);
+        decode_unit(t, p, mu, n, b);
+        const int m = 2 * mu + static_cast<int>(rank);
         const TileB tb = tile_b(p, n);
         if (p.h_ready != nullptr && m * kBM < p.rows) {
           const int g = (p.h_row_base + m * kBM) / p.h_group_rows;
@@ -706,22 +694,11 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
               for (int j = 0; j < kBM / 64; ++j)
                 tma_load_3d_pair(smem_u32(adst + j * 8192), &p.tmA2, fb, m0 + 64 * j, kb * kBK, l);
             }
-            if (kCl == 2) {
-              for (int j = 0; j < half / 64; ++j)
-                tma_load_3d_pair(smem_u32(bdst + j * 8192), &p.tmB[0], fb,
-                                 tb.nrow + (j / bpm) * nmma + (nmma / 2) * static_cast<int>(rank) +
-                                     64 * (j % bpm),
-                                 kb * kBK, 0);
-            } else {
-              // this pair's share of the boxes, to this CTA and its counterpart in the other pair
-              const int nbox = half / 64, j0 = static_cast<int>(sub) * (nbox / 2);
-              const uint16_t mask = static_cast<uint16_t>((1u << rank) | (1u << (rank + 2)));
-              for (int j = j0; j < j0 + nbox / 2; ++j)
-                tma_load_3d_pair_mc(smem_u32(bdst + j * 8192), &p.tmB[0], fb,
-                                    tb.nrow + (j / bpm) * nmma +
-                                        (nmma / 2) * static_cast<int>(rank) + 64 * (j % bpm),
-                                    kb * kBK, 0, mask);
-            }
+            for (int j = 0; j < half / 64; ++j)
+              tma_load_3d_pair(smem_u32(bdst + j * 8192), &p.tmB[0], fb,
+                               tb.nrow + (j / bpm) * nmma + (nmma / 2) * static_cast<int>(rank) +
+                                   64 * (j % bpm),
+                               kb * kBK, 0);
           } else {
             tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, kb * kBK, m * kBM, b);
           }
@@ -753,7 +730,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
       bool ok = true;
       for (int t = cl; t < total && ok; t += ncl, ++it) {
         int mu, n, b;
-        decode_unit<kCl>(t, p, mu, n, b);
+        decode_unit(t, p, mu, n, b);
         const TileB tb = tile_b(p, n);
         const bool mn = !kQ8 && p.mode == kModeGram;
         const uint32_t idesc =
@@ -799,17 +776,17 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
               mma_bf16_pair(dt + 256, ad + 128 * k, bd1 + 128 * k, idesc, accum);
             }
           }
-          // frees the stage in every CTA whose copies write it
-          mma_commit_pair(&empty[stage], kCl == 4 ? 0xF : 0x3);
+          // frees the stage in both CTAs
+          mma_commit_pair(&empty[stage], 0x3);
           if (++stage == nst) {
             stage = 0;
             phase ^= 1;
           }
         }
-        if (ok) mma_commit_pair(&tfull[acc], static_cast<uint16_t>(3u << lead));
+        if (ok) mma_commit_pair(&tfull[acc], 0x3);
       }
       // every MMA issued has finished before TMEM is released
-      mma_commit_pair(fin, static_cast<uint16_t>(1u << lead));
+      mma_commit_pair(fin, 0x1);
       mbar_drain(fin, 0);
     }
   } else if (kQ8 && warp == 3) {
@@ -821,7 +798,7 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
       bool ok = true;
       for (int t = cl; t < total && ok; t += ncl) {
         int mu, n, b;
-        decode_unit<kCl>(t, p, mu, n, b);
+        decode_unit(t, p, mu, n, b);
         const TileB tb = tile_b(p, n);
         const int half = tb.bn / 2;
         const int brow0 = tb.nrow + half * static_cast<int>(rank);
@@ -853,8 +830,8 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
     int it = 0;
     for (int t = cl; t < total; t += ncl, ++it) {
       int mu, n, b;
-      decode_unit<kCl>(t, p, mu, n, b);
-      const int m = 2 * (mu * (kCl / 2) + static_cast<int>(sub)) + static_cast<int>(rank);
+      decode_unit(t, p, mu, n, b);
+      const int m = 2 * mu + static_cast<int>(rank);
       const bool wide = !kQ8 && p.mode == kModeGram && p.bn == kGramWideCols;
       const int acc = wide ? 0 : it & 1;
       const uint32_t acc_phase = wide ? it & 1 : (it >> 1) & 1;
@@ -936,44 +913,20 @@ __global__ void __cluster_dims__(kCl, 1, 1) __launch_bounds__(kQ8 ? kGemmThreads
 cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream) {
   // set on every launch: the attribute belongs to the current device, and the call is
   // cheap next to the kernel
-  cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<false, 2>,
+  cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
-  rf_gemm2_kernel<false, 2><<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(p);
-  return cudaGetLastError();
-}
-
-int gemm2_cl4_max_clusters() {
-  if (cudaFuncSetAttribute(rf_gemm2_kernel<false, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kGemmSmem) != cudaSuccess)
-    return 0;
-  cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(4 * 64, 1, 1);
-  cfg.blockDim = dim3(kGemmThreads, 1, 1);
-  cfg.dynamicSmemBytes = kGemmSmem;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, rf_gemm2_kernel<false, 4>, &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
-cudaError_t launch_gemm2_cl4(const GemmParams& p, int clusters, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<false, 4>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
-  if (e != cudaSuccess) return e;
-  rf_gemm2_kernel<false, 4><<<4 * clusters, kGemmThreads, kGemmSmem, stream>>>(p);
+  rf_gemm2_kernel<false><<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream) {
   // set on every launch: the attribute belongs to the current device, and the call is
   // cheap next to the kernel
-  cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<true, 2>,
+  cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<true>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
-  rf_gemm2_kernel<true, 2><<<2 * pairs, kGemmThreadsQ8, kGemmSmem, stream>>>(p);
+  rf_gemm2_kernel<true><<<2 * pairs, kGemmThreadsQ8, kGemmSmem, stream>>>(p);
   return cudaGetLastError();
 }
 

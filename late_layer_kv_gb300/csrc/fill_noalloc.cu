@@ -17,10 +17,11 @@
 //    the GPU (different streams without ordering, or different host threads)
 //    race on the array; order them on one stream.
 //  - The first call on a device looks up the array's device address (once per
-//    device, with that device current); make that first call before any
-//    stream capture.
-//  - Host-memory maps (maps_on_host = 1) are not supported here: their two
-//    map slots would not fit in the array.
+//    device and context, with that device current); make that first call
+//    before any stream capture.
+//  - Host-memory maps (maps_on_host = 1) are not supported here: their three
+//    map slots would not fit in the array.  Nor is a split state in host
+//    memory (h_on_host = 1).
 //  - The call itself allocates nothing: no cudaMalloc, cudaFree or allocating
 //    library routine.
 #include <mutex>
@@ -34,21 +35,58 @@ static __device__ __align__(256) unsigned char g_fill_scratch[RF_NOALLOC_SCRATCH
 
 constexpr int kMaxDev = 64;
 
-// Device address of g_fill_scratch on the current device (host code must not
-// use the symbol itself: on the host it only names a stand-in).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the context current on this thread (driver entry points looked up once).
+rf_status current_context_id(unsigned long long* id) {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (get_cur == nullptr || get_id == nullptr)
+    return fail(RF_ERR_CUDA, "driver entry points cuCtxGetCurrent / cuCtxGetId unavailable");
+  CUcontext ctx = nullptr;
+  if (get_cur(&ctx) != CUDA_SUCCESS) return fail(RF_ERR_CUDA, "cuCtxGetCurrent failed");
+  *id = 0;  // no context current yet
+  if (ctx != nullptr && get_id(ctx, id) != CUDA_SUCCESS)
+    return fail(RF_ERR_CUDA, "cuCtxGetId failed");
+  return RF_OK;
+}
+
+// Device address of g_fill_scratch in the current device's context (host code must not
+// use the symbol itself: on the host it only names a stand-in).  Looked up the first time
+// a device is used and again whenever that device's context has changed since (a reset
+// gives it a new context and the array a new address).
 rf_status scratch_address(void** out) {
   static void* addr[kMaxDev] = {};
+  static unsigned long long ctx_of[kMaxDev] = {};
   static std::mutex mu;
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDev) return fail(RF_ERR_CUDA, "device index %d out of range", dev);
+  unsigned long long ctx = 0;
+  rf_status st = current_context_id(&ctx);
+  if (st != RF_OK) return st;
   std::lock_guard<std::mutex> lk(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == 0 || ctx_of[dev] != ctx) {
     void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_fill_scratch);
+    e = cudaGetSymbolAddress(&p, g_fill_scratch);  // initialises the context if needed
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+    if (ctx == 0 && (st = current_context_id(&ctx)) != RF_OK) return st;
     addr[dev] = p;
+    ctx_of[dev] = ctx;
   }
   *out = addr[dev];
   return RF_OK;

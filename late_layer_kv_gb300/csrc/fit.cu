@@ -583,19 +583,10 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   p.gram_ld = d;
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
-  const int max_cl4 = wide ? gemm2_cl4_max_clusters() : 0;
-  cudaError_t e;
-  if (max_cl4 > 0) {
-    // two pairs per cluster share each B panel; as many clusters as can be resident
-    const int64_t tiles = static_cast<int64_t>((p.m_tiles + 3) / 4) * p.n_tiles;
-    const int clusters = static_cast<int>(tiles < max_cl4 ? tiles : max_cl4);
-    e = launch_gemm2_cl4(p, clusters, s);
-  } else {
-    const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
-    const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
-    if (pairs <= 0) return RF_OK;
-    e = launch_gemm2(p, pairs, s);
-  }
+  const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+  const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  if (pairs <= 0) return RF_OK;
+  const cudaError_t e = launch_gemm2(p, pairs, s);
   if (e != cudaSuccess) return cuda_fail(e, "Gram GEMM launch");
   return RF_OK;
 }

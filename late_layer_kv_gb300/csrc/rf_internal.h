@@ -131,10 +131,6 @@ struct GemmParams {
 cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream);
 // map mode on CTA pairs with int8 maps (p.q8, p.q8_scale); tmB unused
 cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream);
-// Gram mode with 512-column tiles on clusters of two CTA pairs sharing each B panel by
-// multicast; `clusters` clusters of 4, at most gemm2_cl4_max_clusters() (0 if unknown)
-cudaError_t launch_gemm2_cl4(const GemmParams& p, int clusters, cudaStream_t stream);
-int gemm2_cl4_max_clusters();
 
 // ------------------------------------------------------------ GDN state
 struct GdnStateParams {

@@ -322,18 +322,6 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-// The same load multicast to the CTAs of `mask` (same shared-memory offset in each); each
-// destination's bytes are counted on the mbarrier at `bar`'s offset in the MMA CTA of the
-// destination's own pair (`bar` names this CTA's pair leader)
-__device__ __forceinline__ void tma_load_3d_pair_mc(uint32_t dst, const CUtensorMap* tm, uint32_t bar,
-                                                    int32_t c0, int32_t c1, int32_t c2,
-                                                    uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(tm)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-      : "memory");
-}
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                    smem_u32(dst_smem)),

@@ -203,3 +203,34 @@ def test_host_split_state_bitwise_equal_device():
     K0, V0 = out[0]
     for K, V in out[1:]:
         assert torch.equal(K, K0) and torch.equal(V, V0)
+
+
+def test_full_size_dense27b_120k_chunked():
+    """The 27B-class shape at its longest prompt (d = 5120, 43 late layers, theta = 1e6,
+    115,904 prefix rows, positions up to 115,903), launched as the benchmark launches it:
+    16,384-row chunks.  Each cache tensor holds 43 * 8 * 120,000 * 128 elements, more
+    than 2^31, so the later layers are written at element offsets past 2^31.  Checked on
+    every layer at rows 0, 1, the last prefix row, both sides of every chunk boundary and
+    40 seeded random rows; the tail rows stay untouched."""
+    shape = WORKLOADS["dense27b_120k"]
+    rpc = 16384
+    inp = fill_inputs(shape, seed=1002)
+    Kc, Vc = _run(shape, inp, rows_per_chunk=rpc)
+    rows = shape.rows
+    assert Kc.numel() > 2 ** 31
+    rng = np.random.default_rng(3)
+    bounds = [c * rpc + e for c in range(1, -(-rows // rpc)) for e in (-1, 0)]
+    idx = sorted(set([0, 1, rows - 1] + bounds + rng.integers(0, rows, 40).tolist()))
+    gk = to_f64(Kc[:, :, idx])
+    gv = to_f64(Vc[:, :, idx])
+    Hs = to_f64(inp["H"][idx])
+    for l in range(shape.n_layers):
+        K, V = oracle.fill_attention(Hs, np.asarray(idx), to_f64(inp["A"][l:l + 1]),
+                                     to_f64(inp["b"][l:l + 1]), to_f64(inp["g"][l:l + 1]),
+                                     to_f64(inp["Wk"][l:l + 1]), to_f64(inp["Wv"][l:l + 1]),
+                                     shape.rms_eps, shape.rope_theta, shape.n_kv,
+                                     shape.head_dim)
+        compare(gk[l], K[0], f"K layer {l}")
+        compare(gv[l], V[0], f"V layer {l}")
+    for C in (Kc, Vc):
+        assert bool((C[:, :, rows:] == SENTINEL).all()), "fill wrote into the tail rows"

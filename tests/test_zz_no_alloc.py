@@ -4,8 +4,8 @@ Some callers (a host engine that owns every device buffer, or code running
 after the engine has divided up all device memory) can pass inputs and
 outputs but no workspace.  This entry point keeps its scratch in a
 library-owned static device array.  Here it is called through the C ABI and
-checked against ridgefill_fill on two calls in a row: the second call must not
-be affected by what the first left in the shared array.
+checked bit for bit against ridgefill_fill on two calls in a row: the second
+call must not be affected by what the first left in the shared array.
 
 This file is named to run last in a full test session; it also passes alone.
 """
@@ -14,8 +14,8 @@ import ctypes
 import pytest
 import torch
 
-from synthetic import FillShape, fill_inputs, to_f64
-from tests._fill_helpers import SENTINEL, compare, new_cache, to_cuda
+from synthetic import FillShape, fill_inputs
+from tests._fill_helpers import SENTINEL, new_cache, to_cuda
 
 pytestmark = pytest.mark.gpu
 
@@ -54,9 +54,10 @@ def test_noalloc_matches_workspace_fill_on_two_calls():
     for shape, seed, rpc in ((big, 21, 0), (small, 22, 256)):
         (K1, V1), (K2, V2) = _both(shape, seed, rpc)
         rows = shape.rows
-        for l in range(shape.n_layers):
-            compare(to_f64(K2[l, :, :rows]), to_f64(K1[l, :, :rows]), f"{shape.name} K layer {l}")
-            compare(to_f64(V2[l, :, :rows]), to_f64(V1[l, :, :rows]), f"{shape.name} V layer {l}")
+        # the per-row arithmetic does not depend on the chunking, so the two agree bit for
+        # bit; any difference would be left over from the shared array's previous contents
+        assert torch.equal(K2[:, :, :rows], K1[:, :, :rows]), f"{shape.name}: K differs"
+        assert torch.equal(V2[:, :, :rows], V1[:, :, :rows]), f"{shape.name}: V differs"
         assert bool((K2[:, :, rows:] == SENTINEL).all()) and bool((V2[:, :, rows:] == SENTINEL).all())
 
 
