@@ -42,8 +42,6 @@ from synthetic import (WORKLOADS, FillShape, GdnShape, calibration_device,  # no
 METRIC = "filled token-layers/s (fill-stage ms and % of GB300 bf16 tensor peak alongside)"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                   "sm_max_mhz": 2070.0}
-N_SM = 152
-FP32_LANES_PER_SM = 128
 
 # DRAM bytes per launch of the dominant kernel from an ncu capture (dram__bytes_read.sum +
 # dram__bytes_write.sum, one pass, full size), keyed by the bench line's workload and valid
@@ -226,10 +224,10 @@ class AttnWorkload:
         # rescale: map GEMM, true-input norm, value GEMM, ratio
         return chunks * per_chunk + (4 if self.c else 0)
 
-    def setup(self, dev, seed):
+    def setup(self, dev, seed, inp=None):
         from late_layer_kv_gb300 import ridgefill as rb
         s = self.shape
-        self.inp = fill_inputs(s, seed=seed)
+        self.inp = fill_inputs(s, seed=seed) if inp is None else inp
         self.d = {k: v.to(dev) for k, v in self.inp.items()}
         self.A_scale = None
         if self.q8:  # int8 maps with one bf16 scale per 128 weights, made on the device
@@ -373,6 +371,22 @@ class AttnWorkload:
                     s.n_layers * s.d * s.d * 2 >> 20, s.rows * s.d * 2 >> 20)}
 
 
+def gdn_state_tensor_flop(rows: int, layers: int, heads: int, chunk: int = 64,
+                          d: int = 128) -> float:
+    """FLOPs the chunked gated-delta-rule state kernel issues on the tensor cores (one
+    (layer, head) state of d x d per CTA, chunks of 64 rows; every product on bf16 high
+    and low parts).  Per chunk, in M x N x K shapes of 2 M N K FLOP each:
+    P = K K^T: 16 of 128 x 64 x 16 (the stacked [K_hi; K_lo] against K_hi, K_lo);
+    U^T: 4 of 128 x 128 x 16 and 4 of 128 x 64 x 16;  W^T: 12 of 128 x 64 x 16;
+    NEW^T = U^T - S W^T: 8 of 128 x 128 x 16 and 8 of 128 x 64 x 16;
+    S += NEW'^T K: 12 of 128 x 128 x 16."""
+    n128 = 4 + 8 + 12          # 128 x 128 x 16 products
+    n64 = 16 + 4 + 12 + 8      # 128 x 64 x 16 products
+    per_chunk = 2.0 * 16 * d * (n128 * d + n64 * chunk)
+    chunks = -(-rows // chunk)
+    return per_chunk * chunks * layers * heads
+
+
 class HybridWorkload:
     """Gated DeltaNet late layers (ridgefill_fill_gdn) plus attention late layers."""
 
@@ -393,12 +407,13 @@ class HybridWorkload:
             # with exact rows the GDN map GEMM runs on the filled rows only
             "gdn_map_gemm": 2.0 * (s.rows - self.n_exact) * Lg * s.d * s.d,
             "gdn_proj_gemm": 2.0 * s.rows * Lg * s.d * proj,
-            # per row and head: dot product and rank-1 update, one FMA per state element each
-            "gdn_state": 4.0 * s.rows * Lg * H * s.d_v * s.d_k,
+            "gdn_state": gdn_state_tensor_flop(s.rows, Lg, H),
         }
         self.stage_bound = {k: "tensor" for k in self.stage_names}
-        self.stage_bound["gdn_state"] = "alu"
-        self.total_flops = sum(v for k, v in self.stage_work.items() if k != "gdn_state")
+        # the layer's own work counted once: the state as the recurrence's 4 d_v d_k per row
+        # and head (the chunked form issues more on the tensor cores, its split products)
+        self.total_flops = sum(v for k, v in self.stage_work.items() if k != "gdn_state") + \
+            4.0 * s.rows * Lg * H * s.d_v * s.d_k
 
     def launches_per_step(self):
         # attention map + K/V + RoPE table (+ gather), GDN map, projection, state (+ filled-row
@@ -720,26 +735,18 @@ def h2d_rate_gbs(dev, nbytes=32 << 20, reps=20):
     return best
 
 
-def run_ours(args):
-    world, rank, local = _dist()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
+def _measure(wl, stream, steps, warmup, world, dev, local):
+    """Warm-up, then `steps` timed steps bracketed by a barrier and a device sync, with
+    the library's stage events per step and nvidia-smi clocks sampled meanwhile.
+    Returns (timed-region ms, the max over ranks; per-step events; clocks)."""
     from late_layer_kv_gb300 import device_error
-    wl = make_workload(args.workload, args)
-    wl.setup(dev, seed=1001 + rank)
-    stream = torch.cuda.current_stream(dev)
-    steps = args.steps
     ev = [_events(wl.n_events()) for _ in range(steps)]
     for e in sum(ev, []):
         e.record(stream)  # torch creates the CUDA event on first record
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         wl.step(stream)
     torch.cuda.synchronize()
     assert device_error(stream) == 0, "device wait ran out during warm-up"
-
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -756,35 +763,128 @@ def run_ours(args):
         torch.distributed.barrier()
     clk = clocks.stop()
     assert device_error(stream) == 0, "device wait ran out during the timed region"
-    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
-    ms_step = ms / steps
-    value = whole_job_rate(wl.token_layers, world, ms_step)
+    return max_over_ranks(t0.elapsed_time(t1), world, dev), ev, clk
 
+
+def _stages(wl, ev, ms):
+    """Per-stage mean ms, achieved TFLOP/s and fraction of the bf16 peak (burst for timed
+    regions under 2 s, sustained otherwise), and the dominant stage's roofline."""
     peaks, src = _peaks()
-    sustained = ms >= 2000.0  # long regions run under the power cap
-    pkey = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    pkey = "bf16_tflops_sustained" if ms >= 2000.0 else "bf16_tflops"
     tpeak = float(peaks[pkey])
-    alu_mhz = float(peaks.get("sm_max_mhz", 2070.0))
-    alu_peak = N_SM * FP32_LANES_PER_SM * 2 * alu_mhz * 1e6 / 1e12
     stages = {}
     for name in wl.stage_names:
         sm = float(np.mean([wl.stage_ms(e)[name] for e in ev]))
         ach = wl.stage_work[name] / (sm / 1000.0) / 1e12
-        pk = tpeak if wl.stage_bound[name] == "tensor" else alu_peak
         stages[name] = {"ms": sm, "achieved_tflops": ach, "bound": wl.stage_bound[name],
-                        "frac": ach / pk}
+                        "frac": ach / tpeak}
     dom = max(stages, key=lambda k: stages[k]["ms"])
     traffic = None
     pt = PROFILED_TRAFFIC.get(wl.config()["workload"])
     if pt and pt["kernel_sha256"] == _kernel_digest(pt["sources"]):
         traffic = pt["bytes_per_launch"]
-    dpk = tpeak if stages[dom]["bound"] == "tensor" else alu_peak
     roofline = {"bound": stages[dom]["bound"], "kernel": dom,
-                "achieved": stages[dom]["achieved_tflops"], "peak": dpk, "unit": "TFLOP/s",
-                "frac": stages[dom]["achieved_tflops"] / dpk, "traffic": traffic,
-                "peak_source": (f"{src} {pkey}" if stages[dom]["bound"] == "tensor" else
-                                f"{N_SM} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {alu_mhz} MHz"),
-                "timed_region_ms": ms}
+                "achieved": stages[dom]["achieved_tflops"], "peak": tpeak, "unit": "TFLOP/s",
+                "frac": stages[dom]["achieved_tflops"] / tpeak, "traffic": traffic,
+                "peak_source": f"{src} {pkey}", "timed_region_ms": ms}
+    return stages, roofline, tpeak
+
+
+def _host_link(wl, ev, stages, dev):
+    """Map-copy rates of a host-map fill against the measured pinned host-to-device link."""
+    s = wl.shape
+    link = h2d_rate_gbs(dev)
+    # bytes per layer on the link: bf16 maps, or int8 codes plus bf16 scales
+    layer_bytes = s.d * s.d * 2 if not wl.q8 else s.d * s.d + s.d * (s.d // 128) * 2
+    map_bytes = s.n_layers * layer_bytes
+    mstage = stages["map_gemm"]["ms"]
+    cms = [t for e in ev for t in wl.copy_ms(e)]
+    # median per copy: the pool's host link shows stalls of tens of ms from other tenants,
+    # which the mean (also reported) takes in
+    copy_gbs = layer_bytes / (float(np.median(cms)) / 1000.0) / 1e9
+    copy_gbs_mean = layer_bytes / (float(np.mean(cms)) / 1000.0) / 1e9
+    one = wl.A[0].view(-1)  # the maps' own pinned buffer, alone on the link
+    tmp = torch.empty_like(one, device=dev)
+    maps_buf = max(one.numel() * one.element_size() / (t / 1000.0) / 1e9 for t in
+                   [_copy_ms(tmp, one) for _ in range(10)])
+    return {"h2d_gbs_measured": link, "maps_buffer_h2d_gbs": maps_buf,
+            "map_bytes_per_step": map_bytes,
+            "copy_gbs": copy_gbs, "copy_gbs_mean": copy_gbs_mean,
+            "copy_frac_of_link": copy_gbs / link,
+            "map_stage_gbs": map_bytes / (mstage / 1000.0) / 1e9,
+            "note": "maps copied per layer on a side stream while the previous layer "
+                    "computes; copy_gbs is the median rate of those copies (events on "
+                    "the copy stream), copy_gbs_mean their mean, map_stage_gbs the rate "
+                    "the maps flowed through the map stage"}
+
+
+def _secondary(args, head, dev, stream, local):
+    """The other workloads, each timed on its own (CUDA events on the launching stream,
+    its own warm-up and clocks): maps streamed from host memory, the hybrid Gated
+    DeltaNet fill, the 27B-class fill at its shortest and longest prompt, and the fit."""
+    out = {}
+
+    def run(name, wl, steps, setup):
+        t = time.perf_counter()
+        setup(wl)
+        ms, ev, clk = _measure(wl, stream, steps, max(3, min(args.warmup, 5)), 1, dev, local)
+        stages, roof, _ = _stages(wl, ev, ms)
+        ms_step = ms / steps
+        e = {"config": wl.config(), "steps": steps, "ms_per_step": ms_step,
+             "value": wl.token_layers / (ms_step / 1000.0),
+             "unit": getattr(wl, "unit", "token-layers/s"),
+             "pct_bf16_peak": 100.0 * wl.total_flops / (ms_step / 1000.0) / 1e12 / roof["peak"],
+             "stages": stages, "roofline": roof, "clocks": clk,
+             "gpu_launches": wl.launches_per_step() * steps}
+        if getattr(wl, "host_maps", False):
+            e["host_link"] = _host_link(wl, ev, stages, dev)
+        e["wall_s"] = time.perf_counter() - t
+        out[name] = e
+        return wl
+
+    seed = 1001
+    wl = run("hostmaps_16k", AttnWorkload(WORKLOADS["hostmaps_16k"], host_maps=True),
+             min(args.steps, 20), lambda w: w.setup(dev, seed, inp=head.inp))
+    del wl
+    torch.cuda.empty_cache()
+    wl = run("hybrid_gdn_32k", HybridWorkload(WORKLOADS["hybrid_gdn_32k"]),
+             min(args.steps, 20), lambda w: w.setup(dev, seed))
+    del wl
+    torch.cuda.empty_cache()
+    big = fill_inputs(WORKLOADS["dense27b_120k"], seed=seed)
+    wl = run("dense27b_120k", AttnWorkload(WORKLOADS["dense27b_120k"], rows_per_chunk=16384),
+             min(args.steps, 8), lambda w: w.setup(dev, seed, inp=big))
+    del wl
+    torch.cuda.empty_cache()
+    small = dict(big)
+    small["H"] = big["H"][:WORKLOADS["dense27b_16k"].rows]
+    wl = run("dense27b_16k", AttnWorkload(WORKLOADS["dense27b_16k"], rows_per_chunk=16384),
+             min(args.steps, 20), lambda w: w.setup(dev, seed, inp=small))
+    del wl, big, small
+    torch.cuda.empty_cache()
+    shape = WORKLOADS["hostmaps_16k"]
+    wl = run("fit", FitWorkload(shape, shape.calib_rows), min(args.steps, 10),
+             lambda w: w.setup(dev, seed))
+    del wl
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args):
+    world, rank, local = _dist()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = make_workload(args.workload, args)
+    wl.setup(dev, seed=1001 + rank)
+    stream = torch.cuda.current_stream(dev)
+    steps = args.steps
+    ms, ev, clk = _measure(wl, stream, steps, args.warmup, world, dev, local)
+    ms_step = ms / steps
+    value = whole_job_rate(wl.token_layers, world, ms_step)
+    stages, roofline, tpeak = _stages(wl, ev, ms)
     pct = 100.0 * wl.total_flops / (ms_step / 1000.0) / 1e12 / tpeak
 
     e2e = None
@@ -801,40 +901,27 @@ def run_ours(args):
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1) / steps, world, dev)
         e2e = {"value": whole_job_rate(wl.token_layers, world, ems), "unit": getattr(wl, "unit", "token-layers/s"),
-               "ms_per_step": ems, "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo)}
+               "ms_per_step": ems, "h2d_bytes_per_step": int(bi), "d2h_bytes_per_step": int(bo),
+               "note": "H copied from pinned host memory inside the timed region; the caches "
+                       "stay on the device (their consumer is the exact tail's attention), "
+                       "two cache rows per layer are read back" if isinstance(wl, AttnWorkload)
+                       else None}
 
     host_link = None
     if getattr(wl, "host_maps", False):
-        s = wl.shape
-        link = h2d_rate_gbs(dev)
-        # bytes per layer on the link: bf16 maps, or int8 codes plus bf16 scales
-        layer_bytes = s.d * s.d * 2 if not wl.q8 else s.d * s.d + s.d * (s.d // 128) * 2
-        map_bytes = s.n_layers * layer_bytes
-        mstage = stages["map_gemm"]["ms"]
-        cms = [t for e in ev for t in wl.copy_ms(e)]
-        # median per copy: the pool's host link shows stalls of tens of ms from other
-        # tenants, which the mean (also reported) takes in
-        copy_gbs = layer_bytes / (float(np.median(cms)) / 1000.0) / 1e9
-        copy_gbs_mean = layer_bytes / (float(np.mean(cms)) / 1000.0) / 1e9
-        one = wl.A[0].view(-1)  # the maps' own pinned buffer, alone on the link
-        tmp = torch.empty_like(one, device=dev)
-        maps_buf = max(one.numel() * one.element_size() / (t / 1000.0) / 1e9 for t in
-                       [_copy_ms(tmp, one) for _ in range(10)])
-        host_link = {"h2d_gbs_measured": link, "maps_buffer_h2d_gbs": maps_buf,
-                     "map_bytes_per_step": map_bytes,
-                     "copy_gbs": copy_gbs, "copy_gbs_mean": copy_gbs_mean,
-                     "copy_frac_of_link": copy_gbs / link,
-                     "map_stage_gbs": map_bytes / (mstage / 1000.0) / 1e9,
-                     "note": "maps copied per layer on a side stream while the previous layer "
-                             "computes; copy_gbs is the median rate of those copies (events on "
-                             "the copy stream), copy_gbs_mean their mean, map_stage_gbs the rate "
-                             "the maps flowed through the map stage"}
+        host_link = _host_link(wl, ev, stages, dev)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         r, dt, what = wl.cpu_rate(args.cpu_flop)
         cpu = {"value": r, "unit": getattr(wl, "unit", "token-layers/s"), "cores": _cores(), "kind": "oracle",
                "sample": f"{what} ({dt:.1f} s of f64 numpy work)"}
+
+    secondary = None
+    plain = (args.workload == "llama8b_16k" and not (args.fit or args.rows or args.layers or
+             args.rows_per_chunk or args.exact_frac or args.int8_maps or args.rescale))
+    if world == 1 and plain and not args.no_secondary:
+        secondary = _secondary(args, wl, dev, stream, local)
 
     if rank == 0:
         line = {
@@ -848,6 +935,8 @@ def run_ours(args):
         }
         if host_link:
             line["host_link"] = host_link
+        if secondary:
+            line["secondary"] = secondary
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -898,6 +987,8 @@ def main():
                     help="f64 work per step of the reference arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="default workload: skip the other workloads timed after the headline")
     ap.add_argument("--rows", type=int, default=0, help="override the filled rows (profiling)")
     ap.add_argument("--layers", type=int, default=0, help="override the late layers (profiling)")
     ap.add_argument("--rows-per-chunk", type=int, default=0)

@@ -44,7 +44,10 @@ typedef enum rf_status {
   RF_ERR_CUDA = 5,       /* a CUDA call failed; see ridgefill_last_error()      */
   RF_ERR_TIMEOUT = 6,    /* a device wait ran out (see ridgefill_device_error)  */
   RF_ERR_NUMERIC = 7,    /* the ridge system was not positive definite          */
-  RF_ERR_WORKSPACE = 8   /* workspace pointer NULL or smaller than required     */
+  RF_ERR_WORKSPACE = 8,  /* workspace pointer NULL or smaller than required     */
+  RF_ERR_SOURCE = 9,     /* a host map source (map_source) returned an error    */
+  RF_ERR_BOUNDS = 10     /* debug library only: a kernel store fell outside its
+                            buffer, or a workspace guard band was overwritten   */
 } rf_status;
 
 /* ------------------------------------------------------------------------ */
@@ -120,7 +123,34 @@ typedef enum rf_status {
  *   -1 converts the codes inside the map GEMM's shared-memory stages instead
  *   (no extra workspace, bound by shared-memory bandwidth, about 9 % slower).
  *   Both give bitwise the same results.
+ * map_source, map_source_user, map_staging, host_wait_ms (optional; map_source
+ *   may be NULL): maps produced on the host one layer at a time, for maps that
+ *   are not all held in page-locked memory (read from a file, decompressed,
+ *   paged in): section 4.2's streamed maps with the host side as the source.
+ *   Needs maps_on_host = 1; A (and A_scale) are then ignored and may be NULL,
+ *   except that a non-NULL A_scale still selects int8 maps.  For every row
+ *   chunk and layer l, in order, the call waits until staging half j (layers
+ *   alternate between the two halves of map_staging) is no longer being
+ *   copied, calls map_source(map_source_user, l, half j, slot_bytes), which
+ *   must write layer l's map there and return 0, and enqueues the copy of
+ *   half j into a device map slot.  slot_bytes = d_out * d_in * 2 for bf16
+ *   maps; for int8 maps the codes [d_out, d_in] come first and the bf16 scales
+ *   [d_in / 128, d_out] start at d_out * d_in rounded up to 256, slot_bytes =
+ *   that offset + d_out * (d_in / 128) * 2.  map_staging is page-locked host
+ *   memory of 2 * slot_bytes, 16-byte aligned.  Unlike every other use of
+ *   this call, it returns only after the last layer's map has been handed to
+ *   the copy engine (the kernels may still be running).
+ *   Bounded host waits: a staging half that is still being copied after
+ *   host_wait_ms milliseconds (0 means 10000), or a map_source call that takes
+ *   longer than that, ends the call with RF_ERR_TIMEOUT; a non-zero return of
+ *   map_source ends it with RF_ERR_SOURCE.  Work already enqueued for earlier
+ *   layers then still completes normally (nothing waits for the missing
+ *   layer), the K/V of the current row chunk are not written, and the caller
+ *   should synchronise `stream` before reusing the buffers.  map_source runs
+ *   on the calling thread and must return.
  */
+typedef int32_t (*rf_map_source_fn)(void* user, int32_t layer, void* dst, size_t bytes);
+
 typedef struct rf_fill_args {
   int32_t n_layers;
   int32_t d_in;
@@ -151,6 +181,11 @@ typedef struct rf_fill_args {
   int64_t h_rows;
   int32_t h_on_host;
   int32_t q8_group_layers;
+  rf_map_source_fn map_source;
+  void* map_source_user;
+  void* map_staging;
+  int32_t host_wait_ms;
+  int32_t reserved;
 } rf_fill_args;
 
 /* Bytes of device workspace ridgefill_fill needs for these arguments

@@ -8,6 +8,7 @@ from .ridgefill import (  # noqa: F401
     FitSums,
     RidgeFillError,
     compute_share,
+    debug_library,
     device_error,
     load,
     library_path,

@@ -177,6 +177,8 @@ HostStreamer* host_streamer() {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.side_done, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.h_done, cudaEventDisableTiming);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+      e = cudaEventCreateWithFlags(&h.staged[i], cudaEventDisableTiming);
     if (e != cudaSuccess) {
       cuda_fail(e, "creating the map-copy stream");
       h.copy = nullptr;
@@ -244,6 +246,8 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   p.bias = m.bias;
   p.gain = static_cast<const __nv_bfloat16*>(m.gain);
   p.ss_part = m.ss;
+  p.lim_a = static_cast<int64_t>(m.n_layers) * p.ss_tiles * m.R;
+  p.lim_b = static_cast<int64_t>(m.n_layers) * m.R * m.d_out;
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
   const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
@@ -307,6 +311,43 @@ cudaError_t copy_map_layer(uint8_t* slot, const void* A, const void* A_scale, in
                          cudaMemcpyHostToDevice, copy);
 }
 
+namespace {
+constexpr uint32_t kGuardWord = 0x7FC0DEADu;  // a NaN pattern no kernel result repeats by chance
+
+struct GuardSet {
+  uint64_t off[kMaxGuards];
+  int n;
+};
+
+__global__ void guard_kernel(uint8_t* ws, const __grid_constant__ GuardSet g, int check, int* err) {
+  constexpr int kWords = static_cast<int>(kGuardBytes / 4);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < g.n * kWords; i += gridDim.x * blockDim.x) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(ws + g.off[i / kWords]) + i % kWords;
+    if (!check) *w = kGuardWord;
+    else if (*w != kGuardWord) atomicCAS(err, 0, static_cast<int>(kErrGuard));
+  }
+}
+
+rf_status guards_launch(void* ws, const Layout& lay, int check, cudaStream_t s) {
+  if (!kDebug || lay.n == 0) return RF_OK;
+  GuardSet g{};
+  g.n = lay.n;
+  for (int i = 0; i < lay.n; ++i) g.off[i] = lay.guard[i];
+  int* err = device_error_word();
+  if (err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
+  guard_kernel<<<32, 256, 0, s>>>(static_cast<uint8_t*>(ws), g, check, err);
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? RF_OK : cuda_fail(e, "workspace guard launch");
+}
+}  // namespace
+
+rf_status guards_fill(void* ws, const Layout& lay, cudaStream_t s) {
+  return guards_launch(ws, lay, 0, s);
+}
+rf_status guards_check(void* ws, const Layout& lay, cudaStream_t s) {
+  return guards_launch(ws, lay, 1, s);
+}
+
 rf_status check_pinned(const void* ptr, const char* what) {
   cudaPointerAttributes attr;
   cudaError_t e = cudaPointerGetAttributes(&attr, ptr);
@@ -336,6 +377,8 @@ extern "C" const char* ridgefill_status_string(rf_status s) {
     case RF_ERR_TIMEOUT: return "device wait timed out";
     case RF_ERR_NUMERIC: return "ridge system not positive definite";
     case RF_ERR_WORKSPACE: return "workspace missing or too small";
+    case RF_ERR_SOURCE: return "the host map source reported an error";
+    case RF_ERR_BOUNDS: return "debug build: out-of-bounds store or overwritten guard band";
   }
   return "unknown status";
 }
@@ -362,6 +405,8 @@ extern "C" rf_status ridgefill_device_error(void* stream, int* code) {
   if (v == 0) return RF_OK;
   if (v == rf::kErrNumeric) return rf::fail(RF_ERR_NUMERIC, "ridge system not positive definite");
   if (v == rf::kErrIndex) return rf::fail(RF_ERR_ARG, "a row index list entry was out of range");
+  if (v == rf::kErrGuard) return rf::fail(RF_ERR_BOUNDS, "a workspace guard band was overwritten");
+  if (v == rf::kErrBounds) return rf::fail(RF_ERR_BOUNDS, "a kernel store fell outside its buffer");
   return rf::fail(RF_ERR_TIMEOUT, "device wait ran out at site %d", v);
 }
 
@@ -409,7 +454,7 @@ extern "C" rf_status ridgefill_wait_selftest(int32_t which, void* stream) {
   return RF_OK;
 }
 
-extern "C" int32_t ridgefill_abi_version(void) { return 9; }
+extern "C" int32_t ridgefill_abi_version(void) { return 10; }
 
 extern "C" size_t ridgefill_workspace_size(int32_t which, const void* args) {
   if (args == nullptr) {

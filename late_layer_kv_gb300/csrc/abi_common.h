@@ -33,6 +33,29 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Workspace layout: regions at 256-byte boundaries, in order.  A debug build follows every
+// region with a guard band of kGuardBytes; guards_fill writes a pattern into the bands
+// before a call's first launch and guards_check compares them after its last (a changed
+// word sets kErrGuard in the device error word).  Release builds add no bands.
+constexpr size_t kGuardBytes = 4096;
+constexpr int kMaxGuards = 24;
+struct Layout {
+  size_t off = 0;
+  int n = 0;
+  size_t guard[kMaxGuards] = {};
+  size_t take(size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    if (kDebug && n < kMaxGuards) {
+      guard[n++] = off;
+      off += kGuardBytes;
+    }
+    return o;
+  }
+};
+rf_status guards_fill(void* ws, const Layout& lay, cudaStream_t s);
+rf_status guards_check(void* ws, const Layout& lay, cudaStream_t s);
+
 // Device slots for maps streamed from host memory: the copy of layer l + 2
 // can run while layer l computes and layer l + 1 waits.
 constexpr int kMapSlots = 3;
@@ -48,6 +71,7 @@ struct HostStreamer {
   cudaEvent_t start = nullptr;
   cudaEvent_t h_done = nullptr;  // split state copied from host memory
   uint32_t h_gen = 0;            // value that marks this call's row groups ready
+  cudaEvent_t staged[2] = {};    // host map source: copy out of staging half j done
 };
 
 // Stream write of a 32-bit value by the GPU's front end, no SM involved: marks a

@@ -6,8 +6,10 @@
 // memory the map GEMM runs one layer at a time while the next layer's map is
 // copied into the other device slot on a side stream (paper section 4.2:
 // maps held in VRAM or streamed from host, identical outputs).
+#include <chrono>
 #include <cmath>
 #include <mutex>
+#include <thread>
 
 #include "abi_common.h"
 #include "sm103_ptx.cuh"
@@ -22,6 +24,7 @@ struct FillPlan {
   size_t off_dq = 0;
   size_t off_xhat = 0, off_ss = 0, off_slots = 0, off_gather = 0, off_hdev = 0, off_hflags = 0,
          off_rope = 0, total = 0;
+  Layout lay;
 };
 
 rf_status validate_fill(const rf_fill_args* a) {
@@ -57,7 +60,48 @@ rf_status validate_fill(const rf_fill_args* a) {
   if (a->h_on_host != 0 && a->h_on_host != 1) return fail(RF_ERR_ARG, "h_on_host must be 0 or 1");
   if (a->h_on_host && a->row_idx != nullptr)
     return fail(RF_ERR_ARG, "h_on_host cannot be combined with row_idx");
+  if (a->map_source != nullptr && a->maps_on_host != 1)
+    return fail(RF_ERR_ARG, "map_source needs maps_on_host = 1");
+  if (a->host_wait_ms < 0) return fail(RF_ERR_ARG, "host_wait_ms must be >= 0");
   return RF_OK;
+}
+
+using Clock = std::chrono::steady_clock;
+
+// Bounded host wait for event `ev` (cudaEventQuery polling): RF_ERR_TIMEOUT after `ms`.
+rf_status host_wait_event(cudaEvent_t ev, int ms, const char* what) {
+  const auto t0 = Clock::now();
+  for (;;) {
+    const cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return RF_OK;
+    if (e != cudaErrorNotReady) return cuda_fail(e, what);
+    if (Clock::now() - t0 > std::chrono::milliseconds(ms))
+      return fail(RF_ERR_TIMEOUT, "%s: still pending after %d ms", what, ms);
+    std::this_thread::sleep_for(std::chrono::microseconds(50));
+  }
+}
+
+// Layer l's map from the caller's host source into staging half j, after the previous copy
+// out of that half has finished; then its copy into the device slot on the copy stream.
+rf_status source_map_layer(const rf_fill_args* a, HostStreamer* hs, int j, int l, uint8_t* slot,
+                           size_t slot_bytes, const void** dA, const void** dS) {
+  const int ms = a->host_wait_ms > 0 ? a->host_wait_ms : 10000;
+  rf_status st = host_wait_event(hs->staged[j], ms, "copy out of a map staging half");
+  if (st != RF_OK) return st;
+  uint8_t* half = static_cast<uint8_t*>(a->map_staging) + j * slot_bytes;
+  const auto t0 = Clock::now();
+  const int32_t rc = a->map_source(a->map_source_user, l, half, slot_bytes);
+  const auto took = std::chrono::duration_cast<std::chrono::milliseconds>(Clock::now() - t0).count();
+  if (rc != 0) return fail(RF_ERR_SOURCE, "map_source returned %d for layer %d", rc, l);
+  if (took > ms)
+    return fail(RF_ERR_TIMEOUT, "map_source took %lld ms for layer %d (limit %d ms)",
+                static_cast<long long>(took), l, ms);
+  const size_t n = static_cast<size_t>(a->d_out) * a->d_in;
+  const bool q8 = a->A_scale != nullptr;
+  cudaError_t e = copy_map_layer(slot, half, q8 ? half + align_up(n, 256) : nullptr, 0, a->d_out,
+                                 a->d_in, hs->copy, dA, dS);
+  if (e == cudaSuccess) e = cudaEventRecord(hs->staged[j], hs->copy);
+  return e == cudaSuccess ? RF_OK : cuda_fail(e, "copying a map out of its staging half");
 }
 
 void plan_fill(const rf_fill_args* a, FillPlan* pl) {
@@ -67,23 +111,24 @@ void plan_fill(const rf_fill_args* a, FillPlan* pl) {
   const int64_t all = ceil_div(a->rows > 0 ? a->rows : 1, kBM) * kBM;
   pl->R = a->rows_per_chunk > 0 ? (a->rows_per_chunk < all ? a->rows_per_chunk : all) : all;
   const size_t L = a->n_layers, d = a->d_out;
-  pl->off_xhat = 0;
-  pl->off_ss = align_up(L * pl->R * d * 2, 256);
-  pl->off_slots = align_up(pl->off_ss + L * (d / pl->bn_map) * pl->R * 4, 256);
+  Layout& lay = pl->lay;
+  pl->off_xhat = lay.take(L * pl->R * d * 2);
+  pl->off_ss = lay.take(L * (d / pl->bn_map) * pl->R * 4);
   const size_t slots =
       a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0;
-  pl->off_gather = align_up(pl->off_slots + slots, 256);
+  pl->off_slots = lay.take(slots);
   const size_t gather = a->row_idx != nullptr ? static_cast<size_t>(pl->R) * a->d_in * 2 : 0;
-  pl->off_hdev = align_up(pl->off_gather + gather, 256);
+  pl->off_gather = lay.take(gather);
   size_t hflags = 0;
   const size_t hbytes = a->h_on_host ? host_rows_bytes(a->rows, a->d_in, &hflags) : 0;
+  pl->off_hdev = lay.take(hbytes);
   pl->off_hflags = pl->off_hdev + hflags;
-  pl->off_rope = align_up(pl->off_hdev + hbytes, 256);
   const size_t rope = static_cast<size_t>(a->head_dim / 2) * pl->R * 8;  // (cos, sin) f32 pairs
-  pl->off_dq = align_up(pl->off_rope + rope, 256);
+  pl->off_rope = lay.take(rope);
   pl->dq_layers = q8_group(a->q8_group_layers, a->A_scale != nullptr, a->maps_on_host != 0,
                            a->n_layers);
-  pl->total = align_up(pl->off_dq + static_cast<size_t>(pl->dq_layers) * a->d_out * a->d_in * 2, 256);
+  pl->off_dq = lay.take(static_cast<size_t>(pl->dq_layers) * a->d_out * a->d_in * 2);
+  pl->total = lay.off;
 }
 
 // RoPE angles of one row chunk (rotate-half pairs, frequency f_i = theta^(-2i/hd)):
@@ -185,6 +230,7 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
     p.kv_cache[0] = static_cast<__nv_bfloat16*>(a->Kc);
     p.kv_cache[1] = static_cast<__nv_bfloat16*>(a->Vc);
     p.cache_len = a->cache_len;
+    p.lim_b = static_cast<int64_t>(a->n_layers) * a->n_kv_heads * a->cache_len * a->head_dim;
   }
   for (int i = 0; i < a->head_dim / 2; ++i) {
     const double f = std::pow(a->rope_theta, -2.0 * i / a->head_dim);
@@ -229,18 +275,22 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
   rf_status st = validate_fill(a);
   if (st != RF_OK) return st;
   if (a->rows == 0) return RF_OK;
-  const void* req[] = {a->H, a->A, a->bias, a->Wk, a->Wv, a->Kc, a->Vc};
+  const bool sourced = a->map_source != nullptr;
+  const void* req[] = {a->H, sourced ? a->map_staging : a->A, a->bias, a->Wk, a->Wv, a->Kc, a->Vc};
   for (const void* p : req)
     if (p == nullptr) return fail(RF_ERR_ARG, "a required pointer is NULL");
   const void* dev[] = {a->H, a->bias, a->gain, a->Wk, a->Wv, a->Kc, a->Vc, workspace};
   for (const void* p : dev)
     if (p != nullptr && !aligned16(p)) return fail(RF_ERR_ALIGN, "a device pointer is not 16-byte aligned");
-  if (!aligned16(a->A)) return fail(RF_ERR_ALIGN, "A is not 16-byte aligned");
-  if (a->A_scale != nullptr && !aligned16(a->A_scale))
+  if (!aligned16(a->A) || !aligned16(a->map_staging))
+    return fail(RF_ERR_ALIGN, "A or map_staging is not 16-byte aligned");
+  if (a->A_scale != nullptr && !sourced && !aligned16(a->A_scale))
     return fail(RF_ERR_ALIGN, "A_scale is not 16-byte aligned");
   if ((reinterpret_cast<uintptr_t>(a->row_idx) & 3u) != 0)
     return fail(RF_ERR_ALIGN, "row_idx is not 4-byte aligned");
-  if (a->maps_on_host) {
+  if (sourced) {
+    if ((st = check_pinned(a->map_staging, "map_staging")) != RF_OK) return st;
+  } else if (a->maps_on_host) {
     if ((st = check_pinned(a->A, "A")) != RF_OK) return st;
     if (a->A_scale != nullptr && (st = check_pinned(a->A_scale, "A_scale")) != RF_OK) return st;
   }
@@ -254,6 +304,7 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
   void* xhat = ws + pl.off_xhat;
   float* ss = reinterpret_cast<float*>(ws + pl.off_ss);
   const size_t slot_bytes = map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr);
+  if ((st = guards_fill(ws, pl.lay, s)) != RF_OK) return st;
 
   HostStreamer* hs = nullptr;
   std::unique_lock<std::mutex> lk(host_stream_mutex(), std::defer_lock);
@@ -329,9 +380,15 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
         cudaEvent_t const* cev = reinterpret_cast<cudaEvent_t const*>(a->copy_events);
         if (start > 0 || l >= kMapSlots) e = cudaStreamWaitEvent(hs->copy, hs->freed[k], 0);
         if (e == cudaSuccess && cev != nullptr && start == 0) e = cudaEventRecord(cev[2 * l], hs->copy);
-        if (e == cudaSuccess)
+        if (e != cudaSuccess) return cuda_fail(e, "streaming a map from host memory");
+        if (sourced) {
+          const int j = static_cast<int>((start / pl.R * a->n_layers + l) & 1);
+          if ((st = source_map_layer(a, hs, j, l, slot, slot_bytes, &m.A, &m.A_scale)) != RF_OK)
+            return st;
+        } else {
           e = copy_map_layer(slot, a->A, a->A_scale, l, a->d_out, a->d_in, hs->copy, &m.A,
                              &m.A_scale);
+        }
         if (e == cudaSuccess && cev != nullptr && start == 0)
           e = cudaEventRecord(cev[2 * l + 1], hs->copy);
         if (e == cudaSuccess) e = cudaEventRecord(hs->copied[k], hs->copy);
@@ -365,7 +422,7 @@ extern "C" rf_status ridgefill_fill(const rf_fill_args* a, void* workspace, size
     cudaError_t e = cudaStreamWaitEvent(s, hs->h_done, 0);
     if (e != cudaSuccess) return cuda_fail(e, "ordering after the split-state copy");
   }
-  return RF_OK;
+  return guards_check(ws, pl.lay, s);
 }
 
 // ------------------------------------------------------------------ value / key rescale
@@ -381,6 +438,7 @@ struct RescalePlan {
   FillPlan fp;     // fill plan of the c predicted rows (map tile widths)
   int64_t R2 = 0;  // rows of the stacked buffers: predicted rows [0, c), true rows [c, 2c)
   size_t off_x = 0, off_ss = 0, off_cache = 0, off_scale = 0, total = 0;
+  Layout lay;
 };
 
 rf_status validate_rescale(const rf_rescale_args* a) {
@@ -415,12 +473,12 @@ void plan_rescale(const rf_rescale_args* a, RescalePlan* pl) {
   plan_fill(&f, &pl->fp);
   pl->R2 = ceil_div(2 * a->tail_rows, kBM) * kBM;
   const size_t L = a->n_layers, d = a->d_out, R2 = pl->R2;
-  size_t off = 0;
-  pl->off_x = off;     off = align_up(off + L * R2 * d * 2, 256);
-  pl->off_ss = off;    off = align_up(off + L * (d / pl->fp.bn_map) * R2 * 4, 256);
-  pl->off_cache = off; off = align_up(off + L * a->n_kv_heads * R2 * a->head_dim * 2, 256);
-  pl->off_scale = off; off = align_up(off + L * a->n_kv_heads * 4, 256);
-  pl->total = off;
+  Layout& lay = pl->lay;
+  pl->off_x = lay.take(L * R2 * d * 2);
+  pl->off_ss = lay.take(L * (d / pl->fp.bn_map) * R2 * 4);
+  pl->off_cache = lay.take(L * a->n_kv_heads * R2 * a->head_dim * 2);
+  pl->off_scale = lay.take(L * a->n_kv_heads * 4);
+  pl->total = lay.off;
 }
 
 // One warp per (layer, true row r): X_hat row c + r = bf16(g x) and its sum of
@@ -564,6 +622,7 @@ extern "C" rf_status ridgefill_rescale(const rf_rescale_args* a, void* workspace
   float* ss = reinterpret_cast<float*>(ws + pl.off_ss);
   uint8_t* proj = ws + pl.off_cache;
   float* scale = reinterpret_cast<float*>(ws + pl.off_scale);
+  if ((st = guards_fill(ws, pl.lay, s)) != RF_OK) return st;
 
   // predicted rows: the map GEMM writes X_hat rows [0, c) of every layer
   MapLaunch m{};
@@ -623,5 +682,5 @@ extern "C" rf_status ridgefill_rescale(const rf_rescale_args* a, void* workspace
         a->rows, a->head_dim);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rescale apply launch");
   }
-  return RF_OK;
+  return guards_check(ws, pl.lay, s);
 }

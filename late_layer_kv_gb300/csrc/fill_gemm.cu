@@ -150,8 +150,9 @@ __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
     map_half(r0, bp, gp, ss, w0);
     map_half(r1, bp + 32, gp != nullptr ? gp + 32 : nullptr, ss, w1);
     if constexpr (direct) {
-      if (orow >= 0 && orow < p.map_ld) {
-        __nv_bfloat16* dst = p.map_out + (static_cast<int64_t>(l) * p.map_ld + orow) * p.d_out + col;
+      const int64_t o = (static_cast<int64_t>(l) * p.map_ld + orow) * p.d_out + col;
+      if (orow >= 0 && orow < p.map_ld && in_bounds(o + 63, p.lim_b, p.err)) {
+        __nv_bfloat16* dst = p.map_out + o;
         store32(dst, w0);
         store32(dst + 32, w1);
       }
@@ -170,7 +171,8 @@ __device__ void epilogue_map(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
     }
   }
   if (row < p.rows && orow >= 0 && (!direct || orow < p.map_ld)) {
-    p.ss_part[(static_cast<size_t>(l) * p.ss_tiles + j0 / p.bn) * p.ss_stride + orow] = ss;
+    const int64_t o = (static_cast<int64_t>(l) * p.ss_tiles + j0 / p.bn) * p.ss_stride + orow;
+    if (in_bounds(o, p.lim_a, p.err)) p.ss_part[o] = ss;
   }
 }
 
@@ -211,10 +213,9 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
     const uint32_t hc = tcol + hh * hd;
     // the head's rescale factor folds into the row's RMS scale (both multiply the row)
     const float rh = hscale != nullptr ? rs * hscale[l * p.n_kv + head0 + hh] : rs;
-    __nv_bfloat16* drow =
-        direct ? p.kv_cache[is_k ? 0 : 1] +
-                     ((static_cast<int64_t>(l) * p.n_kv + head0 + hh) * p.cache_len + pos) * hd
-               : nullptr;
+    const int64_t drow_off = ((static_cast<int64_t>(l) * p.n_kv + head0 + hh) * p.cache_len + pos) * hd;
+    __nv_bfloat16* drow = direct ? p.kv_cache[is_k ? 0 : 1] + drow_off : nullptr;
+    const bool keep_h = keep && (!direct || in_bounds(drow_off + hd - 1, p.lim_b, p.err));
     if (!direct && lane == 0) bulk_wait_read<0>();
     __syncwarp();
     if (is_k) {
@@ -241,7 +242,7 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
           w2[j / 2] = pack_bf16(ya * c0 + xa * s0, yb * c1 + xb * s1);
         }
         if (direct) {
-          if (keep) {
+          if (keep_h) {
             store32(drow + i0, w1);
             store32(drow + half + i0, w2);
           }
@@ -259,7 +260,7 @@ __device__ void epilogue_kv(const GemmParams& p, uint32_t tcol, uint8_t* stg, in
 #pragma unroll
         for (int j = 0; j < 32; j += 2) w[j / 2] = pack_bf16(f32(a[j]) * rh, f32(a[j + 1]) * rh);
         if (direct) {
-          if (keep) store32(drow + c0, w);
+          if (keep_h) store32(drow + c0, w);
         } else {
           stage32(stg + (c0 / 64) * kOutBoxBytes, lane, c0 % 64, w);
         }
@@ -366,7 +367,8 @@ __device__ void epilogue_gdn(const GemmParams& p, uint32_t tcol, uint8_t* stg, i
             const float val = 1.f / (1.f + expf(-z));
             const int which = is_a ? 0 : 1;
             const int h = is_a ? c : c - H;
-            p.gdn_gate[((static_cast<size_t>(l) * 2 + which) * H + h) * ra + row] = val;
+            const int64_t o = ((static_cast<int64_t>(l) * 2 + which) * H + h) * ra + row;
+            if (in_bounds(o, p.lim_a, p.err)) p.gdn_gate[o] = val;
           }
         }
       }
@@ -383,15 +385,20 @@ __device__ void epilogue_gram(const GemmParams& p, uint32_t tcol, int q, int lan
                               uint32_t tempty) {
   const int r = q * 32 + lane;
   double* dst;
+  int64_t o, lim;
   if (m < p.gram_x_tiles) {
-    dst = p.gram_G + static_cast<size_t>(m * kBM + r) * p.gram_ld;
+    o = static_cast<int64_t>(m * kBM + r) * p.gram_ld + n * p.bn;
+    dst = p.gram_G + o;
+    lim = p.lim_a;
   } else {
     const int mm = m - p.gram_x_tiles;
     const int l = mm / p.gram_y_tiles_per_layer;
-    const int o = (mm % p.gram_y_tiles_per_layer) * kBM + r;
-    dst = p.gram_C + (static_cast<size_t>(l) * p.d_out + o) * p.gram_ld;
+    const int oc = (mm % p.gram_y_tiles_per_layer) * kBM + r;
+    o = (static_cast<int64_t>(l) * p.d_out + oc) * p.gram_ld + n * p.bn;
+    dst = p.gram_C + o;
+    lim = p.lim_b;
   }
-  dst += n * p.bn;
+  const bool ok = in_bounds(o + p.bn - 1, lim, p.err);
   for (int c0 = 0; c0 < p.bn; c0 += 32) {
     uint32_t a[32];
     tmem_ld32(tcol + c0, a);
@@ -401,6 +408,7 @@ __device__ void epilogue_gram(const GemmParams& p, uint32_t tcol, int q, int lan
       __syncwarp();
       if (lane == 0) mbar_arrive_cl(tempty);
     }
+    if (!ok) continue;
     double2* d2 = reinterpret_cast<double2*>(dst + c0);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -418,7 +426,9 @@ __device__ void epilogue_solve(const GemmParams& p, uint32_t tcol, int q, int la
                                uint32_t tempty) {
   const int o = m * kBM + q * 32 + lane;
   const int c_base = n * p.bn;
-  const bool valid = o < p.rows;
+  const bool valid = o < p.rows &&
+                     in_bounds(static_cast<int64_t>(o) * p.out_ld + c_base + p.bn - 1, p.lim_b, p.err) &&
+                     in_bounds(static_cast<int64_t>(o) * p.n_tiles + n, p.lim_a, p.err);
   float part = 0.f;
   for (int c0 = 0; c0 < p.bn; c0 += 32) {
     uint32_t a[32];

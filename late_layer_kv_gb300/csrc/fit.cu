@@ -502,6 +502,7 @@ struct FitPlan {
   int bn = 0;
   int slabs = 0;
   int64_t slab_rows = 0;
+  Layout lay;
 };
 
 rf_status validate_fit(const rf_fit_args* a) {
@@ -522,28 +523,28 @@ rf_status validate_fit(const rf_fit_args* a) {
 void plan_fit(const rf_fit_args* a, FitPlan* pl) {
   const size_t d = a->d_in, M = static_cast<size_t>(a->n_layers) * a->d_out;
   pl->bn = (a->d_in % 256 == 0) ? 256 : 128;
-  size_t off = 0;
+  Layout& lay = pl->lay;
   if (a->flags & RF_FIT_ACCUMULATE) {
     const int64_t rows = a->rows > 0 ? a->rows : 1;
     pl->slab_rows = ceil_div(ceil_div(rows, 64), 64) * 64;  // at most 64 slabs, 64-row runs
     pl->slabs = static_cast<int>(ceil_div(rows, pl->slab_rows));
-    pl->off_cs = off;    off = align_up(off + static_cast<size_t>(pl->slabs) * (d + M) * 8, 256);
+    pl->off_cs = lay.take(static_cast<size_t>(pl->slabs) * (d + M) * 8);
   }
   if (a->flags & RF_FIT_SOLVE) {
-    pl->off_gh = off;    off = align_up(off + d * d * 4, 256);
-    pl->off_s = off;     off = align_up(off + d * 4, 256);
-    pl->off_mu32 = off;  off = align_up(off + d * 4, 256);
-    pl->off_mu64 = off;  off = align_up(off + d * 8, 256);
-    pl->off_alpha = off; off = align_up(off + 8, 256);
-    pl->off_linv = off;  off = align_up(off + kNB * kNB * 4, 256);
-    pl->off_xhi = off;   off = align_up(off + d * d * 2, 256);
-    pl->off_xlo = off;   off = align_up(off + d * d * 2, 256);
-    pl->off_gi = off;    off = align_up(off + d * d * 8, 256);
-    pl->off_bp = off;    off = align_up(off + d * 3 * d * 2, 256);
-    pl->off_ap = off;    off = align_up(off + M * 3 * d * 2, 256);
-    pl->off_part = off;  off = align_up(off + M * (d / pl->bn) * 4, 256);
+    pl->off_gh = lay.take(d * d * 4);
+    pl->off_s = lay.take(d * 4);
+    pl->off_mu32 = lay.take(d * 4);
+    pl->off_mu64 = lay.take(d * 8);
+    pl->off_alpha = lay.take(8);
+    pl->off_linv = lay.take(kNB * kNB * 4);
+    pl->off_xhi = lay.take(d * d * 2);
+    pl->off_xlo = lay.take(d * d * 2);
+    pl->off_gi = lay.take(d * d * 8);
+    pl->off_bp = lay.take(d * 3 * d * 2);
+    pl->off_ap = lay.take(M * 3 * d * 2);
+    pl->off_part = lay.take(M * (d / pl->bn) * 4);
   }
-  pl->total = off;
+  pl->total = lay.off;
 }
 
 // Gram-mode tcgen05 GEMM: out_G[m, n] += sum_k Xa[k, m] Xb[k, n] for the d-wide
@@ -581,6 +582,8 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   p.gram_G = out_G;
   p.gram_C = out_C;
   p.gram_ld = d;
+  p.lim_a = static_cast<int64_t>(d) * d;
+  p.lim_b = static_cast<int64_t>(L) * dout * d;
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
   const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
@@ -758,6 +761,8 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   p.out_bf16 = static_cast<__nv_bfloat16*>(a->A_out);
   p.bias_part = part;
   p.out_ld = d;
+  p.lim_a = M * p.n_tiles;
+  p.lim_b = M * d;
   p.err = err;
   const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
   const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
@@ -800,11 +805,12 @@ extern "C" rf_status ridgefill_fit(const rf_fit_args* a, void* workspace, size_t
   if (pl.total > 0 && (workspace == nullptr || ws_bytes < pl.total))
     return fail(RF_ERR_WORKSPACE, "workspace needs %zu bytes", pl.total);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if ((st = guards_fill(workspace, pl.lay, s)) != RF_OK) return st;
   if (a->flags & RF_FIT_ACCUMULATE) {
     if ((st = accumulate(a, pl, static_cast<uint8_t*>(workspace), s)) != RF_OK) return st;
   }
   if (a->flags & RF_FIT_SOLVE) {
     if ((st = solve(a, pl, static_cast<uint8_t*>(workspace), s)) != RF_OK) return st;
   }
-  return RF_OK;
+  return guards_check(workspace, pl.lay, s);
 }

@@ -859,6 +859,7 @@ struct GdnPlan {
          off_fill = 0, off_hc = 0, off_hdev = 0, off_hflags = 0, off_dq = 0, total = 0;
   int dq_layers = 0;     // resident int8 maps: layers dequantised ahead of the bf16 GEMM
   bool compact = false;  // map only the filled rows (exact rows, one row chunk, bf16 GEMM)
+  Layout lay;
 };
 
 rf_status validate_gdn(const rf_gdn_args* a) {
@@ -893,36 +894,32 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
   const int64_t all = ceil_div(a->rows > 0 ? a->rows : 1, kBM) * kBM;
   pl->R = a->rows_per_chunk > 0 ? (a->rows_per_chunk < all ? a->rows_per_chunk : all) : all;
   const size_t L = a->n_layers, d = a->d_out, R = pl->R, H = a->n_heads;
-  size_t off = 0;
-  pl->off_xhat = off;  off = align_up(off + L * R * d * 2, 256);
-  pl->off_ss = off;    off = align_up(off + L * (d / pl->bn_map) * R * 4, 256);
-  pl->off_k = off;     off = align_up(off + L * H * R * kDk * 4, 256);
-  pl->off_v = off;     off = align_up(off + L * H * R * kDk * 4, 256);
-  pl->off_gate = off;  off = align_up(off + L * 2 * H * R * 4, 256);
-  pl->off_slots = off;
-  off = align_up(off + (a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0), 256);
-  pl->off_rho = off;   off = align_up(off + L * H * 2 * sizeof(double), 256);
+  Layout& lay = pl->lay;
+  pl->off_xhat = lay.take(L * R * d * 2);
+  pl->off_ss = lay.take(L * (d / pl->bn_map) * R * 4);
+  pl->off_k = lay.take(L * H * R * kDk * 4);
+  pl->off_v = lay.take(L * H * R * kDk * 4);
+  pl->off_gate = lay.take(L * 2 * H * R * 4);
+  pl->off_slots = lay.take(a->maps_on_host ? kMapSlots * map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr) : 0);
+  pl->off_rho = lay.take(L * H * 2 * sizeof(double));
   if (a->h_on_host) {
     size_t fo = 0;
-    pl->off_hdev = off;
-    off = align_up(off + host_rows_bytes(a->rows, a->d_in, &fo), 256);
+    pl->off_hdev = lay.take(host_rows_bytes(a->rows, a->d_in, &fo));
     pl->off_hflags = pl->off_hdev + fo;
   }
   pl->dq_layers = q8_group(a->q8_group_layers, a->A_scale != nullptr, a->maps_on_host != 0,
                            a->n_layers);
-  if (pl->dq_layers > 0) {
-    pl->off_dq = off;
-    off = align_up(off + static_cast<size_t>(pl->dq_layers) * a->d_out * a->d_in * 2, 256);
-  }
+  if (pl->dq_layers > 0)
+    pl->off_dq = lay.take(static_cast<size_t>(pl->dq_layers) * a->d_out * a->d_in * 2);
   // the compacted map GEMM writes rows by index: the bf16 GEMM only (not the in-GEMM int8
   // conversion)
   pl->compact = a->n_exact > 0 && pl->R >= a->rows && (a->A_scale == nullptr || pl->dq_layers > 0);
   if (pl->compact) {
     const size_t n_fill = static_cast<size_t>(a->rows - a->n_exact);
-    pl->off_fill = off; off = align_up(off + static_cast<size_t>(a->rows) * 4, 256);
-    pl->off_hc = off;   off = align_up(off + n_fill * a->d_in * 2, 256);
+    pl->off_fill = lay.take(static_cast<size_t>(a->rows) * 4);
+    pl->off_hc = lay.take(n_fill * a->d_in * 2);
   }
-  pl->total = off;
+  pl->total = lay.off;
 }
 
 rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, const void* xhat,
@@ -973,6 +970,7 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
   p.gdn_gate = gb;
   p.gdn_heads = H;
   p.gdn_rows_alloc = static_cast<int32_t>(pl.R);
+  p.lim_a = static_cast<int64_t>(a->n_layers) * 2 * H * pl.R;
   p.l2_eps = static_cast<float>(a->l2_eps);
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
@@ -1046,6 +1044,7 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
   __nv_bfloat16* kb = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_k);
   __nv_bfloat16* vb = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_v);
   float* gb = reinterpret_cast<float*>(ws + pl.off_gate);
+  if ((st = guards_fill(ws, pl.lay, s)) != RF_OK) return st;
 
   GdnStateParams sp{};
   sp.gate = gb;
@@ -1079,7 +1078,7 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
       rho_finish_kernel<<<LH, 256, 0, s>>>(nullptr, 1, a->rho, nullptr, a->S, kDk * kDk);
       if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rho launch");
     }
-    return RF_OK;
+    return guards_check(ws, pl.lay, s);
   }
 
   HostStreamer* hs = nullptr;
@@ -1212,5 +1211,5 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "rho launch");
   }
-  return RF_OK;
+  return guards_check(ws, pl.lay, s);
 }

@@ -6,7 +6,17 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// Debug builds (RF_DEBUG=1, a separate library) check the index of every plain global
+// store of the kernels against its buffer's extent, skip a store outside and record it,
+// and put a guard band after every workspace region that each call fills with a pattern
+// first and checks last.  Release builds compile none of this.
+#ifndef RF_DEBUG
+#define RF_DEBUG 0
+#endif
+
 namespace rf {
+
+constexpr bool kDebug = RF_DEBUG != 0;
 
 // ------------------------------------------------------------ GEMM tiling
 constexpr int kBM = 128;           // rows per CTA (one TMEM lane per row)
@@ -41,7 +51,25 @@ enum ErrSite : int {
   kErrHostRows = 8,  // a split-state row group copied from host memory never arrived
   kErrProbe = 20,    // ridgefill_wait_selftest: + 0 mbarrier wait, + 1 flag wait
   kErrNumeric = 7,   // the ridge system was not positive definite (Cholesky pivot <= 0)
+  kErrGuard = 9,     // debug builds: a workspace guard band was overwritten
+  kErrBounds = 10,   // debug builds: a kernel store fell outside its buffer (skipped)
 };
+
+// True when element index i lies in [0, n).  Debug builds record a miss in the error
+// word; release builds assume it (no check is compiled).
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n, int* err) {
+#if RF_DEBUG
+  if (i < 0 || i >= n) {
+    atomicCAS(err, 0, static_cast<int>(kErrBounds));
+    return false;
+  }
+#else
+  (void)i;
+  (void)n;
+  (void)err;
+#endif
+  return true;
+}
 
 struct GemmParams {
   CUtensorMap tmA;     // A operand, K-major 3D {K, rows, batch}, box {64, 128, 1}
@@ -122,6 +150,10 @@ struct GemmParams {
   float* bias_part;         // [M, n_tiles]
   int32_t out_ld;
   int* err;
+  // elements of the buffers the epilogue writes with plain stores (checked by debug
+  // builds): map mode ss_part, map_out; K/V mode with a row list the caches (per tensor);
+  // GDN mode gdn_gate; Gram mode gram_G, gram_C; solve mode the outputs, bias_part
+  int64_t lim_a, lim_b;
   float inv_freq_hi[64];
   float inv_freq_lo[64];
 };

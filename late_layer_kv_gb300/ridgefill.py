@@ -8,6 +8,7 @@ raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional
@@ -16,7 +17,8 @@ import torch
 
 from . import build as _build
 
-_lib = None
+_libs = {}
+_use_debug = False
 
 RF_FIT_ACCUMULATE = 1
 RF_FIT_SOLVE = 2
@@ -24,9 +26,13 @@ RF_FIT_SOLVE = 2
 STATUS = {
     0: "RF_OK", 1: "RF_ERR_ARG", 2: "RF_ERR_SHAPE", 3: "RF_ERR_ALIGN", 4: "RF_ERR_NOT_PINNED",
     5: "RF_ERR_CUDA", 6: "RF_ERR_TIMEOUT", 7: "RF_ERR_NUMERIC", 8: "RF_ERR_WORKSPACE",
+    9: "RF_ERR_SOURCE", 10: "RF_ERR_BOUNDS",
 }
 
 _vp = ctypes.c_void_p
+
+# int32_t (*)(void* user, int32_t layer, void* dst, size_t bytes): the host map source
+MAP_SOURCE_FN = ctypes.CFUNCTYPE(ctypes.c_int32, _vp, ctypes.c_int32, _vp, ctypes.c_size_t)
 
 
 class FillArgs(ctypes.Structure):
@@ -40,7 +46,9 @@ class FillArgs(ctypes.Structure):
         ("Kc", _vp), ("Vc", _vp), ("stage_events", _vp), ("copy_events", _vp),
         ("k_scale", _vp), ("v_scale", _vp), ("A_scale", _vp), ("row_idx", _vp),
         ("h_rows", ctypes.c_int64), ("h_on_host", ctypes.c_int32),
-        ("q8_group_layers", ctypes.c_int32),
+        ("q8_group_layers", ctypes.c_int32), ("map_source", MAP_SOURCE_FN),
+        ("map_source_user", _vp), ("map_staging", _vp), ("host_wait_ms", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -97,19 +105,33 @@ class RidgeFillError(RuntimeError):
 
 
 # the argument structs below match include/ridgefill.h at this version
-ABI_VERSION = 9
+ABI_VERSION = 10
 
 
-def library_path() -> str:
-    return _build.LIB
+def library_path(debug: Optional[bool] = None) -> str:
+    return _build.LIB_DEBUG if (_use_debug if debug is None else debug) else _build.LIB
 
 
-def load(rebuild: bool = True) -> ctypes.CDLL:
-    """Load ``libridgefill.so`` (building it first if it is stale)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    path = _build.build() if rebuild else _build.LIB
+@contextlib.contextmanager
+def debug_library():
+    """Within the block every call of this binding goes through ``libridgefill_debug.so``:
+    the same kernels with every plain global store checked against its buffer and guard
+    bands around the workspace regions (reported as RF_ERR_BOUNDS by device_error)."""
+    global _use_debug
+    prev, _use_debug = _use_debug, True
+    try:
+        yield load()
+    finally:
+        _use_debug = prev
+
+
+def load(rebuild: bool = True, debug: Optional[bool] = None) -> ctypes.CDLL:
+    """Load ``libridgefill.so`` (building it first if it is stale); with ``debug`` (or
+    inside :func:`debug_library`) the debug build of the same sources."""
+    dbg = _use_debug if debug is None else debug
+    if dbg in _libs:
+        return _libs[dbg]
+    path = _build.build(debug=dbg) if rebuild else library_path(dbg)
     if not os.path.exists(path):
         raise RuntimeError(f"RidgeFill CUDA library not found at {path}")
     lib = ctypes.CDLL(path)
@@ -149,7 +171,7 @@ def load(rebuild: bool = True) -> ctypes.CDLL:
     if lib.ridgefill_abi_version() != ABI_VERSION:
         raise RuntimeError(f"{path} has ABI version {lib.ridgefill_abi_version()}, this binding "
                            f"expects {ABI_VERSION}: rebuild the library")
-    _lib = lib
+    _libs[dbg] = lib
     return lib
 
 
@@ -193,6 +215,13 @@ def _check_maps(A, A_scale) -> bool:
     return host
 
 
+def map_slot_bytes(d_out: int, d_in: int, int8: bool) -> int:
+    """Bytes of one layer's map as a host map source writes it: bf16 [d_out, d_in], or int8
+    codes followed, at a 256-byte boundary, by the bf16 scales [d_in / 128, d_out]."""
+    n = d_out * d_in
+    return 2 * n if not int8 else (n + 255) // 256 * 256 + d_out * (d_in // Q8_GROUP) * 2
+
+
 def _stream(stream) -> int:
     s = torch.cuda.current_stream() if stream is None else stream
     return s.cuda_stream
@@ -208,8 +237,15 @@ def _event_array(events):
 def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: float,
               rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
               stage_events=None, copy_events=None, k_scale=None, v_scale=None,
-              A_scale=None, row_idx=None, q8_group_layers: int = 0) -> FillArgs:
-    L, d_out, d_in = A.shape
+              A_scale=None, row_idx=None, q8_group_layers: int = 0, map_source=None,
+              map_staging=None, host_wait_ms: int = 0, map_shape=None) -> FillArgs:
+    """With ``map_source`` (a callable ``(layer, dst_address, nbytes) -> int``) the maps
+    come from the host one layer at a time through the pinned ``map_staging`` buffer;
+    ``A`` may then be None, with ``map_shape`` = (L, d_out, d_in) giving the sizes."""
+    if map_source is not None and A is None:
+        L, d_out, d_in = map_shape
+    else:
+        L, d_out, d_in = A.shape
     rows = H.shape[0] if row_idx is None else row_idx.shape[0]
     h_rows = H.shape[0] if row_idx is not None else 0
     if row_idx is not None:
@@ -224,7 +260,17 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
             raise ValueError("H must be [rows, d_in]")
     else:
         _dev(H, "H", torch.bfloat16, (H.shape[0], d_in))
-    host = _check_maps(A, A_scale)
+    if map_source is not None:
+        host = True
+        if map_staging is None or map_staging.is_cuda or not map_staging.is_pinned():
+            raise ValueError("map_source needs a pinned host map_staging buffer")
+        need = 2 * map_slot_bytes(d_out, d_in, A_scale is not None)
+        if map_staging.numel() * map_staging.element_size() < need:
+            raise ValueError(f"map_staging needs {need} bytes (two layers)")
+        if A is not None:
+            _check_maps(A, A_scale)
+    else:
+        host = _check_maps(A, A_scale)
     _dev(bias, "bias", torch.float32, (L, d_out))
     if gain is not None:
         _dev(gain, "gain", torch.bfloat16, (L, d_out))
@@ -246,7 +292,18 @@ def fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_theta: fl
                  ctypes.cast(cev, ctypes.c_void_p) if cev is not None else None,
                  _ptr(k_scale), _ptr(v_scale), _ptr(A_scale), _ptr(row_idx), h_rows,
                  1 if h_host else 0, int(q8_group_layers))
-    a._events_keepalive = (ev, cev)
+    cb = None
+    if map_source is not None:
+        def _source(user, layer, dst, nbytes, _f=map_source):
+            try:
+                return int(_f(int(layer), int(dst), int(nbytes)))
+            except Exception:  # an exception must not cross the C frame
+                return -1
+        cb = MAP_SOURCE_FN(_source)
+        a.map_source = cb
+        a.map_staging = _ptr(map_staging)
+        a.host_wait_ms = int(host_wait_ms)
+    a._events_keepalive = (ev, cev, cb)
     return a
 
 
@@ -270,7 +327,8 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
                    rms_eps: float, pos0: int = 0, rows_per_chunk: int = 0,
                    workspace: Optional[torch.Tensor] = None, stream=None,
                    stage_events=None, copy_events=None, k_scale=None, v_scale=None,
-                   A_scale=None, row_idx=None, q8_group_layers: int = 0) -> None:
+                   A_scale=None, row_idx=None, q8_group_layers: int = 0, map_source=None,
+                   map_staging=None, host_wait_ms: int = 0, map_shape=None) -> None:
     """Write the K/V cache of the prefix rows of every late attention layer.
 
     ``H`` [rows, d_in] bf16, ``A`` [L, d_out, d_in] bf16 (device, or pinned host
@@ -289,13 +347,20 @@ def ridgefill_fill(H, A, bias, gain, Wk, Wv, Kc, Vc, *, head_dim: int, rope_thet
     then copied by the library, overlapped with the map GEMM.  ``q8_group_layers``:
     resident int8 maps are dequantised 4 (or this many) layers at a time into the
     workspace ahead of the bf16 map GEMM; -1 converts them inside the GEMM instead
-    (no extra workspace, slower; bitwise the same results).
+    (no extra workspace, slower; bitwise the same results).  ``map_source``: a callable
+    ``(layer, dst_address, nbytes) -> int`` that writes one layer's map (in the layout of
+    one layer of ``A``, int8 scales after the codes at a 256-byte boundary) into pinned
+    staging memory and returns 0; the maps then stream from it through ``map_staging``
+    (pinned, two layers' bytes) instead of from ``A``, which may be None with
+    ``map_shape`` = (L, d_out, d_in).  Host waits of such a call are bounded by
+    ``host_wait_ms`` (0: ten seconds); see the C header for what a timeout leaves behind.
     """
     args = fill_args(H, A, bias, gain, Wk, Wv, Kc, Vc, head_dim=head_dim, rope_theta=rope_theta,
                      rms_eps=rms_eps, pos0=pos0, rows_per_chunk=rows_per_chunk,
                      stage_events=stage_events, copy_events=copy_events, k_scale=k_scale,
                      v_scale=v_scale, A_scale=A_scale, row_idx=row_idx,
-                     q8_group_layers=q8_group_layers)
+                     q8_group_layers=q8_group_layers, map_source=map_source,
+                     map_staging=map_staging, host_wait_ms=host_wait_ms, map_shape=map_shape)
     lib = load()
     need = int(lib.ridgefill_fill_workspace_size(ctypes.byref(args)))
     if need == 0:

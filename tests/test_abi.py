@@ -184,3 +184,39 @@ def test_new_argument_checks_fail_without_a_gpu(lib):
     assert lib.ridgefill_fill_gdn(ctypes.byref(g), None, 0, None) == RF_ERR_ARG
     g.n_exact = 5  # exact rows without their indices and inputs
     assert lib.ridgefill_fill_gdn(ctypes.byref(g), None, 0, None) == RF_ERR_ARG
+
+
+def test_map_source_arguments_fail_without_a_gpu(lib):
+    """A host map source needs maps_on_host = 1 and a non-negative wait bound; both are
+    checked before anything is enqueued."""
+    from late_layer_kv_gb300 import ridgefill as rb
+    a = _fill_ok(rb)
+    a.map_source = rb.MAP_SOURCE_FN(lambda user, layer, dst, n: 0)
+    assert lib.ridgefill_fill(ctypes.byref(a), None, 0, None) == 1  # maps_on_host = 0
+    assert b"maps_on_host" in lib.ridgefill_last_error()
+    a.maps_on_host, a.host_wait_ms = 1, -1
+    assert lib.ridgefill_fill(ctypes.byref(a), None, 0, None) == 1
+    assert lib.ridgefill_status_string(9) == b"the host map source reported an error"
+
+
+def test_debug_library_builds_and_adds_guard_bands():
+    """The debug build (RF_DEBUG=1) loads without a GPU, exports the same symbols, and its
+    workspaces hold one guard band after every region: the fill of a resident-map call has
+    seven regions (predicted inputs, partial sums, map slots, row gather, host split
+    state, RoPE table, int8 layer groups), the fit with both steps thirteen."""
+    from late_layer_kv_gb300 import build as b
+    from late_layer_kv_gb300 import ridgefill as rb
+    dbg = rb.load(debug=True)
+    rel = rb.load(debug=False)
+    for n in _declared():
+        assert hasattr(dbg, n), f"{n} not exported by the debug library"
+    assert dbg.ridgefill_abi_version() == rel.ridgefill_abi_version()
+    fa = rb.FillArgs(20, 4096, 4096, 8, 128, 0, 14336, 0, 16384, 0, 5e5, 1e-6)
+    ta = rb.FitArgs()
+    ta.n_layers, ta.d_in, ta.d_out, ta.flags, ta.rows, ta.lam = 20, 4096, 4096, 3, 65536, 1e-3
+    guard = 4096
+    assert (dbg.ridgefill_fill_workspace_size(ctypes.byref(fa)) ==
+            rel.ridgefill_fill_workspace_size(ctypes.byref(fa)) + 7 * guard)
+    assert (dbg.ridgefill_fit_workspace_size(ctypes.byref(ta)) ==
+            rel.ridgefill_fit_workspace_size(ctypes.byref(ta)) + 13 * guard)
+    assert os.path.basename(b.LIB_DEBUG) == "libridgefill_debug.so"
