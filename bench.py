@@ -820,8 +820,8 @@ def _host_link(wl, ev, stages, dev):
 
 def _secondary(args, head, dev, stream, local):
     """The other workloads, each timed on its own (CUDA events on the launching stream,
-    its own warm-up and clocks): maps streamed from host memory, the hybrid Gated
-    DeltaNet fill, the 27B-class fill at its shortest and longest prompt, and the fit."""
+    its own warm-up and clocks): maps streamed from host memory at both prompt lengths, the
+    hybrid Gated DeltaNet fill, the 27B-class fill at all four prompt lengths, and the fit."""
     out = {}
 
     def run(name, wl, steps, setup):
@@ -843,25 +843,27 @@ def _secondary(args, head, dev, stream, local):
         return wl
 
     seed = 1001
-    wl = run("hostmaps_16k", AttnWorkload(WORKLOADS["hostmaps_16k"], host_maps=True),
-             min(args.steps, 20), lambda w: w.setup(dev, seed, inp=head.inp))
-    del wl
-    torch.cuda.empty_cache()
+    # maps streamed from pinned host memory: the headline's inputs at 16K, then the 64K prompt
+    for name, steps, inp in (("hostmaps_16k", 20, head.inp), ("hostmaps_64k", 10, None)):
+        wl = run(name, AttnWorkload(WORKLOADS[name], host_maps=True), min(args.steps, steps),
+                 lambda w, inp=inp: w.setup(dev, seed, inp=inp))
+        del wl
+        torch.cuda.empty_cache()
     wl = run("hybrid_gdn_32k", HybridWorkload(WORKLOADS["hybrid_gdn_32k"]),
              min(args.steps, 20), lambda w: w.setup(dev, seed))
     del wl
     torch.cuda.empty_cache()
+    # the 27B-class sweep: one draw at the longest prompt, whose first rows serve the shorter
     big = fill_inputs(WORKLOADS["dense27b_120k"], seed=seed)
-    wl = run("dense27b_120k", AttnWorkload(WORKLOADS["dense27b_120k"], rows_per_chunk=16384),
-             min(args.steps, 8), lambda w: w.setup(dev, seed, inp=big))
-    del wl
-    torch.cuda.empty_cache()
-    small = dict(big)
-    small["H"] = big["H"][:WORKLOADS["dense27b_16k"].rows]
-    wl = run("dense27b_16k", AttnWorkload(WORKLOADS["dense27b_16k"], rows_per_chunk=16384),
-             min(args.steps, 20), lambda w: w.setup(dev, seed, inp=small))
-    del wl, big, small
-    torch.cuda.empty_cache()
+    for name, steps in (("dense27b_120k", 5), ("dense27b_64k", 8), ("dense27b_32k", 10),
+                        ("dense27b_16k", 20)):
+        inp = dict(big)
+        inp["H"] = big["H"][:WORKLOADS[name].rows]
+        wl = run(name, AttnWorkload(WORKLOADS[name], rows_per_chunk=16384), min(args.steps, steps),
+                 lambda w, inp=inp: w.setup(dev, seed, inp=inp))
+        del wl, inp
+        torch.cuda.empty_cache()
+    del big
     shape = WORKLOADS["hostmaps_16k"]
     wl = run("fit", FitWorkload(shape, shape.calib_rows), min(args.steps, 10),
              lambda w: w.setup(dev, seed))
