@@ -51,12 +51,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # The fit depends only on d, the number of maps and the calibration rows, which the Llama-8B
 # fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
 _FIT_LLAMA8B = {"sources": "fit",
-                "kernel_sha256": "c2bfcf9009a383123195d1a207ee52288dadb380ea9123bf2b227ac499869780",
-                "bytes_per_launch": 92237788416 + 2804967936}
+                "kernel_sha256": "7ad51637bf3e960c6f33e78de3a9426b1f0e485b2de6860bcb1cb8173be8df05",
+                "bytes_per_launch": 101483784960 + 2813207552}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "d7e39f3da74229b752c94c267b93e566a620e262b4a5146ab9330825cd4fe11c",
-                    "bytes_per_launch": 5977021184 + 2355833600},
+                    "kernel_sha256": "97bd83d168cbb8bf882e5c56393468033083957afd19f1887d7cb11e592b96a3",
+                    "bytes_per_launch": 5779580364},
     "llama8b_16k_fit": _FIT_LLAMA8B,
     "hostmaps_16k_fit": _FIT_LLAMA8B,
     "hostmaps_64k_fit": _FIT_LLAMA8B,
