@@ -1,5 +1,6 @@
 // abi_common.cu -- status handling, tensor-map encoding, per-device state,
 // and the map-GEMM launch shared by the attention and GDN fills.
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -14,6 +15,8 @@ namespace {
 thread_local std::string g_last_error;
 constexpr int kMaxDevices = 64;
 __device__ int g_device_error = 0;
+constexpr int kTileCtrSlots = 1024;
+__device__ int g_tile_ctr[kTileCtrSlots];
 __device__ uint32_t g_probe_flag = 0;  // never written: the flag ridgefill_wait_selftest waits on
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -67,6 +70,23 @@ int* device_error_word() {
     ptr[d] = static_cast<int*>(p);
   }
   return ptr[d];
+}
+
+int* tile_counter_slot() {
+  static int* base[kMaxDevices] = {};
+  static std::atomic<unsigned> seq{0};
+  static std::mutex mu;
+  const int d = current_device();
+  if (d < 0) return nullptr;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (base[d] == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_tile_ctr) != cudaSuccess) return nullptr;
+      base[d] = static_cast<int*>(p);
+    }
+  }
+  return base[d] + (seq.fetch_add(1) % kTileCtrSlots);
 }
 
 int sm_count() {

@@ -18,6 +18,10 @@
 // kStages-deep ring, warp 1 issues tcgen05.mma (M=128, N=bn, K=16) into one of
 // two TMEM accumulators, warp 2 owns the TMEM allocation, warps 4-7 drain the
 // accumulators (TMEM lane = tile row) while the next tile accumulates.
+// Tiles are handed out in raster order by a launch-wide counter: CTA 0's producer takes
+// the next tile and passes its index through a small ring in both CTAs' shared memory to
+// the other roles, so the pairs that share an operand panel start its tiles together
+// (with a fixed round-robin they drift apart over a long launch and re-read the panel).
 // rf_gemm2_kernel runs the map, K/V and GDN modes on CTA pairs (M=256); its
 // int8-map variant (section 2.2 "Size and cost") adds warp 3 loading int8 codes
 // and scales and warps 8-15 dequantising them into the MMA stages.
@@ -474,6 +478,7 @@ __device__ void epilogue_solve(const GemmParams& p, uint32_t tcol, int q, int la
 // release both CTAs' stages and accumulators; both CTAs' epilogues release the
 // accumulator on CTA 0's `tempty` barrier.
 constexpr int kStages2 = 6;
+constexpr int kRing = 4;  // tile ids handed from CTA 0's producer to every other role
 constexpr int kHalfBytes = 128 * kBK * 2;  // 128 rows x 64 K of bf16
 // Wide Gram tiles (bn = kGramWideCols): the pair accumulates 256 x 512 in both TMEM
 // halves with two N = 256 MMAs per K step that share one A stage.  A stage then holds this CTA's A half and
@@ -517,7 +522,8 @@ constexpr int kOutBoxesQ8 = 1;            // one store box per epilogue warp (ma
 constexpr int kConvGroups = 2;            // converter warp groups taking alternate stages
 // scale ring padded so the epilogue's 128-byte-swizzled staging stays 1024-byte aligned
 constexpr int kRawScaleRegion = (kRawStages * kRawScaleBytes + 1023) / 1024 * 1024;
-static_assert(1024 + kStages2 * 2 * kHalfBytes + 4 * kOutWarpBytes + 8 * (2 * kStages2 + 5) + 8 <=
+static_assert(1024 + kStages2 * 2 * kHalfBytes + 4 * kOutWarpBytes + 8 * (2 * kStages2 + 5 + 2 * kRing) +
+                      8 + 4 * kRing <=
                   kGemmSmem, "pair GEMM shared memory");
 static_assert(1024 + kStagesQ8 * 2 * kHalfBytes + kRawStages * kRawBytes + kRawScaleRegion +
                       4 * kOutBoxesQ8 * kOutBoxBytes + 8 * (2 * kStagesQ8 + 5 + 2 * kRawStages) + 8 <=
@@ -599,10 +605,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   uint64_t* tfull = bars + 2 * kS;
   uint64_t* tempty = tfull + 2;
   uint64_t* fin = tempty + 2;
-  uint64_t* raw_full = fin + 1;                            // kQ8 only
+  uint64_t* ring_full = fin + 1;                           // tile-id ring (both CTAs)
+  uint64_t* ring_empty = ring_full + kRing;                // CTA 0's only
+  uint64_t* raw_full = ring_empty + kRing;                 // kQ8 only
   uint64_t* raw_empty = raw_full + (kQ8 ? kRawStages : 0);  // kQ8 only
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(raw_empty + (kQ8 ? kRawStages : 0));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* ring = reinterpret_cast<int*>(tmem_slot + 2);
+  // tiles in the order a launch-wide counter hands them out (pairs that share an operand
+  // panel then run its tiles together); the int8 kernel keeps the static order
+  constexpr bool kDyn = !kQ8;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -620,6 +632,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       mbar_init(&tempty[a], 8);  // four epilogue warps in each CTA
     }
     mbar_init(fin, 1);
+    for (int r = 0; r < kRing; ++r) {
+      mbar_init(&ring_full[r], 1);    // CTA 0's producer
+      mbar_init(&ring_empty[r], 10);  // MMA, CTA 1's producer, four epilogue warps in each CTA
+    }
     if (kQ8) {
       for (int s = 0; s < kRawStages; ++s) {
         mbar_init(&raw_full[s], 1);   // this CTA's raw producer (+ its copies' bytes)
@@ -650,7 +666,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   const int total = units_m(p) * p.n_tiles * p.batches;
   const uint32_t full0 = cluster_addr(smem_u32(full), 0);
   const uint32_t tempty0 = cluster_addr(smem_u32(tempty), 0);
-
+  const uint32_t ring_empty0 = cluster_addr(smem_u32(ring_empty), 0);
+  // tile of the it-th turn of this pair: the static order, or the ring (every role but CTA
+  // 0's producer, which fills it); -1 after the last tile, -2 when a wait gave up
+  auto tile_of = [&](int it, bool all_lanes, int site) -> int {
+    if constexpr (!kDyn) {
+      const int t = cl + it * ncl;
+      return t < total ? t : -1;
+    } else {
+      const int slot = it % kRing;
+      if (!mbar_wait_acq_cluster(&ring_full[slot], static_cast<uint32_t>(it / kRing) & 1u,
+                                 abort_flag, p.err, site))
+        return -2;
+      const int t = *reinterpret_cast<volatile int*>(&ring[slot]);
+      if (all_lanes) __syncwarp();
+      if (!all_lanes || lane == 0) {
+        if (rank == 0) mbar_arrive(&ring_empty[slot]);
+        else mbar_arrive_cl(ring_empty0 + 8 * slot);
+      }
+      return t;
+    }
+  };
   if (warp == 0) {
     if (lane == 0) {
       // ---------------- TMA producer of this CTA's halves
@@ -661,7 +697,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       for (int s = 0; s < kS; ++s) issued[s] = -1;
       bool ok = true;
       int h_seen = -1;  // last split-state row group known to be in device memory
-      for (int t = cl; t < total && ok; t += ncl) {
+      for (int it = 0; ok; ++it) {
+        int t;
+        if (kDyn && rank == 0) {
+          // take the next tile and hand it to the other roles of both CTAs
+          const int slot = it % kRing;
+          if (it >= kRing &&
+              !mbar_wait_acq_cluster(&ring_empty[slot], (static_cast<uint32_t>(it / kRing) & 1u) ^ 1u,
+                                     abort_flag, p.err, kErrProducer)) {
+            ok = false;
+            break;
+          }
+          t = atomicAdd(p.tile_ctr, 1);
+          if (t >= total) t = -1;
+          ring[slot] = t;
+          st_cluster_u32(cluster_addr(smem_u32(&ring[slot]), 1), static_cast<uint32_t>(t));
+          mbar_arrive(&ring_full[slot]);
+          mbar_arrive_cl(cluster_addr(smem_u32(&ring_full[slot]), 1));
+        } else {
+          t = tile_of(it, false, kErrProducer);
+        }
+        if (t < 0) {
+          if (t == -2) ok = false;
+          break;
+        }
         int mu, n, b;
         decode_unit(t, p, mu, n, b);
         const int m = 2 * mu + static_cast<int>(rank);
@@ -736,9 +795,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
       const bool wide = !kQ8 && p.mode == kModeGram && p.bn == kGramWideCols;
       const uint32_t nst = wide ? kStagesWide : kS;
       uint32_t stage = 0, phase = 0;
-      int it = 0;
       bool ok = true;
-      for (int t = cl; t < total && ok; t += ncl, ++it) {
+      for (int it = 0; ok; ++it) {
+        const int t = tile_of(it, false, kErrMma);
+        if (t < 0) break;
         int mu, n, b;
         decode_unit(t, p, mu, n, b);
         const TileB tb = tile_b(p, n);
@@ -837,8 +897,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
     // ---------------- epilogue warpgroup (both CTAs)
     const int q = warp - 4;
     uint8_t* stg = stg_all + q * kStgWarpBytes;
-    int it = 0;
-    for (int t = cl; t < total; t += ncl, ++it) {
+    for (int it = 0;; ++it) {
+      const int t = tile_of(it, true, kErrEpilogue);
+      if (t < 0) break;
       int mu, n, b;
       decode_unit(t, p, mu, n, b);
       const int m = 2 * mu + static_cast<int>(rank);
@@ -926,7 +987,11 @@ cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream) {
   cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
-  rf_gemm2_kernel<false><<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(p);
+  GemmParams q = p;
+  q.tile_ctr = tile_counter_slot();
+  if (q.tile_ctr == nullptr) return cudaErrorInvalidSymbol;
+  if ((e = cudaMemsetAsync(q.tile_ctr, 0, sizeof(int), stream)) != cudaSuccess) return e;
+  rf_gemm2_kernel<false><<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(q);
   return cudaGetLastError();
 }
 

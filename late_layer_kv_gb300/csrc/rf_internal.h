@@ -150,6 +150,7 @@ struct GemmParams {
   float* bias_part;         // [M, n_tiles]
   int32_t out_ld;
   int* err;
+  int* tile_ctr;  // this launch's tile counter (zeroed before the launch): tiles are taken in order
   // elements of the buffers the epilogue writes with plain stores (checked by debug
   // builds): map mode ss_part, map_out; K/V mode with a row list the caches (per tensor);
   // GDN mode gdn_gate; Gram mode gram_G, gram_C; solve mode the outputs, bias_part
@@ -157,6 +158,10 @@ struct GemmParams {
   float inv_freq_hi[64];
   float inv_freq_lo[64];
 };
+
+// A zeroed-before-use counter for one pair-GEMM launch's dynamic tile order (a slot of a
+// library-owned device array of the current device; slots rotate over launches)
+int* tile_counter_slot();
 
 // every mode on CTA pairs (B tensor maps with boxes of half a tile's columns); `pairs`
 // clusters of 2

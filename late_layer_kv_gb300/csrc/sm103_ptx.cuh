@@ -296,6 +296,10 @@ __device__ __forceinline__ void mbar_arrive_cl(uint32_t addr) {
 __device__ __forceinline__ void fence_release_smem_cluster() {
   asm volatile("fence.release.sync_restrict::shared::cta.cluster;" ::: "memory");
 }
+// 32-bit store to shared::cluster address `addr` (this or the peer CTA)
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 // relaxed arrive on an mbarrier given by its shared::cluster address
 __device__ __forceinline__ void mbar_arrive_relaxed_cl(uint32_t addr) {
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(addr) : "memory");
