@@ -423,6 +423,14 @@ class HybridWorkload:
     def setup(self, dev, seed):
         from late_layer_kv_gb300 import ridgefill as rb
         s = self.shape
+        # the library runs the states of the first layers beside the projection GEMM of the
+        # rest when all rows fit one chunk and the states outnumber the SMs (one per SM): the
+        # "gdn_proj_gemm" stage then holds those states too, and "gdn_state" the last layers'
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        per_wave = sms // s.n_heads
+        la = s.n_gdn - per_wave if 0 < per_wave < s.n_gdn else 0
+        self.overlap_layers = la
+        self.stage_work["gdn_state"] = gdn_state_tensor_flop(s.rows, s.n_gdn - la, s.n_heads)
         self.inp = gdn_inputs(s, seed=seed)
         self.d = {k: v.to(dev) for k, v in self.inp.items()}
         self.Kc = torch.zeros((s.n_attn, s.n_kv, s.N, s.head_dim), dtype=torch.bfloat16,
@@ -545,6 +553,7 @@ class HybridWorkload:
                 "exact_prefix_rows": self.n_exact,
                 "terminal_correction": bool(self.exact_frac),
                 "kv_heads": s.n_kv, "head_dim": s.head_dim, "maps": "hbm",
+                "gdn_states_beside_projection": getattr(self, "overlap_layers", 0),
                 "l2": "inputs larger than L2 (maps %d MiB)" % (
                     (s.n_attn + s.n_gdn) * s.d * s.d * 2 >> 20)}
 

@@ -505,6 +505,7 @@ __device__ __forceinline__ void decode_unit(int t, const GemmParams& p, int& mu,
   const int rr = r - g * gsz;
   mu = first + rr % gm;
   n = rr / gm;
+  b += p.batch_base;
 }
 
 // ---- int8 maps.  A third ring ("raw", kRawStages deep) holds this CTA's half of

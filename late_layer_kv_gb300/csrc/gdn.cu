@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
   float* Bs = reinterpret_cast<float*>(sm + kOffScr);
   float* Xs = reinterpret_cast<float*>(sm + kOffT);  // scratch while T is formed
 
-  const int h = blockIdx.x, l = blockIdx.y;
+  const int h = blockIdx.x, l = blockIdx.y + p.layer_base;
   const int H = p.heads;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int lh = l * H + h;
@@ -922,9 +922,10 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
   pl->total = lay.off;
 }
 
+// The projection GEMM of layers [l0, l0 + nl) of the chunk (all of them by default).
 rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, const void* xhat,
                           const float* ss, __nv_bfloat16* kb, __nv_bfloat16* vb, float* gb,
-                          cudaStream_t s) {
+                          cudaStream_t s, int l0 = 0, int nl = -1) {
   GemmParams p{};
   p.mode = kModeGdnProj;
   p.k_blocks = a->d_out / kBK;
@@ -955,7 +956,8 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
   p.n_k_tiles = H / 2;
   p.n_v_tiles = H / 2;
   p.n_tiles = H + 1;
-  p.batches = a->n_layers;
+  p.batches = nl < 0 ? a->n_layers : nl;
+  p.batch_base = l0;
   p.bn = 256;
   p.group_m = 2;  // one pair row tile per group: every column tile of a row panel in turn
   p.rows = static_cast<int32_t>(rc);
@@ -1081,10 +1083,21 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     return guards_check(ws, pl.lay, s);
   }
 
+  // With all rows in one chunk and more (layer, head) states than SMs, the states of the
+  // first `la` layers run on a high-priority side stream as soon as their projections are
+  // done, beside the projection GEMM of the other layers, whose persistent CTAs take the
+  // SMs the state kernel leaves and join as its CTAs finish (tiles come from a counter).
+  // The last `L - la` layers' states then fill one wave of the SMs.  Without the split the
+  // states of all layers run in two waves, the second one on part of the GPU.
+  int la = 0;
+  {
+    const int per_wave = sm_count() / a->n_heads;  // layers whose states fill one wave
+    if (pl.R >= a->rows && per_wave > 0 && a->n_layers > per_wave) la = a->n_layers - per_wave;
+  }
   HostStreamer* hs = nullptr;
   std::unique_lock<std::mutex> lk(host_stream_mutex(), std::defer_lock);
   const size_t slot_bytes = map_slot_bytes(a->d_out, a->d_in, a->A_scale != nullptr);
-  if (a->maps_on_host || a->h_on_host) {
+  if (a->maps_on_host || a->h_on_host || la > 0) {
     lk.lock();
     hs = host_streamer();
     if (hs == nullptr) return RF_ERR_CUDA;
@@ -1187,7 +1200,27 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
       if (e != cudaSuccess) return cuda_fail(e, "exact-row input launch");
     }
     if ((st = mark(start, 1)) != RF_OK) return st;
-    if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s)) != RF_OK) return st;
+    sp.rows = static_cast<int32_t>(rc);
+    sp.first = start == 0 ? 1 : 0;
+    if (!state_maps(rc)) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the GDN state");
+    if (la > 0) {
+      // the first layers' projections, their states on the side stream, then the others'
+      // projections beside them
+      if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s, 0, la)) != RF_OK) return st;
+      cudaError_t e = cudaEventRecord(hs->prio_start, s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->prio, hs->prio_start, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "ordering the first layers' states");
+      GdnStateParams spa = sp;
+      spa.layers = la;
+      spa.layer_base = 0;
+      if ((e = launch_gdn_state(spa, hs->prio)) != cudaSuccess) return cuda_fail(e, "GDN state launch");
+      if ((e = cudaEventRecord(hs->prio_done, hs->prio)) != cudaSuccess)
+        return cuda_fail(e, "recording the first layers' states");
+      if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s, la, a->n_layers - la)) != RF_OK)
+        return st;
+    } else if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s)) != RF_OK) {
+      return st;
+    }
     if (want_rho) {
       rho_chunk_kernel<<<LH, kRhoThreads, 0, s>>>(gb, a->n_heads, pl.R, rc, start, a->exact_idx,
                                                   a->n_exact, rho_acc, start == 0 ? 1 : 0);
@@ -1195,11 +1228,13 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
       if (e != cudaSuccess) return cuda_fail(e, "rho launch");
     }
     if ((st = mark(start, 2)) != RF_OK) return st;
-    sp.rows = static_cast<int32_t>(rc);
-    sp.first = start == 0 ? 1 : 0;
-    if (!state_maps(rc)) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the GDN state");
-    cudaError_t e = launch_gdn_state(sp, s);
+    GdnStateParams spb = sp;
+    spb.layers = a->n_layers - la;
+    spb.layer_base = la;
+    cudaError_t e = launch_gdn_state(spb, s);
     if (e != cudaSuccess) return cuda_fail(e, "GDN state launch");
+    if (la > 0 && (e = cudaStreamWaitEvent(s, hs->prio_done, 0)) != cudaSuccess)
+      return cuda_fail(e, "ordering after the first layers' states");
     if ((st = mark(start, 3)) != RF_OK) return st;
   }
   if (a->h_on_host) {  // later work on `s` (and the caller's reuse of H) follows the copy

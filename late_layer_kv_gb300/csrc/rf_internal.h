@@ -81,6 +81,7 @@ struct GemmParams {
   int32_t m_tiles;
   int32_t n_tiles;     // tiles along N per batch entry
   int32_t batches;     // batch entries (layers) the tile loop covers
+  int32_t batch_base;  // batch entry of the first (a layer subset starts past 0)
   int32_t bn;          // MMA N of a tile
   int32_t group_m;     // raster group height
   int32_t rows;        // valid rows of this launch
@@ -181,6 +182,7 @@ struct GdnStateParams {
   int32_t rows;        // rows of this launch
   int32_t rows_alloc;
   int32_t first;       // 1 if S starts from S0/zero, 0 if it continues from S
+  int32_t layer_base;  // layer of grid row 0 (a layer subset starts past 0)
   int* err;
 };
 cudaError_t launch_gdn_state(const GdnStateParams& p, cudaStream_t stream);

@@ -75,6 +75,16 @@ def test_zero_rows_returns_initial_state():
     assert np.array_equal(zero, np.zeros_like(zero))
 
 
+def test_state_parity_states_beside_projection():
+    """More (layer, head) states than SMs with every row in one chunk (3 layers x 64 heads):
+    the states of the first layer run on a side stream beside the projection GEMM of the
+    other two; every state against the oracle, from S0."""
+    shape = _shape(d=256, L=3, H=64, N=300)
+    inp = gdn_inputs(shape, seed=35)
+    S0 = torch.randn((3, 64, 128, 128), generator=torch.Generator().manual_seed(7)) * 0.1
+    _cmp(_gpu(shape, inp, S0=S0), _oracle(shape, inp, S0=S0), "S overlapped")
+
+
 def test_long_memory_gates():
     """Gates near 0.99 (long memory) stress the carried state; w_a is aimed at the mean
     normalised input so that alpha = sigmoid(u . w_a) is large on every row."""
