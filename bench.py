@@ -51,12 +51,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # The fit depends only on d, the number of maps and the calibration rows, which the Llama-8B
 # fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
 _FIT_LLAMA8B = {"sources": "fit",
-                "kernel_sha256": "7ad51637bf3e960c6f33e78de3a9426b1f0e485b2de6860bcb1cb8173be8df05",
-                "bytes_per_launch": 101483784960 + 2813207552}
+                "kernel_sha256": "d6de737f32e4f88d01cb325e1ec4ca8f857e7f7f3c922c0ae3bbdfe4346c338e",
+                "bytes_per_launch": 73577685504 + 2790565632}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "97bd83d168cbb8bf882e5c56393468033083957afd19f1887d7cb11e592b96a3",
-                    "bytes_per_launch": 5779580364},
+                    "kernel_sha256": "261feb0584e3841ee1e64bf3333bcff3efc5b0dec77dc6880f491f9e8d27aecb",
+                    "bytes_per_launch": 5238894028},
     "llama8b_16k_fit": _FIT_LLAMA8B,
     "hostmaps_16k_fit": _FIT_LLAMA8B,
     "hostmaps_64k_fit": _FIT_LLAMA8B,
