@@ -590,9 +590,9 @@ class FitWorkload:
         # solve: preparation, equilibration, Cholesky (per block column the diagonal block,
         # then panel, next-column update and, while more columns remain, the rest of the
         # trailing update), zero fill, diagonal-block inverses, the doubling products, the
-        # bf16 split, three G^-1 products, two operand splits, the solve GEMM, the offsets
+        # bf16 split, the G^-1 product, two operand splits, the solve GEMM, the offsets
         chol = nb + 2 * (nb - 1) + max(0, nb - 2)
-        return 5 + 2 + chol + 2 + inv + 1 + 3 + 2 + 1 + 1
+        return 5 + 2 + chol + 2 + inv + 1 + 1 + 2 + 1 + 1
 
     def setup(self, dev, seed):
         """Calibration pairs drawn on the device (synthetic.calibration_device)."""

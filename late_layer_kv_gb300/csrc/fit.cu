@@ -112,15 +112,99 @@ __global__ void prep_kernel(const double* G, const double* sx, const double* cou
   }
 }
 
-// G^ = diag(s) (G - n mu mu^T + alpha I) diag(s), f32 [d, d]
-__global__ void equilibrate_kernel(const double* G, const double* count, const double* mu,
-                                   const float* s, const double* alpha, int d, float* Gh) {
+// ------------------------------------------------------------ f64 inputs without f64 math
+// This GPU's f64 pipe runs at a small fraction of its f32 rate, so kernels that read the
+// f64 sums take each value apart with integer operations into a double-float pair
+// (hi, lo): hi holds the 24 leading significant bits (truncated) and lo the next 23, so
+// |v - (hi + lo)| < 2^-46 |v|.  Magnitudes below 2^-126 give hi = 0 (below 2^-103, lo = 0);
+// magnitudes above the f32 range give hi = +-inf, and a NaN stays a NaN.  w0 and w1 are
+// the low and high 32-bit words of the f64.
+__device__ __forceinline__ float2 ff_of_bits(uint32_t w0, uint32_t w1) {
+  const uint32_t sign = w1 & 0x80000000u;
+  const int e = static_cast<int>((w1 >> 20) & 0x7ffu);  // biased f64 exponent
+  float hi, lo = 0.f;
+  if (e > 1150) {
+    const bool nan = e == 2047 && ((w1 & 0xfffffu) | w0) != 0u;
+    hi = __uint_as_float(sign | 0x7f800000u | (nan ? 0x400000u : 0u));
+  } else if (e < 897) {
+    hi = __uint_as_float(sign);
+  } else {
+    // same exponent, the top 23 of the 52 fraction bits
+    hi = __uint_as_float(sign | (static_cast<uint32_t>(e - 896) << 23) | ((w1 & 0xfffffu) << 3) |
+                         (w0 >> 29));
+    if (e >= 920) {
+      // the next 23 fraction bits r, worth r * 2^(E - 23) with 2^E = 2^-23 ulp(hi): written
+      // as (1 + r 2^-23) 2^E - 2^E, a difference that f32 takes exactly
+      const uint32_t base = sign | (static_cast<uint32_t>(e - 919) << 23);
+      lo = __uint_as_float(base | ((w0 & 0x1fffffffu) >> 6)) - __uint_as_float(base);
+    }
+  }
+  return make_float2(hi, lo);
+}
+
+__device__ __forceinline__ float2 ff_load(const double* p) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  return ff_of_bits(w.x, w.y);
+}
+
+// a - b c for double-float a, b, c, rounded once to f32.  The product's high part and its
+// exact error (fma), then an exact two-sum of the high parts; the low-order terms are
+// carried to about 2^-46 of |a|, so a difference down to 2^-22 |a| still comes out within
+// about one f32 ulp (f64 arithmetic rounded to f32 would hold down to about 2^-29 |a|).
+__device__ __forceinline__ float ff_sub_mul(float2 a, float2 b, float2 c) {
+  const float ph = __fmul_rn(b.x, c.x);  // kept apart from the subtraction below
+  const float pl = fmaf(b.x, c.x, -ph) + fmaf(b.x, c.y, b.y * c.x);
+  const float sh = __fsub_rn(a.x, ph);
+  const float z = __fsub_rn(sh, a.x);
+  const float se = __fadd_rn(__fsub_rn(a.x, __fsub_rn(sh, z)), __fsub_rn(-ph, z));
+  return sh + (se + (a.y - pl));
+}
+
+constexpr int kCentreRows = 8;  // rows per thread of the centring kernels
+
+// G^ = diag(s) (G - sx mu^T + alpha I) diag(s), f32 [d, d] (sx mu^T = n mu mu^T); eight
+// consecutive columns of kCentreRows rows per thread (d is a multiple of 128)
+__global__ void __launch_bounds__(256) equilibrate_kernel(const double* __restrict__ G,
+                                                          const double* __restrict__ sx,
+                                                          const double* __restrict__ mu,
+                                                          const float* __restrict__ s,
+                                                          const double* __restrict__ alpha, int d,
+                                                          float* __restrict__ Gh) {
+  const int g = d / 8;
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= static_cast<int64_t>(d) * d) return;
-  const int i = static_cast<int>(t / d), j = static_cast<int>(t % d);
-  double v = G[t] - (*count) * mu[i] * mu[j];
-  if (i == j) v += *alpha;
-  Gh[t] = static_cast<float>(v * s[i] * s[j]);
+  const int j0 = static_cast<int>(t % g) * 8;
+  const int64_t i0 = t / g * kCentreRows;
+  if (i0 >= d) return;
+  float2 m[8];
+  float sj[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    m[c] = ff_load(mu + j0 + c);
+    sj[c] = s[j0 + c];
+  }
+  const float2 al = ff_load(alpha);
+  const float a = al.x + al.y;
+  for (int r = 0; r < kCentreRows && i0 + r < d; ++r) {
+    const int64_t i = i0 + r;
+    const float2 b = ff_load(sx + i);
+    const float si = s[i];
+    const uint4* src = reinterpret_cast<const uint4*>(G + i * d + j0);
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = src[q];
+      v[2 * q] = ff_sub_mul(ff_of_bits(w.x, w.y), b, m[2 * q]);
+      v[2 * q + 1] = ff_sub_mul(ff_of_bits(w.z, w.w), b, m[2 * q + 1]);
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      if (i == j0 + c) v[c] += a;
+      v[c] = v[c] * si * sj[c];
+    }
+    float4* dst = reinterpret_cast<float4*>(Gh + i * d + j0);
+    dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+    dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+  }
 }
 
 // ------------------------------------------------------------ Cholesky (f32)
@@ -426,62 +510,112 @@ __device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(v - __bfloat162float(hi));
 }
 
-// B' [d, 3d] = [hi(G^-1) | lo(G^-1) | hi(G^-1)] from the f64 inverse
-__global__ void split_ginv_kernel(const double* Gi, int d, __nv_bfloat16* Bp) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= static_cast<int64_t>(d) * d) return;
-  const int64_t i = t / d, k = t % d;
-  const double v = Gi[t];
-  const __nv_bfloat16 hi = __float2bfloat16_rn(static_cast<float>(v));
-  const __nv_bfloat16 lo = __float2bfloat16_rn(static_cast<float>(v - static_cast<double>(__bfloat162float(hi))));
-  __nv_bfloat16* row = Bp + i * 3 * d;
-  row[k] = hi;
-  row[d + k] = lo;
-  row[2 * d + k] = hi;
+__device__ __forceinline__ uint32_t bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
 }
 
-// X = L^-1 (f32, lower) split into bf16 hi and lo parts
-__global__ void split2_kernel(const float* X, int64_t n, __nv_bfloat16* hi, __nv_bfloat16* lo) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= n) return;
-  __nv_bfloat16 h, l;
-  split_bf16(X[t], h, l);
-  hi[t] = h;
-  lo[t] = l;
-}
-
-// A' [L*d_out, 3d] = [hi(c) | hi(c) | lo(c)],  c[o, k] = s_k (C[o, k] - n mu_y[o] mu_x[k]);
-// eight consecutive k per thread (d is a multiple of 128): 64-byte reads of C,
-// 16-byte stores of each part
-__global__ void split_rhs_kernel(const double* C, const double* sy, const double* count,
-                                 const double* mu_x, const float* s, int64_t rows_out, int d,
-                                 __nv_bfloat16* Ap) {
+// B' [d, 3d] = [hi(G^-1) | lo(G^-1) | hi(G^-1)] from the f64 inverse: hi = bf16(v_hi) and
+// lo = bf16((v_hi - hi) + v_lo) of the double-float (v_hi, v_lo), the first difference
+// exact; eight consecutive k per thread
+__global__ void split_ginv_kernel(const double* __restrict__ Gi, int d, __nv_bfloat16* __restrict__ Bp) {
   const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const int g = d / 8;
-  if (t >= rows_out * g) return;
-  const int64_t o = t / g;
+  if (t >= static_cast<int64_t>(d) * g) return;
+  const int64_t i = t / g;
   const int k0 = static_cast<int>(t % g) * 8;
-  const double2* c2 = reinterpret_cast<const double2*>(C + o * d + k0);
-  const double syo = sy[o];  // n mu_y[o] mu_x[k] = sy[o] mu_x[k]
+  const uint4* src = reinterpret_cast<const uint4*>(Gi + i * d + k0);
   uint32_t hw[4], lw[4];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const double2 c = c2[j];
-    const float v0 = static_cast<float>(fma(-syo, mu_x[k0 + 2 * j], c.x)) * s[k0 + 2 * j];
-    const float v1 = static_cast<float>(fma(-syo, mu_x[k0 + 2 * j + 1], c.y)) * s[k0 + 2 * j + 1];
-    __nv_bfloat16 h0, l0, h1, l1;
-    split_bf16(v0, h0, l0);
-    split_bf16(v1, h1, l1);
-    hw[j] = static_cast<uint32_t>(__bfloat16_as_ushort(h0)) |
-            (static_cast<uint32_t>(__bfloat16_as_ushort(h1)) << 16);
-    lw[j] = static_cast<uint32_t>(__bfloat16_as_ushort(l0)) |
-            (static_cast<uint32_t>(__bfloat16_as_ushort(l1)) << 16);
+  for (int q = 0; q < 4; ++q) {
+    const uint4 w = src[q];
+    const float2 v0 = ff_of_bits(w.x, w.y), v1 = ff_of_bits(w.z, w.w);
+    const __nv_bfloat16 h0 = __float2bfloat16_rn(v0.x), h1 = __float2bfloat16_rn(v1.x);
+    const __nv_bfloat16 l0 = __float2bfloat16_rn((v0.x - __bfloat162float(h0)) + v0.y);
+    const __nv_bfloat16 l1 = __float2bfloat16_rn((v1.x - __bfloat162float(h1)) + v1.y);
+    hw[q] = bf16x2(h0, h1);
+    lw[q] = bf16x2(l0, l1);
   }
-  __nv_bfloat16* row = Ap + o * 3 * d;
+  __nv_bfloat16* row = Bp + i * 3 * d;
   const uint4 h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
   *reinterpret_cast<uint4*>(row + k0) = h;
-  *reinterpret_cast<uint4*>(row + d + k0) = h;
-  *reinterpret_cast<uint4*>(row + 2 * d + k0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  *reinterpret_cast<uint4*>(row + d + k0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  *reinterpret_cast<uint4*>(row + 2 * d + k0) = h;
+}
+
+// X = L^-1 (f32, lower, n elements) split into the four bf16 planes [hi; lo; hi; hi] of n
+// elements each: planes 0-2 against planes 1-3, summed over the stacked rows, give
+// hi^T lo + lo^T hi + hi^T hi in one Gram product.  Eight elements per thread.
+__global__ void split2_kernel(const float* __restrict__ X, int64_t n, __nv_bfloat16* __restrict__ P) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (t >= n / 8) return;
+  const float4* src = reinterpret_cast<const float4*>(X) + 2 * t;
+  const float4 x0 = src[0], x1 = src[1];
+  const float v[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+  uint32_t hw[4], lw[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    __nv_bfloat16 h0, l0, h1, l1;
+    split_bf16(v[2 * q], h0, l0);
+    split_bf16(v[2 * q + 1], h1, l1);
+    hw[q] = bf16x2(h0, h1);
+    lw[q] = bf16x2(l0, l1);
+  }
+  const uint4 h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  uint4* dst = reinterpret_cast<uint4*>(P) + t;
+  const int64_t plane = n / 8;  // uint4 per plane
+  dst[0] = h;
+  dst[plane] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  dst[2 * plane] = h;
+  dst[3 * plane] = h;
+}
+
+// A' [L*d_out, 3d] = [hi(c) | hi(c) | lo(c)],  c[o, k] = s_k (C[o, k] - sy[o] mu_x[k])
+// (sy[o] mu_x[k] = n mu_y[o] mu_x[k]), centred in double-float as above; eight consecutive
+// k of kCentreRows rows per thread (d is a multiple of 128): 64-byte reads of C, 16-byte
+// stores of each part
+__global__ void __launch_bounds__(256) split_rhs_kernel(const double* __restrict__ C,
+                                                        const double* __restrict__ sy,
+                                                        const double* __restrict__ mu_x,
+                                                        const float* __restrict__ s,
+                                                        int64_t rows_out, int d,
+                                                        __nv_bfloat16* __restrict__ Ap) {
+  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const int g = d / 8;
+  const int k0 = static_cast<int>(t % g) * 8;
+  const int64_t o0 = t / g * kCentreRows;
+  if (o0 >= rows_out) return;
+  float2 m[8];
+  float sk[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    m[c] = ff_load(mu_x + k0 + c);
+    sk[c] = s[k0 + c];
+  }
+#pragma unroll 2
+  for (int r = 0; r < kCentreRows; ++r) {
+    const int64_t o = o0 + r;
+    if (o >= rows_out) break;
+    const float2 b = ff_load(sy + o);
+    const uint4* src = reinterpret_cast<const uint4*>(C + o * d + k0);
+    uint32_t hw[4], lw[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = src[q];
+      const float v0 = ff_sub_mul(ff_of_bits(w.x, w.y), b, m[2 * q]) * sk[2 * q];
+      const float v1 = ff_sub_mul(ff_of_bits(w.z, w.w), b, m[2 * q + 1]) * sk[2 * q + 1];
+      __nv_bfloat16 h0, l0, h1, l1;
+      split_bf16(v0, h0, l0);
+      split_bf16(v1, h1, l1);
+      hw[q] = bf16x2(h0, h1);
+      lw[q] = bf16x2(l0, l1);
+    }
+    __nv_bfloat16* row = Ap + o * 3 * d;
+    const uint4 h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(row + k0) = h;
+    *reinterpret_cast<uint4*>(row + d + k0) = h;
+    *reinterpret_cast<uint4*>(row + 2 * d + k0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  }
 }
 
 // b[o] = mu_y[o] - sum_t part[o, t]
@@ -497,7 +631,7 @@ __global__ void bias_kernel(const double* sy, const double* count, const float* 
 // ------------------------------------------------------------ plan
 struct FitPlan {
   size_t off_gh = 0, off_s = 0, off_mu32 = 0, off_mu64 = 0, off_alpha = 0,
-         off_xhi = 0, off_xlo = 0, off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0,
+         off_xs = 0, off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0,
          off_cs = 0, off_linv = 0, total = 0;
   int bn = 0;
   int slabs = 0;
@@ -537,8 +671,7 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->off_mu64 = lay.take(d * 8);
     pl->off_alpha = lay.take(8);
     pl->off_linv = lay.take(kNB * kNB * 4);
-    pl->off_xhi = lay.take(d * d * 2);
-    pl->off_xlo = lay.take(d * d * 2);
+    pl->off_xs = lay.take(4 * d * d * 2);  // bf16 planes [hi; lo; hi; hi] of L^-1
     pl->off_gi = lay.take(d * d * 8);
     pl->off_bp = lay.take(d * 3 * d * 2);
     pl->off_ap = lay.take(M * 3 * d * 2);
@@ -639,8 +772,7 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   double* mu64 = reinterpret_cast<double*>(ws + pl.off_mu64);
   double* alpha = reinterpret_cast<double*>(ws + pl.off_alpha);
   double* Gi = reinterpret_cast<double*>(ws + pl.off_gi);
-  __nv_bfloat16* Xhi = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xhi);
-  __nv_bfloat16* Xlo = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xlo);
+  __nv_bfloat16* Xs = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_xs);
   __nv_bfloat16* Bp = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_bp);
   __nv_bfloat16* Ap = reinterpret_cast<__nv_bfloat16*>(ws + pl.off_ap);
   float* part = reinterpret_cast<float*>(ws + pl.off_part);
@@ -650,8 +782,9 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
 
   prep_kernel<<<1, 256, 0, s>>>(a->G, a->sx, a->count, d, a->lambda, sc, mu32, mu64, alpha,
                                 a->alpha_out);
-  equilibrate_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(a->G, a->count, mu64,
-                                                                              sc, alpha, d, Gh);
+  const int64_t eq_threads = ceil_div(d, kCentreRows) * (d / 8);
+  equilibrate_kernel<<<static_cast<unsigned>(ceil_div(eq_threads, 256)), 256, 0, s>>>(
+      a->G, a->sx, mu64, sc, alpha, d, Gh);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fit preparation launch");
 
@@ -699,10 +832,10 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   // X = L^-1 in place: the 64 x 64 diagonal blocks, then recursive doubling:
   // blocks [s1 | s2] of size s (already inverted) merge as
   //   X_21 = -X_22 (L_21 X_11),
-  // every pair of a level in one batched product (the scratch T is the X_hi/X_lo
-  // area, free until the split below)
+  // every pair of a level in one batched product (the scratch T is the area of the
+  // bf16 planes, free until the split below)
   trinv_diag_kernel<<<nb, 256, 0, s>>>(Gh, d);
-  float* T = reinterpret_cast<float*>(Xhi);
+  float* T = reinterpret_cast<float*>(Xs);
   for (int sz = kNB; sz < d; sz *= 2) {
     const int full = d / (2 * sz);        // pairs with both halves of size sz
     const int rest = d - full * 2 * sz;   // a last pair [sz | rest - sz] if rest > sz
@@ -724,19 +857,20 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
       if ((e = sgemm(false, g2, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
     }
   }
-  // G^-1 = X^T X on the tensor cores: three MN-major Gram products of the bf16
-  // split of X (hi hi + hi lo + lo hi), summed in f64
-  split2_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gh, dd, Xhi, Xlo);
+  // G^-1 = X^T X on the tensor cores: one MN-major Gram product over the stacked bf16
+  // planes, [hi; lo; hi] against [lo; hi; hi] (K = 3d, summed in f32 in TMEM), added into
+  // the cleared f64 inverse
+  split2_kernel<<<static_cast<unsigned>(ceil_div(dd / 8, 256)), 256, 0, s>>>(Gh, dd, Xs);
   if ((e = cudaMemsetAsync(Gi, 0, static_cast<size_t>(dd) * 8, s)) != cudaSuccess)
     return cuda_fail(e, "clearing the inverse");
   rf_status st;
-  if ((st = launch_gram(Xhi, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
-  if ((st = launch_gram(Xhi, Xlo, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
-  if ((st = launch_gram(Xlo, Xhi, nullptr, 0, d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK) return st;
+  if ((st = launch_gram(Xs, Xs + dd, nullptr, 0, 3 * d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK)
+    return st;
 
-  split_ginv_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gi, d, Bp);
-  split_rhs_kernel<<<static_cast<unsigned>((M * (d / 8) + 255) / 256), 256, 0, s>>>(
-      a->C, a->sy, a->count, mu64, sc, M, d, Ap);
+  split_ginv_kernel<<<static_cast<unsigned>(ceil_div(dd / 8, 256)), 256, 0, s>>>(Gi, d, Bp);
+  const int64_t rhs_threads = ceil_div(M, kCentreRows) * (d / 8);
+  split_rhs_kernel<<<static_cast<unsigned>(ceil_div(rhs_threads, 256)), 256, 0, s>>>(
+      a->C, a->sy, mu64, sc, M, d, Ap);
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "operand split launch");
 
   GemmParams p{};

@@ -176,6 +176,40 @@ def test_solve_matches_closed_form(d, L, n, lam):
                                                             .to(torch.bfloat16)))
 
 
+def test_solve_centres_sums_with_large_means():
+    """Sums of columns whose means are 1,000 standard deviations from zero (and outputs 500
+    from zero), built in f64 and handed to the solve directly: the centred Gram and
+    cross terms cancel about 20 of the leading bits of every entry, which the solve's
+    centring keeps (a plain f32 centring would leave errors of order 2^-3)."""
+    rng = np.random.default_rng(47)
+    d, L, n, lam = 256, 2, 3000, 1e-3
+    X = rng.standard_normal((n, d))
+    X[:, : d // 2] += 1000.0
+    W = rng.standard_normal((L, d, d)) / np.sqrt(d)
+    Y = np.einsum("nk,lko->lno", X - X.mean(axis=0), W) + 500.0 + 0.1 * rng.standard_normal((L, n, d))
+    cnt, sx, sy, G, C = oracle.fit_sums(X, Y)
+    sums = FitSums(L, d, d)
+    sums.G.copy_(torch.from_numpy(G))
+    sums.C.copy_(torch.from_numpy(C.T.reshape(L, d, d)))
+    sums.sx.copy_(torch.from_numpy(sx))
+    sums.sy.copy_(torch.from_numpy(sy))
+    sums.count.fill_(float(cnt))
+    A32 = torch.empty((L, d, d), dtype=torch.float32, device="cuda")
+    b = torch.empty((L, d), dtype=torch.float32, device="cuda")
+    ridgefill_fit_solve(sums, lam, A_out_f32=A32, b_out=b)
+    torch.cuda.synchronize()
+    assert device_error() == 0
+    Ao, bo, _ = oracle.ridge_solve_from_sums(cnt, sx, sy, G, C, lam)
+    A = A32.cpu().double().numpy()
+    bg = b.cpu().double().numpy()
+    mu_x = sx / cnt
+    for l in range(L):
+        assert _rel(A[l], Ao[l]) <= W_REL_FRO, f"layer {l}: {_rel(A[l], Ao[l]):.2e}"
+        # b = mu_y - A mu_x: the map's error is carried by mu_x, whose entries are 1,000
+        scale = np.linalg.norm(Ao[l]) * np.linalg.norm(mu_x) + np.linalg.norm(bo[l])
+        assert np.linalg.norm(bg[l] - bo[l]) <= W_REL_FRO * scale
+
+
 def test_batch_split_does_not_change_the_fit():
     cal = calibration(d=256, n_layers=2, n=2048, seed=43)
     _, A1, _, b1, _ = _gpu_fit(cal["X"], cal["Y"], 1e-3)
