@@ -579,20 +579,21 @@ class FitWorkload:
     def launches_per_step(self):
         d = self.shape.d
         nb = d // 64
-        # triangular inverse by recursive doubling: two batched products per part of a level
+        # triangular inverse by recursive doubling: per part of a level four operand splits
+        # and two batched products
         inv, sz = 0, 64
         while sz < d:
             full = d // (2 * sz)
             rest = d - full * 2 * sz
-            inv += 2 * ((1 if full > 0 else 0) + (1 if rest > sz else 0))
+            inv += 6 * ((1 if full > 0 else 0) + (1 if rest > sz else 0))
             sz *= 2
         # accumulate: two column-sum passes, their reduction, the count, the Gram products;
-        # solve: preparation, equilibration, Cholesky (per block column the diagonal block,
-        # then panel, next-column update and, while more columns remain, the rest of the
-        # trailing update), zero fill, diagonal-block inverses, the doubling products, the
+        # solve: preparation, equilibration, Cholesky (per block column the diagonal block
+        # with its inverse, then panel with the next-column update and, while more columns
+        # remain, the rest of the trailing update), zero fill, the doubling products, the
         # bf16 split, the G^-1 product, two operand splits, the solve GEMM, the offsets
-        chol = nb + 2 * (nb - 1) + max(0, nb - 2)
-        return 5 + 2 + chol + 2 + inv + 1 + 1 + 2 + 1 + 1
+        chol = nb + (nb - 1) + max(0, nb - 2)
+        return 5 + 2 + chol + 1 + inv + 1 + 1 + 2 + 1 + 1
 
     def setup(self, dev, seed):
         """Calibration pairs drawn on the device (synthetic.calibration_device)."""

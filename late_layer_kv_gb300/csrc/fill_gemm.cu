@@ -61,7 +61,7 @@ struct TileB {
 
 __device__ __forceinline__ TileB tile_b(const GemmParams& p, int n) {
   TileB t;
-  if (p.mode == kModeMap || p.mode == kModeGram || p.mode == kModeSolve) {
+  if (p.mode == kModeMap || p.mode == kModeGram || p.mode == kModeSolve || p.mode == kModeF32) {
     t.seg = 0; t.nrow = n * p.bn; t.bn = p.bn;
   } else if (p.mode == kModeKV) {
     const bool v = n >= p.n_k_tiles;
@@ -467,6 +467,56 @@ __device__ void epilogue_solve(const GemmParams& p, uint32_t tcol, int q, int la
   if (valid) p.bias_part[static_cast<size_t>(o) * p.n_tiles + n] = part;
 }
 
+// Plain f32 product: out[b, o, c] = alpha acc, plus the stored value when beta_one (rows
+// below p.rows, columns below p.cols, a multiple of 32).  The stored values of the next
+// 32 columns are loaded while the current ones are written, so two chunks of the row's
+// read-modify-write are in flight at a time.
+__device__ void epilogue_f32(const GemmParams& p, uint32_t tcol, int q, int lane, int m, int n,
+                             int b, uint32_t tempty) {
+  const int o = m * kBM + q * 32 + lane;
+  const int c_base = n * p.bn;
+  const int64_t row0 = static_cast<int64_t>(b) * p.out_bstride + static_cast<int64_t>(o) * p.out_ld;
+  // chunk c0 of this row is stored when it lies inside the output (and, in debug builds,
+  // inside the buffer)
+  auto live = [&](int c0) {
+    if (o >= p.rows || c_base + c0 >= p.cols) return false;
+    const int64_t e0 = row0 + c_base + c0;
+    return in_bounds(e0, p.lim_b, p.err) && in_bounds(e0 + 31, p.lim_b, p.err);
+  };
+  auto load_old = [&](int c0, bool ok, float4 (&v)[8]) {
+    const float4* s4 = reinterpret_cast<const float4*>(p.out_f32 + row0 + c_base + c0);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = (ok && p.beta_one) ? s4[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+  };
+  bool ok = live(0);
+  float4 cur[8];
+  load_old(0, ok, cur);
+  for (int c0 = 0; c0 < p.bn; c0 += 32) {
+    uint32_t a[32];
+    tmem_ld32(tcol + c0, a);
+    const bool more = c0 + 32 < p.bn;
+    const bool ok_next = more && live(c0 + 32);
+    float4 nxt[8];
+    load_old(c0 + 32, ok_next, nxt);
+    tmem_wait_ld();
+    if (!more) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cl(tempty);
+    }
+    if (ok) {
+      float4* d4 = reinterpret_cast<float4*>(p.out_f32 + row0 + c_base + c0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        d4[j] = make_float4(fmaf(p.alpha, f32(a[4 * j]), cur[j].x), fmaf(p.alpha, f32(a[4 * j + 1]), cur[j].y),
+                            fmaf(p.alpha, f32(a[4 * j + 2]), cur[j].z), fmaf(p.alpha, f32(a[4 * j + 3]), cur[j].w));
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) cur[j] = nxt[j];
+    ok = ok_next;
+  }
+}
+
 }  // namespace
 
 // ------------------------------------------------------------------ CTA pairs
@@ -492,7 +542,22 @@ namespace {
 // Tile t of the pair grid: pair row tile mu (row tiles 2 mu and 2 mu + 1, one per CTA) of
 // column tile n, in batch b; grouped raster over pair row tiles.
 __device__ __forceinline__ int units_m(const GemmParams& p) { return (p.m_tiles + 1) / 2; }
+// Tiles of one launch: pair row tiles x column tiles x batches, or the pair tiles on and below
+// the diagonal (lower: n <= mu)
+__device__ __forceinline__ int tiles_total(const GemmParams& p) {
+  const int u = units_m(p);
+  return p.lower ? u * (u + 1) / 2 : u * p.n_tiles * p.batches;
+}
 __device__ __forceinline__ void decode_unit(int t, const GemmParams& p, int& mu, int& n, int& b) {
+  if (p.lower) {  // row-major over the lower triangle: t = mu (mu + 1) / 2 + n
+    int r = static_cast<int>((sqrtf(8.f * static_cast<float>(t) + 1.f) - 1.f) * 0.5f);
+    while ((r + 1) * (r + 2) / 2 <= t) ++r;
+    while (r * (r + 1) / 2 > t) --r;
+    mu = r;
+    n = t - r * (r + 1) / 2;
+    b = 0;
+    return;
+  }
   const int m_units = units_m(p);
   const int gp = p.group_m / 2 > 0 ? p.group_m / 2 : 1;
   const int per_b = m_units * p.n_tiles;
@@ -664,7 +729,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   cluster_sync();  // both CTAs' barriers are initialised and their TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int total = units_m(p) * p.n_tiles * p.batches;
+  const int total = tiles_total(p);
   const uint32_t full0 = cluster_addr(smem_u32(full), 0);
   const uint32_t tempty0 = cluster_addr(smem_u32(tempty), 0);
   const uint32_t ring_empty0 = cluster_addr(smem_u32(ring_empty), 0);
@@ -928,6 +993,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         epilogue_gram(p, tcol, q, lane, m, n, tempty0 + 8 * acc);
       } else if (p.mode == kModeSolve) {
         epilogue_solve(p, tcol, q, lane, m, n, tempty0 + 8 * acc);
+      } else if (p.mode == kModeF32) {
+        epilogue_f32(p, tcol, q, lane, m, n, b, tempty0 + 8 * acc);
       } else {
         epilogue_gdn(p, tcol, stg, q, lane, m, n, b, rs, tempty0 + 8 * acc);
       }

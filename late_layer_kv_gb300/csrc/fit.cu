@@ -207,26 +207,110 @@ __global__ void __launch_bounds__(256) equilibrate_kernel(const double* __restri
   }
 }
 
+// ------------------------------------------------------------ bf16 splits
+__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
+  hi = __float2bfloat16_rn(v);
+  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+__device__ __forceinline__ uint32_t bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
+}
+
+// Products to about f32 precision on the bf16 tensor cores.  x = h + m + l with h = bf16(x),
+// m = bf16(x - h), l = bf16(x - h - m) (both differences exact in f32).  A matrix is stored
+// as seven K-wide bf16 planes [h, h, m, m, h, l, h] per row; planes 0-5 of one such split
+// against planes 1-6 of another pair h h, h m, m m, m h, h l and l h, so one product over
+// the stacked K (6 K) sums every term but m l, l m and l l, each within about 2^-24 of the
+// result.
+constexpr int kPlanes = 7;
+
+__device__ __forceinline__ void split3_bf16(float x, __nv_bfloat16& h, __nv_bfloat16& m,
+                                            __nv_bfloat16& l) {
+  h = __float2bfloat16_rn(x);
+  const float r = x - __bfloat162float(h);
+  m = __float2bfloat16_rn(r);
+  l = __float2bfloat16_rn(r - __bfloat162float(m));
+}
+
+// the seven planes of n consecutive values (n = 2 or 4 here) as bf16 words: w[plane][n / 2]
+template <int N>
+__device__ __forceinline__ void planes_of(const float (&x)[N], uint32_t (&w)[kPlanes][N / 2]) {
+#pragma unroll
+  for (int i = 0; i < N; i += 2) {
+    __nv_bfloat16 h0, m0, l0, h1, m1, l1;
+    split3_bf16(x[i], h0, m0, l0);
+    split3_bf16(x[i + 1], h1, m1, l1);
+    const uint32_t h = bf16x2(h0, h1), m = bf16x2(m0, m1), l = bf16x2(l0, l1);
+    w[0][i / 2] = h; w[1][i / 2] = h; w[2][i / 2] = m; w[3][i / 2] = m;
+    w[4][i / 2] = h; w[5][i / 2] = l; w[6][i / 2] = h;
+  }
+}
+
+// Seven-plane split of a batch of row-major f32 matrices: output row r of batch entry bat,
+// [kPlanes * K] bf16 at out + (bat * rows + r) * kPlanes * K, holds element (r, k) of the
+// source, src[bat * sstride + r * ld + k], or, transposed (TR), src[bat * sstride + k * ld + r].
+// One 64 x 64 tile per CTA through shared memory (grid K / 64, ceil(rows / 64), batches);
+// K is a multiple of 64.
+template <bool TR>
+__global__ void __launch_bounds__(256) split7_kernel(const float* __restrict__ src, int64_t ld,
+                                                     int64_t sstride, int rows, int K,
+                                                     __nv_bfloat16* __restrict__ out) {
+  __shared__ float t[64][65];
+  const int k0 = blockIdx.x * 64, r0 = blockIdx.y * 64;
+  const int64_t bat = blockIdx.z;
+  const float* sb = src + bat * sstride;
+  float v[16];  // all loads in flight before the shared-memory stores
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    const int i = e / 64, j = e % 64;  // i: source row in the tile, j: source column
+    if (TR) v[q] = r0 + j < rows ? sb[static_cast<int64_t>(k0 + i) * ld + r0 + j] : 0.f;
+    else v[q] = r0 + i < rows ? sb[static_cast<int64_t>(r0 + i) * ld + k0 + j] : 0.f;
+  }
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    const int i = e / 64, j = e % 64;
+    if (TR) t[j][i] = v[q];
+    else t[i][j] = v[q];
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < 64 * 16; e += 256) {
+    const int r = e / 16, kq = (e % 16) * 4;
+    if (r0 + r >= rows) continue;
+    const float x[4] = {t[r][kq], t[r][kq + 1], t[r][kq + 2], t[r][kq + 3]};
+    uint32_t w[kPlanes][2];
+    planes_of(x, w);
+    __nv_bfloat16* o = out + (bat * rows + r0 + r) * static_cast<int64_t>(kPlanes) * K + k0 + kq;
+#pragma unroll
+    for (int pl = 0; pl < kPlanes; ++pl)
+      *reinterpret_cast<uint2*>(o + static_cast<int64_t>(pl) * K) = make_uint2(w[pl][0], w[pl][1]);
+  }
+}
+
 // ------------------------------------------------------------ Cholesky (f32)
-// One 64x64 diagonal block: the lower factor L_kk in place (zeros above) and its
-// inverse into Linv [64, 64] (lower), both right-looking in one sweep over the
+// One 64x64 diagonal block: the lower factor L_kk and its inverse, both right-looking
+// in one sweep over the
 // columns j: the pivot, column j of L and row j of L^-1 scaled by its reciprocal,
 // then the rank-1 updates a_ik -= l_ij l_kj and x_ic -= l_ij x_jc.  A pivot <= 0
 // records kErrNumeric in the device error word and continues with pivot 1.
 // 256 threads, ti = tid % 16, tk = tid / 16, all cells in registers: thread
 // (ti, tk) keeps a_ik for rows i = ti + 16u and columns k = tk + 16v, and x_ic
 // transposed, rows i = tk + 16v and columns c = ti + 16u, so column j of L and
-// row j of L^-1 both sit in the sixteen threads tk = j % 16 (half a warp).  They
-// take the pivot's square root and reciprocal themselves and publish the column
-// and the row through shared memory with zeros outside i > j and c <= j.  The
-// updates then need no masks: the zeros leave every other cell unchanged, and
-// only the (never read) upper triangle of a takes stray updates.  The owner of
-// the next diagonal cell publishes it after the update: two barriers a step.
+// row j of L^-1 both sit in the sixteen threads tk = j % 16 (half a warp).  That
+// half-warp reads the pivot a_jj from its lane ti = j % 16 by a shuffle, takes its
+// root and reciprocal and publishes the column and the row through shared memory
+// (double-buffered by the parity of j) with zeros outside i > j and c <= j.  The
+// updates then need no masks: the zeros leave every other cell unchanged, and only
+// the (never read) upper triangle of a takes stray updates.  One barrier a step.  The
+// inverse L_kk^-1 (zeros above) goes to Linv [64, 64] and over the diagonal block: later
+// steps read only the blocks below it, and the triangular inverse starts from it.
 __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int kb, int* err,
                                                          float* Linv) {
-  __shared__ float col[kNB];   // l_ij for i > j, else 0
-  __shared__ float xrow[kNB];  // x_jc for c <= j, else 0
-  __shared__ float diag;       // a_jj before its square root
+  __shared__ float col[2][kNB];   // l_ij for i > j, else 0
+  __shared__ float xrow[2][kNB];  // x_jc for c <= j, else 0
   float* blk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
   const int tid = threadIdx.x, ti = tid & 15, tk = tid >> 4;
   float a[4][4], x[4][4];
@@ -237,20 +321,20 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int k
       a[u][v] = blk[static_cast<size_t>(ti + 16 * u) * ld + tk + 16 * v];
       x[v][u] = (tk + 16 * v == ti + 16 * u) ? 1.f : 0.f;
     }
-  if (tid == 0) diag = a[0][0];
-  __syncthreads();
+  const int hl = 16 * (tk & 1);                   // this half-warp's first lane
+  const unsigned half = 0xffffu << hl;
   // j = 16 jw + jt with jw unrolled, so every register index below is static
 #pragma unroll
   for (int jw = 0; jw < 4; ++jw) {
     for (int jt = 0; jt < 16; ++jt) {
-      const int j = 16 * jw + jt;
+      const int j = 16 * jw + jt, buf = j & 1;
       if (tk == jt) {  // column j of L (a[u][jw]) and row j of L^-1 (x[jw][u])
-        float v = diag;
+        float v = __shfl_sync(half, a[jw][jw], hl + jt);  // a_jj, from lane ti = jt
         if (!(v > 0.f)) {
           if (ti == 0) atomicCAS(err, 0, kErrNumeric);
           v = 1.f;
         }
-        const float p = sqrtf(v), r = 1.f / p;
+        const float r = rsqrtf(v), p = v * r;
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int i = ti + 16 * u;  // row of a, column of x
@@ -263,17 +347,17 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int k
             x[jw][u] *= r;
             xv = x[jw][u];
           }
-          col[i] = lv;
-          xrow[i] = xv;
+          col[buf][i] = lv;
+          xrow[buf][i] = xv;
         }
       }
       __syncthreads();
       float ci[4], xr[4], ck[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
-        ci[u] = col[ti + 16 * u];
-        xr[u] = xrow[ti + 16 * u];
-        ck[u] = col[tk + 16 * u];
+        ci[u] = col[buf][ti + 16 * u];
+        xr[u] = xrow[buf][ti + 16 * u];
+        ck[u] = col[buf][tk + 16 * u];
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -282,13 +366,6 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int k
           a[u][v] = fmaf(-ci[u], ck[v], a[u][v]);
           x[v][u] = fmaf(-ck[v], xr[u], x[v][u]);
         }
-      // the owner of the next diagonal cell publishes it
-      const int jn = (j + 1) & 15;
-      if (ti == jn && tk == jn) {
-        if (jt < 15) diag = a[jw][jw];
-        else if (jw < 3) diag = a[jw < 3 ? jw + 1 : 3][jw < 3 ? jw + 1 : 3];
-      }
-      __syncthreads();
     }
   }
 #pragma unroll
@@ -296,38 +373,45 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int k
 #pragma unroll
     for (int v = 0; v < 4; ++v) {
       const int i = ti + 16 * u, k = tk + 16 * v;
-      blk[static_cast<size_t>(i) * ld + k] = k <= i ? a[u][v] : 0.f;
-      Linv[k * kNB + i] = i <= k ? x[v][u] : 0.f;  // x cell: row k, column i
+      const float xv = i <= k ? x[v][u] : 0.f;  // x cell: row k, column i
+      blk[static_cast<size_t>(k) * ld + i] = xv;
+      Linv[k * kNB + i] = xv;
     }
 }
 
-// Panel: A_ik <- A_ik L_kk^-T = A_ik Linv^T for block rows i > kb (one 64x64 block
-// per CTA; 256 threads with 4 x 4 outputs each).
-__global__ void __launch_bounds__(256) trsm_panel_kernel(float* A, int ld, int kb,
-                                                         const float* Linv) {
-  __shared__ float X[kNB][kNB + 1];
-  __shared__ __align__(16) float Lt[kNB][kNB + 4];  // Lt[k][c] = Linv[c][k]
-  const int ib = kb + 1 + blockIdx.x;
-  float* aik = A + static_cast<size_t>(ib) * kNB * ld + static_cast<size_t>(kb) * kNB;
-  {
-    float xv[16], lv[16];  // all loads in flight before the shared-memory stores
+// Panel and next block column of Cholesky step kb, one 64-row block ib = kb + 1 + blockIdx.x
+// per CTA (256 threads, 4 x 4 outputs each):
+//   P_ib = A[ib, kb] L_kk^-T = A[ib, kb] Linv^T     (the block of L, written back)
+//   A[ib, kb + 1] -= P_ib P_(kb+1)^T                 (the next column's share of the update)
+// Every CTA forms P_(kb+1) itself (one more 64 x 64 product) rather than waiting for the CTA
+// that owns it.  With `planes` set, the blocks ib >= kb + 2 also go there as seven-plane
+// splits, row (ib - kb - 2) * 64 + r, for the trailing update on the tensor cores.  Dynamic
+// shared memory: Lt = Linv^T [64][68] (later P_ib), X [64][65] (the block being solved) and
+// P0 = P_(kb+1) [64][65].
+constexpr int kPanelSmem = (kNB * (kNB + 4) + 2 * kNB * (kNB + 1)) * 4;
+
+__device__ __forceinline__ void load_block(const float* src, int ld, float (*dst)[kNB + 1]) {
+  float v[16];  // all loads in flight before the shared-memory stores
 #pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int e = threadIdx.x + 256 * q;
-      xv[q] = aik[static_cast<size_t>(e / kNB) * ld + e % kNB];
-      lv[q] = Linv[e];
-    }
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int e = threadIdx.x + 256 * q;
-      X[e / kNB][e % kNB] = xv[q];
-      Lt[e % kNB][e / kNB] = lv[q];
-    }
+  for (int q = 0; q < 16; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    v[q] = src[static_cast<size_t>(e / kNB) * ld + e % kNB];
   }
-  __syncthreads();
-  const int r0 = (threadIdx.x / 16) * 4, c0 = (threadIdx.x % 16) * 4;
-  float acc[4][4] = {};
-  for (int k = 0; k < c0 + 4; ++k) {  // Linv[c][k] = 0 for k > c
+#pragma unroll
+  for (int q = 0; q < 16; ++q) {
+    const int e = threadIdx.x + 256 * q;
+    dst[e / kNB][e % kNB] = v[q];
+  }
+}
+
+// acc = X Linv^T for this thread's rows r0 + u and columns c0 + w (Linv[c][k] = 0 for k > c)
+__device__ __forceinline__ void solve_block(const float (*X)[kNB + 1], const float (*Lt)[kNB + 4],
+                                            int r0, int c0, float (&acc)[4][4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) acc[u][w] = 0.f;
+  for (int k = 0; k < c0 + 4; ++k) {
     const float4 l = *reinterpret_cast<const float4*>(&Lt[k][c0]);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -338,36 +422,88 @@ __global__ void __launch_bounds__(256) trsm_panel_kernel(float* A, int ld, int k
       acc[u][3] = fmaf(xv, l.w, acc[u][3]);
     }
   }
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    float4* dst = reinterpret_cast<float4*>(aik + static_cast<size_t>(r0 + u) * ld + c0);
-    *dst = make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
-  }
 }
 
-// Inverse of each 64x64 lower diagonal block of L, in place (upper part zero).
-__global__ void trinv_diag_kernel(float* A, int ld) {
-  __shared__ float L[kNB][kNB + 1];
-  __shared__ float X[kNB][kNB + 1];
-  float* blk = A + static_cast<size_t>(blockIdx.x) * kNB * (ld + 1);
-  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x)
-    L[e / kNB][e % kNB] = blk[static_cast<size_t>(e / kNB) * ld + e % kNB];
-  __syncthreads();
-  if (threadIdx.x < kNB) {
-    const int c = threadIdx.x;
-    for (int r = 0; r < kNB; ++r) {
-      if (r < c) {
-        X[r][c] = 0.f;
-        continue;
-      }
-      float s = (r == c) ? 1.f : 0.f;
-      for (int k = c; k < r; ++k) s -= L[r][k] * X[k][c];
-      X[r][c] = s / L[r][r];
+__global__ void __launch_bounds__(256) panel_next_kernel(float* A, int ld, int kb,
+                                                         const float* Linv,
+                                                         __nv_bfloat16* planes) {
+  extern __shared__ __align__(16) float psm[];
+  auto Lt = reinterpret_cast<float (*)[kNB + 4]>(psm);
+  auto X = reinterpret_cast<float (*)[kNB + 1]>(psm + kNB * (kNB + 4));
+  auto P0 = reinterpret_cast<float (*)[kNB + 1]>(psm + kNB * (kNB + 4) + kNB * (kNB + 1));
+  const int ib = kb + 1 + blockIdx.x;
+  const int tid = threadIdx.x;
+  const int r0 = (tid / 16) * 4, c0 = (tid % 16) * 4;
+  float* a0 = A + static_cast<size_t>(kb + 1) * kNB * ld + static_cast<size_t>(kb) * kNB;
+  float* ai = A + static_cast<size_t>(ib) * kNB * ld + static_cast<size_t>(kb) * kNB;
+  {
+    float lv[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) lv[q] = Linv[tid + 256 * q];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int e = tid + 256 * q;
+      Lt[e % kNB][e / kNB] = lv[q];
     }
   }
+  load_block(a0, ld, X);
   __syncthreads();
-  for (int e = threadIdx.x; e < kNB * kNB; e += blockDim.x)
-    blk[static_cast<size_t>(e / kNB) * ld + e % kNB] = X[e / kNB][e % kNB];
+  float acc[4][4];
+  solve_block(X, Lt, r0, c0, acc);  // P_(kb+1)
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) P0[r0 + u][c0 + w] = acc[u][w];
+  if (ib != kb + 1) {
+    __syncthreads();  // X free
+    load_block(ai, ld, X);
+    __syncthreads();
+    solve_block(X, Lt, r0, c0, acc);  // P_ib
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<float4*>(ai + static_cast<size_t>(r0 + u) * ld + c0) =
+        make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
+  if (planes != nullptr && ib >= kb + 2) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      uint32_t w[kPlanes][2];
+      planes_of(acc[u], w);
+      __nv_bfloat16* o = planes + (static_cast<int64_t>(ib - kb - 2) * kNB + r0 + u) * kPlanes * kNB + c0;
+#pragma unroll
+      for (int pl = 0; pl < kPlanes; ++pl)
+        *reinterpret_cast<uint2*>(o + pl * kNB) = make_uint2(w[pl][0], w[pl][1]);
+    }
+  }
+  __syncthreads();  // Lt free, P0 complete
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) Lt[r0 + u][c0 + w] = acc[u][w];  // P_ib [r][k]
+  __syncthreads();
+  float* cb = ai + kNB;  // A[ib, kb + 1]
+  float cv[4][4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float4 c4 = *reinterpret_cast<const float4*>(cb + static_cast<size_t>(r0 + u) * ld + c0);
+    cv[u][0] = c4.x; cv[u][1] = c4.y; cv[u][2] = c4.z; cv[u][3] = c4.w;
+  }
+  for (int k = 0; k < kNB; ++k) {
+    float pr[4], pc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      pr[u] = Lt[r0 + u][k];
+      pc[u] = P0[c0 + u][k];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) cv[u][w] = fmaf(-pr[u], pc[w], cv[u][w]);
+  }
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<float4*>(cb + static_cast<size_t>(r0 + u) * ld + c0) =
+        make_float4(cv[u][0], cv[u][1], cv[u][2], cv[u][3]);
 }
 
 __global__ void zero_upper_kernel(float* A, int d) {
@@ -376,144 +512,8 @@ __global__ void zero_upper_kernel(float* A, int d) {
   if (t % d > t / d) A[t] = 0.f;
 }
 
-// ------------------------------------------------------------ f32 SIMT GEMM
-// C = alpha op(A) op(B) + beta C for row-major f32 matrices.  lower_only skips
-// tiles wholly above the diagonal; k_from_n starts the K loop at the tile's first
-// column (op(B) lower triangular); k_end_tri stops it after the tile's last row
-// (op(A) lower).  A batch of `batch` products (grid z) steps the three operands
-// by sa, sb, sc elements.
-struct SgemmArgs {
-  int M, N, K;
-  float alpha, beta;
-  const float* A; int lda;
-  const float* B; int ldb;
-  float* C; int ldc;
-  int lower_only, k_from_n, k_end_tri;
-  int batch = 1;
-  int64_t sa = 0, sb = 0, sc = 0;
-};
-
-// 128 x 128 tiles, 256 threads with 8 x 8 outputs each (rows ty*4 + {0..3} and
-// 64 + ty*4 + {0..3}, likewise the columns, so a warp's shared-memory reads are
-// contiguous); K in steps of 8, the next step's tiles loaded into registers while
-// the current one is multiplied (two shared-memory buffers, one barrier a step).
-// op(A) = A (row-major [M, lda]); op(B) = B^T ([N, ldb]) if TB, else B ([K, ldb]).
-// M, N and K are multiples of 8; every pointer and leading dimension keeps rows
-// 16-byte aligned.
-constexpr int kSgT = 128, kSgK = 8;
-
-template <bool TB>
-__global__ void __launch_bounds__(256) sgemm_kernel(const SgemmArgs g) {
-  __shared__ __align__(16) float As[2][kSgK][kSgT + 4];
-  __shared__ __align__(16) float Bs[2][kSgK][kSgT + 4];
-  const int m0 = blockIdx.y * kSgT, n0 = blockIdx.x * kSgT;
-  if (g.lower_only && n0 > m0 + kSgT - 1) return;
-  const float* __restrict__ Ag = g.A + blockIdx.z * g.sa;
-  const float* __restrict__ Bg = g.B + blockIdx.z * g.sb;
-  float* Cg = g.C + blockIdx.z * g.sc;
-  const int tid = threadIdx.x;
-  const int tx = tid % 16, ty = tid / 16;
-  int kbeg = 0, kend = g.K;
-  if (g.k_from_n) kbeg = n0;
-  if (g.k_end_tri) kend = min(g.K, m0 + kSgT);
-  // loader roles: A (and B^T) tile rows tid / 2, four K at (tid % 2) * 4; B tile row
-  // tid / 32 of K, four columns at (tid % 32) * 4
-  const int ar = tid / 2, ak = (tid % 2) * 4;
-  const int bk = tid / 32, bc = (tid % 32) * 4;
-  auto load = [&](int k0, float4& av, float4& bv) {
-    av = make_float4(0.f, 0.f, 0.f, 0.f);
-    bv = av;
-    if (m0 + ar < g.M)
-      av = *reinterpret_cast<const float4*>(Ag + static_cast<size_t>(m0 + ar) * g.lda + k0 + ak);
-    if (TB) {
-      if (n0 + ar < g.N)
-        bv = *reinterpret_cast<const float4*>(Bg + static_cast<size_t>(n0 + ar) * g.ldb + k0 + ak);
-    } else if (n0 + bc < g.N) {
-      bv = *reinterpret_cast<const float4*>(Bg + static_cast<size_t>(k0 + bk) * g.ldb + n0 + bc);
-    }
-  };
-  auto store = [&](int buf, const float4& av, const float4& bv) {
-    As[buf][ak + 0][ar] = av.x;
-    As[buf][ak + 1][ar] = av.y;
-    As[buf][ak + 2][ar] = av.z;
-    As[buf][ak + 3][ar] = av.w;
-    if (TB) {
-      Bs[buf][ak + 0][ar] = bv.x;
-      Bs[buf][ak + 1][ar] = bv.y;
-      Bs[buf][ak + 2][ar] = bv.z;
-      Bs[buf][ak + 3][ar] = bv.w;
-    } else {
-      *reinterpret_cast<float4*>(&Bs[buf][bk][bc]) = bv;
-    }
-  };
-  float acc[8][8] = {};
-  if (kbeg < kend) {
-    float4 av, bv;
-    load(kbeg, av, bv);
-    store(0, av, bv);
-    __syncthreads();
-    int buf = 0;
-    for (int k0 = kbeg; k0 < kend; k0 += kSgK) {
-      const bool more = k0 + kSgK < kend;
-      if (more) load(k0 + kSgK, av, bv);
-#pragma unroll
-      for (int kk = 0; kk < kSgK; ++kk) {
-        float a[8], b[8];
-        *reinterpret_cast<float4*>(&a[0]) = *reinterpret_cast<const float4*>(&As[buf][kk][ty * 4]);
-        *reinterpret_cast<float4*>(&a[4]) = *reinterpret_cast<const float4*>(&As[buf][kk][64 + ty * 4]);
-        *reinterpret_cast<float4*>(&b[0]) = *reinterpret_cast<const float4*>(&Bs[buf][kk][tx * 4]);
-        *reinterpret_cast<float4*>(&b[4]) = *reinterpret_cast<const float4*>(&Bs[buf][kk][64 + tx * 4]);
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
-      }
-      if (more) store(buf ^ 1, av, bv);
-      __syncthreads();
-      buf ^= 1;
-    }
-  }
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int m = m0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
-    if (m >= g.M) continue;
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int n = n0 + h * 64 + tx * 4;
-      if (n >= g.N) continue;
-      float4* c = reinterpret_cast<float4*>(Cg + static_cast<size_t>(m) * g.ldc + n);
-      float4 o = make_float4(g.alpha * acc[i][4 * h], g.alpha * acc[i][4 * h + 1],
-                             g.alpha * acc[i][4 * h + 2], g.alpha * acc[i][4 * h + 3]);
-      if (g.beta != 0.f) {
-        const float4 cv = *c;
-        o.x = fmaf(g.beta, cv.x, o.x);
-        o.y = fmaf(g.beta, cv.y, o.y);
-        o.z = fmaf(g.beta, cv.z, o.z);
-        o.w = fmaf(g.beta, cv.w, o.w);
-      }
-      *c = o;
-    }
-  }
-}
-
-cudaError_t sgemm(bool tb, const SgemmArgs& g, cudaStream_t s) {
-  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
-  dim3 grid((g.N + kSgT - 1) / kSgT, (g.M + kSgT - 1) / kSgT, g.batch);
-  if (tb) sgemm_kernel<true><<<grid, 256, 0, s>>>(g);
-  else sgemm_kernel<false><<<grid, 256, 0, s>>>(g);
-  return cudaGetLastError();
-}
-
 // ------------------------------------------------------------ split operands
-__device__ __forceinline__ void split_bf16(float v, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-  hi = __float2bfloat16_rn(v);
-  lo = __float2bfloat16_rn(v - __bfloat162float(hi));
-}
 
-__device__ __forceinline__ uint32_t bf16x2(__nv_bfloat16 a, __nv_bfloat16 b) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(a)) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(b)) << 16);
-}
 
 // B' [d, 3d] = [hi(G^-1) | lo(G^-1) | hi(G^-1)] from the f64 inverse: hi = bf16(v_hi) and
 // lo = bf16((v_hi - hi) + v_lo) of the double-float (v_hi, v_lo), the first difference
@@ -727,6 +727,49 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   return RF_OK;
 }
 
+// out_b = alpha A_b B_b^T (+ out_b when beta_one) on the tensor cores for b < batches, from
+// the seven-plane splits of A_b [M, K] (Ap7) and B_b [N, K] (Bp7), each batch entry's rows
+// following the previous entry's: planes 0-5 of A against planes 1-6 of B, K' = 6 K.
+// out_b = out + b * out_bstride, rows out_ld apart; lower: one square product (M = N), only
+// the pair tiles on and below the diagonal (the upper part of a diagonal tile is written
+// too).  `lim` elements of out are in bounds (checked by debug builds).
+rf_status launch_f32_product(const __nv_bfloat16* Ap7, const __nv_bfloat16* Bp7, int M, int N,
+                             int K, int batches, float* out, int64_t out_ld, int64_t out_bstride,
+                             float alpha, bool beta_one, bool lower, int64_t lim, cudaStream_t s) {
+  if (M <= 0 || N <= 0 || batches <= 0) return RF_OK;
+  GemmParams p{};
+  p.mode = kModeF32;
+  p.k_blocks = 6 * K / kBK;
+  const uint64_t row = static_cast<uint64_t>(kPlanes) * K * 2;
+  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap7, 6 * K, M, batches, row,
+                         row * M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp7 + K, 6 * K, N, batches,
+                          row, row * N, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for an f32 product");
+  p.m_tiles = static_cast<int32_t>(ceil_div(M, kBM));
+  p.bn = 256;
+  p.n_tiles = static_cast<int32_t>(ceil_div(N, 256));
+  p.batches = lower ? 1 : batches;
+  p.group_m = 16;
+  p.rows = M;
+  p.cols = N;
+  p.out_f32 = out;
+  p.out_ld = static_cast<int32_t>(out_ld);
+  p.out_bstride = out_bstride;
+  p.alpha = alpha;
+  p.beta_one = beta_one ? 1 : 0;
+  p.lower = lower ? 1 : 0;
+  p.lim_b = lim;
+  p.err = device_error_word();
+  if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
+  const int64_t u = (p.m_tiles + 1) / 2;
+  const int64_t tiles = lower ? u * (u + 1) / 2 : u * p.n_tiles * p.batches;
+  const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  const cudaError_t e = launch_gemm2(p, pairs, s);
+  if (e != cudaSuccess) return cuda_fail(e, "f32 product launch");
+  return RF_OK;
+}
+
 rf_status accumulate(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream_t s) {
   const int64_t rows = a->rows;
   if (rows == 0) return RF_OK;
@@ -789,52 +832,57 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   if (e != cudaSuccess) return cuda_fail(e, "fit preparation launch");
 
   // blocked Cholesky, lower factor in place, with a look-ahead of one block column:
-  // after the panel of step kb, block column kb+1 is updated on `s` and the rest of
-  // the trailing matrix on the side stream, so the next diagonal factor and panel run
-  // beside the large update.  The two parts write disjoint blocks and every element
-  // takes the same sum as one whole update; the skipped blocks above the diagonal are
-  // never read.
+  // after the diagonal factor of step kb, one launch solves the panel and updates block
+  // column kb+1 on `s`, and the rest of the trailing matrix is updated on the side stream,
+  // so the next diagonal factor runs beside the large update.  The two updates write
+  // disjoint blocks and every element takes the same sum as one whole update; the skipped
+  // blocks above the diagonal are never read.  The diagonal blocks receive L_kk^-1 (the
+  // first step of the inverse below); the panels read the factor's copy in `linv`.
   const int nb = d / kNB;
   float* linv = reinterpret_cast<float*>(ws + pl.off_linv);
+  // seven-plane splits of the trailing updates' panels and of the inverse's operands, in the
+  // area of the f64 inverse (8 d^2 bytes, free until the G^-1 product)
+  __nv_bfloat16* cplanes = reinterpret_cast<__nv_bfloat16*>(Gi);
   HostStreamer* hs = host_streamer();
   if (hs == nullptr) return RF_ERR_CUDA;
+  if ((e = cudaFuncSetAttribute(panel_next_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                kPanelSmem)) != cudaSuccess)
+    return cuda_fail(e, "Cholesky panel attributes");
   {
     // one caller at a time on the device's side stream and its events
     std::lock_guard<std::mutex> lk(host_stream_mutex());
     for (int kb = 0; kb < nb; ++kb) {
       potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb, err, linv);
       if (kb + 1 == nb) break;
-      trsm_panel_kernel<<<nb - kb - 1, 256, 0, s>>>(Gh, d, kb, linv);
       // block column kb+1 was last written by step kb-1's trailing update
       if (kb > 0 && (e = cudaStreamWaitEvent(s, hs->side_done, 0)) != cudaSuccess)
         return cuda_fail(e, "Cholesky look-ahead");
+      panel_next_kernel<<<nb - kb - 1, 256, kPanelSmem, s>>>(Gh, d, kb, linv, cplanes);
       if ((e = cudaEventRecord(hs->side_start, s)) == cudaSuccess)
         e = cudaStreamWaitEvent(hs->side, hs->side_start, 0);
       if (e != cudaSuccess) return cuda_fail(e, "Cholesky look-ahead");
       const int rem = d - (kb + 1) * kNB;
-      const float* panel = Gh + static_cast<size_t>(kb + 1) * kNB * d + static_cast<size_t>(kb) * kNB;
-      float* trail = Gh + static_cast<size_t>(kb + 1) * kNB * d + static_cast<size_t>(kb + 1) * kNB;
       if (rem > kNB) {
-        const size_t skip = static_cast<size_t>(kNB) * d;
-        SgemmArgs g{rem - kNB, rem - kNB, kNB, -1.f, 1.f, panel + skip, d, panel + skip, d,
-                    trail + skip + kNB, d, 1, 0, 0};
-        if ((e = sgemm(true, g, hs->side)) != cudaSuccess) return cuda_fail(e, "Cholesky update");
+        const int64_t off = static_cast<int64_t>(kb + 2) * kNB * (d + 1);
+        rf_status st = launch_f32_product(cplanes, cplanes, rem - kNB, rem - kNB, kNB, 1, Gh + off, d,
+                                          0, -1.f, true, true, dd - off, hs->side);
+        if (st != RF_OK) return st;
       }
       if ((e = cudaEventRecord(hs->side_done, hs->side)) != cudaSuccess)
         return cuda_fail(e, "Cholesky look-ahead");
-      SgemmArgs g{rem, kNB, kNB, -1.f, 1.f, panel, d, panel, d, trail, d, 0, 0, 0};
-      if ((e = sgemm(true, g, s)) != cudaSuccess) return cuda_fail(e, "Cholesky update");
     }
     if (nb > 1 && (e = cudaStreamWaitEvent(s, hs->side_done, 0)) != cudaSuccess)
       return cuda_fail(e, "Cholesky look-ahead");
   }
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "Cholesky launch");
   zero_upper_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gh, d);
-  // X = L^-1 in place: the 64 x 64 diagonal blocks, then recursive doubling:
-  // blocks [s1 | s2] of size s (already inverted) merge as
-  //   X_21 = -X_22 (L_21 X_11),
-  // every pair of a level in one batched product (the scratch T is the area of the
-  // bf16 planes, free until the split below)
-  trinv_diag_kernel<<<nb, 256, 0, s>>>(Gh, d);
+  // X = L^-1 in place: the 64 x 64 diagonal blocks are inverted already; recursive
+  // doubling: blocks [s1 | s2] of size s (already inverted) merge as
+  //   T = L_21 X_11,  X_21 = -X_22 T,
+  // every pair of a level in one batched f32 product on the tensor cores (the blocks above
+  // the diagonal are zero, so the triangular operands are used whole).  T lives in the
+  // area of the bf16 planes of X (free until the split below), the operands' seven-plane
+  // splits in `cplanes`.
   float* T = reinterpret_cast<float*>(Xs);
   for (int sz = kNB; sz < d; sz *= 2) {
     const int full = d / (2 * sz);        // pairs with both halves of size sz
@@ -849,12 +897,24 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
       const float* x11 = Gh + static_cast<size_t>(b0) * d + b0;
       const float* x22 = Gh + static_cast<size_t>(b0 + sz) * d + b0 + sz;
       float* x21 = Gh + static_cast<size_t>(b0 + sz) * d + b0;
-      SgemmArgs g1{s2, sz, sz, 1.f, 0.f, l21, d, x11, d, T, sz, 0, 1, 0};   // T = L_21 X_11
-      g1.batch = cnt; g1.sa = step; g1.sb = step; g1.sc = static_cast<int64_t>(sz) * sz;
-      if ((e = sgemm(false, g1, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
-      SgemmArgs g2{s2, sz, s2, -1.f, 0.f, x22, d, T, sz, x21, d, 0, 0, 1};  // X_21 = -X_22 T
-      g2.batch = cnt; g2.sa = step; g2.sb = static_cast<int64_t>(sz) * sz; g2.sc = step;
-      if ((e = sgemm(false, g2, s)) != cudaSuccess) return cuda_fail(e, "triangular inverse");
+      const int64_t tb = static_cast<int64_t>(s2) * sz;  // T entries per pair
+      __nv_bfloat16* pa = cplanes;
+      __nv_bfloat16* pb = cplanes + cnt * static_cast<int64_t>(s2) * kPlanes * sz;
+      // T = L_21 X_11: A rows are the rows of L_21, B rows the columns of X_11
+      split7_kernel<false><<<dim3(sz / 64, ceil_div(s2, 64), cnt), 256, 0, s>>>(l21, d, step, s2, sz, pa);
+      split7_kernel<true><<<dim3(sz / 64, sz / 64, cnt), 256, 0, s>>>(x11, d, step, sz, sz, pb);
+      if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "triangular inverse split");
+      rf_status st = launch_f32_product(pa, pb, s2, sz, sz, cnt, T, sz, tb, 1.f, false, false,
+                                        cnt * tb, s);
+      if (st != RF_OK) return st;
+      // X_21 = -X_22 T: A rows are the rows of X_22, B rows the columns of T
+      pb = cplanes + cnt * static_cast<int64_t>(s2) * kPlanes * s2;
+      split7_kernel<false><<<dim3(s2 / 64, ceil_div(s2, 64), cnt), 256, 0, s>>>(x22, d, step, s2, s2, pa);
+      split7_kernel<true><<<dim3(s2 / 64, sz / 64, cnt), 256, 0, s>>>(T, sz, tb, sz, s2, pb);
+      if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "triangular inverse split");
+      st = launch_f32_product(pa, pb, s2, sz, s2, cnt, x21, d, step, -1.f, false, false,
+                              dd - (static_cast<int64_t>(b0 + sz) * d + b0), s);
+      if (st != RF_OK) return st;
     }
   }
   // G^-1 = X^T X on the tensor cores: one MN-major Gram product over the stacked bf16

@@ -38,6 +38,7 @@ enum GemmMode : int {
   kModeGdnProj = 2,  // GDN projections: RMS scale, k L2-norm, v, sigmoid gates
   kModeGram = 3,     // fit sums: [X | Y_1 .. Y_L]^T X over rows, MN-major operands, f64 add
   kModeSolve = 4,    // fit solve: A = C~^T G^-1 (split bf16), column scale, f32/bf16 out
+  kModeF32 = 5,      // plain product, f32 out: alpha acc (+ the stored value), batched or lower tiles
 };
 
 // Device error word sites (which wait ran out).
@@ -150,11 +151,20 @@ struct GemmParams {
   __nv_bfloat16* out_bf16;  // [M, N] or null
   float* bias_part;         // [M, n_tiles]
   int32_t out_ld;
+  // plain f32 epilogue: out_f32[b * out_bstride + row * out_ld + col] = alpha acc (plus the
+  // stored value when beta_one) for rows < rows and cols < cols; with lower set the tiles
+  // are the pair tiles on and below the diagonal of a square product (bn = 2 kBM, one batch)
+  int64_t out_bstride;
+  float alpha;
+  int32_t beta_one;
+  int32_t lower;
+  int32_t cols;
   int* err;
   int* tile_ctr;  // this launch's tile counter (zeroed before the launch): tiles are taken in order
   // elements of the buffers the epilogue writes with plain stores (checked by debug
   // builds): map mode ss_part, map_out; K/V mode with a row list the caches (per tensor);
-  // GDN mode gdn_gate; Gram mode gram_G, gram_C; solve mode the outputs, bias_part
+  // GDN mode gdn_gate; Gram mode gram_G, gram_C; solve mode the outputs, bias_part; f32
+  // mode out_f32 (lim_b)
   int64_t lim_a, lim_b;
   float inv_freq_hi[64];
   float inv_freq_lo[64];
