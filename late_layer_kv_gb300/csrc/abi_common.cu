@@ -199,11 +199,6 @@ HostStreamer* host_streamer() {
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.h_done, cudaEventDisableTiming);
     for (int i = 0; i < 2 && e == cudaSuccess; ++i)
       e = cudaEventCreateWithFlags(&h.staged[i], cudaEventDisableTiming);
-    int lo = 0, hi = 0;
-    if (e == cudaSuccess) e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
-    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&h.prio, cudaStreamNonBlocking, hi);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.prio_start, cudaEventDisableTiming);
-    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.prio_done, cudaEventDisableTiming);
     if (e != cudaSuccess) {
       cuda_fail(e, "creating the map-copy stream");
       h.copy = nullptr;

@@ -63,7 +63,7 @@ constexpr int kMapSlots = 3;
 // Per-device side stream and events for streaming maps from host memory.
 struct HostStreamer {
   cudaStream_t copy = nullptr;
-  cudaStream_t side = nullptr;       // small kernels beside a persistent GEMM (fit column sums)
+  cudaStream_t side = nullptr;       // work beside a persistent GEMM (fit column sums, GDN projections)
   cudaEvent_t side_start = nullptr;
   cudaEvent_t side_done = nullptr;
   cudaEvent_t copied[kMapSlots] = {};
@@ -72,9 +72,6 @@ struct HostStreamer {
   cudaEvent_t h_done = nullptr;  // split state copied from host memory
   uint32_t h_gen = 0;            // value that marks this call's row groups ready
   cudaEvent_t staged[2] = {};    // host map source: copy out of staging half j done
-  cudaStream_t prio = nullptr;   // highest priority: GDN state of the first layers (see gdn.cu)
-  cudaEvent_t prio_start = nullptr;
-  cudaEvent_t prio_done = nullptr;
 };
 
 // Stream write of a 32-bit value by the GPU's front end, no SM involved: marks a

@@ -1049,16 +1049,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
   }
 }
 
-cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream) {
+cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream, int* ctr) {
   // set on every launch: the attribute belongs to the current device, and the call is
   // cheap next to the kernel
   cudaError_t e = cudaFuncSetAttribute(rf_gemm2_kernel<false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmem);
   if (e != cudaSuccess) return e;
   GemmParams q = p;
-  q.tile_ctr = tile_counter_slot();
-  if (q.tile_ctr == nullptr) return cudaErrorInvalidSymbol;
-  if ((e = cudaMemsetAsync(q.tile_ctr, 0, sizeof(int), stream)) != cudaSuccess) return e;
+  if (ctr != nullptr) {
+    q.tile_ctr = ctr;
+  } else {
+    q.tile_ctr = tile_counter_slot();
+    if (q.tile_ctr == nullptr) return cudaErrorInvalidSymbol;
+    if ((e = cudaMemsetAsync(q.tile_ctr, 0, sizeof(int), stream)) != cudaSuccess) return e;
+  }
   rf_gemm2_kernel<false><<<2 * pairs, kGemmThreads, kGemmSmem, stream>>>(q);
   return cudaGetLastError();
 }

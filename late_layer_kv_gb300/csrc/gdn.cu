@@ -925,7 +925,8 @@ void plan_gdn(const rf_gdn_args* a, GdnPlan* pl) {
 // The projection GEMM of layers [l0, l0 + nl) of the chunk (all of them by default).
 rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, const void* xhat,
                           const float* ss, __nv_bfloat16* kb, __nv_bfloat16* vb, float* gb,
-                          cudaStream_t s, int l0 = 0, int nl = -1) {
+                          cudaStream_t s, int l0 = 0, int nl = -1, int max_pairs = 0,
+                          int* ctr = nullptr) {
   GemmParams p{};
   p.mode = kModeGdnProj;
   p.k_blocks = a->d_out / kBK;
@@ -977,9 +978,10 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
   const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles * p.batches;
-  const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
   if (pairs <= 0) return RF_OK;
-  cudaError_t e = launch_gemm2(p, pairs, s);
+  cudaError_t e = launch_gemm2(p, pairs, s, ctr);
   if (e != cudaSuccess) return cuda_fail(e, "GDN projection GEMM launch");
   return RF_OK;
 }
@@ -1084,11 +1086,12 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
   }
 
   // With all rows in one chunk and more (layer, head) states than SMs, the states of the
-  // first `la` layers run on a high-priority side stream as soon as their projections are
-  // done, beside the projection GEMM of the other layers, whose persistent CTAs take the
-  // SMs the state kernel leaves and join as its CTAs finish (tiles come from a counter).
-  // The last `L - la` layers' states then fill one wave of the SMs.  Without the split the
-  // states of all layers run in two waves, the second one on part of the GPU.
+  // first `la` layers run as soon as their projections are done, beside the projection GEMM
+  // of the other layers: a first launch of it on the side stream holds only the SMs the
+  // states leave, and a second one after the states, on the same tile counter, takes over
+  // the freed SMs and shares the remaining tiles with it.  The last `L - la` layers' states
+  // then fill one wave of the SMs.  Without the split the states of all layers run in two
+  // waves, the second one on part of the GPU.
   int la = 0;
   {
     const int per_wave = sm_count() / a->n_heads;  // layers whose states fill one wave
@@ -1204,20 +1207,33 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     sp.first = start == 0 ? 1 : 0;
     if (!state_maps(rc)) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the GDN state");
     if (la > 0) {
-      // the first layers' projections, their states on the side stream, then the others'
-      // projections beside them
+      // the first layers' projections; then their states on `s`, beside the others'
+      // projections on the side stream limited to the SMs the states leave (whichever is
+      // dispatched first, neither can take the other's SMs); then the others' projections
+      // on every SM, sharing the side launch's tile counter
       if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s, 0, la)) != RF_OK) return st;
-      cudaError_t e = cudaEventRecord(hs->prio_start, s);
-      if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->prio, hs->prio_start, 0);
-      if (e != cudaSuccess) return cuda_fail(e, "ordering the first layers' states");
+      int* ctr = tile_counter_slot();
+      if (ctr == nullptr) return fail(RF_ERR_CUDA, "tile counter unavailable");
+      cudaError_t e = cudaMemsetAsync(ctr, 0, sizeof(int), s);
+      if (e == cudaSuccess) e = cudaEventRecord(hs->side_start, s);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->side, hs->side_start, 0);
+      if (e != cudaSuccess) return cuda_fail(e, "ordering the other layers' projections");
+      const int free_pairs = (sm_count() - la * a->n_heads) / 2;
+      if (free_pairs > 0 &&
+          (st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, hs->side, la, a->n_layers - la,
+                                free_pairs, ctr)) != RF_OK)
+        return st;
+      if ((e = cudaEventRecord(hs->side_done, hs->side)) != cudaSuccess)
+        return cuda_fail(e, "recording the other layers' projections");
       GdnStateParams spa = sp;
       spa.layers = la;
       spa.layer_base = 0;
-      if ((e = launch_gdn_state(spa, hs->prio)) != cudaSuccess) return cuda_fail(e, "GDN state launch");
-      if ((e = cudaEventRecord(hs->prio_done, hs->prio)) != cudaSuccess)
-        return cuda_fail(e, "recording the first layers' states");
-      if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s, la, a->n_layers - la)) != RF_OK)
+      if ((e = launch_gdn_state(spa, s)) != cudaSuccess) return cuda_fail(e, "GDN state launch");
+      if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s, la, a->n_layers - la, 0,
+                                ctr)) != RF_OK)
         return st;
+      if ((e = cudaStreamWaitEvent(s, hs->side_done, 0)) != cudaSuccess)
+        return cuda_fail(e, "ordering after the other layers' projections");
     } else if ((st = launch_gdn_proj(a, pl, rc, xhat, ss, kb, vb, gb, s)) != RF_OK) {
       return st;
     }
@@ -1233,8 +1249,6 @@ extern "C" rf_status ridgefill_fill_gdn(const rf_gdn_args* a, void* workspace, s
     spb.layer_base = la;
     cudaError_t e = launch_gdn_state(spb, s);
     if (e != cudaSuccess) return cuda_fail(e, "GDN state launch");
-    if (la > 0 && (e = cudaStreamWaitEvent(s, hs->prio_done, 0)) != cudaSuccess)
-      return cuda_fail(e, "ordering after the first layers' states");
     if ((st = mark(start, 3)) != RF_OK) return st;
   }
   if (a->h_on_host) {  // later work on `s` (and the caller's reuse of H) follows the copy

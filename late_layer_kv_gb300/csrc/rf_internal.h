@@ -175,8 +175,10 @@ struct GemmParams {
 int* tile_counter_slot();
 
 // every mode on CTA pairs (B tensor maps with boxes of half a tile's columns); `pairs`
-// clusters of 2
-cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream);
+// clusters of 2.  With `ctr` set, the launch takes its tiles from that counter (zeroed by
+// the caller before the first of the launches that share it) instead of a fresh one: two
+// launches of the same tiles on one counter split the tiles between them.
+cudaError_t launch_gemm2(const GemmParams& p, int pairs, cudaStream_t stream, int* ctr = nullptr);
 // map mode on CTA pairs with int8 maps (p.q8, p.q8_scale); tmB unused
 cudaError_t launch_gemm2_q8(const GemmParams& p, int pairs, cudaStream_t stream);
 
