@@ -195,6 +195,8 @@ HostStreamer* host_streamer() {
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.side, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.side_start, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.side_done, cudaEventDisableTiming);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i)
+      e = cudaEventCreateWithFlags(&h.side_ev[i], cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.h_done, cudaEventDisableTiming);
     for (int i = 0; i < 2 && e == cudaSuccess; ++i)

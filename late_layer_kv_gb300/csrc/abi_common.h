@@ -66,6 +66,7 @@ struct HostStreamer {
   cudaStream_t side = nullptr;       // work beside a persistent GEMM (fit column sums, GDN projections)
   cudaEvent_t side_start = nullptr;
   cudaEvent_t side_done = nullptr;
+  cudaEvent_t side_ev[2] = {};     // side-stream steps taken in turn (Cholesky trailing updates)
   cudaEvent_t copied[kMapSlots] = {};
   cudaEvent_t freed[kMapSlots] = {};
   cudaEvent_t start = nullptr;

@@ -307,12 +307,24 @@ __global__ void __launch_bounds__(256) split7_kernel(const float* __restrict__ s
 // the (never read) upper triangle of a takes stray updates.  One barrier a step.  The
 // inverse L_kk^-1 (zeros above) goes to Linv [64, 64] and over the diagonal block: later
 // steps read only the blocks below it, and the triangular inverse starts from it.
+// It first copies the n_pst panel blocks of the previous step held back in `pst` (rows kb
+// and kb + 1 of block column kb - 1) into place.
 __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int kb, int* err,
-                                                         float* Linv) {
+                                                         float* Linv, const float* pst,
+                                                         int n_pst) {
   __shared__ float col[2][kNB];   // l_ij for i > j, else 0
   __shared__ float xrow[2][kNB];  // x_jc for c <= j, else 0
   float* blk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
   const int tid = threadIdx.x, ti = tid & 15, tk = tid >> 4;
+  for (int b = 0; b < n_pst; ++b) {
+    float* dst = A + static_cast<size_t>(kb + b) * kNB * ld + static_cast<size_t>(kb - 1) * kNB;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = 4 * (tid + 256 * q);  // four consecutive floats of one row
+      *reinterpret_cast<float4*>(dst + static_cast<size_t>(e / kNB) * ld + e % kNB) =
+          *reinterpret_cast<const float4*>(pst + b * kNB * kNB + e);
+    }
+  }
   float a[4][4], x[4][4];
 #pragma unroll
   for (int u = 0; u < 4; ++u)
@@ -379,16 +391,20 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int k
     }
 }
 
-// Panel and next block column of Cholesky step kb, one 64-row block ib = kb + 1 + blockIdx.x
-// per CTA (256 threads, 4 x 4 outputs each):
-//   P_ib = A[ib, kb] L_kk^-T = A[ib, kb] Linv^T     (the block of L, written back)
-//   A[ib, kb + 1] -= P_ib P_(kb+1)^T                 (the next column's share of the update)
-// Every CTA forms P_(kb+1) itself (one more 64 x 64 product) rather than waiting for the CTA
-// that owns it.  With `planes` set, the blocks ib >= kb + 2 also go there as seven-plane
-// splits, row (ib - kb - 2) * 64 + r, for the trailing update on the tensor cores.  Dynamic
-// shared memory: Lt = Linv^T [64][68] (later P_ib), X [64][65] (the block being solved) and
-// P0 = P_(kb+1) [64][65].
-constexpr int kPanelSmem = (kNB * (kNB + 4) + 2 * kNB * (kNB + 1)) * 4;
+// Panel of Cholesky step kb and its two look-ahead block columns, one 64-row block
+// ib = kb + 1 + blockIdx.x per CTA (256 threads, 4 x 4 outputs each):
+//   P_ib = A[ib, kb] L_kk^-T = A[ib, kb] Linv^T          (the block of L, written back)
+//   A[ib, kb + 1] -= P_ib P_(kb+1)^T                      (step kb)
+//   A[ib, kb + 2] -= L[ib, kb-1] L[kb+2, kb-1]^T + P_ib P_(kb+2)^T   (steps kb - 1, kb)
+// Every CTA forms P_(kb+1) and P_(kb+2) itself rather than waiting for the CTAs that own
+// them.  Column kb + 2 takes step kb - 1 here (not in the trailing update of step kb - 1),
+// so the trailing update of step kb covers the columns from kb + 4 on and the panel of step
+// kb needs only the trailing update of step kb - 2: one step of the factorisation runs
+// between the two.  With `planes` set, the blocks ib >= kb + 4 also go there as seven-plane
+// splits, row (ib - kb - 4) * 64 + r, for that trailing update on the tensor cores.
+// Dynamic shared memory: Lt = Linv^T [64][68], then X (the block being solved, later
+// L[ib, kb-1]), P1 = P_(kb+1), P2 = P_(kb+2), Pi = P_ib and Q = L[kb+2, kb-1], [64][65] each.
+constexpr int kPanelSmem = (kNB * (kNB + 4) + 5 * kNB * (kNB + 1)) * 4;
 
 __device__ __forceinline__ void load_block(const float* src, int ld, float (*dst)[kNB + 1]) {
   float v[16];  // all loads in flight before the shared-memory stores
@@ -424,18 +440,63 @@ __device__ __forceinline__ void solve_block(const float (*X)[kNB + 1], const flo
   }
 }
 
-__global__ void __launch_bounds__(256) panel_next_kernel(float* A, int ld, int kb,
-                                                         const float* Linv,
-                                                         __nv_bfloat16* planes) {
+__device__ __forceinline__ void store_tile(float (*dst)[kNB + 1], int r0, int c0,
+                                           const float (&acc)[4][4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int w = 0; w < 4; ++w) dst[r0 + u][c0 + w] = acc[u][w];
+}
+
+// cv -= Lf Rf^T for this thread's rows r0 + u (rows of Lf) and columns c0 + w (rows of Rf)
+__device__ __forceinline__ void sub_product(const float (*Lf)[kNB + 1], const float (*Rf)[kNB + 1],
+                                            int r0, int c0, float (&cv)[4][4]) {
+  for (int k = 0; k < kNB; ++k) {
+    float pr[4], pc[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      pr[u] = Lf[r0 + u][k];
+      pc[u] = Rf[c0 + u][k];
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int w = 0; w < 4; ++w) cv[u][w] = fmaf(-pr[u], pc[w], cv[u][w]);
+  }
+}
+
+__device__ __forceinline__ void load_tile(const float* blk, int ld, int r0, int c0, float (&cv)[4][4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const float4 c4 = *reinterpret_cast<const float4*>(blk + static_cast<size_t>(r0 + u) * ld + c0);
+    cv[u][0] = c4.x; cv[u][1] = c4.y; cv[u][2] = c4.z; cv[u][3] = c4.w;
+  }
+}
+
+__device__ __forceinline__ void put_tile(float* blk, int ld, int r0, int c0, const float (&cv)[4][4]) {
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+    *reinterpret_cast<float4*>(blk + static_cast<size_t>(r0 + u) * ld + c0) =
+        make_float4(cv[u][0], cv[u][1], cv[u][2], cv[u][3]);
+}
+
+__global__ void __launch_bounds__(256) panel_ahead_kernel(float* A, int ld, int kb,
+                                                          const float* Linv, float* pst,
+                                                          __nv_bfloat16* planes) {
   extern __shared__ __align__(16) float psm[];
+  typedef float Tile[kNB + 1];
   auto Lt = reinterpret_cast<float (*)[kNB + 4]>(psm);
-  auto X = reinterpret_cast<float (*)[kNB + 1]>(psm + kNB * (kNB + 4));
-  auto P0 = reinterpret_cast<float (*)[kNB + 1]>(psm + kNB * (kNB + 4) + kNB * (kNB + 1));
+  Tile* X = reinterpret_cast<Tile*>(psm + kNB * (kNB + 4));
+  Tile* P1 = X + kNB;
+  Tile* P2 = P1 + kNB;
+  Tile* Pi = P2 + kNB;
+  Tile* Q = Pi + kNB;
   const int ib = kb + 1 + blockIdx.x;
   const int tid = threadIdx.x;
   const int r0 = (tid / 16) * 4, c0 = (tid % 16) * 4;
-  float* a0 = A + static_cast<size_t>(kb + 1) * kNB * ld + static_cast<size_t>(kb) * kNB;
-  float* ai = A + static_cast<size_t>(ib) * kNB * ld + static_cast<size_t>(kb) * kNB;
+  auto blk = [&](int bi, int bj) {
+    return A + static_cast<size_t>(bi) * kNB * ld + static_cast<size_t>(bj) * kNB;
+  };
   {
     float lv[16];
 #pragma unroll
@@ -446,64 +507,61 @@ __global__ void __launch_bounds__(256) panel_next_kernel(float* A, int ld, int k
       Lt[e % kNB][e / kNB] = lv[q];
     }
   }
-  load_block(a0, ld, X);
+  load_block(blk(kb + 1, kb), ld, X);
   __syncthreads();
   float acc[4][4];
   solve_block(X, Lt, r0, c0, acc);  // P_(kb+1)
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-#pragma unroll
-    for (int w = 0; w < 4; ++w) P0[r0 + u][c0 + w] = acc[u][w];
-  if (ib != kb + 1) {
+  store_tile(P1, r0, c0, acc);
+  if (ib >= kb + 2) {
     __syncthreads();  // X free
-    load_block(ai, ld, X);
+    load_block(blk(kb + 2, kb), ld, X);
     __syncthreads();
-    solve_block(X, Lt, r0, c0, acc);  // P_ib
+    solve_block(X, Lt, r0, c0, acc);  // P_(kb+2)
+    store_tile(P2, r0, c0, acc);
+    if (ib >= kb + 3) {
+      __syncthreads();
+      load_block(blk(ib, kb), ld, X);
+      __syncthreads();
+      solve_block(X, Lt, r0, c0, acc);  // P_ib
+      store_tile(Pi, r0, c0, acc);
+    }
   }
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-    *reinterpret_cast<float4*>(ai + static_cast<size_t>(r0 + u) * ld + c0) =
-        make_float4(acc[u][0], acc[u][1], acc[u][2], acc[u][3]);
-  if (planes != nullptr && ib >= kb + 2) {
+  const Tile* own = ib == kb + 1 ? P1 : (ib == kb + 2 ? P2 : Pi);
+  // the blocks of rows kb + 1 and kb + 2 are still to be read (unsolved) by the other CTAs:
+  // they go to `pst`, and the next diagonal-factor launch copies them into place
+  if (ib <= kb + 2) put_tile(pst + (ib - kb - 1) * kNB * kNB, kNB, r0, c0, acc);
+  else put_tile(blk(ib, kb), ld, r0, c0, acc);
+  if (planes != nullptr && ib >= kb + 4) {
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       uint32_t w[kPlanes][2];
       planes_of(acc[u], w);
-      __nv_bfloat16* o = planes + (static_cast<int64_t>(ib - kb - 2) * kNB + r0 + u) * kPlanes * kNB + c0;
+      __nv_bfloat16* o =
+          planes + (static_cast<int64_t>(ib - kb - 4) * kNB + r0 + u) * kPlanes * kNB + c0;
 #pragma unroll
       for (int pl = 0; pl < kPlanes; ++pl)
         *reinterpret_cast<uint2*>(o + pl * kNB) = make_uint2(w[pl][0], w[pl][1]);
     }
   }
-  __syncthreads();  // Lt free, P0 complete
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-#pragma unroll
-    for (int w = 0; w < 4; ++w) Lt[r0 + u][c0 + w] = acc[u][w];  // P_ib [r][k]
-  __syncthreads();
-  float* cb = ai + kNB;  // A[ib, kb + 1]
+  const bool prev = kb >= 1 && ib >= kb + 2;  // step kb - 1 on column kb + 2
+  __syncthreads();  // every solve is done (X free); P1, P2 and Pi are complete
+  if (prev) {
+    load_block(blk(ib, kb - 1), ld, X);   // L[ib, kb - 1]
+    load_block(blk(kb + 2, kb - 1), ld, Q);  // L[kb + 2, kb - 1]
+  }
   float cv[4][4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const float4 c4 = *reinterpret_cast<const float4*>(cb + static_cast<size_t>(r0 + u) * ld + c0);
-    cv[u][0] = c4.x; cv[u][1] = c4.y; cv[u][2] = c4.z; cv[u][3] = c4.w;
-  }
-  for (int k = 0; k < kNB; ++k) {
-    float pr[4], pc[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      pr[u] = Lt[r0 + u][k];
-      pc[u] = P0[c0 + u][k];
+  load_tile(blk(ib, kb + 1), ld, r0, c0, cv);
+  sub_product(own, P1, r0, c0, cv);
+  put_tile(blk(ib, kb + 1), ld, r0, c0, cv);
+  if (ib >= kb + 2) {
+    load_tile(blk(ib, kb + 2), ld, r0, c0, cv);
+    if (prev) {
+      __syncthreads();  // X and Q complete
+      sub_product(X, Q, r0, c0, cv);
     }
-#pragma unroll
-    for (int u = 0; u < 4; ++u)
-#pragma unroll
-      for (int w = 0; w < 4; ++w) cv[u][w] = fmaf(-pr[u], pc[w], cv[u][w]);
+    sub_product(own, P2, r0, c0, cv);
+    put_tile(blk(ib, kb + 2), ld, r0, c0, cv);
   }
-#pragma unroll
-  for (int u = 0; u < 4; ++u)
-    *reinterpret_cast<float4*>(cb + static_cast<size_t>(r0 + u) * ld + c0) =
-        make_float4(cv[u][0], cv[u][1], cv[u][2], cv[u][3]);
 }
 
 __global__ void zero_upper_kernel(float* A, int d) {
@@ -632,7 +690,7 @@ __global__ void bias_kernel(const double* sy, const double* count, const float* 
 struct FitPlan {
   size_t off_gh = 0, off_s = 0, off_mu32 = 0, off_mu64 = 0, off_alpha = 0,
          off_xs = 0, off_gi = 0, off_bp = 0, off_ap = 0, off_part = 0,
-         off_cs = 0, off_linv = 0, total = 0;
+         off_cs = 0, off_linv = 0, off_pst = 0, total = 0;
   int bn = 0;
   int slabs = 0;
   int64_t slab_rows = 0;
@@ -671,6 +729,7 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->off_mu64 = lay.take(d * 8);
     pl->off_alpha = lay.take(8);
     pl->off_linv = lay.take(kNB * kNB * 4);
+    pl->off_pst = lay.take(2 * kNB * kNB * 4);
     pl->off_xs = lay.take(4 * d * d * 2);  // bf16 planes [hi; lo; hi; hi] of L^-1
     pl->off_gi = lay.take(d * d * 8);
     pl->off_bp = lay.take(d * 3 * d * 2);
@@ -831,47 +890,57 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fit preparation launch");
 
-  // blocked Cholesky, lower factor in place, with a look-ahead of one block column:
-  // after the diagonal factor of step kb, one launch solves the panel and updates block
-  // column kb+1 on `s`, and the rest of the trailing matrix is updated on the side stream,
-  // so the next diagonal factor runs beside the large update.  The two updates write
-  // disjoint blocks and every element takes the same sum as one whole update; the skipped
-  // blocks above the diagonal are never read.  The diagonal blocks receive L_kk^-1 (the
-  // first step of the inverse below); the panels read the factor's copy in `linv`.
+  // blocked Cholesky, lower factor in place, right-looking with a look-ahead of two block
+  // columns: the panel launch of step kb (on `s`) solves block column kb and applies step kb
+  // to block column kb + 1 and steps kb - 1 and kb to block column kb + 2; the update of the
+  // rest of the trailing matrix (the columns from kb + 4 on) by step kb runs on the side
+  // stream, and the panel of step kb + 2 is the first launch that waits for it, so the
+  // trailing updates leave the chain of diagonal factors and panels.  Concurrent launches
+  // write disjoint blocks, and every element takes its updates in step order; the blocks
+  // above the diagonal are never read.  The diagonal blocks receive L_kk^-1 (the first step
+  // of the inverse below); the panels read the factor's copy in `linv`.
   const int nb = d / kNB;
   float* linv = reinterpret_cast<float*>(ws + pl.off_linv);
-  // seven-plane splits of the trailing updates' panels and of the inverse's operands, in the
-  // area of the f64 inverse (8 d^2 bytes, free until the G^-1 product)
+  float* pst = reinterpret_cast<float*>(ws + pl.off_pst);
+  // seven-plane splits of the trailing updates' panels (one buffer per step parity) and of
+  // the inverse's operands, in the area of the f64 inverse (8 d^2 bytes, free until the
+  // G^-1 product)
   __nv_bfloat16* cplanes = reinterpret_cast<__nv_bfloat16*>(Gi);
+  const int64_t plane_buf = static_cast<int64_t>(d) * kPlanes * kNB;
   HostStreamer* hs = host_streamer();
   if (hs == nullptr) return RF_ERR_CUDA;
-  if ((e = cudaFuncSetAttribute(panel_next_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if ((e = cudaFuncSetAttribute(panel_ahead_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 kPanelSmem)) != cudaSuccess)
     return cuda_fail(e, "Cholesky panel attributes");
   {
     // one caller at a time on the device's side stream and its events
     std::lock_guard<std::mutex> lk(host_stream_mutex());
-    for (int kb = 0; kb < nb; ++kb) {
-      potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb, err, linv);
-      if (kb + 1 == nb) break;
-      // block column kb+1 was last written by step kb-1's trailing update
-      if (kb > 0 && (e = cudaStreamWaitEvent(s, hs->side_done, 0)) != cudaSuccess)
+    int last_trailing = -1;
+    potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, 0, err, linv, nullptr, 0);
+    for (int kb = 0; kb + 1 < nb; ++kb) {
+      // block column kb + 2 was last written by the trailing update of step kb - 2
+      if (kb >= 2 && kb + 2 < nb && (e = cudaStreamWaitEvent(s, hs->side_ev[kb % 2], 0)) != cudaSuccess)
         return cuda_fail(e, "Cholesky look-ahead");
-      panel_next_kernel<<<nb - kb - 1, 256, kPanelSmem, s>>>(Gh, d, kb, linv, cplanes);
-      if ((e = cudaEventRecord(hs->side_start, s)) == cudaSuccess)
-        e = cudaStreamWaitEvent(hs->side, hs->side_start, 0);
-      if (e != cudaSuccess) return cuda_fail(e, "Cholesky look-ahead");
-      const int rem = d - (kb + 1) * kNB;
-      if (rem > kNB) {
-        const int64_t off = static_cast<int64_t>(kb + 2) * kNB * (d + 1);
-        rf_status st = launch_f32_product(cplanes, cplanes, rem - kNB, rem - kNB, kNB, 1, Gh + off, d,
-                                          0, -1.f, true, true, dd - off, hs->side);
+      __nv_bfloat16* planes = cplanes + (kb % 2) * plane_buf;
+      panel_ahead_kernel<<<nb - kb - 1, 256, kPanelSmem, s>>>(Gh, d, kb, linv, pst, planes);
+      const int rem = d - (kb + 4) * kNB;
+      if (rem > 0) {
+        if ((e = cudaEventRecord(hs->side_start, s)) == cudaSuccess)
+          e = cudaStreamWaitEvent(hs->side, hs->side_start, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "Cholesky look-ahead");
+        const int64_t off = static_cast<int64_t>(kb + 4) * kNB * (d + 1);
+        rf_status st = launch_f32_product(planes, planes, rem, rem, kNB, 1, Gh + off, d, 0, -1.f,
+                                          true, true, dd - off, hs->side);
         if (st != RF_OK) return st;
+        if ((e = cudaEventRecord(hs->side_ev[kb % 2], hs->side)) != cudaSuccess)
+          return cuda_fail(e, "Cholesky look-ahead");
+        last_trailing = kb;
       }
-      if ((e = cudaEventRecord(hs->side_done, hs->side)) != cudaSuccess)
-        return cuda_fail(e, "Cholesky look-ahead");
+      const int held = nb - kb - 1 < 2 ? nb - kb - 1 : 2;  // panel blocks of rows kb+1, kb+2
+      potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb + 1, err, linv, pst, held);
     }
-    if (nb > 1 && (e = cudaStreamWaitEvent(s, hs->side_done, 0)) != cudaSuccess)
+    if (last_trailing >= 0 &&
+        (e = cudaStreamWaitEvent(s, hs->side_ev[last_trailing % 2], 0)) != cudaSuccess)
       return cuda_fail(e, "Cholesky look-ahead");
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "Cholesky launch");
