@@ -290,6 +290,20 @@ __global__ void __launch_bounds__(256) split7_kernel(const float* __restrict__ s
   }
 }
 
+// Copies n held-back panel blocks (rows kb and kb + 1 of block column kb - 1) from `pst`
+// into place (256 threads).
+__device__ __forceinline__ void copy_held(float* A, int ld, int kb, const float* pst, int n) {
+  for (int b = 0; b < n; ++b) {
+    float* dst = A + static_cast<size_t>(kb + b) * kNB * ld + static_cast<size_t>(kb - 1) * kNB;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = 4 * (static_cast<int>(threadIdx.x) + 256 * q);  // four floats of one row
+      *reinterpret_cast<float4*>(dst + static_cast<size_t>(e / kNB) * ld + e % kNB) =
+          *reinterpret_cast<const float4*>(pst + b * kNB * kNB + e);
+    }
+  }
+}
+
 // ------------------------------------------------------------ Cholesky (f32)
 // One 64x64 diagonal block: the lower factor L_kk and its inverse, both right-looking
 // in one sweep over the
@@ -306,25 +320,11 @@ __global__ void __launch_bounds__(256) split7_kernel(const float* __restrict__ s
 // updates then need no masks: the zeros leave every other cell unchanged, and only
 // the (never read) upper triangle of a takes stray updates.  One barrier a step.  The
 // inverse L_kk^-1 (zeros above) goes to Linv [64, 64] and over the diagonal block: later
-// steps read only the blocks below it, and the triangular inverse starts from it.
-// It first copies the n_pst panel blocks of the previous step held back in `pst` (rows kb
-// and kb + 1 of block column kb - 1) into place.
-__global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int kb, int* err,
-                                                         float* Linv, const float* pst,
-                                                         int n_pst) {
-  __shared__ float col[2][kNB];   // l_ij for i > j, else 0
-  __shared__ float xrow[2][kNB];  // x_jc for c <= j, else 0
-  float* blk = A + static_cast<size_t>(kb) * kNB * ld + static_cast<size_t>(kb) * kNB;
+// steps read only the blocks below it, and the triangular inverse starts from it.  col and
+// xrow are [2][64] floats of shared memory each.
+__device__ void factor_diag(float* blk, int ld, int* err, float* Linv, float (*col)[kNB],
+                            float (*xrow)[kNB]) {
   const int tid = threadIdx.x, ti = tid & 15, tk = tid >> 4;
-  for (int b = 0; b < n_pst; ++b) {
-    float* dst = A + static_cast<size_t>(kb + b) * kNB * ld + static_cast<size_t>(kb - 1) * kNB;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int e = 4 * (tid + 256 * q);  // four consecutive floats of one row
-      *reinterpret_cast<float4*>(dst + static_cast<size_t>(e / kNB) * ld + e % kNB) =
-          *reinterpret_cast<const float4*>(pst + b * kNB * kNB + e);
-    }
-  }
   float a[4][4], x[4][4];
 #pragma unroll
   for (int u = 0; u < 4; ++u)
@@ -391,6 +391,18 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int k
     }
 }
 
+// The first diagonal block (the later ones are factored by the panel launches).
+__global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int* err, float* Linv) {
+  __shared__ float col[2][kNB];   // l_ij for i > j, else 0
+  __shared__ float xrow[2][kNB];  // x_jc for c <= j, else 0
+  factor_diag(A, ld, err, Linv, col, xrow);
+}
+
+__global__ void __launch_bounds__(256) copy_held_kernel(float* A, int ld, int kb, const float* pst,
+                                                        int n) {
+  copy_held(A, ld, kb, pst, n);
+}
+
 // Panel of Cholesky step kb and its two look-ahead block columns, one 64-row block
 // ib = kb + 1 + blockIdx.x per CTA (256 threads, 4 x 4 outputs each):
 //   P_ib = A[ib, kb] L_kk^-T = A[ib, kb] Linv^T          (the block of L, written back)
@@ -402,6 +414,11 @@ __global__ void __launch_bounds__(256) potrf_diag_kernel(float* A, int ld, int k
 // kb needs only the trailing update of step kb - 2: one step of the factorisation runs
 // between the two.  With `planes` set, the blocks ib >= kb + 4 also go there as seven-plane
 // splits, row (ib - kb - 4) * 64 + r, for that trailing update on the tensor cores.
+// CTA 0 (ib = kb + 1), whose block of column kb + 1 is the next diagonal block, then
+// factors it (factor_diag, L_(kb+1)^-1 to Linv_out), so the launch chain of the
+// factorisation is one launch per step.  The blocks of rows kb + 1 and kb + 2 of column kb
+// are read unsolved by every CTA: they go to `pst` and the next launch's last CTA copies
+// them into place (with `held` blocks of the previous step from `pst_prev`).
 // Dynamic shared memory: Lt = Linv^T [64][68], then X (the block being solved, later
 // L[ib, kb-1]), P1 = P_(kb+1), P2 = P_(kb+2), Pi = P_ib and Q = L[kb+2, kb-1], [64][65] each.
 constexpr int kPanelSmem = (kNB * (kNB + 4) + 5 * kNB * (kNB + 1)) * 4;
@@ -481,8 +498,10 @@ __device__ __forceinline__ void put_tile(float* blk, int ld, int r0, int c0, con
 }
 
 __global__ void __launch_bounds__(256) panel_ahead_kernel(float* A, int ld, int kb,
-                                                          const float* Linv, float* pst,
-                                                          __nv_bfloat16* planes) {
+                                                          const float* Linv, float* Linv_out,
+                                                          float* pst, const float* pst_prev,
+                                                          int held, __nv_bfloat16* planes,
+                                                          int* err) {
   extern __shared__ __align__(16) float psm[];
   typedef float Tile[kNB + 1];
   auto Lt = reinterpret_cast<float (*)[kNB + 4]>(psm);
@@ -497,6 +516,9 @@ __global__ void __launch_bounds__(256) panel_ahead_kernel(float* A, int ld, int 
   auto blk = [&](int bi, int bj) {
     return A + static_cast<size_t>(bi) * kNB * ld + static_cast<size_t>(bj) * kNB;
   };
+  // the previous step's held-back blocks (rows kb, kb + 1 of column kb - 1): read by no
+  // launch of the factorisation from here on
+  if (held > 0 && blockIdx.x + 1 == gridDim.x) copy_held(A, ld, kb, pst_prev, held);
   {
     float lv[16];
 #pragma unroll
@@ -561,6 +583,11 @@ __global__ void __launch_bounds__(256) panel_ahead_kernel(float* A, int ld, int 
     }
     sub_product(own, P2, r0, c0, cv);
     put_tile(blk(ib, kb + 2), ld, r0, c0, cv);
+  }
+  if (ib == kb + 1) {  // block (kb + 1, kb + 1) is complete: factor it
+    __syncthreads();   // its rows, written above, are visible to the whole CTA
+    factor_diag(blk(kb + 1, kb + 1), ld, err, Linv_out, reinterpret_cast<float (*)[kNB]>(&X[0][0]),
+                reinterpret_cast<float (*)[kNB]>(&X[0][0] + 2 * kNB));
   }
 }
 
@@ -728,8 +755,8 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->off_mu32 = lay.take(d * 4);
     pl->off_mu64 = lay.take(d * 8);
     pl->off_alpha = lay.take(8);
-    pl->off_linv = lay.take(kNB * kNB * 4);
-    pl->off_pst = lay.take(2 * kNB * kNB * 4);
+    pl->off_linv = lay.take(2 * kNB * kNB * 4);
+    pl->off_pst = lay.take(4 * kNB * kNB * 4);
     pl->off_xs = lay.take(4 * d * d * 2);  // bf16 planes [hi; lo; hi; hi] of L^-1
     pl->off_gi = lay.take(d * d * 8);
     pl->off_bp = lay.take(d * 3 * d * 2);
@@ -791,10 +818,12 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
 // following the previous entry's: planes 0-5 of A against planes 1-6 of B, K' = 6 K.
 // out_b = out + b * out_bstride, rows out_ld apart; lower: one square product (M = N), only
 // the pair tiles on and below the diagonal (the upper part of a diagonal tile is written
-// too).  `lim` elements of out are in bounds (checked by debug builds).
+// too).  `lim` elements of out are in bounds (checked by debug builds).  max_pairs > 0
+// caps the CTA pairs (the SMs the launch takes).
 rf_status launch_f32_product(const __nv_bfloat16* Ap7, const __nv_bfloat16* Bp7, int M, int N,
                              int K, int batches, float* out, int64_t out_ld, int64_t out_bstride,
-                             float alpha, bool beta_one, bool lower, int64_t lim, cudaStream_t s) {
+                             float alpha, bool beta_one, bool lower, int64_t lim, cudaStream_t s,
+                             int max_pairs = 0) {
   if (M <= 0 || N <= 0 || batches <= 0) return RF_OK;
   GemmParams p{};
   p.mode = kModeF32;
@@ -823,7 +852,8 @@ rf_status launch_f32_product(const __nv_bfloat16* Ap7, const __nv_bfloat16* Bp7,
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
   const int64_t u = (p.m_tiles + 1) / 2;
   const int64_t tiles = lower ? u * (u + 1) / 2 : u * p.n_tiles * p.batches;
-  const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
+  if (max_pairs > 0 && pairs > max_pairs) pairs = max_pairs;
   const cudaError_t e = launch_gemm2(p, pairs, s);
   if (e != cudaSuccess) return cuda_fail(e, "f32 product launch");
   return RF_OK;
@@ -895,10 +925,11 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   // to block column kb + 1 and steps kb - 1 and kb to block column kb + 2; the update of the
   // rest of the trailing matrix (the columns from kb + 4 on) by step kb runs on the side
   // stream, and the panel of step kb + 2 is the first launch that waits for it, so the
-  // trailing updates leave the chain of diagonal factors and panels.  Concurrent launches
-  // write disjoint blocks, and every element takes its updates in step order; the blocks
-  // above the diagonal are never read.  The diagonal blocks receive L_kk^-1 (the first step
-  // of the inverse below); the panels read the factor's copy in `linv`.
+  // trailing updates leave the chain of panel launches; each panel launch also factors the
+  // next diagonal block.  Concurrent launches write disjoint blocks, and every element takes
+  // its updates in step order; the blocks above the diagonal are never read.  The diagonal
+  // blocks receive L_kk^-1 (the first step of the inverse below); the panels read the
+  // factor's copy in `linv` (two buffers, by step parity).
   const int nb = d / kNB;
   float* linv = reinterpret_cast<float*>(ws + pl.off_linv);
   float* pst = reinterpret_cast<float*>(ws + pl.off_pst);
@@ -915,30 +946,37 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   {
     // one caller at a time on the device's side stream and its events
     std::lock_guard<std::mutex> lk(host_stream_mutex());
-    int last_trailing = -1;
-    potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, 0, err, linv, nullptr, 0);
+    int last_trailing = -1, held = 0;
+    constexpr int kBlk = kNB * kNB;
+    potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, err, linv);
     for (int kb = 0; kb + 1 < nb; ++kb) {
       // block column kb + 2 was last written by the trailing update of step kb - 2
       if (kb >= 2 && kb + 2 < nb && (e = cudaStreamWaitEvent(s, hs->side_ev[kb % 2], 0)) != cudaSuccess)
         return cuda_fail(e, "Cholesky look-ahead");
       __nv_bfloat16* planes = cplanes + (kb % 2) * plane_buf;
-      panel_ahead_kernel<<<nb - kb - 1, 256, kPanelSmem, s>>>(Gh, d, kb, linv, pst, planes);
+      // L_kk^-1 and the held-back blocks alternate between two buffers by step parity
+      panel_ahead_kernel<<<nb - kb - 1, 256, kPanelSmem, s>>>(
+          Gh, d, kb, linv + (kb % 2) * kBlk, linv + ((kb + 1) % 2) * kBlk, pst + (kb % 2) * 2 * kBlk,
+          pst + ((kb + 1) % 2) * 2 * kBlk, held, planes, err);
+      held = nb - kb - 1 < 2 ? nb - kb - 1 : 2;  // blocks of rows kb + 1, kb + 2 held back
       const int rem = d - (kb + 4) * kNB;
       if (rem > 0) {
         if ((e = cudaEventRecord(hs->side_start, s)) == cudaSuccess)
           e = cudaStreamWaitEvent(hs->side, hs->side_start, 0);
         if (e != cudaSuccess) return cuda_fail(e, "Cholesky look-ahead");
+        // the next panel launch (nb - kb - 2 CTAs, one per SM) keeps its SMs
+        const int pairs = (sm_count() - (nb - kb - 2)) / 2;
         const int64_t off = static_cast<int64_t>(kb + 4) * kNB * (d + 1);
         rf_status st = launch_f32_product(planes, planes, rem, rem, kNB, 1, Gh + off, d, 0, -1.f,
-                                          true, true, dd - off, hs->side);
+                                          true, true, dd - off, hs->side, pairs > 0 ? pairs : 1);
         if (st != RF_OK) return st;
         if ((e = cudaEventRecord(hs->side_ev[kb % 2], hs->side)) != cudaSuccess)
           return cuda_fail(e, "Cholesky look-ahead");
         last_trailing = kb;
       }
-      const int held = nb - kb - 1 < 2 ? nb - kb - 1 : 2;  // panel blocks of rows kb+1, kb+2
-      potrf_diag_kernel<<<1, 256, 0, s>>>(Gh, d, kb + 1, err, linv, pst, held);
     }
+    if (held > 0)  // the last step's held-back block
+      copy_held_kernel<<<1, 256, 0, s>>>(Gh, d, nb - 1, pst + ((nb - 2) % 2) * 2 * kBlk, held);
     if (last_trailing >= 0 &&
         (e = cudaStreamWaitEvent(s, hs->side_ev[last_trailing % 2], 0)) != cudaSuccess)
       return cuda_fail(e, "Cholesky look-ahead");
