@@ -403,6 +403,12 @@ __device__ void epilogue_gram(const GemmParams& p, uint32_t tcol, int q, int lan
     lim = p.lim_b;
   }
   const bool ok = in_bounds(o + p.bn - 1, lim, p.err);
+  // symmetric product: a pair tile below the diagonal (column tile n < pair row m / 2) also
+  // writes its transpose, column c of this row to row c (lanes: consecutive addresses)
+  const bool mirror = p.gram_sym && n != m / 2;
+  const int64_t rg = static_cast<int64_t>(m) * kBM + r;
+  const bool ok_t = !mirror || in_bounds(static_cast<int64_t>(n * p.bn + p.bn - 1) * p.gram_ld + rg,
+                                         p.lim_a, p.err);
   for (int c0 = 0; c0 < p.bn; c0 += 32) {
     uint32_t a[32];
     tmem_ld32(tcol + c0, a);
@@ -414,6 +420,17 @@ __device__ void epilogue_gram(const GemmParams& p, uint32_t tcol, int q, int lan
     }
     if (!ok) continue;
     double2* d2 = reinterpret_cast<double2*>(dst + c0);
+    if (p.gram_sym) {
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        d2[j] = make_double2(static_cast<double>(f32(a[2 * j])), static_cast<double>(f32(a[2 * j + 1])));
+      if (mirror && ok_t) {
+        double* col = p.gram_G + static_cast<int64_t>(n * p.bn + c0) * p.gram_ld + rg;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) col[static_cast<int64_t>(j) * p.gram_ld] = static_cast<double>(f32(a[j]));
+      }
+      continue;
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
       double2 v = d2[j];

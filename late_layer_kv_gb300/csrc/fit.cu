@@ -773,7 +773,8 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
 // the tile's X columns).
 
 rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int64_t rows, int d,
-                      int dout, int bn, double* out_G, double* out_C, cudaStream_t s) {
+                      int dout, int bn, double* out_G, double* out_C, cudaStream_t s,
+                      bool sym = false) {
   GemmParams p{};
   p.mode = kModeGram;
   p.k_blocks = static_cast<int32_t>(ceil_div(rows, kBK));
@@ -792,7 +793,8 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   // pairs take 512-column tiles where d allows and the tiles fill eight waves: each A
   // stage then feeds two MMAs, which halves the A reads per flop
   const int64_t wide_tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * (d / kGramWideCols);
-  const bool wide = d % kGramWideCols == 0 && wide_tiles >= 8 * (sm_count() / 2);
+  sym = sym && Y == nullptr && bn == 2 * kBM;
+  const bool wide = !sym && d % kGramWideCols == 0 && wide_tiles >= 8 * (sm_count() / 2);
   p.bn = wide ? kGramWideCols : bn;
   p.n_tiles = d / p.bn;
   p.batches = 1;
@@ -805,7 +807,10 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   p.lim_b = static_cast<int64_t>(L) * dout * d;
   p.err = device_error_word();
   if (p.err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
-  const int64_t tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * p.n_tiles;
+  p.lower = sym ? 1 : 0;
+  p.gram_sym = sym ? 1 : 0;
+  const int64_t u = (p.m_tiles + 1) / 2;
+  const int64_t tiles = sym ? u * (u + 1) / 2 : u * p.n_tiles;
   const int pairs = static_cast<int>(tiles < sm_count() / 2 ? tiles : sm_count() / 2);
   if (pairs <= 0) return RF_OK;
   const cudaError_t e = launch_gemm2(p, pairs, s);
@@ -1025,13 +1030,15 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
     }
   }
   // G^-1 = X^T X on the tensor cores: one MN-major Gram product over the stacked bf16
-  // planes, [hi; lo; hi] against [lo; hi; hi] (K = 3d, summed in f32 in TMEM), added into
-  // the cleared f64 inverse
+  // planes, [hi; lo; hi] against [lo; hi; hi] (K = 3d, summed in f32 in TMEM).  With
+  // 256-column tiles only the pair tiles on and below the diagonal are computed, each
+  // stored with its transpose; otherwise every tile is added into the cleared inverse.
   split2_kernel<<<static_cast<unsigned>(ceil_div(dd / 8, 256)), 256, 0, s>>>(Gh, dd, Xs);
-  if ((e = cudaMemsetAsync(Gi, 0, static_cast<size_t>(dd) * 8, s)) != cudaSuccess)
+  const bool sym = pl.bn == 2 * kBM;
+  if (!sym && (e = cudaMemsetAsync(Gi, 0, static_cast<size_t>(dd) * 8, s)) != cudaSuccess)
     return cuda_fail(e, "clearing the inverse");
   rf_status st;
-  if ((st = launch_gram(Xs, Xs + dd, nullptr, 0, 3 * d, d, 128, pl.bn, Gi, nullptr, s)) != RF_OK)
+  if ((st = launch_gram(Xs, Xs + dd, nullptr, 0, 3 * d, d, 128, pl.bn, Gi, nullptr, s, sym)) != RF_OK)
     return st;
 
   split_ginv_kernel<<<static_cast<unsigned>(ceil_div(dd / 8, 256)), 256, 0, s>>>(Gi, d, Bp);

@@ -144,6 +144,9 @@ struct GemmParams {
   double* gram_G;      // [d_in, d_in]
   double* gram_C;      // [L, d_out, d_in]
   int32_t gram_ld;     // d_in
+  // symmetric Gram product (with `lower`): G is stored, not added to, and each pair tile
+  // below the diagonal also stores its transpose
+  int32_t gram_sym;
   // solve epilogue
   const float* col_scale;   // [N]
   const float* mu_x;        // [N]
