@@ -852,9 +852,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
                                    64 * (j % bpm),
                                kb * kBK, 0);
           } else {
-            tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, kb * kBK, m * kBM, b);
+            // solve mode: K = 3 planes of d over two-plane operands, A' hi, hi, lo against
+            // B' hi, lo, hi (k-block kb of the product reads A' k-block ka, B' k-block kbb)
+            const int np = p.k_blocks / 3;
+            const bool sv = !kQ8 && p.mode == kModeSolve;
+            const int ka = sv && kb >= np ? kb - np : kb;
+            tma_load_3d_pair(smem_u32(sA + stage * kHalfBytes), &p.tmA, fb, ka * kBK, m * kBM, b);
+            if (sv) {
+              const int kbb = kb >= 2 * np ? kb - 2 * np : kb;
+              tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[0], fb, kbb * kBK,
+                               tb.nrow + half * static_cast<int>(rank), b);
+            }
           }
-          if (kQ8 || p.mode == kModeGram) {
+          if (kQ8 || p.mode == kModeGram || p.mode == kModeSolve) {
             // B comes from the converter warps, or was loaded above
           } else if (tb.seg < 2)
             tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[tb.seg], fb, kb * kBK,

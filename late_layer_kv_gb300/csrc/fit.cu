@@ -600,7 +600,7 @@ __global__ void zero_upper_kernel(float* A, int d) {
 // ------------------------------------------------------------ split operands
 
 
-// B' [d, 3d] = [hi(G^-1) | lo(G^-1) | hi(G^-1)] from the f64 inverse: hi = bf16(v_hi) and
+// B' [d, 2d] = [hi(G^-1) | lo(G^-1)] from the f64 inverse: hi = bf16(v_hi) and
 // lo = bf16((v_hi - hi) + v_lo) of the double-float (v_hi, v_lo), the first difference
 // exact; eight consecutive k per thread
 __global__ void split_ginv_kernel(const double* __restrict__ Gi, int d, __nv_bfloat16* __restrict__ Bp) {
@@ -621,11 +621,9 @@ __global__ void split_ginv_kernel(const double* __restrict__ Gi, int d, __nv_bfl
     hw[q] = bf16x2(h0, h1);
     lw[q] = bf16x2(l0, l1);
   }
-  __nv_bfloat16* row = Bp + i * 3 * d;
-  const uint4 h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-  *reinterpret_cast<uint4*>(row + k0) = h;
+  __nv_bfloat16* row = Bp + i * 2 * d;
+  *reinterpret_cast<uint4*>(row + k0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
   *reinterpret_cast<uint4*>(row + d + k0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-  *reinterpret_cast<uint4*>(row + 2 * d + k0) = h;
 }
 
 // X = L^-1 (f32, lower, n elements) split into the four bf16 planes [hi; lo; hi; hi] of n
@@ -655,7 +653,7 @@ __global__ void split2_kernel(const float* __restrict__ X, int64_t n, __nv_bfloa
   dst[3 * plane] = h;
 }
 
-// A' [L*d_out, 3d] = [hi(c) | hi(c) | lo(c)],  c[o, k] = s_k (C[o, k] - sy[o] mu_x[k])
+// A' [L*d_out, 2d] = [hi(c) | lo(c)],  c[o, k] = s_k (C[o, k] - sy[o] mu_x[k])
 // (sy[o] mu_x[k] = n mu_y[o] mu_x[k]), centred in double-float as above; eight consecutive
 // k of kCentreRows rows per thread (d is a multiple of 128): 64-byte reads of C, 16-byte
 // stores of each part
@@ -695,11 +693,9 @@ __global__ void __launch_bounds__(256) split_rhs_kernel(const double* __restrict
       hw[q] = bf16x2(h0, h1);
       lw[q] = bf16x2(l0, l1);
     }
-    __nv_bfloat16* row = Ap + o * 3 * d;
-    const uint4 h = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-    *reinterpret_cast<uint4*>(row + k0) = h;
-    *reinterpret_cast<uint4*>(row + d + k0) = h;
-    *reinterpret_cast<uint4*>(row + 2 * d + k0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    __nv_bfloat16* row = Ap + o * 2 * d;
+    *reinterpret_cast<uint4*>(row + k0) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+    *reinterpret_cast<uint4*>(row + d + k0) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   }
 }
 
@@ -759,8 +755,8 @@ void plan_fit(const rf_fit_args* a, FitPlan* pl) {
     pl->off_pst = lay.take(4 * kNB * kNB * 4);
     pl->off_xs = lay.take(4 * d * d * 2);  // bf16 planes [hi; lo; hi; hi] of L^-1
     pl->off_gi = lay.take(d * d * 8);
-    pl->off_bp = lay.take(d * 3 * d * 2);
-    pl->off_ap = lay.take(M * 3 * d * 2);
+    pl->off_bp = lay.take(d * 2 * d * 2);
+    pl->off_ap = lay.take(M * 2 * d * 2);
     pl->off_part = lay.take(M * (d / pl->bn) * 4);
   }
   pl->total = lay.off;
@@ -1049,12 +1045,14 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
 
   GemmParams p{};
   p.mode = kModeSolve;
+  // K = 3d over two-plane operands: the producer reads A' planes hi, hi, lo against B'
+  // planes hi, lo, hi
   p.k_blocks = 3 * d / kBK;
-  const uint64_t krow = static_cast<uint64_t>(3 * d) * 2;
-  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap, 3 * d, M, 1, krow, 0, kBK,
+  const uint64_t krow = static_cast<uint64_t>(2 * d) * 2;
+  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap, 2 * d, M, 1, krow, 0, kBK,
                          kBM, CU_TENSOR_MAP_SWIZZLE_128B);
   // on CTA pairs: each CTA stages half of the tile's B rows
-  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, 3 * d, d, 1, krow, 0,
+  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, 2 * d, d, 1, krow, 0,
                           kBK, pl.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the solve GEMM");
   p.m_tiles = static_cast<int32_t>(ceil_div(M, kBM));
