@@ -82,10 +82,12 @@ __global__ void add_count_kernel(double* count, double rows) { *count += rows; }
 
 // ------------------------------------------------------------ solve: centring
 // One block: mu_x, alpha (trace of the centred Gram), the equilibration s.
-__global__ void prep_kernel(const double* G, const double* sx, const double* count, int d,
+constexpr int kPrepThreads = 1024;  // the diagonal reads are latency-bound: many in flight
+__global__ void __launch_bounds__(kPrepThreads) prep_kernel(const double* G, const double* sx,
+                                                            const double* count, int d,
                             double lam, float* s_f32, float* mu_f32, double* mu_f64,
                             double* alpha_ws, double* alpha_out) {
-  __shared__ double red[256];
+  __shared__ double red[kPrepThreads];
   const double n = *count;
   double tr = 0.0;
   for (int i = threadIdx.x; i < d; i += blockDim.x) {
@@ -591,10 +593,23 @@ __global__ void __launch_bounds__(256) panel_ahead_kernel(float* A, int ld, int 
   }
 }
 
+// Zeros above the diagonal of the f32 [d, d] matrix, four columns per thread (d * d < 2^31)
 __global__ void zero_upper_kernel(float* A, int d) {
-  const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (t >= static_cast<int64_t>(d) * d) return;
-  if (t % d > t / d) A[t] = 0.f;
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  const int q = d / 4;
+  if (t >= d * q) return;
+  const int r = t / q, c = (t - r * q) * 4;
+  if (c + 3 <= r) return;  // on or below the diagonal
+  float4* p = reinterpret_cast<float4*>(A) + t;
+  if (c > r) {
+    *p = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    float4 v = *p;
+    if (c + 1 > r) v.y = 0.f;
+    if (c + 2 > r) v.z = 0.f;
+    if (c + 3 > r) v.w = 0.f;
+    *p = v;
+  }
 }
 
 // ------------------------------------------------------------ split operands
@@ -913,7 +928,7 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   if (err == nullptr) return fail(RF_ERR_CUDA, "device error word unavailable");
   const int64_t dd = static_cast<int64_t>(d) * d;
 
-  prep_kernel<<<1, 256, 0, s>>>(a->G, a->sx, a->count, d, a->lambda, sc, mu32, mu64, alpha,
+  prep_kernel<<<1, kPrepThreads, 0, s>>>(a->G, a->sx, a->count, d, a->lambda, sc, mu32, mu64, alpha,
                                 a->alpha_out);
   const int64_t eq_threads = ceil_div(d, kCentreRows) * (d / 8);
   equilibrate_kernel<<<static_cast<unsigned>(ceil_div(eq_threads, 256)), 256, 0, s>>>(
@@ -983,7 +998,7 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
       return cuda_fail(e, "Cholesky look-ahead");
   }
   if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "Cholesky launch");
-  zero_upper_kernel<<<static_cast<unsigned>((dd + 255) / 256), 256, 0, s>>>(Gh, d);
+  zero_upper_kernel<<<static_cast<unsigned>((dd / 4 + 255) / 256), 256, 0, s>>>(Gh, d);
   // X = L^-1 in place: the 64 x 64 diagonal blocks are inverted already; recursive
   // doubling: blocks [s1 | s2] of size s (already inverted) merge as
   //   T = L_21 X_11,  X_21 = -X_22 T,
