@@ -51,12 +51,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # The fit depends only on d, the number of maps and the calibration rows, which the Llama-8B
 # fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
 _FIT_LLAMA8B = {"sources": "fit",
-                "kernel_sha256": "d6de737f32e4f88d01cb325e1ec4ca8f857e7f7f3c922c0ae3bbdfe4346c338e",
-                "bytes_per_launch": 73577685504 + 2790565632}
+                "kernel_sha256": "962d61774f4cd927138513c00fe53a0ee8acb44a7c673c53890fb1b284c82026",
+                "bytes_per_launch": 86277598080 + 2794465088}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "261feb0584e3841ee1e64bf3333bcff3efc5b0dec77dc6880f491f9e8d27aecb",
-                    "bytes_per_launch": 5238894028},
+                    "kernel_sha256": "e2652f03c6abb3c2499a316f683deef3e9b8d82b2d9710fe4738264c0187aa3c",
+                    "bytes_per_launch": 5276000256},
     "llama8b_16k_fit": _FIT_LLAMA8B,
     "hostmaps_16k_fit": _FIT_LLAMA8B,
     "hostmaps_64k_fit": _FIT_LLAMA8B,
@@ -588,11 +588,12 @@ class FitWorkload:
             inv += 6 * ((1 if full > 0 else 0) + (1 if rest > sz else 0))
             sz *= 2
         # accumulate: two column-sum passes, their reduction, the count, the Gram products;
-        # solve: preparation, equilibration, Cholesky (per block column the diagonal block
-        # with its inverse, then panel with the next-column update and, while more columns
-        # remain, the rest of the trailing update), zero fill, the doubling products, the
-        # bf16 split, the G^-1 product, two operand splits, the solve GEMM, the offsets
-        chol = nb + (nb - 1) + max(0, nb - 2)
+        # solve: preparation, equilibration, Cholesky (the first diagonal block, then per
+        # step a panel launch that also factors the next diagonal block and, while columns
+        # from four blocks on remain, the trailing update; the last held-back block's copy),
+        # zero fill, the doubling products, the bf16 split, the G^-1 product, two operand
+        # splits, the solve GEMM, the offsets
+        chol = 1 + (nb - 1) + max(0, nb - 4) + (1 if nb > 1 else 0)
         return 5 + 2 + chol + 1 + inv + 1 + 1 + 2 + 1 + 1
 
     def setup(self, dev, seed):
