@@ -203,7 +203,9 @@ def test_debug_library_builds_and_adds_guard_bands():
     """The debug build (RF_DEBUG=1) loads without a GPU, exports the same symbols, and its
     workspaces hold one guard band after every region: the fill of a resident-map call has
     seven regions (predicted inputs, partial sums, map slots, row gather, host split
-    state, RoPE table, int8 layer groups), the fit with both steps twelve."""
+    state, RoPE table, int8 layer groups), the fit with both steps thirteen (column-sum
+    partials; G^, scales, two means, alpha, L^-1 copies, held-back panel blocks, inverse
+    planes, G^-1, both solve operands, offset partials)."""
     from late_layer_kv_gb300 import build as b
     from late_layer_kv_gb300 import ridgefill as rb
     dbg = rb.load(debug=True)
@@ -218,5 +220,5 @@ def test_debug_library_builds_and_adds_guard_bands():
     assert (dbg.ridgefill_fill_workspace_size(ctypes.byref(fa)) ==
             rel.ridgefill_fill_workspace_size(ctypes.byref(fa)) + 7 * guard)
     assert (dbg.ridgefill_fit_workspace_size(ctypes.byref(ta)) ==
-            rel.ridgefill_fit_workspace_size(ctypes.byref(ta)) + 12 * guard)
+            rel.ridgefill_fit_workspace_size(ctypes.byref(ta)) + 13 * guard)
     assert os.path.basename(b.LIB_DEBUG) == "libridgefill_debug.so"
