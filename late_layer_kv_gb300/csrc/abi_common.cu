@@ -89,6 +89,20 @@ int* tile_counter_slot() {
   return base[d] + (seq.fetch_add(1) % kTileCtrSlots);
 }
 
+bool make_tmap_4d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base,
+                  const uint64_t (&dims)[4], const uint64_t (&strides)[3], const uint32_t (&box)[4],
+                  CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+  cuuint32_t b[4] = {box[0], box[1], box[2], box[3]};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  CUresult r = fn(tm, dtype, 4, const_cast<void*>(base), d, st, b, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 int sm_count() {
   static int cnt[kMaxDevices] = {};
   const int d = current_device();

@@ -28,6 +28,11 @@ int sm_count();
 bool make_tmap_3d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, uint64_t d0,
                   uint64_t d1, uint64_t d2, uint64_t stride1, uint64_t stride2, uint32_t box0,
                   uint32_t box1, CUtensorMapSwizzle swizzle);
+// 4D tiled tensor map (dims innermost first, strides in bytes for dims 1-3, any order of
+// magnitude: a dimension may step through memory more finely than the one before it).
+bool make_tmap_4d(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base,
+                  const uint64_t (&dims)[4], const uint64_t (&strides)[3], const uint32_t (&box)[4],
+                  CUtensorMapSwizzle swizzle);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }

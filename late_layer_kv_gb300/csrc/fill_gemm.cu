@@ -835,7 +835,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
             const int nmma = tb.bn < 256 ? tb.bn : 256;
             const int bpm = nmma / 128;  // 64-column boxes per MMA in this CTA's half
             // (the empty second half of an odd last row tile reads past X: zero fill)
-            if (m < p.gram_x_tiles || m >= p.m_tiles) {
+            if (wide) {
+              // rank-4 views {64 columns, rows, column blocks, layers}: one copy stages two
+              // 64-column blocks (16 KB), the A half in one, each MMA's B half in one
+              if (m < p.gram_x_tiles || m >= p.m_tiles) {
+                tma_load_4d_pair(smem_u32(adst), &p.tmA, fb, 0, kb * kBK, m * (kBM / 64), 0);
+              } else {
+                const int mm = m - p.gram_x_tiles;
+                tma_load_4d_pair(smem_u32(adst), &p.tmA2, fb, 0, kb * kBK,
+                                 (mm % p.gram_y_tiles_per_layer) * (kBM / 64),
+                                 mm / p.gram_y_tiles_per_layer);
+              }
+              for (int jj = 0; jj < 2; ++jj)
+                tma_load_4d_pair(smem_u32(bdst + jj * 16384), &p.tmB[0], fb, 0, kb * kBK,
+                                 (tb.nrow + 256 * jj + 128 * static_cast<int>(rank)) / 64, 0);
+            } else if (m < p.gram_x_tiles || m >= p.m_tiles) {
               for (int j = 0; j < kBM / 64; ++j)
                 tma_load_3d_pair(smem_u32(adst + j * 8192), &p.tmA, fb, m * kBM + 64 * j,
                                  kb * kBK, 0);
@@ -846,7 +860,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
               for (int j = 0; j < kBM / 64; ++j)
                 tma_load_3d_pair(smem_u32(adst + j * 8192), &p.tmA2, fb, m0 + 64 * j, kb * kBK, l);
             }
-            for (int j = 0; j < half / 64; ++j)
+            for (int j = 0; j < (wide ? 0 : half / 64); ++j)
               tma_load_3d_pair(smem_u32(bdst + j * 8192), &p.tmB[0], fb,
                                tb.nrow + (j / bpm) * nmma + (nmma / 2) * static_cast<int>(rank) +
                                    64 * (j % bpm),

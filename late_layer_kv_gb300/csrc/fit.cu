@@ -806,6 +806,25 @@ rf_status launch_gram(const void* Xa, const void* Xb, const void* Y, int L, int6
   const int64_t wide_tiles = static_cast<int64_t>((p.m_tiles + 1) / 2) * (d / kGramWideCols);
   sym = sym && Y == nullptr && bn == 2 * kBM;
   const bool wide = !sym && d % kGramWideCols == 0 && wide_tiles >= 8 * (sm_count() / 2);
+  if (wide) {
+    // wide tiles stage two 64-column blocks per copy: rank-4 views {64 columns, rows,
+    // column blocks, layers} whose third dimension steps 128 bytes
+    const uint64_t dx[4] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(d / 64), 1};
+    const uint64_t sx[3] = {xrow, 128, xrow * static_cast<uint64_t>(rows)};
+    const uint32_t bx[4] = {64, 64, 2, 1};
+    ok = make_tmap_4d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xa, dx, sx, bx,
+                      CU_TENSOR_MAP_SWIZZLE_128B);
+    ok = ok && make_tmap_4d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Xb, dx, sx, bx,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    if (Y != nullptr) {
+      const uint64_t dy[4] = {64, static_cast<uint64_t>(rows), static_cast<uint64_t>(dout / 64),
+                              static_cast<uint64_t>(L)};
+      const uint64_t sy[3] = {yrow, 128, yrow * static_cast<uint64_t>(rows)};
+      ok = ok && make_tmap_4d(&p.tmA2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, dy, sy, bx,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the wide Gram GEMM");
+  }
   p.bn = wide ? kGramWideCols : bn;
   p.n_tiles = d / p.bn;
   p.batches = 1;
