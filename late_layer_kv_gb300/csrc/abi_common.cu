@@ -235,8 +235,16 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   const uint64_t in_row = static_cast<uint64_t>(m.d_in) * 2;
   const uint64_t out_row = static_cast<uint64_t>(m.d_out) * 2;
   const bool q8 = m.A_scale != nullptr;
-  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.H, m.d_in, m.rows, 1, in_row,
-                         0, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
+  // bf16 maps: stages of two k-blocks, each operand's staged by one copy through a rank-4
+  // view {64 k, rows, k-blocks, 1} whose third dimension steps 128 bytes
+  const uint64_t kblocks = static_cast<uint64_t>(m.d_in / kBK);
+  const uint64_t dh[4] = {kBK, static_cast<uint64_t>(m.rows), kblocks, 1};
+  const uint64_t sh[3] = {in_row, 128, in_row * static_cast<uint64_t>(m.rows)};
+  const uint32_t bh[4] = {kBK, kBM, 2, 1};
+  bool ok = q8 ? make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.H, m.d_in, m.rows, 1,
+                              in_row, 0, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B)
+               : make_tmap_4d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.H, dh, sh, bh,
+                              CU_TENSOR_MAP_SWIZZLE_128B);
   // B boxes of bn / 2 rows: each CTA of a pair stages half of a tile's columns
   if (q8) {
     // codes {d_in, B rows} int8 in boxes {128, bn / 2} (two k-blocks, one scale group);
@@ -254,8 +262,12 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
     p.q8_scale = static_cast<const __nv_bfloat16*>(m.A_scale);
     p.q8_ld = m.d_in;
   } else {
-    ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A, m.d_in, brows, 1,
-                            in_row, 0, kBK, m.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+    const uint64_t da[4] = {kBK, brows, kblocks, 1};
+    const uint64_t sa[3] = {in_row, 128, in_row * brows};
+    const uint32_t ba[4] = {kBK, static_cast<uint32_t>(m.bn / 2), 2, 1};
+    ok = ok && make_tmap_4d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.A, da, sa, ba,
+                            CU_TENSOR_MAP_SWIZZLE_128B);
+    p.k2 = 1;
   }
   ok = ok && make_tmap_3d(&p.tmO[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, m.xhat, m.d_out, m.rows,
                           m.n_layers, out_row, out_row * m.R, 64, 32, CU_TENSOR_MAP_SWIZZLE_128B);

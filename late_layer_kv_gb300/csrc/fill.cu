@@ -188,14 +188,24 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   const uint64_t drow = static_cast<uint64_t>(a->d_out) * 2;
   const uint64_t hd = a->head_dim;
   const uint64_t pos_end = static_cast<uint64_t>(a->pos0 + start + rc);
-  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xhat, a->d_out, rc,
-                         a->n_layers, drow, drow * pl.R, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-  // pair kernel: B boxes of bn / 2 rows (each CTA of a pair stages half of a tile's columns)
-  const uint32_t bbox = pl.bn_kv / 2;  // each CTA of a pair stages half of the B rows
-  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wk, a->d_out, kvw,
-                          a->n_layers, drow, drow * kvw, kBK, bbox, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wv, a->d_out, kvw,
-                          a->n_layers, drow, drow * kvw, kBK, bbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  // stages of two k-blocks: each operand staged by one copy through a rank-4 view
+  // {64 k, rows, k-blocks, layers} whose third dimension steps 128 bytes; B boxes of bn / 2
+  // rows (each CTA of a pair stages half of a tile's columns)
+  const uint64_t kblocks = static_cast<uint64_t>(a->d_out / kBK);
+  const uint64_t L = static_cast<uint64_t>(a->n_layers);
+  const uint64_t dx[4] = {kBK, static_cast<uint64_t>(rc), kblocks, L};
+  const uint64_t sx[3] = {drow, 128, drow * static_cast<uint64_t>(pl.R)};
+  const uint32_t bx[4] = {kBK, kBM, 2, 1};
+  bool ok = make_tmap_4d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xhat, dx, sx, bx,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t dw[4] = {kBK, static_cast<uint64_t>(kvw), kblocks, L};
+  const uint64_t sw[3] = {drow, 128, drow * static_cast<uint64_t>(kvw)};
+  const uint32_t bw[4] = {kBK, static_cast<uint32_t>(pl.bn_kv / 2), 2, 1};
+  ok = ok && make_tmap_4d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wk, dw, sw, bw,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_4d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wv, dw, sw, bw,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  p.k2 = 1;
   const uint64_t planes = static_cast<uint64_t>(a->n_layers) * a->n_kv_heads;
   const uint64_t plane_bytes = static_cast<uint64_t>(a->cache_len) * hd * 2;
   ok = ok && make_tmap_3d(&p.tmO[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Kc, hd, pos_end, planes,

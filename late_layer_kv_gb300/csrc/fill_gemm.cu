@@ -774,7 +774,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
     if (lane == 0) {
       // ---------------- TMA producer of this CTA's halves
       const bool wide = !kQ8 && p.mode == kModeGram && p.bn == kGramWideCols;
-      const uint32_t nst = wide ? kStagesWide : kS;
+      const bool k2 = !kQ8 && p.k2 != 0;
+      const uint32_t nst = wide ? kStagesWide : (k2 ? kS / 2 : kS);
       uint32_t stage = 0, phase = 0;
       int issued[kS];
       for (int s = 0; s < kS; ++s) issued[s] = -1;
@@ -816,17 +817,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
             h_seen = g;
           }
         }
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < p.k_blocks; kb += k2 ? 2 : 1) {
           if (!mbar_wait(&empty[stage], phase ^ 1, abort_flag, p.err, kErrProducer)) {
             ok = false;
             break;
           }
           const uint32_t fb = full0 + 8 * stage;
           const int half = tb.bn / 2;  // B rows (tile columns) this CTA stages
-          const uint32_t tx = kQ8 ? kHalfBytes : kHalfBytes + half * kBK * 2;
+          const uint32_t tx = kQ8 ? kHalfBytes : (k2 ? 2 : 1) * (kHalfBytes + half * kBK * 2);
           if (rank == 0) mbar_expect_tx(&full[stage], tx);
           else mbar_expect_tx_cl(fb, tx);
-          if (!kQ8 && p.mode == kModeGram) {
+          if (k2) {
+            // two k-blocks of A and of this CTA's B half, one copy each (rank-4 views
+            // {64 k, rows, k-blocks, batch})
+            tma_load_4d_pair(smem_u32(sA + stage * 2 * kHalfBytes), &p.tmA, fb, 0, m * kBM, kb, b);
+            tma_load_4d_pair(smem_u32(sB + stage * 2 * kHalfBytes), &p.tmB[tb.seg], fb, 0,
+                             tb.nrow + half * static_cast<int>(rank), kb, b);
+          } else if (!kQ8 && p.mode == kModeGram) {
             // MN-major operands: 64-wide column blocks of [rows, width] arrays, 64 rows of K;
             // A: this CTA's 128 columns of [X | Y_1 .. Y_L], B: its half of the X columns of
             // each N <= 256 MMA (a wide tile's second MMA starts 256 columns on)
@@ -878,7 +885,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
                                tb.nrow + half * static_cast<int>(rank), b);
             }
           }
-          if (kQ8 || p.mode == kModeGram || p.mode == kModeSolve) {
+          if (kQ8 || k2 || p.mode == kModeGram || p.mode == kModeSolve) {
             // B comes from the converter warps, or was loaded above
           } else if (tb.seg < 2)
             tma_load_3d_pair(smem_u32(sB + stage * kHalfBytes), &p.tmB[tb.seg], fb, kb * kBK,
@@ -900,7 +907,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
     if (lane == 0 && rank == 0) {
       // ---------------- MMA issuer (CTA 0 only)
       const bool wide = !kQ8 && p.mode == kModeGram && p.bn == kGramWideCols;
-      const uint32_t nst = wide ? kStagesWide : kS;
+      const bool k2 = !kQ8 && p.k2 != 0;
+      const uint32_t nst = wide ? kStagesWide : (k2 ? kS / 2 : kS);
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int it = 0; ok; ++it) {
@@ -918,7 +926,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, p.err, kErrMma)) break;
         tc_fence_after();
         const uint32_t dt = tmem_base + acc * kBNMax;
-        for (int kb = 0; kb < p.k_blocks; ++kb) {
+        for (int kb = 0; kb < p.k_blocks; kb += k2 ? 2 : 1) {
           const bool got = kQ8 ? mbar_wait_acq_cluster(&full[stage], phase, abort_flag, p.err, kErrMma)
                                : mbar_wait(&full[stage], phase, abort_flag, p.err, kErrMma);
           if (!got) {
@@ -926,7 +934,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
             break;
           }
           tc_fence_after();
-          if (!mn) {
+          if (k2) {
+            // two k-blocks: A's 16 KB apart, B's (bn / 2 rows of 128 bytes) bn * 64 bytes apart
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + (2 * stage + h) * kHalfBytes));
+              const uint64_t bd = sdesc_kmajor_sw128(
+                  smem_u32(sB + 2 * stage * kHalfBytes + h * (tb.bn / 2) * 128));
+#pragma unroll
+              for (int k = 0; k < kBK / 16; ++k)
+                mma_bf16_pair(dt, ad + 2 * k, bd + 2 * k, idesc, (kb | h | k) != 0 ? 1u : 0u);
+            }
+          } else if (!mn) {
             const uint64_t ad = sdesc_kmajor_sw128(smem_u32(sA + stage * kHalfBytes));
             const uint64_t bd = sdesc_kmajor_sw128(smem_u32(sB + stage * kHalfBytes));
 #pragma unroll

@@ -164,6 +164,9 @@ struct GemmParams {
   int32_t cols;
   int* err;
   int* tile_ctr;  // this launch's tile counter (zeroed before the launch): tiles are taken in order
+  // K-major bf16 map mode: stages of two k-blocks, each operand staged by one copy through a
+  // rank-3 view {64 k, rows, k-blocks} (three stages in the space of six)
+  int32_t k2;
   // elements of the buffers the epilogue writes with plain stores (checked by debug
   // builds): map mode ss_part, map_out; K/V mode with a row list the caches (per tensor);
   // GDN mode gdn_gate; Gram mode gram_G, gram_C; solve mode the outputs, bias_part; f32
