@@ -829,10 +829,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
           else mbar_expect_tx_cl(fb, tx);
           if (k2) {
             // two k-blocks of A and of this CTA's B half, one copy each (rank-4 views
-            // {64 k, rows, k-blocks, batch})
-            tma_load_4d_pair(smem_u32(sA + stage * 2 * kHalfBytes), &p.tmA, fb, 0, m * kBM, kb, b);
-            tma_load_4d_pair(smem_u32(sB + stage * 2 * kHalfBytes), &p.tmB[tb.seg], fb, 0,
-                             tb.nrow + half * static_cast<int>(rank), kb, b);
+            // {64 k, rows, k-blocks, batch}); solve mode: K = 3 planes of d over two-plane
+            // operands, A' hi, hi, lo against B' hi, lo, hi (k-block kb of the product reads
+            // A' k-block ka, B' k-block kbb; d / 64 is even, so no pair straddles two planes)
+            int ka = kb, kbb = kb;
+            if (p.mode == kModeSolve) {
+              const int np = p.k_blocks / 3;
+              ka = kb >= np ? kb - np : kb;
+              kbb = kb >= 2 * np ? kb - 2 * np : kb;
+            }
+            tma_load_4d_pair(smem_u32(sA + stage * 2 * kHalfBytes), &p.tmA, fb, 0, m * kBM, ka, b);
+            if (tb.seg < 2)
+              tma_load_4d_pair(smem_u32(sB + stage * 2 * kHalfBytes), &p.tmB[tb.seg], fb, 0,
+                               tb.nrow + half * static_cast<int>(rank), kbb, b);
+            else  // GDN gate tile: CTA 0 stages the alpha weights, CTA 1 the beta weights
+              tma_load_4d_pair(smem_u32(sB + stage * 2 * kHalfBytes), &p.tmB[2 + rank], fb, 0, 0,
+                               kb, b);
           } else if (!kQ8 && p.mode == kModeGram) {
             // MN-major operands: 64-wide column blocks of [rows, width] arrays, 64 rows of K;
             // A: this CTA's 128 columns of [X | Y_1 .. Y_L], B: its half of the X columns of

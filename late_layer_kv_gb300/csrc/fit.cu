@@ -863,11 +863,20 @@ rf_status launch_f32_product(const __nv_bfloat16* Ap7, const __nv_bfloat16* Bp7,
   GemmParams p{};
   p.mode = kModeF32;
   p.k_blocks = 6 * K / kBK;
+  // stages of two k-blocks (6K / 64 is even), each operand staged by one copy through a
+  // rank-4 view {64 k, rows, k-blocks, batches}
   const uint64_t row = static_cast<uint64_t>(kPlanes) * K * 2;
-  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap7, 6 * K, M, batches, row,
-                         row * M, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp7 + K, 6 * K, N, batches,
-                          row, row * N, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t kbl = static_cast<uint64_t>(6 * K / kBK), nb = static_cast<uint64_t>(batches);
+  const uint64_t dA[4] = {kBK, static_cast<uint64_t>(M), kbl, nb};
+  const uint64_t sA[3] = {row, 128, row * static_cast<uint64_t>(M)};
+  const uint64_t dB[4] = {kBK, static_cast<uint64_t>(N), kbl, nb};
+  const uint64_t sB[3] = {row, 128, row * static_cast<uint64_t>(N)};
+  const uint32_t bx[4] = {kBK, 128, 2, 1};
+  bool ok = make_tmap_4d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap7, dA, sA, bx,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+  ok = ok && make_tmap_4d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp7 + K, dB, sB, bx,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  p.k2 = 1;
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for an f32 product");
   p.m_tiles = static_cast<int32_t>(ceil_div(M, kBM));
   p.bn = 256;
@@ -1082,12 +1091,21 @@ rf_status solve(const rf_fit_args* a, const FitPlan& pl, uint8_t* ws, cudaStream
   // K = 3d over two-plane operands: the producer reads A' planes hi, hi, lo against B'
   // planes hi, lo, hi
   p.k_blocks = 3 * d / kBK;
+  // stages of two k-blocks, each operand staged by one copy through a rank-4 view
+  // {64 k, rows, k-blocks, 1}; on CTA pairs each CTA stages half of the tile's B rows
   const uint64_t krow = static_cast<uint64_t>(2 * d) * 2;
-  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap, 2 * d, M, 1, krow, 0, kBK,
-                         kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-  // on CTA pairs: each CTA stages half of the tile's B rows
-  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, 2 * d, d, 1, krow, 0,
-                          kBK, pl.bn / 2, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t kbl = static_cast<uint64_t>(2 * d / kBK);
+  const uint64_t dA[4] = {kBK, static_cast<uint64_t>(M), kbl, 1};
+  const uint64_t sA[3] = {krow, 128, krow * static_cast<uint64_t>(M)};
+  const uint32_t bA[4] = {kBK, kBM, 2, 1};
+  bool ok = make_tmap_4d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Ap, dA, sA, bA,
+                         CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t dB[4] = {kBK, static_cast<uint64_t>(d), kbl, 1};
+  const uint64_t sB[3] = {krow, 128, krow * static_cast<uint64_t>(d)};
+  const uint32_t bB[4] = {kBK, static_cast<uint32_t>(pl.bn / 2), 2, 1};
+  ok = ok && make_tmap_4d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Bp, dB, sB, bB,
+                          CU_TENSOR_MAP_SWIZZLE_128B);
+  p.k2 = 1;
   if (!ok) return fail(RF_ERR_CUDA, "cuTensorMapEncodeTiled failed for the solve GEMM");
   p.m_tiles = static_cast<int32_t>(ceil_div(M, kBM));
   p.bn = pl.bn;

@@ -933,18 +933,26 @@ rf_status launch_gdn_proj(const rf_gdn_args* a, const GdnPlan& pl, int64_t rc, c
   const int H = a->n_heads;
   const uint64_t drow = static_cast<uint64_t>(a->d_out) * 2;
   const uint64_t hk = static_cast<uint64_t>(H) * kDk;
-  bool ok = make_tmap_3d(&p.tmA, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, xhat, a->d_out, rc, a->n_layers,
-                         drow, drow * pl.R, kBK, kBM, CU_TENSOR_MAP_SWIZZLE_128B);
-  // B boxes of half a tile's columns: each CTA of a pair stages one half (the gate
-  // tile's halves are the H rows of w_a and of w_b)
-  ok = ok && make_tmap_3d(&p.tmB[0], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wk, a->d_out, hk,
-                          a->n_layers, drow, drow * hk, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_tmap_3d(&p.tmB[1], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wv, a->d_out, hk,
-                          a->n_layers, drow, drow * hk, kBK, 128, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_tmap_3d(&p.tmB[2], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wa, a->d_out, H,
-                          a->n_layers, drow, drow * H, kBK, H, CU_TENSOR_MAP_SWIZZLE_128B);
-  ok = ok && make_tmap_3d(&p.tmB[3], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a->Wb, a->d_out, H,
-                          a->n_layers, drow, drow * H, kBK, H, CU_TENSOR_MAP_SWIZZLE_128B);
+  // stages of two k-blocks: each operand staged by one copy through a rank-4 view
+  // {64 k, rows, k-blocks, layers} whose third dimension steps 128 bytes.  B boxes of half
+  // a tile's columns: each CTA of a pair stages one half (the gate tile's halves are the H
+  // rows of w_a and of w_b)
+  const uint64_t kblocks = static_cast<uint64_t>(a->d_out / kBK);
+  const uint64_t L = static_cast<uint64_t>(a->n_layers);
+  auto view = [&](CUtensorMap* tm, const void* base, uint64_t rows, uint64_t layer_stride,
+                  uint32_t box_rows) {
+    const uint64_t dims[4] = {kBK, rows, kblocks, L};
+    const uint64_t strides[3] = {drow, 128, layer_stride};
+    const uint32_t box[4] = {kBK, box_rows, 2, 1};
+    return make_tmap_4d(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, dims, strides, box,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  };
+  bool ok = view(&p.tmA, xhat, static_cast<uint64_t>(rc), drow * pl.R, kBM);
+  ok = ok && view(&p.tmB[0], a->Wk, hk, drow * hk, 128);
+  ok = ok && view(&p.tmB[1], a->Wv, hk, drow * hk, 128);
+  ok = ok && view(&p.tmB[2], a->Wa, H, drow * H, static_cast<uint32_t>(H));
+  ok = ok && view(&p.tmB[3], a->Wb, H, drow * H, static_cast<uint32_t>(H));
+  p.k2 = 1;
   // outputs: k and v planes {d_k, rows, L*H*2} (high part, then remainder, per layer and head)
   const uint64_t prow = static_cast<uint64_t>(kDk) * 2, pplane = prow * pl.R;
   const uint64_t planes = static_cast<uint64_t>(a->n_layers) * H * 2;
