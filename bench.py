@@ -51,12 +51,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # The fit depends only on d, the number of maps and the calibration rows, which the Llama-8B
 # fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
 _FIT_LLAMA8B = {"sources": "fit",
-                "kernel_sha256": "962d61774f4cd927138513c00fe53a0ee8acb44a7c673c53890fb1b284c82026",
-                "bytes_per_launch": 86277598080 + 2794465088}
+                "kernel_sha256": "5a5b8257edebd3830a5fa2c6bfe3b7714ed763eaa19e30dd7dba7e6f2c18f9c5",
+                "bytes_per_launch": 74632458816 + 2789447616}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "e2652f03c6abb3c2499a316f683deef3e9b8d82b2d9710fe4738264c0187aa3c",
-                    "bytes_per_launch": 5276000256},
+                    "kernel_sha256": "6aabb0cba9d00a2799de36123f8ae6ed0eb16652ba825931836718860fdddc1a",
+                    "bytes_per_launch": 5361767168},
     "llama8b_16k_fit": _FIT_LLAMA8B,
     "hostmaps_16k_fit": _FIT_LLAMA8B,
     "hostmaps_64k_fit": _FIT_LLAMA8B,
