@@ -290,6 +290,7 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   p.h_ready = m.h_ready;
   p.h_gen = m.h_gen;
   p.h_group_rows = kHostRowGroup;
+  if (m.h_ready != nullptr) p.group_m0 = 2 * (kHostRowGroup / (2 * kBM));  // first group: one flag's rows
   p.h_row_base = static_cast<int32_t>(m.h_row_base);
   p.bias = m.bias;
   p.gain = static_cast<const __nv_bfloat16*>(m.gain);

@@ -86,9 +86,10 @@ struct HostStreamer {
 using StreamWrite32 = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 StreamWrite32 stream_write32();
 
-// Rows of split state per ready flag when H streams from host memory (a multiple
-// of the pair GEMM's 256-row tiles; one raster group of the map GEMM).
-constexpr int kHostRowGroup = 4096;
+// Rows of split state per ready flag when H streams from host memory (a multiple of the
+// pair GEMM's 256-row tiles; the height of the map GEMM's first raster group, so the GEMM
+// starts once the first 1,024 rows have landed).
+constexpr int kHostRowGroup = 1024;
 
 // Split state in page-locked host memory, streamed into device memory `dev` in groups of
 // kHostRowGroup rows on the copy stream.  Each group's flag (flags[g], in device memory)

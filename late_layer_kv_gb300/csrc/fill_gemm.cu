@@ -579,15 +579,25 @@ __device__ __forceinline__ void decode_unit(int t, const GemmParams& p, int& mu,
   const int gp = p.group_m / 2 > 0 ? p.group_m / 2 : 1;
   const int per_b = m_units * p.n_tiles;
   b = t / per_b;
-  const int r = t - b * per_b;
+  int r = t - b * per_b;
+  b += p.batch_base;
+  // a shorter first group: the rows it needs land first when the split state streams in
+  const int g0 = min(p.group_m0 / 2, m_units);
+  if (g0 > 0) {
+    if (r < g0 * p.n_tiles) {
+      mu = r % g0;
+      n = r / g0;
+      return;
+    }
+    r -= g0 * p.n_tiles;
+  }
   const int gsz = gp * p.n_tiles;
   const int g = r / gsz;
-  const int first = g * gp;
+  const int first = g0 + g * gp;
   const int gm = min(m_units - first, gp);
   const int rr = r - g * gsz;
   mu = first + rr % gm;
   n = rr / gm;
-  b += p.batch_base;
 }
 
 // ---- int8 maps.  A third ring ("raw", kRawStages deep) holds this CTA's half of

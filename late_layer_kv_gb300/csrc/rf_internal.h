@@ -85,6 +85,7 @@ struct GemmParams {
   int32_t batch_base;  // batch entry of the first (a layer subset starts past 0)
   int32_t bn;          // MMA N of a tile
   int32_t group_m;     // raster group height
+  int32_t group_m0;    // > 0: height of the first raster group (split state streaming in)
   int32_t rows;        // valid rows of this launch
   int32_t ss_stride;   // row stride of the sum-of-squares partials
   int32_t d_out;
