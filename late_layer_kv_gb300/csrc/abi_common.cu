@@ -156,25 +156,25 @@ std::mutex& host_stream_mutex() {
 size_t host_rows_bytes(int64_t rows, int d_in, size_t* flags_off) {
   const size_t data = align_up(static_cast<size_t>(rows) * d_in * 2, 256);
   *flags_off = data;
-  return data + align_up(static_cast<size_t>(ceil_div(rows, kHostRowGroup)) * 4, 256);
+  return data + align_up(static_cast<size_t>(host_row_groups(rows)) * 4, 256);
 }
 
 rf_status stream_host_rows(HostStreamer* hs, const void* H, int64_t rows, int d_in, uint8_t* dev,
                            uint32_t* flags, cudaStream_t s, HostRows* out) {
   out->flags = flags;
   out->gen = ++hs->h_gen == 0 ? ++hs->h_gen : hs->h_gen;
-  const int64_t groups = ceil_div(rows, kHostRowGroup);
+  const int64_t groups = host_row_groups(rows);
   StreamWrite32 wr = stream_write32();
   out->overlap = wr != nullptr;
-  for (int64_t g = 0; g < groups && out->overlap; ++g)  // clear the flags, in order on `s`
-    out->overlap = wr(reinterpret_cast<CUstream>(s), reinterpret_cast<CUdeviceptr>(flags + g), 0,
-                      0) == CUDA_SUCCESS;
+  // clear the flags, in order on `s` (one call: few API calls keep the host ahead of the GPU)
+  cudaError_t e = cudaMemsetAsync(flags, 0, static_cast<size_t>(groups) * 4, s);
   const uint8_t* src = static_cast<const uint8_t*>(H);
-  cudaError_t e = cudaEventRecord(hs->start, s);
+  if (e == cudaSuccess) e = cudaEventRecord(hs->start, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hs->copy, hs->start, 0);
   for (int64_t g = 0; g < groups && e == cudaSuccess; ++g) {
-    const int64_t r0 = g * kHostRowGroup;
-    const int64_t nr = rows - r0 < kHostRowGroup ? rows - r0 : kHostRowGroup;
+    const int64_t r0 = g == 0 ? 0 : kHostFirstRows + (g - 1) * kHostRowGroup;
+    const int64_t gr = g == 0 ? kHostFirstRows : kHostRowGroup;
+    const int64_t nr = rows - r0 < gr ? rows - r0 : gr;
     const size_t off = static_cast<size_t>(r0) * d_in * 2;
     e = cudaMemcpyAsync(dev + off, src + off, static_cast<size_t>(nr) * d_in * 2,
                         cudaMemcpyHostToDevice, hs->copy);
@@ -290,7 +290,8 @@ rf_status launch_map(const MapLaunch& m, cudaStream_t s) {
   p.h_ready = m.h_ready;
   p.h_gen = m.h_gen;
   p.h_group_rows = kHostRowGroup;
-  if (m.h_ready != nullptr) p.group_m0 = 2 * (kHostRowGroup / (2 * kBM));  // first group: one flag's rows
+  p.h_first_rows = kHostFirstRows;
+  if (m.h_ready != nullptr) p.group_m0 = kHostFirstRows / kBM;  // first raster group: the first flag's rows
   p.h_row_base = static_cast<int32_t>(m.h_row_base);
   p.bias = m.bias;
   p.gain = static_cast<const __nv_bfloat16*>(m.gain);

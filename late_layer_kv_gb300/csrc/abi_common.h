@@ -86,10 +86,16 @@ struct HostStreamer {
 using StreamWrite32 = CUresult (*)(CUstream, CUdeviceptr, cuuint32_t, unsigned int);
 StreamWrite32 stream_write32();
 
-// Rows of split state per ready flag when H streams from host memory (a multiple of the
-// pair GEMM's 256-row tiles; the height of the map GEMM's first raster group, so the GEMM
-// starts once the first 1,024 rows have landed).
-constexpr int kHostRowGroup = 1024;
+// Rows of split state per ready flag when H streams from host memory: a first group of
+// kHostFirstRows (the height of the map GEMM's first raster group, so the GEMM starts once
+// those rows have landed), then groups of kHostRowGroup (one raster group of the map GEMM);
+// both multiples of the pair GEMM's 256-row tiles.
+constexpr int kHostFirstRows = 1024;
+constexpr int kHostRowGroup = 4096;
+// Flag groups of `rows` streamed rows, and the group of row r.
+inline int64_t host_row_groups(int64_t rows) {
+  return rows <= kHostFirstRows ? 1 : 1 + (rows - kHostFirstRows + kHostRowGroup - 1) / kHostRowGroup;
+}
 
 // Split state in page-locked host memory, streamed into device memory `dev` in groups of
 // kHostRowGroup rows on the copy stream.  Each group's flag (flags[g], in device memory)

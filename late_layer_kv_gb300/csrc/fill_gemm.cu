@@ -820,7 +820,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kQ8 ? kGemmThreadsQ8
         const int m = 2 * mu + static_cast<int>(rank);
         const TileB tb = tile_b(p, n);
         if (p.h_ready != nullptr && m * kBM < p.rows) {
-          const int g = (p.h_row_base + m * kBM) / p.h_group_rows;
+          const int hr = p.h_row_base + m * kBM;
+          const int g = hr < p.h_first_rows ? 0 : 1 + (hr - p.h_first_rows) / p.h_group_rows;
           if (g != h_seen) {
             if (!flag_wait(p.h_ready + g, p.h_gen, abort_flag, p.err, kErrHostRows)) break;
             fence_acq_rel_gpu();

@@ -96,11 +96,13 @@ struct GemmParams {
   const int8_t* q8;
   const __nv_bfloat16* q8_scale;
   int32_t q8_ld;
-  // split state streamed from host memory (map mode): rows of group g = row / h_group_rows
-  // (row counted from h_row_base) may be read once h_ready[g] == h_gen
+  // split state streamed from host memory (map mode): rows of group g (row < h_first_rows:
+  // g = 0, else g = 1 + (row - h_first_rows) / h_group_rows; row counted from h_row_base)
+  // may be read once h_ready[g] == h_gen
   const uint32_t* h_ready;
   uint32_t h_gen;
   int32_t h_group_rows;
+  int32_t h_first_rows;  // rows of group 0 (the later groups have h_group_rows)
   int32_t h_row_base;
   // map epilogue; with map_rows set, tile row r is stored as X_hat row map_rows[r] (row by
   // row, straight from registers) into map_out [L, map_ld, d_out]
