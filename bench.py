@@ -51,12 +51,12 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # The fit depends only on d, the number of maps and the calibration rows, which the Llama-8B
 # fill workloads share (4096, 20, 65,536): one capture serves all of their fits.
 _FIT_LLAMA8B = {"sources": "fit",
-                "kernel_sha256": "5a5b8257edebd3830a5fa2c6bfe3b7714ed763eaa19e30dd7dba7e6f2c18f9c5",
-                "bytes_per_launch": 74632458816 + 2789447616}
+                "kernel_sha256": "9b89e6533986f9df6cb73884b54521314b2e6a844b321568addfc22fbedc6876",
+                "bytes_per_launch": 85647740160 + 2792289024}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "6aabb0cba9d00a2799de36123f8ae6ed0eb16652ba825931836718860fdddc1a",
-                    "bytes_per_launch": 5361767168},
+                    "kernel_sha256": "557d17418e57def1c459588b450df3d230e53b535a987abbd4958d176dbe5348",
+                    "bytes_per_launch": 2970848307 + 2344046080},
     "llama8b_16k_fit": _FIT_LLAMA8B,
     "hostmaps_16k_fit": _FIT_LLAMA8B,
     "hostmaps_64k_fit": _FIT_LLAMA8B,
