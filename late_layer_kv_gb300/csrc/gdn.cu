@@ -147,7 +147,7 @@ __device__ __forceinline__ void tile_product(const float* A, const float* B, int
                                              float4& y0, float4& y1) {
   y0 = make_float4(0.f, 0.f, 0.f, 0.f);
   y1 = y0;
-#pragma unroll
+#pragma unroll 1
   for (int k = 0; k < 16 * N; k += 4) {
     const float4 a0 = ld4(A + r * kLd + k), a1 = ld4(A + (r + 8) * kLd + k);
     const float a0v[4] = {a0.x, a0.y, a0.z, a0.w}, a1v[4] = {a1.x, a1.y, a1.z, a1.w};
@@ -519,7 +519,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         st4(Bs + (16 * a2 + r + 8) * kLd + 16 * b2 + 4 * cg, make_float4(-y1.x, -y1.y, -y1.z, -y1.w));
         named_bar_sync(kPreBar, 128);
       }
-#pragma unroll
+#pragma unroll 1
       for (int m = 0; m < 4; ++m) {
         const int idx = pt + 128 * m;
         const int t = idx >> 3, ch = idx & 7;
@@ -591,6 +591,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       if (ok) {
         const float* ga = reinterpret_cast<const float*>(sm + kOffGateRaw);
         const float g = exp2f(chunk_log2_decay(ga, min(kC, p.rows), lane));
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t r[2][32];
 #pragma unroll
@@ -614,20 +615,22 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       {  // -W as the MN-major B operand of NEW^T: row j holds W^T[j][0..63]
         if (!mbar_wait(&bar[kBarUW], c & 1, abort_flag, p.err, kErrGdn)) break;
         tc_fence_after();
-        uint32_t r[2][32];
-        tmem_ld32(lrow + kColW, r[0]);
-        tmem_ld32(lrow + kColW + 32, r[1]);
-        tmem_wait_ld();
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          uint32_t r[32];
+          tmem_ld32(lrow + kColW + 32 * h, r);
+          tmem_wait_ld();
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          float x[8];
+          for (int c4 = 0; c4 < 4; ++c4) {
+            float x[8];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) x[e] = -__uint_as_float(r[c8 >> 2][8 * (c8 & 3) + e]);
-          uint4 hi, lo;
-          split8(x, hi, lo);
-          const uint32_t off = swz(i, c8);
-          *reinterpret_cast<uint4*>(sm + kOffW + off) = hi;
-          *reinterpret_cast<uint4*>(sm + kOffW + 2 * kBox + off) = lo;
+            for (int e = 0; e < 8; ++e) x[e] = -__uint_as_float(r[8 * c4 + e]);
+            uint4 hi, lo;
+            split8(x, hi, lo);
+            const uint32_t off = swz(i, 4 * h + c4);
+            *reinterpret_cast<uint4*>(sm + kOffW + off) = hi;
+            *reinterpret_cast<uint4*>(sm + kOffW + 2 * kBox + off) = lo;
+          }
         }
         fence_async_smem();
         tc_fence_before();
@@ -640,7 +643,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
         const float* dec = reinterpret_cast<const float*>(sm + kOffGate + (c % 3) * 1024) + 128;
         // t in [32 half, 32 half + 32): both parts are read before the split of the
         // same t range overwrites them
-#pragma unroll
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t r0[32], r1[32];
           tmem_ld32(lrow + kColN + 32 * half, r0);
@@ -673,6 +676,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       if (!mbar_wait(&bar[kBarDB], c & 1, abort_flag, p.err, kErrGdn)) break;
       tc_fence_after();
       if (c + 1 == nch) {
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t r[2][32];
           tmem_ld32(lrow + kColS + 64 * half, r[0]);
@@ -686,6 +690,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
                             __uint_as_float(r[j >> 5][(j & 31) + 3]));
         }
       } else {
+#pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           uint32_t r[2][32];
           tmem_ld32(lrow + kColS + 64 * half, r[0]);
