@@ -160,6 +160,22 @@ __device__ __forceinline__ void tile_product(const float* A, const float* B, int
   }
 }
 
+// P = K K^T of one chunk: 16 MMAs with A = [K_hi; K_lo] (128 K-major rows: a box of high
+// parts and the box of remainders after it, `kd` its descriptor) and B = K_hi, then K_lo.
+// Out of line: the MMA warp issues it from inside each of its waits.
+__device__ __noinline__ void issue_p_mmas(uint32_t d_tmem, uint64_t kd, uint32_t id_p) {
+#pragma unroll
+  for (int g = 0; g < 2; ++g)
+#pragma unroll
+    for (int kblk = 0; kblk < 2; ++kblk)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        const uint32_t o = (kblk * 2 * kBox + 32 * ks) >> 4;
+        mma_bf16(d_tmem, kd + o, kd + o + (g == 1 ? kBox >> 4 : 0), id_p,
+                 (g | kblk | ks) != 0 ? 1u : 0u);
+      }
+}
+
 __global__ void __launch_bounds__(kStateThreads, 1)
     gdn_state_kernel(const __grid_constant__ GdnStateParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -268,17 +284,7 @@ __global__ void __launch_bounds__(kStateThreads, 1)
       // the box of remainders after it) and B = K_hi, then K_lo: rows 0-63 of the
       // result hold K_hi K^T, rows 64-127 K_lo K^T; their sum is P.
       auto issue_p = [&](int c) {
-        const uint64_t kd = dk + ((kOffK + (c % kKBufs) * kKV) >> 4);
-#pragma unroll
-        for (int g = 0; g < 2; ++g)
-#pragma unroll
-          for (int kblk = 0; kblk < 2; ++kblk)
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-              const uint32_t o = (kblk * 2 * kBox + 32 * ks) >> 4;
-              mma_bf16(tb + kColP, kd + o, kd + o + (g == 1 ? kBox >> 4 : 0), id_p,
-                       (g | kblk | ks) != 0 ? 1u : 0u);
-            }
+        issue_p_mmas(tb + kColP, dk + ((kOffK + (c % kKBufs) * kKV) >> 4), id_p);
         mma_commit(&bar[kBarP]);
       };
       // P of the next chunk needs only its keys and the P columns (free once the
