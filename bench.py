@@ -55,8 +55,8 @@ _FIT_LLAMA8B = {"sources": "fit",
                 "bytes_per_launch": 85647740160 + 2792289024}
 PROFILED_TRAFFIC = {
     "llama8b_16k": {"sources": "fill",
-                    "kernel_sha256": "557d17418e57def1c459588b450df3d230e53b535a987abbd4958d176dbe5348",
-                    "bytes_per_launch": 2970848307 + 2344046080},
+                    "kernel_sha256": "259339cf000223d74faccc3fe2a396ba9465fa5247a05d574d759b2453f90dcb",
+                    "bytes_per_launch": 2978276403 + 2344075468},
     "llama8b_16k_fit": _FIT_LLAMA8B,
     "hostmaps_16k_fit": _FIT_LLAMA8B,
     "hostmaps_64k_fit": _FIT_LLAMA8B,

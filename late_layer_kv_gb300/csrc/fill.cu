@@ -218,7 +218,9 @@ rf_status launch_kv(const rf_fill_args* a, const FillPlan& pl, int64_t start, in
   p.n_tiles = only == 0 ? 2 * p.n_k_tiles : kvw / pl.bn_kv;
   p.batches = a->n_layers;
   p.bn = pl.bn_kv;
-  p.group_m = 16;
+  // raster groups of one pair row tile: the pairs that take a row tile's column tiles
+  // together share its first (DRAM) read of X_hat, and W_kv of the layer stays in L2
+  p.group_m = 2;
   p.rows = static_cast<int32_t>(rc);
   p.ss_stride = static_cast<int32_t>(pl.R);
   p.d_out = a->d_out;
